@@ -1,0 +1,142 @@
+"""CPU oracle for the DSA lightning-indexer forward (fp64, plain C).
+
+TEST INFRASTRUCTURE ONLY: import this package only from `tests/`, from the
+smoke check and from the benchmark's CPU-baseline leg.  The product path
+(`dsa_sparse_attention_fwd_gb300`) never imports it, and it imports nothing
+from the product path.
+
+The arithmetic lives in `indexer_oracle.c`; this module only builds that file
+with gcc, marshals numpy arrays into it and returns numpy arrays.  See the C
+file's header for what is computed and which page passage each rule follows.
+
+Parity pins for every function are in `tests/test_oracle.py`.  The one part
+with no pin is the fp32 accumulation order of the GPU side, which only the
+tolerance covers ("parity unpinned" for that aspect alone).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "indexer_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (IEEE double, no FMA contraction)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+           "-ffp-contract=off", "-fno-fast-math", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            P = ctypes.c_void_p
+            lib.oracle_indexer_fwd.restype = ctypes.c_int
+            lib.oracle_indexer_fwd.argtypes = [
+                P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                P, P, P, ctypes.c_longlong, P, P, P, P, P, P, ctypes.c_int]
+            lib.oracle_key_visible.restype = ctypes.c_int
+            lib.oracle_key_visible.argtypes = [ctypes.c_longlong,
+                                               ctypes.c_longlong, ctypes.c_int]
+            _lib = lib
+    return _lib
+
+
+def _bits(x) -> np.ndarray:
+    """bf16 input as a contiguous uint16 array of bit patterns."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach().cpu().contiguous()
+            assert x.dtype == torch.bfloat16, x.dtype
+            return x.view(torch.int16).numpy().view(np.uint16)
+    except ImportError:  # pragma: no cover
+        pass
+    x = np.ascontiguousarray(x)
+    assert x.dtype == np.uint16, x.dtype
+    return x
+
+
+def _arr(x, dtype) -> np.ndarray:
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach().cpu().contiguous().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(x, dtype=dtype)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def key_visible(j: int, t: int, ratio: int) -> bool:
+    """Causal rule: compressed key j is visible at position t."""
+    return bool(_load().oracle_key_visible(j, t, ratio))
+
+
+def indexer_fwd(q, k, w, compress_ratio: int, topk: int, q_pos=None,
+                in_idx=None, rows=None, n_threads: int | None = None,
+                want_logits: bool = False):
+    """Run the oracle on a list of rows.
+
+    q [S,B,H,D] bf16, k [S_kv,B,D] bf16, w [S,B,H] fp32, q_pos [B] int32 or
+    None, in_idx [B,S,topk] int32 or None.  `rows` lists row ids b*S+s
+    (default: every row, in (b, s) order).  Returns a dict of numpy arrays,
+    one line per requested row: idx, scores (fp32), scores64, next (the
+    (topk+1)-th visible score, -inf if none), nvis, logits (if asked),
+    plus `threads` (threads used) and `rows`.
+    """
+    lib = _load()
+    qb, kb = _bits(q), _bits(k)
+    wf = _arr(w, np.float32)
+    S, B, H, D = qb.shape
+    S_kv = kb.shape[0]
+    assert kb.shape == (S_kv, B, D), kb.shape
+    assert wf.shape == (S, B, H), wf.shape
+    qp = None if q_pos is None else _arr(q_pos, np.int32).reshape(B)
+    gi = None if in_idx is None else _arr(in_idx, np.int32).reshape(B, S, topk)
+    if rows is None:
+        rows = np.arange(B * S, dtype=np.int64)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    n = rows.size
+    out = {
+        "idx": np.empty((n, topk), np.int32),
+        "scores": np.empty((n, topk), np.float32),
+        "scores64": np.empty((n, topk), np.float64),
+        "next": np.empty((n,), np.float64),
+        "nvis": np.empty((n,), np.int32),
+    }
+    logits = np.empty((n, S_kv), np.float64) if want_logits else None
+    if n_threads is None:
+        n_threads = os.cpu_count() or 1
+    used = lib.oracle_indexer_fwd(
+        _ptr(qb), _ptr(kb), _ptr(wf), S, B, H, D, S_kv, int(compress_ratio),
+        int(topk), _ptr(qp), _ptr(gi), _ptr(rows), n,
+        _ptr(out["idx"]), _ptr(out["scores"]), _ptr(out["scores64"]),
+        _ptr(out["next"]), _ptr(out["nvis"]), _ptr(logits), int(n_threads))
+    if want_logits:
+        out["logits"] = logits
+    out["threads"] = used
+    out["rows"] = rows
+    return out

@@ -1,0 +1,250 @@
+/*
+ * CPU oracle for the DSA lightning-indexer forward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  The CUDA product path
+ * never links, calls or includes it, and this file shares no code with it.
+ *
+ * Plain, slow, obviously correct: every product and sum in double precision,
+ * straight loops in the order the definition is written, a library sort for
+ * the selection.  bf16 inputs are widened exactly to double; the only
+ * rounding to fp32 happens when a score is stored into an fp32 output.
+ *
+ * What it computes (all page references are to the NeMo AutoModel page
+ * "nemo_automodel.components.models.deepseek_v4.kernels.tilelang_indexer",
+ * unless another page is named):
+ *
+ *  - Layouts, from the `V4IndexerFunction` docstring and the
+ *    `v4_lighting_indexer` parameter list:
+ *        q [S, B, H, D] bf16, k [S_kv, B, D] bf16, w [S, B, H] fp32,
+ *        topk_indices [B, S, topk] int32, returned scores [B, S, topk] fp32.
+ *  - The lightning-indexer score of query t against compressed key j:
+ *        I[t, j] = sum_h w[t, h] * ReLU( sum_d q[t, h, d] * k[j, d] )
+ *    (the pages name the "lighting_indexer" but do not print the formula;
+ *    this is the DeepSeek Sparse Attention lightning-indexer definition).
+ *  - Causal masking over compressed keys ("Adapts GLM-5's lighting_indexer
+ *    to V4's SBHD data layout and causal masking"; `compress_ratio`,
+ *    "compression ratio (4 for C4 layers)"): compressed key j summarises
+ *    source tokens [j*r, (j+1)*r), and a key counts only when its whole block
+ *    is at or before the query position, (j+1)*r - 1 <= t.  This is the same
+ *    rule as "a trailing partial pool is not a pool" on the metrale.ai page
+ *    "Module glm5next_dsa", section "Checkpoint and kernel facts".
+ *  - Top-k: the `topk` visible keys with the largest score, returned in
+ *    descending score order, equal scores ordered by the lower key index
+ *    first; slots past the number of visible keys hold index -1 ("-1 =
+ *    invalid", page "Module glm5next_dsa", section "Shape of the pipeline";
+ *    "writes -1 over the whole index row before it stores any index",
+ *    section "Checkpoint and kernel facts") and score -inf.
+ *  - Given indices (`topk_indices` parameter, and `pytorch_extract_topk_scores
+ *    (logits, topk_indices, dim=-1)`): the score of each given slot is the
+ *    logit at that index, -inf where the index is -1, out of range or not
+ *    visible (a masked logit is -inf); the indices are returned unchanged.
+ *
+ * Query positions: prefill rows sit at position t = s; when q_pos is given,
+ * row s of sequence b sits at position q_pos[b] + s (decode rows).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* exact widening of a bf16 bit pattern: bf16 is the top half of an fp32 */
+static double bf16_to_double(uint16_t bits)
+{
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* causal visibility of compressed key j for a query at position t */
+int oracle_key_visible(long long j, long long t, int ratio)
+{
+    return (j + 1) * (long long)ratio - 1 <= t;
+}
+
+static long long row_position(const int32_t *q_pos, int b, int s)
+{
+    return q_pos ? (long long)q_pos[b] + s : (long long)s;
+}
+
+typedef struct {
+    const uint16_t *q;
+    const uint16_t *k;
+    const float *w;
+    int S, B, H, D, S_kv, ratio;
+} problem_t;
+
+/* I[t, j] for one (row, key) pair, the definition written out */
+static double score_one(const problem_t *p, int b, int s, long long j)
+{
+    double total = 0.0;
+    for (int h = 0; h < p->H; ++h) {
+        const uint16_t *qh = p->q + (((size_t)s * p->B + b) * p->H + h) * p->D;
+        const uint16_t *kj = p->k + ((size_t)j * p->B + b) * p->D;
+        double dot = 0.0;
+        for (int d = 0; d < p->D; ++d)
+            dot += bf16_to_double(qh[d]) * bf16_to_double(kj[d]);
+        double relu = dot > 0.0 ? dot : 0.0;
+        double wt = (double)p->w[((size_t)s * p->B + b) * p->H + h];
+        total += wt * relu;
+    }
+    return total;
+}
+
+typedef struct {
+    double score;
+    int32_t j;
+} cand_t;
+
+/* descending score, then ascending key index (equal scores: lower j first) */
+static int cand_cmp(const void *a, const void *b)
+{
+    const cand_t *x = (const cand_t *)a, *y = (const cand_t *)b;
+    if (x->score > y->score) return -1;
+    if (x->score < y->score) return 1;
+    return (x->j > y->j) - (x->j < y->j);
+}
+
+/* ---- row-parallel driver ------------------------------------------------ */
+
+typedef struct {
+    const problem_t *p;
+    const int32_t *q_pos;
+    const int64_t *rows; /* row id = b * S + s */
+    long long n_rows;
+    int topk;
+    const int32_t *in_idx; /* [B, S, topk] or NULL */
+    /* outputs, one line of `topk` per requested row */
+    int32_t *out_idx;
+    float *out_scores;
+    double *out_scores_f64;
+    double *out_next; /* score of the (topk+1)-th visible key, or -inf */
+    int32_t *out_nvis;
+    double *logits; /* [n_rows, S_kv] or NULL */
+    long long next_row;
+    pthread_mutex_t lock;
+} job_t;
+
+static void do_row(job_t *jb, long long r)
+{
+    const problem_t *p = jb->p;
+    long long row = jb->rows[r];
+    int b = (int)(row / p->S), s = (int)(row % p->S);
+    long long t = row_position(jb->q_pos, b, s);
+    int topk = jb->topk;
+
+    if (jb->logits) {
+        double *L = jb->logits + (size_t)r * p->S_kv;
+        for (long long j = 0; j < p->S_kv; ++j)
+            L[j] = oracle_key_visible(j, t, p->ratio) ? score_one(p, b, s, j)
+                                                       : -INFINITY;
+    }
+
+    if (jb->in_idx) {
+        const int32_t *given = jb->in_idx + ((size_t)b * p->S + s) * topk;
+        int32_t nvis = 0;
+        for (long long j = 0; j < p->S_kv; ++j)
+            nvis += oracle_key_visible(j, t, p->ratio);
+        for (int i = 0; i < topk; ++i) {
+            int32_t j = given[i];
+            double v = -INFINITY;
+            if (j >= 0 && j < p->S_kv && oracle_key_visible(j, t, p->ratio))
+                v = score_one(p, b, s, j);
+            if (jb->out_idx) jb->out_idx[(size_t)r * topk + i] = j;
+            if (jb->out_scores) jb->out_scores[(size_t)r * topk + i] = (float)v;
+            if (jb->out_scores_f64) jb->out_scores_f64[(size_t)r * topk + i] = v;
+        }
+        if (jb->out_nvis) jb->out_nvis[r] = nvis;
+        if (jb->out_next) jb->out_next[r] = -INFINITY;
+        return;
+    }
+
+    if (!jb->out_idx && !jb->out_scores && !jb->out_scores_f64) return;
+
+    cand_t *c = (cand_t *)malloc(sizeof(cand_t) * (size_t)(p->S_kv > 0 ? p->S_kv : 1));
+    long long n = 0;
+    for (long long j = 0; j < p->S_kv; ++j) {
+        if (!oracle_key_visible(j, t, p->ratio)) continue;
+        c[n].score = jb->logits ? jb->logits[(size_t)r * p->S_kv + j]
+                                : score_one(p, b, s, j);
+        c[n].j = (int32_t)j;
+        ++n;
+    }
+    qsort(c, (size_t)n, sizeof(cand_t), cand_cmp);
+    for (int i = 0; i < topk; ++i) {
+        int32_t j = i < n ? c[i].j : -1;
+        double v = i < n ? c[i].score : -INFINITY;
+        if (jb->out_idx) jb->out_idx[(size_t)r * topk + i] = j;
+        if (jb->out_scores) jb->out_scores[(size_t)r * topk + i] = (float)v;
+        if (jb->out_scores_f64) jb->out_scores_f64[(size_t)r * topk + i] = v;
+    }
+    if (jb->out_next) jb->out_next[r] = topk < n ? c[topk].score : -INFINITY;
+    if (jb->out_nvis) jb->out_nvis[r] = (int32_t)n;
+    free(c);
+}
+
+static void *worker(void *arg)
+{
+    job_t *jb = (job_t *)arg;
+    for (;;) {
+        pthread_mutex_lock(&jb->lock);
+        long long r = jb->next_row++;
+        pthread_mutex_unlock(&jb->lock);
+        if (r >= jb->n_rows) break;
+        do_row(jb, r);
+    }
+    return NULL;
+}
+
+/*
+ * The whole forward for a list of rows.
+ *
+ * q, k: bf16 bit patterns; w fp32; q_pos [B] or NULL; rows: row ids b*S+s.
+ * in_idx NULL -> top-k path; else the given-indices path.
+ * Any output pointer may be NULL.  Per requested row r:
+ *   out_idx[r*topk + i], out_scores[...] (fp32), out_scores_f64[...] (fp64),
+ *   out_next[r] = (topk+1)-th visible score (-inf if none; top-k path),
+ *   out_nvis[r] = number of visible keys,
+ *   logits[r*S_kv + j] = I[t, j] or -inf where key j is not visible.
+ * Returns the number of threads used.
+ */
+int oracle_indexer_fwd(const uint16_t *q, const uint16_t *k, const float *w,
+                       int S, int B, int H, int D, int S_kv, int ratio,
+                       int topk, const int32_t *q_pos, const int32_t *in_idx,
+                       const int64_t *rows, long long n_rows,
+                       int32_t *out_idx, float *out_scores,
+                       double *out_scores_f64, double *out_next,
+                       int32_t *out_nvis, double *logits, int n_threads)
+{
+    problem_t p = {q, k, w, S, B, H, D, S_kv, ratio};
+    job_t jb;
+    memset(&jb, 0, sizeof jb);
+    jb.p = &p;
+    jb.q_pos = q_pos;
+    jb.rows = rows;
+    jb.n_rows = n_rows;
+    jb.topk = topk;
+    jb.in_idx = in_idx;
+    jb.out_idx = out_idx;
+    jb.out_scores = out_scores;
+    jb.out_scores_f64 = out_scores_f64;
+    jb.out_next = out_next;
+    jb.out_nvis = out_nvis;
+    jb.logits = logits;
+    jb.next_row = 0;
+    pthread_mutex_init(&jb.lock, NULL);
+
+    if (n_threads < 1) n_threads = 1;
+    if (n_threads > 256) n_threads = 256;
+    if ((long long)n_threads > n_rows) n_threads = n_rows > 0 ? (int)n_rows : 1;
+    pthread_t th[256];
+    int started = 0;
+    for (int i = 1; i < n_threads; ++i)
+        if (pthread_create(&th[started], NULL, worker, &jb) == 0) ++started;
+    worker(&jb);
+    for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
+    pthread_mutex_destroy(&jb.lock);
+    return started + 1;
+}

@@ -1,0 +1,321 @@
+"""Pins for the CPU oracle (no GPU).
+
+Each test ties the oracle to something other than itself: a hand-worked
+example, a library routine that the definition reduces to in a special case,
+exact rational brute force, closed forms and invariants.  The plausible
+mistakes each one catches are named in its docstring.
+"""
+from __future__ import annotations
+
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dsa_inputs import WORKLOADS, Workload, make_given_indices, make_inputs
+from tests.helpers import n_visible_closed_form
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_example.txt")
+
+
+def _f(s: str) -> float:
+    return -math.inf if s == "-inf" else float(s)
+
+
+def load_hand_example():
+    q = np.zeros((5, 1, 2, 2), np.float32)
+    k = np.zeros((4, 1, 2), np.float32)
+    w = np.zeros((5, 1, 2), np.float32)
+    topk, gather = [], []
+    with open(GOLDEN) as fh:
+        for line in fh:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            tag, *v = line.split()
+            if tag == "q":
+                t, h, a, b = v
+                q[int(t), 0, int(h)] = (float(a), float(b))
+            elif tag == "k":
+                j, a, b = v
+                k[int(j), 0] = (float(a), float(b))
+            elif tag == "w":
+                t, a, b = v
+                w[int(t), 0] = (float(a), float(b))
+            elif tag == "topk":
+                r, t, i0, i1, s0, s1 = v
+                topk.append((int(r), int(t), [int(i0), int(i1)], [_f(s0), _f(s1)]))
+            elif tag == "gather":
+                t, i0, i1, s0, s1 = v
+                gather.append((int(t), [int(i0), int(i1)], [_f(s0), _f(s1)]))
+    to_bf = lambda a: torch.from_numpy(a).to(torch.bfloat16)
+    return to_bf(q), to_bf(k), torch.from_numpy(w), topk, gather
+
+
+def test_hand_example_topk():
+    """Hand-derived values: pins the head sum, ReLU, w multiply, the causal
+    rule at r = 1, 2, 4, the tie order (three-way tie at t=3) and padding."""
+    q, k, w, topk, _ = load_hand_example()
+    for r in (1, 2, 4):
+        out = oracle.indexer_fwd(q, k, w, r, 2)
+        for rr, t, idx, sc in topk:
+            if rr != r:
+                continue
+            assert out["idx"][t].tolist() == idx, (r, t, out["idx"][t])
+            assert out["scores"][t].tolist() == sc, (r, t, out["scores"][t])
+
+
+def test_hand_example_gather():
+    """Hand-derived given-indices values: -1, invisible and out-of-range
+    indices give -inf; indices are returned unchanged."""
+    q, k, w, _, gather = load_hand_example()
+    in_idx = torch.tensor([[g[1] for g in gather]], dtype=torch.int32)
+    out = oracle.indexer_fwd(q, k, w, 1, 2, in_idx=in_idx)
+    for t, idx, sc in gather:
+        assert out["idx"][t].tolist() == idx
+        assert out["scores"][t].tolist() == sc
+
+
+def _rand_problem(S, B, H, D, S_kv, seed, w_scale=0.5):
+    wl = Workload("t", B=B, S=S, S_kv=S_kv, H=H, D=D, compress_ratio=1,
+                  topk=4, w_scale=w_scale, seed=seed)
+    q, k, w, _ = make_inputs(wl)
+    return q, k, w
+
+
+def test_single_head_unit_weight_is_relu_of_matmul():
+    """H=1, w=1, r=1: I = ReLU(Q K^T) under a lower-triangular mask.  Checked
+    against numpy's matmul; catches a transposed operand, a wrong q or k
+    stride, or a wrong mask direction."""
+    S, B, H, D = 40, 2, 1, 24
+    q, k, _ = _rand_problem(S, B, H, D, S, seed=7)
+    w = torch.ones((S, B, H), dtype=torch.float32)
+    out = oracle.indexer_fwd(q, k, w, 1, 4, want_logits=True)
+    L = out["logits"].reshape(B, S, S)
+    qd = q.float().double().numpy()
+    kd = k.float().double().numpy()
+    for b in range(B):
+        ref = np.maximum(qd[:, b, 0, :] @ kd[:, b, :].T, 0.0)
+        mask = np.tril(np.ones((S, S), bool))
+        ref = np.where(mask, ref, -np.inf)
+        np.testing.assert_allclose(L[b], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_relu_odd_part_is_linear():
+    """ReLU(x) - ReLU(-x) = x, so I(q) - I(-q) = (sum_h w_h q_h) . k_j, a
+    plain matmul.  Catches a dropped head, a wrong w index, a sign error and
+    a wrong batch stride (B=2, H=3)."""
+    S, B, H, D = 24, 2, 3, 16
+    q, k, w = _rand_problem(S, B, H, D, S, seed=8)
+    a = oracle.indexer_fwd(q, k, w, 1, 4, want_logits=True)["logits"]
+    b_ = oracle.indexer_fwd(-q, k, w, 1, 4, want_logits=True)["logits"]
+    with np.errstate(invalid="ignore"):
+        diff = (a - b_).reshape(B, S, S)
+    qd = q.float().double().numpy()
+    kd = k.float().double().numpy()
+    wd = w.double().numpy()
+    for b in range(B):
+        qbar = np.einsum("sh,shd->sd", wd[:, b, :], qd[:, b, :, :])
+        ref = qbar @ kd[:, b, :].T
+        mask = np.tril(np.ones((S, S), bool))
+        np.testing.assert_allclose(diff[b][mask], ref[mask], rtol=1e-10,
+                                   atol=1e-10)
+
+
+def test_batches_are_independent():
+    """The oracle on a B=2 problem equals the oracle on each batch alone.
+    Catches a batch/sequence stride mix-up in the SBHD layouts."""
+    S, B, H, D = 20, 2, 4, 8
+    q, k, w = _rand_problem(S, B, H, D, S, seed=9)
+    both = oracle.indexer_fwd(q, k, w, 1, 5, want_logits=True)
+    for b in range(B):
+        one = oracle.indexer_fwd(q[:, b:b + 1].contiguous(),
+                                 k[:, b:b + 1].contiguous(),
+                                 w[:, b:b + 1].contiguous(), 1, 5,
+                                 want_logits=True)
+        sl = slice(b * S, (b + 1) * S)
+        np.testing.assert_array_equal(both["logits"][sl], one["logits"])
+        np.testing.assert_array_equal(both["idx"][sl], one["idx"])
+
+
+def test_head_permutation_invariance():
+    """Permuting heads of q and w together leaves I unchanged; permuting
+    only w changes it (so w really is indexed per head)."""
+    S, B, H, D = 16, 1, 6, 8
+    q, k, w = _rand_problem(S, B, H, D, S, seed=10)
+    perm = torch.tensor([3, 0, 5, 1, 4, 2])
+    L0 = oracle.indexer_fwd(q, k, w, 1, 3, want_logits=True)["logits"]
+    L1 = oracle.indexer_fwd(q[:, :, perm].contiguous(), k,
+                            w[:, :, perm].contiguous(), 1, 3,
+                            want_logits=True)["logits"]
+    L2 = oracle.indexer_fwd(q, k, w[:, :, perm].contiguous(), 1, 3,
+                            want_logits=True)["logits"]
+    fin = np.isfinite(L0)
+    np.testing.assert_allclose(L1[fin], L0[fin], rtol=1e-12, atol=1e-12)
+    assert not np.allclose(L2[fin], L0[fin])
+
+
+@pytest.mark.parametrize("ratio", [1, 2, 3, 4, 7])
+def test_visible_counts_closed_form(ratio):
+    """Visible-key count and -1 padding count follow the closed forms
+    n_vis = clamp(floor((t+1)/r), 0, S_kv), pad = max(0, topk - n_vis)."""
+    S, B, H, D, S_kv, topk = 50, 1, 2, 8, 9, 5
+    q, k, w = _rand_problem(S, B, H, D, S_kv, seed=11)
+    out = oracle.indexer_fwd(q, k, w, ratio, topk, want_logits=True)
+    for t in range(S):
+        n = n_visible_closed_form(t, ratio, S_kv)
+        assert out["nvis"][t] == n
+        assert np.sum(np.isfinite(out["logits"][t])) == n
+        assert np.all(np.isfinite(out["logits"][t][:n]))
+        assert np.sum(out["idx"][t] == -1) == max(0, topk - n)
+        for j in range(S_kv):
+            assert oracle.key_visible(j, t, ratio) == (j < n)
+
+
+def test_decode_position_matches_prefill_row():
+    """A decode row at q_pos = p scores like prefill row p of the same
+    query: pins the q_pos reading pos = q_pos[b] + s."""
+    S, B, H, D, S_kv, r = 37, 1, 4, 16, 9, 4
+    q, k, w = _rand_problem(S, B, H, D, S_kv, seed=12)
+    pre = oracle.indexer_fwd(q, k, w, r, 6, want_logits=True)
+    for p in (0, 3, 4, 18, 36):
+        dec = oracle.indexer_fwd(q[p:p + 1].contiguous(), k,
+                                 w[p:p + 1].contiguous(), r, 6,
+                                 q_pos=torch.tensor([p], dtype=torch.int32),
+                                 want_logits=True)
+        np.testing.assert_array_equal(dec["logits"][0], pre["logits"][p])
+        np.testing.assert_array_equal(dec["idx"][0], pre["idx"][p])
+
+
+def _exact_scores(qi, ki, wi, ratio, b, s, t):
+    """Exact rational I[t, j] for integer q, k and dyadic w, by brute force."""
+    S, B, H, D = qi.shape
+    S_kv = ki.shape[0]
+    out = {}
+    for j in range(S_kv):
+        if (j + 1) * ratio - 1 > t:
+            continue
+        tot = Fraction(0)
+        for h in range(H):
+            dot = sum(int(qi[s, b, h, d]) * int(ki[j, b, d]) for d in range(D))
+            tot += Fraction(wi[s, b, h]) * max(dot, 0)
+        out[j] = tot
+    return out
+
+
+@pytest.mark.parametrize("ratio,topk", [(1, 6), (2, 4), (4, 3), (1, 40)])
+def test_integer_inputs_match_exact_brute_force(ratio, topk):
+    """Integer q, k in [-3, 3] and w in {+-1, +-1/2, +-1/4}: every score is
+    exact, ties are frequent.  The oracle must equal exact rational brute
+    force with k rounds of argmax (lowest j wins a tie), bit for bit."""
+    rng = np.random.default_rng(123 + ratio)
+    S, B, H, D, S_kv = 30, 2, 3, 5, 12
+    qi = rng.integers(-3, 4, size=(S, B, H, D))
+    ki = rng.integers(-3, 4, size=(S_kv, B, D))
+    wi = rng.choice([1, -1, 0.5, -0.5, 0.25, -0.25], size=(S, B, H))
+    q = torch.from_numpy(qi.astype(np.float32)).to(torch.bfloat16)
+    k = torch.from_numpy(ki.astype(np.float32)).to(torch.bfloat16)
+    w = torch.from_numpy(wi.astype(np.float32))
+    out = oracle.indexer_fwd(q, k, w, ratio, topk)
+    for b in range(B):
+        for s in range(S):
+            sc = _exact_scores(qi, ki, wi, ratio, b, s, s)
+            left = dict(sc)
+            want_i, want_s = [], []
+            for _ in range(topk):
+                if not left:
+                    want_i.append(-1)
+                    want_s.append(-math.inf)
+                    continue
+                best = max(left.values())
+                j = min(jj for jj, v in left.items() if v == best)
+                want_i.append(j)
+                want_s.append(float(best))
+                del left[j]
+            r = b * S + s
+            assert out["idx"][r].tolist() == want_i, (b, s)
+            assert out["scores"][r].tolist() == want_s, (b, s)
+
+
+def test_topk_invariants_random():
+    """On random bf16 inputs: kept indices are visible and distinct, scores
+    non-increasing, every kept score >= every dropped visible score, and the
+    (k+1)-th score reported equals the largest dropped one."""
+    S, B, H, D, S_kv, r, topk = 64, 2, 4, 32, 32, 2, 7
+    q, k, w = _rand_problem(S, B, H, D, S_kv, seed=13)
+    out = oracle.indexer_fwd(q, k, w, r, topk, want_logits=True)
+    for row in range(B * S):
+        s = row % S
+        L = out["logits"][row]
+        idx = out["idx"][row]
+        sc = out["scores64"][row]
+        valid = idx >= 0
+        n = n_visible_closed_form(s, r, S_kv)
+        assert valid.sum() == min(topk, n)
+        assert np.all(idx[valid] < n)
+        assert len(set(idx[valid].tolist())) == valid.sum()
+        assert np.all(np.diff(sc[valid]) <= 0)
+        np.testing.assert_array_equal(sc[valid], L[idx[valid]])
+        dropped = np.setdiff1d(np.arange(n), idx[valid])
+        if dropped.size:
+            assert sc[valid].min() >= L[dropped].max()
+            assert out["next"][row] == L[dropped].max()
+        else:
+            assert out["next"][row] == -np.inf
+
+
+def test_topk_at_least_visible_returns_all():
+    """topk >= n_vis returns every visible key, sorted."""
+    S, B, H, D, S_kv = 12, 1, 2, 8, 12
+    q, k, w = _rand_problem(S, B, H, D, S_kv, seed=14)
+    out = oracle.indexer_fwd(q, k, w, 1, S_kv + 3, want_logits=True)
+    for t in range(S):
+        idx = out["idx"][t]
+        assert sorted(idx[idx >= 0].tolist()) == list(range(t + 1))
+
+
+def test_gather_reproduces_topk_scores():
+    """Feeding the oracle's own top-k indices back through the given-indices
+    path reproduces its scores exactly; -1 slots give -inf."""
+    S, B, H, D, S_kv, r, topk = 40, 2, 4, 16, 20, 2, 6
+    q, k, w = _rand_problem(S, B, H, D, S_kv, seed=15)
+    top = oracle.indexer_fwd(q, k, w, r, topk)
+    in_idx = torch.from_numpy(top["idx"].reshape(B, S, topk))
+    g = oracle.indexer_fwd(q, k, w, r, topk, in_idx=in_idx)
+    np.testing.assert_array_equal(g["idx"], top["idx"])
+    np.testing.assert_array_equal(g["scores"], top["scores"])
+
+
+def test_gather_random_valid_indices():
+    """Random valid indices (the input generator's recipe) gather the same
+    values as the full logit row."""
+    S, B, H, D, S_kv, r, topk = 30, 2, 2, 8, 16, 2, 5
+    q, k, w = _rand_problem(S, B, H, D, S_kv, seed=16)
+    lim = np.array([[n_visible_closed_form(s, r, S_kv) for s in range(S)]
+                    for _ in range(B)])
+    in_idx = make_given_indices(B, S, topk, lim, seed=3)
+    full = oracle.indexer_fwd(q, k, w, r, topk, want_logits=True)
+    g = oracle.indexer_fwd(q, k, w, r, topk, in_idx=in_idx)
+    gi = in_idx.numpy().reshape(B * S, topk)
+    for row in range(B * S):
+        for i in range(topk):
+            j = gi[row, i]
+            want = -np.inf if j < 0 else full["logits"][row, j]
+            assert g["scores64"][row, i] == want
+
+
+def test_workload_recipes_have_stated_shapes():
+    """The synthetic recipes keep the shapes and scales they are named for."""
+    wl = WORKLOADS["tiny"]
+    q, k, w, pos = make_inputs(wl)
+    assert q.shape == (128, 1, 4, 32) and q.dtype == torch.bfloat16
+    assert k.shape == (128, 1, 32) and w.shape == (128, 1, 4)
+    assert pos is None
+    dec = WORKLOADS["decode"]
+    assert dec.S_kv * dec.compress_ratio >= dec.pos_range[1]
+    g = torch.Generator().manual_seed(0)
+    assert abs(float(torch.randn(10000, generator=g).std()) - 1.0) < 0.05
