@@ -118,15 +118,7 @@ def make_given_indices(B: int, S: int, topk: int, row_limits: np.ndarray,
             m = min(topk, n)
             if m <= 0:
                 continue
-            if n <= 4 * m:
-                perm = rng.permutation(n)[:m]
-            else:
-                # sparse draw: rejection of duplicates keeps it O(m)
-                perm = np.unique(rng.integers(0, n, size=2 * m))
-                while perm.size < m:
-                    perm = np.unique(np.concatenate(
-                        [perm, rng.integers(0, n, size=m)]))
-                perm = rng.permutation(perm)[:m]
+            perm = rng.choice(n, size=m, replace=False, shuffle=True)
             out[b, s, :m] = perm
     return torch.from_numpy(out)
 

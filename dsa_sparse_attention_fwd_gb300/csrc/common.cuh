@@ -1,0 +1,69 @@
+// Shared definitions of the CUDA library: problem description, the causal
+// visibility rule and the launchers each kernel file provides.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dsa {
+
+// Bits of the device status word at the start of the workspace.
+constexpr int kStatusIndexRange = 1;  // a given index outside [-1, S_kv)
+constexpr int kStatusTimeout = 2;     // a bounded wait expired
+
+// One indexer problem, as the C ABI receives it (device pointers).
+struct Problem {
+  const void *q;         // [S, B, H, D] bf16
+  const void *k;         // [S_kv, B, D] bf16
+  const float *w;        // [S, B, H] fp32
+  const int32_t *q_pos;  // [B] or nullptr: row s of sequence b at q_pos[b]+s
+  int S, B, H, D, S_kv, ratio;
+};
+
+// Position of query row s of sequence b.
+__device__ __forceinline__ long long row_pos(const int32_t *q_pos, int b,
+                                             int s) {
+  return q_pos ? (long long)__ldg(q_pos + b) + s : (long long)s;
+}
+
+// Causal rule over compressed keys (DeepSeek-V4 indexer, "causal masking";
+// a compressed key stands for source tokens [j*r, (j+1)*r) and is visible
+// only when the whole block is at or before the query): (j+1)*r - 1 <= pos.
+// Returns how many keys (a prefix 0..n-1) are visible.
+__host__ __device__ __forceinline__ int n_visible(long long pos, int ratio,
+                                                  int S_kv) {
+  if (pos < 0) return 0;
+  long long n = (pos + 1) / ratio;
+  return n < (long long)S_kv ? (int)n : S_kv;
+}
+
+// Scoring kernel tile geometry.
+constexpr int kTileKeys = 128;      // MMA M: compressed keys per tile
+constexpr int kTileCols = 256;      // MMA N: (query, head) columns per tile
+constexpr int kChunk = 64;          // bf16 per 128-byte swizzled row
+constexpr int kStages = 4;          // K-tile pipeline depth
+constexpr int kScoreThreads = 320;  // TMA warp, MMA warp, 8 epilogue warps
+
+// Launchers (return cudaSuccess or the launch error).  `logits` is
+// [B, S, S_kv] fp32; only visible entries are written.
+cudaError_t launch_index_scores(const Problem &p, const CUtensorMap &tm_q,
+                                const CUtensorMap &tm_k, float *logits,
+                                int *status, int num_sms, cudaStream_t st);
+size_t index_scores_smem_bytes(int D);
+
+cudaError_t launch_topk_select(const Problem &p, const float *logits, int topk,
+                               int32_t *out_idx, float *out_scores,
+                               cudaStream_t st);
+size_t topk_select_smem_bytes(int S_kv, int topk);
+
+cudaError_t launch_gather_scores(const Problem &p, const float *logits,
+                                 const int32_t *in_idx, int topk,
+                                 int32_t *out_idx, float *out_scores,
+                                 int *status, int num_sms, cudaStream_t st);
+
+cudaError_t launch_fill_masked(float *logits, size_t n, cudaStream_t st);
+
+cudaError_t launch_wait_selftest(int limit_us, int *status, cudaStream_t st);
+
+}  // namespace dsa

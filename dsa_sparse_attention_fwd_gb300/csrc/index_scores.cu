@@ -1,0 +1,340 @@
+// index_scores: the lightning-indexer score I[t, j] = sum_h w[t,h] *
+// ReLU(q[t,h,:] . k[j,:]) for every visible (query, compressed key) pair,
+// on the sm_103a tensor cores.
+//
+// Orientation: one MMA tile is 128 keys (M) x 256 (query, head) columns (N),
+// K = D.  A = a K tile [128 keys x D] and B = a Q tile [256/H queries x H
+// heads x D], both K-major in shared memory with the 128-byte swizzle, staged
+// by TMA.  The fp32 accumulator lives in tensor memory: TMEM lane = key,
+// column = (query, head).  Each epilogue thread owns one key, so the per-head
+// weighted ReLU sum runs along its own registers with no cross-thread
+// reduction.  Two accumulators (2 x 256 TMEM columns) let the epilogue of
+// tile i overlap the MMA of tile i+1.
+//
+// Warp roles (320 threads, one CTA per SM, persistent):
+//   warp 0      TMA producer: Q tile once per work item, K tiles through a
+//               4-stage ring.
+//   warp 1      TMEM allocator and MMA issuer (one thread).
+//   warps 2..9  epilogue: TMEM -> registers, ReLU, weight multiply-reduce over
+//               heads, causal mask, store of the visible scores.
+// A work item is (sequence b, block of 256/H consecutive queries); its key
+// tiles stop at the last tile any of its queries can see, so fully masked
+// tiles are never loaded or multiplied.  Items are dealt to CTAs in a
+// zig-zag over a longest-first order to balance the causal triangle.
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace dsa {
+namespace {
+
+template <int KC>
+struct ScoreSmem {
+  static constexpr int kQBytes = KC * kTileCols * 128;  // Q tile
+  static constexpr int kKBytes = KC * kTileKeys * 128;  // one K stage
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kQBytes;
+  static constexpr int kOffW = kOffK + kStages * kKBytes;
+  static constexpr int kOffBar = kOffW + kTileCols * 4;
+  // barriers: k_full[S], k_empty[S], q_full, q_empty, acc_full[2], acc_empty[2]
+  static constexpr int kNumBars = 2 * kStages + 2 + 4;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kBytes = kOffMisc + 16;
+  static constexpr int kAlloc = kBytes + 1024;  // room to align the base
+};
+
+struct ItemInfo {
+  int b, t0, ntiles;
+};
+
+template <int H>
+__device__ __forceinline__ ItemInfo item_info(int item, int S, int B,
+                                              int S_kv, int ratio,
+                                              const int32_t *q_pos) {
+  constexpr int TQ = kTileCols / H;
+  const int n_qb = (S + TQ - 1) / TQ;
+  ItemInfo it;
+  const int qb = n_qb - 1 - item / B;  // longest (latest) query blocks first
+  it.b = item % B;
+  it.t0 = qb * TQ;
+  const int t_last = min(it.t0 + TQ - 1, S - 1);
+  const int nv = n_visible(row_pos(q_pos, it.b, t_last), ratio, S_kv);
+  it.ntiles = (nv + kTileKeys - 1) / kTileKeys;
+  return it;
+}
+
+// Zig-zag deal of items to CTAs: round r gives CTA c item r*G + c (r even) or
+// r*G + G-1-c (r odd).  Returns -1 past the end.
+__device__ __forceinline__ int item_for(int round, int n_items) {
+  const int G = gridDim.x, c = blockIdx.x;
+  const int idx = round * G + ((round & 1) ? (G - 1 - c) : c);
+  return idx < n_items ? idx : -1;
+}
+
+template <int H, int KC>
+__global__ void __launch_bounds__(kScoreThreads, 1)
+    index_scores_kernel(const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_k,
+                        const float *__restrict__ w,
+                        const int32_t *__restrict__ q_pos,
+                        float *__restrict__ logits, int S, int B, int S_kv,
+                        int ratio, int *status) {
+  using L = ScoreSmem<KC>;
+  constexpr int TQ = kTileCols / H;  // queries per work item
+  constexpr int QH = TQ / 2;         // queries per epilogue column half
+  constexpr uint32_t kIdesc = idesc_bf16_f32(kTileKeys, kTileCols);
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t *smem = smem_raw + (base - raw_addr);
+
+  const uint32_t sQ = base + L::kOffQ;
+  const uint32_t sK = base + L::kOffK;
+  float *sW = reinterpret_cast<float *>(smem + L::kOffW);
+  const uint32_t bars = base + L::kOffBar;
+  auto k_full = [&](int s) { return bars + 8u * s; };
+  auto k_empty = [&](int s) { return bars + 8u * (kStages + s); };
+  const uint32_t q_full = bars + 8u * (2 * kStages);
+  const uint32_t q_empty = q_full + 8u;
+  auto acc_full = [&](int a) { return bars + 8u * (2 * kStages + 2 + a); };
+  auto acc_empty = [&](int a) { return bars + 8u * (2 * kStages + 4 + a); };
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kOffMisc);
+  volatile int *abort_flag = reinterpret_cast<int *>(smem + L::kOffMisc + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n_items = ((S + TQ - 1) / TQ) * B;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(k_full(s), 1);
+      mbar_init(k_empty(s), 1);
+    }
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(acc_full(a), 1);
+      mbar_init(acc_empty(a), 8);  // one arrival per epilogue warp
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      uint32_t kst = 0, kph = 0, qph = 0;
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const int item = item_for(r, n_items);
+        if (item < 0) break;
+        const ItemInfo it = item_info<H>(item, S, B, S_kv, ratio, q_pos);
+        if (it.ntiles == 0) continue;
+        if (!(ok = wait_bar(q_empty, qph ^ 1u, abort_flag, status))) break;
+        qph ^= 1u;
+        mbar_arrive_expect_tx(q_full, L::kQBytes);
+        for (int c = 0; c < KC; ++c)
+          tma_load_4d(sQ + c * (kTileCols * 128), &tm_q, q_full, c * kChunk,
+                      0, it.b, it.t0);
+        for (int tile = 0; tile < it.ntiles; ++tile) {
+          if (!(ok = wait_bar(k_empty(kst), kph ^ 1u, abort_flag, status)))
+            break;
+          mbar_arrive_expect_tx(k_full(kst), L::kKBytes);
+          for (int c = 0; c < KC; ++c)
+            tma_load_3d(sK + kst * L::kKBytes + c * (kTileKeys * 128), &tm_k,
+                        k_full(kst), c * kChunk, it.b, tile * kTileKeys);
+          if (++kst == kStages) {
+            kst = 0;
+            kph ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      uint32_t kst = 0, kph = 0, qph = 0, acc = 0, aph = 0;
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const int item = item_for(r, n_items);
+        if (item < 0) break;
+        const ItemInfo it = item_info<H>(item, S, B, S_kv, ratio, q_pos);
+        if (it.ntiles == 0) continue;
+        if (!(ok = wait_bar(q_full, qph, abort_flag, status))) break;
+        qph ^= 1u;
+        for (int tile = 0; tile < it.ntiles; ++tile) {
+          if (!(ok = wait_bar(acc_empty(acc), aph ^ 1u, abort_flag, status)))
+            break;
+          if (!(ok = wait_bar(k_full(kst), kph, abort_flag, status))) break;
+          tc_fence_after();
+          const uint32_t d_tmem = tmem + acc * kTileCols;
+#pragma unroll
+          for (int c = 0; c < KC; ++c) {
+#pragma unroll
+            for (int kk = 0; kk < kChunk / 16; ++kk) {
+              const uint64_t ad = sdesc_k_sw128(
+                  sK + kst * L::kKBytes + c * (kTileKeys * 128) + kk * 32);
+              const uint64_t bd =
+                  sdesc_k_sw128(sQ + c * (kTileCols * 128) + kk * 32);
+              mma_bf16(d_tmem, ad, bd, kIdesc, (c | kk) != 0);
+            }
+          }
+          mma_commit(k_empty(kst));   // K stage reusable when done
+          mma_commit(acc_full(acc));  // accumulator ready
+          if (tile == it.ntiles - 1) mma_commit(q_empty);
+          if (++kst == kStages) {
+            kst = 0;
+            kph ^= 1u;
+          }
+          acc ^= 1u;
+          if (acc == 0) aph ^= 1u;
+        }
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 2..9) ----------------
+    const int ew = warp - 2;          // 0..7
+    const int sp = warp & 3;          // TMEM sub-partition of this warp
+    const int half = ew >> 2;         // which 128 columns
+    const int et = threadIdx.x - 64;  // 0..255
+    uint32_t acc = 0, aph = 0;
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+      const int item = item_for(r, n_items);
+      if (item < 0) break;
+      const ItemInfo it = item_info<H>(item, S, B, S_kv, ratio, q_pos);
+      if (it.ntiles == 0) continue;
+      named_bar_sync(1, 256);  // everyone is done with the previous weights
+      {
+        const int tq = et / H, h = et % H;
+        const int t = it.t0 + tq;
+        sW[et] = t < S ? __ldg(w + ((size_t)t * B + it.b) * H + h) : 0.f;
+      }
+      named_bar_sync(1, 256);
+      // position of query row t is qbase + t
+      const long long qbase = row_pos(q_pos, it.b, 0);
+
+      for (int tile = 0; tile < it.ntiles; ++tile) {
+        bool got = wait_bar(acc_full(acc), aph, abort_flag, status);
+        got = __all_sync(0xffffffffu, got);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem + ((uint32_t)(sp * 32) << 16) +
+                               acc * kTileCols + half * 128;
+        uint32_t v[4][32];
+        tmem_ld32(taddr + 0, v[0]);
+        tmem_ld32(taddr + 32, v[1]);
+        tmem_ld32(taddr + 64, v[2]);
+        tmem_ld32(taddr + 96, v[3]);
+        tmem_ld_wait();
+        reg_fence32(v[0]);
+        reg_fence32(v[1]);
+        reg_fence32(v[2]);
+        reg_fence32(v[3]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acc_empty(acc));
+
+        const int j = tile * kTileKeys + sp * 32 + lane;
+#pragma unroll
+        for (int qq = 0; qq < QH; ++qq) {
+          const int tq = half * QH + qq;
+          const float *wq = sW + tq * H;
+          float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+          for (int h = 0; h < H; h += 2) {
+            const int c0 = qq * H + h;
+            s0 = fmaf(wq[h], fmaxf(__uint_as_float(v[c0 >> 5][c0 & 31]), 0.f),
+                      s0);
+            if (h + 1 < H) {
+              const int c1 = c0 + 1;
+              s1 = fmaf(wq[h + 1],
+                        fmaxf(__uint_as_float(v[c1 >> 5][c1 & 31]), 0.f), s1);
+            }
+          }
+          const int t = it.t0 + tq;
+          const bool vis = (long long)(j + 1) * ratio - 1 <= qbase + t;
+          if (t < S && vis && j < S_kv)
+            logits[((size_t)it.b * S + t) * S_kv + j] = s0 + s1;
+        }
+        acc ^= 1u;
+        if (acc == 0) aph ^= 1u;
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int H, int KC>
+cudaError_t launch_t(const Problem &p, const CUtensorMap &tm_q,
+                     const CUtensorMap &tm_k, float *logits, int *status,
+                     int num_sms, cudaStream_t st) {
+  constexpr int TQ = kTileCols / H;
+  auto kern = index_scores_kernel<H, KC>;
+  const int smem = ScoreSmem<KC>::kAlloc;
+  cudaError_t e = cudaFuncSetAttribute(
+      kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const long long n_items = (long long)((p.S + TQ - 1) / TQ) * p.B;
+  const int grid = (int)(n_items < num_sms ? n_items : num_sms);
+  if (grid <= 0) return cudaSuccess;
+  kern<<<grid, kScoreThreads, smem, st>>>(tm_q, tm_k, p.w, p.q_pos, logits,
+                                          p.S, p.B, p.S_kv, p.ratio, status);
+  return cudaGetLastError();
+}
+
+template <int KC>
+cudaError_t launch_kc(const Problem &p, const CUtensorMap &tm_q,
+                      const CUtensorMap &tm_k, float *logits, int *status,
+                      int num_sms, cudaStream_t st) {
+  switch (p.H) {
+    case 1: return launch_t<1, KC>(p, tm_q, tm_k, logits, status, num_sms, st);
+    case 2: return launch_t<2, KC>(p, tm_q, tm_k, logits, status, num_sms, st);
+    case 4: return launch_t<4, KC>(p, tm_q, tm_k, logits, status, num_sms, st);
+    case 8: return launch_t<8, KC>(p, tm_q, tm_k, logits, status, num_sms, st);
+    case 16:
+      return launch_t<16, KC>(p, tm_q, tm_k, logits, status, num_sms, st);
+    case 32:
+      return launch_t<32, KC>(p, tm_q, tm_k, logits, status, num_sms, st);
+    case 64:
+      return launch_t<64, KC>(p, tm_q, tm_k, logits, status, num_sms, st);
+    case 128:
+      return launch_t<128, KC>(p, tm_q, tm_k, logits, status, num_sms, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+size_t index_scores_smem_bytes(int D) {
+  return D <= kChunk ? ScoreSmem<1>::kAlloc : ScoreSmem<2>::kAlloc;
+}
+
+cudaError_t launch_index_scores(const Problem &p, const CUtensorMap &tm_q,
+                                const CUtensorMap &tm_k, float *logits,
+                                int *status, int num_sms, cudaStream_t st) {
+  if (p.D <= kChunk)
+    return launch_kc<1>(p, tm_q, tm_k, logits, status, num_sms, st);
+  return launch_kc<2>(p, tm_q, tm_k, logits, status, num_sms, st);
+}
+
+}  // namespace dsa

@@ -1,0 +1,171 @@
+/*
+ * dsa_indexer.h -- C ABI of the GB300 (sm_103a) DSA lightning-indexer forward.
+ *
+ * The operation follows the DeepSeek-V4 SBHD indexer interface documented on
+ * the NeMo AutoModel page
+ * "nemo_automodel.components.models.deepseek_v4.kernels.tilelang_indexer":
+ *   - `V4IndexerFunction` / `v4_lighting_indexer(index_q, index_k, weights,
+ *     compress_ratio, topk, topk_indices=None)`: inputs in SBHD layout,
+ *     q [seqlen, batch, heads, dim] bf16, k [seqlen_kv, batch, dim] bf16,
+ *     weights [seqlen, batch, heads] fp32, `compress_ratio` ("4 for C4
+ *     layers"), `topk`, optional pre-computed `topk_indices [batch, seqlen,
+ *     topk] int32`; result `[batch, seqlen, topk] fp32` ("Returns").
+ *   - `pytorch_extract_topk_scores(logits, topk_indices, dim=-1)`: the
+ *     given-indices path gathers the scores at caller-supplied indices.
+ *   - "causal masking" (module summary).
+ * and the index conventions of the metrale.ai page "Module glm5next_dsa"
+ * ("-1 = invalid", section "Shape of the pipeline"; the whole index row is
+ * written, -1 first, section "Checkpoint and kernel facts"; kernels refuse
+ * shapes they cannot hold instead of dropping data, section "Constants").
+ *
+ * Score of query t against compressed key j (DSA lightning indexer):
+ *     I[t, j] = sum_h w[t, h] * ReLU( q[t, h, :] . k[j, :] )
+ * Key j is visible to a query at position t iff (j + 1) * compress_ratio - 1
+ * <= t (a key counts only when its whole compressed block is at or before
+ * t).  A prefill row s sits at position s; with `q_pos`, row s of sequence b
+ * sits at q_pos[b] + s.
+ *
+ * Memory: every pointer argument is DEVICE memory owned by the caller,
+ * dense and contiguous in the stated layout; q and k must be 16-byte
+ * aligned.  The library allocates no device memory: it works in the
+ * caller's workspace.  Every call is asynchronous on `cuda_stream` (a
+ * cudaStream_t; NULL = the legacy default stream): outputs are valid once
+ * that stream has synchronised.  Calls that share a workspace must be
+ * ordered on one stream.
+ *
+ * Errors: argument problems are returned synchronously, before anything is
+ * enqueued, and leave the outputs untouched.  Problems only the device can
+ * see (a given index outside [-1, S_kv), a bounded wait that expired) are
+ * recorded in the workspace's status word; read them with
+ * dsa_indexer_check().
+ */
+#ifndef DSA_INDEXER_H
+#define DSA_INDEXER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DSA_API __attribute__((visibility("default")))
+#else
+#define DSA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum dsa_status {
+    DSA_OK = 0,
+    DSA_ERR_INVALID_ARG = 1,    /* NULL pointer, size <= 0, misaligned q/k */
+    DSA_ERR_UNSUPPORTED = 2,    /* shape outside the compiled envelope, or
+                                   the current device is not sm_103 */
+    DSA_ERR_WORKSPACE = 3,      /* workspace NULL or smaller than required */
+    DSA_ERR_CUDA = 4,           /* a CUDA runtime call or launch failed */
+    DSA_ERR_DEVICE_TIMEOUT = 5, /* a bounded device-side wait expired */
+    DSA_ERR_INDEX_RANGE = 6     /* a given index was outside [-1, S_kv) */
+} dsa_status;
+
+/* Compiled envelope (shapes outside it return DSA_ERR_UNSUPPORTED):
+ *   H in {1, 2, 4, 8, 16, 32, 64, 128}; 8 <= D <= 128 with D % 8 == 0;
+ *   1 <= topk <= DSA_MAX_TOPK; B * S < 2^31; S_kv < 2^31; and the
+ *   per-row selection must fit in shared memory (S_kv * 4 + pow2(topk) * 8
+ *   bytes plus a few KB, checked against the device limit). */
+#define DSA_MAX_TOPK 8192
+#define DSA_MAX_D 128
+
+/*
+ * Bytes of device workspace dsa_indexer_fwd() needs for this shape
+ * (has_in_idx != 0 selects the given-indices path).  Returns 0 when the
+ * shape is invalid.  The workspace holds a 256-byte status header followed
+ * by the fp32 logits [B, S, S_kv] of the visible keys.
+ */
+DSA_API size_t dsa_indexer_workspace_size(int S, int B, int H, int D,
+                                          int S_kv, int compress_ratio,
+                                          int topk, int has_in_idx);
+
+/*
+ * The indexer forward (v4_lighting_indexer / V4IndexerFunction.forward).
+ *
+ *   q        [S, B, H, D] bf16          (index_q)
+ *   k        [S_kv, B, D] bf16          (index_k, already compressed)
+ *   w        [S, B, H] fp32             (weights)
+ *   q_pos    [B] int32 or NULL          (first query position per sequence)
+ *   in_idx   [B, S, topk] int32 or NULL (topk_indices)
+ *   out_idx  [B, S, topk] int32
+ *   out_scores [B, S, topk] fp32
+ *
+ * in_idx == NULL: per row, the min(topk, n_visible) visible keys with the
+ * largest score, sorted by descending score, equal scores by ascending key
+ * index; remaining slots hold -1 and -inf.
+ * in_idx != NULL: out_idx is a copy of in_idx; out_scores holds the score at
+ * each given index, or -inf where the index is -1, not visible, or outside
+ * [0, S_kv) (the latter also sets DSA_ERR_INDEX_RANGE in the status word).
+ *
+ * Returns DSA_OK once the work is enqueued, else the synchronous error.
+ */
+DSA_API int dsa_indexer_fwd(const void *q, const void *k, const float *w,
+                            int S, int B, int H, int D, int S_kv,
+                            int compress_ratio, int topk,
+                            const int32_t *q_pos, const int32_t *in_idx,
+                            int32_t *out_idx, float *out_scores,
+                            void *workspace, size_t workspace_bytes,
+                            void *cuda_stream);
+
+/*
+ * dsa_indexer_fwd() with stage timing: `stage_events` holds `n_events` (0..3)
+ * caller-created cudaEvent_t handles, recorded on `cuda_stream` before the
+ * scoring kernel (0), after it (1) and after the selection or gather kernel
+ * (2).  Events past n_events are not recorded.  Same work, outputs and
+ * errors as dsa_indexer_fwd() (plus DSA_ERR_INVALID_ARG for a NULL event).
+ */
+DSA_API int dsa_indexer_fwd_profiled(const void *q, const void *k,
+                                     const float *w, int S, int B, int H,
+                                     int D, int S_kv, int compress_ratio,
+                                     int topk, const int32_t *q_pos,
+                                     const int32_t *in_idx, int32_t *out_idx,
+                                     float *out_scores, void *workspace,
+                                     size_t workspace_bytes,
+                                     void *cuda_stream,
+                                     void *const *stage_events, int n_events);
+
+/*
+ * The scoring step alone: logits [B, S, S_kv] fp32 (`logits`, caller-owned
+ * device memory), I[t, j] at visible keys and -inf elsewhere -- the
+ * `logits` tensor that pytorch_extract_topk_scores() gathers from.
+ * `workspace` needs dsa_indexer_logits_workspace_size() bytes (the status
+ * header only).
+ */
+DSA_API size_t dsa_indexer_logits_workspace_size(void);
+DSA_API int dsa_indexer_logits(const void *q, const void *k, const float *w,
+                               int S, int B, int H, int D, int S_kv,
+                               int compress_ratio, const int32_t *q_pos,
+                               float *logits, void *workspace,
+                               size_t workspace_bytes, void *cuda_stream);
+
+/*
+ * Synchronises `cuda_stream`, then reads and clears the device status word
+ * of `workspace`.  Returns DSA_OK, DSA_ERR_INDEX_RANGE,
+ * DSA_ERR_DEVICE_TIMEOUT or DSA_ERR_CUDA (a sticky CUDA error).
+ */
+DSA_API int dsa_indexer_check(void *workspace, void *cuda_stream);
+
+/* Static description of a status code. */
+DSA_API const char *dsa_status_string(int status);
+
+/*
+ * Self-test of the device wait limit: launches one block that waits on a
+ * barrier nothing will complete, with a limit of `limit_us` microseconds
+ * (clamped to [1, 1000000]), and records DSA_ERR_DEVICE_TIMEOUT in the
+ * status word of `workspace` when the limit expires.  Used by the tests to
+ * show a hung wait ends with an error the host can read.
+ */
+DSA_API int dsa_selftest_wait_limit(int limit_us, void *workspace,
+                                    size_t workspace_bytes,
+                                    void *cuda_stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_INDEXER_H */
