@@ -1,0 +1,399 @@
+#!/usr/bin/env python3
+"""Benchmark of the DSA lightning-indexer forward on GB300.
+
+One step = the whole forward (scoring + top-k selection) over one batch of
+synthetic input of the V3.2-style prefill workload (B=1, S=4096, S_kv=4096,
+H=64, D=128, topk=2048, causal, ratio 1), inputs resident in HBM.  Metric:
+TFLOP/s over visible (query, key) pairs, 2*H*D FLOPs per pair, plus
+queries/s.  L2 is flushed (a 256 MiB write, outside the timed events)
+before every timed step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica of the same
+workload (the forward has no exchange step); the reported value is the sum
+of all ranks' work over the slowest rank's time.  `--impl reference` times
+the CPU oracle (plain C, fp64) on the host cores on a bounded row sample of
+the same workload; only rank 0 runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("indexer fwd TFLOP/s (visible pairs) + queries/s; "
+          "% of bf16 TC peak / HBM BW")
+WORKLOAD = "v32_prefill"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def visible_pairs(wl, q_pos=None) -> int:
+    """Sum over rows of the number of visible compressed keys."""
+    total = 0
+    for b in range(wl.B):
+        base = 0 if q_pos is None else int(q_pos[b])
+        for s in range(wl.S):
+            t = base + s
+            total += max(0, min(wl.S_kv, (t + 1) // wl.compress_ratio))
+    return total
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            return json.load(fh), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+                "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dsa_sparse_attention_fwd_gb300", "csrc")
+    for name in ("index_scores.cu", "ptx.cuh", "common.cuh"):
+        with open(os.path.join(csrc, name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def read_traffic():
+    """DRAM bytes per launch of the scoring kernel from the committed ncu
+    summary, only if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "index_scores_traffic.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    if d.get("source_sha") != kernel_source_sha():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}",
+                 f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "samples": 0, "note": "nvidia-smi unavailable"}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [v for v in (num(r[1]) for r in rows) if v is not None]
+        mx = [v for v in (num(r[2]) for r in rows) if v is not None]
+        pw = [v for v in (num(r[3]) for r in rows) if v is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def cpu_oracle_sample(wl, rows_every: int):
+    """Time the oracle on every `rows_every`-th row (from the last row down,
+    so the longest rows are in the sample)."""
+    import numpy as np
+
+    import oracle
+    from dsa_inputs import make_inputs
+    q, k, w, q_pos = make_inputs(wl)
+    rows = np.arange(wl.B * wl.S - 1, -1, -rows_every, dtype=np.int64)
+    oracle.build()
+    t0 = time.perf_counter()
+    out = oracle.indexer_fwd(q, k, w, wl.compress_ratio, wl.topk, q_pos=q_pos,
+                             rows=rows)
+    dt = time.perf_counter() - t0
+    pairs = int(np.asarray(out["nvis"], dtype=np.int64).sum())
+    flops = 2.0 * wl.H * wl.D * pairs
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s",
+            "cores": int(out["threads"]), "kind": "oracle",
+            "sample": f"{rows.size} of {wl.B * wl.S} rows (every "
+                      f"{rows_every}th from the last), {pairs} visible pairs, "
+                      f"{dt:.2f} s",
+            "queries_per_s": rows.size / dt}
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle, timed on the host cores."""
+    rank, _, _ = dist_env()
+    if rank != 0:
+        return 0
+    import numpy as np
+
+    import oracle
+    from dsa_inputs import WORKLOADS, make_inputs
+    wl = WORKLOADS[args.workload]
+    q, k, w, q_pos = make_inputs(wl)
+    oracle.build()
+    n = wl.B * wl.S
+    per_step = 16  # stride-spaced rows per step, rotating through the rows
+    stride = max(1, n // per_step)
+    times, pairs_total, threads = [], 0, 1
+    for i in range(args.warmup + args.steps):
+        off = (i * 7919) % stride
+        rows = np.arange(off, n, stride, dtype=np.int64)[:per_step]
+        t0 = time.perf_counter()
+        out = oracle.indexer_fwd(q, k, w, wl.compress_ratio, wl.topk,
+                                 q_pos=q_pos, rows=rows)
+        dt = time.perf_counter() - t0
+        threads = int(out["threads"])
+        if i >= args.warmup:
+            times.append(dt)
+            pairs_total += int(np.asarray(out["nvis"], np.int64).sum())
+    tot = sum(times)
+    value = 2.0 * wl.H * wl.D * pairs_total / tot / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value,
+        "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "S": wl.S,
+                   "S_kv": wl.S_kv, "H": wl.H, "D": wl.D,
+                   "compress_ratio": wl.compress_ratio, "topk": wl.topk,
+                   "step": f"{per_step} stride-spaced rows per step"},
+        "queries_per_s": per_step * len(times) / tot,
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": f"{per_step} rows per step x {len(times)} "
+                                   f"steps, {pairs_total} visible pairs"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import dsa_sparse_attention_fwd_gb300 as dsa
+    from dsa_inputs import WORKLOADS, describe, make_inputs
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dsa.build()
+    dsa.load_library()
+
+    wl = WORKLOADS[args.workload]
+    q, k, w, q_pos = make_inputs(wl)
+    pairs = visible_pairs(wl, None if q_pos is None else q_pos.tolist())
+    flops = 2.0 * wl.H * wl.D * pairs
+    qd, kd, wd = q.to(dev), k.to(dev), w.to(dev)
+    pd = q_pos.to(dev) if q_pos is not None else None
+    out_idx = torch.empty((wl.B, wl.S, wl.topk), dtype=torch.int32, device=dev)
+    out_sc = torch.empty((wl.B, wl.S, wl.topk), dtype=torch.float32,
+                         device=dev)
+    ws = torch.empty(dsa.dsa_indexer_workspace_size(
+        wl.S, wl.B, wl.H, wl.D, wl.S_kv, wl.compress_ratio, wl.topk),
+        dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(evs=None):
+        dsa.dsa_indexer_fwd(qd, kd, wd, wl.compress_ratio, wl.topk, q_pos=pd,
+                            out_idx=out_idx, out_scores=out_sc, workspace=ws,
+                            stream=stream, stage_events=evs)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    rc = dsa.dsa_indexer_check(ws)
+    if rc != 0:
+        raise RuntimeError(f"device status {dsa.STATUS.get(rc, rc)}")
+
+    K = args.steps
+    mk = lambda: torch.cuda.Event(enable_timing=True)
+    ev = [(mk(), mk(), mk(), mk()) for _ in range(K)]
+    sampler = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.2)
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.fill_(1.0)
+        e_start, e_s0, e_s1, e_end = ev[i]
+        e_start.record(stream)
+        step((e_s0, e_s1, e_end))
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    rc = dsa.dsa_indexer_check(ws)
+    if rc != 0:
+        raise RuntimeError(f"device status {dsa.STATUS.get(rc, rc)}")
+
+    step_ms = [a.elapsed_time(d) for a, _, _, d in ev]
+    score_ms = [b.elapsed_time(c) for _, b, c, _ in ev]
+    select_ms = [c.elapsed_time(d) for _, _, c, d in ev]
+    t_step = sum(step_ms) / K
+    if world > 1:
+        t = torch.tensor([t_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_step = float(t.item())
+
+    # ---- end to end through the public call, host buffers ----
+    qh, kh, wh = q.pin_memory(), k.pin_memory(), w.pin_memory()
+    ph = q_pos.pin_memory() if q_pos is not None else None
+    for _ in range(2):
+        dsa.v4_lighting_indexer(qh, kh, wh, wl.compress_ratio, wl.topk,
+                                q_pos=ph, check=False)
+    torch.cuda.synchronize()
+    Ke = max(3, min(K, 50))
+    e2e_ms = []
+    for _ in range(Ke):
+        a, b = mk(), mk()
+        a.record(stream)
+        sc_h, idx_h = dsa.v4_lighting_indexer(qh, kh, wh, wl.compress_ratio,
+                                              wl.topk, q_pos=ph, check=False)
+        b.record(stream)
+        b.synchronize()
+        e2e_ms.append(a.elapsed_time(b))
+    t_e2e = sum(e2e_ms) / Ke
+    if world > 1:
+        t = torch.tensor([t_e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_e2e = float(t.item())
+    h2d = q.numel() * 2 + k.numel() * 2 + w.numel() * 4 + (
+        q_pos.numel() * 4 if q_pos is not None else 0)
+    d2h = sc_h.numel() * 4 + idx_h.numel() * 4
+
+    if rank != 0:
+        dist.destroy_process_group()
+        return 0
+
+    peaks, peak_src = read_peaks()
+    t_score = statistics.mean(score_ms)
+    tc_peak = float(peaks["bf16_tflops"])
+    achieved = flops / (t_score * 1e-3) / 1e12
+    value = world * flops / (t_step * 1e-3) / 1e12
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": t_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "desc": describe(wl),
+                   "visible_pairs": pairs, "flops_per_step": flops,
+                   "l2": "flushed before each step (256 MiB write, outside "
+                         "the timed events)",
+                   "parallelism": f"replicas x{world}"},
+        "queries_per_s": world * wl.B * wl.S / (t_step * 1e-3),
+        "pct_of_bf16_peak": 100.0 * value / world / tc_peak,
+        "kernels_ms": {"index_scores": t_score,
+                       "topk_select": statistics.mean(select_ms),
+                       "step": t_step},
+        "roofline": {"kernel": "index_scores", "bound": "tensor",
+                     "achieved": achieved, "peak": tc_peak,
+                     "unit": "TFLOP/s", "frac": achieved / tc_peak,
+                     "peak_source": f"{peak_src} bf16 burst",
+                     "traffic": read_traffic()},
+        "e2e": {"value": world * flops / (t_e2e * 1e-3) / 1e12,
+                "unit": "TFLOP/s", "ms_per_step": t_e2e,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "api": "v4_lighting_indexer(host pinned tensors)"},
+        "gpu_launches": 2 * K,
+        "clocks": clocks,
+        "wall_s_timed_region": wall,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_sample(wl, 2)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

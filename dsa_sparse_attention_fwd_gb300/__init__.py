@@ -1,0 +1,247 @@
+"""GB300 (sm_103a) DSA lightning-indexer forward.
+
+A thin ctypes binding over the C ABI in `include/dsa_indexer.h`.  This module
+only marshals arguments: it allocates outputs and workspace with PyTorch,
+passes raw device pointers and the current CUDA stream, and raises on error
+codes.  Every step of the computation runs in the library's CUDA kernels; if
+the library is missing, every call raises instead of falling back.
+
+Interface after the DeepSeek-V4 SBHD indexer of NeMo AutoModel
+("tilelang_indexer" page: `v4_lighting_indexer(index_q, index_k, weights,
+compress_ratio, topk, topk_indices=None)`):
+    index_q  [S, B, H, D] bf16, index_k [S_kv, B, D] bf16,
+    weights  [S, B, H] fp32, topk_indices [B, S, topk] int32 (optional)
+returns (scores [B, S, topk] fp32, indices [B, S, topk] int32).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from ._build import LIB_PATH, build
+
+__all__ = [
+    "DsaError", "load_library", "build", "dsa_indexer_workspace_size",
+    "dsa_indexer_fwd", "dsa_indexer_logits", "dsa_indexer_check",
+    "dsa_status_string", "dsa_selftest_wait_limit", "v4_lighting_indexer",
+    "indexer_logits", "STATUS",
+]
+
+STATUS = {
+    0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED",
+    3: "DSA_ERR_WORKSPACE", 4: "DSA_ERR_CUDA", 5: "DSA_ERR_DEVICE_TIMEOUT",
+    6: "DSA_ERR_INDEX_RANGE",
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class DsaError(RuntimeError):
+    """A non-zero dsa_status from the library."""
+
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS.get(code, code)} "
+                         f"({dsa_status_string(code)})")
+
+
+def load_library(path: str | None = None):
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"CUDA library not built ({p}); run "
+                "dsa_sparse_attention_fwd_gb300.build() first")
+        lib = ctypes.CDLL(p)
+        P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        lib.dsa_indexer_workspace_size.restype = Z
+        lib.dsa_indexer_workspace_size.argtypes = [I] * 8
+        lib.dsa_indexer_fwd.restype = I
+        lib.dsa_indexer_fwd.argtypes = [P, P, P, I, I, I, I, I, I, I, P, P, P,
+                                        P, P, Z, P]
+        lib.dsa_indexer_fwd_profiled.restype = I
+        lib.dsa_indexer_fwd_profiled.argtypes = [P, P, P, I, I, I, I, I, I, I,
+                                                 P, P, P, P, P, Z, P, P, I]
+        lib.dsa_indexer_logits_workspace_size.restype = Z
+        lib.dsa_indexer_logits_workspace_size.argtypes = []
+        lib.dsa_indexer_logits.restype = I
+        lib.dsa_indexer_logits.argtypes = [P, P, P, I, I, I, I, I, I, P, P, P,
+                                           Z, P]
+        lib.dsa_indexer_check.restype = I
+        lib.dsa_indexer_check.argtypes = [P, P]
+        lib.dsa_status_string.restype = ctypes.c_char_p
+        lib.dsa_status_string.argtypes = [I]
+        lib.dsa_selftest_wait_limit.restype = I
+        lib.dsa_selftest_wait_limit.argtypes = [I, P, Z, P]
+        _lib = lib
+        return lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def dsa_status_string(code: int) -> str:
+    return load_library().dsa_status_string(int(code)).decode()
+
+
+def dsa_indexer_workspace_size(S, B, H, D, S_kv, compress_ratio, topk,
+                               has_in_idx=False) -> int:
+    return int(load_library().dsa_indexer_workspace_size(
+        S, B, H, D, S_kv, compress_ratio, topk, int(bool(has_in_idx))))
+
+
+def _check_inputs(q, k, w, q_pos, in_idx):
+    for name, t, dt in (("index_q", q, torch.bfloat16),
+                        ("index_k", k, torch.bfloat16),
+                        ("weights", w, torch.float32)):
+        if t.dtype != dt:
+            raise TypeError(f"{name} must be {dt}, got {t.dtype}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    S, B, H, D = q.shape
+    S_kv = k.shape[0]
+    if tuple(k.shape) != (S_kv, B, D):
+        raise ValueError(f"index_k shape {tuple(k.shape)} != "
+                         f"({S_kv}, {B}, {D})")
+    if tuple(w.shape) != (S, B, H):
+        raise ValueError(f"weights shape {tuple(w.shape)} != ({S}, {B}, {H})")
+    if q_pos is not None and (q_pos.dtype != torch.int32
+                              or q_pos.numel() != B):
+        raise ValueError("q_pos must be int32 [B]")
+    if in_idx is not None and (in_idx.dtype != torch.int32
+                               or not in_idx.is_contiguous()):
+        raise ValueError("topk_indices must be contiguous int32")
+    return S, B, H, D, S_kv
+
+
+def dsa_indexer_fwd(q, k, w, compress_ratio, topk, q_pos=None, in_idx=None,
+                    out_idx=None, out_scores=None, workspace=None,
+                    stream=None, stage_events=None):
+    """Enqueue the forward on device tensors; returns (out_scores, out_idx,
+    workspace).  Raises DsaError on a synchronous error.  `stage_events`
+    (up to 3 torch.cuda.Event, created with enable_timing) are recorded
+    before the scoring kernel, after it, and after the selection kernel."""
+    lib = load_library()
+    S, B, H, D, S_kv = _check_inputs(q, k, w, q_pos, in_idx)
+    dev = q.device
+    if in_idx is not None and tuple(in_idx.shape) != (B, S, topk):
+        raise ValueError("topk_indices must be [B, S, topk]")
+    if out_idx is None:
+        out_idx = torch.empty((B, S, topk), dtype=torch.int32, device=dev)
+    if out_scores is None:
+        out_scores = torch.empty((B, S, topk), dtype=torch.float32,
+                                 device=dev)
+    ws = dsa_indexer_workspace_size(S, B, H, D, S_kv, compress_ratio, topk,
+                                    in_idx is not None)
+    if workspace is None:
+        workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev)
+    if stage_events:
+        evs = (ctypes.c_void_p * len(stage_events))(
+            *[ctypes.c_void_p(e.cuda_event) for e in stage_events])
+        rc = lib.dsa_indexer_fwd_profiled(
+            _ptr(q), _ptr(k), _ptr(w), S, B, H, D, S_kv, int(compress_ratio),
+            int(topk), _ptr(q_pos), _ptr(in_idx), _ptr(out_idx),
+            _ptr(out_scores), _ptr(workspace), workspace.numel(),
+            _stream(stream), evs, len(stage_events))
+    else:
+        rc = lib.dsa_indexer_fwd(
+            _ptr(q), _ptr(k), _ptr(w), S, B, H, D, S_kv, int(compress_ratio),
+            int(topk), _ptr(q_pos), _ptr(in_idx), _ptr(out_idx),
+            _ptr(out_scores), _ptr(workspace), workspace.numel(),
+            _stream(stream))
+    if rc != 0:
+        raise DsaError(rc, "dsa_indexer_fwd")
+    return out_scores, out_idx, workspace
+
+
+def dsa_indexer_logits(q, k, w, compress_ratio, q_pos=None, logits=None,
+                       workspace=None, stream=None):
+    """Enqueue the scoring step alone: logits [B, S, S_kv] fp32 (-inf where
+    a key is not visible).  Returns (logits, workspace)."""
+    lib = load_library()
+    S, B, H, D, S_kv = _check_inputs(q, k, w, q_pos, None)
+    dev = q.device
+    if logits is None:
+        logits = torch.empty((B, S, S_kv), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(int(lib.dsa_indexer_logits_workspace_size()),
+                                dtype=torch.uint8, device=dev)
+    rc = lib.dsa_indexer_logits(
+        _ptr(q), _ptr(k), _ptr(w), S, B, H, D, S_kv, int(compress_ratio),
+        _ptr(q_pos), _ptr(logits), _ptr(workspace), workspace.numel(),
+        _stream(stream))
+    if rc != 0:
+        raise DsaError(rc, "dsa_indexer_logits")
+    return logits, workspace
+
+
+def dsa_indexer_check(workspace, stream=None) -> int:
+    """Synchronise the stream and return the device status code (0 = ok)."""
+    return int(load_library().dsa_indexer_check(_ptr(workspace),
+                                                 _stream(stream)))
+
+
+def dsa_selftest_wait_limit(limit_us: int, workspace, stream=None) -> int:
+    return int(load_library().dsa_selftest_wait_limit(
+        int(limit_us), _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def v4_lighting_indexer(index_q, index_k, weights, compress_ratio, topk,
+                        topk_indices=None, q_pos=None, check=True):
+    """The indexer forward with the V4 argument order.
+
+    Device tensors run on the current stream.  Host (CPU) tensors are copied
+    to the current CUDA device, run there, and the results copied back into
+    host tensors (pinned when the inputs are pinned); the whole host round
+    trip happens inside this call.  Returns (scores [B,S,topk] fp32,
+    indices [B,S,topk] int32).  With check=True the call synchronises and
+    raises on a device-side status (bad given index, expired wait).
+    """
+    host = index_q.device.type == "cpu"
+    pinned = host and index_q.is_pinned()
+    if host:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        index_q = index_q.to(dev, non_blocking=pinned)
+        index_k = index_k.to(dev, non_blocking=pinned)
+        weights = weights.to(dev, non_blocking=pinned)
+        if topk_indices is not None:
+            topk_indices = topk_indices.to(dev, non_blocking=pinned)
+        if q_pos is not None:
+            q_pos = q_pos.to(dev, non_blocking=pinned)
+    scores, idx, ws = dsa_indexer_fwd(index_q, index_k, weights,
+                                      compress_ratio, topk, q_pos=q_pos,
+                                      in_idx=topk_indices)
+    if check:
+        rc = dsa_indexer_check(ws)
+        if rc != 0:
+            raise DsaError(rc, "device status")
+    if host:
+        sc_h = torch.empty(scores.shape, dtype=scores.dtype, pin_memory=pinned)
+        idx_h = torch.empty(idx.shape, dtype=idx.dtype, pin_memory=pinned)
+        sc_h.copy_(scores, non_blocking=pinned)
+        idx_h.copy_(idx, non_blocking=pinned)
+        torch.cuda.current_stream().synchronize()
+        scores, idx = sc_h, idx_h
+    return scores, idx
+
+
+def indexer_logits(index_q, index_k, weights, compress_ratio, q_pos=None):
+    """Logits [B, S, S_kv] fp32 on the device (-inf where masked)."""
+    logits, _ = dsa_indexer_logits(index_q, index_k, weights, compress_ratio,
+                                   q_pos=q_pos)
+    return logits

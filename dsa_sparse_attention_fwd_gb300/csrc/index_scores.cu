@@ -39,7 +39,10 @@ struct ScoreSmem {
   static constexpr int kNumBars = 2 * kStages + 2 + 4;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16;
-  static constexpr int kAlloc = kBytes + 1024;  // room to align the base
+  // room to align the base; at least 120 KB so that only one CTA fits on
+  // an SM (each CTA allocates all 512 TMEM columns)
+  static constexpr int kAlloc =
+      kBytes + 1024 > 120 * 1024 ? kBytes + 1024 : 120 * 1024;
 };
 
 struct ItemInfo {

@@ -1,0 +1,155 @@
+"""The C ABI library: it builds, loads, exports every declared entry point
+and rejects bad arguments synchronously (no GPU needed: every case here
+returns before the library touches a device)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from dsa_sparse_attention_fwd_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+INCLUDE = os.path.join(ROOT, "include")
+
+OK, INVALID, UNSUPPORTED, WORKSPACE, CUDA, TIMEOUT, RANGE = range(7)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = _build.build()
+    L = ctypes.CDLL(path)
+    P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    L.dsa_indexer_fwd.restype = I
+    L.dsa_indexer_fwd.argtypes = [P, P, P, I, I, I, I, I, I, I, P, P, P, P,
+                                  P, Z, P]
+    L.dsa_indexer_fwd_profiled.restype = I
+    L.dsa_indexer_fwd_profiled.argtypes = [P, P, P, I, I, I, I, I, I, I, P, P,
+                                           P, P, P, Z, P, P, I]
+    L.dsa_indexer_logits.restype = I
+    L.dsa_indexer_logits.argtypes = [P, P, P, I, I, I, I, I, I, P, P, P, Z, P]
+    L.dsa_indexer_workspace_size.restype = Z
+    L.dsa_indexer_workspace_size.argtypes = [I] * 8
+    L.dsa_indexer_logits_workspace_size.restype = Z
+    L.dsa_status_string.restype = ctypes.c_char_p
+    L.dsa_status_string.argtypes = [I]
+    L.dsa_indexer_check.restype = I
+    L.dsa_indexer_check.argtypes = [P, P]
+    L.dsa_selftest_wait_limit.restype = I
+    L.dsa_selftest_wait_limit.argtypes = [I, P, Z, P]
+    return L
+
+
+def declared_functions():
+    names = set()
+    for h in os.listdir(INCLUDE):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(INCLUDE, h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"\b(dsa_[a-z_0-9]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for n in ("dsa_indexer_fwd", "dsa_indexer_workspace_size",
+              "dsa_status_string", "dsa_indexer_check", "dsa_indexer_logits",
+              "dsa_indexer_fwd_profiled"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_library_exports_nothing_else(lib):
+    """Only the declared C entry points are visible (hidden visibility)."""
+    out = subprocess.run(["nm", "-D", "--defined-only", _build.LIB_PATH],
+                         capture_output=True, text=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines()
+                if " T " in l and l.split()[-1].startswith("dsa_")}
+    assert exported == set(declared_functions())
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        s = lib.dsa_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert lib.dsa_status_string(99).decode() == "unknown status"
+
+
+def test_workspace_size(lib):
+    ws = lib.dsa_indexer_workspace_size
+    assert ws(4096, 1, 64, 128, 4096, 1, 2048, 0) == 256 + 4096 * 4096 * 4
+    assert ws(16384, 2, 64, 128, 4096, 4, 512, 0) == 256 + 2 * 16384 * 4096 * 4
+    assert ws(0, 1, 64, 128, 4096, 1, 2048, 0) == 0
+    assert ws(16, 1, 3, 128, 16, 1, 4, 0) == 0
+    assert ws(16, 1, 4, 128, 16, 1, 0, 0) == 0
+    assert lib.dsa_indexer_logits_workspace_size() == 256
+
+
+FAKE = 1 << 20  # aligned, never dereferenced: every case fails before use
+
+
+def _fwd(lib, q=FAKE, k=FAKE, w=FAKE, S=16, B=1, H=4, D=32, S_kv=16, r=1,
+         topk=4, q_pos=None, in_idx=None, oi=FAKE, os_=FAKE, ws=FAKE,
+         wsb=1 << 30):
+    return lib.dsa_indexer_fwd(q, k, w, S, B, H, D, S_kv, r, topk, q_pos,
+                               in_idx, oi, os_, ws, wsb, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), INVALID), (dict(k=None), INVALID), (dict(w=None), INVALID),
+    (dict(oi=None), INVALID), (dict(os_=None), INVALID),
+    (dict(S=0), INVALID), (dict(B=-1), INVALID), (dict(S_kv=0), INVALID),
+    (dict(r=0), INVALID), (dict(topk=0), INVALID), (dict(D=0), INVALID),
+    (dict(H=3), UNSUPPORTED), (dict(H=256), UNSUPPORTED),
+    (dict(D=12), UNSUPPORTED), (dict(D=136), UNSUPPORTED),
+    (dict(topk=8193), UNSUPPORTED),
+    (dict(q=FAKE + 8), INVALID), (dict(k=FAKE + 2), INVALID),
+    (dict(ws=None), WORKSPACE), (dict(wsb=100), WORKSPACE),
+    (dict(ws=FAKE + 4), INVALID),
+])
+def test_fwd_rejects_bad_arguments(lib, kw, code):
+    assert _fwd(lib, **kw) == code
+
+
+def test_profiled_rejects_bad_events(lib):
+    f = lib.dsa_indexer_fwd_profiled
+    args = [FAKE, FAKE, FAKE, 16, 1, 4, 32, 16, 1, 4, None, None, FAKE, FAKE,
+            FAKE, 1 << 30, None]
+    assert f(*args, None, 2) == INVALID
+    assert f(*args, None, -1) == INVALID
+    evs = (ctypes.c_void_p * 2)(None, None)
+    assert f(*args, evs, 2) == INVALID
+
+
+def test_logits_rejects_bad_arguments(lib):
+    f = lib.dsa_indexer_logits
+    assert f(None, FAKE, FAKE, 8, 1, 4, 32, 8, 1, None, FAKE, FAKE, 256,
+             None) == INVALID
+    assert f(FAKE, FAKE, FAKE, 8, 1, 5, 32, 8, 1, None, FAKE, FAKE, 256,
+             None) == UNSUPPORTED
+    assert f(FAKE, FAKE, FAKE, 8, 1, 4, 32, 8, 1, None, FAKE, FAKE, 16,
+             None) == WORKSPACE
+
+
+def test_check_rejects_null_workspace(lib):
+    assert lib.dsa_indexer_check(None, None) == INVALID
+    assert lib.dsa_selftest_wait_limit(10, None, 0, None) == WORKSPACE
+
+
+def test_python_binding_fails_loudly_without_library(tmp_path):
+    import dsa_sparse_attention_fwd_gb300 as m
+    saved = m._lib
+    try:
+        m._lib = None
+        with pytest.raises(RuntimeError, match="not built"):
+            m.load_library(str(tmp_path / "missing.so"))
+    finally:
+        m._lib = saved
