@@ -272,6 +272,9 @@ def run_ours(args):
     K = args.steps
     mk = lambda: torch.cuda.Event(enable_timing=True)
     ev = [(mk(), mk(), mk(), mk()) for _ in range(K)]
+    for quad in ev:  # torch creates the CUDA event at its first record
+        for e in quad:
+            e.record(stream)
     sampler = ClockSampler(local)
     if world > 1:
         dist.barrier()

@@ -59,7 +59,8 @@ def check_invariants(sc, idx, nvis, topk):
                                                idx.shape)[valid]), "visible"
     assert np.all(np.isneginf(sc[~valid])), "padding scores"
     assert np.all(np.isfinite(sc[valid])), "finite scores"
-    d = np.diff(np.where(valid, sc, -np.inf), axis=-1)
+    with np.errstate(invalid="ignore"):
+        d = np.diff(np.where(valid, sc, -np.inf), axis=-1)
     vv = valid[..., 1:]
     assert np.all(d[vv] <= 0), "non-increasing"
     srt = np.sort(np.where(valid, idx, -1 - np.arange(topk)), axis=-1)
