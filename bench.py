@@ -377,7 +377,7 @@ def run_ours(args):
         "wall_s_timed_region": wall,
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_oracle_sample(wl, 2)
+        line["cpu_baseline"] = cpu_oracle_sample(wl, 1)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
