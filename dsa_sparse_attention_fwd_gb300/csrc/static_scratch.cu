@@ -1,0 +1,74 @@
+// An indexer forward for callers that cannot allocate device memory.
+//
+// Some callers cannot call cudaMalloc: code that runs while a caching
+// allocator owns all free memory, plugin hosts that hand out only the
+// tensors they manage, and hot paths where an allocation would synchronise
+// the device.  For them this entry point runs the same forward as
+// dsa_indexer_fwd() with its scratch (the status header and the fp32 logits)
+// taken from a fixed array in this file instead of a caller workspace.
+//
+// The array is a file-scope __device__ variable: each GPU on which this
+// library's module is loaded holds its own copy until the process exits.
+// Host code cannot use the array's name as a device address (on the host
+// the name is only a stand-in), so the device address is looked up once per
+// device with cudaGetSymbolAddress while that device is current.
+#include <mutex>
+
+#include "dsa_indexer.h"
+
+namespace {
+
+static __device__ __align__(256) unsigned char
+    g_static_scratch[DSA_STATIC_SCRATCH_BYTES];
+
+std::mutex g_scratch_mu;
+void *g_scratch_ptr[64] = {};
+
+// Device address of this device's copy of the scratch array (looked up on
+// the first call per device, with that device current).
+int static_scratch_address(void **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DSA_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return DSA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p)
+      return DSA_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return DSA_OK;
+}
+
+}  // namespace
+
+extern "C" int dsa_indexer_fwd_static_scratch(
+    const void *q, const void *k, const float *w, int S, int B, int H, int D,
+    int S_kv, int compress_ratio, int topk, const int32_t *q_pos,
+    const int32_t *in_idx, int32_t *out_idx, float *out_scores,
+    int32_t *out_status, void *cuda_stream) {
+  const size_t need = dsa_indexer_workspace_size(
+      S, B, H, D, S_kv, compress_ratio, topk, in_idx != nullptr);
+  if (need == 0)  // invalid shape: report the forward's own argument error
+    return dsa_indexer_fwd(q, k, w, S, B, H, D, S_kv, compress_ratio, topk,
+                           q_pos, in_idx, out_idx, out_scores, nullptr, 0,
+                           cuda_stream);
+  if (need > (size_t)DSA_STATIC_SCRATCH_BYTES) return DSA_ERR_UNSUPPORTED;
+  void *scratch = nullptr;
+  int rc = static_scratch_address(&scratch);
+  if (rc != DSA_OK) return rc;
+  // The forward clears the status header itself before its kernels run;
+  // the logits region needs no clearing (every entry that is read was
+  // written earlier in the same call).
+  rc = dsa_indexer_fwd(q, k, w, S, B, H, D, S_kv, compress_ratio, topk, q_pos,
+                       in_idx, out_idx, out_scores, scratch,
+                       (size_t)DSA_STATIC_SCRATCH_BYTES, cuda_stream);
+  if (rc != DSA_OK) return rc;
+  if (out_status &&
+      cudaMemcpyAsync(out_status, scratch, sizeof(int32_t),
+                      cudaMemcpyDeviceToDevice,
+                      static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  return DSA_OK;
+}

@@ -28,7 +28,8 @@
  * Memory: every pointer argument is DEVICE memory owned by the caller,
  * dense and contiguous in the stated layout; q and k must be 16-byte
  * aligned.  The library allocates no device memory: it works in the
- * caller's workspace.  Every call is asynchronous on `cuda_stream` (a
+ * caller's workspace (dsa_indexer_fwd_static_scratch() instead uses a fixed
+ * array inside the library).  Every call is asynchronous on `cuda_stream` (a
  * cudaStream_t; NULL = the legacy default stream): outputs are valid once
  * that stream has synchronised.  Calls that share a workspace must be
  * ordered on one stream.
@@ -163,6 +164,44 @@ DSA_API const char *dsa_status_string(int status);
 DSA_API int dsa_selftest_wait_limit(int limit_us, void *workspace,
                                     size_t workspace_bytes,
                                     void *cuda_stream);
+
+/*
+ * Allocation-free variant of dsa_indexer_fwd() (the pages have no
+ * counterpart; this is a library convenience).
+ *
+ * For callers that cannot call cudaMalloc -- code running while a caching
+ * allocator holds all free device memory, plugin hosts that only hand out
+ * the tensors they own, or paths where an allocation would synchronise the
+ * device.  The forward's scratch (status header + fp32 logits) comes from a
+ * fixed array of DSA_STATIC_SCRATCH_BYTES inside the library instead of a
+ * caller workspace; the caller still passes every input and output.
+ *
+ *   - Limit: problems whose dsa_indexer_workspace_size() exceeds
+ *     DSA_STATIC_SCRATCH_BYTES (64 MiB of logits, B*S*S_kv <= 16,777,216,
+ *     plus a 256-byte header) are refused with DSA_ERR_UNSUPPORTED before
+ *     any device work.  Other argument errors are those of dsa_indexer_fwd().
+ *   - Memory: every GPU that loads this part of the library holds one copy
+ *     of the array until the process exits.  No call allocates or frees
+ *     device memory.
+ *   - Set-up: the first call on each device looks up that device's copy of
+ *     the array (cudaGetSymbolAddress, with the device current); make that
+ *     first call before any stream capture.
+ *   - Sharing: all calls on a device share the one array, which keeps the
+ *     last call's contents.  Calls that overlap on the GPU (different
+ *     streams, or threads without ordering) race on it; order them on one
+ *     stream.  Each call clears the status word it uses; the logits need no
+ *     clearing.
+ *   - out_status: NULL, or one device int32 that receives this call's device
+ *     status bits (0 = ok; bit 0 = a given index outside [-1, S_kv); bit 1 =
+ *     a bounded wait expired), written asynchronously on `cuda_stream`.
+ * Asynchronous on `cuda_stream` like dsa_indexer_fwd().
+ */
+#define DSA_STATIC_SCRATCH_BYTES ((size_t)64 * 1024 * 1024 + 256)
+DSA_API int dsa_indexer_fwd_static_scratch(
+    const void *q, const void *k, const float *w, int S, int B, int H, int D,
+    int S_kv, int compress_ratio, int topk, const int32_t *q_pos,
+    const int32_t *in_idx, int32_t *out_idx, float *out_scores,
+    int32_t *out_status, void *cuda_stream);
 
 #ifdef __cplusplus
 }
