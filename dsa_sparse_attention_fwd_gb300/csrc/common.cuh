@@ -45,6 +45,10 @@ constexpr int kChunk = 64;          // bf16 per 128-byte swizzled row
 constexpr int kStages = 4;          // K-tile pipeline depth
 constexpr int kScoreThreads = 320;  // TMA warp, MMA warp, 8 epilogue warps
 
+// Top-k selection: a sort pass handles up to 256 threads x this many
+// elements, so topk <= 256 * DSA_SEL_MAX_EPT (= DSA_MAX_TOPK).
+#define DSA_SEL_MAX_EPT 32
+
 // Launchers (return cudaSuccess or the launch error).  `logits` is
 // [B, S, S_kv] fp32; only visible entries are written.
 cudaError_t launch_index_scores(const Problem &p, const CUtensorMap &tm_q,

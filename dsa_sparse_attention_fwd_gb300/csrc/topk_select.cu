@@ -2,22 +2,26 @@
 // sorted by descending score with equal scores ordered by ascending key
 // index; the rest of the row is -1 / -inf.
 //
-// One CTA per row.  The row's n visible fp32 scores are staged in shared
-// memory as order-preserving unsigned keys (larger float <-> larger key;
-// -0.0 folded onto +0.0 so the index tie-break decides between them).  A
-// most-significant-digit-first radix select (four 8-bit digits, block
-// histograms in shared memory) finds T, the k-th largest key.  One ordered
-// pass then keeps every key > T and the lowest-index keys == T, and a
-// bitonic sort over 64-bit (key << 32 | ~j) composites orders the survivors;
-// the composite makes every key distinct, so the sort realises the
-// "lower index first" tie rule exactly.
+// One CTA (8 warps) per row.  The row's n visible fp32 scores are staged in
+// shared memory as order-preserving unsigned keys (larger float <-> larger
+// key; -0.0 folded onto +0.0 so the index tie-break decides between them).
+//   1. When n > topk, a most-significant-digit-first radix select (four 8-bit
+//      digits; histogram updates aggregated per warp with match_any) finds T,
+//      the topk-th largest key, and an ordered two-walk compaction keeps every
+//      key > T and the lowest-index keys == T, in index order.
+//   2. A stable least-significant-digit radix sort (four 8-bit digits,
+//      descending) orders the m = min(n, topk) survivors, packed as
+//      (key << 32 | j).  Stability keeps equal keys in index order, which is
+//      exactly the "lower index first" tie rule.  A pass whose digit is the
+//      same for every element is skipped.
 #include "common.cuh"
 
 namespace dsa {
 namespace {
 
-constexpr int kSelThreads = 512;
+constexpr int kSelThreads = 256;
 constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kMaxEpt = DSA_SEL_MAX_EPT;  // elements per lane per sort pass
 
 __device__ __forceinline__ uint32_t ordered_key(float f) {
   uint32_t u = __float_as_uint(f);
@@ -29,24 +33,116 @@ __device__ __forceinline__ float key_to_float(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-__host__ __device__ inline int pow2_at_least(int x) {
-  int p = 1;
-  while (p < x) p <<= 1;
-  return p;
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+struct SelShared {
+  uint32_t whist[kSelWarps][256];  // per-warp digit counts / offsets
+  uint32_t hist[256];              // block histogram / digit bases
+  uint32_t wsum[kSelWarps];
+  uint32_t wgt[kSelWarps], weq[kSelWarps];
+  uint32_t sel_digit, sel_above;
+  int skip;
+};
+
+// Exclusive prefix sum of one value per thread over the 256-thread block.
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, SelShared &sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += t;
+  }
+  if (lane == 31) sh.wsum[warp] = incl;
+  __syncthreads();
+  uint32_t pre = 0;
+#pragma unroll
+  for (int w = 0; w < kSelWarps; ++w)
+    if (w < warp) pre += sh.wsum[w];
+  return pre + incl - v;
+}
+
+// One stable counting-sort pass on digit (key >> shift) & 255, descending.
+// Returns true when the pass moved data into dst, false when every element
+// has the same digit (then src already holds the pass's result).
+__device__ __forceinline__ bool lsd_pass(const uint64_t *src, uint64_t *dst,
+                                         int m, int shift, SelShared &sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int tid = threadIdx.x;
+  const int per_warp = ((m + kSelThreads - 1) / kSelThreads) * 32;
+  const int ept = per_warp / 32;
+  const int seg = warp * per_warp;
+  uint32_t *wh = sh.whist[warp];
+  const uint32_t lt = lanemask_lt();
+  for (int i = lane; i < 256; i += 32) wh[i] = 0;
+  __syncwarp();
+  uint32_t off[kMaxEpt];
+#pragma unroll
+  for (int it = 0; it < kMaxEpt; ++it) {
+    if (it < ept) {
+      const int e = seg + it * 32 + lane;
+      const bool valid = e < m;
+      const uint64_t v = valid ? src[e] : 0ull;
+      const uint32_t d =
+          valid ? 255u - (uint32_t)((v >> (32 + shift)) & 255u) : 256u;
+      const uint32_t peers = __match_any_sync(0xffffffffu, d);
+      const uint32_t rank = __popc(peers & lt);
+      const uint32_t base = valid ? wh[d] : 0u;
+      __syncwarp();
+      if (valid && rank == 0) wh[d] = base + __popc(peers);
+      __syncwarp();
+      off[it] = base + rank;
+    }
+  }
+  if (tid == 0) sh.skip = 0;
+  __syncthreads();
+  {
+    const int d = tid;  // 256 threads, one digit each
+    uint32_t run = 0;
+#pragma unroll
+    for (int w = 0; w < kSelWarps; ++w) {
+      const uint32_t c = sh.whist[w][d];
+      sh.whist[w][d] = run;
+      run += c;
+    }
+    if (run == (uint32_t)m) sh.skip = 1;
+    const uint32_t b = block_excl_scan(run, sh);
+    sh.hist[d] = b;
+  }
+  __syncthreads();
+  const bool skip = sh.skip != 0;
+  __syncthreads();  // everyone has read the flag before it is reset
+  if (skip) return false;  // block-uniform
+#pragma unroll
+  for (int it = 0; it < kMaxEpt; ++it) {
+    if (it < ept) {
+      const int e = seg + it * 32 + lane;
+      if (e < m) {
+        const uint64_t v = src[e];
+        const uint32_t d = 255u - (uint32_t)((v >> (32 + shift)) & 255u);
+        dst[sh.hist[d] + wh[d] + off[it]] = v;
+      }
+    }
+  }
+  __syncthreads();
+  return true;
 }
 
 __global__ void __launch_bounds__(kSelThreads)
     topk_select_kernel(const float *__restrict__ logits,
                        const int32_t *__restrict__ q_pos, int S, int S_kv,
-                       int ratio, int topk, int kpad,
+                       int ratio, int topk, int mcap,
                        int32_t *__restrict__ out_idx,
                        float *__restrict__ out_scores) {
   extern __shared__ __align__(16) uint8_t smem[];
-  uint64_t *cand = reinterpret_cast<uint64_t *>(smem);         // [kpad]
-  uint32_t *keys = reinterpret_cast<uint32_t *>(cand + kpad);  // [S_kv]
-  __shared__ uint32_t hist[256];
-  __shared__ uint32_t warp_gt[kSelWarps], warp_eq[kSelWarps];
-  __shared__ uint32_t sel_digit, sel_above;
+  uint64_t *bufA = reinterpret_cast<uint64_t *>(smem);      // [mcap]
+  uint64_t *bufB = bufA + mcap;                              // [mcap]
+  uint32_t *keys = reinterpret_cast<uint32_t *>(bufB + mcap);  // [S_kv]
+  __shared__ SelShared sh;
 
   const int row = blockIdx.x;  // row id = b * S + s, the output order
   const int b = row / S, s = row % S;
@@ -54,23 +150,29 @@ __global__ void __launch_bounds__(kSelThreads)
   const int nv = n_visible(row_pos(q_pos, b, s), ratio, S_kv);
   const float *L = logits + (size_t)row * S_kv;
   const int m = nv < topk ? nv : topk;
-
-  for (int j = tid; j < nv; j += kSelThreads) keys[j] = ordered_key(L[j]);
-  __syncthreads();
+  const uint32_t lt = lanemask_lt();
 
   if (nv <= topk) {
     for (int j = tid; j < nv; j += kSelThreads)
-      cand[j] = ((uint64_t)keys[j] << 32) | (uint32_t)(~(uint32_t)j);
+      bufA[j] = ((uint64_t)ordered_key(__ldg(L + j)) << 32) | (uint32_t)j;
+    __syncthreads();
   } else {
+    for (int j = tid; j < nv; j += kSelThreads)
+      keys[j] = ordered_key(__ldg(L + j));
+    __syncthreads();
     // ---- radix select of T, the topk-th largest key ----
     uint32_t prefix = 0, pmask = 0;
-    int need = topk;  // how many still to take among keys matching prefix
+    int need = topk;  // still to take among keys matching prefix
     for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int i = tid; i < 256; i += kSelThreads) hist[i] = 0;
+      sh.hist[tid] = 0;
       __syncthreads();
-      for (int j = tid; j < nv; j += kSelThreads) {
-        const uint32_t u = keys[j];
-        if ((u & pmask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
+      for (int c0 = 0; c0 < nv; c0 += kSelThreads) {
+        const int j = c0 + tid;
+        const uint32_t u = j < nv ? keys[j] : 0u;
+        const bool ok = j < nv && (u & pmask) == prefix;
+        const uint32_t d = ok ? (u >> shift) & 255u : 256u;
+        const uint32_t peers = __match_any_sync(0xffffffffu, d);
+        if (ok && (peers & lt) == 0) atomicAdd(&sh.hist[d], __popc(peers));
       }
       __syncthreads();
       if (warp == 0) {
@@ -80,24 +182,22 @@ __global__ void __launch_bounds__(kSelThreads)
         uint32_t lsum = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          c[i] = hist[lane * 8 + i];
+          c[i] = sh.hist[lane * 8 + i];
           lsum += c[i];
         }
-        // inclusive suffix sum over lanes
-        uint32_t incl = lsum;
+        uint32_t incl = lsum;  // inclusive suffix sum over lanes
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
           const uint32_t o = __shfl_down_sync(0xffffffffu, incl, off);
           if (lane + off < 32) incl += o;
         }
-        const uint32_t above = incl - lsum;  // digits owned by higher lanes
-        // the owning lane: above < need <= incl
+        const uint32_t above = incl - lsum;
         if (above < (uint32_t)need && (uint32_t)need <= incl) {
           uint32_t run = above;
           for (int i = 7; i >= 0; --i) {
             if (run + c[i] >= (uint32_t)need) {
-              sel_digit = (uint32_t)(lane * 8 + i);
-              sel_above = run;
+              sh.sel_digit = (uint32_t)(lane * 8 + i);
+              sh.sel_above = run;
               break;
             }
             run += c[i];
@@ -105,70 +205,59 @@ __global__ void __launch_bounds__(kSelThreads)
         }
       }
       __syncthreads();
-      need -= (int)sel_above;
-      prefix |= sel_digit << shift;
+      need -= (int)sh.sel_above;
+      prefix |= sh.sel_digit << shift;
       pmask |= 255u << shift;
       __syncthreads();
     }
     const uint32_t T = prefix;
     const int n_gt = topk - need;  // keys strictly above T, all kept
 
-    // ---- ordered compaction: keys > T, then the `need` lowest-j ties ----
-    uint32_t gt_base = 0, eq_base = 0;
-    for (int c0 = 0; c0 < nv; c0 += kSelThreads) {
-      const int j = c0 + tid;
-      const uint32_t u = j < nv ? keys[j] : 0u;
-      const bool is_gt = j < nv && u > T;
-      const bool is_eq = j < nv && u == T;
+    // ---- ordered compaction, two walks over contiguous warp segments ----
+    const int seg = ((nv + kSelThreads - 1) / kSelThreads) * 32;
+    const int lo = warp * seg, hi = min(nv, lo + seg);
+    uint32_t cgt = 0, ceq = 0;
+    for (int c = lo; c < lo + seg; c += 32) {
+      const int j = c + lane;
+      const uint32_t u = j < hi ? keys[j] : 0u;
+      cgt += __popc(__ballot_sync(0xffffffffu, j < hi && u > T));
+      ceq += __popc(__ballot_sync(0xffffffffu, j < hi && u == T));
+    }
+    if (lane == 0) {
+      sh.wgt[warp] = cgt;
+      sh.weq[warp] = ceq;
+    }
+    __syncthreads();
+    uint32_t gpos = 0, epos = 0;
+    for (int w = 0; w < warp; ++w) {
+      gpos += sh.wgt[w];
+      epos += sh.weq[w];
+    }
+    for (int c = lo; c < lo + seg; c += 32) {
+      const int j = c + lane;
+      const uint32_t u = j < hi ? keys[j] : 0u;
+      const bool is_gt = j < hi && u > T, is_eq = j < hi && u == T;
       const uint32_t bgt = __ballot_sync(0xffffffffu, is_gt);
       const uint32_t beq = __ballot_sync(0xffffffffu, is_eq);
-      if (lane == 0) {
-        warp_gt[warp] = __popc(bgt);
-        warp_eq[warp] = __popc(beq);
-      }
-      __syncthreads();
-      uint32_t pre_gt = 0, pre_eq = 0, tot_gt = 0, tot_eq = 0;
-#pragma unroll
-      for (int w = 0; w < kSelWarps; ++w) {
-        const uint32_t g = warp_gt[w], e = warp_eq[w];
-        if (w < warp) {
-          pre_gt += g;
-          pre_eq += e;
-        }
-        tot_gt += g;
-        tot_eq += e;
-      }
-      const uint32_t lt_mask = (1u << lane) - 1u;
-      const uint64_t comp = ((uint64_t)u << 32) | (uint32_t)(~(uint32_t)j);
-      if (is_gt) cand[gt_base + pre_gt + __popc(bgt & lt_mask)] = comp;
+      const uint64_t comp = ((uint64_t)u << 32) | (uint32_t)j;
+      if (is_gt) bufA[gpos + __popc(bgt & lt)] = comp;
       if (is_eq) {
-        const uint32_t r = eq_base + pre_eq + __popc(beq & lt_mask);
-        if (r < (uint32_t)need) cand[n_gt + r] = comp;
+        const uint32_t r = epos + __popc(beq & lt);
+        if (r < (uint32_t)need) bufA[n_gt + r] = comp;
       }
-      gt_base += tot_gt;
-      eq_base += tot_eq;
-      __syncthreads();
+      gpos += __popc(bgt);
+      epos += __popc(beq);
     }
+    __syncthreads();
   }
-  // pad to a power of two with the smallest composite (below any real key)
-  for (int i = m + tid; i < kpad; i += kSelThreads) cand[i] = 0ull;
-  __syncthreads();
 
-  // ---- bitonic sort, descending ----
-  const int n2 = pow2_at_least(m < 1 ? 1 : m);
-  for (int size = 2; size <= n2; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = tid; i < n2 / 2; i += kSelThreads) {
-        const int lo = 2 * i - (i & (stride - 1));
-        const int hi = lo + stride;
-        const bool desc = (lo & size) == 0;
-        const uint64_t a = cand[lo], c = cand[hi];
-        if ((a < c) == desc) {
-          cand[lo] = c;
-          cand[hi] = a;
-        }
-      }
-      __syncthreads();
+  // ---- stable LSD radix sort of the m survivors, descending ----
+  uint64_t *cur = bufA, *alt = bufB;
+  for (int shift = 0; shift < 32; shift += 8) {
+    if (lsd_pass(cur, alt, m, shift, sh)) {
+      uint64_t *t = cur;
+      cur = alt;
+      alt = t;
     }
   }
 
@@ -176,8 +265,8 @@ __global__ void __launch_bounds__(kSelThreads)
   float *os = out_scores + (size_t)row * topk;
   for (int i = tid; i < topk; i += kSelThreads) {
     if (i < m) {
-      const uint64_t c = cand[i];
-      oi[i] = (int32_t)(~(uint32_t)c);
+      const uint64_t c = cur[i];
+      oi[i] = (int32_t)(uint32_t)c;
       os[i] = key_to_float((uint32_t)(c >> 32));
     } else {
       oi[i] = -1;
@@ -221,22 +310,22 @@ __global__ void fill_neg_inf_kernel(float *p, size_t n) {
 }  // namespace
 
 size_t topk_select_smem_bytes(int S_kv, int topk) {
-  const int kpad = pow2_at_least(topk < S_kv ? topk : S_kv);
-  return (size_t)kpad * 8 + (size_t)S_kv * 4;
+  const int mcap = topk < S_kv ? topk : S_kv;
+  return (size_t)mcap * 16 + (size_t)S_kv * 4 + sizeof(SelShared);
 }
 
 cudaError_t launch_topk_select(const Problem &p, const float *logits, int topk,
                                int32_t *out_idx, float *out_scores,
                                cudaStream_t st) {
-  const int kpad = pow2_at_least(topk < p.S_kv ? topk : p.S_kv);
-  const size_t smem = topk_select_smem_bytes(p.S_kv, topk);
+  const int mcap = topk < p.S_kv ? topk : p.S_kv;
+  const size_t smem = (size_t)mcap * 16 + (size_t)p.S_kv * 4;
   cudaError_t e = cudaFuncSetAttribute(
       topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
       (int)smem);
   if (e != cudaSuccess) return e;
   const long long rows = (long long)p.B * p.S;
   topk_select_kernel<<<(unsigned)rows, kSelThreads, smem, st>>>(
-      logits, p.q_pos, p.S, p.S_kv, p.ratio, topk, kpad, out_idx, out_scores);
+      logits, p.q_pos, p.S, p.S_kv, p.ratio, topk, mcap, out_idx, out_scores);
   return cudaGetLastError();
 }
 
