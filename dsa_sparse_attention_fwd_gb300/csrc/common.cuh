@@ -42,7 +42,6 @@ __host__ __device__ __forceinline__ int n_visible(long long pos, int ratio,
 constexpr int kTileKeys = 128;      // MMA M: compressed keys per tile
 constexpr int kTileCols = 256;      // MMA N: (query, head) columns per tile
 constexpr int kChunk = 64;          // bf16 per 128-byte swizzled row
-constexpr int kStages = 4;          // K-tile pipeline depth
 constexpr int kScoreThreads = 320;  // TMA warp, MMA warp, 8 epilogue warps
 
 // Top-k selection: a sort pass handles up to 256 threads x this many

@@ -12,8 +12,9 @@
 // tile i overlap the MMA of tile i+1.
 //
 // Warp roles (320 threads, one CTA per SM, persistent):
-//   warp 0      TMA producer: Q tile once per work item, K tiles through a
-//               4-stage ring.
+//   warp 0      TMA producer: Q tile once per work item into one of two Q
+//               buffers (so the next item's Q lands while the current one is
+//               multiplied), K tiles through a 3- or 4-stage ring.
 //   warp 1      TMEM allocator and MMA issuer (one thread).
 //   warps 2..9  epilogue: TMEM -> registers, ReLU, weight multiply-reduce over
 //               heads, causal mask, store of the visible scores.
@@ -29,14 +30,16 @@ namespace {
 
 template <int KC>
 struct ScoreSmem {
-  static constexpr int kQBytes = KC * kTileCols * 128;  // Q tile
+  static constexpr int kStages = KC == 1 ? 4 : 3;        // K ring depth
+  static constexpr int kQBytes = KC * kTileCols * 128;  // one Q tile
   static constexpr int kKBytes = KC * kTileKeys * 128;  // one K stage
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kQBytes;
+  static constexpr int kOffQ = 0;                        // 2 Q buffers
+  static constexpr int kOffK = kOffQ + 2 * kQBytes;
   static constexpr int kOffW = kOffK + kStages * kKBytes;
   static constexpr int kOffBar = kOffW + kTileCols * 4;
-  // barriers: k_full[S], k_empty[S], q_full, q_empty, acc_full[2], acc_empty[2]
-  static constexpr int kNumBars = 2 * kStages + 2 + 4;
+  // barriers: k_full[S], k_empty[S], q_full[2], q_empty[2], acc_full[2],
+  // acc_empty[2]
+  static constexpr int kNumBars = 2 * kStages + 4 + 4;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16;
   // room to align the base; at least 120 KB so that only one CTA fits on
@@ -82,6 +85,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                         float *__restrict__ logits, int S, int B, int S_kv,
                         int ratio, int *status) {
   using L = ScoreSmem<KC>;
+  constexpr int kStages = L::kStages;
   constexpr int TQ = kTileCols / H;  // queries per work item
   constexpr int QH = TQ / 2;         // queries per epilogue column half
   constexpr uint32_t kIdesc = idesc_bf16_f32(kTileKeys, kTileCols);
@@ -97,10 +101,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   const uint32_t bars = base + L::kOffBar;
   auto k_full = [&](int s) { return bars + 8u * s; };
   auto k_empty = [&](int s) { return bars + 8u * (kStages + s); };
-  const uint32_t q_full = bars + 8u * (2 * kStages);
-  const uint32_t q_empty = q_full + 8u;
-  auto acc_full = [&](int a) { return bars + 8u * (2 * kStages + 2 + a); };
-  auto acc_empty = [&](int a) { return bars + 8u * (2 * kStages + 4 + a); };
+  auto q_full = [&](int qs) { return bars + 8u * (2 * kStages + qs); };
+  auto q_empty = [&](int qs) { return bars + 8u * (2 * kStages + 2 + qs); };
+  auto acc_full = [&](int a) { return bars + 8u * (2 * kStages + 4 + a); };
+  auto acc_empty = [&](int a) { return bars + 8u * (2 * kStages + 6 + a); };
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kOffMisc);
   volatile int *abort_flag = reinterpret_cast<int *>(smem + L::kOffMisc + 4);
 
@@ -113,9 +117,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       mbar_init(k_full(s), 1);
       mbar_init(k_empty(s), 1);
     }
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
     for (int a = 0; a < 2; ++a) {
+      mbar_init(q_full(a), 1);
+      mbar_init(q_empty(a), 1);
       mbar_init(acc_full(a), 1);
       mbar_init(acc_empty(a), 8);  // one arrival per epilogue warp
     }
@@ -136,19 +140,21 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      uint32_t kst = 0, kph = 0, qph = 0;
+      uint32_t kst = 0, kph = 0, nq = 0;
       bool ok = true;
       for (int r = 0; ok; ++r) {
         const int item = item_for(r, n_items);
         if (item < 0) break;
         const ItemInfo it = item_info<H>(item, S, B, S_kv, ratio, q_pos);
         if (it.ntiles == 0) continue;
-        if (!(ok = wait_bar(q_empty, qph ^ 1u, abort_flag, status))) break;
-        qph ^= 1u;
-        mbar_arrive_expect_tx(q_full, L::kQBytes);
+        const int qs = nq & 1;
+        const uint32_t qph = (nq >> 1) & 1u;
+        ++nq;
+        if (!(ok = wait_bar(q_empty(qs), qph ^ 1u, abort_flag, status))) break;
+        mbar_arrive_expect_tx(q_full(qs), L::kQBytes);
         for (int c = 0; c < KC; ++c)
-          tma_load_4d(sQ + c * (kTileCols * 128), &tm_q, q_full, c * kChunk,
-                      0, it.b, it.t0);
+          tma_load_4d(sQ + qs * L::kQBytes + c * (kTileCols * 128), &tm_q,
+                      q_full(qs), c * kChunk, 0, it.b, it.t0);
         for (int tile = 0; tile < it.ntiles; ++tile) {
           if (!(ok = wait_bar(k_empty(kst), kph ^ 1u, abort_flag, status)))
             break;
@@ -166,15 +172,18 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      uint32_t kst = 0, kph = 0, qph = 0, acc = 0, aph = 0;
+      uint32_t kst = 0, kph = 0, nq = 0, acc = 0, aph = 0;
       bool ok = true;
       for (int r = 0; ok; ++r) {
         const int item = item_for(r, n_items);
         if (item < 0) break;
         const ItemInfo it = item_info<H>(item, S, B, S_kv, ratio, q_pos);
         if (it.ntiles == 0) continue;
-        if (!(ok = wait_bar(q_full, qph, abort_flag, status))) break;
-        qph ^= 1u;
+        const int qs = nq & 1;
+        const uint32_t qph = (nq >> 1) & 1u;
+        ++nq;
+        if (!(ok = wait_bar(q_full(qs), qph, abort_flag, status))) break;
+        const uint32_t sQi = sQ + qs * L::kQBytes;
         for (int tile = 0; tile < it.ntiles; ++tile) {
           if (!(ok = wait_bar(acc_empty(acc), aph ^ 1u, abort_flag, status)))
             break;
@@ -188,13 +197,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
               const uint64_t ad = sdesc_k_sw128(
                   sK + kst * L::kKBytes + c * (kTileKeys * 128) + kk * 32);
               const uint64_t bd =
-                  sdesc_k_sw128(sQ + c * (kTileCols * 128) + kk * 32);
+                  sdesc_k_sw128(sQi + c * (kTileCols * 128) + kk * 32);
               mma_bf16(d_tmem, ad, bd, kIdesc, (c | kk) != 0);
             }
           }
           mma_commit(k_empty(kst));   // K stage reusable when done
           mma_commit(acc_full(acc));  // accumulator ready
-          if (tile == it.ntiles - 1) mma_commit(q_empty);
+          if (tile == it.ntiles - 1) mma_commit(q_empty(qs));
           if (++kst == kStages) {
             kst = 0;
             kph ^= 1u;
