@@ -5,15 +5,19 @@
 // One CTA (8 warps) per row.  The row's n visible fp32 scores are staged in
 // shared memory as order-preserving unsigned keys (larger float <-> larger
 // key; -0.0 folded onto +0.0 so the index tie-break decides between them).
-//   1. When n > topk, a most-significant-digit-first radix select (four 8-bit
-//      digits; histogram updates aggregated per warp with match_any) finds T,
-//      the topk-th largest key, and an ordered two-walk compaction keeps every
-//      key > T and the lowest-index keys == T, in index order.
-//   2. A stable least-significant-digit radix sort (four 8-bit digits,
+//   1. When n > topk, a most-significant-digit-first radix select finds T,
+//      the topk-th largest key, in three histogram passes (12, 12 and 8
+//      bits; the first 12 bits are the sign, the exponent and three mantissa
+//      bits, which spreads typical scores over many bins).  An ordered
+//      two-walk compaction then keeps every key > T and the lowest-index
+//      keys == T, in index order.
+//   2. A stable least-significant-digit radix sort (8-bit digits,
 //      descending) orders the m = min(n, topk) survivors, packed as
-//      (key << 32 | j).  Stability keeps equal keys in index order, which is
-//      exactly the "lower index first" tie rule.  A pass whose digit is the
-//      same for every element is skipped.
+//      (key << 32 | j).  Within a warp, equal digits are ranked with eight
+//      ballots (one per digit bit), so the rank follows element order and
+//      the sort is stable; stability keeps equal keys in index order, which
+//      is the "lower index first" tie rule.  Digit positions on which every
+//      survivor agrees (found by an AND/OR reduction) are skipped.
 #include "common.cuh"
 
 namespace dsa {
@@ -21,7 +25,7 @@ namespace {
 
 constexpr int kSelThreads = 256;
 constexpr int kSelWarps = kSelThreads / 32;
-constexpr int kMaxEpt = DSA_SEL_MAX_EPT;  // elements per lane per sort pass
+constexpr int kHistBins = 4096;  // 12-bit select digit
 
 __device__ __forceinline__ uint32_t ordered_key(float f) {
   uint32_t u = __float_as_uint(f);
@@ -39,13 +43,26 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
   return m;
 }
 
+// Lanes of this warp whose 8-bit digit equals mine (0 for invalid lanes).
+__device__ __forceinline__ uint32_t digit_peers(uint32_t d, bool valid) {
+  uint32_t m = __ballot_sync(0xffffffffu, valid);
+#pragma unroll
+  for (int b = 0; b < 8; ++b) {
+    const bool bit = (d >> b) & 1u;
+    const uint32_t bal = __ballot_sync(0xffffffffu, bit);
+    m &= bit ? bal : ~bal;
+  }
+  return valid ? m : 0u;
+}
+
 struct SelShared {
-  uint32_t whist[kSelWarps][256];  // per-warp digit counts / offsets
-  uint32_t hist[256];              // block histogram / digit bases
+  uint32_t (*whist)[256];          // per-warp digit counts / offsets; lives
+                                   // in the row-key buffer, dead by then
+  uint32_t dbase[256];             // digit bases of a sort pass
   uint32_t wsum[kSelWarps];
   uint32_t wgt[kSelWarps], weq[kSelWarps];
+  uint32_t wand[kSelWarps], wor[kSelWarps];
   uint32_t sel_digit, sel_above;
-  int skip;
 };
 
 // Exclusive prefix sum of one value per thread over the 256-thread block.
@@ -63,16 +80,16 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, SelShared &sh) {
 #pragma unroll
   for (int w = 0; w < kSelWarps; ++w)
     if (w < warp) pre += sh.wsum[w];
+  __syncthreads();  // wsum may be rewritten by the next scan
   return pre + incl - v;
 }
 
-// One stable counting-sort pass on digit (key >> shift) & 255, descending.
-// Returns true when the pass moved data into dst, false when every element
-// has the same digit (then src already holds the pass's result).
-__device__ __forceinline__ bool lsd_pass(const uint64_t *src, uint64_t *dst,
+// One stable counting-sort pass of src[0..m) into dst on digit
+// (key >> shift) & 255, descending.
+template <int EPT>
+__device__ __forceinline__ void lsd_pass(const uint64_t *src, uint64_t *dst,
                                          int m, int shift, SelShared &sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int tid = threadIdx.x;
   const int per_warp = ((m + kSelThreads - 1) / kSelThreads) * 32;
   const int ept = per_warp / 32;
   const int seg = warp * per_warp;
@@ -80,16 +97,15 @@ __device__ __forceinline__ bool lsd_pass(const uint64_t *src, uint64_t *dst,
   const uint32_t lt = lanemask_lt();
   for (int i = lane; i < 256; i += 32) wh[i] = 0;
   __syncwarp();
-  uint32_t off[kMaxEpt];
+  uint32_t off[EPT];
 #pragma unroll
-  for (int it = 0; it < kMaxEpt; ++it) {
+  for (int it = 0; it < EPT; ++it) {
     if (it < ept) {
       const int e = seg + it * 32 + lane;
       const bool valid = e < m;
       const uint64_t v = valid ? src[e] : 0ull;
-      const uint32_t d =
-          valid ? 255u - (uint32_t)((v >> (32 + shift)) & 255u) : 256u;
-      const uint32_t peers = __match_any_sync(0xffffffffu, d);
+      const uint32_t d = 255u - (uint32_t)((v >> (32 + shift)) & 255u);
+      const uint32_t peers = digit_peers(d, valid);
       const uint32_t rank = __popc(peers & lt);
       const uint32_t base = valid ? wh[d] : 0u;
       __syncwarp();
@@ -98,10 +114,9 @@ __device__ __forceinline__ bool lsd_pass(const uint64_t *src, uint64_t *dst,
       off[it] = base + rank;
     }
   }
-  if (tid == 0) sh.skip = 0;
   __syncthreads();
   {
-    const int d = tid;  // 256 threads, one digit each
+    const int d = threadIdx.x;  // 256 threads, one digit each
     uint32_t run = 0;
 #pragma unroll
     for (int w = 0; w < kSelWarps; ++w) {
@@ -109,40 +124,38 @@ __device__ __forceinline__ bool lsd_pass(const uint64_t *src, uint64_t *dst,
       sh.whist[w][d] = run;
       run += c;
     }
-    if (run == (uint32_t)m) sh.skip = 1;
-    const uint32_t b = block_excl_scan(run, sh);
-    sh.hist[d] = b;
+    sh.dbase[d] = block_excl_scan(run, sh);
   }
   __syncthreads();
-  const bool skip = sh.skip != 0;
-  __syncthreads();  // everyone has read the flag before it is reset
-  if (skip) return false;  // block-uniform
 #pragma unroll
-  for (int it = 0; it < kMaxEpt; ++it) {
+  for (int it = 0; it < EPT; ++it) {
     if (it < ept) {
       const int e = seg + it * 32 + lane;
       if (e < m) {
         const uint64_t v = src[e];
         const uint32_t d = 255u - (uint32_t)((v >> (32 + shift)) & 255u);
-        dst[sh.hist[d] + wh[d] + off[it]] = v;
+        dst[sh.dbase[d] + wh[d] + off[it]] = v;
       }
     }
   }
   __syncthreads();
-  return true;
 }
 
+template <int EPT>
 __global__ void __launch_bounds__(kSelThreads)
     topk_select_kernel(const float *__restrict__ logits,
                        const int32_t *__restrict__ q_pos, int S, int S_kv,
-                       int ratio, int topk, int mcap,
+                       int ratio, int topk, int mcap, int bcap,
                        int32_t *__restrict__ out_idx,
                        float *__restrict__ out_scores) {
   extern __shared__ __align__(16) uint8_t smem[];
-  uint64_t *bufA = reinterpret_cast<uint64_t *>(smem);      // [mcap]
-  uint64_t *bufB = bufA + mcap;                              // [mcap]
-  uint32_t *keys = reinterpret_cast<uint32_t *>(bufB + mcap);  // [S_kv]
+  uint64_t *bufA = reinterpret_cast<uint64_t *>(smem);  // [mcap]
+  uint64_t *bufB = bufA + mcap;                          // [bcap] (>= 4096 u32)
+  uint32_t *hist = reinterpret_cast<uint32_t *>(bufB);   // select histogram
+  uint32_t *keys = reinterpret_cast<uint32_t *>(bufB + bcap);  // [S_kv]
   __shared__ SelShared sh;
+  if (threadIdx.x == 0)
+    sh.whist = reinterpret_cast<uint32_t(*)[256]>(keys);
 
   const int row = blockIdx.x;  // row id = b * S + s, the output order
   const int b = row / S, s = row % S;
@@ -159,55 +172,44 @@ __global__ void __launch_bounds__(kSelThreads)
   } else {
     for (int j = tid; j < nv; j += kSelThreads)
       keys[j] = ordered_key(__ldg(L + j));
-    __syncthreads();
-    // ---- radix select of T, the topk-th largest key ----
+    // ---- radix select of T, the topk-th largest key: 12 + 12 + 8 bits ----
     uint32_t prefix = 0, pmask = 0;
     int need = topk;  // still to take among keys matching prefix
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      sh.hist[tid] = 0;
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+      const int shift = pass == 0 ? 20 : (pass == 1 ? 8 : 0);
+      const int bits = pass == 2 ? 8 : 12;
+      const int nb = 1 << bits, per = nb / kSelThreads;
+      const uint32_t dmask = (uint32_t)nb - 1u;
+      for (int i = tid; i < nb; i += kSelThreads) hist[i] = 0;
       __syncthreads();
-      for (int c0 = 0; c0 < nv; c0 += kSelThreads) {
-        const int j = c0 + tid;
-        const uint32_t u = j < nv ? keys[j] : 0u;
-        const bool ok = j < nv && (u & pmask) == prefix;
-        const uint32_t d = ok ? (u >> shift) & 255u : 256u;
-        const uint32_t peers = __match_any_sync(0xffffffffu, d);
-        if (ok && (peers & lt) == 0) atomicAdd(&sh.hist[d], __popc(peers));
+      for (int j = tid; j < nv; j += kSelThreads) {
+        const uint32_t u = keys[j];
+        if ((u & pmask) == prefix) atomicAdd(&hist[(u >> shift) & dmask], 1u);
       }
       __syncthreads();
-      if (warp == 0) {
-        // lane l owns digits [8l, 8l+8); find the largest digit d with
-        // count(digit >= d) >= need
-        uint32_t c[8];
-        uint32_t lsum = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          c[i] = sh.hist[lane * 8 + i];
-          lsum += c[i];
-        }
-        uint32_t incl = lsum;  // inclusive suffix sum over lanes
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const uint32_t o = __shfl_down_sync(0xffffffffu, incl, off);
-          if (lane + off < 32) incl += o;
-        }
-        const uint32_t above = incl - lsum;
-        if (above < (uint32_t)need && (uint32_t)need <= incl) {
-          uint32_t run = above;
-          for (int i = 7; i >= 0; --i) {
-            if (run + c[i] >= (uint32_t)need) {
-              sh.sel_digit = (uint32_t)(lane * 8 + i);
-              sh.sel_above = run;
-              break;
-            }
-            run += c[i];
+      // thread t owns bins [o*per, o*per+per) with o = 255 - t, so an
+      // exclusive scan in thread order counts the bins above its own
+      const int o = kSelThreads - 1 - tid;
+      uint32_t lsum = 0;
+      for (int i = 0; i < per; ++i) lsum += hist[o * per + i];
+      const uint32_t above = block_excl_scan(lsum, sh);
+      if (above < (uint32_t)need && (uint32_t)need <= above + lsum) {
+        uint32_t run = above;
+        for (int i = per - 1; i >= 0; --i) {
+          const uint32_t c = hist[o * per + i];
+          if (run + c >= (uint32_t)need) {
+            sh.sel_digit = (uint32_t)(o * per + i);
+            sh.sel_above = run;
+            break;
           }
+          run += c;
         }
       }
       __syncthreads();
       need -= (int)sh.sel_above;
       prefix |= sh.sel_digit << shift;
-      pmask |= 255u << shift;
+      pmask |= dmask << shift;
       __syncthreads();
     }
     const uint32_t T = prefix;
@@ -251,14 +253,39 @@ __global__ void __launch_bounds__(kSelThreads)
     __syncthreads();
   }
 
+  // ---- bits on which the survivors differ ----
+  uint32_t kand = 0xffffffffu, kor = 0u;
+  for (int i = tid; i < m; i += kSelThreads) {
+    const uint32_t k = (uint32_t)(bufA[i] >> 32);
+    kand &= k;
+    kor |= k;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    kand &= __shfl_xor_sync(0xffffffffu, kand, off);
+    kor |= __shfl_xor_sync(0xffffffffu, kor, off);
+  }
+  if (lane == 0) {
+    sh.wand[warp] = kand;
+    sh.wor[warp] = kor;
+  }
+  __syncthreads();
+  uint32_t diff = 0, all_and = 0xffffffffu, all_or = 0u;
+#pragma unroll
+  for (int w = 0; w < kSelWarps; ++w) {
+    all_and &= sh.wand[w];
+    all_or |= sh.wor[w];
+  }
+  diff = all_and ^ all_or;  // block-uniform
+
   // ---- stable LSD radix sort of the m survivors, descending ----
   uint64_t *cur = bufA, *alt = bufB;
   for (int shift = 0; shift < 32; shift += 8) {
-    if (lsd_pass(cur, alt, m, shift, sh)) {
-      uint64_t *t = cur;
-      cur = alt;
-      alt = t;
-    }
+    if (((diff >> shift) & 255u) == 0u) continue;  // every digit equal
+    lsd_pass<EPT>(cur, alt, m, shift, sh);
+    uint64_t *t = cur;
+    cur = alt;
+    alt = t;
   }
 
   int32_t *oi = out_idx + (size_t)row * topk;
@@ -307,26 +334,54 @@ __global__ void fill_neg_inf_kernel(float *p, size_t n) {
     p[i] = neg_inf;
 }
 
+// Dynamic shared memory of one selection CTA: bufA [mcap] u64, bufB
+// [bcap] u64 (also the 4096-bin select histogram), keys [S_kv] u32 (at least
+// 8 KB: the sort's per-warp histograms reuse it once the keys are dead).
+struct SelLayout {
+  int mcap, bcap;
+  size_t dyn;
+};
+
+SelLayout sel_layout(int S_kv, int topk) {
+  SelLayout l;
+  l.mcap = topk < S_kv ? topk : S_kv;
+  l.bcap = l.mcap > kHistBins / 2 ? l.mcap : kHistBins / 2;
+  const size_t key_bytes = (size_t)S_kv * 4;
+  const size_t whist_bytes = (size_t)kSelWarps * 256 * 4;
+  l.dyn = (size_t)(l.mcap + l.bcap) * 8 +
+          (key_bytes > whist_bytes ? key_bytes : whist_bytes);
+  return l;
+}
+
+template <int EPT>
+cudaError_t launch_sel(const Problem &p, const float *logits, int topk,
+                       int32_t *out_idx, float *out_scores, cudaStream_t st) {
+  const SelLayout l = sel_layout(p.S_kv, topk);
+  auto kern = topk_select_kernel<EPT>;
+  cudaError_t e = cudaFuncSetAttribute(
+      kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)l.dyn);
+  if (e != cudaSuccess) return e;
+  const long long rows = (long long)p.B * p.S;
+  kern<<<(unsigned)rows, kSelThreads, l.dyn, st>>>(
+      logits, p.q_pos, p.S, p.S_kv, p.ratio, topk, l.mcap, l.bcap, out_idx,
+      out_scores);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 size_t topk_select_smem_bytes(int S_kv, int topk) {
-  const int mcap = topk < S_kv ? topk : S_kv;
-  return (size_t)mcap * 16 + (size_t)S_kv * 4 + sizeof(SelShared);
+  return sel_layout(S_kv, topk).dyn + sizeof(SelShared);
 }
 
 cudaError_t launch_topk_select(const Problem &p, const float *logits, int topk,
                                int32_t *out_idx, float *out_scores,
                                cudaStream_t st) {
-  const int mcap = topk < p.S_kv ? topk : p.S_kv;
-  const size_t smem = (size_t)mcap * 16 + (size_t)p.S_kv * 4;
-  cudaError_t e = cudaFuncSetAttribute(
-      topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-      (int)smem);
-  if (e != cudaSuccess) return e;
-  const long long rows = (long long)p.B * p.S;
-  topk_select_kernel<<<(unsigned)rows, kSelThreads, smem, st>>>(
-      logits, p.q_pos, p.S, p.S_kv, p.ratio, topk, mcap, out_idx, out_scores);
-  return cudaGetLastError();
+  const int m = topk < p.S_kv ? topk : p.S_kv;
+  if (m <= kSelThreads * 8)
+    return launch_sel<8>(p, logits, topk, out_idx, out_scores, st);
+  return launch_sel<DSA_SEL_MAX_EPT>(p, logits, topk, out_idx, out_scores,
+                                     st);
 }
 
 cudaError_t launch_gather_scores(const Problem &p, const float *logits,
