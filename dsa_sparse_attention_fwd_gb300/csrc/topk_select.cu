@@ -13,11 +13,16 @@
 //      keys == T, in index order.
 //   2. A stable least-significant-digit radix sort (8-bit digits,
 //      descending) orders the m = min(n, topk) survivors, packed as
-//      (key << 32 | j).  Within a warp, equal digits are ranked with eight
-//      ballots (one per digit bit), so the rank follows element order and
-//      the sort is stable; stability keeps equal keys in index order, which
-//      is the "lower index first" tie rule.  Digit positions on which every
-//      survivor agrees (found by an AND/OR reduction) are skipped.
+//      (key << 32 | j), on the top 16 key bits only.  Within a warp, equal
+//      digits are ranked with eight ballots (one per digit bit), so the rank
+//      follows element order and the sort is stable; stability keeps equal
+//      keys in index order, which is the "lower index first" tie rule.
+//      Digit positions on which every survivor agrees (found by an AND/OR
+//      reduction) are skipped.
+//   3. Runs of equal top 16 bits (a few elements for real score
+//      distributions) are ordered by the low 16 bits by counting inside the
+//      run.  If any run is longer than 32 (heavily tied inputs), the
+//      candidates are rebuilt and sorted on all four digits instead.
 #include "common.cuh"
 
 namespace dsa {
@@ -63,6 +68,7 @@ struct SelShared {
   uint32_t wgt[kSelWarps], weq[kSelWarps];
   uint32_t wand[kSelWarps], wor[kSelWarps];
   uint32_t sel_digit, sel_above;
+  int overflow;
 };
 
 // Exclusive prefix sum of one value per thread over the 256-thread block.
@@ -141,6 +147,53 @@ __device__ __forceinline__ void lsd_pass(const uint64_t *src, uint64_t *dst,
   __syncthreads();
 }
 
+// Fix-up after sorting on the top 16 key bits: inside each run of equal top
+// 16 bits (already in index order), order by the low 16 bits, descending,
+// keeping index order among equal keys.  Writes the result to dst.  Returns
+// true (block-uniform) when some run is longer than kRunLimit, in which case
+// dst is incomplete and the caller falls back to a full sort.
+constexpr int kRunLimit = 32;
+
+__device__ __forceinline__ bool run_fixup(const uint64_t *src, uint64_t *dst,
+                                          int m, SelShared &sh) {
+  if (threadIdx.x == 0) sh.overflow = 0;
+  __syncthreads();
+  bool over = false;
+  for (int i = threadIdx.x; i < m; i += kSelThreads) {
+    const uint64_t v = src[i];
+    const uint32_t top = (uint32_t)(v >> 48);
+    const uint32_t low = (uint32_t)(v >> 32) & 0xFFFFu;
+    int cnt = 0, r = i - 1, steps = 0;
+    while (r >= 0 && steps < kRunLimit) {
+      const uint64_t u = src[r];
+      if ((uint32_t)(u >> 48) != top) break;
+      cnt += (((uint32_t)(u >> 32) & 0xFFFFu) >= low);
+      --r;
+      ++steps;
+    }
+    if (steps == kRunLimit && r >= 0 && (uint32_t)(src[r] >> 48) == top)
+      over = true;
+    const int start = r + 1;
+    r = i + 1;
+    steps = 0;
+    while (r < m && steps < kRunLimit) {
+      const uint64_t u = src[r];
+      if ((uint32_t)(u >> 48) != top) break;
+      cnt += (((uint32_t)(u >> 32) & 0xFFFFu) > low);
+      ++r;
+      ++steps;
+    }
+    if (steps == kRunLimit && r < m && (uint32_t)(src[r] >> 48) == top)
+      over = true;
+    if (!over) dst[start + cnt] = v;
+  }
+  if (over) sh.overflow = 1;
+  __syncthreads();
+  const bool any = sh.overflow != 0;
+  __syncthreads();
+  return any;
+}
+
 template <int EPT>
 __global__ void __launch_bounds__(kSelThreads)
     topk_select_kernel(const float *__restrict__ logits,
@@ -165,16 +218,66 @@ __global__ void __launch_bounds__(kSelThreads)
   const int m = nv < topk ? nv : topk;
   const uint32_t lt = lanemask_lt();
 
-  if (nv <= topk) {
+  // the candidates, (key << 32 | j) in index order (within each of the
+  // "above T" and "equal to T" groups), into bufA
+  uint32_t T = 0;
+  int need = 0, n_gt = 0;
+  auto load_keys = [&]() {
+    for (int j = tid; j < nv; j += kSelThreads)
+      keys[j] = ordered_key(__ldg(L + j));
+  };
+  auto load_all = [&]() {
     for (int j = tid; j < nv; j += kSelThreads)
       bufA[j] = ((uint64_t)ordered_key(__ldg(L + j)) << 32) | (uint32_t)j;
     __syncthreads();
+  };
+  // ordered compaction, two walks over contiguous warp segments
+  auto compact = [&]() {
+    __syncthreads();
+    const int seg = ((nv + kSelThreads - 1) / kSelThreads) * 32;
+    const int lo = warp * seg, hi = min(nv, lo + seg);
+    uint32_t cgt = 0, ceq = 0;
+    for (int c = lo; c < lo + seg; c += 32) {
+      const int j = c + lane;
+      const uint32_t u = j < hi ? keys[j] : 0u;
+      cgt += __popc(__ballot_sync(0xffffffffu, j < hi && u > T));
+      ceq += __popc(__ballot_sync(0xffffffffu, j < hi && u == T));
+    }
+    if (lane == 0) {
+      sh.wgt[warp] = cgt;
+      sh.weq[warp] = ceq;
+    }
+    __syncthreads();
+    uint32_t gpos = 0, epos = 0;
+    for (int w = 0; w < warp; ++w) {
+      gpos += sh.wgt[w];
+      epos += sh.weq[w];
+    }
+    for (int c = lo; c < lo + seg; c += 32) {
+      const int j = c + lane;
+      const uint32_t u = j < hi ? keys[j] : 0u;
+      const bool is_gt = j < hi && u > T, is_eq = j < hi && u == T;
+      const uint32_t bgt = __ballot_sync(0xffffffffu, is_gt);
+      const uint32_t beq = __ballot_sync(0xffffffffu, is_eq);
+      const uint64_t comp = ((uint64_t)u << 32) | (uint32_t)j;
+      if (is_gt) bufA[gpos + __popc(bgt & lt)] = comp;
+      if (is_eq) {
+        const uint32_t r = epos + __popc(beq & lt);
+        if (r < (uint32_t)need) bufA[n_gt + r] = comp;
+      }
+      gpos += __popc(bgt);
+      epos += __popc(beq);
+    }
+    __syncthreads();
+  };
+
+  if (nv <= topk) {
+    load_all();
   } else {
-    for (int j = tid; j < nv; j += kSelThreads)
-      keys[j] = ordered_key(__ldg(L + j));
+    load_keys();
     // ---- radix select of T, the topk-th largest key: 12 + 12 + 8 bits ----
     uint32_t prefix = 0, pmask = 0;
-    int need = topk;  // still to take among keys matching prefix
+    need = topk;  // still to take among keys matching prefix
 #pragma unroll 1
     for (int pass = 0; pass < 3; ++pass) {
       const int shift = pass == 0 ? 20 : (pass == 1 ? 8 : 0);
@@ -212,45 +315,9 @@ __global__ void __launch_bounds__(kSelThreads)
       pmask |= dmask << shift;
       __syncthreads();
     }
-    const uint32_t T = prefix;
-    const int n_gt = topk - need;  // keys strictly above T, all kept
-
-    // ---- ordered compaction, two walks over contiguous warp segments ----
-    const int seg = ((nv + kSelThreads - 1) / kSelThreads) * 32;
-    const int lo = warp * seg, hi = min(nv, lo + seg);
-    uint32_t cgt = 0, ceq = 0;
-    for (int c = lo; c < lo + seg; c += 32) {
-      const int j = c + lane;
-      const uint32_t u = j < hi ? keys[j] : 0u;
-      cgt += __popc(__ballot_sync(0xffffffffu, j < hi && u > T));
-      ceq += __popc(__ballot_sync(0xffffffffu, j < hi && u == T));
-    }
-    if (lane == 0) {
-      sh.wgt[warp] = cgt;
-      sh.weq[warp] = ceq;
-    }
-    __syncthreads();
-    uint32_t gpos = 0, epos = 0;
-    for (int w = 0; w < warp; ++w) {
-      gpos += sh.wgt[w];
-      epos += sh.weq[w];
-    }
-    for (int c = lo; c < lo + seg; c += 32) {
-      const int j = c + lane;
-      const uint32_t u = j < hi ? keys[j] : 0u;
-      const bool is_gt = j < hi && u > T, is_eq = j < hi && u == T;
-      const uint32_t bgt = __ballot_sync(0xffffffffu, is_gt);
-      const uint32_t beq = __ballot_sync(0xffffffffu, is_eq);
-      const uint64_t comp = ((uint64_t)u << 32) | (uint32_t)j;
-      if (is_gt) bufA[gpos + __popc(bgt & lt)] = comp;
-      if (is_eq) {
-        const uint32_t r = epos + __popc(beq & lt);
-        if (r < (uint32_t)need) bufA[n_gt + r] = comp;
-      }
-      gpos += __popc(bgt);
-      epos += __popc(beq);
-    }
-    __syncthreads();
+    T = prefix;
+    n_gt = topk - need;  // keys strictly above T, all kept
+    compact();
   }
 
   // ---- bits on which the survivors differ ----
@@ -270,22 +337,47 @@ __global__ void __launch_bounds__(kSelThreads)
     sh.wor[warp] = kor;
   }
   __syncthreads();
-  uint32_t diff = 0, all_and = 0xffffffffu, all_or = 0u;
+  uint32_t all_and = 0xffffffffu, all_or = 0u;
 #pragma unroll
   for (int w = 0; w < kSelWarps; ++w) {
     all_and &= sh.wand[w];
     all_or |= sh.wor[w];
   }
-  diff = all_and ^ all_or;  // block-uniform
+  const uint32_t diff = all_and ^ all_or;  // block-uniform
 
-  // ---- stable LSD radix sort of the m survivors, descending ----
+  // ---- stable LSD radix sort on the top 16 key bits, then a run fix-up
+  // on the low 16 bits; a full four-digit sort when runs are long ----
   uint64_t *cur = bufA, *alt = bufB;
-  for (int shift = 0; shift < 32; shift += 8) {
+  for (int shift = 16; shift < 32; shift += 8) {
     if (((diff >> shift) & 255u) == 0u) continue;  // every digit equal
     lsd_pass<EPT>(cur, alt, m, shift, sh);
     uint64_t *t = cur;
     cur = alt;
     alt = t;
+  }
+  if ((diff & 0xFFFFu) != 0u) {
+    if (!run_fixup(cur, alt, m, sh)) {
+      uint64_t *t = cur;
+      cur = alt;
+      alt = t;
+    } else {
+      // long runs of equal top bits: rebuild the candidates, sort all digits
+      if (nv <= topk) {
+        load_all();
+      } else {
+        load_keys();  // the sort's counters reused the key buffer
+        compact();
+      }
+      cur = bufA;
+      alt = bufB;
+      for (int shift = 0; shift < 32; shift += 8) {
+        if (((diff >> shift) & 255u) == 0u) continue;
+        lsd_pass<EPT>(cur, alt, m, shift, sh);
+        uint64_t *t = cur;
+        cur = alt;
+        alt = t;
+      }
+    }
   }
 
   int32_t *oi = out_idx + (size_t)row * topk;
