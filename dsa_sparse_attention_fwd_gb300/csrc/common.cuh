@@ -44,8 +44,9 @@ constexpr int kTileCols = 256;      // MMA N: (query, head) columns per tile
 constexpr int kChunk = 64;          // bf16 per 128-byte swizzled row
 constexpr int kScoreThreads = 320;  // TMA warp, MMA warp, 8 epilogue warps
 
-// Top-k selection: a sort pass handles up to 256 threads x this many
-// elements, so topk <= 256 * DSA_SEL_MAX_EPT (= DSA_MAX_TOPK).
+// Top-k selection: a sort pass handles up to 256 threads x (this + 2)
+// elements, i.e. topk + 256 candidates with topk <= 256 * DSA_SEL_MAX_EPT
+// (= DSA_MAX_TOPK).
 #define DSA_SEL_MAX_EPT 32
 
 // Launchers (return cudaSuccess or the launch error).  `logits` is

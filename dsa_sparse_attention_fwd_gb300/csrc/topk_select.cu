@@ -31,6 +31,7 @@ namespace {
 constexpr int kSelThreads = 256;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kHistBins = 4096;  // 12-bit select digit
+constexpr int kSelSlack = 256;   // extra candidates a one-pass select keeps
 
 __device__ __forceinline__ uint32_t ordered_key(float f) {
   uint32_t u = __float_as_uint(f);
@@ -67,7 +68,7 @@ struct SelShared {
   uint32_t wsum[kSelWarps];
   uint32_t wgt[kSelWarps], weq[kSelWarps];
   uint32_t wand[kSelWarps], wor[kSelWarps];
-  uint32_t sel_digit, sel_above;
+  uint32_t sel_digit, sel_above, sel_count;
   int overflow;
 };
 
@@ -147,8 +148,8 @@ __device__ __forceinline__ void lsd_pass(const uint64_t *src, uint64_t *dst,
   __syncthreads();
 }
 
-// Fix-up after sorting on the top 16 key bits: inside each run of equal top
-// 16 bits (already in index order), order by the low 16 bits, descending,
+// Fix-up after sorting on the top 24 key bits: inside each run of equal top
+// 24 bits (already in index order), order by the low 8 bits, descending,
 // keeping index order among equal keys.  Writes the result to dst.  Returns
 // true (block-uniform) when some run is longer than kRunLimit, in which case
 // dst is incomplete and the caller falls back to a full sort.
@@ -161,29 +162,29 @@ __device__ __forceinline__ bool run_fixup(const uint64_t *src, uint64_t *dst,
   bool over = false;
   for (int i = threadIdx.x; i < m; i += kSelThreads) {
     const uint64_t v = src[i];
-    const uint32_t top = (uint32_t)(v >> 48);
-    const uint32_t low = (uint32_t)(v >> 32) & 0xFFFFu;
+    const uint32_t top = (uint32_t)(v >> 40);
+    const uint32_t low = (uint32_t)(v >> 32) & 0xFFu;
     int cnt = 0, r = i - 1, steps = 0;
     while (r >= 0 && steps < kRunLimit) {
       const uint64_t u = src[r];
-      if ((uint32_t)(u >> 48) != top) break;
-      cnt += (((uint32_t)(u >> 32) & 0xFFFFu) >= low);
+      if ((uint32_t)(u >> 40) != top) break;
+      cnt += (((uint32_t)(u >> 32) & 0xFFu) >= low);
       --r;
       ++steps;
     }
-    if (steps == kRunLimit && r >= 0 && (uint32_t)(src[r] >> 48) == top)
+    if (steps == kRunLimit && r >= 0 && (uint32_t)(src[r] >> 40) == top)
       over = true;
     const int start = r + 1;
     r = i + 1;
     steps = 0;
     while (r < m && steps < kRunLimit) {
       const uint64_t u = src[r];
-      if ((uint32_t)(u >> 48) != top) break;
-      cnt += (((uint32_t)(u >> 32) & 0xFFFFu) > low);
+      if ((uint32_t)(u >> 40) != top) break;
+      cnt += (((uint32_t)(u >> 32) & 0xFFu) > low);
       ++r;
       ++steps;
     }
-    if (steps == kRunLimit && r < m && (uint32_t)(src[r] >> 48) == top)
+    if (steps == kRunLimit && r < m && (uint32_t)(src[r] >> 40) == top)
       over = true;
     if (!over) dst[start + cnt] = v;
   }
@@ -215,7 +216,6 @@ __global__ void __launch_bounds__(kSelThreads)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nv = n_visible(row_pos(q_pos, b, s), ratio, S_kv);
   const float *L = logits + (size_t)row * S_kv;
-  const int m = nv < topk ? nv : topk;
   const uint32_t lt = lanemask_lt();
 
   // the candidates, (key << 32 | j) in index order (within each of the
@@ -240,8 +240,8 @@ __global__ void __launch_bounds__(kSelThreads)
     for (int c = lo; c < lo + seg; c += 32) {
       const int j = c + lane;
       const uint32_t u = j < hi ? keys[j] : 0u;
-      cgt += __popc(__ballot_sync(0xffffffffu, j < hi && u > T));
-      ceq += __popc(__ballot_sync(0xffffffffu, j < hi && u == T));
+      cgt += __popc(__ballot_sync(0xffffffffu, j < hi && (u > T || (need == 0 && u == T))));
+      ceq += __popc(__ballot_sync(0xffffffffu, j < hi && need > 0 && u == T));
     }
     if (lane == 0) {
       sh.wgt[warp] = cgt;
@@ -256,7 +256,8 @@ __global__ void __launch_bounds__(kSelThreads)
     for (int c = lo; c < lo + seg; c += 32) {
       const int j = c + lane;
       const uint32_t u = j < hi ? keys[j] : 0u;
-      const bool is_gt = j < hi && u > T, is_eq = j < hi && u == T;
+      const bool is_gt = j < hi && (u > T || (need == 0 && u == T));
+      const bool is_eq = j < hi && need > 0 && u == T;
       const uint32_t bgt = __ballot_sync(0xffffffffu, is_gt);
       const uint32_t beq = __ballot_sync(0xffffffffu, is_eq);
       const uint64_t comp = ((uint64_t)u << 32) | (uint32_t)j;
@@ -271,12 +272,14 @@ __global__ void __launch_bounds__(kSelThreads)
     __syncthreads();
   };
 
+  int m = nv < topk ? nv : topk;  // candidates to sort
   if (nv <= topk) {
     load_all();
   } else {
     load_keys();
-    // ---- radix select of T, the topk-th largest key: 12 + 12 + 8 bits ----
+    // ---- radix select: 12 + 12 + 8 bits, usually only the first ----
     uint32_t prefix = 0, pmask = 0;
+    bool one_pass = false;
     need = topk;  // still to take among keys matching prefix
 #pragma unroll 1
     for (int pass = 0; pass < 3; ++pass) {
@@ -304,19 +307,36 @@ __global__ void __launch_bounds__(kSelThreads)
           if (run + c >= (uint32_t)need) {
             sh.sel_digit = (uint32_t)(o * per + i);
             sh.sel_above = run;
+            sh.sel_count = c;
             break;
           }
           run += c;
         }
       }
       __syncthreads();
-      need -= (int)sh.sel_above;
-      prefix |= sh.sel_digit << shift;
+      const uint32_t dsel = sh.sel_digit, dabove = sh.sel_above;
+      const uint32_t dcount = sh.sel_count;
+      if (pass == 0 && dabove + dcount <= (uint32_t)mcap) {
+        // keep every key whose top 12 bits reach the threshold bucket; the
+        // exact sort below settles the boundary (and its ties)
+        T = dsel << shift;
+        need = 0;
+        n_gt = (int)(dabove + dcount);
+        m = n_gt;
+        one_pass = true;
+        break;
+      }
+      need -= (int)dabove;
+      prefix |= dsel << shift;
       pmask |= dmask << shift;
       __syncthreads();
     }
-    T = prefix;
-    n_gt = topk - need;  // keys strictly above T, all kept
+    if (!one_pass) {
+      // full select ran: keep keys > T plus the `need` lowest-index ties
+      T = prefix;
+      n_gt = topk - need;
+      m = topk;
+    }
     compact();
   }
 
@@ -345,17 +365,17 @@ __global__ void __launch_bounds__(kSelThreads)
   }
   const uint32_t diff = all_and ^ all_or;  // block-uniform
 
-  // ---- stable LSD radix sort on the top 16 key bits, then a run fix-up
-  // on the low 16 bits; a full four-digit sort when runs are long ----
+  // ---- stable LSD radix sort on the top 24 key bits, then a run fix-up
+  // on the low 8 bits; a full four-digit sort when runs are long ----
   uint64_t *cur = bufA, *alt = bufB;
-  for (int shift = 16; shift < 32; shift += 8) {
+  for (int shift = 8; shift < 32; shift += 8) {
     if (((diff >> shift) & 255u) == 0u) continue;  // every digit equal
     lsd_pass<EPT>(cur, alt, m, shift, sh);
     uint64_t *t = cur;
     cur = alt;
     alt = t;
   }
-  if ((diff & 0xFFFFu) != 0u) {
+  if ((diff & 0xFFu) != 0u) {
     if (!run_fixup(cur, alt, m, sh)) {
       uint64_t *t = cur;
       cur = alt;
@@ -383,7 +403,7 @@ __global__ void __launch_bounds__(kSelThreads)
   int32_t *oi = out_idx + (size_t)row * topk;
   float *os = out_scores + (size_t)row * topk;
   for (int i = tid; i < topk; i += kSelThreads) {
-    if (i < m) {
+    if (i < m) {  // m >= topk or m = n_visible < topk
       const uint64_t c = cur[i];
       oi[i] = (int32_t)(uint32_t)c;
       os[i] = key_to_float((uint32_t)(c >> 32));
@@ -436,7 +456,9 @@ struct SelLayout {
 
 SelLayout sel_layout(int S_kv, int topk) {
   SelLayout l;
-  l.mcap = topk < S_kv ? topk : S_kv;
+  // room for the candidates of a one-pass select: topk plus the rest of
+  // the threshold bucket (up to kSelSlack keys)
+  l.mcap = topk + kSelSlack < S_kv ? topk + kSelSlack : S_kv;
   l.bcap = l.mcap > kHistBins / 2 ? l.mcap : kHistBins / 2;
   const size_t key_bytes = (size_t)S_kv * 4;
   const size_t whist_bytes = (size_t)kSelWarps * 256 * 4;
@@ -469,11 +491,13 @@ size_t topk_select_smem_bytes(int S_kv, int topk) {
 cudaError_t launch_topk_select(const Problem &p, const float *logits, int topk,
                                int32_t *out_idx, float *out_scores,
                                cudaStream_t st) {
-  const int m = topk < p.S_kv ? topk : p.S_kv;
-  if (m <= kSelThreads * 8)
+  const int mcap = sel_layout(p.S_kv, topk).mcap;
+  if (mcap <= kSelThreads * 8)
     return launch_sel<8>(p, logits, topk, out_idx, out_scores, st);
-  return launch_sel<DSA_SEL_MAX_EPT>(p, logits, topk, out_idx, out_scores,
-                                     st);
+  if (mcap <= kSelThreads * 16)
+    return launch_sel<16>(p, logits, topk, out_idx, out_scores, st);
+  return launch_sel<DSA_SEL_MAX_EPT + 2>(p, logits, topk, out_idx, out_scores,
+                                         st);
 }
 
 cudaError_t launch_gather_scores(const Problem &p, const float *logits,
