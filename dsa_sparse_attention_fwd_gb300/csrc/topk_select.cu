@@ -11,17 +11,18 @@
 //      bits, which spreads typical scores over many bins).  An ordered
 //      two-walk compaction then keeps every key > T and the lowest-index
 //      keys == T, in index order.
-//   2. A stable least-significant-digit radix sort (4-bit digits,
-//      descending) orders the candidates, packed as (key << 32 | j), on the
-//      top 24 key bits.  Each thread counts the digits of its own contiguous
-//      elements in a private counter column, so ranks follow element order
-//      and the sort is stable; stability keeps equal keys in index order,
-//      which is the "lower index first" tie rule.  Digit positions on which
-//      every candidate agrees (found by an AND/OR reduction) are skipped.
-//   3. Runs of equal top 24 bits (rare for real score distributions) are
-//      ordered by the low 8 bits by counting inside the run.  If any run is
-//      longer than 32 (heavily tied inputs), the candidates are rebuilt and
-//      sorted on all eight digits instead.
+//   2. A stable least-significant-digit radix sort (8-bit digits,
+//      descending) orders the m = min(n, topk) survivors, packed as
+//      (key << 32 | j), on the top 16 key bits only.  Within a warp, equal
+//      digits are ranked with eight ballots (one per digit bit), so the rank
+//      follows element order and the sort is stable; stability keeps equal
+//      keys in index order, which is the "lower index first" tie rule.
+//      Digit positions on which every survivor agrees (found by an AND/OR
+//      reduction) are skipped.
+//   3. Runs of equal top 16 bits (a few elements for real score
+//      distributions) are ordered by the low 16 bits by counting inside the
+//      run.  If any run is longer than 32 (heavily tied inputs), the
+//      candidates are rebuilt and sorted on all four digits instead.
 #include "common.cuh"
 
 namespace dsa {
@@ -48,9 +49,22 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
   return m;
 }
 
+// Lanes of this warp whose 8-bit digit equals mine (0 for invalid lanes).
+__device__ __forceinline__ uint32_t digit_peers(uint32_t d, bool valid) {
+  uint32_t m = __ballot_sync(0xffffffffu, valid);
+#pragma unroll
+  for (int b = 0; b < 8; ++b) {
+    const bool bit = (d >> b) & 1u;
+    const uint32_t bal = __ballot_sync(0xffffffffu, bit);
+    m &= bit ? bal : ~bal;
+  }
+  return valid ? m : 0u;
+}
+
 struct SelShared {
-  uint16_t *cnt16;                 // sort counters [16][256]; live in the
-                                   // row-key buffer, dead by then
+  uint32_t (*whist)[256];          // per-warp digit counts / offsets; lives
+                                   // in the row-key buffer, dead by then
+  uint32_t dbase[256];             // digit bases of a sort pass
   uint32_t wsum[kSelWarps];
   uint32_t wgt[kSelWarps], weq[kSelWarps];
   uint32_t wand[kSelWarps], wor[kSelWarps];
@@ -77,70 +91,58 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, SelShared &sh) {
   return pre + incl - v;
 }
 
-// Candidate buffers are padded with one u64 every 16 elements so that a
-// thread's contiguous run of elements does not collide on shared-memory
-// banks with its neighbours'.
-__host__ __device__ __forceinline__ int pad(int e) { return e + (e >> 4); }
-
-// One stable counting-sort pass of src[0..m) into dst on the 4-bit digit
-// (key >> shift) & 15, descending.  Thread t owns the contiguous elements
-// [ept*t, ept*t + ept), ept = ceil(m / 256) <= EPT, and counts its digits in its own column of
-// cnt[16][256] (u16), so a thread's rank for an element is simply how many
-// of its earlier elements had the same digit; an exclusive scan over cnt in
-// digit-major order then places threads (and so elements) in order, which
-// makes the pass stable.
+// One stable counting-sort pass of src[0..m) into dst on digit
+// (key >> shift) & 255, descending.
 template <int EPT>
 __device__ __forceinline__ void lsd_pass(const uint64_t *src, uint64_t *dst,
                                          int m, int shift, SelShared &sh) {
-  const int t = threadIdx.x;
-  const int ept = (m + kSelThreads - 1) / kSelThreads;
-  uint16_t *cnt = sh.cnt16;                       // [16][256]
-  uint32_t *cnt32 = reinterpret_cast<uint32_t *>(cnt);  // 2048 words
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int per_warp = ((m + kSelThreads - 1) / kSelThreads) * 32;
+  const int ept = per_warp / 32;
+  const int seg = warp * per_warp;
+  uint32_t *wh = sh.whist[warp];
+  const uint32_t lt = lanemask_lt();
+  for (int i = lane; i < 256; i += 32) wh[i] = 0;
+  __syncwarp();
+  uint32_t off[EPT];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) cnt32[8 * t + k] = 0u;
-  __syncthreads();
-  uint32_t local[(EPT + 1) / 2];  // per-element ranks, two u16 per word
-#pragma unroll
-  for (int i = 0; i < EPT; ++i) {
-    const int e = ept * t + i;
-    if (i < ept && e < m) {
-      const uint64_t v = src[pad(e)];
-      const uint32_t d = 15u - (uint32_t)((v >> (32 + shift)) & 15u);
-      const int a = (int)(d << 8) + t;
-      const uint32_t c = cnt[a];
-      if (i & 1)
-        local[i >> 1] |= c << 16;
-      else
-        local[i >> 1] = c;
-      cnt[a] = (uint16_t)(c + 1u);
+  for (int it = 0; it < EPT; ++it) {
+    if (it < ept) {
+      const int e = seg + it * 32 + lane;
+      const bool valid = e < m;
+      const uint64_t v = valid ? src[e] : 0ull;
+      const uint32_t d = 255u - (uint32_t)((v >> (32 + shift)) & 255u);
+      const uint32_t peers = digit_peers(d, valid);
+      const uint32_t rank = __popc(peers & lt);
+      const uint32_t base = valid ? wh[d] : 0u;
+      __syncwarp();
+      if (valid && rank == 0) wh[d] = base + __popc(peers);
+      __syncwarp();
+      off[it] = base + rank;
     }
   }
   __syncthreads();
-  // exclusive scan of the 4096 u16 counters in digit-major order: thread t
-  // rakes words [8t, 8t+8) (u16 entries [16t, 16t+16)); totals fit 16 bits
-  uint32_t w[8];
-  uint32_t run = 0;
+  {
+    const int d = threadIdx.x;  // 256 threads, one digit each
+    uint32_t run = 0;
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const uint32_t x = cnt32[8 * t + k];
-    const uint32_t lo = x & 0xFFFFu, hi = x >> 16;
-    w[k] = run | ((run + lo) << 16);
-    run += lo + hi;
+    for (int w = 0; w < kSelWarps; ++w) {
+      const uint32_t c = sh.whist[w][d];
+      sh.whist[w][d] = run;
+      run += c;
+    }
+    sh.dbase[d] = block_excl_scan(run, sh);
   }
-  const uint32_t excl = block_excl_scan(run, sh);
-  const uint32_t add = excl | (excl << 16);
-#pragma unroll
-  for (int k = 0; k < 8; ++k) cnt32[8 * t + k] = w[k] + add;
   __syncthreads();
 #pragma unroll
-  for (int i = 0; i < EPT; ++i) {
-    const int e = ept * t + i;
-    if (i < ept && e < m) {
-      const uint64_t v = src[pad(e)];
-      const uint32_t d = 15u - (uint32_t)((v >> (32 + shift)) & 15u);
-      const uint32_t rank = (local[i >> 1] >> ((i & 1) * 16)) & 0xFFFFu;
-      const uint32_t base = cnt[((int)d << 8) + t];
-      dst[pad((int)(base + rank))] = v;
+  for (int it = 0; it < EPT; ++it) {
+    if (it < ept) {
+      const int e = seg + it * 32 + lane;
+      if (e < m) {
+        const uint64_t v = src[e];
+        const uint32_t d = 255u - (uint32_t)((v >> (32 + shift)) & 255u);
+        dst[sh.dbase[d] + wh[d] + off[it]] = v;
+      }
     }
   }
   __syncthreads();
@@ -159,32 +161,32 @@ __device__ __forceinline__ bool run_fixup(const uint64_t *src, uint64_t *dst,
   __syncthreads();
   bool over = false;
   for (int i = threadIdx.x; i < m; i += kSelThreads) {
-    const uint64_t v = src[pad(i)];
+    const uint64_t v = src[i];
     const uint32_t top = (uint32_t)(v >> 40);
     const uint32_t low = (uint32_t)(v >> 32) & 0xFFu;
     int cnt = 0, r = i - 1, steps = 0;
     while (r >= 0 && steps < kRunLimit) {
-      const uint64_t u = src[pad(r)];
+      const uint64_t u = src[r];
       if ((uint32_t)(u >> 40) != top) break;
       cnt += (((uint32_t)(u >> 32) & 0xFFu) >= low);
       --r;
       ++steps;
     }
-    if (steps == kRunLimit && r >= 0 && (uint32_t)(src[pad(r)] >> 40) == top)
+    if (steps == kRunLimit && r >= 0 && (uint32_t)(src[r] >> 40) == top)
       over = true;
     const int start = r + 1;
     r = i + 1;
     steps = 0;
     while (r < m && steps < kRunLimit) {
-      const uint64_t u = src[pad(r)];
+      const uint64_t u = src[r];
       if ((uint32_t)(u >> 40) != top) break;
       cnt += (((uint32_t)(u >> 32) & 0xFFu) > low);
       ++r;
       ++steps;
     }
-    if (steps == kRunLimit && r < m && (uint32_t)(src[pad(r)] >> 40) == top)
+    if (steps == kRunLimit && r < m && (uint32_t)(src[r] >> 40) == top)
       over = true;
-    if (!over) dst[pad(start + cnt)] = v;
+    if (!over) dst[start + cnt] = v;
   }
   if (over) sh.overflow = 1;
   __syncthreads();
@@ -194,19 +196,20 @@ __device__ __forceinline__ bool run_fixup(const uint64_t *src, uint64_t *dst,
 }
 
 template <int EPT>
-__global__ void __launch_bounds__(kSelThreads, 4)
+__global__ void __launch_bounds__(kSelThreads)
     topk_select_kernel(const float *__restrict__ logits,
                        const int32_t *__restrict__ q_pos, int S, int S_kv,
-                       int ratio, int topk, int mcap, int pa, int pb,
+                       int ratio, int topk, int mcap, int bcap,
                        int32_t *__restrict__ out_idx,
                        float *__restrict__ out_scores) {
   extern __shared__ __align__(16) uint8_t smem[];
-  uint64_t *bufA = reinterpret_cast<uint64_t *>(smem);  // [pa] (padded)
-  uint64_t *bufB = bufA + pa;                            // [pb] (>= 4096 u32)
+  uint64_t *bufA = reinterpret_cast<uint64_t *>(smem);  // [mcap]
+  uint64_t *bufB = bufA + mcap;                          // [bcap] (>= 4096 u32)
   uint32_t *hist = reinterpret_cast<uint32_t *>(bufB);   // select histogram
-  uint32_t *keys = reinterpret_cast<uint32_t *>(bufB + pb);  // [S_kv]
+  uint32_t *keys = reinterpret_cast<uint32_t *>(bufB + bcap);  // [S_kv]
   __shared__ SelShared sh;
-  if (threadIdx.x == 0) sh.cnt16 = reinterpret_cast<uint16_t *>(keys);
+  if (threadIdx.x == 0)
+    sh.whist = reinterpret_cast<uint32_t(*)[256]>(keys);
 
   const int row = blockIdx.x;  // row id = b * S + s, the output order
   const int b = row / S, s = row % S;
@@ -225,7 +228,7 @@ __global__ void __launch_bounds__(kSelThreads, 4)
   };
   auto load_all = [&]() {
     for (int j = tid; j < nv; j += kSelThreads)
-      bufA[pad(j)] = ((uint64_t)ordered_key(__ldg(L + j)) << 32) | (uint32_t)j;
+      bufA[j] = ((uint64_t)ordered_key(__ldg(L + j)) << 32) | (uint32_t)j;
     __syncthreads();
   };
   // ordered compaction, two walks over contiguous warp segments
@@ -258,10 +261,10 @@ __global__ void __launch_bounds__(kSelThreads, 4)
       const uint32_t bgt = __ballot_sync(0xffffffffu, is_gt);
       const uint32_t beq = __ballot_sync(0xffffffffu, is_eq);
       const uint64_t comp = ((uint64_t)u << 32) | (uint32_t)j;
-      if (is_gt) bufA[pad(gpos + __popc(bgt & lt))] = comp;
+      if (is_gt) bufA[gpos + __popc(bgt & lt)] = comp;
       if (is_eq) {
         const uint32_t r = epos + __popc(beq & lt);
-        if (r < (uint32_t)need) bufA[pad(n_gt + (int)r)] = comp;
+        if (r < (uint32_t)need) bufA[n_gt + r] = comp;
       }
       gpos += __popc(bgt);
       epos += __popc(beq);
@@ -340,7 +343,7 @@ __global__ void __launch_bounds__(kSelThreads, 4)
   // ---- bits on which the survivors differ ----
   uint32_t kand = 0xffffffffu, kor = 0u;
   for (int i = tid; i < m; i += kSelThreads) {
-    const uint32_t k = (uint32_t)(bufA[pad(i)] >> 32);
+    const uint32_t k = (uint32_t)(bufA[i] >> 32);
     kand &= k;
     kor |= k;
   }
@@ -365,8 +368,8 @@ __global__ void __launch_bounds__(kSelThreads, 4)
   // ---- stable LSD radix sort on the top 24 key bits, then a run fix-up
   // on the low 8 bits; a full four-digit sort when runs are long ----
   uint64_t *cur = bufA, *alt = bufB;
-  for (int shift = 8; shift < 32; shift += 4) {
-    if (((diff >> shift) & 15u) == 0u) continue;  // every digit equal
+  for (int shift = 8; shift < 32; shift += 8) {
+    if (((diff >> shift) & 255u) == 0u) continue;  // every digit equal
     lsd_pass<EPT>(cur, alt, m, shift, sh);
     uint64_t *t = cur;
     cur = alt;
@@ -387,8 +390,8 @@ __global__ void __launch_bounds__(kSelThreads, 4)
       }
       cur = bufA;
       alt = bufB;
-      for (int shift = 0; shift < 32; shift += 4) {
-        if (((diff >> shift) & 15u) == 0u) continue;
+      for (int shift = 0; shift < 32; shift += 8) {
+        if (((diff >> shift) & 255u) == 0u) continue;
         lsd_pass<EPT>(cur, alt, m, shift, sh);
         uint64_t *t = cur;
         cur = alt;
@@ -401,7 +404,7 @@ __global__ void __launch_bounds__(kSelThreads, 4)
   float *os = out_scores + (size_t)row * topk;
   for (int i = tid; i < topk; i += kSelThreads) {
     if (i < m) {  // m >= topk or m = n_visible < topk
-      const uint64_t c = cur[pad(i)];
+      const uint64_t c = cur[i];
       oi[i] = (int32_t)(uint32_t)c;
       os[i] = key_to_float((uint32_t)(c >> 32));
     } else {
@@ -447,7 +450,7 @@ __global__ void fill_neg_inf_kernel(float *p, size_t n) {
 // [bcap] u64 (also the 4096-bin select histogram), keys [S_kv] u32 (at least
 // 8 KB: the sort's per-warp histograms reuse it once the keys are dead).
 struct SelLayout {
-  int mcap, bcap, pa, pb;
+  int mcap, bcap;
   size_t dyn;
 };
 
@@ -458,11 +461,9 @@ SelLayout sel_layout(int S_kv, int topk) {
   l.mcap = topk + kSelSlack < S_kv ? topk + kSelSlack : S_kv;
   l.bcap = l.mcap > kHistBins / 2 ? l.mcap : kHistBins / 2;
   const size_t key_bytes = (size_t)S_kv * 4;
-  const size_t cnt_bytes = (size_t)16 * 256 * 2;
-  l.pa = pad(l.mcap) + 16;  // padded capacity of bufA
-  l.pb = pad(l.bcap) + 16;  // of bufB
-  l.dyn = (size_t)(l.pa + l.pb) * 8 +
-          (key_bytes > cnt_bytes ? key_bytes : cnt_bytes);
+  const size_t whist_bytes = (size_t)kSelWarps * 256 * 4;
+  l.dyn = (size_t)(l.mcap + l.bcap) * 8 +
+          (key_bytes > whist_bytes ? key_bytes : whist_bytes);
   return l;
 }
 
@@ -476,8 +477,8 @@ cudaError_t launch_sel(const Problem &p, const float *logits, int topk,
   if (e != cudaSuccess) return e;
   const long long rows = (long long)p.B * p.S;
   kern<<<(unsigned)rows, kSelThreads, l.dyn, st>>>(
-      logits, p.q_pos, p.S, p.S_kv, p.ratio, topk, l.mcap, l.pa, l.pb,
-      out_idx, out_scores);
+      logits, p.q_pos, p.S, p.S_kv, p.ratio, topk, l.mcap, l.bcap, out_idx,
+      out_scores);
   return cudaGetLastError();
 }
 
