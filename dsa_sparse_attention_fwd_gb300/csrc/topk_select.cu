@@ -92,22 +92,23 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, SelShared &sh) {
 }
 
 // One stable counting-sort pass of src[0..m) into dst on digit
-// (key >> shift) & 255, descending.
-template <int EPT>
+// (key >> shift) & 255, descending.  Warp w ranks the contiguous elements
+// [32*E*w, 32*E*(w+1)); E is the smallest instantiated count that covers m,
+// so no iteration runs past the data (warps past the end skip the loops).
+template <int E>
 __device__ __forceinline__ void lsd_pass(const uint64_t *src, uint64_t *dst,
                                          int m, int shift, SelShared &sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int per_warp = ((m + kSelThreads - 1) / kSelThreads) * 32;
-  const int ept = per_warp / 32;
-  const int seg = warp * per_warp;
+  const int seg = warp * 32 * E;
+  const bool active = seg < m;  // warp-uniform
   uint32_t *wh = sh.whist[warp];
   const uint32_t lt = lanemask_lt();
   for (int i = lane; i < 256; i += 32) wh[i] = 0;
   __syncwarp();
-  uint32_t off[EPT];
+  uint32_t off[E];
+  if (active) {
 #pragma unroll
-  for (int it = 0; it < EPT; ++it) {
-    if (it < ept) {
+    for (int it = 0; it < E; ++it) {
       const int e = seg + it * 32 + lane;
       const bool valid = e < m;
       const uint64_t v = valid ? src[e] : 0ull;
@@ -134,9 +135,9 @@ __device__ __forceinline__ void lsd_pass(const uint64_t *src, uint64_t *dst,
     sh.dbase[d] = block_excl_scan(run, sh);
   }
   __syncthreads();
+  if (active) {
 #pragma unroll
-  for (int it = 0; it < EPT; ++it) {
-    if (it < ept) {
+    for (int it = 0; it < E; ++it) {
       const int e = seg + it * 32 + lane;
       if (e < m) {
         const uint64_t v = src[e];
@@ -146,6 +147,23 @@ __device__ __forceinline__ void lsd_pass(const uint64_t *src, uint64_t *dst,
     }
   }
   __syncthreads();
+}
+
+// Runs one pass with the smallest element count per lane that covers m
+// (at most EMAX, the kernel's instantiation limit).
+template <int EMAX>
+__device__ __forceinline__ void lsd_dispatch(const uint64_t *src,
+                                             uint64_t *dst, int m, int shift,
+                                             SelShared &sh) {
+  const int ept = (m + kSelThreads - 1) / kSelThreads;
+  if (ept <= 1) return lsd_pass<1>(src, dst, m, shift, sh);
+  if (ept <= 2) return lsd_pass<2>(src, dst, m, shift, sh);
+  if (ept <= 4) return lsd_pass<4>(src, dst, m, shift, sh);
+  if (EMAX <= 8 || ept <= 8) return lsd_pass<(EMAX < 8 ? EMAX : 8)>(src, dst, m, shift, sh);
+  if (EMAX <= 12 || ept <= 12) return lsd_pass<(EMAX < 12 ? EMAX : 12)>(src, dst, m, shift, sh);
+  if (EMAX <= 16 || ept <= 16) return lsd_pass<(EMAX < 16 ? EMAX : 16)>(src, dst, m, shift, sh);
+  if (EMAX <= 24 || ept <= 24) return lsd_pass<(EMAX < 24 ? EMAX : 24)>(src, dst, m, shift, sh);
+  return lsd_pass<EMAX>(src, dst, m, shift, sh);
 }
 
 // Fix-up after sorting on the top 24 key bits: inside each run of equal top
@@ -196,7 +214,7 @@ __device__ __forceinline__ bool run_fixup(const uint64_t *src, uint64_t *dst,
 }
 
 template <int EPT>
-__global__ void __launch_bounds__(kSelThreads)
+__global__ void __launch_bounds__(kSelThreads, 4)
     topk_select_kernel(const float *__restrict__ logits,
                        const int32_t *__restrict__ q_pos, int S, int S_kv,
                        int ratio, int topk, int mcap, int bcap,
@@ -370,7 +388,7 @@ __global__ void __launch_bounds__(kSelThreads)
   uint64_t *cur = bufA, *alt = bufB;
   for (int shift = 8; shift < 32; shift += 8) {
     if (((diff >> shift) & 255u) == 0u) continue;  // every digit equal
-    lsd_pass<EPT>(cur, alt, m, shift, sh);
+    lsd_dispatch<EPT>(cur, alt, m, shift, sh);
     uint64_t *t = cur;
     cur = alt;
     alt = t;
@@ -392,7 +410,7 @@ __global__ void __launch_bounds__(kSelThreads)
       alt = bufB;
       for (int shift = 0; shift < 32; shift += 8) {
         if (((diff >> shift) & 255u) == 0u) continue;
-        lsd_pass<EPT>(cur, alt, m, shift, sh);
+        lsd_dispatch<EPT>(cur, alt, m, shift, sh);
         uint64_t *t = cur;
         cur = alt;
         alt = t;
