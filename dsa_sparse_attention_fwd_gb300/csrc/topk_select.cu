@@ -61,6 +61,14 @@ __device__ __forceinline__ uint32_t digit_peers(uint32_t d, bool valid) {
   return valid ? m : 0u;
 }
 
+// The same mask from one match instruction (a different execution pipe
+// from the ballots, so alternating the two keeps both busy).
+__device__ __forceinline__ uint32_t digit_peers_match(uint32_t d, bool valid) {
+  const uint32_t key = valid ? d : 0x100u;  // invalid lanes group apart
+  const uint32_t m = __match_any_sync(0xffffffffu, key);
+  return valid ? m : 0u;
+}
+
 struct SelShared {
   uint32_t (*whist)[256];          // per-warp digit counts / offsets; lives
                                    // in the row-key buffer, dead by then
@@ -113,7 +121,8 @@ __device__ __forceinline__ void lsd_pass(const uint64_t *src, uint64_t *dst,
       const bool valid = e < m;
       const uint64_t v = valid ? src[e] : 0ull;
       const uint32_t d = 255u - (uint32_t)((v >> (32 + shift)) & 255u);
-      const uint32_t peers = digit_peers(d, valid);
+      const uint32_t peers = ((it + warp) & 1) ? digit_peers_match(d, valid)
+                                                : digit_peers(d, valid);
       const uint32_t rank = __popc(peers & lt);
       const uint32_t base = valid ? wh[d] : 0u;
       __syncwarp();
