@@ -90,8 +90,9 @@ bool aligned16(const void *p) {
 }
 
 // q [S, B, H, D] bf16 viewed as the 4-D tensor (d, h, b, s); one box is
-// 64 d x H heads x 1 sequence x 256/H queries = 256 rows of 128 bytes.
-int encode_q(CUtensorMap *m, const Problem &p) {
+// 64 d x H heads x 1 sequence x `queries` queries (256/H for the prefill
+// tile = 256 rows of 128 bytes; 1 for decode).
+int encode_q(CUtensorMap *m, const Problem &p, int queries) {
   auto fn = encode_fn();
   if (!fn) return DSA_ERR_CUDA;
   const cuuint64_t dims[4] = {(cuuint64_t)p.D, (cuuint64_t)p.H,
@@ -100,7 +101,7 @@ int encode_q(CUtensorMap *m, const Problem &p) {
                                  (cuuint64_t)p.H * p.D * 2,
                                  (cuuint64_t)p.B * p.H * p.D * 2};
   const cuuint32_t box[4] = {(cuuint32_t)dsa::kChunk, (cuuint32_t)p.H, 1,
-                             (cuuint32_t)(dsa::kTileCols / p.H)};
+                             (cuuint32_t)queries};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
                   const_cast<void *>(p.q), dims, strides, box, estr,
@@ -129,20 +130,31 @@ int encode_k(CUtensorMap *m, const Problem &p) {
   return r == CUDA_SUCCESS ? DSA_OK : DSA_ERR_UNSUPPORTED;
 }
 
+// Rows with fewer queries per sequence than one prefill tile packs (256/H)
+// go to the decode kernel, which splits each row over its keys instead.
+bool use_decode_path(const Problem &p, const DeviceInfo &dev) {
+  return p.S < dsa::kTileCols / p.H && dsa::decode_supported(p.H, p.D) &&
+         (size_t)dev.max_smem_optin >= dsa::decode_smem_bytes(p.H, p.D);
+}
+
 // Device checks + tensor maps + the scoring launch.
 int run_scores(const Problem &p, float *logits, int *status,
                const DeviceInfo &dev, cudaStream_t st) {
-  if ((size_t)dev.max_smem_optin < dsa::index_scores_smem_bytes(p.D))
+  const bool decode = use_decode_path(p, dev);
+  if (!decode &&
+      (size_t)dev.max_smem_optin < dsa::index_scores_smem_bytes(p.D))
     return DSA_ERR_UNSUPPORTED;
   CUtensorMap tm_q, tm_k;
-  int rc = encode_q(&tm_q, p);
+  int rc = encode_q(&tm_q, p, decode ? 1 : dsa::kTileCols / p.H);
   if (rc != DSA_OK) return rc;
   rc = encode_k(&tm_k, p);
   if (rc != DSA_OK) return rc;
-  return dsa::launch_index_scores(p, tm_q, tm_k, logits, status, dev.num_sms,
-                                  st) == cudaSuccess
-             ? DSA_OK
-             : DSA_ERR_CUDA;
+  const cudaError_t e =
+      decode ? dsa::launch_decode_scores(p, tm_q, tm_k, logits, status,
+                                         dev.num_sms, st)
+             : dsa::launch_index_scores(p, tm_q, tm_k, logits, status,
+                                        dev.num_sms, st);
+  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
 }  // namespace

@@ -43,6 +43,7 @@ constexpr int kTileKeys = 128;      // MMA M: compressed keys per tile
 constexpr int kTileCols = 256;      // MMA N: (query, head) columns per tile
 constexpr int kChunk = 64;          // bf16 per 128-byte swizzled row
 constexpr int kScoreThreads = 320;  // TMA warp, MMA warp, 8 epilogue warps
+constexpr int kDecChunkTiles = 2;   // decode: key tiles per work item
 
 // Top-k selection: a sort pass handles up to 256 threads x (this + 2)
 // elements, i.e. topk + 256 candidates with topk <= 256 * DSA_SEL_MAX_EPT
@@ -65,6 +66,14 @@ cudaError_t launch_gather_scores(const Problem &p, const float *logits,
                                  const int32_t *in_idx, int topk,
                                  int32_t *out_idx, float *out_scores,
                                  int *status, int num_sms, cudaStream_t st);
+
+// Decode scoring (one MMA column per head of a single query); returns
+// cudaErrorNotSupported when (H, D) has no decode instantiation.
+cudaError_t launch_decode_scores(const Problem &p, const CUtensorMap &tm_q,
+                                 const CUtensorMap &tm_k, float *logits,
+                                 int *status, int num_sms, cudaStream_t st);
+bool decode_supported(int H, int D);
+size_t decode_smem_bytes(int H, int D);
 
 cudaError_t launch_fill_masked(float *logits, size_t n, cudaStream_t st);
 

@@ -1,0 +1,320 @@
+// decode_scores: lightning-indexer scores for rows with few queries per
+// sequence (decode), split over the keys so that every SM streams its share
+// of k from HBM.
+//
+// A work item is (query row r = b*S + s, chunk of kDecChunkTiles x 128 keys).
+// One MMA tile is 128 keys (M) x H heads of the row's single query (N = H),
+// K = D, so no MMA column is padding.  The K ring (kDecStages x 128 keys) is
+// filled by TMA; the row's Q tile (H x D) is loaded once per item into one of
+// two buffers.  The fp32 accumulator sits in TMEM (lane = key, column =
+// head); each of the four epilogue warps owns 32 keys and reduces the
+// weighted ReLU over the heads in its own registers, then stores the visible
+// scores.  Items whose chunk starts past the row's last visible key are
+// skipped, so masked keys are never read.
+//
+// Warp roles (192 threads, one CTA per SM, persistent): warp 0 TMA producer,
+// warp 1 TMEM allocator and MMA issuer, warps 2..5 epilogue.
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr int kDecStages = 5;
+constexpr int kDecThreads = 192;
+
+template <int H, int KC>
+struct DecSmem {
+  static constexpr int kQBytes = KC * H * 128;           // one Q tile
+  static constexpr int kKBytes = KC * kTileKeys * 128;   // one K stage
+  static constexpr int kOffQ = 0;                        // 2 Q buffers
+  static constexpr int kOffK = kOffQ + 2 * kQBytes;
+  static constexpr int kOffW = kOffK + kDecStages * kKBytes;
+  static constexpr int kOffBar = kOffW + 2 * H * 4;      // 2 weight rows
+  // k_full[S], k_empty[S], q_full[2], q_empty[2], acc_full[2], acc_empty[2]
+  static constexpr int kNumBars = 2 * kDecStages + 8;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kBytes = kOffMisc + 16;
+  static constexpr int kAlloc = kBytes + 1024;
+};
+
+struct DecItem {
+  int row, b, s, tile0, ntiles;
+};
+
+// Item i covers chunk (i / rows) of row (i % rows): consecutive items are
+// different rows, so the long rows' chunks spread over all CTAs.
+__device__ __forceinline__ DecItem dec_item(int item, int rows, int S,
+                                            int S_kv, int ratio,
+                                            const int32_t *q_pos) {
+  DecItem it;
+  it.row = item % rows;
+  const int chunk = item / rows;
+  it.b = it.row / S;
+  it.s = it.row % S;
+  const int nv = n_visible(row_pos(q_pos, it.b, it.s), ratio, S_kv);
+  const int tiles = (nv + kTileKeys - 1) / kTileKeys;
+  it.tile0 = chunk * kDecChunkTiles;
+  const int left = tiles - it.tile0;
+  it.ntiles = left <= 0 ? 0 : (left < kDecChunkTiles ? left : kDecChunkTiles);
+  return it;
+}
+
+__device__ __forceinline__ int dec_item_for(int round, int n_items) {
+  const int G = gridDim.x, c = blockIdx.x;
+  const int idx = round * G + ((round & 1) ? (G - 1 - c) : c);
+  return idx < n_items ? idx : -1;
+}
+
+template <int H, int KC>
+__global__ void __launch_bounds__(kDecThreads, 1)
+    decode_scores_kernel(const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_k,
+                         const float *__restrict__ w,
+                         const int32_t *__restrict__ q_pos,
+                         float *__restrict__ logits, int S, int B, int S_kv,
+                         int ratio, int n_items, int *status) {
+  using L = DecSmem<H, KC>;
+  constexpr uint32_t kIdesc = idesc_bf16_f32(kTileKeys, H);
+  constexpr int kAccCols = H;  // TMEM columns per accumulator
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t *smem = smem_raw + (base - raw_addr);
+  const uint32_t sQ = base + L::kOffQ;
+  const uint32_t sK = base + L::kOffK;
+  float *sW = reinterpret_cast<float *>(smem + L::kOffW);  // [2][H]
+  const uint32_t bars = base + L::kOffBar;
+  auto k_full = [&](int i) { return bars + 8u * i; };
+  auto k_empty = [&](int i) { return bars + 8u * (kDecStages + i); };
+  auto q_full = [&](int i) { return bars + 8u * (2 * kDecStages + i); };
+  auto q_empty = [&](int i) { return bars + 8u * (2 * kDecStages + 2 + i); };
+  auto acc_full = [&](int i) { return bars + 8u * (2 * kDecStages + 4 + i); };
+  auto acc_empty = [&](int i) { return bars + 8u * (2 * kDecStages + 6 + i); };
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kOffMisc);
+  volatile int *abort_flag = reinterpret_cast<int *>(smem + L::kOffMisc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rows = B * S;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kDecStages; ++i) {
+      mbar_init(k_full(i), 1);
+      mbar_init(k_empty(i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(q_full(i), 1);
+      mbar_init(q_empty(i), 1);
+      mbar_init(acc_full(i), 1);
+      mbar_init(acc_empty(i), 4);  // one arrival per epilogue warp
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), 2 * kAccCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      uint32_t kst = 0, kph = 0, nq = 0;
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const int item = dec_item_for(r, n_items);
+        if (item < 0) break;
+        const DecItem it = dec_item(item, rows, S, S_kv, ratio, q_pos);
+        if (it.ntiles == 0) continue;
+        const int qs = nq & 1;
+        const uint32_t qph = (nq >> 1) & 1u;
+        ++nq;
+        if (!(ok = wait_bar(q_empty(qs), qph ^ 1u, abort_flag, status))) break;
+        mbar_arrive_expect_tx(q_full(qs), L::kQBytes);
+        for (int c = 0; c < KC; ++c)
+          tma_load_4d(sQ + qs * L::kQBytes + c * (H * 128), &tm_q, q_full(qs),
+                      c * kChunk, 0, it.b, it.s);
+        for (int t = 0; t < it.ntiles; ++t) {
+          if (!(ok = wait_bar(k_empty(kst), kph ^ 1u, abort_flag, status)))
+            break;
+          mbar_arrive_expect_tx(k_full(kst), L::kKBytes);
+          for (int c = 0; c < KC; ++c)
+            tma_load_3d(sK + kst * L::kKBytes + c * (kTileKeys * 128), &tm_k,
+                        k_full(kst), c * kChunk, it.b,
+                        (it.tile0 + t) * kTileKeys);
+          if (++kst == kDecStages) {
+            kst = 0;
+            kph ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      uint32_t kst = 0, kph = 0, nq = 0, acc = 0, aph = 0;
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const int item = dec_item_for(r, n_items);
+        if (item < 0) break;
+        const DecItem it = dec_item(item, rows, S, S_kv, ratio, q_pos);
+        if (it.ntiles == 0) continue;
+        const int qs = nq & 1;
+        const uint32_t qph = (nq >> 1) & 1u;
+        ++nq;
+        if (!(ok = wait_bar(q_full(qs), qph, abort_flag, status))) break;
+        const uint32_t sQi = sQ + qs * L::kQBytes;
+        for (int t = 0; t < it.ntiles; ++t) {
+          if (!(ok = wait_bar(acc_empty(acc), aph ^ 1u, abort_flag, status)))
+            break;
+          if (!(ok = wait_bar(k_full(kst), kph, abort_flag, status))) break;
+          tc_fence_after();
+          const uint32_t d_tmem = tmem + acc * kAccCols;
+#pragma unroll
+          for (int c = 0; c < KC; ++c) {
+#pragma unroll
+            for (int kk = 0; kk < kChunk / 16; ++kk) {
+              const uint64_t ad = sdesc_k_sw128(
+                  sK + kst * L::kKBytes + c * (kTileKeys * 128) + kk * 32);
+              const uint64_t bd = sdesc_k_sw128(sQi + c * (H * 128) + kk * 32);
+              mma_bf16(d_tmem, ad, bd, kIdesc, (c | kk) != 0);
+            }
+          }
+          mma_commit(k_empty(kst));
+          mma_commit(acc_full(acc));
+          if (t == it.ntiles - 1) mma_commit(q_empty(qs));
+          if (++kst == kDecStages) {
+            kst = 0;
+            kph ^= 1u;
+          }
+          acc ^= 1u;
+          if (acc == 0) aph ^= 1u;
+        }
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int sp = warp & 3;            // TMEM sub-partition of this warp
+    const int et = threadIdx.x - 64;    // 0..127
+    uint32_t acc = 0, aph = 0, nw = 0;
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+      const int item = dec_item_for(r, n_items);
+      if (item < 0) break;
+      const DecItem it = dec_item(item, rows, S, S_kv, ratio, q_pos);
+      if (it.ntiles == 0) continue;
+      // weights of this row into one of two buffers (the other may still be
+      // read by a slower epilogue warp finishing the previous item)
+      float *wq = sW + (nw & 1) * H;
+      ++nw;
+      named_bar_sync(1, 128);
+      for (int h = et; h < H; h += 128)
+        wq[h] = __ldg(w + ((size_t)it.s * B + it.b) * H + h);
+      named_bar_sync(1, 128);
+      const long long pos = row_pos(q_pos, it.b, it.s);
+      float *out = logits + (size_t)it.row * S_kv;
+      for (int t = 0; t < it.ntiles; ++t) {
+        bool got = wait_bar(acc_full(acc), aph, abort_flag, status);
+        got = __all_sync(0xffffffffu, got);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr =
+            tmem + ((uint32_t)(sp * 32) << 16) + acc * kAccCols;
+        uint32_t v[H / 32][32];
+#pragma unroll
+        for (int c = 0; c < H / 32; ++c) tmem_ld32(taddr + c * 32, v[c]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < H / 32; ++c) reg_fence32(v[c]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acc_empty(acc));
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int h = 0; h < H; h += 2) {
+          s0 = fmaf(wq[h], fmaxf(__uint_as_float(v[h >> 5][h & 31]), 0.f), s0);
+          s1 = fmaf(wq[h + 1],
+                    fmaxf(__uint_as_float(v[(h + 1) >> 5][(h + 1) & 31]), 0.f),
+                    s1);
+        }
+        const int j = (it.tile0 + t) * kTileKeys + sp * 32 + lane;
+        if ((long long)(j + 1) * ratio - 1 <= pos && j < S_kv) out[j] = s0 + s1;
+        acc ^= 1u;
+        if (acc == 0) aph ^= 1u;
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 2 * kAccCols);
+  }
+}
+
+template <int H, int KC>
+cudaError_t launch_dec(const Problem &p, const CUtensorMap &tm_q,
+                       const CUtensorMap &tm_k, float *logits, int *status,
+                       int num_sms, cudaStream_t st) {
+  auto kern = decode_scores_kernel<H, KC>;
+  const int smem = DecSmem<H, KC>::kAlloc;
+  cudaError_t e = cudaFuncSetAttribute(
+      kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int rows = p.B * p.S;
+  const int tiles = (p.S_kv + kTileKeys - 1) / kTileKeys;
+  const int chunks = (tiles + kDecChunkTiles - 1) / kDecChunkTiles;
+  const long long n_items = (long long)rows * chunks;
+  if (n_items <= 0) return cudaSuccess;
+  if (n_items > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const int grid = (int)(n_items < num_sms ? n_items : num_sms);
+  kern<<<grid, kDecThreads, smem, st>>>(tm_q, tm_k, p.w, p.q_pos, logits,
+                                        p.S, p.B, p.S_kv, p.ratio,
+                                        (int)n_items, status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool decode_supported(int H, int D) {
+  return (H == 32 || H == 64 || H == 128) && D <= 2 * kChunk;
+}
+
+size_t decode_smem_bytes(int H, int D) {
+  const int kc = D <= kChunk ? 1 : 2;
+  if (H == 32) return kc == 1 ? DecSmem<32, 1>::kAlloc : DecSmem<32, 2>::kAlloc;
+  if (H == 64) return kc == 1 ? DecSmem<64, 1>::kAlloc : DecSmem<64, 2>::kAlloc;
+  return kc == 1 ? DecSmem<128, 1>::kAlloc : DecSmem<128, 2>::kAlloc;
+}
+
+cudaError_t launch_decode_scores(const Problem &p, const CUtensorMap &tm_q,
+                                 const CUtensorMap &tm_k, float *logits,
+                                 int *status, int num_sms, cudaStream_t st) {
+  const bool k1 = p.D <= kChunk;
+  switch (p.H) {
+    case 32:
+      return k1 ? launch_dec<32, 1>(p, tm_q, tm_k, logits, status, num_sms, st)
+                : launch_dec<32, 2>(p, tm_q, tm_k, logits, status, num_sms, st);
+    case 64:
+      return k1 ? launch_dec<64, 1>(p, tm_q, tm_k, logits, status, num_sms, st)
+                : launch_dec<64, 2>(p, tm_q, tm_k, logits, status, num_sms, st);
+    case 128:
+      return k1 ? launch_dec<128, 1>(p, tm_q, tm_k, logits, status, num_sms, st)
+                : launch_dec<128, 2>(p, tm_q, tm_k, logits, status, num_sms, st);
+    default:
+      return cudaErrorNotSupported;
+  }
+}
+
+}  // namespace dsa

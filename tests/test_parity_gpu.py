@@ -277,3 +277,39 @@ def test_wait_limit_reports_timeout(dsa):
     assert dsa.dsa_selftest_wait_limit(2000, ws) == 0
     assert dsa.dsa_indexer_check(ws) == 5  # DSA_ERR_DEVICE_TIMEOUT
     assert dsa.dsa_indexer_check(ws) == 0  # read-and-clear
+
+
+@pytest.mark.parametrize("S,B,H,D,S_kv,ratio,topk", [
+    (1, 5, 64, 128, 700, 4, 64),
+    (3, 4, 32, 64, 300, 2, 40),
+    (1, 3, 128, 128, 257, 1, 100),
+    (2, 2, 64, 72, 130, 3, 16),
+    (1, 8, 64, 128, 4096, 4, 512),
+])
+def test_decode_path_match_oracle(dsa, S, B, H, D, S_kv, ratio, topk):
+    """Shapes with fewer queries per sequence than a prefill tile packs run
+    the split-over-keys decode kernel; positions include rows that see no key,
+    a partial key tile and more than every key."""
+    wl = Workload("t", B=B, S=S, S_kv=S_kv, H=H, D=D, compress_ratio=ratio,
+                  topk=topk, w_scale=H ** -0.5, seed=S_kv + B + H)
+    q, k, w, _ = make_inputs(wl)
+    rng = np.random.default_rng(S_kv)
+    pos = rng.integers(0, S_kv * ratio + 40, size=B)
+    pos[0] = 0
+    pos = torch.from_numpy(pos.astype(np.int32))
+    sc, idx, st = gpu_run(dsa, q, k, w, ratio, topk, q_pos=pos)
+    assert st == 0
+    sc = sc.reshape(B, S, topk)
+    idx = idx.reshape(B, S, topk)
+    check_invariants(sc, idx, row_nvis(S, B, ratio, S_kv, pos), topk)
+    ref = oracle.indexer_fwd(q, k, w, ratio, topk, q_pos=pos,
+                             want_logits=True)
+    compare_rows(sc, idx, ref, np.arange(B * S), S)
+    logits = dsa.indexer_logits(q.cuda(), k.cuda(), w.cuda(), ratio,
+                                q_pos=pos.cuda())
+    torch.cuda.synchronize()
+    L = logits.cpu().numpy().reshape(B * S, S_kv)
+    R = ref["logits"]
+    assert np.array_equal(np.isneginf(L), np.isneginf(R))
+    fin = np.isfinite(R)
+    assert np.all(np.abs(L[fin] - R[fin]) <= score_tol(R[fin]))
