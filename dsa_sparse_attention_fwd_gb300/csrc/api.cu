@@ -132,14 +132,25 @@ int encode_k(CUtensorMap *m, const Problem &p) {
 
 // Rows with fewer queries per sequence than one prefill tile packs (256/H)
 // go to the decode kernel, which splits each row over its keys instead.
+bool decode_shape(int S, int H, int D) {
+  return S < dsa::kTileCols / H && dsa::decode_supported(H, D);
+}
+
 bool use_decode_path(const Problem &p, const DeviceInfo &dev) {
-  return p.S < dsa::kTileCols / p.H && dsa::decode_supported(p.H, p.D) &&
+  return decode_shape(p.S, p.H, p.D) && aligned16(p.w) &&
          (size_t)dev.max_smem_optin >= dsa::decode_smem_bytes(p.H, p.D);
 }
 
+// Bytes of the per-row key histograms the decode path adds to the workspace.
+size_t row_hist_bytes(int S, int B, int H, int D) {
+  return decode_shape(S, H, D)
+             ? (size_t)B * S * dsa::kRowHistBins * sizeof(uint32_t)
+             : 0;
+}
+
 // Device checks + tensor maps + the scoring launch.
-int run_scores(const Problem &p, float *logits, int *status,
-               const DeviceInfo &dev, cudaStream_t st) {
+int run_scores(const Problem &p, float *logits, uint32_t *row_hist,
+               int *status, const DeviceInfo &dev, cudaStream_t st) {
   const bool decode = use_decode_path(p, dev);
   if (!decode &&
       (size_t)dev.max_smem_optin < dsa::index_scores_smem_bytes(p.D))
@@ -150,8 +161,8 @@ int run_scores(const Problem &p, float *logits, int *status,
   rc = encode_k(&tm_k, p);
   if (rc != DSA_OK) return rc;
   const cudaError_t e =
-      decode ? dsa::launch_decode_scores(p, tm_q, tm_k, logits, status,
-                                         dev.num_sms, st)
+      decode ? dsa::launch_decode_scores(p, tm_q, tm_k, logits, row_hist,
+                                         status, dev.num_sms, st)
              : dsa::launch_index_scores(p, tm_q, tm_k, logits, status,
                                         dev.num_sms, st);
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
@@ -180,7 +191,7 @@ size_t dsa_indexer_workspace_size(int S, int B, int H, int D, int S_kv,
   (void)has_in_idx;
   if (check_shape(S, B, H, D, S_kv, compress_ratio) != DSA_OK) return 0;
   if (topk <= 0 || topk > DSA_MAX_TOPK) return 0;
-  return kHeaderBytes + logits_bytes(S, B, S_kv);
+  return kHeaderBytes + logits_bytes(S, B, S_kv) + row_hist_bytes(S, B, H, D);
 }
 
 size_t dsa_indexer_logits_workspace_size(void) { return kHeaderBytes; }
@@ -227,10 +238,21 @@ int dsa_indexer_fwd_profiled(const void *q, const void *k, const float *w,
                : cudaSuccess;
   };
 
+  // per-row key histograms (decode path, top-k only): filled by the scoring
+  // kernel, read by the selection
+  uint32_t *row_hist = nullptr;
+  if (!in_idx && use_decode_path(p, dev))
+    row_hist = reinterpret_cast<uint32_t *>(
+        static_cast<char *>(workspace) + kHeaderBytes +
+        logits_bytes(S, B, S_kv));
   if (cudaMemsetAsync(status, 0, kHeaderBytes, st) != cudaSuccess)
     return DSA_ERR_CUDA;
+  if (row_hist &&
+      cudaMemsetAsync(row_hist, 0, row_hist_bytes(S, B, H, D), st) !=
+          cudaSuccess)
+    return DSA_ERR_CUDA;
   if (mark(0) != cudaSuccess) return DSA_ERR_CUDA;
-  rc = run_scores(p, logits, status, dev, st);
+  rc = run_scores(p, logits, row_hist, status, dev, st);
   if (rc != DSA_OK) return rc;
   if (mark(1) != cudaSuccess) return DSA_ERR_CUDA;
   cudaError_t e;
@@ -238,7 +260,8 @@ int dsa_indexer_fwd_profiled(const void *q, const void *k, const float *w,
     e = dsa::launch_gather_scores(p, logits, in_idx, topk, out_idx, out_scores,
                                   status, dev.num_sms, st);
   else
-    e = dsa::launch_topk_select(p, logits, topk, out_idx, out_scores, st);
+    e = dsa::launch_topk_select(p, logits, topk, row_hist, out_idx,
+                                out_scores, st);
   if (e != cudaSuccess) return DSA_ERR_CUDA;
   if (mark(2) != cudaSuccess) return DSA_ERR_CUDA;
   return DSA_OK;
@@ -275,7 +298,7 @@ int dsa_indexer_logits(const void *q, const void *k, const float *w, int S,
   if (dsa::launch_fill_masked(logits, logits_bytes(S, B, S_kv) / 4, st) !=
       cudaSuccess)
     return DSA_ERR_CUDA;
-  return run_scores(p, logits, status, dev, st);
+  return run_scores(p, logits, nullptr, status, dev, st);
 }
 
 int dsa_indexer_check(void *workspace, void *cuda_stream) {

@@ -38,6 +38,23 @@ __host__ __device__ __forceinline__ int n_visible(long long pos, int ratio,
   return n < (long long)S_kv ? (int)n : S_kv;
 }
 
+// Order-preserving unsigned key of an fp32 score (larger float <-> larger
+// key; -0.0 folded onto +0.0 so the index tie-break decides between them).
+__device__ __forceinline__ uint32_t ordered_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_to_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Per-row histogram of the top 12 key bits, built by the decode scoring
+// kernel and read by the selection (bins per row).
+constexpr int kRowHistBins = 4096;
+constexpr int kRowHistShift = 20;
+
 // Scoring kernel tile geometry.
 constexpr int kTileKeys = 128;      // MMA M: compressed keys per tile
 constexpr int kTileCols = 256;      // MMA N: (query, head) columns per tile
@@ -57,9 +74,11 @@ cudaError_t launch_index_scores(const Problem &p, const CUtensorMap &tm_q,
                                 int *status, int num_sms, cudaStream_t st);
 size_t index_scores_smem_bytes(int D);
 
+// row_hist: per-row top-12-bit key histograms from the decode scoring
+// kernel, or nullptr (the selection then builds its own).
 cudaError_t launch_topk_select(const Problem &p, const float *logits, int topk,
-                               int32_t *out_idx, float *out_scores,
-                               cudaStream_t st);
+                               const uint32_t *row_hist, int32_t *out_idx,
+                               float *out_scores, cudaStream_t st);
 size_t topk_select_smem_bytes(int S_kv, int topk);
 
 cudaError_t launch_gather_scores(const Problem &p, const float *logits,
@@ -71,7 +90,8 @@ cudaError_t launch_gather_scores(const Problem &p, const float *logits,
 // cudaErrorNotSupported when (H, D) has no decode instantiation.
 cudaError_t launch_decode_scores(const Problem &p, const CUtensorMap &tm_q,
                                  const CUtensorMap &tm_k, float *logits,
-                                 int *status, int num_sms, cudaStream_t st);
+                                 uint32_t *row_hist, int *status, int num_sms,
+                                 cudaStream_t st);
 bool decode_supported(int H, int D);
 size_t decode_smem_bytes(int H, int D);
 

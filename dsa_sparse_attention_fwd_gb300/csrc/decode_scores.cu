@@ -31,6 +31,7 @@ struct DecSmem {
   static constexpr int kOffK = kOffQ + 2 * kQBytes;
   static constexpr int kOffW = kOffK + kDecStages * kKBytes;
   static constexpr int kOffBar = kOffW + 2 * H * 4;      // 2 weight rows
+  static constexpr int kWBytes = H * 4;                  // one weight row
   // k_full[S], k_empty[S], q_full[2], q_empty[2], acc_full[2], acc_empty[2]
   static constexpr int kNumBars = 2 * kDecStages + 8;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
@@ -72,8 +73,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                          const __grid_constant__ CUtensorMap tm_k,
                          const float *__restrict__ w,
                          const int32_t *__restrict__ q_pos,
-                         float *__restrict__ logits, int S, int B, int S_kv,
-                         int ratio, int n_items, int *status) {
+                         float *__restrict__ logits,
+                         uint32_t *__restrict__ row_hist, int S, int B,
+                         int S_kv, int ratio, int n_items, int *status) {
   using L = DecSmem<H, KC>;
   constexpr uint32_t kIdesc = idesc_bf16_f32(kTileKeys, H);
   constexpr int kAccCols = H;  // TMEM columns per accumulator
@@ -105,7 +107,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(q_full(i), 1);
-      mbar_init(q_empty(i), 1);
+      mbar_init(q_empty(i), 5);  // the MMA issuer + four epilogue warps
       mbar_init(acc_full(i), 1);
       mbar_init(acc_empty(i), 4);  // one arrival per epilogue warp
     }
@@ -137,10 +139,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         const uint32_t qph = (nq >> 1) & 1u;
         ++nq;
         if (!(ok = wait_bar(q_empty(qs), qph ^ 1u, abort_flag, status))) break;
-        mbar_arrive_expect_tx(q_full(qs), L::kQBytes);
+        mbar_arrive_expect_tx(q_full(qs), L::kQBytes + L::kWBytes);
         for (int c = 0; c < KC; ++c)
           tma_load_4d(sQ + qs * L::kQBytes + c * (H * 128), &tm_q, q_full(qs),
                       c * kChunk, 0, it.b, it.s);
+        bulk_load(smem_u32(sW) + qs * L::kWBytes,
+                  w + ((size_t)it.s * B + it.b) * H, L::kWBytes, q_full(qs));
         for (int t = 0; t < it.ntiles; ++t) {
           if (!(ok = wait_bar(k_empty(kst), kph ^ 1u, abort_flag, status)))
             break;
@@ -202,22 +206,20 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
     const int sp = warp & 3;            // TMEM sub-partition of this warp
-    const int et = threadIdx.x - 64;    // 0..127
-    uint32_t acc = 0, aph = 0, nw = 0;
+    uint32_t acc = 0, aph = 0, nq = 0;
     bool ok = true;
     for (int r = 0; ok; ++r) {
       const int item = dec_item_for(r, n_items);
       if (item < 0) break;
       const DecItem it = dec_item(item, rows, S, S_kv, ratio, q_pos);
       if (it.ntiles == 0) continue;
-      // weights of this row into one of two buffers (the other may still be
-      // read by a slower epilogue warp finishing the previous item)
-      float *wq = sW + (nw & 1) * H;
-      ++nw;
-      named_bar_sync(1, 128);
-      for (int h = et; h < H; h += 128)
-        wq[h] = __ldg(w + ((size_t)it.s * B + it.b) * H + h);
-      named_bar_sync(1, 128);
+      // the row's weights arrive with its Q tile (same slot, same barrier)
+      const int qs = nq & 1;
+      const uint32_t qph = (nq >> 1) & 1u;
+      ++nq;
+      bool wok = wait_bar(q_full(qs), qph, abort_flag, status);
+      if (!__all_sync(0xffffffffu, wok)) break;
+      const float *wq = sW + qs * H;
       const long long pos = row_pos(q_pos, it.b, it.s);
       float *out = logits + (size_t)it.row * S_kv;
       for (int t = 0; t < it.ntiles; ++t) {
@@ -248,10 +250,19 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                     s1);
         }
         const int j = (it.tile0 + t) * kTileKeys + sp * 32 + lane;
-        if ((long long)(j + 1) * ratio - 1 <= pos && j < S_kv) out[j] = s0 + s1;
+        if ((long long)(j + 1) * ratio - 1 <= pos && j < S_kv) {
+          const float sc = s0 + s1;
+          out[j] = sc;
+          if (row_hist)
+            atomicAdd(row_hist + (size_t)it.row * kRowHistBins +
+                          (ordered_key(sc) >> kRowHistShift),
+                      1u);
+        }
         acc ^= 1u;
         if (acc == 0) aph ^= 1u;
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_empty(qs));  // done with this Q/w slot
     }
   }
 
@@ -265,8 +276,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 
 template <int H, int KC>
 cudaError_t launch_dec(const Problem &p, const CUtensorMap &tm_q,
-                       const CUtensorMap &tm_k, float *logits, int *status,
-                       int num_sms, cudaStream_t st) {
+                       const CUtensorMap &tm_k, float *logits,
+                       uint32_t *row_hist, int *status, int num_sms,
+                       cudaStream_t st) {
   auto kern = decode_scores_kernel<H, KC>;
   const int smem = DecSmem<H, KC>::kAlloc;
   cudaError_t e = cudaFuncSetAttribute(
@@ -280,7 +292,7 @@ cudaError_t launch_dec(const Problem &p, const CUtensorMap &tm_q,
   if (n_items > 0x7fffffffLL) return cudaErrorInvalidValue;
   const int grid = (int)(n_items < num_sms ? n_items : num_sms);
   kern<<<grid, kDecThreads, smem, st>>>(tm_q, tm_k, p.w, p.q_pos, logits,
-                                        p.S, p.B, p.S_kv, p.ratio,
+                                        row_hist, p.S, p.B, p.S_kv, p.ratio,
                                         (int)n_items, status);
   return cudaGetLastError();
 }
@@ -300,18 +312,19 @@ size_t decode_smem_bytes(int H, int D) {
 
 cudaError_t launch_decode_scores(const Problem &p, const CUtensorMap &tm_q,
                                  const CUtensorMap &tm_k, float *logits,
-                                 int *status, int num_sms, cudaStream_t st) {
+                                 uint32_t *row_hist, int *status, int num_sms,
+                                 cudaStream_t st) {
   const bool k1 = p.D <= kChunk;
   switch (p.H) {
     case 32:
-      return k1 ? launch_dec<32, 1>(p, tm_q, tm_k, logits, status, num_sms, st)
-                : launch_dec<32, 2>(p, tm_q, tm_k, logits, status, num_sms, st);
+      return k1 ? launch_dec<32, 1>(p, tm_q, tm_k, logits, row_hist, status, num_sms, st)
+                : launch_dec<32, 2>(p, tm_q, tm_k, logits, row_hist, status, num_sms, st);
     case 64:
-      return k1 ? launch_dec<64, 1>(p, tm_q, tm_k, logits, status, num_sms, st)
-                : launch_dec<64, 2>(p, tm_q, tm_k, logits, status, num_sms, st);
+      return k1 ? launch_dec<64, 1>(p, tm_q, tm_k, logits, row_hist, status, num_sms, st)
+                : launch_dec<64, 2>(p, tm_q, tm_k, logits, row_hist, status, num_sms, st);
     case 128:
-      return k1 ? launch_dec<128, 1>(p, tm_q, tm_k, logits, status, num_sms, st)
-                : launch_dec<128, 2>(p, tm_q, tm_k, logits, status, num_sms, st);
+      return k1 ? launch_dec<128, 1>(p, tm_q, tm_k, logits, row_hist, status, num_sms, st)
+                : launch_dec<128, 2>(p, tm_q, tm_k, logits, row_hist, status, num_sms, st);
     default:
       return cudaErrorNotSupported;
   }

@@ -33,16 +33,6 @@ constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kHistBins = 4096;  // 12-bit select digit
 constexpr int kSelSlack = 256;   // extra candidates a one-pass select keeps
 
-__device__ __forceinline__ uint32_t ordered_key(float f) {
-  uint32_t u = __float_as_uint(f);
-  if (u == 0x80000000u) u = 0u;  // -0.0 -> +0.0
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-__device__ __forceinline__ float key_to_float(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
-}
-
 __device__ __forceinline__ uint32_t lanemask_lt() {
   uint32_t m;
   asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
@@ -225,6 +215,7 @@ __device__ __forceinline__ bool run_fixup(const uint64_t *src, uint64_t *dst,
 template <int EPT>
 __global__ void __launch_bounds__(kSelThreads, 4)
     topk_select_kernel(const float *__restrict__ logits,
+                       const uint32_t *__restrict__ row_hist,
                        const int32_t *__restrict__ q_pos, int S, int S_kv,
                        int ratio, int topk, int mcap, int bcap,
                        int32_t *__restrict__ out_idx,
@@ -249,6 +240,10 @@ __global__ void __launch_bounds__(kSelThreads, 4)
   // "above T" and "equal to T" groups), into bufA
   uint32_t T = 0;
   int need = 0, n_gt = 0;
+  bool keys_global = false;  // compact from the logits instead of keys[]
+  auto key_at = [&](int j) -> uint32_t {
+    return keys_global ? ordered_key(__ldg(L + j)) : keys[j];
+  };
   auto load_keys = [&]() {
     for (int j = tid; j < nv; j += kSelThreads)
       keys[j] = ordered_key(__ldg(L + j));
@@ -266,7 +261,7 @@ __global__ void __launch_bounds__(kSelThreads, 4)
     uint32_t cgt = 0, ceq = 0;
     for (int c = lo; c < lo + seg; c += 32) {
       const int j = c + lane;
-      const uint32_t u = j < hi ? keys[j] : 0u;
+      const uint32_t u = j < hi ? key_at(j) : 0u;
       cgt += __popc(__ballot_sync(0xffffffffu, j < hi && (u > T || (need == 0 && u == T))));
       ceq += __popc(__ballot_sync(0xffffffffu, j < hi && need > 0 && u == T));
     }
@@ -282,7 +277,7 @@ __global__ void __launch_bounds__(kSelThreads, 4)
     }
     for (int c = lo; c < lo + seg; c += 32) {
       const int j = c + lane;
-      const uint32_t u = j < hi ? keys[j] : 0u;
+      const uint32_t u = j < hi ? key_at(j) : 0u;
       const bool is_gt = j < hi && (u > T || (need == 0 && u == T));
       const bool is_eq = j < hi && need > 0 && u == T;
       const uint32_t bgt = __ballot_sync(0xffffffffu, is_gt);
@@ -300,9 +295,51 @@ __global__ void __launch_bounds__(kSelThreads, 4)
   };
 
   int m = nv < topk ? nv : topk;  // candidates to sort
+  bool done = false;
   if (nv <= topk) {
     load_all();
-  } else {
+    done = true;
+  } else if (row_hist) {
+    // the scoring kernel already counted this row's top 12 key bits: find
+    // the threshold bucket there and compact straight from the logits
+    const uint32_t *gh = row_hist + (size_t)row * kRowHistBins;
+    constexpr int per = kRowHistBins / kSelThreads;
+    const int o = kSelThreads - 1 - tid;
+    uint32_t c[per];
+    uint32_t lsum = 0;
+#pragma unroll
+    for (int i = 0; i < per; ++i) {
+      c[i] = __ldg(gh + o * per + i);
+      lsum += c[i];
+    }
+    const uint32_t above = block_excl_scan(lsum, sh);
+    if (above < (uint32_t)topk && (uint32_t)topk <= above + lsum) {
+      uint32_t run = above;
+      for (int i = per - 1; i >= 0; --i) {
+        if (run + c[i] >= (uint32_t)topk) {
+          sh.sel_digit = (uint32_t)(o * per + i);
+          sh.sel_above = run;
+          sh.sel_count = c[i];
+          break;
+        }
+        run += c[i];
+      }
+    }
+    __syncthreads();
+    const uint32_t dsel = sh.sel_digit, dabove = sh.sel_above;
+    const uint32_t dcount = sh.sel_count;
+    __syncthreads();
+    if (dabove + dcount <= (uint32_t)mcap) {
+      T = dsel << kRowHistShift;
+      need = 0;
+      n_gt = (int)(dabove + dcount);
+      m = n_gt;
+      keys_global = true;
+      compact();
+      done = true;
+    }
+  }
+  if (!done) {
     load_keys();
     // ---- radix select: 12 + 12 + 8 bits, usually only the first ----
     uint32_t prefix = 0, pmask = 0;
@@ -412,7 +449,7 @@ __global__ void __launch_bounds__(kSelThreads, 4)
       if (nv <= topk) {
         load_all();
       } else {
-        load_keys();  // the sort's counters reused the key buffer
+        if (!keys_global) load_keys();  // the sort reused the key buffer
         compact();
       }
       cur = bufA;
@@ -496,7 +533,8 @@ SelLayout sel_layout(int S_kv, int topk) {
 
 template <int EPT>
 cudaError_t launch_sel(const Problem &p, const float *logits, int topk,
-                       int32_t *out_idx, float *out_scores, cudaStream_t st) {
+                       const uint32_t *row_hist, int32_t *out_idx,
+                       float *out_scores, cudaStream_t st) {
   const SelLayout l = sel_layout(p.S_kv, topk);
   auto kern = topk_select_kernel<EPT>;
   cudaError_t e = cudaFuncSetAttribute(
@@ -504,8 +542,8 @@ cudaError_t launch_sel(const Problem &p, const float *logits, int topk,
   if (e != cudaSuccess) return e;
   const long long rows = (long long)p.B * p.S;
   kern<<<(unsigned)rows, kSelThreads, l.dyn, st>>>(
-      logits, p.q_pos, p.S, p.S_kv, p.ratio, topk, l.mcap, l.bcap, out_idx,
-      out_scores);
+      logits, row_hist, p.q_pos, p.S, p.S_kv, p.ratio, topk, l.mcap, l.bcap,
+      out_idx, out_scores);
   return cudaGetLastError();
 }
 
@@ -516,15 +554,15 @@ size_t topk_select_smem_bytes(int S_kv, int topk) {
 }
 
 cudaError_t launch_topk_select(const Problem &p, const float *logits, int topk,
-                               int32_t *out_idx, float *out_scores,
-                               cudaStream_t st) {
+                               const uint32_t *row_hist, int32_t *out_idx,
+                               float *out_scores, cudaStream_t st) {
   const int mcap = sel_layout(p.S_kv, topk).mcap;
   if (mcap <= kSelThreads * 8)
-    return launch_sel<8>(p, logits, topk, out_idx, out_scores, st);
+    return launch_sel<8>(p, logits, topk, row_hist, out_idx, out_scores, st);
   if (mcap <= kSelThreads * 16)
-    return launch_sel<16>(p, logits, topk, out_idx, out_scores, st);
-  return launch_sel<DSA_SEL_MAX_EPT + 2>(p, logits, topk, out_idx, out_scores,
-                                         st);
+    return launch_sel<16>(p, logits, topk, row_hist, out_idx, out_scores, st);
+  return launch_sel<DSA_SEL_MAX_EPT + 2>(p, logits, topk, row_hist, out_idx,
+                                         out_scores, st);
 }
 
 cudaError_t launch_gather_scores(const Problem &p, const float *logits,

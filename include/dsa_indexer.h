@@ -79,7 +79,9 @@ typedef enum dsa_status {
  * Bytes of device workspace dsa_indexer_fwd() needs for this shape
  * (has_in_idx != 0 selects the given-indices path).  Returns 0 when the
  * shape is invalid.  The workspace holds a 256-byte status header followed
- * by the fp32 logits [B, S, S_kv] of the visible keys.
+ * by the fp32 logits [B, S, S_kv] of the visible keys and, for shapes with
+ * fewer than 256/H queries per sequence (the decode kernel), one 4096-bin
+ * u32 key histogram per query row.
  */
 DSA_API size_t dsa_indexer_workspace_size(int S, int B, int H, int D,
                                           int S_kv, int compress_ratio,
