@@ -21,6 +21,8 @@ namespace dsa {
 namespace {
 
 constexpr int kDecStages = 5;
+static_assert(kDecChunkTiles <= kDecStages,
+              "an item's K tiles are issued before its Q and must fit the ring");
 constexpr int kDecThreads = 192;
 
 template <int H, int KC>
@@ -138,13 +140,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         const int qs = nq & 1;
         const uint32_t qph = (nq >> 1) & 1u;
         ++nq;
-        if (!(ok = wait_bar(q_empty(qs), qph ^ 1u, abort_flag, status))) break;
-        mbar_arrive_expect_tx(q_full(qs), L::kQBytes + L::kWBytes);
-        for (int c = 0; c < KC; ++c)
-          tma_load_4d(sQ + qs * L::kQBytes + c * (H * 128), &tm_q, q_full(qs),
-                      c * kChunk, 0, it.b, it.s);
-        bulk_load(smem_u32(sW) + qs * L::kWBytes,
-                  w + ((size_t)it.s * B + it.b) * H, L::kWBytes, q_full(qs));
+        // K tiles first, then the Q/weights slot: the tiles only need free
+        // ring stages (an item has at most kDecChunkTiles <= kDecStages of
+        // them, and every older item already has its Q), so the ring keeps
+        // streaming while the Q slot waits for the item two back to finish.
         for (int t = 0; t < it.ntiles; ++t) {
           if (!(ok = wait_bar(k_empty(kst), kph ^ 1u, abort_flag, status)))
             break;
@@ -158,6 +157,14 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             kph ^= 1u;
           }
         }
+        if (!ok) break;
+        if (!(ok = wait_bar(q_empty(qs), qph ^ 1u, abort_flag, status))) break;
+        mbar_arrive_expect_tx(q_full(qs), L::kQBytes + L::kWBytes);
+        for (int c = 0; c < KC; ++c)
+          tma_load_4d(sQ + qs * L::kQBytes + c * (H * 128), &tm_q, q_full(qs),
+                      c * kChunk, 0, it.b, it.s);
+        bulk_load(smem_u32(sW) + qs * L::kWBytes,
+                  w + ((size_t)it.s * B + it.b) * H, L::kWBytes, q_full(qs));
       }
     }
   } else if (warp == 1) {

@@ -244,13 +244,37 @@ __global__ void __launch_bounds__(kSelThreads, 4)
   auto key_at = [&](int j) -> uint32_t {
     return keys_global ? ordered_key(__ldg(L + j)) : keys[j];
   };
+  // row loads keep four independent global loads in flight per thread
   auto load_keys = [&]() {
-    for (int j = tid; j < nv; j += kSelThreads)
-      keys[j] = ordered_key(__ldg(L + j));
+    for (int j0 = tid; j0 < nv; j0 += 4 * kSelThreads) {
+      float v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + u * kSelThreads;
+        v[u] = j < nv ? __ldg(L + j) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + u * kSelThreads;
+        if (j < nv) keys[j] = ordered_key(v[u]);
+      }
+    }
   };
   auto load_all = [&]() {
-    for (int j = tid; j < nv; j += kSelThreads)
-      bufA[j] = ((uint64_t)ordered_key(__ldg(L + j)) << 32) | (uint32_t)j;
+    for (int j0 = tid; j0 < nv; j0 += 4 * kSelThreads) {
+      float v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + u * kSelThreads;
+        v[u] = j < nv ? __ldg(L + j) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + u * kSelThreads;
+        if (j < nv)
+          bufA[j] = ((uint64_t)ordered_key(v[u]) << 32) | (uint32_t)j;
+      }
+    }
     __syncthreads();
   };
   // ordered compaction, two walks over contiguous warp segments
@@ -334,7 +358,7 @@ __global__ void __launch_bounds__(kSelThreads, 4)
       need = 0;
       n_gt = (int)(dabove + dcount);
       m = n_gt;
-      keys_global = true;
+      load_keys();
       compact();
       done = true;
     }
