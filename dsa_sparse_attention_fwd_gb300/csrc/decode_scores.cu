@@ -27,15 +27,18 @@ constexpr int kDecThreads = 192;
 
 template <int H, int KC>
 struct DecSmem {
+  // Q/weight slots: enough lookahead that the next items' Q tiles are in
+  // flight while the current (short) item is multiplied
+  static constexpr int kQSlots = H <= 64 ? 4 : 2;
   static constexpr int kQBytes = KC * H * 128;           // one Q tile
   static constexpr int kKBytes = KC * kTileKeys * 128;   // one K stage
-  static constexpr int kOffQ = 0;                        // 2 Q buffers
-  static constexpr int kOffK = kOffQ + 2 * kQBytes;
-  static constexpr int kOffW = kOffK + kDecStages * kKBytes;
-  static constexpr int kOffBar = kOffW + 2 * H * 4;      // 2 weight rows
   static constexpr int kWBytes = H * 4;                  // one weight row
-  // k_full[S], k_empty[S], q_full[2], q_empty[2], acc_full[2], acc_empty[2]
-  static constexpr int kNumBars = 2 * kDecStages + 8;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kQSlots * kQBytes;
+  static constexpr int kOffW = kOffK + kDecStages * kKBytes;
+  static constexpr int kOffBar = kOffW + kQSlots * kWBytes;
+  // k_full[S], k_empty[S], q_full[Q], q_empty[Q], acc_full[2], acc_empty[2]
+  static constexpr int kNumBars = 2 * kDecStages + 2 * kQSlots + 4;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;
@@ -88,14 +91,21 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   uint8_t *smem = smem_raw + (base - raw_addr);
   const uint32_t sQ = base + L::kOffQ;
   const uint32_t sK = base + L::kOffK;
-  float *sW = reinterpret_cast<float *>(smem + L::kOffW);  // [2][H]
+  float *sW = reinterpret_cast<float *>(smem + L::kOffW);  // [slots][H]
   const uint32_t bars = base + L::kOffBar;
   auto k_full = [&](int i) { return bars + 8u * i; };
   auto k_empty = [&](int i) { return bars + 8u * (kDecStages + i); };
+  constexpr int NQ = L::kQSlots;
   auto q_full = [&](int i) { return bars + 8u * (2 * kDecStages + i); };
-  auto q_empty = [&](int i) { return bars + 8u * (2 * kDecStages + 2 + i); };
-  auto acc_full = [&](int i) { return bars + 8u * (2 * kDecStages + 4 + i); };
-  auto acc_empty = [&](int i) { return bars + 8u * (2 * kDecStages + 6 + i); };
+  auto q_empty = [&](int i) {
+    return bars + 8u * (2 * kDecStages + NQ + i);
+  };
+  auto acc_full = [&](int i) {
+    return bars + 8u * (2 * kDecStages + 2 * NQ + i);
+  };
+  auto acc_empty = [&](int i) {
+    return bars + 8u * (2 * kDecStages + 2 * NQ + 2 + i);
+  };
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kOffMisc);
   volatile int *abort_flag = reinterpret_cast<int *>(smem + L::kOffMisc + 4);
 
@@ -107,9 +117,11 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       mbar_init(k_full(i), 1);
       mbar_init(k_empty(i), 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NQ; ++i) {
       mbar_init(q_full(i), 1);
       mbar_init(q_empty(i), 5);  // the MMA issuer + four epilogue warps
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(acc_full(i), 1);
       mbar_init(acc_empty(i), 4);  // one arrival per epilogue warp
     }
@@ -137,8 +149,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         if (item < 0) break;
         const DecItem it = dec_item(item, rows, S, S_kv, ratio, q_pos);
         if (it.ntiles == 0) continue;
-        const int qs = nq & 1;
-        const uint32_t qph = (nq >> 1) & 1u;
+        const int qs = nq % NQ;
+        const uint32_t qph = (nq / NQ) & 1u;
         ++nq;
         // K tiles first, then the Q/weights slot: the tiles only need free
         // ring stages (an item has at most kDecChunkTiles <= kDecStages of
@@ -177,8 +189,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         if (item < 0) break;
         const DecItem it = dec_item(item, rows, S, S_kv, ratio, q_pos);
         if (it.ntiles == 0) continue;
-        const int qs = nq & 1;
-        const uint32_t qph = (nq >> 1) & 1u;
+        const int qs = nq % NQ;
+        const uint32_t qph = (nq / NQ) & 1u;
         ++nq;
         if (!(ok = wait_bar(q_full(qs), qph, abort_flag, status))) break;
         const uint32_t sQi = sQ + qs * L::kQBytes;
@@ -221,8 +233,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       const DecItem it = dec_item(item, rows, S, S_kv, ratio, q_pos);
       if (it.ntiles == 0) continue;
       // the row's weights arrive with its Q tile (same slot, same barrier)
-      const int qs = nq & 1;
-      const uint32_t qph = (nq >> 1) & 1u;
+      const int qs = nq % NQ;
+      const uint32_t qph = (nq / NQ) & 1u;
       ++nq;
       bool wok = wait_bar(q_full(qs), qph, abort_flag, status);
       if (!__all_sync(0xffffffffu, wok)) break;
