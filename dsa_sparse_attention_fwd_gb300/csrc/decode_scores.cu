@@ -5,14 +5,14 @@
 // A work item is (query row r = b*S + s, chunk of kDecChunkTiles x 128 keys).
 // One MMA tile is 128 keys (M) x H heads of the row's single query (N = H),
 // K = D, so no MMA column is padding.  The K ring (kDecStages x 128 keys) is
-// filled by the producer warp with cp.async; the row's Q tile (H x D) and
-// weights are loaded once per item by TMA into one of several slots.  The fp32 accumulator sits in TMEM (lane = key, column =
+// filled by TMA; the row's Q tile (H x D) is loaded once per item into one of
+// two buffers.  The fp32 accumulator sits in TMEM (lane = key, column =
 // head); each of the four epilogue warps owns 32 keys and reduces the
 // weighted ReLU over the heads in its own registers, then stores the visible
 // scores.  Items whose chunk starts past the row's last visible key are
 // skipped, so masked keys are never read.
 //
-// Warp roles (192 threads, one CTA per SM, persistent): warp 0 producer,
+// Warp roles (192 threads, one CTA per SM, persistent): warp 0 TMA producer,
 // warp 1 TMEM allocator and MMA issuer, warps 2..5 epilogue.
 #include "common.cuh"
 #include "ptx.cuh"
@@ -75,13 +75,12 @@ __device__ __forceinline__ int dec_item_for(int round, int n_items) {
 template <int H, int KC>
 __global__ void __launch_bounds__(kDecThreads, 1)
     decode_scores_kernel(const __grid_constant__ CUtensorMap tm_q,
-                         const uint16_t *__restrict__ kbits,
+                         const __grid_constant__ CUtensorMap tm_k,
                          const float *__restrict__ w,
                          const int32_t *__restrict__ q_pos,
                          float *__restrict__ logits,
                          uint32_t *__restrict__ row_hist, int S, int B,
-                         int D, int S_kv, int ratio, int n_items,
-                         int *status) {
+                         int S_kv, int ratio, int n_items, int *status) {
   using L = DecSmem<H, KC>;
   constexpr uint32_t kIdesc = idesc_bf16_f32(kTileKeys, H);
   constexpr int kAccCols = H;  // TMEM columns per accumulator
@@ -115,7 +114,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kDecStages; ++i) {
-      mbar_init(k_full(i), 32);  // one cp.async arrival per producer lane
+      mbar_init(k_full(i), 1);
       mbar_init(k_empty(i), 1);
     }
     for (int i = 0; i < NQ; ++i) {
@@ -129,6 +128,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_holder), 2 * kAccCols);
@@ -140,67 +140,44 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   const uint32_t tmem = *tmem_holder;
 
   if (warp == 0) {
-    // ---------------- producer warp ----------------
-    // K rows of one sequence are B*D*2 bytes apart in k [S_kv, B, D]; the
-    // tensor-copy engine moves such scattered 128-byte rows slowly, so the
-    // whole warp streams K with 16-byte cp.async copies into the same
-    // 128-byte-swizzled layout (16-byte chunk c of row r at c ^ (r & 7)),
-    // one arrival per lane on k_full.  Q and the weights (contiguous) still
-    // come by TMA / bulk copy from lane 0.
-    constexpr int kChunksPerKey = KC * 8;  // 16-byte chunks per key row
-    uint32_t kst = 0, kph = 0, nq = 0;
-    bool ok = true;
-    for (int r = 0; ok; ++r) {
-      const int item = dec_item_for(r, n_items);
-      if (item < 0) break;
-      const DecItem it = dec_item(item, rows, S, S_kv, ratio, q_pos);
-      if (it.ntiles == 0) continue;
-      const int qs = nq % NQ;
-      const uint32_t qph = (nq / NQ) & 1u;
-      ++nq;
-      // K tiles first, then the Q/weights slot: the tiles only need free
-      // ring stages (an item has at most kDecChunkTiles <= kDecStages of
-      // them, and every older item already has its Q), so the ring keeps
-      // streaming while the Q slot waits for an older item to finish.
-      for (int t = 0; t < it.ntiles; ++t) {
-        bool got = true;
-        if (lane == 0)
-          got = wait_bar(k_empty(kst), kph ^ 1u, abort_flag, status);
-        got = __shfl_sync(0xffffffffu, got, 0);
-        if (!(ok = got)) break;
-        const uint32_t sbase = sK + kst * L::kKBytes;
-        const int j0 = (it.tile0 + t) * kTileKeys;
-        for (int c = lane; c < kTileKeys * kChunksPerKey; c += 32) {
-          const int rr = c / kChunksPerKey, cc = c % kChunksPerKey;
-          const int h = cc >> 3, ch = cc & 7;
-          const int j = j0 + rr, d0 = h * kChunk + ch * 8;
-          const bool valid = j < S_kv && d0 < D;
-          const uint16_t *src =
-              valid ? kbits + ((size_t)j * B + it.b) * D + d0 : kbits;
-          cp_async16(sbase + h * (kTileKeys * 128) + rr * 128 +
-                         ((uint32_t)(ch ^ (rr & 7)) << 4),
-                     src, valid ? 16u : 0u);
-        }
-        cp_async_arrive(k_full(kst));
-        if (++kst == kDecStages) {
-          kst = 0;
-          kph ^= 1u;
-        }
-      }
-      if (!ok) break;
-      if (lane == 0) {
-        ok = wait_bar(q_empty(qs), qph ^ 1u, abort_flag, status);
-        if (ok) {
-          mbar_arrive_expect_tx(q_full(qs), L::kQBytes + L::kWBytes);
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      uint32_t kst = 0, kph = 0, nq = 0;
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const int item = dec_item_for(r, n_items);
+        if (item < 0) break;
+        const DecItem it = dec_item(item, rows, S, S_kv, ratio, q_pos);
+        if (it.ntiles == 0) continue;
+        const int qs = nq % NQ;
+        const uint32_t qph = (nq / NQ) & 1u;
+        ++nq;
+        // K tiles first, then the Q/weights slot: the tiles only need free
+        // ring stages (an item has at most kDecChunkTiles <= kDecStages of
+        // them, and every older item already has its Q), so the ring keeps
+        // streaming while the Q slot waits for the item two back to finish.
+        for (int t = 0; t < it.ntiles; ++t) {
+          if (!(ok = wait_bar(k_empty(kst), kph ^ 1u, abort_flag, status)))
+            break;
+          mbar_arrive_expect_tx(k_full(kst), L::kKBytes);
           for (int c = 0; c < KC; ++c)
-            tma_load_4d(sQ + qs * L::kQBytes + c * (H * 128), &tm_q,
-                        q_full(qs), c * kChunk, 0, it.b, it.s);
-          bulk_load(smem_u32(sW) + qs * L::kWBytes,
-                    w + ((size_t)it.s * B + it.b) * H, L::kWBytes,
-                    q_full(qs));
+            tma_load_3d(sK + kst * L::kKBytes + c * (kTileKeys * 128), &tm_k,
+                        k_full(kst), c * kChunk, it.b,
+                        (it.tile0 + t) * kTileKeys);
+          if (++kst == kDecStages) {
+            kst = 0;
+            kph ^= 1u;
+          }
         }
+        if (!ok) break;
+        if (!(ok = wait_bar(q_empty(qs), qph ^ 1u, abort_flag, status))) break;
+        mbar_arrive_expect_tx(q_full(qs), L::kQBytes + L::kWBytes);
+        for (int c = 0; c < KC; ++c)
+          tma_load_4d(sQ + qs * L::kQBytes + c * (H * 128), &tm_q, q_full(qs),
+                      c * kChunk, 0, it.b, it.s);
+        bulk_load(smem_u32(sW) + qs * L::kWBytes,
+                  w + ((size_t)it.s * B + it.b) * H, L::kWBytes, q_full(qs));
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
@@ -221,7 +198,6 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           if (!(ok = wait_bar(acc_empty(acc), aph ^ 1u, abort_flag, status)))
             break;
           if (!(ok = wait_bar(k_full(kst), kph, abort_flag, status))) break;
-          fence_proxy_async_smem();  // cp.async data -> tcgen05 operand reads
           tc_fence_after();
           const uint32_t d_tmem = tmem + acc * kAccCols;
 #pragma unroll
@@ -334,9 +310,9 @@ cudaError_t launch_dec(const Problem &p, const CUtensorMap &tm_q,
   if (n_items <= 0) return cudaSuccess;
   if (n_items > 0x7fffffffLL) return cudaErrorInvalidValue;
   const int grid = (int)(n_items < num_sms ? n_items : num_sms);
-  kern<<<grid, kDecThreads, smem, st>>>(
-      tm_q, static_cast<const uint16_t *>(p.k), p.w, p.q_pos, logits,
-      row_hist, p.S, p.B, p.D, p.S_kv, p.ratio, (int)n_items, status);
+  kern<<<grid, kDecThreads, smem, st>>>(tm_q, tm_k, p.w, p.q_pos, logits,
+                                        row_hist, p.S, p.B, p.S_kv, p.ratio,
+                                        (int)n_items, status);
   return cudaGetLastError();
 }
 

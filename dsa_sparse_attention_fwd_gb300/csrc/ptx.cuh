@@ -118,29 +118,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src,
       : "memory");
 }
 
-// 16-byte asynchronous copy global -> shared (L2 only); `src_bytes` < 16
-// zero-fills the rest (0 reads nothing).
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src,
-                                           uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst),
-               "l"(src), "r"(src_bytes)
-               : "memory");
-}
-
-// Arrive on `bar` once all earlier cp.async copies of this thread have
-// landed (the barrier's count must include this arrival).
-__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(
-                   bar)
-               : "memory");
-}
-
-// Orders this thread's generic-proxy view of shared memory before its later
-// async-proxy accesses (tcgen05.mma operand reads).
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // ---- tcgen05: tensor memory and the 5th-generation MMA ----------------------
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
