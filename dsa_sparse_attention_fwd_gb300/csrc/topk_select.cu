@@ -67,6 +67,7 @@ struct SelShared {
   uint32_t wgt[kSelWarps], weq[kSelWarps];
   uint32_t wand[kSelWarps], wor[kSelWarps];
   uint32_t sel_digit, sel_above, sel_count;
+  uint32_t cursor;
   int overflow;
 };
 
@@ -166,8 +167,8 @@ __device__ __forceinline__ void lsd_dispatch(const uint64_t *src,
 }
 
 // Fix-up after sorting on the top 24 key bits: inside each run of equal top
-// 24 bits (already in index order), order by the low 8 bits, descending,
-// keeping index order among equal keys.  Writes the result to dst.  Returns
+// 24 bits, order by the low 8 bits, descending, and equal keys by ascending
+// index (compared explicitly, so the run may arrive in any order).  Writes the result to dst.  Returns
 // true (block-uniform) when some run is longer than kRunLimit, in which case
 // dst is incomplete and the caller falls back to a full sort.
 constexpr int kRunLimit = 32;
@@ -181,11 +182,17 @@ __device__ __forceinline__ bool run_fixup(const uint64_t *src, uint64_t *dst,
     const uint64_t v = src[i];
     const uint32_t top = (uint32_t)(v >> 40);
     const uint32_t low = (uint32_t)(v >> 32) & 0xFFu;
+    const uint32_t jv = (uint32_t)v;
+    // does candidate u come before v in the final order?
+    auto before = [&](uint64_t u) -> int {
+      const uint32_t lu = (uint32_t)(u >> 32) & 0xFFu;
+      return lu > low || (lu == low && (uint32_t)u < jv);
+    };
     int cnt = 0, r = i - 1, steps = 0;
     while (r >= 0 && steps < kRunLimit) {
       const uint64_t u = src[r];
       if ((uint32_t)(u >> 40) != top) break;
-      cnt += (((uint32_t)(u >> 32) & 0xFFu) >= low);
+      cnt += before(u);
       --r;
       ++steps;
     }
@@ -197,7 +204,7 @@ __device__ __forceinline__ bool run_fixup(const uint64_t *src, uint64_t *dst,
     while (r < m && steps < kRunLimit) {
       const uint64_t u = src[r];
       if ((uint32_t)(u >> 40) != top) break;
-      cnt += (((uint32_t)(u >> 32) & 0xFFu) > low);
+      cnt += before(u);
       ++r;
       ++steps;
     }
@@ -240,10 +247,8 @@ __global__ void __launch_bounds__(kSelThreads, 4)
   // "above T" and "equal to T" groups), into bufA
   uint32_t T = 0;
   int need = 0, n_gt = 0;
-  bool keys_global = false;  // compact from the logits instead of keys[]
-  auto key_at = [&](int j) -> uint32_t {
-    return keys_global ? ordered_key(__ldg(L + j)) : keys[j];
-  };
+  bool unordered = false;  // candidates not in index order (fix-up needed)
+  auto key_at = [&](int j) -> uint32_t { return keys[j]; };
   // row loads keep four independent global loads in flight per thread
   auto load_keys = [&]() {
     for (int j0 = tid; j0 < nv; j0 += 4 * kSelThreads) {
@@ -354,12 +359,40 @@ __global__ void __launch_bounds__(kSelThreads, 4)
     const uint32_t dcount = sh.sel_count;
     __syncthreads();
     if (dabove + dcount <= (uint32_t)mcap) {
+      // one pass over the row: keep keys whose top 12 bits reach the
+      // threshold bucket, appended in any order (the fix-up below orders
+      // equal keys by index explicitly)
       T = dsel << kRowHistShift;
       need = 0;
       n_gt = (int)(dabove + dcount);
       m = n_gt;
-      load_keys();
-      compact();
+      if (tid == 0) sh.cursor = 0;
+      __syncthreads();
+      for (int c0 = 0; c0 < nv; c0 += 4 * kSelThreads) {
+        float v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int j = c0 + u * kSelThreads + tid;
+          v[u] = j < nv ? __ldg(L + j) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int j = c0 + u * kSelThreads + tid;
+          const uint32_t key = ordered_key(v[u]);
+          const bool keep = j < nv && key >= T;
+          const uint32_t bal = __ballot_sync(0xffffffffu, keep);
+          uint32_t base = 0;
+          if (lane == 0 && bal) base = atomicAdd(&sh.cursor, __popc(bal));
+          base = __shfl_sync(0xffffffffu, base, 0);
+          const uint32_t pos = base + __popc(bal & lt);
+          if (keep && pos < (uint32_t)mcap)
+            bufA[pos] = ((uint64_t)key << 32) | (uint32_t)j;
+        }
+      }
+      __syncthreads();
+      // equals the histogram's count; the bound only guards the buffer
+      m = min((int)sh.cursor, mcap);
+      unordered = true;
       done = true;
     }
   }
@@ -463,7 +496,7 @@ __global__ void __launch_bounds__(kSelThreads, 4)
     cur = alt;
     alt = t;
   }
-  if ((diff & 0xFFu) != 0u) {
+  if ((diff & 0xFFu) != 0u || unordered) {
     if (!run_fixup(cur, alt, m, sh)) {
       uint64_t *t = cur;
       cur = alt;
@@ -473,7 +506,7 @@ __global__ void __launch_bounds__(kSelThreads, 4)
       if (nv <= topk) {
         load_all();
       } else {
-        if (!keys_global) load_keys();  // the sort reused the key buffer
+        load_keys();  // the sort reused the key buffer
         compact();
       }
       cur = bufA;
