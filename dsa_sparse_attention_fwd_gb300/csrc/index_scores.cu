@@ -221,18 +221,43 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     const int et = threadIdx.x - 64;  // 0..255
     uint32_t acc = 0, aph = 0;
     bool ok = true;
-    for (int r = 0; ok; ++r) {
-      const int item = item_for(r, n_items);
-      if (item < 0) break;
-      const ItemInfo it = item_info<H>(item, S, B, S_kv, ratio, q_pos);
-      if (it.ntiles == 0) continue;
-      named_bar_sync(1, 256);  // everyone is done with the previous weights
-      {
-        const int tq = et / H, h = et % H;
-        const int t = it.t0 + tq;
-        sW[et] = t < S ? __ldg(w + ((size_t)t * B + it.b) * H + h) : 0.f;
+    const int tq_mine = et / H, h_mine = et % H;  // the weight this thread loads
+    auto weight_of = [&](const ItemInfo &it) -> float {
+      const int t = it.t0 + tq_mine;
+      return t < S ? __ldg(w + ((size_t)t * B + it.b) * H + h_mine) : 0.f;
+    };
+    // first item with work at or after round r (ntiles = -1: none)
+    auto next_item = [&](int r, int &round) -> ItemInfo {
+      for (;; ++r) {
+        const int item = item_for(r, n_items);
+        if (item < 0) break;
+        const ItemInfo it = item_info<H>(item, S, B, S_kv, ratio, q_pos);
+        if (it.ntiles > 0) {
+          round = r;
+          return it;
+        }
       }
+      ItemInfo none;
+      none.b = 0;
+      none.t0 = 0;
+      none.ntiles = -1;
+      round = r;
+      return none;
+    };
+    int r = 0;
+    ItemInfo it = next_item(0, r);
+    // the weights of the next item are loaded one item ahead, so their
+    // global-memory latency hides behind the current item's tiles
+    float w_next = it.ntiles > 0 ? weight_of(it) : 0.f;
+    while (it.ntiles > 0) {
+      // everyone is done with the previous weights; stop together if any
+      // epilogue warp gave up on a wait
+      if (named_bar_or(1, 256, !ok)) break;
+      sW[et] = w_next;
       named_bar_sync(1, 256);
+      int r_next;
+      const ItemInfo nx = next_item(r + 1, r_next);
+      if (nx.ntiles > 0) w_next = weight_of(nx);
       // position of query row t is qbase + t
       const long long qbase = row_pos(q_pos, it.b, 0);
 
@@ -265,26 +290,54 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         for (int qq = 0; qq < QH; ++qq) {
           const int tq = half * QH + qq;
           const float *wq = sW + tq * H;
-          float s0 = 0.f, s1 = 0.f;
+          float score;
+          if constexpr (H % 4 == 0) {
+            // even heads in .x, odd heads in .y; weights four at a time
+            float2 acc2 = make_float2(0.f, 0.f);
+            const float4 *wq4 = reinterpret_cast<const float4 *>(wq);
 #pragma unroll
-          for (int h = 0; h < H; h += 2) {
-            const int c0 = qq * H + h;
-            s0 = fmaf(wq[h], fmaxf(__uint_as_float(v[c0 >> 5][c0 & 31]), 0.f),
-                      s0);
-            if (h + 1 < H) {
-              const int c1 = c0 + 1;
-              s1 = fmaf(wq[h + 1],
-                        fmaxf(__uint_as_float(v[c1 >> 5][c1 & 31]), 0.f), s1);
+            for (int h = 0; h < H; h += 4) {
+              const float4 wv = wq4[h >> 2];
+              const int c = qq * H + h;
+              const float r0 = fmaxf(__uint_as_float(v[c >> 5][c & 31]), 0.f);
+              const float r1 =
+                  fmaxf(__uint_as_float(v[(c + 1) >> 5][(c + 1) & 31]), 0.f);
+              const float r2 =
+                  fmaxf(__uint_as_float(v[(c + 2) >> 5][(c + 2) & 31]), 0.f);
+              const float r3 =
+                  fmaxf(__uint_as_float(v[(c + 3) >> 5][(c + 3) & 31]), 0.f);
+              acc2 = __ffma2_rn(make_float2(wv.x, wv.y), make_float2(r0, r1),
+                                acc2);
+              acc2 = __ffma2_rn(make_float2(wv.z, wv.w), make_float2(r2, r3),
+                                acc2);
             }
+            score = acc2.x + acc2.y;
+          } else {
+            float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+            for (int h = 0; h < H; h += 2) {
+              const int c0 = qq * H + h;
+              s0 = fmaf(wq[h],
+                        fmaxf(__uint_as_float(v[c0 >> 5][c0 & 31]), 0.f), s0);
+              if (h + 1 < H) {
+                const int c1 = c0 + 1;
+                s1 = fmaf(wq[h + 1],
+                          fmaxf(__uint_as_float(v[c1 >> 5][c1 & 31]), 0.f),
+                          s1);
+              }
+            }
+            score = s0 + s1;
           }
           const int t = it.t0 + tq;
           const bool vis = (long long)(j + 1) * ratio - 1 <= qbase + t;
           if (t < S && vis && j < S_kv)
-            logits[((size_t)it.b * S + t) * S_kv + j] = s0 + s1;
+            logits[((size_t)it.b * S + t) * S_kv + j] = score;
         }
         acc ^= 1u;
         if (acc == 0) aph ^= 1u;
       }
+      it = nx;
+      r = r_next;
     }
   }
 
