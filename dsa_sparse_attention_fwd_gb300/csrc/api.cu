@@ -141,9 +141,15 @@ bool use_decode_path(const Problem &p, const DeviceInfo &dev) {
          (size_t)dev.max_smem_optin >= dsa::decode_smem_bytes(p.H, p.D);
 }
 
-// Bytes of the per-row key histograms the decode path adds to the workspace.
+// Scoring kernels that also count each row's top 12 key bits for the
+// selection: the decode kernel, and the prefill kernel when H >= 64.
+bool hist_shape(int S, int H, int D) {
+  return decode_shape(S, H, D) || dsa::index_scores_histograms(H);
+}
+
+// Bytes of the per-row key histograms in the workspace.
 size_t row_hist_bytes(int S, int B, int H, int D) {
-  return decode_shape(S, H, D)
+  return hist_shape(S, H, D)
              ? (size_t)B * S * dsa::kRowHistBins * sizeof(uint32_t)
              : 0;
 }
@@ -153,7 +159,7 @@ int run_scores(const Problem &p, float *logits, uint32_t *row_hist,
                int *status, const DeviceInfo &dev, cudaStream_t st) {
   const bool decode = use_decode_path(p, dev);
   if (!decode &&
-      (size_t)dev.max_smem_optin < dsa::index_scores_smem_bytes(p.D))
+      (size_t)dev.max_smem_optin < dsa::index_scores_smem_bytes(p.H, p.D))
     return DSA_ERR_UNSUPPORTED;
   CUtensorMap tm_q, tm_k;
   int rc = encode_q(&tm_q, p, decode ? 1 : dsa::kTileCols / p.H);
@@ -163,8 +169,8 @@ int run_scores(const Problem &p, float *logits, uint32_t *row_hist,
   const cudaError_t e =
       decode ? dsa::launch_decode_scores(p, tm_q, tm_k, logits, row_hist,
                                          status, dev.num_sms, st)
-             : dsa::launch_index_scores(p, tm_q, tm_k, logits, status,
-                                        dev.num_sms, st);
+             : dsa::launch_index_scores(p, tm_q, tm_k, logits, row_hist,
+                                        status, dev.num_sms, st);
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
@@ -238,16 +244,19 @@ int dsa_indexer_fwd_profiled(const void *q, const void *k, const float *w,
                : cudaSuccess;
   };
 
-  // per-row key histograms (decode path, top-k only): filled by the scoring
-  // kernel, read by the selection
+  // per-row key histograms (top-k path): filled by the scoring kernel, read
+  // by the selection.  The decode kernel counts with global atomics (so the
+  // region starts at zero); the prefill kernel writes every row it scores.
   uint32_t *row_hist = nullptr;
-  if (!in_idx && use_decode_path(p, dev))
+  const bool decode = use_decode_path(p, dev);
+  if (!in_idx && ((decode && hist_shape(S, H, D)) ||
+                  (!decode && dsa::index_scores_histograms(H))))
     row_hist = reinterpret_cast<uint32_t *>(
         static_cast<char *>(workspace) + kHeaderBytes +
         logits_bytes(S, B, S_kv));
   if (cudaMemsetAsync(status, 0, kHeaderBytes, st) != cudaSuccess)
     return DSA_ERR_CUDA;
-  if (row_hist &&
+  if (row_hist && decode &&
       cudaMemsetAsync(row_hist, 0, row_hist_bytes(S, B, H, D), st) !=
           cudaSuccess)
     return DSA_ERR_CUDA;

@@ -28,15 +28,23 @@
 namespace dsa {
 namespace {
 
-template <int KC>
+template <int H, int KC>
 struct ScoreSmem {
+  static constexpr int kTQ = kTileCols / H;              // queries per item
+  // Per-query top-12-bit key histograms (u32 bins) for the selection, kept
+  // in shared memory while an item is scored; only when an item has few
+  // queries (H >= 64), which leaves room by using a single Q buffer.
+  static constexpr bool kHist = H >= 64;
+  static constexpr int kHistBytes = kHist ? kTQ * kRowHistBins * 4 : 0;
+  static constexpr int kQSlots = kHist ? 1 : 2;
   static constexpr int kStages = KC == 1 ? 4 : 3;        // K ring depth
   static constexpr int kQBytes = KC * kTileCols * 128;  // one Q tile
   static constexpr int kKBytes = KC * kTileKeys * 128;  // one K stage
-  static constexpr int kOffQ = 0;                        // 2 Q buffers
-  static constexpr int kOffK = kOffQ + 2 * kQBytes;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kQSlots * kQBytes;
   static constexpr int kOffW = kOffK + kStages * kKBytes;
-  static constexpr int kOffBar = kOffW + kTileCols * 4;
+  static constexpr int kOffHist = kOffW + kTileCols * 4;
+  static constexpr int kOffBar = kOffHist + kHistBytes;
   // barriers: k_full[S], k_empty[S], q_full[2], q_empty[2], acc_full[2],
   // acc_empty[2]
   static constexpr int kNumBars = 2 * kStages + 4 + 4;
@@ -82,9 +90,12 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                         const __grid_constant__ CUtensorMap tm_k,
                         const float *__restrict__ w,
                         const int32_t *__restrict__ q_pos,
-                        float *__restrict__ logits, int S, int B, int S_kv,
-                        int ratio, int *status) {
-  using L = ScoreSmem<KC>;
+                        float *__restrict__ logits,
+                        uint32_t *__restrict__ row_hist, int S, int B,
+                        int S_kv, int ratio, int *status) {
+  using L = ScoreSmem<H, KC>;
+  constexpr int NQ = L::kQSlots;
+  const bool do_hist = L::kHist && row_hist != nullptr;
   constexpr int kStages = L::kStages;
   constexpr int TQ = kTileCols / H;  // queries per work item
   constexpr int QH = TQ / 2;         // queries per epilogue column half
@@ -98,6 +109,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   const uint32_t sQ = base + L::kOffQ;
   const uint32_t sK = base + L::kOffK;
   float *sW = reinterpret_cast<float *>(smem + L::kOffW);
+  uint32_t *sHist = reinterpret_cast<uint32_t *>(smem + L::kOffHist);
   const uint32_t bars = base + L::kOffBar;
   auto k_full = [&](int s) { return bars + 8u * s; };
   auto k_empty = [&](int s) { return bars + 8u * (kStages + s); };
@@ -128,6 +140,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
   }
+  if (do_hist)
+    for (int i = threadIdx.x; i < L::kHistBytes / 4; i += kScoreThreads)
+      sHist[i] = 0u;
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_holder), 512);
     tmem_relinquish();
@@ -147,8 +162,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         if (item < 0) break;
         const ItemInfo it = item_info<H>(item, S, B, S_kv, ratio, q_pos);
         if (it.ntiles == 0) continue;
-        const int qs = nq & 1;
-        const uint32_t qph = (nq >> 1) & 1u;
+        const int qs = nq % NQ;
+        const uint32_t qph = (nq / NQ) & 1u;
         ++nq;
         if (!(ok = wait_bar(q_empty(qs), qph ^ 1u, abort_flag, status))) break;
         mbar_arrive_expect_tx(q_full(qs), L::kQBytes);
@@ -179,8 +194,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         if (item < 0) break;
         const ItemInfo it = item_info<H>(item, S, B, S_kv, ratio, q_pos);
         if (it.ntiles == 0) continue;
-        const int qs = nq & 1;
-        const uint32_t qph = (nq >> 1) & 1u;
+        const int qs = nq % NQ;
+        const uint32_t qph = (nq / NQ) & 1u;
         ++nq;
         if (!(ok = wait_bar(q_full(qs), qph, abort_flag, status))) break;
         const uint32_t sQi = sQ + qs * L::kQBytes;
@@ -330,11 +345,28 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           }
           const int t = it.t0 + tq;
           const bool vis = (long long)(j + 1) * ratio - 1 <= qbase + t;
-          if (t < S && vis && j < S_kv)
+          if (t < S && vis && j < S_kv) {
             logits[((size_t)it.b * S + t) * S_kv + j] = score;
+            if (do_hist)
+              atomicAdd(&sHist[tq * kRowHistBins +
+                               (ordered_key(score) >> kRowHistShift)],
+                        1u);
+          }
         }
         acc ^= 1u;
         if (acc == 0) aph ^= 1u;
+      }
+      if (do_hist) {
+        // the item's rows are complete: write their histograms out and clear
+        // them (the next item starts after the barrier at its top)
+        named_bar_sync(2, 256);
+        for (int i = et; i < L::kTQ * kRowHistBins; i += 256) {
+          const int t = it.t0 + (i / kRowHistBins);
+          if (t < S)
+            row_hist[((size_t)it.b * S + t) * kRowHistBins +
+                     (i % kRowHistBins)] = sHist[i];
+          sHist[i] = 0u;
+        }
       }
       it = nx;
       r = r_next;
@@ -351,11 +383,12 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 
 template <int H, int KC>
 cudaError_t launch_t(const Problem &p, const CUtensorMap &tm_q,
-                     const CUtensorMap &tm_k, float *logits, int *status,
-                     int num_sms, cudaStream_t st) {
+                     const CUtensorMap &tm_k, float *logits,
+                     uint32_t *row_hist, int *status, int num_sms,
+                     cudaStream_t st) {
   constexpr int TQ = kTileCols / H;
   auto kern = index_scores_kernel<H, KC>;
-  const int smem = ScoreSmem<KC>::kAlloc;
+  const int smem = ScoreSmem<H, KC>::kAlloc;
   cudaError_t e = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -363,43 +396,55 @@ cudaError_t launch_t(const Problem &p, const CUtensorMap &tm_q,
   const int grid = (int)(n_items < num_sms ? n_items : num_sms);
   if (grid <= 0) return cudaSuccess;
   kern<<<grid, kScoreThreads, smem, st>>>(tm_q, tm_k, p.w, p.q_pos, logits,
-                                          p.S, p.B, p.S_kv, p.ratio, status);
+                                          row_hist, p.S, p.B, p.S_kv, p.ratio,
+                                          status);
   return cudaGetLastError();
 }
 
 template <int KC>
 cudaError_t launch_kc(const Problem &p, const CUtensorMap &tm_q,
-                      const CUtensorMap &tm_k, float *logits, int *status,
-                      int num_sms, cudaStream_t st) {
+                      const CUtensorMap &tm_k, float *logits,
+                      uint32_t *row_hist, int *status, int num_sms,
+                      cudaStream_t st) {
   switch (p.H) {
-    case 1: return launch_t<1, KC>(p, tm_q, tm_k, logits, status, num_sms, st);
-    case 2: return launch_t<2, KC>(p, tm_q, tm_k, logits, status, num_sms, st);
-    case 4: return launch_t<4, KC>(p, tm_q, tm_k, logits, status, num_sms, st);
-    case 8: return launch_t<8, KC>(p, tm_q, tm_k, logits, status, num_sms, st);
+    case 1: return launch_t<1, KC>(p, tm_q, tm_k, logits, row_hist, status, num_sms, st);
+    case 2: return launch_t<2, KC>(p, tm_q, tm_k, logits, row_hist, status, num_sms, st);
+    case 4: return launch_t<4, KC>(p, tm_q, tm_k, logits, row_hist, status, num_sms, st);
+    case 8: return launch_t<8, KC>(p, tm_q, tm_k, logits, row_hist, status, num_sms, st);
     case 16:
-      return launch_t<16, KC>(p, tm_q, tm_k, logits, status, num_sms, st);
+      return launch_t<16, KC>(p, tm_q, tm_k, logits, row_hist, status, num_sms, st);
     case 32:
-      return launch_t<32, KC>(p, tm_q, tm_k, logits, status, num_sms, st);
+      return launch_t<32, KC>(p, tm_q, tm_k, logits, row_hist, status, num_sms, st);
     case 64:
-      return launch_t<64, KC>(p, tm_q, tm_k, logits, status, num_sms, st);
+      return launch_t<64, KC>(p, tm_q, tm_k, logits, row_hist, status, num_sms, st);
     case 128:
-      return launch_t<128, KC>(p, tm_q, tm_k, logits, status, num_sms, st);
+      return launch_t<128, KC>(p, tm_q, tm_k, logits, row_hist, status, num_sms, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
-size_t index_scores_smem_bytes(int D) {
-  return D <= kChunk ? ScoreSmem<1>::kAlloc : ScoreSmem<2>::kAlloc;
+size_t index_scores_smem_bytes(int H, int D) {
+  size_t m = 0;
+#define DSA_SMEM_CASE(HH)                                                  \
+  if (H == HH)                                                             \
+    m = D <= kChunk ? ScoreSmem<HH, 1>::kAlloc : ScoreSmem<HH, 2>::kAlloc;
+  DSA_SMEM_CASE(1) DSA_SMEM_CASE(2) DSA_SMEM_CASE(4) DSA_SMEM_CASE(8)
+  DSA_SMEM_CASE(16) DSA_SMEM_CASE(32) DSA_SMEM_CASE(64) DSA_SMEM_CASE(128)
+#undef DSA_SMEM_CASE
+  return m;
 }
+
+bool index_scores_histograms(int H) { return H >= 64; }
 
 cudaError_t launch_index_scores(const Problem &p, const CUtensorMap &tm_q,
                                 const CUtensorMap &tm_k, float *logits,
-                                int *status, int num_sms, cudaStream_t st) {
+                                uint32_t *row_hist, int *status, int num_sms,
+                                cudaStream_t st) {
   if (p.D <= kChunk)
-    return launch_kc<1>(p, tm_q, tm_k, logits, status, num_sms, st);
-  return launch_kc<2>(p, tm_q, tm_k, logits, status, num_sms, st);
+    return launch_kc<1>(p, tm_q, tm_k, logits, row_hist, status, num_sms, st);
+  return launch_kc<2>(p, tm_q, tm_k, logits, row_hist, status, num_sms, st);
 }
 
 }  // namespace dsa

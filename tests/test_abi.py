@@ -85,8 +85,14 @@ def test_status_strings(lib):
 
 def test_workspace_size(lib):
     ws = lib.dsa_indexer_workspace_size
-    assert ws(4096, 1, 64, 128, 4096, 1, 2048, 0) == 256 + 4096 * 4096 * 4
-    assert ws(16384, 2, 64, 128, 4096, 4, 512, 0) == 256 + 2 * 16384 * 4096 * 4
+    hist = 4096 * 4  # per-row key histogram (H >= 64 or decode shapes)
+    assert ws(4096, 1, 64, 128, 4096, 1, 2048, 0) == (256 + 4096 * 4096 * 4
+                                                      + 4096 * hist)
+    assert ws(16384, 2, 64, 128, 4096, 4, 512, 0) == (
+        256 + 2 * 16384 * 4096 * 4 + 2 * 16384 * hist)
+    assert ws(64, 1, 16, 64, 64, 1, 8, 0) == 256 + 64 * 64 * 4  # no histograms
+    assert ws(1, 64, 32, 64, 8192, 4, 512, 0) == (256 + 64 * 8192 * 4
+                                                  + 64 * hist)  # decode
     assert ws(0, 1, 64, 128, 4096, 1, 2048, 0) == 0
     assert ws(16, 1, 3, 128, 16, 1, 4, 0) == 0
     assert ws(16, 1, 4, 128, 16, 1, 0, 0) == 0
