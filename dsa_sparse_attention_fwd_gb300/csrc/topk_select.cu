@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(kSelThreads, 4)
     topk_select_kernel(const float *__restrict__ logits,
                        const uint32_t *__restrict__ row_hist,
                        const int32_t *__restrict__ q_pos, int S, int S_kv,
-                       int ratio, int topk, int mcap, int bcap,
+                       int ratio, int topk, int mcap, int bcap, int keys_cap,
                        int32_t *__restrict__ out_idx,
                        float *__restrict__ out_scores) {
   extern __shared__ __align__(16) uint8_t smem[];
@@ -248,9 +248,15 @@ __global__ void __launch_bounds__(kSelThreads, 4)
   uint32_t T = 0;
   int need = 0, n_gt = 0;
   bool unordered = false;  // candidates not in index order (fix-up needed)
-  auto key_at = [&](int j) -> uint32_t { return keys[j]; };
+  // without a row-key buffer (the histogram route) keys come straight from
+  // the logits; only the rare fallbacks read them that way
+  const bool staged = keys_cap >= nv;
+  auto key_at = [&](int j) -> uint32_t {
+    return staged ? keys[j] : ordered_key(__ldg(L + j));
+  };
   // row loads keep four independent global loads in flight per thread
   auto load_keys = [&]() {
+    if (!staged) return;
     for (int j0 = tid; j0 < nv; j0 += 4 * kSelThreads) {
       float v[4];
 #pragma unroll
@@ -261,7 +267,7 @@ __global__ void __launch_bounds__(kSelThreads, 4)
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int j = j0 + u * kSelThreads;
-        if (j < nv) keys[j] = ordered_key(v[u]);
+        if (j < nv && staged) keys[j] = ordered_key(v[u]);
       }
     }
   };
@@ -411,7 +417,7 @@ __global__ void __launch_bounds__(kSelThreads, 4)
       for (int i = tid; i < nb; i += kSelThreads) hist[i] = 0;
       __syncthreads();
       for (int j = tid; j < nv; j += kSelThreads) {
-        const uint32_t u = keys[j];
+        const uint32_t u = key_at(j);
         if ((u & pmask) == prefix) atomicAdd(&hist[(u >> shift) & dmask], 1u);
       }
       __syncthreads();
@@ -571,18 +577,21 @@ __global__ void fill_neg_inf_kernel(float *p, size_t n) {
 // [bcap] u64 (also the 4096-bin select histogram), keys [S_kv] u32 (at least
 // 8 KB: the sort's per-warp histograms reuse it once the keys are dead).
 struct SelLayout {
-  int mcap, bcap;
+  int mcap, bcap, keys_cap;
   size_t dyn;
 };
 
-SelLayout sel_layout(int S_kv, int topk) {
+SelLayout sel_layout(int S_kv, int topk, bool hist) {
   SelLayout l;
   // room for the candidates of a one-pass select: topk plus the rest of
   // the threshold bucket (up to kSelSlack keys)
   l.mcap = topk + kSelSlack < S_kv ? topk + kSelSlack : S_kv;
   l.bcap = l.mcap > kHistBins / 2 ? l.mcap : kHistBins / 2;
-  const size_t key_bytes = (size_t)S_kv * 4;
+  // with precomputed row histograms the row is never staged in shared
+  // memory; the region then only holds the sort's per-warp counters
+  const size_t key_bytes = hist ? 0 : (size_t)S_kv * 4;
   const size_t whist_bytes = (size_t)kSelWarps * 256 * 4;
+  l.keys_cap = hist ? 0 : S_kv;
   l.dyn = (size_t)(l.mcap + l.bcap) * 8 +
           (key_bytes > whist_bytes ? key_bytes : whist_bytes);
   return l;
@@ -592,7 +601,7 @@ template <int EPT>
 cudaError_t launch_sel(const Problem &p, const float *logits, int topk,
                        const uint32_t *row_hist, int32_t *out_idx,
                        float *out_scores, cudaStream_t st) {
-  const SelLayout l = sel_layout(p.S_kv, topk);
+  const SelLayout l = sel_layout(p.S_kv, topk, row_hist != nullptr);
   auto kern = topk_select_kernel<EPT>;
   cudaError_t e = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)l.dyn);
@@ -600,20 +609,20 @@ cudaError_t launch_sel(const Problem &p, const float *logits, int topk,
   const long long rows = (long long)p.B * p.S;
   kern<<<(unsigned)rows, kSelThreads, l.dyn, st>>>(
       logits, row_hist, p.q_pos, p.S, p.S_kv, p.ratio, topk, l.mcap, l.bcap,
-      out_idx, out_scores);
+      l.keys_cap, out_idx, out_scores);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 size_t topk_select_smem_bytes(int S_kv, int topk) {
-  return sel_layout(S_kv, topk).dyn + sizeof(SelShared);
+  return sel_layout(S_kv, topk, false).dyn + sizeof(SelShared);
 }
 
 cudaError_t launch_topk_select(const Problem &p, const float *logits, int topk,
                                const uint32_t *row_hist, int32_t *out_idx,
                                float *out_scores, cudaStream_t st) {
-  const int mcap = sel_layout(p.S_kv, topk).mcap;
+  const int mcap = sel_layout(p.S_kv, topk, row_hist != nullptr).mcap;
   if (mcap <= kSelThreads * 8)
     return launch_sel<8>(p, logits, topk, row_hist, out_idx, out_scores, st);
   if (mcap <= kSelThreads * 16)
