@@ -143,13 +143,13 @@ bool use_decode_path(const Problem &p, const DeviceInfo &dev) {
 
 // Scoring kernels that also count each row's top 12 key bits for the
 // selection: the decode kernel, and the prefill kernel when H >= 64.
-bool hist_shape(int S, int H, int D) {
-  return decode_shape(S, H, D) || dsa::index_scores_histograms(H);
+bool hist_shape(int S, int H, int D, int S_kv) {
+  return decode_shape(S, H, D) || dsa::index_scores_histograms(H, S_kv);
 }
 
 // Bytes of the per-row key histograms in the workspace.
-size_t row_hist_bytes(int S, int B, int H, int D) {
-  return hist_shape(S, H, D)
+size_t row_hist_bytes(int S, int B, int H, int D, int S_kv) {
+  return hist_shape(S, H, D, S_kv)
              ? (size_t)B * S * dsa::kRowHistBins * sizeof(uint32_t)
              : 0;
 }
@@ -197,7 +197,8 @@ size_t dsa_indexer_workspace_size(int S, int B, int H, int D, int S_kv,
   (void)has_in_idx;
   if (check_shape(S, B, H, D, S_kv, compress_ratio) != DSA_OK) return 0;
   if (topk <= 0 || topk > DSA_MAX_TOPK) return 0;
-  return kHeaderBytes + logits_bytes(S, B, S_kv) + row_hist_bytes(S, B, H, D);
+  return kHeaderBytes + logits_bytes(S, B, S_kv) +
+         row_hist_bytes(S, B, H, D, S_kv);
 }
 
 size_t dsa_indexer_logits_workspace_size(void) { return kHeaderBytes; }
@@ -249,15 +250,15 @@ int dsa_indexer_fwd_profiled(const void *q, const void *k, const float *w,
   // region starts at zero); the prefill kernel writes every row it scores.
   uint32_t *row_hist = nullptr;
   const bool decode = use_decode_path(p, dev);
-  if (!in_idx && ((decode && hist_shape(S, H, D)) ||
-                  (!decode && dsa::index_scores_histograms(H))))
+  if (!in_idx && ((decode && hist_shape(S, H, D, S_kv)) ||
+                  (!decode && dsa::index_scores_histograms(H, S_kv))))
     row_hist = reinterpret_cast<uint32_t *>(
         static_cast<char *>(workspace) + kHeaderBytes +
         logits_bytes(S, B, S_kv));
   if (cudaMemsetAsync(status, 0, kHeaderBytes, st) != cudaSuccess)
     return DSA_ERR_CUDA;
   if (row_hist && decode &&
-      cudaMemsetAsync(row_hist, 0, row_hist_bytes(S, B, H, D), st) !=
+      cudaMemsetAsync(row_hist, 0, row_hist_bytes(S, B, H, D, S_kv), st) !=
           cudaSuccess)
     return DSA_ERR_CUDA;
   if (mark(0) != cudaSuccess) return DSA_ERR_CUDA;

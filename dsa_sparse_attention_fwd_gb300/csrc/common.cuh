@@ -70,13 +70,13 @@ constexpr int kDecChunkTiles = 2;   // decode: key tiles per work item
 // Launchers (return cudaSuccess or the launch error).  `logits` is
 // [B, S, S_kv] fp32; only visible entries are written.
 // row_hist (nullable): per-row top-12-bit key histograms, written for every
-// scored row when index_scores_histograms(H).
+// scored row (pass it only when index_scores_histograms(H, S_kv)).
 cudaError_t launch_index_scores(const Problem &p, const CUtensorMap &tm_q,
                                 const CUtensorMap &tm_k, float *logits,
                                 uint32_t *row_hist, int *status, int num_sms,
                                 cudaStream_t st);
 size_t index_scores_smem_bytes(int H, int D);
-bool index_scores_histograms(int H);
+bool index_scores_histograms(int H, int S_kv);
 
 // row_hist: per-row top-12-bit key histograms from the decode scoring
 // kernel, or nullptr (the selection then builds its own).

@@ -28,13 +28,13 @@
 namespace dsa {
 namespace {
 
-template <int H, int KC>
+template <int H, int KC, bool HIST>
 struct ScoreSmem {
   static constexpr int kTQ = kTileCols / H;              // queries per item
   // Per-query top-12-bit key histograms (u32 bins) for the selection, kept
-  // in shared memory while an item is scored; only when an item has few
-  // queries (H >= 64), which leaves room by using a single Q buffer.
-  static constexpr bool kHist = H >= 64;
+  // in shared memory while an item is scored; only instantiated when an item
+  // has few queries (H >= 64), making room with a single Q buffer.
+  static constexpr bool kHist = HIST && H >= 64;
   static constexpr int kHistBytes = kHist ? kTQ * kRowHistBins * 4 : 0;
   static constexpr int kQSlots = kHist ? 1 : 2;
   static constexpr int kStages = KC == 1 ? 4 : 3;        // K ring depth
@@ -84,7 +84,7 @@ __device__ __forceinline__ int item_for(int round, int n_items) {
   return idx < n_items ? idx : -1;
 }
 
-template <int H, int KC>
+template <int H, int KC, bool HIST>
 __global__ void __launch_bounds__(kScoreThreads, 1)
     index_scores_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                         float *__restrict__ logits,
                         uint32_t *__restrict__ row_hist, int S, int B,
                         int S_kv, int ratio, int *status) {
-  using L = ScoreSmem<H, KC>;
+  using L = ScoreSmem<H, KC, HIST>;
   constexpr int NQ = L::kQSlots;
   const bool do_hist = L::kHist && row_hist != nullptr;
   constexpr int kStages = L::kStages;
@@ -381,14 +381,14 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   }
 }
 
-template <int H, int KC>
-cudaError_t launch_t(const Problem &p, const CUtensorMap &tm_q,
+template <int H, int KC, bool HIST>
+cudaError_t launch_h(const Problem &p, const CUtensorMap &tm_q,
                      const CUtensorMap &tm_k, float *logits,
                      uint32_t *row_hist, int *status, int num_sms,
                      cudaStream_t st) {
   constexpr int TQ = kTileCols / H;
-  auto kern = index_scores_kernel<H, KC>;
-  const int smem = ScoreSmem<H, KC>::kAlloc;
+  auto kern = index_scores_kernel<H, KC, HIST>;
+  const int smem = ScoreSmem<H, KC, HIST>::kAlloc;
   cudaError_t e = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -399,6 +399,20 @@ cudaError_t launch_t(const Problem &p, const CUtensorMap &tm_q,
                                           row_hist, p.S, p.B, p.S_kv, p.ratio,
                                           status);
   return cudaGetLastError();
+}
+
+template <int H, int KC>
+cudaError_t launch_t(const Problem &p, const CUtensorMap &tm_q,
+                     const CUtensorMap &tm_k, float *logits,
+                     uint32_t *row_hist, int *status, int num_sms,
+                     cudaStream_t st) {
+  if constexpr (H >= 64) {
+    if (row_hist)
+      return launch_h<H, KC, true>(p, tm_q, tm_k, logits, row_hist, status,
+                                   num_sms, st);
+  }
+  return launch_h<H, KC, false>(p, tm_q, tm_k, logits, nullptr, status,
+                                num_sms, st);
 }
 
 template <int KC>
@@ -427,16 +441,22 @@ cudaError_t launch_kc(const Problem &p, const CUtensorMap &tm_q,
 
 size_t index_scores_smem_bytes(int H, int D) {
   size_t m = 0;
-#define DSA_SMEM_CASE(HH)                                                  \
-  if (H == HH)                                                             \
-    m = D <= kChunk ? ScoreSmem<HH, 1>::kAlloc : ScoreSmem<HH, 2>::kAlloc;
+#define DSA_SMEM_CASE(HH)                                           \
+  if (H == HH)                                                      \
+    m = D <= kChunk ? ScoreSmem<HH, 1, HH >= 64>::kAlloc            \
+                    : ScoreSmem<HH, 2, HH >= 64>::kAlloc;
   DSA_SMEM_CASE(1) DSA_SMEM_CASE(2) DSA_SMEM_CASE(4) DSA_SMEM_CASE(8)
   DSA_SMEM_CASE(16) DSA_SMEM_CASE(32) DSA_SMEM_CASE(64) DSA_SMEM_CASE(128)
 #undef DSA_SMEM_CASE
   return m;
 }
 
-bool index_scores_histograms(int H) { return H >= 64; }
+// Histograms pay off when the selection would otherwise stage long rows
+// (S_kv >= 8192 keys) in shared memory; for shorter rows the extra work in
+// the scoring epilogue costs more than the selection saves.
+bool index_scores_histograms(int H, int S_kv) {
+  return H >= 64 && S_kv >= 8192;
+}
 
 cudaError_t launch_index_scores(const Problem &p, const CUtensorMap &tm_q,
                                 const CUtensorMap &tm_k, float *logits,

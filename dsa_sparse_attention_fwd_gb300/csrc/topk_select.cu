@@ -584,8 +584,9 @@ struct SelLayout {
 SelLayout sel_layout(int S_kv, int topk, bool hist) {
   SelLayout l;
   // room for the candidates of a one-pass select: topk plus the rest of
-  // the threshold bucket (up to kSelSlack keys)
-  l.mcap = topk + kSelSlack < S_kv ? topk + kSelSlack : S_kv;
+  // the threshold bucket (up to kSelSlack keys, twice that for small topk)
+  const int slack = topk < 1024 ? 2 * kSelSlack : kSelSlack;
+  l.mcap = topk + slack < S_kv ? topk + slack : S_kv;
   l.bcap = l.mcap > kHistBins / 2 ? l.mcap : kHistBins / 2;
   // with precomputed row histograms the row is never staged in shared
   // memory; the region then only holds the sort's per-warp counters
@@ -597,11 +598,18 @@ SelLayout sel_layout(int S_kv, int topk, bool hist) {
   return l;
 }
 
+// Rows skip the shared-memory copy of their keys when histograms are
+// precomputed and there are enough rows that more CTAs per SM pay off; a
+// few rows (decode) keep it, so their rare fallbacks stay fast.
+bool unstaged_rows(const Problem &p, const uint32_t *row_hist) {
+  return row_hist != nullptr && (long long)p.B * p.S >= 2048;
+}
+
 template <int EPT>
 cudaError_t launch_sel(const Problem &p, const float *logits, int topk,
                        const uint32_t *row_hist, int32_t *out_idx,
                        float *out_scores, cudaStream_t st) {
-  const SelLayout l = sel_layout(p.S_kv, topk, row_hist != nullptr);
+  const SelLayout l = sel_layout(p.S_kv, topk, unstaged_rows(p, row_hist));
   auto kern = topk_select_kernel<EPT>;
   cudaError_t e = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)l.dyn);
@@ -622,7 +630,7 @@ size_t topk_select_smem_bytes(int S_kv, int topk) {
 cudaError_t launch_topk_select(const Problem &p, const float *logits, int topk,
                                const uint32_t *row_hist, int32_t *out_idx,
                                float *out_scores, cudaStream_t st) {
-  const int mcap = sel_layout(p.S_kv, topk, row_hist != nullptr).mcap;
+  const int mcap = sel_layout(p.S_kv, topk, unstaged_rows(p, row_hist)).mcap;
   if (mcap <= kSelThreads * 8)
     return launch_sel<8>(p, logits, topk, row_hist, out_idx, out_scores, st);
   if (mcap <= kSelThreads * 16)

@@ -79,9 +79,10 @@ typedef enum dsa_status {
  * Bytes of device workspace dsa_indexer_fwd() needs for this shape
  * (has_in_idx != 0 selects the given-indices path).  Returns 0 when the
  * shape is invalid.  The workspace holds a 256-byte status header followed
- * by the fp32 logits [B, S, S_kv] of the visible keys and, when H >= 64 or
- * a sequence has fewer than 256/H queries (the decode kernel), one 4096-bin
- * u32 key histogram per query row (16 KiB per row).
+ * by the fp32 logits [B, S, S_kv] of the visible keys and, when H >= 64
+ * with S_kv >= 8192 or when a sequence has fewer than 256/H queries (the
+ * decode kernel), one 4096-bin u32 key histogram per query row (16 KiB per
+ * row).
  */
 DSA_API size_t dsa_indexer_workspace_size(int S, int B, int H, int D,
                                           int S_kv, int compress_ratio,
@@ -179,9 +180,9 @@ DSA_API int dsa_selftest_wait_limit(int limit_us, void *workspace,
  * caller workspace; the caller still passes every input and output.
  *
  *   - Limit: problems whose dsa_indexer_workspace_size() exceeds
- *     DSA_STATIC_SCRATCH_BYTES (128 MiB plus a 256-byte header: e.g. the
- *     4096 x 4096 prefill's 64 MiB of logits and 64 MiB of row histograms)
- *     are refused with DSA_ERR_UNSUPPORTED before any device work.  Other
+ *     DSA_STATIC_SCRATCH_BYTES (64 MiB plus a 256-byte header: e.g. the
+ *     4096 x 4096 prefill's 64 MiB of logits, B*S*S_kv <= 16,777,216 when no
+ *     row histograms apply) are refused with DSA_ERR_UNSUPPORTED before any device work.  Other
  *     argument errors are those of dsa_indexer_fwd().
  *   - Memory: every GPU that loads this part of the library holds one copy
  *     of the array until the process exits.  No call allocates or frees
@@ -199,7 +200,7 @@ DSA_API int dsa_selftest_wait_limit(int limit_us, void *workspace,
  *     a bounded wait expired), written asynchronously on `cuda_stream`.
  * Asynchronous on `cuda_stream` like dsa_indexer_fwd().
  */
-#define DSA_STATIC_SCRATCH_BYTES ((size_t)128 * 1024 * 1024 + 256)
+#define DSA_STATIC_SCRATCH_BYTES ((size_t)64 * 1024 * 1024 + 256)
 DSA_API int dsa_indexer_fwd_static_scratch(
     const void *q, const void *k, const float *w, int S, int B, int H, int D,
     int S_kv, int compress_ratio, int topk, const int32_t *q_pos,

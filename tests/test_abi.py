@@ -85,11 +85,12 @@ def test_status_strings(lib):
 
 def test_workspace_size(lib):
     ws = lib.dsa_indexer_workspace_size
-    hist = 4096 * 4  # per-row key histogram (H >= 64 or decode shapes)
-    assert ws(4096, 1, 64, 128, 4096, 1, 2048, 0) == (256 + 4096 * 4096 * 4
-                                                      + 4096 * hist)
-    assert ws(16384, 2, 64, 128, 4096, 4, 512, 0) == (
-        256 + 2 * 16384 * 4096 * 4 + 2 * 16384 * hist)
+    hist = 4096 * 4  # per-row key histogram (decode shapes, long H >= 64)
+    assert ws(4096, 1, 64, 128, 4096, 1, 2048, 0) == 256 + 4096 * 4096 * 4
+    assert ws(16384, 2, 64, 128, 4096, 4, 512, 0) == 256 + 2 * 16384 * 4096 * 4
+    assert ws(8192, 1, 64, 128, 8192, 1, 2048, 0) == (256 + 8192 * 8192 * 4
+                                                      + 8192 * hist)
+    assert ws(8192, 1, 32, 128, 8192, 1, 2048, 0) == 256 + 8192 * 8192 * 4
     assert ws(64, 1, 16, 64, 64, 1, 8, 0) == 256 + 64 * 64 * 4  # no histograms
     assert ws(1, 64, 32, 64, 8192, 4, 512, 0) == (256 + 64 * 8192 * 4
                                                   + 64 * hist)  # decode

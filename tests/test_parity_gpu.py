@@ -313,3 +313,30 @@ def test_decode_path_match_oracle(dsa, S, B, H, D, S_kv, ratio, topk):
     assert np.array_equal(np.isneginf(L), np.isneginf(R))
     fin = np.isfinite(R)
     assert np.all(np.abs(L[fin] - R[fin]) <= score_tol(R[fin]))
+
+
+@pytest.mark.parametrize("S,B,S_kv,ratio,topk", [
+    (42, 2, 9000, 4, 512),    # ragged query tail and key tail
+    (9, 1, 8192, 1, 2048),    # exactly 64 key tiles, large topk
+])
+def test_long_rows_histogram_path(dsa, S, B, S_kv, ratio, topk):
+    """Prefill shapes with H >= 64 and S_kv >= 8192 score with the kernel that
+    also counts each row's key histogram for the selection.  Query positions
+    deep into the sequence give every row thousands of visible keys while
+    keeping the rows few enough for the oracle."""
+    H, D = 64, 128
+    wl = Workload("t", B=B, S=S, S_kv=S_kv, H=H, D=D, compress_ratio=ratio,
+                  topk=topk, w_scale=H ** -0.5, seed=S_kv + S)
+    q, k, w, _ = make_inputs(wl)
+    rng = np.random.default_rng(S)
+    pos = rng.integers(S_kv * ratio // 2, S_kv * ratio, size=B)
+    pos[-1] = S_kv * ratio - S // 2   # the last rows see every key
+    pos = torch.from_numpy(pos.astype(np.int32))
+    sc, idx, st = gpu_run(dsa, q, k, w, ratio, topk, q_pos=pos)
+    assert st == 0
+    sc = sc.reshape(B, S, topk)
+    idx = idx.reshape(B, S, topk)
+    check_invariants(sc, idx, row_nvis(S, B, ratio, S_kv, pos), topk)
+    ref = oracle.indexer_fwd(q, k, w, ratio, topk, q_pos=pos,
+                             want_logits=True)
+    compare_rows(sc, idx, ref, np.arange(B * S), S)

@@ -23,7 +23,7 @@ from tests.helpers import score_tol
 pytestmark = pytest.mark.gpu
 
 OK, UNSUPPORTED = 0, 2
-STATIC_SCRATCH_BYTES = 128 * 1024 * 1024 + 256
+STATIC_SCRATCH_BYTES = 64 * 1024 * 1024 + 256
 
 
 @pytest.fixture(scope="module")
