@@ -9,6 +9,11 @@ queries/s.  L2 is flushed (a 256 MiB write, outside the timed events)
 before every timed step.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--given-indices]
+
+`--given-indices` times the given-indices forward instead (scores gathered
+at caller-supplied indices: per row min(topk, n_vis) distinct visible keys,
+the rest -1); its TFLOP/s counts 2*H*D per valid given index.
 
 Under torchrun (N > 1) every rank runs an independent replica of the same
 workload (the forward has no exchange step); the reported value is the sum
@@ -48,6 +53,15 @@ def visible_pairs(wl, q_pos=None) -> int:
     return total
 
 
+def row_visible(wl, q_pos=None):
+    """[B, S] number of visible compressed keys of every row."""
+    import numpy as np
+    pos = np.arange(wl.S, dtype=np.int64)[None, :].repeat(wl.B, 0)
+    if q_pos is not None:
+        pos = pos + np.asarray(q_pos, dtype=np.int64)[:, None]
+    return np.clip((pos + 1) // wl.compress_ratio, 0, wl.S_kv)
+
+
 def read_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -58,25 +72,25 @@ def read_peaks():
                 "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def kernel_source_sha() -> str:
+def kernel_source_sha(kernel: str = "index_scores") -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dsa_sparse_attention_fwd_gb300", "csrc")
-    for name in ("index_scores.cu", "ptx.cuh", "common.cuh"):
+    for name in (kernel + ".cu", "ptx.cuh", "common.cuh"):
         with open(os.path.join(csrc, name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def read_traffic():
-    """DRAM bytes per launch of the scoring kernel from the committed ncu
-    summary, only if it was taken on the current kernel source."""
-    path = os.path.join(ROOT, "profiles", "index_scores_traffic.json")
+def read_traffic(kernel: str = "index_scores"):
+    """DRAM bytes per launch of a kernel from the committed ncu summary,
+    only if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_traffic.json")
     try:
         with open(path) as fh:
             d = json.load(fh)
     except (OSError, ValueError):
         return None
-    if d.get("source_sha") != kernel_source_sha():
+    if d.get("source_sha") != kernel_source_sha(kernel):
         return None
     return d.get("dram_bytes_per_launch")
 
@@ -150,7 +164,7 @@ def dist_env():
     return rank, world, local
 
 
-def cpu_oracle_sample(wl, rows_every: int):
+def cpu_oracle_sample(wl, rows_every: int, in_idx=None):
     """Time the oracle on every `rows_every`-th row (from the last row down,
     so the longest rows are in the sample)."""
     import numpy as np
@@ -162,9 +176,12 @@ def cpu_oracle_sample(wl, rows_every: int):
     oracle.build()
     t0 = time.perf_counter()
     out = oracle.indexer_fwd(q, k, w, wl.compress_ratio, wl.topk, q_pos=q_pos,
-                             rows=rows)
+                             rows=rows, in_idx=in_idx)
     dt = time.perf_counter() - t0
-    pairs = int(np.asarray(out["nvis"], dtype=np.int64).sum())
+    if in_idx is None:
+        pairs = int(np.asarray(out["nvis"], dtype=np.int64).sum())
+    else:
+        pairs = int((in_idx.reshape(-1, wl.topk)[rows] >= 0).sum())
     flops = 2.0 * wl.H * wl.D * pairs
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s",
             "cores": int(out["threads"]), "kind": "oracle",
@@ -243,7 +260,15 @@ def run_ours(args):
 
     wl = WORKLOADS[args.workload]
     q, k, w, q_pos = make_inputs(wl)
-    pairs = visible_pairs(wl, None if q_pos is None else q_pos.tolist())
+    gi = gid = None
+    if args.given_indices:
+        from dsa_inputs import make_given_indices
+        nv = row_visible(wl, None if q_pos is None else q_pos.tolist())
+        gi = make_given_indices(wl.B, wl.S, wl.topk, nv, wl.idx_seed)
+        pairs = int((gi >= 0).sum())
+        gid = gi.to(dev)
+    else:
+        pairs = visible_pairs(wl, None if q_pos is None else q_pos.tolist())
     flops = 2.0 * wl.H * wl.D * pairs
     qd, kd, wd = q.to(dev), k.to(dev), w.to(dev)
     pd = q_pos.to(dev) if q_pos is not None else None
@@ -251,15 +276,16 @@ def run_ours(args):
     out_sc = torch.empty((wl.B, wl.S, wl.topk), dtype=torch.float32,
                          device=dev)
     ws = torch.empty(dsa.dsa_indexer_workspace_size(
-        wl.S, wl.B, wl.H, wl.D, wl.S_kv, wl.compress_ratio, wl.topk),
+        wl.S, wl.B, wl.H, wl.D, wl.S_kv, wl.compress_ratio, wl.topk,
+        gi is not None),
         dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
     def step(evs=None):
         dsa.dsa_indexer_fwd(qd, kd, wd, wl.compress_ratio, wl.topk, q_pos=pd,
-                            out_idx=out_idx, out_scores=out_sc, workspace=ws,
-                            stream=stream, stage_events=evs)
+                            in_idx=gid, out_idx=out_idx, out_scores=out_sc,
+                            workspace=ws, stream=stream, stage_events=evs)
 
     for _ in range(max(args.warmup, 3)):
         flush.fill_(1.0)
@@ -308,9 +334,10 @@ def run_ours(args):
     # ---- end to end through the public call, host buffers ----
     qh, kh, wh = q.pin_memory(), k.pin_memory(), w.pin_memory()
     ph = q_pos.pin_memory() if q_pos is not None else None
+    gh = gi.pin_memory() if gi is not None else None
     for _ in range(2):
         dsa.v4_lighting_indexer(qh, kh, wh, wl.compress_ratio, wl.topk,
-                                q_pos=ph, check=False)
+                                topk_indices=gh, q_pos=ph, check=False)
     torch.cuda.synchronize()
     Ke = max(3, min(K, 50))
     e2e_ms = []
@@ -318,7 +345,8 @@ def run_ours(args):
         a, b = mk(), mk()
         a.record(stream)
         sc_h, idx_h = dsa.v4_lighting_indexer(qh, kh, wh, wl.compress_ratio,
-                                              wl.topk, q_pos=ph, check=False)
+                                              wl.topk, topk_indices=gh,
+                                              q_pos=ph, check=False)
         b.record(stream)
         b.synchronize()
         e2e_ms.append(a.elapsed_time(b))
@@ -328,7 +356,8 @@ def run_ours(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         t_e2e = float(t.item())
     h2d = q.numel() * 2 + k.numel() * 2 + w.numel() * 4 + (
-        q_pos.numel() * 4 if q_pos is not None else 0)
+        q_pos.numel() * 4 if q_pos is not None else 0) + (
+        gi.numel() * 4 if gi is not None else 0)
     d2h = sc_h.numel() * 4 + idx_h.numel() * 4
 
     if rank != 0:
@@ -338,8 +367,20 @@ def run_ours(args):
     peaks, peak_src = read_peaks()
     t_score = statistics.mean(score_ms)
     tc_peak = float(peaks["bf16_tflops"])
-    achieved = flops / (t_score * 1e-3) / 1e12
     value = world * flops / (t_step * 1e-3) / 1e12
+    # the given-indices path is one kernel when H has a gather instantiation
+    direct = gi is not None and wl.H in (16, 32, 64, 128)
+    top = "gather_scores" if direct else "index_scores"
+    if direct:
+        kernels = {"gather_scores": t_score, "step": t_step}
+        t_top, launches = t_score, 1
+    else:
+        second = "gather_logits" if gi is not None else "topk_select"
+        kernels = {"index_scores": t_score,
+                   second: statistics.mean(select_ms), "step": t_step}
+        t_top, launches = t_score, 2
+    achieved = flops / (t_top * 1e-3) / 1e12
+    name = wl.name + (" given-indices" if gi is not None else "")
     line = {
         "metric": METRIC,
         "value": value,
@@ -353,31 +394,35 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": wl.name, "desc": describe(wl),
+        "config": {"workload": name, "desc": describe(wl),
+                   "pairs": ("valid given indices" if gi is not None
+                             else "visible (query, key) pairs"),
                    "visible_pairs": pairs, "flops_per_step": flops,
                    "l2": "flushed before each step (256 MiB write, outside "
                          "the timed events)",
                    "parallelism": f"replicas x{world}"},
         "queries_per_s": world * wl.B * wl.S / (t_step * 1e-3),
         "pct_of_bf16_peak": 100.0 * value / world / tc_peak,
-        "kernels_ms": {"index_scores": t_score,
-                       "topk_select": statistics.mean(select_ms),
-                       "step": t_step},
-        "roofline": {"kernel": "index_scores", "bound": "tensor",
+        "kernels_ms": kernels,
+        "roofline": {"kernel": top, "bound": "tensor",
                      "achieved": achieved, "peak": tc_peak,
                      "unit": "TFLOP/s", "frac": achieved / tc_peak,
                      "peak_source": f"{peak_src} bf16 burst",
-                     "traffic": read_traffic()},
+                     "traffic": read_traffic(top)},
         "e2e": {"value": world * flops / (t_e2e * 1e-3) / 1e12,
                 "unit": "TFLOP/s", "ms_per_step": t_e2e,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "api": "v4_lighting_indexer(host pinned tensors)"},
-        "gpu_launches": 2 * K,
+        "gpu_launches": launches * K,
         "clocks": clocks,
         "wall_s_timed_region": wall,
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_oracle_sample(wl, 1)
+        if gi is None:
+            line["cpu_baseline"] = cpu_oracle_sample(wl, 1)
+        else:
+            every = max(1, wl.B * wl.S // 1024)
+            line["cpu_baseline"] = cpu_oracle_sample(wl, every, in_idx=gi)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -392,6 +437,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--given-indices", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

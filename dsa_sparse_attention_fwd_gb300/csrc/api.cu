@@ -130,6 +130,15 @@ int encode_k(CUtensorMap *m, const Problem &p) {
   return r == CUDA_SUCCESS ? DSA_OK : DSA_ERR_UNSUPPORTED;
 }
 
+// Given indices are scored from the gathered keys (no logits) when the
+// gather kernel has an instantiation for (H, D); otherwise the logits are
+// written and read back.
+bool gather_direct_shape(int B, int H, int D, int S_kv) {
+  (void)B;
+  (void)S_kv;
+  return dsa::gather_supported(H, D);
+}
+
 // Rows with fewer queries per sequence than one prefill tile packs (256/H)
 // go to the decode kernel, which splits each row over its keys instead.
 bool decode_shape(int S, int H, int D) {
@@ -194,9 +203,12 @@ const char *dsa_status_string(int status) {
 size_t dsa_indexer_workspace_size(int S, int B, int H, int D, int S_kv,
                                   int compress_ratio, int topk,
                                   int has_in_idx) {
-  (void)has_in_idx;
   if (check_shape(S, B, H, D, S_kv, compress_ratio) != DSA_OK) return 0;
   if (topk <= 0 || topk > DSA_MAX_TOPK) return 0;
+  if (has_in_idx)
+    return gather_direct_shape(B, H, D, S_kv)
+               ? kHeaderBytes
+               : kHeaderBytes + logits_bytes(S, B, S_kv);
   return kHeaderBytes + logits_bytes(S, B, S_kv) +
          row_hist_bytes(S, B, H, D, S_kv);
 }
@@ -257,6 +269,21 @@ int dsa_indexer_fwd_profiled(const void *q, const void *k, const float *w,
         logits_bytes(S, B, S_kv));
   if (cudaMemsetAsync(status, 0, kHeaderBytes, st) != cudaSuccess)
     return DSA_ERR_CUDA;
+  if (in_idx && gather_direct_shape(B, H, D, S_kv)) {
+    // one kernel: gathered keys -> scores at the given slots
+    if ((size_t)dev.max_smem_optin < dsa::gather_smem_bytes(H, D))
+      return DSA_ERR_UNSUPPORTED;
+    CUtensorMap tm_q;
+    rc = encode_q(&tm_q, p, 1);
+    if (rc != DSA_OK) return rc;
+    if (mark(0) != cudaSuccess) return DSA_ERR_CUDA;
+    if (dsa::launch_gather_scores(p, tm_q, in_idx, topk, out_idx,
+                                  out_scores, status, dev.num_sms,
+                                  st) != cudaSuccess)
+      return DSA_ERR_CUDA;
+    if (mark(1) != cudaSuccess || mark(2) != cudaSuccess) return DSA_ERR_CUDA;
+    return DSA_OK;
+  }
   if (row_hist && decode &&
       cudaMemsetAsync(row_hist, 0, row_hist_bytes(S, B, H, D, S_kv), st) !=
           cudaSuccess)
@@ -267,7 +294,7 @@ int dsa_indexer_fwd_profiled(const void *q, const void *k, const float *w,
   if (mark(1) != cudaSuccess) return DSA_ERR_CUDA;
   cudaError_t e;
   if (in_idx)
-    e = dsa::launch_gather_scores(p, logits, in_idx, topk, out_idx, out_scores,
+    e = dsa::launch_gather_logits(p, logits, in_idx, topk, out_idx, out_scores,
                                   status, dev.num_sms, st);
   else
     e = dsa::launch_topk_select(p, logits, topk, row_hist, out_idx,

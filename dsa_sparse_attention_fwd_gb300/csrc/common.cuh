@@ -85,10 +85,21 @@ cudaError_t launch_topk_select(const Problem &p, const float *logits, int topk,
                                float *out_scores, cudaStream_t st);
 size_t topk_select_smem_bytes(int S_kv, int topk);
 
-cudaError_t launch_gather_scores(const Problem &p, const float *logits,
+// Given indices, scores read from written logits (any H).
+cudaError_t launch_gather_logits(const Problem &p, const float *logits,
                                  const int32_t *in_idx, int topk,
                                  int32_t *out_idx, float *out_scores,
                                  int *status, int num_sms, cudaStream_t st);
+
+// Given indices, scores computed from the gathered keys on the tensor cores
+// (no logits).  tm_q: q with a box of one query.  Returns
+// cudaErrorNotSupported when (H, D) has no instantiation.
+cudaError_t launch_gather_scores(const Problem &p, const CUtensorMap &tm_q,
+                                 const int32_t *in_idx, int topk,
+                                 int32_t *out_idx, float *out_scores,
+                                 int *status, int num_sms, cudaStream_t st);
+bool gather_supported(int H, int D);
+size_t gather_smem_bytes(int H, int D);
 
 // Decode scoring (one MMA column per head of a single query); returns
 // cudaErrorNotSupported when (H, D) has no decode instantiation.

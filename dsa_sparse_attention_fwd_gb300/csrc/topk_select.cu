@@ -541,7 +541,7 @@ __global__ void __launch_bounds__(kSelThreads, 4)
   }
 }
 
-__global__ void gather_scores_kernel(const float *__restrict__ logits,
+__global__ void gather_logits_kernel(const float *__restrict__ logits,
                                      const int32_t *__restrict__ in_idx,
                                      const int32_t *__restrict__ q_pos, int S,
                                      int S_kv, int ratio, int topk,
@@ -639,7 +639,7 @@ cudaError_t launch_topk_select(const Problem &p, const float *logits, int topk,
                                          out_scores, st);
 }
 
-cudaError_t launch_gather_scores(const Problem &p, const float *logits,
+cudaError_t launch_gather_logits(const Problem &p, const float *logits,
                                  const int32_t *in_idx, int topk,
                                  int32_t *out_idx, float *out_scores,
                                  int *status, int num_sms, cudaStream_t st) {
@@ -648,7 +648,7 @@ cudaError_t launch_gather_scores(const Problem &p, const float *logits,
   const long long cap = (long long)num_sms * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  gather_scores_kernel<<<(unsigned)blocks, 256, 0, st>>>(
+  gather_logits_kernel<<<(unsigned)blocks, 256, 0, st>>>(
       logits, in_idx, p.q_pos, p.S, p.S_kv, p.ratio, topk, total, out_idx,
       out_scores, status);
   return cudaGetLastError();

@@ -94,6 +94,12 @@ def test_workspace_size(lib):
     assert ws(64, 1, 16, 64, 64, 1, 8, 0) == 256 + 64 * 64 * 4  # no histograms
     assert ws(1, 64, 32, 64, 8192, 4, 512, 0) == (256 + 64 * 8192 * 4
                                                   + 64 * hist)  # decode
+    # given indices: H in {16, 32, 64, 128} gathers keys (status header
+    # only); other H read the scores back from logits
+    assert ws(65536, 1, 64, 128, 16384, 4, 2048, 1) == 256
+    assert ws(1, 64, 16, 64, 8192, 4, 512, 1) == 256
+    assert ws(64, 1, 4, 32, 64, 1, 8, 1) == 256 + 64 * 64 * 4
+    assert ws(0, 1, 64, 128, 4096, 1, 2048, 1) == 0
     assert ws(0, 1, 64, 128, 4096, 1, 2048, 0) == 0
     assert ws(16, 1, 3, 128, 16, 1, 4, 0) == 0
     assert ws(16, 1, 4, 128, 16, 1, 0, 0) == 0
