@@ -75,7 +75,8 @@ def read_peaks():
 def kernel_source_sha(kernel: str = "index_scores") -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dsa_sparse_attention_fwd_gb300", "csrc")
-    for name in (kernel + ".cu", "ptx.cuh", "common.cuh"):
+    for name in (kernel.replace("gather_logits", "topk_select") + ".cu",
+                 "ptx.cuh", "common.cuh"):
         with open(os.path.join(csrc, name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -366,20 +367,54 @@ def run_ours(args):
 
     peaks, peak_src = read_peaks()
     t_score = statistics.mean(score_ms)
+    t_second = statistics.mean(select_ms)
     tc_peak = float(peaks["bf16_tflops"])
+    hbm_peak = float(peaks["hbm_gbs"])
     value = world * flops / (t_step * 1e-3) / 1e12
+    rows = wl.B * wl.S
     # the given-indices path is one kernel when H has a gather instantiation
     direct = gi is not None and wl.H in (16, 32, 64, 128)
-    top = "gather_scores" if direct else "index_scores"
+    decode_shape = wl.S < 256 // wl.H
+
+    def tensor_line(kernel, ms):
+        a = flops / (ms * 1e-3) / 1e12
+        return {"kernel": kernel, "bound": "tensor", "achieved": a,
+                "peak": tc_peak, "unit": "TFLOP/s", "frac": a / tc_peak,
+                "peak_source": f"{peak_src} bf16 burst",
+                "algorithmic": f"{flops:.4g} FLOP per launch (2*H*D per pair)",
+                "traffic": read_traffic(kernel)}
+
+    def hbm_line(kernel, ms, nbytes, what):
+        a = nbytes / (ms * 1e-3) / 1e9
+        return {"kernel": kernel, "bound": "hbm", "achieved": a,
+                "peak": hbm_peak, "unit": "GB/s", "frac": a / hbm_peak,
+                "peak_source": f"{peak_src} copy bandwidth",
+                "algorithmic": f"{nbytes:.4g} B per launch ({what})",
+                "traffic": read_traffic(kernel)}
+
     if direct:
         kernels = {"gather_scores": t_score, "step": t_step}
-        t_top, launches = t_score, 1
+        rooflines = {"gather_scores": tensor_line("gather_scores", t_score)}
+        launches = 1
     else:
+        if decode_shape and gi is None:
+            sname = "decode_scores"
+            kbytes = pairs * wl.D * 2 + rows * (wl.H * wl.D * 2 + wl.H * 4)
+            first = hbm_line(sname, t_score, kbytes, "visible k rows + q + w")
+        else:
+            sname = "index_scores"
+            first = tensor_line(sname, t_score)
         second = "gather_logits" if gi is not None else "topk_select"
-        kernels = {"index_scores": t_score,
-                   second: statistics.mean(select_ms), "step": t_step}
-        t_top, launches = t_score, 2
-    achieved = flops / (t_top * 1e-3) / 1e12
+        # the selection reads each visible logit once and writes the outputs
+        sbytes = (pairs * 4 if gi is None else gi.numel() * 4 * 2) + \
+            rows * wl.topk * 8
+        kernels = {sname: t_score, second: t_second, "step": t_step}
+        rooflines = {sname: first,
+                     second: hbm_line(second, t_second, sbytes,
+                                      "visible logits read + idx/scores "
+                                      "written")}
+        launches = 2
+    top = max((k for k in kernels if k != "step"), key=lambda k: kernels[k])
     name = wl.name + (" given-indices" if gi is not None else "")
     line = {
         "metric": METRIC,
@@ -404,11 +439,8 @@ def run_ours(args):
         "queries_per_s": world * wl.B * wl.S / (t_step * 1e-3),
         "pct_of_bf16_peak": 100.0 * value / world / tc_peak,
         "kernels_ms": kernels,
-        "roofline": {"kernel": top, "bound": "tensor",
-                     "achieved": achieved, "peak": tc_peak,
-                     "unit": "TFLOP/s", "frac": achieved / tc_peak,
-                     "peak_source": f"{peak_src} bf16 burst",
-                     "traffic": read_traffic(top)},
+        "roofline": rooflines[top],
+        "rooflines": rooflines,
         "e2e": {"value": world * flops / (t_e2e * 1e-3) / 1e12,
                 "unit": "TFLOP/s", "ms_per_step": t_e2e,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
