@@ -78,11 +78,14 @@ typedef enum dsa_status {
 /*
  * Bytes of device workspace dsa_indexer_fwd() needs for this shape
  * (has_in_idx != 0 selects the given-indices path).  Returns 0 when the
- * shape is invalid.  The workspace holds a 256-byte status header followed
- * by the fp32 logits [B, S, S_kv] of the visible keys and, when H >= 64
- * with S_kv >= 8192 or when a sequence has fewer than 256/H queries (the
- * decode kernel), one 4096-bin u32 key histogram per query row (16 KiB per
- * row).
+ * shape is invalid.  The workspace starts with a 256-byte status header.
+ * Top-k path: the header is followed by the fp32 logits [B, S, S_kv] of the
+ * visible keys and, when H >= 64 with S_kv >= 8192 or when a sequence has
+ * fewer than 256/H queries (the decode kernel), one 4096-bin u32 key
+ * histogram per query row (16 KiB per row).
+ * Given-indices path: H in {16, 32, 64, 128} scores the gathered keys
+ * directly and needs the header only; other H take the header plus the
+ * logits.
  */
 DSA_API size_t dsa_indexer_workspace_size(int S, int B, int H, int D,
                                           int S_kv, int compress_ratio,
@@ -105,6 +108,8 @@ DSA_API size_t dsa_indexer_workspace_size(int S, int B, int H, int D,
  * in_idx != NULL: out_idx is a copy of in_idx; out_scores holds the score at
  * each given index, or -inf where the index is -1, not visible, or outside
  * [0, S_kv) (the latter also sets DSA_ERR_INDEX_RANGE in the status word).
+ * Each slot is scored on its own: repeated indices repeat the score, order
+ * is kept.  No alignment is asked of w or in_idx beyond their element size.
  *
  * Returns DSA_OK once the work is enqueued, else the synchronous error.
  */
