@@ -160,7 +160,9 @@ __device__ __forceinline__ void lsd_dispatch(const uint64_t *src,
   if (ept <= 2) return lsd_pass<2>(src, dst, m, shift, sh);
   if (ept <= 4) return lsd_pass<4>(src, dst, m, shift, sh);
   if (EMAX <= 8 || ept <= 8) return lsd_pass<(EMAX < 8 ? EMAX : 8)>(src, dst, m, shift, sh);
-  if (EMAX <= 12 || ept <= 12) return lsd_pass<(EMAX < 12 ? EMAX : 12)>(src, dst, m, shift, sh);
+  // covers the topk + slack candidates of a one-pass select (2304 for
+  // topk 2048)
+  if (EMAX <= 10 || ept <= 10) return lsd_pass<(EMAX < 10 ? EMAX : 10)>(src, dst, m, shift, sh);
   if (EMAX <= 16 || ept <= 16) return lsd_pass<(EMAX < 16 ? EMAX : 16)>(src, dst, m, shift, sh);
   if (EMAX <= 24 || ept <= 24) return lsd_pass<(EMAX < 24 ? EMAX : 24)>(src, dst, m, shift, sh);
   return lsd_pass<EMAX>(src, dst, m, shift, sh);
