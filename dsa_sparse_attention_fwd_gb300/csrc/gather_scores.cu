@@ -122,14 +122,6 @@ __device__ __forceinline__ bool gat_next(GatCursor &c, const GatGeom &g) {
   return true;
 }
 
-// One cp.async of 16 bytes; src_bytes < 16 fills the rest with zeros.
-__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void *src,
-                                                 uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst),
-               "l"(src), "r"(src_bytes)
-               : "memory");
-}
-
 template <int H, int KC>
 __global__ void __launch_bounds__(GatRoles<H>::kThreads, 1)
     gather_scores_kernel(const __grid_constant__ CUtensorMap tm_q,

@@ -113,6 +113,15 @@ __device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
                : "memory");
 }
 
+// One cp.async of 16 bytes global -> shared; src_bytes < 16 fills the rest
+// with zeros (src_bytes = 0 reads nothing).
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void *src,
+                                                 uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst),
+               "l"(src), "r"(src_bytes)
+               : "memory");
+}
+
 // Arrive on `bar` once every cp.async this thread issued so far has landed
 // (the arrival is counted in the barrier's initial count).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
