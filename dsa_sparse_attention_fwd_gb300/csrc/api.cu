@@ -298,7 +298,7 @@ int dsa_indexer_fwd_profiled(const void *q, const void *k, const float *w,
                                   status, dev.num_sms, st);
   else
     e = dsa::launch_topk_select(p, logits, topk, row_hist, out_idx,
-                                out_scores, st);
+                                out_scores, dev.num_sms, st);
   if (e != cudaSuccess) return DSA_ERR_CUDA;
   if (mark(2) != cudaSuccess) return DSA_ERR_CUDA;
   return DSA_OK;

@@ -60,7 +60,7 @@ constexpr int kTileKeys = 128;      // MMA M: compressed keys per tile
 constexpr int kTileCols = 256;      // MMA N: (query, head) columns per tile
 constexpr int kChunk = 64;          // bf16 per 128-byte swizzled row
 constexpr int kScoreThreads = 320;  // TMA warp, MMA warp, 8 epilogue warps
-constexpr int kDecChunkTiles = 2;   // decode: key tiles per work item
+constexpr int kDecChunkTiles = 4;   // decode: key tiles per work item
 
 // Top-k selection: a sort pass handles up to 256 threads x (this + 2)
 // elements, i.e. topk + 256 candidates with topk <= 256 * DSA_SEL_MAX_EPT
@@ -82,7 +82,8 @@ bool index_scores_histograms(int H, int S_kv);
 // kernel, or nullptr (the selection then builds its own).
 cudaError_t launch_topk_select(const Problem &p, const float *logits, int topk,
                                const uint32_t *row_hist, int32_t *out_idx,
-                               float *out_scores, cudaStream_t st);
+                               float *out_scores, int num_sms,
+                               cudaStream_t st);
 size_t topk_select_smem_bytes(int S_kv, int topk);
 
 // Given indices, scores read from written logits (any H).

@@ -2,34 +2,39 @@
 // sorted by descending score with equal scores ordered by ascending key
 // index; the rest of the row is -1 / -inf.
 //
-// One CTA (8 warps) per row.  The row's n visible fp32 scores are staged in
-// shared memory as order-preserving unsigned keys (larger float <-> larger
-// key; -0.0 folded onto +0.0 so the index tie-break decides between them).
-//   1. When n > topk, a most-significant-digit-first radix select finds T,
-//      the topk-th largest key, in three histogram passes (12, 12 and 8
-//      bits; the first 12 bits are the sign, the exponent and three mantissa
-//      bits, which spreads typical scores over many bins).  An ordered
-//      two-walk compaction then keeps every key > T and the lowest-index
-//      keys == T, in index order.
+// One CTA per row: 256 threads when there are many rows, 1024 when there
+// are fewer rows than SMs.  Scores are compared as order-preserving unsigned
+// keys (larger float <-> larger key; -0.0 folded onto +0.0 so the index
+// tie-break decides between them).
+//   1. n <= topk: every visible key is a candidate.
+//      n > topk: a 4096-bin histogram of the top 12 key bits (the sign, the
+//      exponent and three mantissa bits) -- the scoring kernel's, or one
+//      built here from the row staged in shared memory -- gives the bucket
+//      holding the topk-th largest key.  If the keys in and above that
+//      bucket fit topk plus a slack, one pass keeps them all (in any
+//      order); otherwise two more passes (12 and 8 bits) find the exact
+//      threshold T and an ordered compaction keeps every key > T and the
+//      lowest-index keys == T.
 //   2. A stable least-significant-digit radix sort (8-bit digits,
-//      descending) orders the m = min(n, topk) survivors, packed as
-//      (key << 32 | j), on the top 16 key bits only.  Within a warp, equal
-//      digits are ranked with eight ballots (one per digit bit), so the rank
-//      follows element order and the sort is stable; stability keeps equal
-//      keys in index order, which is the "lower index first" tie rule.
-//      Digit positions on which every survivor agrees (found by an AND/OR
-//      reduction) are skipped.
-//   3. Runs of equal top 16 bits (a few elements for real score
-//      distributions) are ordered by the low 16 bits by counting inside the
-//      run.  If any run is longer than 32 (heavily tied inputs), the
-//      candidates are rebuilt and sorted on all four digits instead.
+//      descending) orders the m candidates, packed as (key << 32 | j), on
+//      key bits 8..31.  Within a warp, equal digits are ranked from a peer
+//      mask (eight ballots or one match instruction), so ranks follow
+//      element order and the sort is stable.  Digit positions on which every
+//      candidate agrees (an AND/OR reduction) are skipped.
+//   3. Runs of equal top 24 bits (a few elements for real score
+//      distributions) are ordered by (low 8 bits desc, index asc) by
+//      counting inside the run, which also fixes the order of candidates
+//      kept out of index order in step 1.  If a run is longer than 32
+//      (heavily tied inputs), the candidates are rebuilt and sorted on all
+//      four digits instead.
 #include "common.cuh"
 
 namespace dsa {
 namespace {
 
-constexpr int kSelThreads = 256;
-constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kSelThreads = 256;       // threads per row, many rows
+constexpr int kSelThreadsWide = 1024;  // threads per row, few rows
+constexpr int kSelMaxWarps = kSelThreadsWide / 32;
 constexpr int kHistBins = 4096;  // 12-bit select digit
 constexpr int kSelSlack = 256;   // extra candidates a one-pass select keeps
 
@@ -63,15 +68,16 @@ struct SelShared {
   uint32_t (*whist)[256];          // per-warp digit counts / offsets; lives
                                    // in the row-key buffer, dead by then
   uint32_t dbase[256];             // digit bases of a sort pass
-  uint32_t wsum[kSelWarps];
-  uint32_t wgt[kSelWarps], weq[kSelWarps];
-  uint32_t wand[kSelWarps], wor[kSelWarps];
+  uint32_t wsum[kSelMaxWarps];
+  uint32_t wgt[kSelMaxWarps], weq[kSelMaxWarps];
+  uint32_t wand[kSelMaxWarps], wor[kSelMaxWarps];
   uint32_t sel_digit, sel_above, sel_count;
   uint32_t cursor;
   int overflow;
 };
 
-// Exclusive prefix sum of one value per thread over the 256-thread block.
+// Exclusive prefix sum of one value per thread over the NT-thread block.
+template <int NT>
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, SelShared &sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t incl = v;
@@ -84,7 +90,7 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, SelShared &sh) {
   __syncthreads();
   uint32_t pre = 0;
 #pragma unroll
-  for (int w = 0; w < kSelWarps; ++w)
+  for (int w = 0; w < NT / 32; ++w)
     if (w < warp) pre += sh.wsum[w];
   __syncthreads();  // wsum may be rewritten by the next scan
   return pre + incl - v;
@@ -94,7 +100,7 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, SelShared &sh) {
 // (key >> shift) & 255, descending.  Warp w ranks the contiguous elements
 // [32*E*w, 32*E*(w+1)); E is the smallest instantiated count that covers m,
 // so no iteration runs past the data (warps past the end skip the loops).
-template <int E>
+template <int E, int NT>
 __device__ __forceinline__ void lsd_pass(const uint64_t *src, uint64_t *dst,
                                          int m, int shift, SelShared &sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -124,15 +130,18 @@ __device__ __forceinline__ void lsd_pass(const uint64_t *src, uint64_t *dst,
   }
   __syncthreads();
   {
-    const int d = threadIdx.x;  // 256 threads, one digit each
+    const int d = threadIdx.x;  // the first 256 threads, one digit each
     uint32_t run = 0;
+    if (d < 256) {
 #pragma unroll
-    for (int w = 0; w < kSelWarps; ++w) {
-      const uint32_t c = sh.whist[w][d];
-      sh.whist[w][d] = run;
-      run += c;
+      for (int w = 0; w < NT / 32; ++w) {
+        const uint32_t c = sh.whist[w][d];
+        sh.whist[w][d] = run;
+        run += c;
+      }
     }
-    sh.dbase[d] = block_excl_scan(run, sh);
+    const uint32_t dbase = block_excl_scan<NT>(run, sh);
+    if (d < 256) sh.dbase[d] = dbase;
   }
   __syncthreads();
   if (active) {
@@ -151,21 +160,21 @@ __device__ __forceinline__ void lsd_pass(const uint64_t *src, uint64_t *dst,
 
 // Runs one pass with the smallest element count per lane that covers m
 // (at most EMAX, the kernel's instantiation limit).
-template <int EMAX>
+template <int EMAX, int NT>
 __device__ __forceinline__ void lsd_dispatch(const uint64_t *src,
                                              uint64_t *dst, int m, int shift,
                                              SelShared &sh) {
-  const int ept = (m + kSelThreads - 1) / kSelThreads;
-  if (ept <= 1) return lsd_pass<1>(src, dst, m, shift, sh);
-  if (ept <= 2) return lsd_pass<2>(src, dst, m, shift, sh);
-  if (ept <= 4) return lsd_pass<4>(src, dst, m, shift, sh);
-  if (EMAX <= 8 || ept <= 8) return lsd_pass<(EMAX < 8 ? EMAX : 8)>(src, dst, m, shift, sh);
+  const int ept = (m + NT - 1) / NT;
+  if (ept <= 1) return lsd_pass<1, NT>(src, dst, m, shift, sh);
+  if (ept <= 2) return lsd_pass<2, NT>(src, dst, m, shift, sh);
+  if (ept <= 4) return lsd_pass<4, NT>(src, dst, m, shift, sh);
+  if (EMAX <= 8 || ept <= 8) return lsd_pass<(EMAX < 8 ? EMAX : 8), NT>(src, dst, m, shift, sh);
   // covers the topk + slack candidates of a one-pass select (2304 for
   // topk 2048)
-  if (EMAX <= 10 || ept <= 10) return lsd_pass<(EMAX < 10 ? EMAX : 10)>(src, dst, m, shift, sh);
-  if (EMAX <= 16 || ept <= 16) return lsd_pass<(EMAX < 16 ? EMAX : 16)>(src, dst, m, shift, sh);
-  if (EMAX <= 24 || ept <= 24) return lsd_pass<(EMAX < 24 ? EMAX : 24)>(src, dst, m, shift, sh);
-  return lsd_pass<EMAX>(src, dst, m, shift, sh);
+  if (EMAX <= 10 || ept <= 10) return lsd_pass<(EMAX < 10 ? EMAX : 10), NT>(src, dst, m, shift, sh);
+  if (EMAX <= 16 || ept <= 16) return lsd_pass<(EMAX < 16 ? EMAX : 16), NT>(src, dst, m, shift, sh);
+  if (EMAX <= 24 || ept <= 24) return lsd_pass<(EMAX < 24 ? EMAX : 24), NT>(src, dst, m, shift, sh);
+  return lsd_pass<EMAX, NT>(src, dst, m, shift, sh);
 }
 
 // Fix-up after sorting on the top 24 key bits: inside each run of equal top
@@ -175,12 +184,13 @@ __device__ __forceinline__ void lsd_dispatch(const uint64_t *src,
 // dst is incomplete and the caller falls back to a full sort.
 constexpr int kRunLimit = 32;
 
+template <int NT>
 __device__ __forceinline__ bool run_fixup(const uint64_t *src, uint64_t *dst,
                                           int m, SelShared &sh) {
   if (threadIdx.x == 0) sh.overflow = 0;
   __syncthreads();
   bool over = false;
-  for (int i = threadIdx.x; i < m; i += kSelThreads) {
+  for (int i = threadIdx.x; i < m; i += NT) {
     const uint64_t v = src[i];
     const uint32_t top = (uint32_t)(v >> 40);
     const uint32_t low = (uint32_t)(v >> 32) & 0xFFu;
@@ -221,8 +231,8 @@ __device__ __forceinline__ bool run_fixup(const uint64_t *src, uint64_t *dst,
   return any;
 }
 
-template <int EPT>
-__global__ void __launch_bounds__(kSelThreads, 4)
+template <int EPT, int NT>
+__global__ void __launch_bounds__(NT, NT == kSelThreads ? 4 : 1)
     topk_select_kernel(const float *__restrict__ logits,
                        const uint32_t *__restrict__ row_hist,
                        const int32_t *__restrict__ q_pos, int S, int S_kv,
@@ -259,31 +269,31 @@ __global__ void __launch_bounds__(kSelThreads, 4)
   // row loads keep four independent global loads in flight per thread
   auto load_keys = [&]() {
     if (!staged) return;
-    for (int j0 = tid; j0 < nv; j0 += 4 * kSelThreads) {
+    for (int j0 = tid; j0 < nv; j0 += 4 * NT) {
       float v[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int j = j0 + u * kSelThreads;
+        const int j = j0 + u * NT;
         v[u] = j < nv ? __ldg(L + j) : 0.f;
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int j = j0 + u * kSelThreads;
+        const int j = j0 + u * NT;
         if (j < nv && staged) keys[j] = ordered_key(v[u]);
       }
     }
   };
   auto load_all = [&]() {
-    for (int j0 = tid; j0 < nv; j0 += 4 * kSelThreads) {
+    for (int j0 = tid; j0 < nv; j0 += 4 * NT) {
       float v[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int j = j0 + u * kSelThreads;
+        const int j = j0 + u * NT;
         v[u] = j < nv ? __ldg(L + j) : 0.f;
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int j = j0 + u * kSelThreads;
+        const int j = j0 + u * NT;
         if (j < nv)
           bufA[j] = ((uint64_t)ordered_key(v[u]) << 32) | (uint32_t)j;
       }
@@ -293,7 +303,7 @@ __global__ void __launch_bounds__(kSelThreads, 4)
   // ordered compaction, two walks over contiguous warp segments
   auto compact = [&]() {
     __syncthreads();
-    const int seg = ((nv + kSelThreads - 1) / kSelThreads) * 32;
+    const int seg = ((nv + NT - 1) / NT) * 32;
     const int lo = warp * seg, hi = min(nv, lo + seg);
     uint32_t cgt = 0, ceq = 0;
     for (int c = lo; c < lo + seg; c += 32) {
@@ -340,8 +350,8 @@ __global__ void __launch_bounds__(kSelThreads, 4)
     // the scoring kernel already counted this row's top 12 key bits: find
     // the threshold bucket there and compact straight from the logits
     const uint32_t *gh = row_hist + (size_t)row * kRowHistBins;
-    constexpr int per = kRowHistBins / kSelThreads;
-    const int o = kSelThreads - 1 - tid;
+    constexpr int per = kRowHistBins / NT;
+    const int o = NT - 1 - tid;
     uint32_t c[per];
     uint32_t lsum = 0;
 #pragma unroll
@@ -349,7 +359,7 @@ __global__ void __launch_bounds__(kSelThreads, 4)
       c[i] = __ldg(gh + o * per + i);
       lsum += c[i];
     }
-    const uint32_t above = block_excl_scan(lsum, sh);
+    const uint32_t above = block_excl_scan<NT>(lsum, sh);
     if (above < (uint32_t)topk && (uint32_t)topk <= above + lsum) {
       uint32_t run = above;
       for (int i = per - 1; i >= 0; --i) {
@@ -376,16 +386,16 @@ __global__ void __launch_bounds__(kSelThreads, 4)
       m = n_gt;
       if (tid == 0) sh.cursor = 0;
       __syncthreads();
-      for (int c0 = 0; c0 < nv; c0 += 4 * kSelThreads) {
+      for (int c0 = 0; c0 < nv; c0 += 4 * NT) {
         float v[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int j = c0 + u * kSelThreads + tid;
+          const int j = c0 + u * NT + tid;
           v[u] = j < nv ? __ldg(L + j) : 0.f;
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int j = c0 + u * kSelThreads + tid;
+          const int j = c0 + u * NT + tid;
           const uint32_t key = ordered_key(v[u]);
           const bool keep = j < nv && key >= T;
           const uint32_t bal = __ballot_sync(0xffffffffu, keep);
@@ -414,22 +424,28 @@ __global__ void __launch_bounds__(kSelThreads, 4)
     for (int pass = 0; pass < 3; ++pass) {
       const int shift = pass == 0 ? 20 : (pass == 1 ? 8 : 0);
       const int bits = pass == 2 ? 8 : 12;
-      const int nb = 1 << bits, per = nb / kSelThreads;
+      const int nb = 1 << bits;
+      // bins per owning thread; with fewer bins than threads, the first nb
+      // threads own one bin each
+      const int per = nb >= NT ? nb / NT : 1, owners = nb / per;
       const uint32_t dmask = (uint32_t)nb - 1u;
-      for (int i = tid; i < nb; i += kSelThreads) hist[i] = 0;
+      for (int i = tid; i < nb; i += NT) hist[i] = 0;
       __syncthreads();
-      for (int j = tid; j < nv; j += kSelThreads) {
+      for (int j = tid; j < nv; j += NT) {
         const uint32_t u = key_at(j);
         if ((u & pmask) == prefix) atomicAdd(&hist[(u >> shift) & dmask], 1u);
       }
       __syncthreads();
-      // thread t owns bins [o*per, o*per+per) with o = 255 - t, so an
-      // exclusive scan in thread order counts the bins above its own
-      const int o = kSelThreads - 1 - tid;
+      // thread t < owners owns bins [o*per, o*per+per) with
+      // o = owners - 1 - t, so an exclusive scan in thread order counts the
+      // bins above its own
+      const int o = owners - 1 - tid;
       uint32_t lsum = 0;
-      for (int i = 0; i < per; ++i) lsum += hist[o * per + i];
-      const uint32_t above = block_excl_scan(lsum, sh);
-      if (above < (uint32_t)need && (uint32_t)need <= above + lsum) {
+      if (o >= 0)
+        for (int i = 0; i < per; ++i) lsum += hist[o * per + i];
+      const uint32_t above = block_excl_scan<NT>(lsum, sh);
+      if (o >= 0 && above < (uint32_t)need &&
+          (uint32_t)need <= above + lsum) {
         uint32_t run = above;
         for (int i = per - 1; i >= 0; --i) {
           const uint32_t c = hist[o * per + i];
@@ -471,7 +487,7 @@ __global__ void __launch_bounds__(kSelThreads, 4)
 
   // ---- bits on which the survivors differ ----
   uint32_t kand = 0xffffffffu, kor = 0u;
-  for (int i = tid; i < m; i += kSelThreads) {
+  for (int i = tid; i < m; i += NT) {
     const uint32_t k = (uint32_t)(bufA[i] >> 32);
     kand &= k;
     kor |= k;
@@ -488,7 +504,7 @@ __global__ void __launch_bounds__(kSelThreads, 4)
   __syncthreads();
   uint32_t all_and = 0xffffffffu, all_or = 0u;
 #pragma unroll
-  for (int w = 0; w < kSelWarps; ++w) {
+  for (int w = 0; w < (NT / 32); ++w) {
     all_and &= sh.wand[w];
     all_or |= sh.wor[w];
   }
@@ -499,13 +515,13 @@ __global__ void __launch_bounds__(kSelThreads, 4)
   uint64_t *cur = bufA, *alt = bufB;
   for (int shift = 8; shift < 32; shift += 8) {
     if (((diff >> shift) & 255u) == 0u) continue;  // every digit equal
-    lsd_dispatch<EPT>(cur, alt, m, shift, sh);
+    lsd_dispatch<EPT, NT>(cur, alt, m, shift, sh);
     uint64_t *t = cur;
     cur = alt;
     alt = t;
   }
   if ((diff & 0xFFu) != 0u || unordered) {
-    if (!run_fixup(cur, alt, m, sh)) {
+    if (!run_fixup<NT>(cur, alt, m, sh)) {
       uint64_t *t = cur;
       cur = alt;
       alt = t;
@@ -521,7 +537,7 @@ __global__ void __launch_bounds__(kSelThreads, 4)
       alt = bufB;
       for (int shift = 0; shift < 32; shift += 8) {
         if (((diff >> shift) & 255u) == 0u) continue;
-        lsd_dispatch<EPT>(cur, alt, m, shift, sh);
+        lsd_dispatch<EPT, NT>(cur, alt, m, shift, sh);
         uint64_t *t = cur;
         cur = alt;
         alt = t;
@@ -531,7 +547,7 @@ __global__ void __launch_bounds__(kSelThreads, 4)
 
   int32_t *oi = out_idx + (size_t)row * topk;
   float *os = out_scores + (size_t)row * topk;
-  for (int i = tid; i < topk; i += kSelThreads) {
+  for (int i = tid; i < topk; i += NT) {
     if (i < m) {  // m >= topk or m = n_visible < topk
       const uint64_t c = cur[i];
       oi[i] = (int32_t)(uint32_t)c;
@@ -583,7 +599,7 @@ struct SelLayout {
   size_t dyn;
 };
 
-SelLayout sel_layout(int S_kv, int topk, bool hist) {
+SelLayout sel_layout(int S_kv, int topk, bool hist, int threads) {
   SelLayout l;
   // room for the candidates of a one-pass select: topk plus the rest of
   // the threshold bucket (up to kSelSlack keys, twice that for small topk)
@@ -593,7 +609,7 @@ SelLayout sel_layout(int S_kv, int topk, bool hist) {
   // with precomputed row histograms the row is never staged in shared
   // memory; the region then only holds the sort's per-warp counters
   const size_t key_bytes = hist ? 0 : (size_t)S_kv * 4;
-  const size_t whist_bytes = (size_t)kSelWarps * 256 * 4;
+  const size_t whist_bytes = (size_t)(threads / 32) * 256 * 4;
   l.keys_cap = hist ? 0 : S_kv;
   l.dyn = (size_t)(l.mcap + l.bcap) * 8 +
           (key_bytes > whist_bytes ? key_bytes : whist_bytes);
@@ -607,17 +623,17 @@ bool unstaged_rows(const Problem &p, const uint32_t *row_hist) {
   return row_hist != nullptr && (long long)p.B * p.S >= 2048;
 }
 
-template <int EPT>
+template <int EPT, int NT>
 cudaError_t launch_sel(const Problem &p, const float *logits, int topk,
                        const uint32_t *row_hist, int32_t *out_idx,
                        float *out_scores, cudaStream_t st) {
-  const SelLayout l = sel_layout(p.S_kv, topk, unstaged_rows(p, row_hist));
-  auto kern = topk_select_kernel<EPT>;
+  const SelLayout l = sel_layout(p.S_kv, topk, unstaged_rows(p, row_hist), NT);
+  auto kern = topk_select_kernel<EPT, NT>;
   cudaError_t e = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)l.dyn);
   if (e != cudaSuccess) return e;
   const long long rows = (long long)p.B * p.S;
-  kern<<<(unsigned)rows, kSelThreads, l.dyn, st>>>(
+  kern<<<(unsigned)rows, NT, l.dyn, st>>>(
       logits, row_hist, p.q_pos, p.S, p.S_kv, p.ratio, topk, l.mcap, l.bcap,
       l.keys_cap, out_idx, out_scores);
   return cudaGetLastError();
@@ -626,19 +642,34 @@ cudaError_t launch_sel(const Problem &p, const float *logits, int topk,
 }  // namespace
 
 size_t topk_select_smem_bytes(int S_kv, int topk) {
-  return sel_layout(S_kv, topk, false).dyn + sizeof(SelShared);
+  return sel_layout(S_kv, topk, false, kSelThreads).dyn + sizeof(SelShared);
 }
+
+// Shared memory the wide (1024-thread) variant may take: its per-warp sort
+// counters need 32 KB, which the key region usually covers already.
+constexpr size_t kWideSmemCap = 160 * 1024;
 
 cudaError_t launch_topk_select(const Problem &p, const float *logits, int topk,
                                const uint32_t *row_hist, int32_t *out_idx,
-                               float *out_scores, cudaStream_t st) {
-  const int mcap = sel_layout(p.S_kv, topk, unstaged_rows(p, row_hist)).mcap;
+                               float *out_scores, int num_sms,
+                               cudaStream_t st) {
+  const bool unstaged = unstaged_rows(p, row_hist);
+  const int mcap = sel_layout(p.S_kv, topk, unstaged, kSelThreads).mcap;
+  // Fewer rows than SMs: each row gets 1024 threads, so a row's passes
+  // take a quarter of the iterations (the rows run side by side anyway).
+  const long long rows = (long long)p.B * p.S;
+  if (rows < num_sms && mcap <= kSelThreadsWide * 4 &&
+      sel_layout(p.S_kv, topk, unstaged, kSelThreadsWide).dyn <= kWideSmemCap)
+    return launch_sel<4, kSelThreadsWide>(p, logits, topk, row_hist, out_idx,
+                                          out_scores, st);
   if (mcap <= kSelThreads * 8)
-    return launch_sel<8>(p, logits, topk, row_hist, out_idx, out_scores, st);
+    return launch_sel<8, kSelThreads>(p, logits, topk, row_hist, out_idx,
+                                      out_scores, st);
   if (mcap <= kSelThreads * 16)
-    return launch_sel<16>(p, logits, topk, row_hist, out_idx, out_scores, st);
-  return launch_sel<DSA_SEL_MAX_EPT + 2>(p, logits, topk, row_hist, out_idx,
-                                         out_scores, st);
+    return launch_sel<16, kSelThreads>(p, logits, topk, row_hist, out_idx,
+                                       out_scores, st);
+  return launch_sel<DSA_SEL_MAX_EPT + 2, kSelThreads>(
+      p, logits, topk, row_hist, out_idx, out_scores, st);
 }
 
 cudaError_t launch_gather_logits(const Problem &p, const float *logits,

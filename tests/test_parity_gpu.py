@@ -340,3 +340,29 @@ def test_long_rows_histogram_path(dsa, S, B, S_kv, ratio, topk):
     ref = oracle.indexer_fwd(q, k, w, ratio, topk, q_pos=pos,
                              want_logits=True)
     compare_rows(sc, idx, ref, np.arange(B * S), S)
+
+
+@pytest.mark.parametrize("topk,distinct_keys", [(7, None), (100, None),
+                                                (300, None), (100, 8),
+                                                (300, 8)])
+def test_integer_inputs_bit_exact_few_rows(dsa, topk, distinct_keys):
+    """Fewer rows than SMs take the 1024-thread selection.  Integer q, k and
+    dyadic w make every score exact and produce runs of tied scores; with
+    only 8 distinct key vectors the runs exceed the fix-up's limit and the
+    full-sort fallback runs.  Order must match the oracle exactly."""
+    rng = np.random.default_rng(topk)
+    S, B, S_kv, H, D = 40, 2, 400, 16, 32
+    qi = rng.integers(-2, 3, size=(S, B, H, D)).astype(np.float32)
+    ki = rng.integers(-2, 3, size=(S_kv, B, D)).astype(np.float32)
+    if distinct_keys:
+        ki = ki[np.arange(S_kv) % distinct_keys]
+    wi = rng.choice([1, -1, 0.5, -0.5], size=(S, B, H)).astype(np.float32)
+    q = torch.from_numpy(qi).to(torch.bfloat16)
+    k = torch.from_numpy(ki).to(torch.bfloat16)
+    w = torch.from_numpy(wi)
+    pos = torch.tensor([200, 355], dtype=torch.int32)
+    sc, idx, st = gpu_run(dsa, q, k, w, 1, topk, q_pos=pos)
+    assert st == 0
+    ref = oracle.indexer_fwd(q, k, w, 1, topk, q_pos=pos)
+    np.testing.assert_array_equal(idx.reshape(-1, topk), ref["idx"])
+    np.testing.assert_array_equal(sc.reshape(-1, topk), ref["scores"])
