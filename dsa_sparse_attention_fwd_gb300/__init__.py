@@ -27,7 +27,8 @@ __all__ = [
     "DsaError", "load_library", "build", "dsa_indexer_workspace_size",
     "dsa_indexer_fwd", "dsa_indexer_logits", "dsa_indexer_check",
     "dsa_status_string", "dsa_selftest_wait_limit", "v4_lighting_indexer",
-    "indexer_logits", "STATUS",
+    "indexer_logits", "dsa_indexer_host_buffer_size", "dsa_indexer_fwd_host",
+    "STATUS",
 ]
 
 STATUS = {
@@ -81,6 +82,11 @@ def load_library(path: str | None = None):
         lib.dsa_status_string.argtypes = [I]
         lib.dsa_selftest_wait_limit.restype = I
         lib.dsa_selftest_wait_limit.argtypes = [I, P, Z, P]
+        lib.dsa_indexer_host_buffer_size.restype = Z
+        lib.dsa_indexer_host_buffer_size.argtypes = [I] * 8
+        lib.dsa_indexer_fwd_host.restype = I
+        lib.dsa_indexer_fwd_host.argtypes = [P, P, P, I, I, I, I, I, I, I, P,
+                                             P, P, P, P, Z, P]
         _lib = lib
         return lib
 
@@ -201,6 +207,54 @@ def dsa_selftest_wait_limit(limit_us: int, workspace, stream=None) -> int:
         int(limit_us), _ptr(workspace), workspace.numel(), _stream(stream)))
 
 
+def dsa_indexer_host_buffer_size(S, B, H, D, S_kv, compress_ratio, topk,
+                                 has_in_idx=False) -> int:
+    return int(load_library().dsa_indexer_host_buffer_size(
+        S, B, H, D, S_kv, compress_ratio, topk, int(bool(has_in_idx))))
+
+
+def dsa_indexer_fwd_host(q, k, w, compress_ratio, topk, q_pos=None,
+                         in_idx=None, out_idx=None, out_scores=None,
+                         device_buf=None, stream=None):
+    """The forward on host (CPU) tensors through the C entry point that
+    pipelines the copies against the kernels; returns (out_scores, out_idx,
+    status).  Outputs are page-locked when q is.  `device_buf` (uint8 on the
+    current CUDA device) is allocated when not given.  The call returns with
+    the results in the host outputs; `status` is the library's return code
+    (0, or the device status of the run)."""
+    lib = load_library()
+    S, B, H, D, S_kv = _check_inputs(q, k, w, q_pos, in_idx)
+    for name, t in (("index_q", q), ("index_k", k), ("weights", w),
+                    ("q_pos", q_pos), ("topk_indices", in_idx)):
+        if t is not None and t.device.type != "cpu":
+            raise ValueError(f"{name} must be a host tensor")
+    if in_idx is not None and tuple(in_idx.shape) != (B, S, topk):
+        raise ValueError("topk_indices must be [B, S, topk]")
+    pinned = q.is_pinned()
+    if out_idx is None:
+        out_idx = torch.empty((B, S, topk), dtype=torch.int32,
+                              pin_memory=pinned)
+    if out_scores is None:
+        out_scores = torch.empty((B, S, topk), dtype=torch.float32,
+                                 pin_memory=pinned)
+    need = dsa_indexer_host_buffer_size(S, B, H, D, S_kv, compress_ratio,
+                                        topk, in_idx is not None)
+    if need == 0:
+        raise DsaError(2, "dsa_indexer_host_buffer_size")
+    if device_buf is None:
+        device_buf = torch.empty(need, dtype=torch.uint8,
+                                 device=torch.device(
+                                     "cuda", torch.cuda.current_device()))
+    rc = lib.dsa_indexer_fwd_host(
+        _ptr(q), _ptr(k), _ptr(w), S, B, H, D, S_kv, int(compress_ratio),
+        int(topk), _ptr(q_pos), _ptr(in_idx), _ptr(out_idx),
+        _ptr(out_scores), _ptr(device_buf), device_buf.numel(),
+        _stream(stream))
+    if rc not in (0, 5, 6):  # device status codes are returned, not raised
+        raise DsaError(rc, "dsa_indexer_fwd_host")
+    return out_scores, out_idx, rc
+
+
 def v4_lighting_indexer(index_q, index_k, weights, compress_ratio, topk,
                         topk_indices=None, q_pos=None, check=True):
     """The indexer forward with the V4 argument order.
@@ -212,17 +266,15 @@ def v4_lighting_indexer(index_q, index_k, weights, compress_ratio, topk,
     indices [B,S,topk] int32).  With check=True the call synchronises and
     raises on a device-side status (bad given index, expired wait).
     """
-    host = index_q.device.type == "cpu"
-    pinned = host and index_q.is_pinned()
-    if host:
-        dev = torch.device("cuda", torch.cuda.current_device())
-        index_q = index_q.to(dev, non_blocking=pinned)
-        index_k = index_k.to(dev, non_blocking=pinned)
-        weights = weights.to(dev, non_blocking=pinned)
-        if topk_indices is not None:
-            topk_indices = topk_indices.to(dev, non_blocking=pinned)
-        if q_pos is not None:
-            q_pos = q_pos.to(dev, non_blocking=pinned)
+    if index_q.device.type == "cpu":
+        # host buffers: the C entry point copies in, runs and copies out,
+        # overlapping the copies with the kernels
+        scores, idx, rc = dsa_indexer_fwd_host(
+            index_q, index_k, weights, compress_ratio, topk, q_pos=q_pos,
+            in_idx=topk_indices)
+        if check and rc != 0:
+            raise DsaError(rc, "device status")
+        return scores, idx
     scores, idx, ws = dsa_indexer_fwd(index_q, index_k, weights,
                                       compress_ratio, topk, q_pos=q_pos,
                                       in_idx=topk_indices)
@@ -230,13 +282,6 @@ def v4_lighting_indexer(index_q, index_k, weights, compress_ratio, topk,
         rc = dsa_indexer_check(ws)
         if rc != 0:
             raise DsaError(rc, "device status")
-    if host:
-        sc_h = torch.empty(scores.shape, dtype=scores.dtype, pin_memory=pinned)
-        idx_h = torch.empty(idx.shape, dtype=idx.dtype, pin_memory=pinned)
-        sc_h.copy_(scores, non_blocking=pinned)
-        idx_h.copy_(idx, non_blocking=pinned)
-        torch.cuda.current_stream().synchronize()
-        scores, idx = sc_h, idx_h
     return scores, idx
 
 

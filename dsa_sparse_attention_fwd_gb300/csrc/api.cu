@@ -257,17 +257,22 @@ int dsa_indexer_fwd_profiled(const void *q, const void *k, const float *w,
                : cudaSuccess;
   };
 
-  // per-row key histograms (top-k path): filled by the scoring kernel, read
-  // by the selection.  The decode kernel counts with global atomics (so the
-  // region starts at zero); the prefill kernel writes every row it scores.
+  // Workspace: status header, then the per-row key histograms when the
+  // scoring kernel counts them (filled by it, read by the selection), then
+  // the logits.  The decode kernel counts with global atomics, so its
+  // histograms start at zero: one memset clears them with the header.
   uint32_t *row_hist = nullptr;
+  size_t clear_bytes = kHeaderBytes;
   const bool decode = use_decode_path(p, dev);
   if (!in_idx && ((decode && hist_shape(S, H, D, S_kv)) ||
-                  (!decode && dsa::index_scores_histograms(H, S_kv))))
-    row_hist = reinterpret_cast<uint32_t *>(
-        static_cast<char *>(workspace) + kHeaderBytes +
-        logits_bytes(S, B, S_kv));
-  if (cudaMemsetAsync(status, 0, kHeaderBytes, st) != cudaSuccess)
+                  (!decode && dsa::index_scores_histograms(H, S_kv)))) {
+    row_hist = reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) +
+                                            kHeaderBytes);
+    logits = reinterpret_cast<float *>(reinterpret_cast<char *>(row_hist) +
+                                       row_hist_bytes(S, B, H, D, S_kv));
+    if (decode) clear_bytes += row_hist_bytes(S, B, H, D, S_kv);
+  }
+  if (cudaMemsetAsync(status, 0, clear_bytes, st) != cudaSuccess)
     return DSA_ERR_CUDA;
   if (in_idx && gather_direct_shape(B, H, D, S_kv)) {
     // one kernel: gathered keys -> scores at the given slots
@@ -284,10 +289,6 @@ int dsa_indexer_fwd_profiled(const void *q, const void *k, const float *w,
     if (mark(1) != cudaSuccess || mark(2) != cudaSuccess) return DSA_ERR_CUDA;
     return DSA_OK;
   }
-  if (row_hist && decode &&
-      cudaMemsetAsync(row_hist, 0, row_hist_bytes(S, B, H, D, S_kv), st) !=
-          cudaSuccess)
-    return DSA_ERR_CUDA;
   if (mark(0) != cudaSuccess) return DSA_ERR_CUDA;
   rc = run_scores(p, logits, row_hist, status, dev, st);
   if (rc != DSA_OK) return rc;

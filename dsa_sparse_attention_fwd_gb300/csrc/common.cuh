@@ -38,6 +38,18 @@ __host__ __device__ __forceinline__ int n_visible(long long pos, int ratio,
   return n < (long long)S_kv ? (int)n : S_kv;
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic
+// stream serialization may start while the previous kernel in the stream is
+// still running; pdl_wait() blocks until that kernel has completed and its
+// memory is visible.  pdl_allow_dependents() lets the next such kernel be
+// scheduled before this one finishes.  Both are no-ops without a dependency.
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_allow_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Order-preserving unsigned key of an fp32 score (larger float <-> larger
 // key; -0.0 folded onto +0.0 so the index tie-break decides between them).
 __device__ __forceinline__ uint32_t ordered_key(float f) {

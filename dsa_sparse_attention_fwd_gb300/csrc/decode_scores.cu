@@ -138,6 +138,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  // the selection kernel may be scheduled now; it waits for this grid to
+  // finish before it reads anything
+  pdl_allow_dependents();
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------

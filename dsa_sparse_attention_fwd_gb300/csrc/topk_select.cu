@@ -239,6 +239,9 @@ __global__ void __launch_bounds__(NT, NT == kSelThreads ? 4 : 1)
                        int ratio, int topk, int mcap, int bcap, int keys_cap,
                        int32_t *__restrict__ out_idx,
                        float *__restrict__ out_scores) {
+  // the logits and histograms come from the scoring kernel, which this
+  // launch may overlap (programmatic dependent launch)
+  pdl_wait();
   extern __shared__ __align__(16) uint8_t smem[];
   uint64_t *bufA = reinterpret_cast<uint64_t *>(smem);  // [mcap]
   uint64_t *bufB = bufA + mcap;                          // [bcap] (>= 4096 u32)
@@ -633,10 +636,21 @@ cudaError_t launch_sel(const Problem &p, const float *logits, int topk,
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)l.dyn);
   if (e != cudaSuccess) return e;
   const long long rows = (long long)p.B * p.S;
-  kern<<<(unsigned)rows, NT, l.dyn, st>>>(
-      logits, row_hist, p.q_pos, p.S, p.S_kv, p.ratio, topk, l.mcap, l.bcap,
-      l.keys_cap, out_idx, out_scores);
-  return cudaGetLastError();
+  // launched with programmatic stream serialization: the CTAs are queued
+  // while the scoring kernel runs and wait for it inside the kernel
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)rows);
+  cfg.blockDim = dim3(NT);
+  cfg.dynamicSmemBytes = l.dyn;
+  cfg.stream = st;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, logits, row_hist, p.q_pos, p.S,
+                            p.S_kv, p.ratio, topk, l.mcap, l.bcap, l.keys_cap,
+                            out_idx, out_scores);
 }
 
 }  // namespace

@@ -79,10 +79,10 @@ typedef enum dsa_status {
  * Bytes of device workspace dsa_indexer_fwd() needs for this shape
  * (has_in_idx != 0 selects the given-indices path).  Returns 0 when the
  * shape is invalid.  The workspace starts with a 256-byte status header.
- * Top-k path: the header is followed by the fp32 logits [B, S, S_kv] of the
- * visible keys and, when H >= 64 with S_kv >= 8192 or when a sequence has
- * fewer than 256/H queries (the decode kernel), one 4096-bin u32 key
- * histogram per query row (16 KiB per row).
+ * Top-k path: the header is followed, when H >= 64 with S_kv >= 8192 or
+ * when a sequence has fewer than 256/H queries (the decode kernel), by one
+ * 4096-bin u32 key histogram per query row (16 KiB per row), then by the
+ * fp32 logits [B, S, S_kv] of the visible keys.
  * Given-indices path: H in {16, 32, 64, 128} scores the gathered keys
  * directly and needs the header only; other H take the header plus the
  * logits.
@@ -120,6 +120,45 @@ DSA_API int dsa_indexer_fwd(const void *q, const void *k, const float *w,
                             int32_t *out_idx, float *out_scores,
                             void *workspace, size_t workspace_bytes,
                             void *cuda_stream);
+
+/*
+ * Bytes of DEVICE memory dsa_indexer_fwd_host() needs for this shape: room
+ * for the inputs, the outputs and the workspace of its chunked pipeline.
+ * Returns 0 when the shape is invalid.
+ */
+DSA_API size_t dsa_indexer_host_buffer_size(int S, int B, int H, int D,
+                                            int S_kv, int compress_ratio,
+                                            int topk, int has_in_idx);
+
+/*
+ * The forward on HOST buffers (the end-to-end call): q, k, w, q_pos,
+ * in_idx are host inputs and out_idx / out_scores host outputs, with the
+ * layouts and meaning of dsa_indexer_fwd().  The call copies the inputs to
+ * `device_buf` (caller-owned device memory of dsa_indexer_host_buffer_size()
+ * bytes, 256-byte aligned), runs the forward there and copies the results
+ * back, pipelining the copies against the kernels: the query rows are split
+ * along S into up to 16 chunks of at least 512 rows (none for S < 1024);
+ * the next chunk's rows are copied in while one chunk is scored, and its
+ * results are copied out while the following ones are scored.  Results are identical to one dsa_indexer_fwd()
+ * call.  The copies overlap only when the host buffers are page-locked
+ * (pinned); pageable buffers work but serialise.
+ *
+ * The work is ordered after everything already queued on `cuda_stream` and
+ * the call returns once the results are in the host outputs (it
+ * synchronises `cuda_stream`).  Calls on one device are serialised.
+ * Returns DSA_OK; a synchronous argument error (DSA_ERR_INVALID_ARG,
+ * DSA_ERR_UNSUPPORTED, DSA_ERR_WORKSPACE); DSA_ERR_CUDA; or the device
+ * status of the run (DSA_ERR_INDEX_RANGE, DSA_ERR_DEVICE_TIMEOUT).  The
+ * library keeps two copy streams, a few events and a small page-locked
+ * staging buffer per device for the life of the process.
+ */
+DSA_API int dsa_indexer_fwd_host(const void *q, const void *k, const float *w,
+                                 int S, int B, int H, int D, int S_kv,
+                                 int compress_ratio, int topk,
+                                 const int32_t *q_pos, const int32_t *in_idx,
+                                 int32_t *out_idx, float *out_scores,
+                                 void *device_buf, size_t device_buf_bytes,
+                                 void *cuda_stream);
 
 /*
  * dsa_indexer_fwd() with stage timing: `stage_events` holds `n_events` (0..3)

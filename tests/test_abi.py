@@ -40,6 +40,11 @@ def lib():
     L.dsa_indexer_check.argtypes = [P, P]
     L.dsa_selftest_wait_limit.restype = I
     L.dsa_selftest_wait_limit.argtypes = [I, P, Z, P]
+    L.dsa_indexer_host_buffer_size.restype = Z
+    L.dsa_indexer_host_buffer_size.argtypes = [I] * 8
+    L.dsa_indexer_fwd_host.restype = I
+    L.dsa_indexer_fwd_host.argtypes = [P, P, P, I, I, I, I, I, I, I, P, P, P,
+                                       P, P, Z, P]
     return L
 
 
@@ -166,3 +171,42 @@ def test_python_binding_fails_loudly_without_library(tmp_path):
             m.load_library(str(tmp_path / "missing.so"))
     finally:
         m._lib = saved
+
+
+def test_host_buffer_size(lib):
+    hb = lib.dsa_indexer_host_buffer_size
+    ws = lib.dsa_indexer_workspace_size
+    assert hb(0, 1, 64, 128, 4096, 1, 2048, 0) == 0
+    assert hb(16, 1, 3, 128, 16, 1, 4, 0) == 0
+    # one chunk: inputs + outputs + status + the workspace of the whole call
+    S, B, H, D, S_kv, k = 128, 1, 4, 32, 128, 16
+    need = hb(S, B, H, D, S_kv, 1, k, 0)
+    inputs = S_kv * B * D * 2 + S * B * H * D * 2 + S * B * H * 4
+    assert need >= inputs + 2 * B * S * k * 4 + ws(S, B, H, D, S_kv, 1, k, 0)
+    # eight chunks of 512 rows: the workspace is one chunk's, not the call's
+    big = hb(4096, 1, 64, 128, 4096, 1, 2048, 0)
+    assert big < (4096 * 64 * 128 * 2 + 2 * 4096 * 2048 * 4
+                  + ws(4096, 1, 64, 128, 4096, 1, 2048, 0))
+    assert big >= 4096 * 64 * 128 * 2 + 2 * 4096 * 2048 * 4 + ws(
+        512, 1, 64, 128, 4096, 1, 2048, 0)
+
+
+def test_host_fwd_rejects_bad_arguments(lib):
+    f = lib.dsa_indexer_fwd_host
+    H = FAKE
+    need = lib.dsa_indexer_host_buffer_size(16, 1, 4, 32, 16, 1, 4, 0)
+    args = dict(q=H, k=H, w=H, oi=H, os_=H, buf=FAKE, nb=need)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return f(a["q"], a["k"], a["w"], 16, 1, 4, 32, 16, 1, 4, None, None,
+                 a["oi"], a["os_"], a["buf"], a["nb"], None)
+    assert call(q=None) == INVALID
+    assert call(oi=None) == INVALID
+    assert call(buf=None) == WORKSPACE
+    assert call(nb=need - 1) == WORKSPACE
+    assert call(buf=FAKE + 16) == INVALID  # not 256-byte aligned
+    assert f(H, H, H, 16, 1, 3, 32, 16, 1, 4, None, None, H, H, FAKE, 1 << 30,
+             None) == UNSUPPORTED
+    assert f(H, H, H, 0, 1, 4, 32, 16, 1, 4, None, None, H, H, FAKE, 1 << 30,
+             None) == INVALID
