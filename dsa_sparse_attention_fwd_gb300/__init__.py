@@ -28,6 +28,7 @@ __all__ = [
     "dsa_indexer_fwd", "dsa_indexer_logits", "dsa_indexer_check",
     "dsa_status_string", "dsa_selftest_wait_limit", "v4_lighting_indexer",
     "indexer_logits", "dsa_indexer_host_buffer_size", "dsa_indexer_fwd_host",
+    "dsa_indexer_varlen_workspace_size", "dsa_indexer_fwd_varlen",
     "STATUS",
 ]
 
@@ -84,6 +85,12 @@ def load_library(path: str | None = None):
         lib.dsa_selftest_wait_limit.argtypes = [I, P, Z, P]
         lib.dsa_indexer_host_buffer_size.restype = Z
         lib.dsa_indexer_host_buffer_size.argtypes = [I] * 8
+        lib.dsa_indexer_varlen_workspace_size.restype = Z
+        lib.dsa_indexer_varlen_workspace_size.argtypes = [I, P, P, I, I, I, I,
+                                                          I]
+        lib.dsa_indexer_fwd_varlen.restype = I
+        lib.dsa_indexer_fwd_varlen.argtypes = [P, P, P, I, P, P, I, I, I, I,
+                                               P, P, P, P, P, Z, P]
         lib.dsa_indexer_fwd_host.restype = I
         lib.dsa_indexer_fwd_host.argtypes = [P, P, P, I, I, I, I, I, I, I, P,
                                              P, P, P, P, Z, P]
@@ -205,6 +212,76 @@ def dsa_indexer_check(workspace, stream=None) -> int:
 def dsa_selftest_wait_limit(limit_us: int, workspace, stream=None) -> int:
     return int(load_library().dsa_selftest_wait_limit(
         int(limit_us), _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def _host_i32(a):
+    """A contiguous host int32 tensor (kept alive by the caller)."""
+    t = torch.as_tensor(a, dtype=torch.int32, device="cpu").contiguous()
+    return t
+
+
+def dsa_indexer_varlen_workspace_size(cu_seqlens_q, cu_seqlens_k, H, D,
+                                      compress_ratio, topk,
+                                      has_in_idx=False) -> int:
+    cq, ck = _host_i32(cu_seqlens_q), _host_i32(cu_seqlens_k)
+    if cq.numel() != ck.numel() or cq.numel() < 2:
+        raise ValueError("cu_seqlens_q / cu_seqlens_k must both be [N + 1]")
+    return int(load_library().dsa_indexer_varlen_workspace_size(
+        cq.numel() - 1, _ptr(cq), _ptr(ck), H, D, compress_ratio, topk,
+        int(bool(has_in_idx))))
+
+
+def dsa_indexer_fwd_varlen(q, k, w, cu_seqlens_q, cu_seqlens_k,
+                           compress_ratio, topk, q_pos=None, in_idx=None,
+                           out_idx=None, out_scores=None, workspace=None,
+                           stream=None):
+    """The forward over packed variable-length sequences: q [T, H, D] bf16,
+    k [T_kv, D] bf16, w [T, H] fp32 and the optional q_pos [N] / in_idx
+    [T, topk] on the device; cu_seqlens_q / cu_seqlens_k are host int32
+    offsets [N + 1].  Returns (out_scores [T, topk], out_idx [T, topk],
+    workspace); indices are local to each row's sequence."""
+    lib = load_library()
+    cq, ck = _host_i32(cu_seqlens_q), _host_i32(cu_seqlens_k)
+    N = cq.numel() - 1
+    if ck.numel() != N + 1 or N < 1:
+        raise ValueError("cu_seqlens_q / cu_seqlens_k must both be [N + 1]")
+    if q.dim() != 3 or k.dim() != 2 or w.dim() != 2:
+        raise ValueError("q [T, H, D], k [T_kv, D], w [T, H] expected")
+    T, H, D = q.shape
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16),
+                        ("w", w, torch.float32)):
+        if t.dtype != dt or not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous {dt}")
+    if int(cq[-1]) != T or int(ck[-1]) != k.shape[0] or k.shape[1] != D or \
+            tuple(w.shape) != (T, H):
+        raise ValueError("shapes do not match the offsets")
+    if q_pos is not None and (q_pos.dtype != torch.int32 or
+                              q_pos.numel() != N):
+        raise ValueError("q_pos must be int32 [N]")
+    if in_idx is not None and (in_idx.dtype != torch.int32 or
+                               tuple(in_idx.shape) != (T, topk) or
+                               not in_idx.is_contiguous()):
+        raise ValueError("in_idx must be contiguous int32 [T, topk]")
+    dev = q.device
+    if out_idx is None:
+        out_idx = torch.empty((T, topk), dtype=torch.int32, device=dev)
+    if out_scores is None:
+        out_scores = torch.empty((T, topk), dtype=torch.float32, device=dev)
+    if workspace is None:
+        need = dsa_indexer_varlen_workspace_size(cq, ck, H, D,
+                                                 compress_ratio, topk,
+                                                 in_idx is not None)
+        if need == 0:
+            raise DsaError(2, "dsa_indexer_varlen_workspace_size")
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    rc = lib.dsa_indexer_fwd_varlen(
+        _ptr(q), _ptr(k), _ptr(w), N, _ptr(cq), _ptr(ck), H, D,
+        int(compress_ratio), int(topk), _ptr(q_pos), _ptr(in_idx),
+        _ptr(out_idx), _ptr(out_scores), _ptr(workspace), workspace.numel(),
+        _stream(stream))
+    if rc != 0:
+        raise DsaError(rc, "dsa_indexer_fwd_varlen")
+    return out_scores, out_idx, workspace
 
 
 def dsa_indexer_host_buffer_size(S, B, H, D, S_kv, compress_ratio, topk,

@@ -223,6 +223,26 @@ int dsa_indexer_fwd_profiled(const void *q, const void *k, const float *w,
                              void *workspace, size_t workspace_bytes,
                              void *cuda_stream, void *const *stage_events,
                              int n_events) {
+  return dsa::forward_core(q, k, w, S, B, H, D, S_kv, compress_ratio, topk,
+                           q_pos, in_idx, out_idx, out_scores, workspace,
+                           workspace_bytes, cuda_stream, stage_events,
+                           n_events, true);
+}
+
+}  // extern "C"
+
+namespace dsa {
+
+// The forward behind every entry point.  clear_status = false keeps the
+// workspace's status word (several forwards sharing one workspace then
+// accumulate their device errors); the decode histograms are cleared either
+// way.
+int forward_core(const void *q, const void *k, const float *w, int S, int B,
+                 int H, int D, int S_kv, int compress_ratio, int topk,
+                 const int32_t *q_pos, const int32_t *in_idx, int32_t *out_idx,
+                 float *out_scores, void *workspace, size_t workspace_bytes,
+                 void *cuda_stream, void *const *stage_events, int n_events,
+                 bool clear_status) {
   if (!q || !k || !w || !out_idx || !out_scores) return DSA_ERR_INVALID_ARG;
   int rc = check_shape(S, B, H, D, S_kv, compress_ratio);
   if (rc != DSA_OK) return rc;
@@ -272,8 +292,14 @@ int dsa_indexer_fwd_profiled(const void *q, const void *k, const float *w,
                                        row_hist_bytes(S, B, H, D, S_kv));
     if (decode) clear_bytes += row_hist_bytes(S, B, H, D, S_kv);
   }
-  if (cudaMemsetAsync(status, 0, clear_bytes, st) != cudaSuccess)
+  if (clear_status) {
+    if (cudaMemsetAsync(status, 0, clear_bytes, st) != cudaSuccess)
+      return DSA_ERR_CUDA;
+  } else if (clear_bytes > kHeaderBytes &&
+             cudaMemsetAsync(row_hist, 0, clear_bytes - kHeaderBytes, st) !=
+                 cudaSuccess) {
     return DSA_ERR_CUDA;
+  }
   if (in_idx && gather_direct_shape(B, H, D, S_kv)) {
     // one kernel: gathered keys -> scores at the given slots
     if ((size_t)dev.max_smem_optin < dsa::gather_smem_bytes(H, D))
@@ -304,6 +330,10 @@ int dsa_indexer_fwd_profiled(const void *q, const void *k, const float *w,
   if (mark(2) != cudaSuccess) return DSA_ERR_CUDA;
   return DSA_OK;
 }
+
+}  // namespace dsa
+
+extern "C" {
 
 int dsa_indexer_fwd(const void *q, const void *k, const float *w, int S,
                     int B, int H, int D, int S_kv, int compress_ratio,

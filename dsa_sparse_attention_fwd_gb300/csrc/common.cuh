@@ -125,6 +125,16 @@ size_t decode_smem_bytes(int H, int D);
 
 cudaError_t launch_fill_masked(float *logits, size_t n, cudaStream_t st);
 
+// The forward behind the C entry points (arguments and return codes of
+// dsa_indexer_fwd_profiled); clear_status = false keeps the workspace's
+// status word, so forwards sharing a workspace accumulate device errors.
+int forward_core(const void *q, const void *k, const float *w, int S, int B,
+                 int H, int D, int S_kv, int compress_ratio, int topk,
+                 const int32_t *q_pos, const int32_t *in_idx, int32_t *out_idx,
+                 float *out_scores, void *workspace, size_t workspace_bytes,
+                 void *cuda_stream, void *const *stage_events, int n_events,
+                 bool clear_status);
+
 cudaError_t launch_wait_selftest(int limit_us, int *status, cudaStream_t st);
 
 }  // namespace dsa

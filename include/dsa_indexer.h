@@ -122,6 +122,49 @@ DSA_API int dsa_indexer_fwd(const void *q, const void *k, const float *w,
                             void *cuda_stream);
 
 /*
+ * Packed variable-length sequences (the packed-sequence dispatch of the V4
+ * indexer adaptation on the NeMo AutoModel "tilelang_indexer" page).
+ * N sequences share one token axis: sequence i owns query rows
+ * [cu_seqlens_q[i], cu_seqlens_q[i+1]) and compressed keys
+ * [cu_seqlens_k[i], cu_seqlens_k[i+1]).  cu_seqlens_q / cu_seqlens_k are
+ * HOST arrays of N + 1 int32, starting at 0, non-decreasing.
+ *
+ *   q        [T, H, D] bf16       (T = cu_seqlens_q[N])
+ *   k        [T_kv, D] bf16       (T_kv = cu_seqlens_k[N])
+ *   w        [T, H] fp32
+ *   q_pos    [N] int32 or NULL    (device; row s of sequence i sits at
+ *                                  q_pos[i] + s, NULL: at s)
+ *   in_idx   [T, topk] int32 or NULL (device; indices local to the row's
+ *                                  sequence)
+ *   out_idx, out_scores [T, topk] (device; indices local to the sequence)
+ *
+ * Per row the result is that of dsa_indexer_fwd() on the row's sequence
+ * alone (B = 1).  Rows of a sequence with no keys get -1 / -inf (given
+ * indices are copied through unchecked).  Sequences run on up to 4 streams
+ * at once, each with its own slice of the workspace; a workspace smaller
+ * than dsa_indexer_varlen_workspace_size() but at least one slice (the
+ * largest sequence's need) runs fewer at once.  Asynchronous on
+ * `cuda_stream`, which the library's other streams join before the call's
+ * work ends; dsa_indexer_check(workspace) reports the device status of all
+ * sequences.  Calls on one device are serialised.
+ */
+DSA_API size_t dsa_indexer_varlen_workspace_size(int N,
+                                                 const int32_t *cu_seqlens_q,
+                                                 const int32_t *cu_seqlens_k,
+                                                 int H, int D,
+                                                 int compress_ratio, int topk,
+                                                 int has_in_idx);
+DSA_API int dsa_indexer_fwd_varlen(const void *q, const void *k,
+                                   const float *w, int N,
+                                   const int32_t *cu_seqlens_q,
+                                   const int32_t *cu_seqlens_k, int H, int D,
+                                   int compress_ratio, int topk,
+                                   const int32_t *q_pos, const int32_t *in_idx,
+                                   int32_t *out_idx, float *out_scores,
+                                   void *workspace, size_t workspace_bytes,
+                                   void *cuda_stream);
+
+/*
  * Bytes of DEVICE memory dsa_indexer_fwd_host() needs for this shape: room
  * for the inputs, the outputs and the workspace of its chunked pipeline.
  * Returns 0 when the shape is invalid.

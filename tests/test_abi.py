@@ -40,6 +40,11 @@ def lib():
     L.dsa_indexer_check.argtypes = [P, P]
     L.dsa_selftest_wait_limit.restype = I
     L.dsa_selftest_wait_limit.argtypes = [I, P, Z, P]
+    L.dsa_indexer_varlen_workspace_size.restype = Z
+    L.dsa_indexer_varlen_workspace_size.argtypes = [I, P, P, I, I, I, I, I]
+    L.dsa_indexer_fwd_varlen.restype = I
+    L.dsa_indexer_fwd_varlen.argtypes = [P, P, P, I, P, P, I, I, I, I, P, P,
+                                         P, P, P, Z, P]
     L.dsa_indexer_host_buffer_size.restype = Z
     L.dsa_indexer_host_buffer_size.argtypes = [I] * 8
     L.dsa_indexer_fwd_host.restype = I
@@ -210,3 +215,48 @@ def test_host_fwd_rejects_bad_arguments(lib):
              None) == UNSUPPORTED
     assert f(H, H, H, 0, 1, 4, 32, 16, 1, 4, None, None, H, H, FAKE, 1 << 30,
              None) == INVALID
+
+
+def _i32(*v):
+    return (ctypes.c_int32 * len(v))(*v)
+
+
+def test_varlen_workspace_size(lib):
+    vw = lib.dsa_indexer_varlen_workspace_size
+    ws = lib.dsa_indexer_workspace_size
+    up = lambda x: (x + 255) // 256 * 256
+    # two sequences with rows: two slices of the larger one's workspace
+    cq, ck = _i32(0, 100, 300), _i32(0, 25, 75)
+    assert vw(2, cq, ck, 64, 128, 4, 32, 0) == 2 * up(
+        ws(200, 1, 64, 128, 50, 4, 32, 0))
+    # an empty sequence and a keyless one add no slices
+    cq, ck = _i32(0, 0, 10, 40), _i32(0, 5, 5, 20)
+    assert vw(3, cq, ck, 16, 64, 1, 8, 0) == 2 * up(
+        ws(30, 1, 16, 64, 15, 1, 8, 0))
+    # at most four slices
+    cq = _i32(*[i * 10 for i in range(9)])
+    ck = _i32(*[i * 10 for i in range(9)])
+    assert vw(8, cq, ck, 4, 32, 1, 4, 0) == 4 * up(ws(10, 1, 4, 32, 10, 1, 4, 0))
+    # malformed offsets
+    assert vw(2, _i32(1, 5, 9), _i32(0, 5, 9), 4, 32, 1, 4, 0) == 0
+    assert vw(2, _i32(0, 5, 4), _i32(0, 5, 9), 4, 32, 1, 4, 0) == 0
+    assert vw(0, _i32(0), _i32(0), 4, 32, 1, 4, 0) == 0
+    assert vw(1, _i32(0, 5), _i32(0, 5), 3, 32, 1, 4, 0) == 0  # H = 3
+
+
+def test_varlen_rejects_bad_arguments(lib):
+    f = lib.dsa_indexer_fwd_varlen
+    cq, ck = _i32(0, 16, 40), _i32(0, 16, 40)
+    need = lib.dsa_indexer_varlen_workspace_size(2, cq, ck, 4, 32, 1, 4, 0)
+
+    def call(q=FAKE, cq=cq, ck=ck, n=2, ws=FAKE, nb=need, topk=4):
+        return f(q, FAKE, FAKE, n, cq, ck, 4, 32, 1, topk, None, None, FAKE,
+                 FAKE, ws, nb, None)
+    assert call(q=None) == INVALID
+    assert call(cq=None) == INVALID
+    assert call(n=0) == INVALID
+    assert call(topk=0) == INVALID
+    assert call(ws=None) == WORKSPACE
+    assert call(nb=need // 2 - 1) == WORKSPACE  # less than one slice
+    assert call(ws=FAKE + 16) == INVALID
+    assert call(cq=_i32(0, 16, 8)) == INVALID
