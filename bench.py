@@ -490,6 +490,130 @@ def run_ours(args):
     return 0
 
 
+def run_varlen(args):
+    """Packed variable-length sequences through dsa_indexer_fwd_varlen."""
+    import numpy as np
+    import torch
+
+    import dsa_sparse_attention_fwd_gb300 as dsa
+    from dsa_inputs import VARLEN_WORKLOADS, make_varlen_inputs
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dsa.build()
+    dsa.load_library()
+    vw = VARLEN_WORKLOADS[args.workload]
+    q, k, w, cq, ck = make_varlen_inputs(vw)
+    pairs = 0
+    for i in range(len(vw.lens_q)):
+        s = np.arange(cq[i + 1] - cq[i], dtype=np.int64)
+        pairs += int(np.clip((s + 1) // vw.compress_ratio, 0,
+                             ck[i + 1] - ck[i]).sum())
+    flops = 2.0 * vw.H * vw.D * pairs
+    qd, kd, wd = q.to(dev), k.to(dev), w.to(dev)
+    T = int(cq[-1])
+    oi = torch.empty((T, vw.topk), dtype=torch.int32, device=dev)
+    osc = torch.empty((T, vw.topk), dtype=torch.float32, device=dev)
+    ws = torch.empty(dsa.dsa_indexer_varlen_workspace_size(
+        cq, ck, vw.H, vw.D, vw.compress_ratio, vw.topk), dtype=torch.uint8,
+        device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        dsa.dsa_indexer_fwd_varlen(qd, kd, wd, cq, ck, vw.compress_ratio,
+                                   vw.topk, out_idx=oi, out_scores=osc,
+                                   workspace=ws, stream=stream)
+    for _ in range(max(args.warmup, 3)):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    if dsa.dsa_indexer_check(ws) != 0:
+        raise RuntimeError("device status")
+    K = args.steps
+    mk = lambda: torch.cuda.Event(enable_timing=True)
+    ev = [(mk(), mk()) for _ in range(K)]
+    for a_, b_ in ev:
+        a_.record(stream)
+        b_.record(stream)
+    sampler = ClockSampler(local)
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.2)
+    for i in range(K):
+        flush.fill_(1.0)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    t_step = sum(a_.elapsed_time(b_) for a_, b_ in ev) / K
+    # end to end: inputs copied in from pinned host memory and the outputs
+    # copied back, around the same call
+    qh, kh, wh = q.pin_memory(), k.pin_memory(), w.pin_memory()
+    oih = torch.empty((T, vw.topk), dtype=torch.int32, pin_memory=True)
+    osh = torch.empty((T, vw.topk), dtype=torch.float32, pin_memory=True)
+    e2e = []
+    for i in range(max(3, min(K, 20)) + 2):
+        a_, b_ = mk(), mk()
+        a_.record(stream)
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        wd.copy_(wh, non_blocking=True)
+        step()
+        oih.copy_(oi, non_blocking=True)
+        osh.copy_(osc, non_blocking=True)
+        b_.record(stream)
+        b_.synchronize()
+        if i >= 2:
+            e2e.append(a_.elapsed_time(b_))
+    t_e2e = sum(e2e) / len(e2e)
+    if rank != 0:
+        return 0
+    peaks, peak_src = read_peaks()
+    tc_peak = float(peaks["bf16_tflops"])
+    value = world * flops / (t_step * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": t_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": vw.name, "lens_q": list(vw.lens_q),
+                   "H": vw.H, "D": vw.D, "compress_ratio": vw.compress_ratio,
+                   "topk": vw.topk, "visible_pairs": pairs,
+                   "flops_per_step": flops,
+                   "l2": "flushed before each step (256 MiB write, outside "
+                         "the timed events)",
+                   "parallelism": f"replicas x{world}"},
+        "queries_per_s": world * T / (t_step * 1e-3),
+        "roofline": {"kernel": "varlen dispatch (every kernel of the call)",
+                     "bound": "tensor", "achieved": value / world,
+                     "peak": tc_peak, "unit": "TFLOP/s",
+                     "frac": value / world / tc_peak,
+                     "peak_source": f"{peak_src} bf16 burst",
+                     "traffic": None},
+        "e2e": {"value": world * flops / (t_e2e * 1e-3) / 1e12,
+                "unit": "TFLOP/s", "ms_per_step": t_e2e,
+                "h2d_bytes_per_step": q.numel() * 2 + k.numel() * 2 +
+                w.numel() * 4,
+                "d2h_bytes_per_step": oi.numel() * 8,
+                "api": "torch copies + dsa_indexer_fwd_varlen"},
+        # two kernels per sequence with keys, plus the status merge when
+        # more than one stream slice ran
+        "gpu_launches": K * (2 * sum(1 for i in range(len(vw.lens_q))
+                                     if ck[i + 1] > ck[i] and cq[i + 1] > cq[i])
+                             + (1 if ws.numel() > ws.numel() // 2 and
+                                len(vw.lens_q) > 1 else 0)),
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -502,6 +626,9 @@ def main():
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    from dsa_inputs import VARLEN_WORKLOADS
+    if args.workload in VARLEN_WORKLOADS:
+        return run_varlen(args)
     return run_ours(args)
 
 

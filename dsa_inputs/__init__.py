@@ -65,6 +65,51 @@ WORKLOADS = {
 }
 
 
+@dataclasses.dataclass(frozen=True)
+class VarlenWorkload:
+    """Packed variable-length sequences: query rows per sequence (lens_q)
+    and compressed keys per sequence (lens_q // compress_ratio)."""
+
+    name: str
+    lens_q: tuple
+    H: int
+    D: int
+    compress_ratio: int
+    topk: int
+    w_scale: float
+    seed: int
+
+
+VARLEN_WORKLOADS = {
+    # a packed C4 batch: one long document and a tail of shorter ones
+    "varlen_c4": VarlenWorkload("varlen_c4",
+                                lens_q=(16384, 8192, 4096, 2048, 1024, 512,
+                                        256, 128),
+                                H=64, D=128, compress_ratio=4, topk=512,
+                                w_scale=0.125, seed=6),
+}
+
+
+def make_varlen_inputs(vw: VarlenWorkload, device: str = "cpu"):
+    """Draw packed (q [T,H,D] bf16, k [T_kv,D] bf16, w [T,H] fp32) and the
+    host offsets (cu_seqlens_q, cu_seqlens_k) for a varlen workload, from
+    one seeded CPU generator in the order q, k, w."""
+    lens_k = [n // vw.compress_ratio for n in vw.lens_q]
+    T, T_kv = sum(vw.lens_q), sum(lens_k)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(vw.seed)
+    q = torch.randn((T, vw.H, vw.D), generator=g,
+                    dtype=torch.float32).to(torch.bfloat16)
+    k = torch.randn((T_kv, vw.D), generator=g,
+                    dtype=torch.float32).to(torch.bfloat16)
+    w = torch.randn((T, vw.H), generator=g, dtype=torch.float32) * vw.w_scale
+    cq = np.concatenate([[0], np.cumsum(vw.lens_q)]).astype(np.int32)
+    ck = np.concatenate([[0], np.cumsum(lens_k)]).astype(np.int32)
+    if device != "cpu":
+        q, k, w = q.to(device), k.to(device), w.to(device)
+    return q, k, w, cq, ck
+
+
 def describe(wl: Workload) -> str:
     pos = (f", q_pos~U{{{wl.pos_range[0]}..{wl.pos_range[1]}}}"
            if wl.pos_range else "")
