@@ -165,6 +165,25 @@ def dist_env():
     return rank, world, local
 
 
+def barrier_ranks(world: int) -> None:
+    """Barrier across the replicas (no-op for one process)."""
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest of every rank's value (the slowest replica's time); the
+    tensor lives on `device` (the GPU under NCCL, the CPU under gloo)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def cpu_oracle_sample(wl, rows_every: int, in_idx=None):
     """Time the oracle on every `rows_every`-th row (from the last row down,
     so the longest rows are in the sample)."""
@@ -305,8 +324,7 @@ def run_ours(args):
         for e in pair:
             e.record(stream)
     sampler = ClockSampler(local)
-    if world > 1:
-        dist.barrier()
+    barrier_ranks(world)
     torch.cuda.synchronize()
     sampler.start()
     time.sleep(0.2)
@@ -318,18 +336,13 @@ def run_ours(args):
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
-    if world > 1:
-        dist.barrier()
+    barrier_ranks(world)
     clocks = sampler.stop()
     rc = dsa.dsa_indexer_check(ws)
     if rc != 0:
         raise RuntimeError(f"device status {dsa.STATUS.get(rc, rc)}")
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    t_step = sum(step_ms) / K
-    if world > 1:
-        t = torch.tensor([t_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_step = float(t.item())
+    t_step = max_over_ranks(sum(step_ms) / K, world, dev)
 
     # per-kernel split: another K steps with events recorded between the
     # stages (these can keep the next kernel from starting early, so they
@@ -379,11 +392,7 @@ def run_ours(args):
         b.record(stream)
         b.synchronize()
         e2e_ms.append(a.elapsed_time(b))
-    t_e2e = sum(e2e_ms) / Ke
-    if world > 1:
-        t = torch.tensor([t_e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_e2e = float(t.item())
+    t_e2e = max_over_ranks(sum(e2e_ms) / Ke, world, dev)
     h2d = q.numel() * 2 + k.numel() * 2 + w.numel() * 4 + (
         q_pos.numel() * 4 if q_pos is not None else 0) + (
         gi.numel() * 4 if gi is not None else 0)
@@ -550,8 +559,10 @@ def run_varlen(args):
         step()
         ev[i][1].record(stream)
     torch.cuda.synchronize()
+    barrier_ranks(world)
     clocks = sampler.stop()
-    t_step = sum(a_.elapsed_time(b_) for a_, b_ in ev) / K
+    t_step = max_over_ranks(sum(a_.elapsed_time(b_) for a_, b_ in ev) / K,
+                            world, dev)
     # end to end: inputs copied in from pinned host memory and the outputs
     # copied back, around the same call
     qh, kh, wh = q.pin_memory(), k.pin_memory(), w.pin_memory()
@@ -571,7 +582,7 @@ def run_varlen(args):
         b_.synchronize()
         if i >= 2:
             e2e.append(a_.elapsed_time(b_))
-    t_e2e = sum(e2e) / len(e2e)
+    t_e2e = max_over_ranks(sum(e2e) / len(e2e), world, dev)
     if rank != 0:
         return 0
     peaks, peak_src = read_peaks()
