@@ -54,6 +54,11 @@ def _load():
                 P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 P, P, P, ctypes.c_longlong, P, P, P, P, P, P, ctypes.c_int]
+            lib.oracle_indexer_bwd.restype = None
+            lib.oracle_indexer_bwd.argtypes = [
+                P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                P, P, P, P, P, P, P, P, P]
             lib.oracle_key_visible.restype = ctypes.c_int
             lib.oracle_key_visible.argtypes = [ctypes.c_longlong,
                                                ctypes.c_longlong, ctypes.c_int]
@@ -139,4 +144,36 @@ def indexer_fwd(q, k, w, compress_ratio: int, topk: int, q_pos=None,
         out["logits"] = logits
     out["threads"] = used
     out["rows"] = rows
+    return out
+
+
+def indexer_bwd(q, k, w, compress_ratio: int, idx, grad_scores, q_pos=None):
+    """Backward of the given-slots forward: gradients of sum(grad_scores *
+    scores) with respect to q, k and w, in double.
+
+    q [S,B,H,D] bf16, k [S_kv,B,D] bf16, w [S,B,H] fp32, idx [B,S,topk]
+    int32 (the slots the forward scored), grad_scores [B,S,topk] fp32,
+    q_pos [B] int32 or None.  Returns a dict: grad_q [S,B,H,D],
+    grad_k [S_kv,B,D], grad_w [S,B,H] and abs_q / abs_k / abs_w, the sums of
+    the absolute values of each output's terms.
+    """
+    lib = _load()
+    qb, kb = _bits(q), _bits(k)
+    wf = _arr(w, np.float32)
+    S, B, H, D = qb.shape
+    S_kv = kb.shape[0]
+    gi = _arr(idx, np.int32)
+    topk = gi.shape[-1]
+    gi = gi.reshape(B, S, topk)
+    gs = _arr(grad_scores, np.float32).reshape(B, S, topk)
+    qp = None if q_pos is None else _arr(q_pos, np.int32).reshape(B)
+    out = {n: np.empty(shape, np.float64) for n, shape in (
+        ("grad_q", (S, B, H, D)), ("grad_k", (S_kv, B, D)),
+        ("grad_w", (S, B, H)), ("abs_q", (S, B, H, D)),
+        ("abs_k", (S_kv, B, D)), ("abs_w", (S, B, H)))}
+    lib.oracle_indexer_bwd(
+        _ptr(qb), _ptr(kb), _ptr(wf), S, B, H, D, S_kv, int(compress_ratio),
+        int(topk), _ptr(qp), _ptr(gi), _ptr(gs), _ptr(out["grad_q"]),
+        _ptr(out["grad_k"]), _ptr(out["grad_w"]), _ptr(out["abs_q"]),
+        _ptr(out["abs_k"]), _ptr(out["abs_w"]))
     return out

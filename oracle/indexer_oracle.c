@@ -248,3 +248,74 @@ int oracle_indexer_fwd(const uint16_t *q, const uint16_t *k, const float *w,
     pthread_mutex_destroy(&jb.lock);
     return started + 1;
 }
+
+/*
+ * Backward of the given-slots forward (V4IndexerFunction.backward, page
+ * "nemo_automodel.components.models.deepseek_v4.kernels.tilelang_indexer":
+ * the gradient of a loss with respect to index_q, index_k and weights given
+ * the gradient of the returned scores).  The pages print no formula; this is
+ * the derivative of the score definition above, slot by slot:
+ *
+ *   slot (b, s, i) with key j = idx[b, s, i] that is in [0, S_kv) and
+ *   visible at the row's position, upstream gradient g = grad_scores[b,s,i]:
+ *     dot_h = sum_d q[s,b,h,d] * k[j,b,d]
+ *     grad_w[s,b,h]   += g * max(dot_h, 0)
+ *     if dot_h > 0 (ReLU'(0) = 0):
+ *       grad_q[s,b,h,:] += g * w[s,b,h] * k[j,b,:]
+ *       grad_k[j,b,:]   += g * w[s,b,h] * q[s,b,h,:]
+ *   other slots (-1, out of range, not visible) contribute nothing.
+ *
+ * All in double, single-threaded (grad_k sums over rows).  abs_q, abs_k and
+ * abs_w (may be NULL) receive the same sums over the absolute values of the
+ * terms, the scale an implementation's rounding error is measured against.
+ * The outputs are overwritten (zeroed first).
+ */
+void oracle_indexer_bwd(const uint16_t *q, const uint16_t *k, const float *w,
+                        int S, int B, int H, int D, int S_kv, int ratio,
+                        int topk, const int32_t *q_pos, const int32_t *idx,
+                        const float *grad_scores, double *grad_q,
+                        double *grad_k, double *grad_w, double *abs_q,
+                        double *abs_k, double *abs_w)
+{
+    const size_t nq = (size_t)S * B * H * D, nk = (size_t)S_kv * B * D;
+    const size_t nw = (size_t)S * B * H;
+    memset(grad_q, 0, nq * sizeof(double));
+    memset(grad_k, 0, nk * sizeof(double));
+    memset(grad_w, 0, nw * sizeof(double));
+    if (abs_q) memset(abs_q, 0, nq * sizeof(double));
+    if (abs_k) memset(abs_k, 0, nk * sizeof(double));
+    if (abs_w) memset(abs_w, 0, nw * sizeof(double));
+    for (int b = 0; b < B; ++b) {
+        for (int s = 0; s < S; ++s) {
+            const long long t = row_position(q_pos, b, s);
+            for (int i = 0; i < topk; ++i) {
+                const size_t slot = ((size_t)b * S + s) * topk + i;
+                const long long j = idx[slot];
+                if (j < 0 || j >= S_kv || !oracle_key_visible(j, t, ratio))
+                    continue;
+                const double g = (double)grad_scores[slot];
+                const uint16_t *kj = k + ((size_t)j * B + b) * D;
+                for (int h = 0; h < H; ++h) {
+                    const size_t qo = (((size_t)s * B + b) * H + h) * D;
+                    double dot = 0.0;
+                    for (int d = 0; d < D; ++d)
+                        dot += bf16_to_double(q[qo + d]) * bf16_to_double(kj[d]);
+                    const size_t wo = ((size_t)s * B + b) * H + h;
+                    const double relu = dot > 0.0 ? dot : 0.0;
+                    grad_w[wo] += g * relu;
+                    if (abs_w) abs_w[wo] += fabs(g * relu);
+                    if (dot <= 0.0) continue;
+                    const double c = g * (double)w[wo];
+                    for (int d = 0; d < D; ++d) {
+                        const double tq = c * bf16_to_double(kj[d]);
+                        const double tk = c * bf16_to_double(q[qo + d]);
+                        grad_q[qo + d] += tq;
+                        grad_k[((size_t)j * B + b) * D + d] += tk;
+                        if (abs_q) abs_q[qo + d] += fabs(tq);
+                        if (abs_k) abs_k[((size_t)j * B + b) * D + d] += fabs(tk);
+                    }
+                }
+            }
+        }
+    }
+}

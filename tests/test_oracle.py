@@ -319,3 +319,97 @@ def test_workload_recipes_have_stated_shapes():
     assert dec.S_kv * dec.compress_ratio >= dec.pos_range[1]
     g = torch.Generator().manual_seed(0)
     assert abs(float(torch.randn(10000, generator=g).std()) - 1.0) < 0.05
+
+
+# ---------------------------------------------------------------------------
+# the backward: pinned to finite differences of the forward oracle
+
+
+def _bwd_case(seed, ratio):
+    rng = np.random.default_rng(seed)
+    S, B, H, D, S_kv, topk = 6, 2, 3, 5, 8, 5
+    q = rng.integers(-3, 4, size=(S, B, H, D)).astype(np.float32)
+    k = rng.integers(-3, 4, size=(S_kv, B, D)).astype(np.float32)
+    w = rng.choice([1.0, -1.0, 0.5, -0.5, 0.25], size=(S, B, H))
+    idx = rng.integers(-1, S_kv, size=(B, S, topk)).astype(np.int32)
+    idx[0, 3, 1] = idx[0, 3, 0]          # a repeated slot counts twice
+    idx[1, 0, 2] = S_kv - 1              # not visible at position 0
+    g = rng.choice([1.0, -2.0, 0.5, 3.0, -0.25], size=(B, S, topk))
+    return q, k, w.astype(np.float32), idx, g.astype(np.float32), ratio
+
+
+def _loss(q, k, w, ratio, idx, g):
+    import torch
+    out = oracle.indexer_fwd(torch.from_numpy(q).to(torch.bfloat16),
+                             torch.from_numpy(k).to(torch.bfloat16),
+                             torch.from_numpy(w), ratio, idx.shape[-1],
+                             in_idx=idx)
+    sc = out["scores64"].reshape(g.shape)
+    fin = np.isfinite(sc)
+    return float((g.astype(np.float64)[fin] * sc[fin]).sum())
+
+
+@pytest.mark.parametrize("seed,ratio", [(1, 1), (2, 2), (3, 1)])
+def test_backward_matches_finite_differences(seed, ratio):
+    import torch
+    q, k, w, idx, g, ratio = _bwd_case(seed, ratio)
+    bwd = oracle.indexer_bwd(torch.from_numpy(q).to(torch.bfloat16),
+                             torch.from_numpy(k).to(torch.bfloat16),
+                             torch.from_numpy(w), ratio, idx, g)
+    base = _loss(q, k, w, ratio, idx, g)
+    # w: the loss is linear in w, so a central difference is exact
+    eps = 2.0 ** -6
+    for pos in np.ndindex(w.shape):
+        wp, wm = w.copy(), w.copy()
+        wp[pos] += eps
+        wm[pos] -= eps
+        fd = (_loss(q, k, wp, ratio, idx, g) - _loss(q, k, wm, ratio, idx, g))
+        assert fd / (2 * eps) == pytest.approx(bwd["grad_w"][pos], abs=1e-9)
+    # q and k: piecewise linear in each entry.  A step of 2^-6 is exact in
+    # bf16 for |x| <= 3 and moves an integer dot product by at most 3/64, so
+    # only a dot that is exactly 0 can change sign.  ReLU has no derivative
+    # there, so entries that feed a zero dot of a scored slot are skipped
+    # (found by listing the dots; the expected value itself still comes only
+    # from the forward's differences).
+    B, S, topk = idx.shape
+    zero_q, zero_k = set(), set()
+    for b in range(B):
+        for s in range(S):
+            for i in range(topk):
+                j = int(idx[b, s, i])
+                if j < 0 or j >= k.shape[0] or not oracle.key_visible(j, s,
+                                                                      ratio):
+                    continue
+                for h in range(q.shape[2]):
+                    if float(q[s, b, h] @ k[j, b]) == 0.0:
+                        zero_q.add((s, b, h))
+                        zero_k.add((j, b))
+    for name, arr, grad in (("q", q, bwd["grad_q"]), ("k", k, bwd["grad_k"])):
+        checked = total = 0
+        for pos in np.ndindex(arr.shape):
+            total += 1
+            if (name == "q" and pos[:3] in zero_q) or \
+                    (name == "k" and pos[:2] in zero_k):
+                continue
+            ap, am = arr.copy(), arr.copy()
+            ap[pos] += eps
+            am[pos] -= eps
+            args_p = (ap, k) if name == "q" else (q, ap)
+            args_m = (am, k) if name == "q" else (q, am)
+            fp = (_loss(*args_p, w, ratio, idx, g) - base) / eps
+            fm = (base - _loss(*args_m, w, ratio, idx, g)) / eps
+            assert fp == pytest.approx(fm, abs=1e-9), (name, pos)
+            checked += 1
+            assert fp == pytest.approx(grad[pos], abs=1e-9), (name, pos)
+        assert checked >= total // 3, (name, checked, total)
+
+
+def test_backward_ignores_invalid_slots():
+    import torch
+    q, k, w, idx, g, ratio = _bwd_case(4, 1)
+    idx[:] = -1
+    bwd = oracle.indexer_bwd(torch.from_numpy(q).to(torch.bfloat16),
+                             torch.from_numpy(k).to(torch.bfloat16),
+                             torch.from_numpy(w), ratio, idx, g)
+    for n in ("grad_q", "grad_k", "grad_w"):
+        assert not bwd[n].any()
