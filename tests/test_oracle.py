@@ -413,3 +413,27 @@ def test_backward_ignores_invalid_slots():
                              torch.from_numpy(w), ratio, idx, g)
     for n in ("grad_q", "grad_k", "grad_w"):
         assert not bwd[n].any()
+
+
+def test_backward_closed_form_and_relu_convention():
+    """One slot, one head: a positive dot gives grad_q = g*w*k,
+    grad_k = g*w*q and grad_w = g*dot; a dot of exactly 0 contributes
+    nothing (the convention ReLU'(0) = 0)."""
+    import torch
+    k = np.array([[[1.0, 2.0, 0.0, -1.0]], [[1.0, 1.0, 1.0, 1.0]]],
+                 np.float32)                          # [S_kv=2, B=1, D=4]
+    q = np.array([[[[1.0, 1.0, 3.0, 0.0]]],           # dot with k0 = 3
+                  [[[1.0, -1.0, 0.0, 0.0]]]],         # dot with k1 = 0
+                 np.float32)                          # [S=2, B=1, H=1, D=4]
+    w = np.array([[[0.5]], [[-2.0]]], np.float32)
+    idx = np.array([[[0], [1]]], np.int32)            # [B, S, topk=1]
+    g = np.array([[[3.0], [5.0]]], np.float32)
+    bwd = oracle.indexer_bwd(torch.from_numpy(q).to(torch.bfloat16),
+                             torch.from_numpy(k).to(torch.bfloat16),
+                             torch.from_numpy(w), 1, idx, g)
+    np.testing.assert_array_equal(bwd["grad_q"][0, 0, 0], 3.0 * 0.5 * k[0, 0])
+    np.testing.assert_array_equal(bwd["grad_q"][1], 0.0)
+    np.testing.assert_array_equal(bwd["grad_k"][0, 0], 3.0 * 0.5 * q[0, 0, 0])
+    np.testing.assert_array_equal(bwd["grad_k"][1], 0.0)
+    assert bwd["grad_w"][0, 0, 0] == 3.0 * 3.0
+    assert bwd["grad_w"][1, 0, 0] == 0.0
