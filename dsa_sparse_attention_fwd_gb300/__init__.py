@@ -29,7 +29,7 @@ __all__ = [
     "dsa_status_string", "dsa_selftest_wait_limit", "v4_lighting_indexer",
     "indexer_logits", "dsa_indexer_host_buffer_size", "dsa_indexer_fwd_host",
     "dsa_indexer_varlen_workspace_size", "dsa_indexer_fwd_varlen",
-    "STATUS",
+    "dsa_indexer_bwd", "dsa_indexer_bwd_workspace_size", "STATUS",
 ]
 
 STATUS = {
@@ -94,6 +94,11 @@ def load_library(path: str | None = None):
         lib.dsa_indexer_fwd_host.restype = I
         lib.dsa_indexer_fwd_host.argtypes = [P, P, P, I, I, I, I, I, I, I, P,
                                              P, P, P, P, Z, P]
+        lib.dsa_indexer_bwd_workspace_size.restype = Z
+        lib.dsa_indexer_bwd_workspace_size.argtypes = []
+        lib.dsa_indexer_bwd.restype = I
+        lib.dsa_indexer_bwd.argtypes = [P, P, P, I, I, I, I, I, I, I, P, P, P,
+                                        P, P, P, P, Z, P]
         _lib = lib
         return lib
 
@@ -180,6 +185,46 @@ def dsa_indexer_fwd(q, k, w, compress_ratio, topk, q_pos=None, in_idx=None,
     if rc != 0:
         raise DsaError(rc, "dsa_indexer_fwd")
     return out_scores, out_idx, workspace
+
+
+def dsa_indexer_bwd_workspace_size() -> int:
+    return int(load_library().dsa_indexer_bwd_workspace_size())
+
+
+def dsa_indexer_bwd(q, k, w, compress_ratio, idx, grad_scores, q_pos=None,
+                    grad_q=None, grad_k=None, grad_w=None, workspace=None,
+                    stream=None):
+    """Enqueue the backward of the given-slots scores on device tensors:
+    idx [B, S, topk] int32 and grad_scores [B, S, topk] fp32 give grad_q
+    [S, B, H, D], grad_k [S_kv, B, D] and grad_w [S, B, H] (fp32).  Returns
+    (grad_q, grad_k, grad_w, workspace)."""
+    lib = load_library()
+    S, B, H, D, S_kv = _check_inputs(q, k, w, q_pos, idx)
+    topk = idx.shape[-1]
+    if tuple(idx.shape) != (B, S, topk):
+        raise ValueError("idx must be [B, S, topk]")
+    if (grad_scores.dtype != torch.float32 or not grad_scores.is_contiguous()
+            or tuple(grad_scores.shape) != (B, S, topk)):
+        raise ValueError("grad_scores must be contiguous fp32 [B, S, topk]")
+    dev = q.device
+    f32 = dict(dtype=torch.float32, device=dev)
+    if grad_q is None:
+        grad_q = torch.empty((S, B, H, D), **f32)
+    if grad_k is None:
+        grad_k = torch.empty((S_kv, B, D), **f32)
+    if grad_w is None:
+        grad_w = torch.empty((S, B, H), **f32)
+    if workspace is None:
+        workspace = torch.empty(dsa_indexer_bwd_workspace_size(),
+                                dtype=torch.uint8, device=dev)
+    rc = lib.dsa_indexer_bwd(
+        _ptr(q), _ptr(k), _ptr(w), S, B, H, D, S_kv, int(compress_ratio),
+        int(topk), _ptr(q_pos), _ptr(idx), _ptr(grad_scores), _ptr(grad_q),
+        _ptr(grad_k), _ptr(grad_w), _ptr(workspace), workspace.numel(),
+        _stream(stream))
+    if rc != 0:
+        raise DsaError(rc, "dsa_indexer_bwd")
+    return grad_q, grad_k, grad_w, workspace
 
 
 def dsa_indexer_logits(q, k, w, compress_ratio, q_pos=None, logits=None,

@@ -89,9 +89,12 @@ bool aligned16(const void *p) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
 }
 
+}  // namespace
+
+namespace dsa {
 // q [S, B, H, D] bf16 viewed as the 4-D tensor (d, h, b, s); one box is
 // 64 d x H heads x 1 sequence x `queries` queries (256/H for the prefill
-// tile = 256 rows of 128 bytes; 1 for decode).
+// tile = 256 rows of 128 bytes; 1 for decode, given indices and backward).
 int encode_q(CUtensorMap *m, const Problem &p, int queries) {
   auto fn = encode_fn();
   if (!fn) return DSA_ERR_CUDA;
@@ -110,6 +113,20 @@ int encode_q(CUtensorMap *m, const Problem &p, int queries) {
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? DSA_OK : DSA_ERR_UNSUPPORTED;
 }
+
+// Multiprocessor count of the current device (DSA_ERR_UNSUPPORTED unless
+// it is an sm_103 device).
+int device_num_sms(int *num_sms) {
+  DeviceInfo d;
+  const int rc = current_device_info(&d);
+  if (rc == DSA_OK) *num_sms = d.num_sms;
+  return rc;
+}
+
+}  // namespace dsa
+
+namespace {
+using dsa::encode_q;
 
 // k [S_kv, B, D] bf16 viewed as (d, b, j); one box is 64 d x 1 x 128 keys.
 int encode_k(CUtensorMap *m, const Problem &p) {

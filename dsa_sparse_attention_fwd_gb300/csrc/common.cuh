@@ -125,6 +125,13 @@ size_t decode_smem_bytes(int H, int D);
 
 cudaError_t launch_fill_masked(float *logits, size_t n, cudaStream_t st);
 
+// TMA map of q [S, B, H, D] bf16 as (d, h, b, s) with a box of 64 d x H
+// heads x 1 x `queries` (returns a dsa_status code).
+int encode_q(CUtensorMap *m, const Problem &p, int queries);
+
+// Multiprocessor count of the current device (a dsa_status code).
+int device_num_sms(int *num_sms);
+
 // The forward behind the C entry points (arguments and return codes of
 // dsa_indexer_fwd_profiled); clear_status = false keeps the workspace's
 // status word, so forwards sharing a workspace accumulate device errors.

@@ -1,0 +1,705 @@
+// indexer_bwd: gradients of the lightning-indexer scores taken at given
+// slots (the backward of V4IndexerFunction, "tilelang_indexer" page of NeMo
+// AutoModel: backward(grad_scores, grad_indices); the indices carry no
+// gradient).  For every slot (t, i) with a valid, visible key j = idx[t, i]
+// and upstream gradient g = grad_scores[t, i], the score
+//     I[t, j] = sum_h w[t, h] * ReLU(q[t, h, :] . k[j, :])
+// gives
+//     grad_w[t, h] += g * ReLU(s_h),                 s_h = q[t, h, :] . k[j, :]
+//     grad_q[t, h] += g * w[t, h] * [s_h > 0] * k[j]
+//     grad_k[j]    += g * w[t, h] * [s_h > 0] * q[t, h]
+// with ReLU'(0) = 0.
+//
+// A work item is one query row (all of its slots), a tile 128 consecutive
+// slots.  Per tile, on the tensor cores:
+//   MMA1   S[slot, h]   = K_g . Q^T        M = 128 slots, N = H, K = D
+//   (epilogue: G[slot, h] = g * w[h] * [S > 0] in bf16, into shared memory)
+//   MMA2   dQ^T[d, h]  += K_g^T . G        M = 128 (d), N = H, K = 128 slots
+//   MMA3   dK[slot, d]  = G . Q            M = 128 slots, N = 128 (d), K = H
+// K_g (the gathered keys) and Q are read twice, once K-major and once
+// MN-major, from the same shared-memory tiles; dQ^T accumulates in tensor
+// memory over the row's tiles and is written once per row; dK rows are
+// added into grad_k with vector atomics (a key is shared by many rows).
+// grad_w is reduced in registers over the row's slots.  D <= 128 runs as
+// D = 128 with zero padding; H = 64 (one 128-byte G row per slot).
+//
+// Warp roles (one CTA per SM, persistent): warp 0 index/gradient and query
+// fetch, warps 1..4 key gathers (16-byte cp.async, zero fill for masked
+// slots), warp 5 TMEM allocator and MMA issuer, warps 6..9 epilogue.
+// The MMA thread issues MMA1 of tile n + 1 before MMA2/MMA3 of tile n, so
+// the tensor core works on the next scores while the epilogue forms G.
+//
+// grad_q and grad_w are plain stores in a fixed order (deterministic);
+// grad_k accumulates with atomics, so its rounding depends on their order.
+#include "common.cuh"
+#include "dsa_indexer.h"
+#include "ptx.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr int kBwdH = 64;
+constexpr int kBwdGatWarps = 4;
+constexpr int kBwdThreads = 32 * (kBwdGatWarps + 6);
+constexpr int kBwdMmaWarp = kBwdGatWarps + 1;
+constexpr int kBwdEpiWarp0 = kBwdGatWarps + 2;  // first of four
+constexpr int kBwdStages = 4;                   // gathered key stages
+constexpr int kBwdRing = 16;                    // index/gradient ring (tiles)
+
+struct BwdSmem {
+  static constexpr int kQBytes = 2 * kBwdH * 128;      // two d-chunks of 64
+  static constexpr int kKBytes = 2 * kTileKeys * 128;  // two d-chunks of 64
+  static constexpr int kGBytes = kTileKeys * 128;      // 128 slots x 64 heads
+  static constexpr int kRingBytes = kTileKeys * 8;     // indices, gradients
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + 2 * kQBytes;
+  static constexpr int kOffG = kOffK + kBwdStages * kKBytes;
+  static constexpr int kOffRing = kOffG + 2 * kGBytes;
+  static constexpr int kOffW = kOffRing + kBwdRing * kRingBytes;  // [2][H]
+  static constexpr int kOffGW = kOffW + 2 * kBwdH * 4;            // [4][H]
+  static constexpr int kOffBar = kOffGW + 4 * kBwdH * 4;
+  // k_full[4] k_empty[4] q_full[2] q_empty[2] r_full[16] r_empty[16]
+  // s_full[2] s_empty[2] g_full[2] g_empty[2] dk_full[2] dk_empty[2]
+  // dq_full[2] dq_empty[2]
+  static constexpr int kBarPairs = 8;  // s, g, dk, dq: full/empty pairs
+  static constexpr int kNumBars =
+      2 * kBwdStages + 4 + 2 * kBwdRing + 2 * kBarPairs;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kBytes = kOffMisc + 16;
+  static constexpr int kAlloc = kBytes + 1024;
+};
+static_assert(BwdSmem::kAlloc <= 227 * 1024, "fits one CTA per SM");
+
+// TMEM columns: S x2 (64 each), dQ^T x2 (64 each), dK x2 (128 each).
+constexpr uint32_t kTmemS = 0, kTmemDq = 128, kTmemDk = 256;
+constexpr uint32_t kBwdTmemCols = 512;
+
+struct BwdGeom {
+  int rows, S, ntiles;
+};
+
+// Walks this CTA's tiles: rows round by round (zig-zag over the CTAs), each
+// row's tiles in order.  Every role walks the same sequence.
+struct BwdCursor {
+  int round, row, b, s, tile;
+  bool valid;
+};
+
+__device__ __forceinline__ void bwd_set_row(BwdCursor &c, const BwdGeom &g) {
+  const int G = gridDim.x, cta = blockIdx.x;
+  const long long r =
+      (long long)c.round * G + ((c.round & 1) ? (G - 1 - cta) : cta);
+  c.valid = r < g.rows;
+  if (!c.valid) return;
+  c.row = (int)r;
+  c.b = c.row / g.S;
+  c.s = c.row % g.S;
+  c.tile = 0;
+}
+
+__device__ __forceinline__ BwdCursor bwd_begin(const BwdGeom &g) {
+  BwdCursor c;
+  c.round = 0;
+  bwd_set_row(c, g);
+  return c;
+}
+
+// Advances by one tile; returns true when a new row starts.
+__device__ __forceinline__ bool bwd_next(BwdCursor &c, const BwdGeom &g) {
+  if (++c.tile < g.ntiles) return false;
+  ++c.round;
+  bwd_set_row(c, g);
+  return true;
+}
+
+// The MMA2/MMA3 half of a tile, issued after the next tile's MMA1.
+struct BwdPending {
+  uint32_t n;     // the tile's sequence number in this CTA
+  int kst, qs;    // its key stage and query slot
+  int dq;         // dQ^T accumulator of its row (row parity)
+  uint32_t dqph;  // phase of that accumulator's barriers
+  bool first, last;
+};
+
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    indexer_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const uint8_t *__restrict__ k,
+                       const float *__restrict__ w,
+                       const int32_t *__restrict__ q_pos,
+                       const int32_t *__restrict__ idx,
+                       const float *__restrict__ grad_scores, BwdGeom g,
+                       int B, int D, int S_kv, int ratio, int topk,
+                       float *__restrict__ grad_q, float *__restrict__ grad_k,
+                       float *__restrict__ grad_w, int *status) {
+  using L = BwdSmem;
+  constexpr int H = kBwdH;
+  constexpr int NS = kBwdStages;
+  // MMA1: both K-major.  MMA2: A = gathered keys read d-major, B = G read
+  // head-major.  MMA3: A = G K-major (heads), B = Q read d-major.
+  constexpr uint32_t kIdescS = idesc_bf16_f32(kTileKeys, H);
+  constexpr uint32_t kIdescDq = idesc_bf16_f32_mn(128, H, true, true);
+  constexpr uint32_t kIdescDk = idesc_bf16_f32_mn(kTileKeys, 128, false, true);
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t *smem = smem_raw + (base - raw_addr);
+  const uint32_t sQ = base + L::kOffQ;
+  const uint32_t sK = base + L::kOffK;
+  const uint32_t sG = base + L::kOffG;
+  const uint8_t *sRing = smem + L::kOffRing;
+  float *sW = reinterpret_cast<float *>(smem + L::kOffW);
+  float *sGW = reinterpret_cast<float *>(smem + L::kOffGW);
+  const uint32_t bars = base + L::kOffBar;
+  auto bar = [&](int i) { return bars + 8u * i; };
+  auto k_full = [&](int i) { return bar(i); };
+  auto k_empty = [&](int i) { return bar(NS + i); };
+  auto q_full = [&](int i) { return bar(2 * NS + i); };
+  auto q_empty = [&](int i) { return bar(2 * NS + 2 + i); };
+  auto r_full = [&](int i) { return bar(2 * NS + 4 + i); };
+  auto r_empty = [&](int i) { return bar(2 * NS + 4 + kBwdRing + i); };
+  constexpr int kB2 = 2 * NS + 4 + 2 * kBwdRing;
+  auto s_full = [&](int i) { return bar(kB2 + i); };
+  auto s_empty = [&](int i) { return bar(kB2 + 2 + i); };
+  auto g_full = [&](int i) { return bar(kB2 + 4 + i); };
+  auto g_empty = [&](int i) { return bar(kB2 + 6 + i); };
+  auto dk_full = [&](int i) { return bar(kB2 + 8 + i); };
+  auto dk_empty = [&](int i) { return bar(kB2 + 10 + i); };
+  auto dq_full = [&](int i) { return bar(kB2 + 12 + i); };
+  auto dq_empty = [&](int i) { return bar(kB2 + 14 + i); };
+  static_assert(kB2 + 14 + 1 < L::kNumBars, "every barrier has its slot");
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kOffMisc);
+  volatile int *abort_flag = reinterpret_cast<int *>(smem + L::kOffMisc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Q chunks the fetch warp loads; with D <= 64 the second chunk of both Q
+  // slots stays zero (written once here), so the padded d never contributes
+  const int q_chunks = D > kChunk ? 2 : 1;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(k_full(i), 32 * kBwdGatWarps);  // one per gather lane
+      mbar_init(k_empty(i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(q_full(i), 1);
+      mbar_init(q_empty(i), 1);
+      mbar_init(s_full(i), 1);
+      mbar_init(s_empty(i), 4);  // epilogue warps
+      mbar_init(g_full(i), 4);
+      mbar_init(g_empty(i), 1);
+      mbar_init(dk_full(i), 1);
+      mbar_init(dk_empty(i), 4);
+      mbar_init(dq_full(i), 1);
+      mbar_init(dq_empty(i), 4);
+    }
+    for (int i = 0; i < kBwdRing; ++i) {
+      mbar_init(r_full(i), 32);  // one cp.async arrival per fetch lane
+      mbar_init(r_empty(i), 4);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+  }
+  if (q_chunks == 1) {
+    for (int o = threadIdx.x * 16; o < 2 * H * 128; o += kBwdThreads * 16) {
+      const int slot = o / (H * 128), off = o % (H * 128);
+      *reinterpret_cast<uint4 *>(smem + L::kOffQ + slot * L::kQBytes +
+                                 H * 128 + off) = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+  }
+  if (warp == kBwdMmaWarp) {
+    tmem_alloc(smem_u32(tmem_holder), kBwdTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0) {
+    // ---------------- index, gradient and query fetch ----------------
+    BwdCursor f = bwd_begin(g);
+    uint32_t nr = 0, nq = 0;
+    bool row_start = true;
+    while (f.valid) {
+      if (row_start) {
+        const int qs = nq & 1;
+        const uint32_t qph = (nq >> 1) & 1u;
+        ++nq;
+        if (!__all_sync(0xffffffffu,
+                        wait_bar(q_empty(qs), qph ^ 1u, abort_flag, status)))
+          break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(q_full(qs), q_chunks * H * 128);
+          for (int cc = 0; cc < q_chunks; ++cc)
+            tma_load_4d(sQ + qs * L::kQBytes + cc * (H * 128), &tm_q,
+                        q_full(qs), cc * kChunk, 0, f.b, f.s);
+        }
+      }
+      const int slot = nr % kBwdRing;
+      const uint32_t ph = (nr / kBwdRing) & 1u;
+      if (!__all_sync(0xffffffffu,
+                      wait_bar(r_empty(slot), ph ^ 1u, abort_flag, status)))
+        break;
+      const size_t off = (size_t)f.row * topk + (size_t)f.tile * kTileKeys;
+      const int cnt = topk - f.tile * kTileKeys;
+      const uint32_t dst = base + L::kOffRing + slot * L::kRingBytes;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = lane + 32 * u;
+        if (i < cnt) {
+          cp_async4(dst + 4 * i, idx + off + i);
+          cp_async4(dst + 4 * (kTileKeys + i), grad_scores + off + i);
+        }
+      }
+      cp_async_arrive_noinc(r_full(slot));
+      ++nr;
+      row_start = bwd_next(f, g);
+    }
+    // nothing may land in shared memory after the CTA is gone
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  } else if (warp <= kBwdGatWarps) {
+    // ---------------- key gathers ----------------
+    constexpr int kSegs = 16;               // 16-byte pieces of a stage row
+    constexpr int kRowsPerOp = 32 / kSegs;  // rows one warp-wide copy covers
+    constexpr int kRows = kTileKeys / kBwdGatWarps;
+    constexpr int kOps = kRows / kRowsPerOp;
+    const int gw = warp - 1;
+    const int seg = lane % kSegs, sub = lane / kSegs;
+    const int c = seg >> 3, s8 = seg & 7;
+    // D is a multiple of 8, so every 16-byte piece is all key or all padding
+    const uint32_t seg_bytes = seg * 16 < D * 2 ? 16u : 0u;
+    const size_t seg_off = seg_bytes ? (size_t)seg * 16 : 0;
+    const size_t key_stride = (size_t)B * D * 2;
+    BwdCursor cur = bwd_begin(g);
+    uint32_t ng = 0, kst = 0, kph = 0;
+    while (cur.valid) {
+      const int slot = ng % kBwdRing;
+      const uint32_t rph = (ng / kBwdRing) & 1u;
+      if (!__all_sync(0xffffffffu,
+                      wait_bar(r_full(slot), rph, abort_flag, status)))
+        break;
+      if (!__all_sync(0xffffffffu,
+                      wait_bar(k_empty(kst), kph ^ 1u, abort_flag, status)))
+        break;
+      const int32_t *sIdx =
+          reinterpret_cast<const int32_t *>(sRing + slot * L::kRingBytes);
+      const uint32_t stage = sK + kst * L::kKBytes + c * (kTileKeys * 128);
+      const uint8_t *kb = k + (size_t)cur.b * D * 2 + seg_off;
+      const int r0 = gw * kRows + sub;
+      const int live = topk - cur.tile * kTileKeys;
+      int js[kOps];
+#pragma unroll
+      for (int u = 0; u < kOps; ++u) {
+        const int rr = r0 + u * kRowsPerOp;
+        const int j = rr < live ? sIdx[rr] : -1;
+        js[u] = (j < 0 || j >= S_kv) ? -1 : j;
+      }
+#pragma unroll
+      for (int u = 0; u < kOps; ++u) {
+        const int rr = r0 + u * kRowsPerOp;
+        const bool valid = js[u] >= 0;
+        cp_async16_zfill(stage + rr * 128 + ((s8 ^ (rr & 7)) << 4),
+                         kb + (valid ? (size_t)js[u] * key_stride : 0),
+                         valid ? seg_bytes : 0u);
+      }
+      cp_async_arrive_noinc(k_full(kst));
+      if (++kst == NS) {
+        kst = 0;
+        kph ^= 1u;
+      }
+      ++ng;
+      bwd_next(cur, g);
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  } else if (warp == kBwdMmaWarp) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      // MMA2 and MMA3 of a finished tile: dQ^T += K_g^T G, dK = G Q
+      auto issue_back = [&](const BwdPending &p) -> bool {
+        const int gb = p.n & 1;
+        const uint32_t gph = (p.n >> 1) & 1u;
+        if (!wait_bar(g_full(gb), gph, abort_flag, status)) return false;
+        if (!wait_bar(dk_empty(gb), gph ^ 1u, abort_flag, status))
+          return false;
+        if (p.first &&
+            !wait_bar(dq_empty(p.dq), p.dqph ^ 1u, abort_flag, status))
+          return false;
+        tc_fence_after();
+        const uint32_t sGb = sG + gb * L::kGBytes;
+        const uint32_t sKs = sK + p.kst * L::kKBytes;
+        const uint32_t sQs = sQ + p.qs * L::kQBytes;
+        // K = 128 slots in steps of 16 (two 8-slot atoms, 2048 bytes)
+#pragma unroll
+        for (int ks = 0; ks < kTileKeys / 16; ++ks) {
+          const uint64_t ad =
+              sdesc_mn_sw128(sKs + ks * 2048, kTileKeys * 128, 1024);
+          // N = 64 is one atom, so the atom stride along N is never used
+          const uint64_t bd = sdesc_mn_sw128(sGb + ks * 2048, 1024, 1024);
+          mma_bf16(tmem + kTmemDq + p.dq * H, ad, bd, kIdescDq,
+                   (p.first && ks == 0) ? 0u : 1u);
+        }
+        // K = 64 heads in steps of 16
+#pragma unroll
+        for (int kk = 0; kk < H / 16; ++kk) {
+          const uint64_t ad = sdesc_k_sw128(sGb + kk * 32);
+          const uint64_t bd = sdesc_mn_sw128(sQs + kk * 2048, H * 128, 1024);
+          mma_bf16(tmem + kTmemDk + gb * 128, ad, bd, kIdescDk,
+                   kk != 0 ? 1u : 0u);
+        }
+        mma_commit(k_empty(p.kst));
+        mma_commit(g_empty(gb));
+        mma_commit(dk_full(gb));
+        if (p.last) {
+          mma_commit(dq_full(p.dq));
+          mma_commit(q_empty(p.qs));
+        }
+        return true;
+      };
+
+      BwdCursor cur = bwd_begin(g);
+      uint32_t kst = 0, kph = 0, nq = 0, n = 0, nrow = 0;
+      bool row_start = true, ok = true, pend = false;
+      BwdPending pd{};
+      int qs = 0;
+      while (cur.valid) {
+        if (row_start) {
+          qs = nq & 1;
+          const uint32_t qph = (nq >> 1) & 1u;
+          ++nq;
+          if (!wait_bar(q_full(qs), qph, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+        }
+        const int sa = n & 1;
+        const uint32_t sph = (n >> 1) & 1u;
+        if (!wait_bar(s_empty(sa), sph ^ 1u, abort_flag, status) ||
+            !wait_bar(k_full(kst), kph, abort_flag, status)) {
+          ok = false;
+          break;
+        }
+        // the stage was written by cp.async (generic proxy)
+        fence_proxy_async_smem();
+        tc_fence_after();
+        const uint32_t sQs = sQ + qs * L::kQBytes;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+#pragma unroll
+          for (int kk = 0; kk < kChunk / 16; ++kk) {
+            const uint64_t ad = sdesc_k_sw128(sK + kst * L::kKBytes +
+                                              cc * (kTileKeys * 128) + kk * 32);
+            const uint64_t bd = sdesc_k_sw128(sQs + cc * (H * 128) + kk * 32);
+            mma_bf16(tmem + kTmemS + sa * H, ad, bd, kIdescS,
+                     (cc | kk) != 0 ? 1u : 0u);
+          }
+        }
+        mma_commit(s_full(sa));
+        if (pend && !issue_back(pd)) {
+          ok = false;
+          break;
+        }
+        pd.n = n;
+        pd.kst = kst;
+        pd.qs = qs;
+        pd.dq = nrow & 1;
+        pd.dqph = (nrow >> 1) & 1u;
+        pd.first = cur.tile == 0;
+        pd.last = cur.tile + 1 == g.ntiles;
+        pend = true;
+        if (pd.last) ++nrow;
+        ++n;
+        if (++kst == NS) {
+          kst = 0;
+          kph ^= 1u;
+        }
+        row_start = bwd_next(cur, g);
+      }
+      if (ok && pend) issue_back(pd);
+    }
+  } else {
+    // ---------------- epilogue (warps kBwdEpiWarp0 .. kBwdEpiWarp0 + 3) ------
+    const int sp = warp & 3;                       // TMEM sub-partition
+    const int et = threadIdx.x - 32 * kBwdEpiWarp0;  // 0..127
+    const int i = sp * 32 + lane;  // TMEM lane: the slot, or d for dQ^T
+    const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
+    BwdCursor cur = bwd_begin(g);
+    uint32_t n = 0, nrow = 0;
+    bool ok = true;
+    float w_next = 0.f;
+    if (cur.valid && et < H)
+      w_next = __ldg(w + ((size_t)cur.s * B + cur.b) * H + et);
+    // the previous tile's dK rows, added into grad_k after this tile's G
+    bool dk_pend = false, dk_live = false;
+    uint32_t dk_n = 0;
+    float *dk_dst = grad_k;
+    auto drain_dk = [&]() -> bool {
+      const int db = dk_n & 1;
+      const uint32_t dph = (dk_n >> 1) & 1u;
+      if (!__all_sync(0xffffffffu,
+                      wait_bar(dk_full(db), dph, abort_flag, status)))
+        return false;
+      tc_fence_after();
+      const uint32_t ta = tmem + lane_off + kTmemDk + db * 128;
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t v[32];
+        __syncwarp();
+        tmem_ld32(ta + c4 * 32, v);
+        tmem_ld_wait();
+        reg_fence32(v);
+        if (dk_live) {
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {
+            const int d = c4 * 32 + q4 * 4;
+            if (d < D)
+              red_add_v4(dk_dst + d, __uint_as_float(v[4 * q4]),
+                         __uint_as_float(v[4 * q4 + 1]),
+                         __uint_as_float(v[4 * q4 + 2]),
+                         __uint_as_float(v[4 * q4 + 3]));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dk_empty(db));
+      return true;
+    };
+
+    while (cur.valid) {
+      float *sWi = sW + (nrow & 1u) * H;
+      if (et < H) sWi[et] = w_next;
+      // every epilogue warp stored its weights, or one of them gave up
+      if (named_bar_or(1, 128, !ok)) break;
+      const int b = cur.b, s = cur.s;
+      const int nv = n_visible(row_pos(q_pos, b, s), ratio, S_kv);
+      const float4 *w4 = reinterpret_cast<const float4 *>(sWi);
+      float gwa[H];
+#pragma unroll
+      for (int h = 0; h < H; ++h) gwa[h] = 0.f;
+      bool bad = false, row_end = false;
+      while (!row_end) {
+        const int slot = n % kBwdRing;
+        const uint32_t rph = (n / kBwdRing) & 1u;
+        const int sa = n & 1;
+        const uint32_t sph = (n >> 1) & 1u;
+        const bool got = wait_bar(s_full(sa), sph, abort_flag, status) &&
+                         wait_bar(r_full(slot), rph, abort_flag, status);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t v[2][32];
+        tmem_ld32(tmem + lane_off + kTmemS + sa * H, v[0]);
+        tmem_ld32(tmem + lane_off + kTmemS + sa * H + 32, v[1]);
+        tmem_ld_wait();
+        reg_fence32(v[0]);
+        reg_fence32(v[1]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_empty(sa));
+        const int e = cur.tile * kTileKeys + i;  // slot within the row
+        const bool in_row = e < topk;
+        const uint8_t *rs = sRing + slot * L::kRingBytes;
+        const int j = in_row ? reinterpret_cast<const int32_t *>(rs)[i] : -1;
+        const float gs =
+            in_row ? reinterpret_cast<const float *>(rs + kTileKeys * 4)[i]
+                   : 0.f;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(r_empty(slot));
+        bad |= in_row && (j < -1 || j >= S_kv);
+        const bool valid = j >= 0 && j < nv;
+        const float ge = valid ? gs : 0.f;
+        // this G buffer is free once MMA2/MMA3 of tile n - 2 are done
+        if (!__all_sync(0xffffffffu,
+                        wait_bar(g_empty(sa), sph ^ 1u, abort_flag, status))) {
+          ok = false;
+          break;
+        }
+        // G[slot, h] = g * w[h] * [S > 0] (bf16, 128-byte swizzled row) and
+        // the slot's share of grad_w[h] = sum g * ReLU(S)
+        const uint32_t grow = sG + sa * L::kGBytes + i * 128;
+        bool any = false;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int hq = 0; hq < 2; ++hq) {
+            const int h = u * 8 + hq * 4;
+            const float4 wv = w4[h >> 2];
+            const float x0 = __uint_as_float(v[h >> 5][h & 31]);
+            const float x1 = __uint_as_float(v[h >> 5][(h + 1) & 31]);
+            const float x2 = __uint_as_float(v[h >> 5][(h + 2) & 31]);
+            const float x3 = __uint_as_float(v[h >> 5][(h + 3) & 31]);
+            gwa[h] = fmaf(ge, fmaxf(x0, 0.f), gwa[h]);
+            gwa[h + 1] = fmaf(ge, fmaxf(x1, 0.f), gwa[h + 1]);
+            gwa[h + 2] = fmaf(ge, fmaxf(x2, 0.f), gwa[h + 2]);
+            gwa[h + 3] = fmaf(ge, fmaxf(x3, 0.f), gwa[h + 3]);
+            any |= (x0 > 0.f) | (x1 > 0.f) | (x2 > 0.f) | (x3 > 0.f);
+            pk[2 * hq] = pack_bf16x2(x0 > 0.f ? ge * wv.x : 0.f,
+                                     x1 > 0.f ? ge * wv.y : 0.f);
+            pk[2 * hq + 1] = pack_bf16x2(x2 > 0.f ? ge * wv.z : 0.f,
+                                         x3 > 0.f ? ge * wv.w : 0.f);
+          }
+          st_shared_v4(grow + ((u ^ (i & 7)) << 4), pk);
+        }
+        // the tensor core (async proxy) reads G next
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(g_full(sa));
+        if (dk_pend && !drain_dk()) {
+          ok = false;
+          break;
+        }
+        dk_pend = true;
+        dk_n = n;
+        dk_live = valid && any && ge != 0.f;
+        dk_dst = grad_k + ((size_t)(dk_live ? j : 0) * B + b) * D;
+        ++n;
+        row_end = bwd_next(cur, g);
+      }
+      // every warp finished the row's tiles, or one of them gave up
+      if (named_bar_or(2, 128, !ok)) break;
+      // the row's last dK rows, then dQ and grad_w
+      dk_pend = false;
+      ok = drain_dk();
+      const int dq = nrow & 1;
+      const uint32_t dqph = (nrow >> 1) & 1u;
+      if (ok)
+        ok = __all_sync(0xffffffffu,
+                        wait_bar(dq_full(dq), dqph, abort_flag, status));
+      if (ok) {
+        tc_fence_after();
+        float *gq = grad_q + ((size_t)s * B + b) * H * D;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t v[32];
+          __syncwarp();
+          tmem_ld32(tmem + lane_off + kTmemDq + dq * H + c * 32, v);
+          tmem_ld_wait();
+          reg_fence32(v);
+          // lane = d: each store instruction writes 32 consecutive d of one h
+          if (i < D) {
+#pragma unroll
+            for (int hh = 0; hh < 32; ++hh)
+              gq[(size_t)(c * 32 + hh) * D + i] = __uint_as_float(v[hh]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(dq_empty(dq));
+      }
+      // grad_w: halve the 64 partial sums over the lanes five times (each
+      // lane keeps the half its lane bit selects), leaving heads 2*lane and
+      // 2*lane + 1 in gwa[0..1]; then add the four warps in a fixed order
+#pragma unroll
+      for (int o = 16, m = H; o >= 1; o >>= 1, m >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int h = 0; h < m / 2; ++h) {
+          const float send = up ? gwa[h] : gwa[h + m / 2];
+          const float keep = up ? gwa[h + m / 2] : gwa[h];
+          gwa[h] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+      }
+      sGW[sp * H + 2 * lane] = gwa[0];
+      sGW[sp * H + 2 * lane + 1] = gwa[1];
+      named_bar_sync(3, 128);
+      if (et < H)
+        grad_w[((size_t)s * B + b) * H + et] =
+            ((sGW[et] + sGW[H + et]) + sGW[2 * H + et]) + sGW[3 * H + et];
+      if (__any_sync(0xffffffffu, bad) && lane == 0)
+        atomicOr(status, kStatusIndexRange);
+      ++nrow;
+      // the next row's weight (cur already points at it)
+      if (cur.valid && et < H)
+        w_next = __ldg(w + ((size_t)cur.s * B + cur.b) * H + et);
+    }
+  }
+
+  __syncthreads();
+  if (warp == kBwdMmaWarp) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kBwdTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_indexer_bwd(const Problem &p, const CUtensorMap &tm_q,
+                               const int32_t *idx, const float *grad_scores,
+                               int topk, float *grad_q, float *grad_k,
+                               float *grad_w, int *status, int num_sms,
+                               cudaStream_t st) {
+  if (p.H != kBwdH || p.D > 2 * kChunk) return cudaErrorNotSupported;
+  const int smem = BwdSmem::kAlloc;
+  cudaError_t e = cudaFuncSetAttribute(
+      indexer_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  BwdGeom g;
+  g.rows = p.B * p.S;
+  g.S = p.S;
+  g.ntiles = (topk + kTileKeys - 1) / kTileKeys;
+  if (g.rows <= 0) return cudaSuccess;
+  const int grid = g.rows < num_sms ? g.rows : num_sms;
+  indexer_bwd_kernel<<<grid, kBwdThreads, smem, st>>>(
+      tm_q, static_cast<const uint8_t *>(p.k), p.w, p.q_pos, idx, grad_scores,
+      g, p.B, p.D, p.S_kv, p.ratio, topk, grad_q, grad_k, grad_w, status);
+  return cudaGetLastError();
+}
+
+}  // namespace dsa
+
+extern "C" {
+
+size_t dsa_indexer_bwd_workspace_size(void) { return 256; }
+
+int dsa_indexer_bwd(const void *q, const void *k, const float *w, int S,
+                    int B, int H, int D, int S_kv, int compress_ratio,
+                    int topk, const int32_t *q_pos, const int32_t *idx,
+                    const float *grad_scores, float *grad_q, float *grad_k,
+                    float *grad_w, void *workspace, size_t workspace_bytes,
+                    void *cuda_stream) {
+  if (!q || !k || !w || !idx || !grad_scores || !grad_q || !grad_k ||
+      !grad_w)
+    return DSA_ERR_INVALID_ARG;
+  if (S <= 0 || B <= 0 || H <= 0 || D <= 0 || S_kv <= 0 ||
+      compress_ratio <= 0 || topk <= 0)
+    return DSA_ERR_INVALID_ARG;
+  if (H != 64 || D % 8 != 0 || D > 128) return DSA_ERR_UNSUPPORTED;
+  if ((long long)B * S >= (1ll << 31) || topk > (1 << 30))
+    return DSA_ERR_UNSUPPORTED;
+  auto al = [](const void *p, unsigned a) {
+    return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+  };
+  if (!al(q, 16) || !al(k, 16) || !al(grad_k, 16) || !al(w, 4) ||
+      !al(idx, 4) || !al(grad_scores, 4) || !al(grad_q, 4) ||
+      !al(grad_w, 4) || (q_pos && !al(q_pos, 4)))
+    return DSA_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < dsa_indexer_bwd_workspace_size())
+    return DSA_ERR_WORKSPACE;
+  if (!al(workspace, 256)) return DSA_ERR_INVALID_ARG;
+  int num_sms = 0;
+  int rc = dsa::device_num_sms(&num_sms);
+  if (rc != DSA_OK) return rc;
+  dsa::Problem p{q, k, w, q_pos, S, B, H, D, S_kv, compress_ratio};
+  CUtensorMap tm_q;
+  rc = dsa::encode_q(&tm_q, p, 1);
+  if (rc != DSA_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  int *status = static_cast<int *>(workspace);
+  if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess ||
+      cudaMemsetAsync(grad_k, 0, (size_t)S_kv * B * D * sizeof(float), st) !=
+          cudaSuccess)
+    return DSA_ERR_CUDA;
+  if (dsa::launch_indexer_bwd(p, tm_q, idx, grad_scores, topk, grad_q, grad_k,
+                              grad_w, status, num_sms, st) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  return DSA_OK;
+}
+
+}  // extern "C"

@@ -192,6 +192,23 @@ __device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
   return d;
 }
 
+// Shared-memory matrix descriptor with the 128-byte swizzle and explicit
+// offsets, for MN-major operands: the operand is stored as rows of 128 bytes
+// (64 bf16 along M or N) with one row per k, in 1024-byte atoms of 8 k;
+// `lbo` is the byte distance between atoms along M/N (the next 64 of M or
+// N), `sbo` the distance between atoms along K (the next 8 of k).  The start
+// address stays atom-aligned; one MMA's K = 16 spans two atoms.
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr, uint32_t lbo,
+                                                   uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1u << 46;
+  d |= (uint64_t)2u << 61;
+  return d;
+}
+
 // Instruction descriptor, kind::f16: bf16 x bf16 -> fp32, both K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4)                     // D format: f32
@@ -199,6 +216,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          | (1u << 10)                  // B format: bf16
          | ((uint32_t)(N >> 3) << 17)  // N / 8
          | ((uint32_t)(M >> 4) << 24); // M / 16
+}
+
+// As idesc_bf16_f32, with A and/or B read MN-major (M, resp. N, the
+// contiguous dimension of the stored operand).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_mn(int M, int N, bool a_mn,
+                                                         bool b_mn) {
+  return idesc_bf16_f32(M, N) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
@@ -275,6 +299,30 @@ __device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
                  "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]),
                  "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
                  "+r"(r[14]), "+r"(r[15]));
+}
+
+// Atomic add of four consecutive fp32 (16-byte aligned) in global memory,
+// without a return value.
+__device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c,
+                                           float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p),
+               "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+// Two fp32 rounded to bf16 (round to nearest even), `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// 16-byte store to shared memory.
+__device__ __forceinline__ void st_shared_v4(uint32_t addr,
+                                             const uint32_t (&v)[4]) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+               "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3])
+               : "memory");
 }
 
 // Named barrier that also ORs a predicate over its participants, so a set

@@ -294,6 +294,45 @@ DSA_API int dsa_indexer_fwd_static_scratch(
     const int32_t *in_idx, int32_t *out_idx, float *out_scores,
     int32_t *out_status, void *cuda_stream);
 
+/*
+ * Backward of the given-slots scores (V4IndexerFunction.backward(grad_scores,
+ * grad_indices) on the NeMo AutoModel "tilelang_indexer" page; the indices
+ * are integers and get no gradient).  With s_h = q[t,h,:] . k[j,:] and
+ * g = grad_scores[b, s, i] for each slot i of row (b, s) whose key
+ * j = idx[b, s, i] is valid (0 <= j < S_kv) and visible to the row:
+ *     grad_w[s, b, h] += g * ReLU(s_h)
+ *     grad_q[s, b, h] += g * w[s, b, h] * [s_h > 0] * k[j, b]
+ *     grad_k[j, b]    += g * w[s, b, h] * [s_h > 0] * q[s, b, h]
+ * (ReLU'(0) taken as 0).  Slots holding -1, an invisible key or an index
+ * outside [-1, S_kv) contribute nothing; the last also sets
+ * DSA_ERR_INDEX_RANGE in the status word.  Duplicate indices in a row
+ * contribute once per slot.
+ *
+ *   q [S, B, H, D] bf16, k [S_kv, B, D] bf16, w [S, B, H] fp32 and q_pos
+ *   (nullable) as for dsa_indexer_fwd(); idx [B, S, topk] int32;
+ *   grad_scores [B, S, topk] fp32.
+ *   Outputs (fp32, caller-owned device memory, every element written):
+ *   grad_q [S, B, H, D], grad_k [S_kv, B, D] (cleared by the call, then
+ *   accumulated with atomics, so its low-order bits vary from run to run),
+ *   grad_w [S, B, H].
+ *   Precision: the scores are accumulated in fp32; g * w is rounded to bf16
+ *   as an operand of the two gradient products, which accumulate in fp32.
+ *   Envelope: H = 64, D a multiple of 8 up to 128; otherwise
+ *   DSA_ERR_UNSUPPORTED.  q, k and grad_k 16-byte aligned.
+ *   workspace: dsa_indexer_bwd_workspace_size() bytes, 256-byte aligned
+ *   (the status header; read it with dsa_indexer_check()).
+ * Asynchronous on `cuda_stream`; argument errors are returned before any
+ * work is enqueued.
+ */
+DSA_API size_t dsa_indexer_bwd_workspace_size(void);
+DSA_API int dsa_indexer_bwd(const void *q, const void *k, const float *w,
+                            int S, int B, int H, int D, int S_kv,
+                            int compress_ratio, int topk,
+                            const int32_t *q_pos, const int32_t *idx,
+                            const float *grad_scores, float *grad_q,
+                            float *grad_k, float *grad_w, void *workspace,
+                            size_t workspace_bytes, void *cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif

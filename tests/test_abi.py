@@ -50,6 +50,11 @@ def lib():
     L.dsa_indexer_fwd_host.restype = I
     L.dsa_indexer_fwd_host.argtypes = [P, P, P, I, I, I, I, I, I, I, P, P, P,
                                        P, P, Z, P]
+    L.dsa_indexer_bwd_workspace_size.restype = Z
+    L.dsa_indexer_bwd_workspace_size.argtypes = []
+    L.dsa_indexer_bwd.restype = I
+    L.dsa_indexer_bwd.argtypes = [P, P, P, I, I, I, I, I, I, I, P, P, P, P, P,
+                                  P, P, Z, P]
     return L
 
 
@@ -260,3 +265,26 @@ def test_varlen_rejects_bad_arguments(lib):
     assert call(nb=need // 2 - 1) == WORKSPACE  # less than one slice
     assert call(ws=FAKE + 16) == INVALID
     assert call(cq=_i32(0, 16, 8)) == INVALID
+
+
+def test_bwd_rejects_bad_arguments(lib):
+    f = lib.dsa_indexer_bwd
+    assert lib.dsa_indexer_bwd_workspace_size() == 256
+
+    def call(q=FAKE, k=FAKE, gk=FAKE, H=64, D=128, S=8, topk=4, ws=FAKE,
+             nb=256, idx=FAKE):
+        return f(q, k, FAKE, S, 1, H, D, 8, 1, topk, None, idx, FAKE, FAKE,
+                 gk, FAKE, ws, nb, None)
+    assert call(q=None) == INVALID
+    assert call(idx=None) == INVALID
+    assert call(gk=None) == INVALID
+    assert call(S=0) == INVALID
+    assert call(topk=0) == INVALID
+    assert call(H=32) == UNSUPPORTED
+    assert call(D=136) == UNSUPPORTED
+    assert call(D=60) == UNSUPPORTED
+    assert call(k=FAKE + 8) == INVALID   # k not 16-byte aligned
+    assert call(gk=FAKE + 4) == INVALID  # grad_k not 16-byte aligned
+    assert call(ws=None) == WORKSPACE
+    assert call(nb=255) == WORKSPACE
+    assert call(ws=FAKE + 16) == INVALID
