@@ -625,6 +625,166 @@ def run_varlen(args):
     return 0
 
 
+def cpu_oracle_bwd_sample(wl, gi, gs, q, k, w, n_rows: int):
+    """Time the oracle's backward on `n_rows` rows spread over the problem,
+    each as a one-row problem at its own position."""
+    import numpy as np
+    import torch
+
+    import oracle
+    oracle.build()
+    rows = np.linspace(0, wl.S - 1, n_rows).astype(np.int64)
+    pairs, dt = 0, 0.0
+    for s in rows:
+        for b in range(wl.B):
+            pos = torch.tensor([int(s)], dtype=torch.int32)
+            ix = gi[b:b + 1, s:s + 1]
+            t0 = time.perf_counter()
+            oracle.indexer_bwd(q[s:s + 1, b:b + 1], k[:, b:b + 1],
+                               w[s:s + 1, b:b + 1], wl.compress_ratio, ix,
+                               gs[b:b + 1, s:s + 1], q_pos=pos)
+            dt += time.perf_counter() - t0
+            pairs += int((ix >= 0).sum())
+    return {"value": 6.0 * wl.H * wl.D * pairs / dt / 1e12,
+            "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": f"{rows.size * wl.B} rows (evenly spaced), {pairs} "
+                      f"valid slots, {dt:.2f} s"}
+
+
+def run_backward(args):
+    """The indexer backward (gradients of the given-slots scores) at the
+    workload's shape, with random valid visible indices and N(0, 1)
+    upstream gradients."""
+    import torch
+
+    import dsa_sparse_attention_fwd_gb300 as dsa
+    from dsa_inputs import WORKLOADS, describe, make_given_indices, make_inputs
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dsa.build()
+    dsa.load_library()
+    wl = WORKLOADS[args.workload]
+    q, k, w, q_pos = make_inputs(wl)
+    nv = row_visible(wl, None if q_pos is None else q_pos.tolist())
+    gi = make_given_indices(wl.B, wl.S, wl.topk, nv, wl.idx_seed)
+    gs = torch.randn((wl.B, wl.S, wl.topk),
+                     generator=torch.Generator().manual_seed(wl.seed + 100))
+    pairs = int((gi >= 0).sum())
+    flops = 6.0 * wl.H * wl.D * pairs  # three products of 2*H*D per slot
+    qd, kd, wd = q.to(dev), k.to(dev), w.to(dev)
+    pd = q_pos.to(dev) if q_pos is not None else None
+    gid, gsd = gi.to(dev), gs.to(dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    gq = torch.empty((wl.S, wl.B, wl.H, wl.D), **f32)
+    gk = torch.empty((wl.S_kv, wl.B, wl.D), **f32)
+    gw = torch.empty((wl.S, wl.B, wl.H), **f32)
+    ws = torch.empty(dsa.dsa_indexer_bwd_workspace_size(), dtype=torch.uint8,
+                     device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        dsa.dsa_indexer_bwd(qd, kd, wd, wl.compress_ratio, gid, gsd,
+                            q_pos=pd, grad_q=gq, grad_k=gk, grad_w=gw,
+                            workspace=ws, stream=stream)
+    for _ in range(max(args.warmup, 3)):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    if dsa.dsa_indexer_check(ws) != 0:
+        raise RuntimeError("device status")
+    K = args.steps
+    mk = lambda: torch.cuda.Event(enable_timing=True)
+    ev = [(mk(), mk()) for _ in range(K)]
+    sampler = ClockSampler(local)
+    torch.cuda.synchronize()
+    barrier_ranks(world)
+    sampler.start()
+    time.sleep(0.2)
+    t0 = time.perf_counter()
+    for i in range(K):
+        flush.fill_(1.0)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    barrier_ranks(world)
+    clocks = sampler.stop()
+    t_step = max_over_ranks(sum(a_.elapsed_time(b_) for a_, b_ in ev) / K,
+                            world, dev)
+    if dsa.dsa_indexer_check(ws) != 0:
+        raise RuntimeError("device status")
+    # end to end: inputs copied in from pinned host memory, the three
+    # gradients copied back
+    hin = [t.pin_memory() for t in (q, k, w, gi, gs)]
+    din = [qd, kd, wd, gid, gsd]
+    hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            for t in (gq, gk, gw)]
+    e2e = []
+    for i in range(max(3, min(K, 20)) + 2):
+        a_, b_ = mk(), mk()
+        a_.record(stream)
+        for d_, h_ in zip(din, hin):
+            d_.copy_(h_, non_blocking=True)
+        step()
+        for h_, d_ in zip(hout, (gq, gk, gw)):
+            h_.copy_(d_, non_blocking=True)
+        b_.record(stream)
+        b_.synchronize()
+        if i >= 2:
+            e2e.append(a_.elapsed_time(b_))
+    t_e2e = max_over_ranks(sum(e2e) / len(e2e), world, dev)
+    h2d = sum(t.numel() * t.element_size() for t in hin)
+    d2h = sum(t.numel() * t.element_size() for t in hout)
+    if rank != 0:
+        return 0
+    peaks, peak_src = read_peaks()
+    tc_peak = float(peaks["bf16_tflops"])
+    value = world * flops / (t_step * 1e-3) / 1e12
+    achieved = flops / (t_step * 1e-3) / 1e12
+    line = {
+        "metric": "indexer bwd TFLOP/s (valid slots)", "value": value,
+        "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": t_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name + " backward", "desc": describe(wl),
+                   "slots": "random distinct visible keys per row",
+                   "valid_slots": pairs, "flops_per_step": flops,
+                   "l2": "flushed before each step (256 MiB write, outside "
+                         "the timed events)",
+                   "parallelism": f"replicas x{world}"},
+        "queries_per_s": world * wl.B * wl.S / (t_step * 1e-3),
+        "kernels_ms": {"indexer_bwd (with the grad_k clear)": t_step},
+        "roofline": {"kernel": "indexer_bwd", "bound": "tensor",
+                     "achieved": achieved, "peak": tc_peak,
+                     "unit": "TFLOP/s", "frac": achieved / tc_peak,
+                     "peak_source": f"{peak_src} bf16 burst",
+                     "algorithmic": f"{flops:.4g} FLOP per launch (6*H*D "
+                                    "per valid slot)",
+                     "timed": "the C call: grad_k clear + status clear + "
+                              "the kernel",
+                     "traffic": read_traffic("indexer_bwd")},
+        "e2e": {"value": world * flops / (t_e2e * 1e-3) / 1e12,
+                "unit": "TFLOP/s", "ms_per_step": t_e2e,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "api": "torch copies + dsa_indexer_bwd"},
+        "gpu_launches": K,
+        "clocks": clocks,
+        "wall_s_timed_region": wall,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_bwd_sample(wl, gi, gs, q, k, w, 24)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -634,12 +794,16 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--given-indices", action="store_true")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the indexer backward instead of the forward")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
     from dsa_inputs import VARLEN_WORKLOADS
     if args.workload in VARLEN_WORKLOADS:
         return run_varlen(args)
+    if args.backward:
+        return run_backward(args)
     return run_ours(args)
 
 

@@ -10,24 +10,33 @@
 //     grad_k[j]    += g * w[t, h] * [s_h > 0] * q[t, h]
 // with ReLU'(0) = 0.
 //
+// Factored form.  With G'[slot, h] = g * [s_h > 0] (no weight) and the
+// row's A[h, :] = sum over slots of G'[slot, h] * k[j_slot]:
+//     grad_q[t, h] = w[t, h] * A[h, :]
+//     grad_w[t, h] = q[t, h, :] . A[h, :]        (= sum g * [s_h > 0] * s_h)
+//     grad_k[j]   += sum_h G'[slot, h] * (w[t, h] q[t, h, :])
+// so the per-slot work is a select, the weights enter once per row (a
+// scaled copy Q' = w * Q of the row's query tile), and grad_w needs no
+// per-slot accumulation.
+//
 // A work item is one query row (all of its slots), a tile 128 consecutive
 // slots.  Per tile, on the tensor cores:
 //   MMA1   S[slot, h]   = K_g . Q^T        M = 128 slots, N = H, K = D
-//   (epilogue: G[slot, h] = g * w[h] * [S > 0] in bf16, into shared memory)
-//   MMA2   dQ^T[d, h]  += K_g^T . G        M = 128 (d), N = H, K = 128 slots
-//   MMA3   dK[slot, d]  = G . Q            M = 128 slots, N = 128 (d), K = H
-// K_g (the gathered keys) and Q are read twice, once K-major and once
-// MN-major, from the same shared-memory tiles; dQ^T accumulates in tensor
-// memory over the row's tiles and is written once per row; dK rows are
-// added into grad_k with vector atomics (a key is shared by many rows).
-// grad_w is reduced in registers over the row's slots.  D <= 128 runs as
-// D = 128 with zero padding; H = 64 (one 128-byte G row per slot).
+//   (epilogue: G'[slot, h] = bf16(g) * [S > 0], into shared memory)
+//   MMA2   A^T[d, h]   += K_g^T . G'       M = 128 (d), N = H, K = 128 slots
+//   MMA3   dK[slot, d]  = G' . Q'          M = 128 slots, N = 128 (d), K = H
+// K_g (the gathered keys) and G' are read twice, once K-major and once
+// MN-major, from the same shared-memory tiles.  A^T accumulates in tensor
+// memory over the row's tiles; dK rows are added into grad_k with vector
+// atomics straight from tensor memory (a key is shared by many rows), each
+// 4-thread group covering one 32-byte sector.  D <= 128 runs as D = 128
+// with zero padding; H = 64 (one 128-byte G' row per slot).
 //
 // Warp roles (one CTA per SM, persistent): warp 0 index/gradient and query
-// fetch, warps 1..4 key gathers (16-byte cp.async, zero fill for masked
-// slots), warp 5 TMEM allocator and MMA issuer, warps 6..9 epilogue.
+// fetch, warps 1..8 key gathers (16-byte cp.async, zero fill for masked
+// slots), warp 9 TMEM allocator and MMA issuer, warps 10..13 epilogue.
 // The MMA thread issues MMA1 of tile n + 1 before MMA2/MMA3 of tile n, so
-// the tensor core works on the next scores while the epilogue forms G.
+// the tensor core works on the next scores while the epilogue forms G'.
 //
 // grad_q and grad_w are plain stores in a fixed order (deterministic);
 // grad_k accumulates with atomics, so its rounding depends on their order.
@@ -39,38 +48,36 @@ namespace dsa {
 namespace {
 
 constexpr int kBwdH = 64;
-constexpr int kBwdGatWarps = 4;
+constexpr int kBwdGatWarps = 8;
 constexpr int kBwdThreads = 32 * (kBwdGatWarps + 6);
 constexpr int kBwdMmaWarp = kBwdGatWarps + 1;
 constexpr int kBwdEpiWarp0 = kBwdGatWarps + 2;  // first of four
 constexpr int kBwdStages = 4;                   // gathered key stages
-constexpr int kBwdRing = 16;                    // index/gradient ring (tiles)
+constexpr int kBwdRing = 8;                     // index/gradient ring (tiles)
 
 struct BwdSmem {
   static constexpr int kQBytes = 2 * kBwdH * 128;      // two d-chunks of 64
   static constexpr int kKBytes = 2 * kTileKeys * 128;  // two d-chunks of 64
   static constexpr int kGBytes = kTileKeys * 128;      // 128 slots x 64 heads
   static constexpr int kRingBytes = kTileKeys * 8;     // indices, gradients
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + 2 * kQBytes;
+  static constexpr int kOffQ = 0;                      // [2] query slots
+  static constexpr int kOffQw = kOffQ + 2 * kQBytes;   // w-scaled query
+  static constexpr int kOffK = kOffQw + kQBytes;
   static constexpr int kOffG = kOffK + kBwdStages * kKBytes;
   static constexpr int kOffRing = kOffG + 2 * kGBytes;
   static constexpr int kOffW = kOffRing + kBwdRing * kRingBytes;  // [2][H]
   static constexpr int kOffGW = kOffW + 2 * kBwdH * 4;            // [4][H]
   static constexpr int kOffBar = kOffGW + 4 * kBwdH * 4;
-  // k_full[4] k_empty[4] q_full[2] q_empty[2] r_full[16] r_empty[16]
-  // s_full[2] s_empty[2] g_full[2] g_empty[2] dk_full[2] dk_empty[2]
-  // dq_full[2] dq_empty[2]
-  static constexpr int kBarPairs = 8;  // s, g, dk, dq: full/empty pairs
-  static constexpr int kNumBars =
-      2 * kBwdStages + 4 + 2 * kBwdRing + 2 * kBarPairs;
+  // k_full[4] k_empty[4] q_full[2] q_empty[2] r_full[8] r_empty[8]
+  // s_full[2] g_full[2] dk_full[2] dq_full[2] dq_empty[2] qw_full qw_empty
+  static constexpr int kNumBars = 2 * kBwdStages + 4 + 2 * kBwdRing + 10 + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;
 };
 static_assert(BwdSmem::kAlloc <= 227 * 1024, "fits one CTA per SM");
 
-// TMEM columns: S x2 (64 each), dQ^T x2 (64 each), dK x2 (128 each).
+// TMEM columns: S x2 (64 each), A^T x2 (64 each), dK x2 (128 each).
 constexpr uint32_t kTmemS = 0, kTmemDq = 128, kTmemDk = 256;
 constexpr uint32_t kBwdTmemCols = 512;
 
@@ -116,7 +123,7 @@ __device__ __forceinline__ bool bwd_next(BwdCursor &c, const BwdGeom &g) {
 struct BwdPending {
   uint32_t n;     // the tile's sequence number in this CTA
   int kst, qs;    // its key stage and query slot
-  int dq;         // dQ^T accumulator of its row (row parity)
+  int dq;         // A^T accumulator of its row (row parity)
   uint32_t dqph;  // phase of that accumulator's barriers
   bool first, last;
 };
@@ -134,8 +141,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   using L = BwdSmem;
   constexpr int H = kBwdH;
   constexpr int NS = kBwdStages;
-  // MMA1: both K-major.  MMA2: A = gathered keys read d-major, B = G read
-  // head-major.  MMA3: A = G K-major (heads), B = Q read d-major.
+  // MMA1: both K-major.  MMA2: A = gathered keys read d-major, B = G' read
+  // head-major.  MMA3: A = G' K-major (heads), B = Q' read d-major.
   constexpr uint32_t kIdescS = idesc_bf16_f32(kTileKeys, H);
   constexpr uint32_t kIdescDq = idesc_bf16_f32_mn(128, H, true, true);
   constexpr uint32_t kIdescDk = idesc_bf16_f32_mn(kTileKeys, 128, false, true);
@@ -145,6 +152,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t *smem = smem_raw + (base - raw_addr);
   const uint32_t sQ = base + L::kOffQ;
+  const uint32_t sQw = base + L::kOffQw;
   const uint32_t sK = base + L::kOffK;
   const uint32_t sG = base + L::kOffG;
   const uint8_t *sRing = smem + L::kOffRing;
@@ -159,15 +167,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto r_full = [&](int i) { return bar(2 * NS + 4 + i); };
   auto r_empty = [&](int i) { return bar(2 * NS + 4 + kBwdRing + i); };
   constexpr int kB2 = 2 * NS + 4 + 2 * kBwdRing;
+  // The S, G' and dK buffers need no "empty" barriers: the epilogue reads
+  // S(n) and drains dK(n - 2) before it signals G'(n), and drains dK(n)
+  // (waiting for MMA2/MMA3 of tile n) before it writes G'(n + 2).
   auto s_full = [&](int i) { return bar(kB2 + i); };
-  auto s_empty = [&](int i) { return bar(kB2 + 2 + i); };
-  auto g_full = [&](int i) { return bar(kB2 + 4 + i); };
-  auto g_empty = [&](int i) { return bar(kB2 + 6 + i); };
-  auto dk_full = [&](int i) { return bar(kB2 + 8 + i); };
-  auto dk_empty = [&](int i) { return bar(kB2 + 10 + i); };
-  auto dq_full = [&](int i) { return bar(kB2 + 12 + i); };
-  auto dq_empty = [&](int i) { return bar(kB2 + 14 + i); };
-  static_assert(kB2 + 14 + 1 < L::kNumBars, "every barrier has its slot");
+  auto g_full = [&](int i) { return bar(kB2 + 2 + i); };
+  auto dk_full = [&](int i) { return bar(kB2 + 4 + i); };
+  auto dq_full = [&](int i) { return bar(kB2 + 6 + i); };
+  auto dq_empty = [&](int i) { return bar(kB2 + 8 + i); };
+  const uint32_t qw_full = bar(kB2 + 10), qw_empty = bar(kB2 + 11);
+  static_assert(kB2 + 11 < L::kNumBars, "every barrier has its slot");
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kOffMisc);
   volatile int *abort_flag = reinterpret_cast<int *>(smem + L::kOffMisc + 4);
 
@@ -183,16 +192,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(q_full(i), 1);
-      mbar_init(q_empty(i), 1);
+      // the row's last MMAs, then each epilogue warp once it is done with Q
+      mbar_init(q_empty(i), 1 + 4);
       mbar_init(s_full(i), 1);
-      mbar_init(s_empty(i), 4);  // epilogue warps
-      mbar_init(g_full(i), 4);
-      mbar_init(g_empty(i), 1);
+      mbar_init(g_full(i), 4);  // epilogue warps
       mbar_init(dk_full(i), 1);
-      mbar_init(dk_empty(i), 4);
       mbar_init(dq_full(i), 1);
       mbar_init(dq_empty(i), 4);
     }
+    mbar_init(qw_full, 4);
+    mbar_init(qw_empty, 1);
     for (int i = 0; i < kBwdRing; ++i) {
       mbar_init(r_full(i), 32);  // one cp.async arrival per fetch lane
       mbar_init(r_empty(i), 4);
@@ -207,7 +216,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       *reinterpret_cast<uint4 *>(smem + L::kOffQ + slot * L::kQBytes +
                                  H * 128 + off) = make_uint4(0, 0, 0, 0);
     }
-    fence_proxy_async_smem();
   }
   if (warp == kBwdMmaWarp) {
     tmem_alloc(smem_u32(tmem_holder), kBwdTmemCols);
@@ -316,114 +324,121 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == kBwdMmaWarp) {
     // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      // MMA2 and MMA3 of a finished tile: dQ^T += K_g^T G, dK = G Q
-      auto issue_back = [&](const BwdPending &p) -> bool {
-        const int gb = p.n & 1;
-        const uint32_t gph = (p.n >> 1) & 1u;
-        if (!wait_bar(g_full(gb), gph, abort_flag, status)) return false;
-        if (!wait_bar(dk_empty(gb), gph ^ 1u, abort_flag, status))
-          return false;
-        if (p.first &&
-            !wait_bar(dq_empty(p.dq), p.dqph ^ 1u, abort_flag, status))
-          return false;
-        tc_fence_after();
-        const uint32_t sGb = sG + gb * L::kGBytes;
-        const uint32_t sKs = sK + p.kst * L::kKBytes;
-        const uint32_t sQs = sQ + p.qs * L::kQBytes;
-        // K = 128 slots in steps of 16 (two 8-slot atoms, 2048 bytes)
-#pragma unroll
-        for (int ks = 0; ks < kTileKeys / 16; ++ks) {
-          const uint64_t ad =
-              sdesc_mn_sw128(sKs + ks * 2048, kTileKeys * 128, 1024);
-          // N = 64 is one atom, so the atom stride along N is never used
-          const uint64_t bd = sdesc_mn_sw128(sGb + ks * 2048, 1024, 1024);
-          mma_bf16(tmem + kTmemDq + p.dq * H, ad, bd, kIdescDq,
-                   (p.first && ks == 0) ? 0u : 1u);
-        }
-        // K = 64 heads in steps of 16
-#pragma unroll
-        for (int kk = 0; kk < H / 16; ++kk) {
-          const uint64_t ad = sdesc_k_sw128(sGb + kk * 32);
-          const uint64_t bd = sdesc_mn_sw128(sQs + kk * 2048, H * 128, 1024);
-          mma_bf16(tmem + kTmemDk + gb * 128, ad, bd, kIdescDk,
-                   kk != 0 ? 1u : 0u);
-        }
-        mma_commit(k_empty(p.kst));
-        mma_commit(g_empty(gb));
-        mma_commit(dk_full(gb));
-        if (p.last) {
-          mma_commit(dq_full(p.dq));
-          mma_commit(q_empty(p.qs));
-        }
-        return true;
-      };
-
-      BwdCursor cur = bwd_begin(g);
-      uint32_t kst = 0, kph = 0, nq = 0, n = 0, nrow = 0;
-      bool row_start = true, ok = true, pend = false;
-      BwdPending pd{};
-      int qs = 0;
-      while (cur.valid) {
-        if (row_start) {
-          qs = nq & 1;
-          const uint32_t qph = (nq >> 1) & 1u;
-          ++nq;
-          if (!wait_bar(q_full(qs), qph, abort_flag, status)) {
-            ok = false;
-            break;
-          }
-        }
-        const int sa = n & 1;
-        const uint32_t sph = (n >> 1) & 1u;
-        if (!wait_bar(s_empty(sa), sph ^ 1u, abort_flag, status) ||
-            !wait_bar(k_full(kst), kph, abort_flag, status)) {
-          ok = false;
-          break;
-        }
-        // the stage was written by cp.async (generic proxy)
-        fence_proxy_async_smem();
-        tc_fence_after();
-        const uint32_t sQs = sQ + qs * L::kQBytes;
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-#pragma unroll
-          for (int kk = 0; kk < kChunk / 16; ++kk) {
-            const uint64_t ad = sdesc_k_sw128(sK + kst * L::kKBytes +
-                                              cc * (kTileKeys * 128) + kk * 32);
-            const uint64_t bd = sdesc_k_sw128(sQs + cc * (H * 128) + kk * 32);
-            mma_bf16(tmem + kTmemS + sa * H, ad, bd, kIdescS,
-                     (cc | kk) != 0 ? 1u : 0u);
-          }
-        }
-        mma_commit(s_full(sa));
-        if (pend && !issue_back(pd)) {
-          ok = false;
-          break;
-        }
-        pd.n = n;
-        pd.kst = kst;
-        pd.qs = qs;
-        pd.dq = nrow & 1;
-        pd.dqph = (nrow >> 1) & 1u;
-        pd.first = cur.tile == 0;
-        pd.last = cur.tile + 1 == g.ntiles;
-        pend = true;
-        if (pd.last) ++nrow;
-        ++n;
-        if (++kst == NS) {
-          kst = 0;
-          kph ^= 1u;
-        }
-        row_start = bwd_next(cur, g);
+    // The whole warp runs the control flow (converged, waits taken
+    // together); lane 0 alone issues the tcgen05 instructions, through a
+    // predicate rather than a branch.
+    const uint32_t lead = lane == 0;
+    auto wait_all = [&](uint32_t b, uint32_t ph) -> bool {
+      return __all_sync(0xffffffffu, wait_bar(b, ph, abort_flag, status));
+    };
+    // MMA2 and MMA3 of a finished tile: A^T += K_g^T G', dK = G' Q'
+    auto issue_back = [&](const BwdPending &p) -> bool {
+      const int gb = p.n & 1;
+      const uint32_t gph = (p.n >> 1) & 1u;
+      // G'(n) is written.  The epilogue forms G'(n) only after it has read
+      // S(n) and drained dK(n - 2), so this one wait also frees the dK
+      // accumulator MMA3 overwrites and the S buffer of tile n (reused by
+      // tile n + 2's MMA1, issued after this).
+      if (!wait_all(g_full(gb), gph)) return false;
+      // a row's first tile: its A^T accumulator is free and its Q' written
+      if (p.first && (!wait_all(dq_empty(p.dq), p.dqph ^ 1u) ||
+                      !wait_all(qw_full, (uint32_t)p.dq)))
+        return false;
+      tc_fence_after();
+      // rolled loops, the start address advanced inside the descriptor
+      // (its low field counts 16-byte units): the issue loop stays small
+      const uint32_t sGb = sG + gb * L::kGBytes;
+      // K = 128 slots in steps of 16 (two 8-slot atoms, 2048 bytes)
+      // N = 64 is one atom, so G's atom stride along N is never used
+      const uint64_t a2 =
+          sdesc_mn_sw128(sK + p.kst * L::kKBytes, kTileKeys * 128, 1024);
+      const uint64_t b2 = sdesc_mn_sw128(sGb, 1024, 1024);
+      const uint32_t d2 = tmem + kTmemDq + p.dq * H;
+#pragma unroll 1
+      for (int ks = 0; ks < kTileKeys / 16; ++ks)
+        mma_bf16_by(d2, a2 + ks * (2048 >> 4), b2 + ks * (2048 >> 4),
+                    kIdescDq, (p.first && ks == 0) ? 0u : 1u, lead);
+      // K = 64 heads in steps of 16
+      const uint64_t a3 = sdesc_k_sw128(sGb);
+      const uint64_t b3 = sdesc_mn_sw128(sQw, H * 128, 1024);
+      const uint32_t d3 = tmem + kTmemDk + gb * 128;
+#pragma unroll 1
+      for (int kk = 0; kk < H / 16; ++kk)
+        mma_bf16_by(d3, a3 + kk * (32 >> 4), b3 + kk * (2048 >> 4), kIdescDk,
+                    kk != 0 ? 1u : 0u, lead);
+      // dk_full also tells the epilogue that G' buffer gb is free again
+      mma_commit_by(k_empty(p.kst), lead);
+      mma_commit_by(dk_full(gb), lead);
+      if (p.last) {
+        mma_commit_by(dq_full(p.dq), lead);
+        mma_commit_by(q_empty(p.qs), lead);
+        mma_commit_by(qw_empty, lead);
       }
-      if (ok && pend) issue_back(pd);
+      return true;
+    };
+
+    BwdCursor cur = bwd_begin(g);
+    uint32_t kst = 0, kph = 0, nq = 0, n = 0, nrow = 0;
+    bool row_start = true, ok = true, pend = false;
+    BwdPending pd{};
+    int qs = 0;
+    while (cur.valid) {
+      if (row_start) {
+        qs = nq & 1;
+        const uint32_t qph = (nq >> 1) & 1u;
+        ++nq;
+        if (!wait_all(q_full(qs), qph)) {
+          ok = false;
+          break;
+        }
+      }
+      const int sa = n & 1;
+      // S buffer sa was read by the epilogue before it signalled G'(n - 2),
+      // which the previous iteration waited for
+      if (!wait_all(k_full(kst), kph)) {
+        ok = false;
+        break;
+      }
+      // the stage was written by cp.async (generic proxy)
+      fence_proxy_async_smem();
+      tc_fence_after();
+      const uint64_t a1 = sdesc_k_sw128(sK + kst * L::kKBytes);
+      const uint64_t b1 = sdesc_k_sw128(sQ + qs * L::kQBytes);
+      const uint32_t d1 = tmem + kTmemS + sa * H;
+      // two d-chunks of four K = 16 steps (32 bytes each)
+#pragma unroll 1
+      for (int t = 0; t < 8; ++t) {
+        const uint32_t ao = ((t >> 2) * (kTileKeys * 128) + (t & 3) * 32) >> 4;
+        const uint32_t bo = ((t >> 2) * (H * 128) + (t & 3) * 32) >> 4;
+        mma_bf16_by(d1, a1 + ao, b1 + bo, kIdescS, t != 0 ? 1u : 0u, lead);
+      }
+      mma_commit_by(s_full(sa), lead);
+      if (pend && !issue_back(pd)) {
+        ok = false;
+        break;
+      }
+      pd.n = n;
+      pd.kst = kst;
+      pd.qs = qs;
+      pd.dq = nrow & 1;
+      pd.dqph = (nrow >> 1) & 1u;
+      pd.first = cur.tile == 0;
+      pd.last = cur.tile + 1 == g.ntiles;
+      pend = true;
+      if (pd.last) ++nrow;
+      ++n;
+      if (++kst == NS) {
+        kst = 0;
+        kph ^= 1u;
+      }
+      row_start = bwd_next(cur, g);
     }
+    if (ok && pend) issue_back(pd);
   } else {
     // ---------------- epilogue (warps kBwdEpiWarp0 .. kBwdEpiWarp0 + 3) ------
-    const int sp = warp & 3;                       // TMEM sub-partition
+    const int sp = warp & 3;                         // TMEM sub-partition
     const int et = threadIdx.x - 32 * kBwdEpiWarp0;  // 0..127
-    const int i = sp * 32 + lane;  // TMEM lane: the slot, or d for dQ^T
+    const int i = sp * 32 + lane;  // TMEM lane: the slot, or d for A^T
     const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
     BwdCursor cur = bwd_begin(g);
     uint32_t n = 0, nrow = 0;
@@ -431,10 +446,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     float w_next = 0.f;
     if (cur.valid && et < H)
       w_next = __ldg(w + ((size_t)cur.s * B + cur.b) * H + et);
-    // the previous tile's dK rows, added into grad_k after this tile's G
+    // the previous tile's dK rows, added into grad_k after this tile's G'
     bool dk_pend = false, dk_live = false;
     uint32_t dk_n = 0;
-    float *dk_dst = grad_k;
+    int dk_off = 0;  // element offset of this lane's dK row in grad_k
     auto drain_dk = [&]() -> bool {
       const int db = dk_n & 1;
       const uint32_t dph = (dk_n >> 1) & 1u;
@@ -442,29 +457,45 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                       wait_bar(dk_full(db), dph, abort_flag, status)))
         return false;
       tc_fence_after();
-      const uint32_t ta = tmem + lane_off + kTmemDk + db * 128;
+      const uint32_t live = __ballot_sync(0xffffffffu, dk_live);
+      if (live) {
+        // 16 rows per load; 4 consecutive lanes hold 8 consecutive d of a
+        // row, so every red covers whole 32-byte sectors
+        const int t4 = lane >> 2, c2 = (lane & 3) * 2;
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
+          const int ra = hf * 16 + t4, rb = ra + 8;
+          const int offa = __shfl_sync(0xffffffffu, dk_off, ra);
+          const int offb = __shfl_sync(0xffffffffu, dk_off, rb);
+          const bool la = (live >> ra) & 1u, lb = (live >> rb) & 1u;
+          const uint32_t ta = tmem + ((uint32_t)(sp * 32 + hf * 16) << 16) +
+                              kTmemDk + db * 128;
+#pragma unroll 1
+          for (int c4 = 0; c4 < 4; ++c4) {
+            uint32_t v[16];
+            __syncwarp();
+            tmem_ld16x256b_x4(ta + c4 * 32, v);
+            tmem_ld_wait();
+            reg_fence16(v);
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t v[32];
-        __syncwarp();
-        tmem_ld32(ta + c4 * 32, v);
-        tmem_ld_wait();
-        reg_fence32(v);
-        if (dk_live) {
-#pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) {
-            const int d = c4 * 32 + q4 * 4;
-            if (d < D)
-              red_add_v4(dk_dst + d, __uint_as_float(v[4 * q4]),
-                         __uint_as_float(v[4 * q4 + 1]),
-                         __uint_as_float(v[4 * q4 + 2]),
-                         __uint_as_float(v[4 * q4 + 3]));
+            for (int kb = 0; kb < 4; ++kb) {
+              const int d = c4 * 32 + kb * 8 + c2;
+              if (d < D) {
+                if (la)
+                  red_add_v2(grad_k + offa + d, __uint_as_float(v[4 * kb]),
+                             __uint_as_float(v[4 * kb + 1]));
+                if (lb)
+                  red_add_v2(grad_k + offb + d,
+                             __uint_as_float(v[4 * kb + 2]),
+                             __uint_as_float(v[4 * kb + 3]));
+              }
+            }
           }
         }
       }
+      // the MMA thread learns that dK buffer db is free from the next G'
+      // signal (g_full), which this warp gives only after this drain
       tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(dk_empty(db));
       return true;
     };
 
@@ -475,12 +506,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (named_bar_or(1, 128, !ok)) break;
       const int b = cur.b, s = cur.s;
       const int nv = n_visible(row_pos(q_pos, b, s), ratio, S_kv);
-      const float4 *w4 = reinterpret_cast<const float4 *>(sWi);
-      float gwa[H];
+      // the fetch warp loads one query tile per row, in this order
+      const int qs = nrow & 1;
+      const uint32_t qph = (nrow >> 1) & 1u;
+      const uint32_t sQs = sQ + qs * L::kQBytes;
+      // Q' = w * Q for this row's MMA3s, once the previous row's are done
+      ok = __all_sync(0xffffffffu,
+                      wait_bar(q_full(qs), qph, abort_flag, status) &&
+                          wait_bar(qw_empty, (nrow & 1u) ^ 1u, abort_flag,
+                                   status));
+      if (ok) {
+#pragma unroll 2
+        for (int u8 = 0; u8 < 8; ++u8) {
+          const uint32_t o = (uint32_t)(u8 * 128 + et) * 16u;
+          const float wh = sWi[(o & (H * 128 - 1)) >> 7];  // the unit's head
+          const float4 x = ld_shared_v4f(sQs + o);
+          const uint32_t xs[4] = {__float_as_uint(x.x), __float_as_uint(x.y),
+                                  __float_as_uint(x.z), __float_as_uint(x.w)};
+          uint32_t y[4];
 #pragma unroll
-      for (int h = 0; h < H; ++h) gwa[h] = 0.f;
+          for (int e = 0; e < 4; ++e)
+            y[e] = pack_bf16x2(__uint_as_float(xs[e] << 16) * wh,
+                               __uint_as_float(xs[e] & 0xFFFF0000u) * wh);
+          st_shared_v4(sQw + o, y);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(qw_full);
+      }
       bool bad = false, row_end = false;
-      while (!row_end) {
+      while (ok && !row_end) {
         const int slot = n % kBwdRing;
         const uint32_t rph = (n / kBwdRing) & 1u;
         const int sa = n & 1;
@@ -492,15 +547,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           break;
         }
         tc_fence_after();
-        uint32_t v[2][32];
-        tmem_ld32(tmem + lane_off + kTmemS + sa * H, v[0]);
-        tmem_ld32(tmem + lane_off + kTmemS + sa * H + 32, v[1]);
-        tmem_ld_wait();
-        reg_fence32(v[0]);
-        reg_fence32(v[1]);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(s_empty(sa));
         const int e = cur.tile * kTileKeys + i;  // slot within the row
         const bool in_row = e < topk;
         const uint8_t *rs = sRing + slot * L::kRingBytes;
@@ -513,40 +559,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bad |= in_row && (j < -1 || j >= S_kv);
         const bool valid = j >= 0 && j < nv;
         const float ge = valid ? gs : 0.f;
-        // this G buffer is free once MMA2/MMA3 of tile n - 2 are done
-        if (!__all_sync(0xffffffffu,
-                        wait_bar(g_empty(sa), sph ^ 1u, abort_flag, status))) {
-          ok = false;
-          break;
-        }
-        // G[slot, h] = g * w[h] * [S > 0] (bf16, 128-byte swizzled row) and
-        // the slot's share of grad_w[h] = sum g * ReLU(S)
+        // this G' buffer was last read by MMA2/MMA3 of tile n - 2, whose
+        // completion the drain of dK(n - 2) has already waited for
+        // G'[slot, h] = bf16(g) where S > 0, else 0: a mask on the packed
+        // pair (bf16 row of 128 bytes, 16-byte units rotated by the row)
+        const uint32_t gg = pack_bf16x2(ge, ge);
         const uint32_t grow = sG + sa * L::kGBytes + i * 128;
-        bool any = false;
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          uint32_t v[32];
+          __syncwarp();
+          tmem_ld32(tmem + lane_off + kTmemS + sa * H + half * 32, v);
+          tmem_ld_wait();
+          reg_fence32(v);
+          if (half == 1) tc_fence_before();
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          uint32_t pk[4];
+          for (int u = 0; u < 4; ++u) {
+            uint32_t pk[4];
 #pragma unroll
-          for (int hq = 0; hq < 2; ++hq) {
-            const int h = u * 8 + hq * 4;
-            const float4 wv = w4[h >> 2];
-            const float x0 = __uint_as_float(v[h >> 5][h & 31]);
-            const float x1 = __uint_as_float(v[h >> 5][(h + 1) & 31]);
-            const float x2 = __uint_as_float(v[h >> 5][(h + 2) & 31]);
-            const float x3 = __uint_as_float(v[h >> 5][(h + 3) & 31]);
-            gwa[h] = fmaf(ge, fmaxf(x0, 0.f), gwa[h]);
-            gwa[h + 1] = fmaf(ge, fmaxf(x1, 0.f), gwa[h + 1]);
-            gwa[h + 2] = fmaf(ge, fmaxf(x2, 0.f), gwa[h + 2]);
-            gwa[h + 3] = fmaf(ge, fmaxf(x3, 0.f), gwa[h + 3]);
-            any |= (x0 > 0.f) | (x1 > 0.f) | (x2 > 0.f) | (x3 > 0.f);
-            pk[2 * hq] = pack_bf16x2(x0 > 0.f ? ge * wv.x : 0.f,
-                                     x1 > 0.f ? ge * wv.y : 0.f);
-            pk[2 * hq + 1] = pack_bf16x2(x2 > 0.f ? ge * wv.z : 0.f,
-                                         x3 > 0.f ? ge * wv.w : 0.f);
+            for (int p2 = 0; p2 < 4; ++p2) {
+              const int h = u * 8 + p2 * 2;
+              const uint32_t m =
+                  (__uint_as_float(v[h]) > 0.f ? 0x0000FFFFu : 0u) |
+                  (__uint_as_float(v[h + 1]) > 0.f ? 0xFFFF0000u : 0u);
+              pk[p2] = gg & m;
+            }
+            const int uu = half * 4 + u;
+            st_shared_v4(grow + ((uu ^ (i & 7)) << 4), pk);
           }
-          st_shared_v4(grow + ((u ^ (i & 7)) << 4), pk);
         }
-        // the tensor core (async proxy) reads G next
+        // the tensor core (async proxy) reads G' next
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(g_full(sa));
@@ -556,14 +598,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         dk_pend = true;
         dk_n = n;
-        dk_live = valid && any && ge != 0.f;
-        dk_dst = grad_k + ((size_t)(dk_live ? j : 0) * B + b) * D;
+        dk_live = valid && ge != 0.f;
+        dk_off = dk_live ? (j * B + b) * D : 0;
         ++n;
         row_end = bwd_next(cur, g);
       }
       // every warp finished the row's tiles, or one of them gave up
       if (named_bar_or(2, 128, !ok)) break;
-      // the row's last dK rows, then dQ and grad_w
+      // the row's last dK rows, then grad_q = w * A and grad_w = q . A
       dk_pend = false;
       ok = drain_dk();
       const int dq = nrow & 1;
@@ -571,44 +613,56 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (ok)
         ok = __all_sync(0xffffffffu,
                         wait_bar(dq_full(dq), dqph, abort_flag, status));
+      // this warp's share of grad_w: zero unless the row completes
+      sGW[sp * H + lane] = 0.f;
+      sGW[sp * H + 32 + lane] = 0.f;
       if (ok) {
         tc_fence_after();
         float *gq = grad_q + ((size_t)s * B + b) * H * D;
-#pragma unroll
+        // q[h, d] of this lane's d in the row's (swizzled) query tile
+        const int dd = i & (kChunk - 1);
+        const uint32_t qcol = sQs + (i >> 6) * (H * 128) + (dd & 7) * 2;
+#pragma unroll 1
         for (int c = 0; c < 2; ++c) {
           uint32_t v[32];
           __syncwarp();
           tmem_ld32(tmem + lane_off + kTmemDq + dq * H + c * 32, v);
           tmem_ld_wait();
           reg_fence32(v);
-          // lane = d: each store instruction writes 32 consecutive d of one h
-          if (i < D) {
+          float gp[32];
 #pragma unroll
-            for (int hh = 0; hh < 32; ++hh)
-              gq[(size_t)(c * 32 + hh) * D + i] = __uint_as_float(v[hh]);
+          for (int hh = 0; hh < 32; ++hh) {
+            const int h = c * 32 + hh;
+            const float a = __uint_as_float(v[hh]);
+            const uint32_t qa =
+                qcol + h * 128 + ((((dd >> 3) ^ (h & 7))) << 4);
+            gp[hh] = a * __uint_as_float((uint32_t)ld_shared_u16(qa) << 16);
+            // lane = d: each store instruction writes 32 consecutive d
+            if (i < D) gq[(size_t)h * D + i] = sWi[h] * a;
           }
+          // sum over the lanes' d: halve the 32 sums five times (each lane
+          // keeps the half its lane bit selects), leaving head c*32 + lane
+#pragma unroll
+          for (int o = 16, m = 32; o >= 1; o >>= 1, m >>= 1) {
+            const bool up = (lane & o) != 0;
+#pragma unroll
+            for (int h = 0; h < m / 2; ++h) {
+              const float send = up ? gp[h] : gp[h + m / 2];
+              const float keep = up ? gp[h + m / 2] : gp[h];
+              gp[h] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+            }
+          }
+          sGW[sp * H + c * 32 + lane] = gp[0];
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(dq_empty(dq));
-      }
-      // grad_w: halve the 64 partial sums over the lanes five times (each
-      // lane keeps the half its lane bit selects), leaving heads 2*lane and
-      // 2*lane + 1 in gwa[0..1]; then add the four warps in a fixed order
-#pragma unroll
-      for (int o = 16, m = H; o >= 1; o >>= 1, m >>= 1) {
-        const bool up = (lane & o) != 0;
-#pragma unroll
-        for (int h = 0; h < m / 2; ++h) {
-          const float send = up ? gwa[h] : gwa[h + m / 2];
-          const float keep = up ? gwa[h + m / 2] : gwa[h];
-          gwa[h] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        if (lane == 0) {
+          mbar_arrive(dq_empty(dq));
+          mbar_arrive(q_empty(qs));
         }
       }
-      sGW[sp * H + 2 * lane] = gwa[0];
-      sGW[sp * H + 2 * lane + 1] = gwa[1];
       named_bar_sync(3, 128);
-      if (et < H)
+      if (ok && et < H)
         grad_w[((size_t)s * B + b) * H + et] =
             ((sGW[et] + sGW[H + et]) + sGW[2 * H + et]) + sGW[3 * H + et];
       if (__any_sync(0xffffffffu, bad) && lane == 0)
@@ -671,7 +725,8 @@ int dsa_indexer_bwd(const void *q, const void *k, const float *w, int S,
       compress_ratio <= 0 || topk <= 0)
     return DSA_ERR_INVALID_ARG;
   if (H != 64 || D % 8 != 0 || D > 128) return DSA_ERR_UNSUPPORTED;
-  if ((long long)B * S >= (1ll << 31) || topk > (1 << 30))
+  if ((long long)B * S >= (1ll << 31) || topk > (1 << 30) ||
+      (long long)S_kv * B * D >= (1ll << 31))
     return DSA_ERR_UNSUPPORTED;
   auto al = [](const void *p, unsigned a) {
     return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;

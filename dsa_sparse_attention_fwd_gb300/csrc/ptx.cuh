@@ -61,13 +61,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait for the phase with parity `parity` of barrier `bar`.
-// Returns false (after raising the CTA's abort flag and the status bit) when
-// the limit expires or another role of the CTA has already aborted.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity,
-                                         volatile int *abort_flag,
-                                         int *status) {
-  if (mbar_try_wait(bar, parity)) return true;
+// The polling loop of wait_bar(), kept out of line: waits are many and
+// mostly satisfied at the first test, so only that test is inlined at each
+// call site and the hot loops stay small in the instruction cache.
+static __device__ __noinline__ bool wait_bar_poll(uint32_t bar, uint32_t parity,
+                                                  volatile int *abort_flag,
+                                                  int *status) {
   const uint64_t t0 = globaltimer_ns();
   for (uint64_t it = 1; it < kWaitMaxPolls; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -79,6 +78,16 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity,
   *abort_flag = 1;
   atomicOr(status, kStatusTimeout);
   return false;
+}
+
+// Bounded wait for the phase with parity `parity` of barrier `bar`.
+// Returns false (after raising the CTA's abort flag and the status bit) when
+// the limit expires or another role of the CTA has already aborted.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity,
+                                         volatile int *abort_flag,
+                                         int *status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_bar_poll(bar, parity, abort_flag, status);
 }
 
 // ---- TMA (tiled tensor loads into shared memory) ----------------------------
@@ -237,6 +246,31 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc,
       : "memory");
 }
 
+// mma_bf16 executed by the whole (converged) warp and issued by the lanes
+// whose `issue` is non-zero (one lane): no branch around the instruction.
+__device__ __forceinline__ void mma_bf16_by(uint32_t d_tmem, uint64_t adesc,
+                                            uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate,
+                                            uint32_t issue) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "setp.ne.b32 q, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(issue)
+      : "memory");
+}
+
+// mma_commit issued by the lanes whose `issue` is non-zero (one lane).
+__device__ __forceinline__ void mma_commit_by(uint32_t bar, uint32_t issue) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t"
+      "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster."
+      "b64 [%0];\n\t}" ::"r"(bar),
+      "r"(issue)
+      : "memory");
+}
+
 // Arrive once on `bar` when every MMA this thread issued so far is done.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
@@ -266,6 +300,23 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]),
+        "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]),
+        "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15])
+      : "r"(taddr));
+}
+
+// 16 TMEM lanes x 32 fp32 columns (four 8-column blocks): for block k,
+// thread t gets r[4k], r[4k+1] = lane t/4, columns 8k + 2(t%4) + {0, 1} and
+// r[4k+2], r[4k+3] = lane 8 + t/4, the same columns (the m16n8 accumulator
+// fragment of mma.sync, repeated along the columns).
+__device__ __forceinline__ void tmem_ld16x256b_x4(uint32_t taddr,
+                                                  uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
       "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
       "%15}, [%16];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]),
@@ -317,11 +368,35 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// 2-byte load from shared memory.
+__device__ __forceinline__ uint16_t ld_shared_u16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// 16-byte load from shared memory.
+__device__ __forceinline__ float4 ld_shared_v4f(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
 // 16-byte store to shared memory.
 __device__ __forceinline__ void st_shared_v4(uint32_t addr,
                                              const uint32_t (&v)[4]) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
                "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3])
+               : "memory");
+}
+
+// Atomic add of two consecutive fp32 (8-byte aligned) in global memory.
+__device__ __forceinline__ void red_add_v2(float *p, float a, float b) {
+  asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(p), "f"(a),
+               "f"(b)
                : "memory");
 }
 

@@ -317,8 +317,8 @@ DSA_API int dsa_indexer_fwd_static_scratch(
  *   grad_w [S, B, H].
  *   Precision: the scores are accumulated in fp32; g * w is rounded to bf16
  *   as an operand of the two gradient products, which accumulate in fp32.
- *   Envelope: H = 64, D a multiple of 8 up to 128; otherwise
- *   DSA_ERR_UNSUPPORTED.  q, k and grad_k 16-byte aligned.
+ *   Envelope: H = 64, D a multiple of 8 up to 128, S_kv * B * D < 2^31;
+ *   otherwise DSA_ERR_UNSUPPORTED.  q, k and grad_k 16-byte aligned.
  *   workspace: dsa_indexer_bwd_workspace_size() bytes, 256-byte aligned
  *   (the status header; read it with dsa_indexer_check()).
  * Asynchronous on `cuda_stream`; argument errors are returned before any
