@@ -32,9 +32,10 @@
 // 4-thread group covering one 32-byte sector.  D <= 128 runs as D = 128
 // with zero padding; H = 64 (one 128-byte G' row per slot).
 //
-// Warp roles (one CTA per SM, persistent): warp 0 index/gradient and query
-// fetch, warps 1..8 key gathers (16-byte cp.async, zero fill for masked
-// slots), warp 9 TMEM allocator and MMA issuer, warps 10..13 epilogue.
+// Warp roles (one CTA per SM, persistent, 16 warps): warp 0 index/gradient
+// and query fetch, warp 1 TMEM allocator and MMA issuer, warps 4..7
+// epilogue, eight warps of key gathers (16-byte cp.async, zero fill for
+// masked slots), two idle.
 // The MMA thread issues MMA1 of tile n + 1 before MMA2/MMA3 of tile n, so
 // the tensor core works on the next scores while the epilogue forms G'.
 //
@@ -48,10 +49,27 @@ namespace dsa {
 namespace {
 
 constexpr int kBwdH = 64;
+// Warp roles.  Warps w and w + 4k share a sub-partition (scheduler); the
+// MMA warp's sub-partition holds only it and one epilogue warp, so the
+// issue of the tensor-core instructions does not queue behind gather
+// copies.  Warps 9 and 13 (that sub-partition's other two) stay idle.
 constexpr int kBwdGatWarps = 8;
-constexpr int kBwdThreads = 32 * (kBwdGatWarps + 6);
-constexpr int kBwdMmaWarp = kBwdGatWarps + 1;
-constexpr int kBwdEpiWarp0 = kBwdGatWarps + 2;  // first of four
+constexpr int kBwdThreads = 512;
+constexpr int kBwdMmaWarp = 1;
+constexpr int kBwdEpiWarp0 = 4;  // warps 4..7, one per sub-partition
+__device__ __forceinline__ int gather_index(int warp) {
+  switch (warp) {
+    case 2: return 0;
+    case 3: return 1;
+    case 8: return 2;
+    case 10: return 3;
+    case 11: return 4;
+    case 12: return 5;
+    case 14: return 6;
+    case 15: return 7;
+    default: return -1;
+  }
+}
 constexpr int kBwdStages = 4;                   // gathered key stages
 constexpr int kBwdRing = 8;                     // index/gradient ring (tiles)
 
@@ -268,13 +286,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     // nothing may land in shared memory after the CTA is gone
     asm volatile("cp.async.wait_all;" ::: "memory");
-  } else if (warp <= kBwdGatWarps) {
+  } else if (gather_index(warp) >= 0) {
     // ---------------- key gathers ----------------
     constexpr int kSegs = 16;               // 16-byte pieces of a stage row
     constexpr int kRowsPerOp = 32 / kSegs;  // rows one warp-wide copy covers
     constexpr int kRows = kTileKeys / kBwdGatWarps;
     constexpr int kOps = kRows / kRowsPerOp;
-    const int gw = warp - 1;
+    const int gw = gather_index(warp);
     const int seg = lane % kSegs, sub = lane / kSegs;
     const int c = seg >> 3, s8 = seg & 7;
     // D is a multiple of 8, so every 16-byte piece is all key or all padding
@@ -434,7 +452,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       row_start = bwd_next(cur, g);
     }
     if (ok && pend) issue_back(pd);
-  } else {
+  } else if (warp >= kBwdEpiWarp0 && warp < kBwdEpiWarp0 + 4) {
     // ---------------- epilogue (warps kBwdEpiWarp0 .. kBwdEpiWarp0 + 3) ------
     const int sp = warp & 3;                         // TMEM sub-partition
     const int et = threadIdx.x - 32 * kBwdEpiWarp0;  // 0..127
