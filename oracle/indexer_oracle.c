@@ -42,6 +42,15 @@
  *
  * Query positions: prefill rows sit at position t = s; when q_pos is given,
  * row s of sequence b sits at position q_pos[b] + s (decode rows).
+ *
+ * Key validity (the pool variant, page "Module glm5next_dsa": "index_scores
+ * -> [Q, P] scores + candidate validity"): when key_valid is given, a key
+ * whose flag is 0 is not a candidate -- it is treated like a key that is not
+ * visible (no top-k slot, -inf when asked for by index or in the logits).
+ *
+ * The pool variant's other two steps (same page, "Shape of the pipeline"
+ * and "Checkpoint and kernel facts") are oracle_kpool_compress and
+ * oracle_expand_selection below.
  */
 #include <math.h>
 #include <pthread.h>
@@ -74,7 +83,15 @@ typedef struct {
     const uint16_t *k;
     const float *w;
     int S, B, H, D, S_kv, ratio;
+    const uint8_t *key_valid; /* [S_kv, B] or NULL (every key valid) */
 } problem_t;
+
+/* key j of sequence b is a candidate for a query at position t */
+static int key_candidate(const problem_t *p, long long j, int b, long long t)
+{
+    if (!oracle_key_visible(j, t, p->ratio)) return 0;
+    return !p->key_valid || p->key_valid[(size_t)j * p->B + b] != 0;
+}
 
 /* I[t, j] for one (row, key) pair, the definition written out */
 static double score_one(const problem_t *p, int b, int s, long long j)
@@ -138,19 +155,19 @@ static void do_row(job_t *jb, long long r)
     if (jb->logits) {
         double *L = jb->logits + (size_t)r * p->S_kv;
         for (long long j = 0; j < p->S_kv; ++j)
-            L[j] = oracle_key_visible(j, t, p->ratio) ? score_one(p, b, s, j)
-                                                       : -INFINITY;
+            L[j] = key_candidate(p, j, b, t) ? score_one(p, b, s, j)
+                                             : -INFINITY;
     }
 
     if (jb->in_idx) {
         const int32_t *given = jb->in_idx + ((size_t)b * p->S + s) * topk;
         int32_t nvis = 0;
         for (long long j = 0; j < p->S_kv; ++j)
-            nvis += oracle_key_visible(j, t, p->ratio);
+            nvis += key_candidate(p, j, b, t);
         for (int i = 0; i < topk; ++i) {
             int32_t j = given[i];
             double v = -INFINITY;
-            if (j >= 0 && j < p->S_kv && oracle_key_visible(j, t, p->ratio))
+            if (j >= 0 && j < p->S_kv && key_candidate(p, j, b, t))
                 v = score_one(p, b, s, j);
             if (jb->out_idx) jb->out_idx[(size_t)r * topk + i] = j;
             if (jb->out_scores) jb->out_scores[(size_t)r * topk + i] = (float)v;
@@ -166,7 +183,7 @@ static void do_row(job_t *jb, long long r)
     cand_t *c = (cand_t *)malloc(sizeof(cand_t) * (size_t)(p->S_kv > 0 ? p->S_kv : 1));
     long long n = 0;
     for (long long j = 0; j < p->S_kv; ++j) {
-        if (!oracle_key_visible(j, t, p->ratio)) continue;
+        if (!key_candidate(p, j, b, t)) continue;
         c[n].score = jb->logits ? jb->logits[(size_t)r * p->S_kv + j]
                                 : score_one(p, b, s, j);
         c[n].j = (int32_t)j;
@@ -202,23 +219,25 @@ static void *worker(void *arg)
  * The whole forward for a list of rows.
  *
  * q, k: bf16 bit patterns; w fp32; q_pos [B] or NULL; rows: row ids b*S+s.
+ * key_valid: [S_kv, B] uint8 or NULL (every key a candidate).
  * in_idx NULL -> top-k path; else the given-indices path.
  * Any output pointer may be NULL.  Per requested row r:
  *   out_idx[r*topk + i], out_scores[...] (fp32), out_scores_f64[...] (fp64),
  *   out_next[r] = (topk+1)-th visible score (-inf if none; top-k path),
- *   out_nvis[r] = number of visible keys,
- *   logits[r*S_kv + j] = I[t, j] or -inf where key j is not visible.
+ *   out_nvis[r] = number of candidate (visible and valid) keys,
+ *   logits[r*S_kv + j] = I[t, j] or -inf where key j is not a candidate.
  * Returns the number of threads used.
  */
 int oracle_indexer_fwd(const uint16_t *q, const uint16_t *k, const float *w,
                        int S, int B, int H, int D, int S_kv, int ratio,
-                       int topk, const int32_t *q_pos, const int32_t *in_idx,
+                       int topk, const int32_t *q_pos,
+                       const uint8_t *key_valid, const int32_t *in_idx,
                        const int64_t *rows, long long n_rows,
                        int32_t *out_idx, float *out_scores,
                        double *out_scores_f64, double *out_next,
                        int32_t *out_nvis, double *logits, int n_threads)
 {
-    problem_t p = {q, k, w, S, B, H, D, S_kv, ratio};
+    problem_t p = {q, k, w, S, B, H, D, S_kv, ratio, key_valid};
     job_t jb;
     memset(&jb, 0, sizeof jb);
     jb.p = &p;
@@ -316,6 +335,91 @@ void oracle_indexer_bwd(const uint16_t *q, const uint16_t *k, const float *w,
                     }
                 }
             }
+        }
+    }
+}
+
+/*
+ * Pool compression (page "Module glm5next_dsa": kpool_compress in "Shape of
+ * the pipeline"; "The pool softmax runs over the pool-slot axis, per
+ * channel", "Pooling starts at first_key. A pool counts only if every one of
+ * its index_kpool slots is valid" in "Checkpoint and kernel facts").
+ *
+ * Pool p of sequence b covers the tokens first_key + p*kpool + s,
+ * s = 0..kpool-1; there are P = (T - first_key) / kpool whole pools (a
+ * trailing partial pool is not a pool).  For channel c, with the slot logits
+ * z_s = gate[token_s, b, c] + ape[s, c]:
+ *     key[p, b, c] = sum_s softmax_s(z)_s * k[token_s, b, c]
+ * (the page names the inputs k, gate, valid and ape and the softmax axis; the
+ * logit of a slot being its gate plus its slot-position embedding is the
+ * reading of "ape").  valid_out[p, b] = 1 iff valid[token_s, b] != 0 for
+ * every slot (valid NULL: every token valid).
+ *
+ * k [T, B, D] bf16 bits, gate [T, B, D] fp32, ape [kpool, D] fp32,
+ * valid [T, B] uint8 or NULL; out_keys [P, B, D] double, out_valid [P, B].
+ * Returns P.
+ */
+long long oracle_kpool_compress(const uint16_t *k, const float *gate,
+                                const float *ape, const uint8_t *valid,
+                                int T, int B, int D, int kpool, int first_key,
+                                double *out_keys, uint8_t *out_valid)
+{
+    long long P = T > first_key ? (long long)(T - first_key) / kpool : 0;
+    for (long long p = 0; p < P; ++p) {
+        for (int b = 0; b < B; ++b) {
+            int all_valid = 1;
+            for (int s = 0; s < kpool; ++s) {
+                long long tok = first_key + p * kpool + s;
+                if (valid && valid[(size_t)tok * B + b] == 0) all_valid = 0;
+            }
+            if (out_valid) out_valid[(size_t)p * B + b] = (uint8_t)all_valid;
+            for (int c = 0; c < D; ++c) {
+                /* softmax over the slots, written with the usual max shift */
+                double zmax = -INFINITY;
+                for (int s = 0; s < kpool; ++s) {
+                    long long tok = first_key + p * kpool + s;
+                    double z = (double)gate[((size_t)tok * B + b) * D + c] +
+                               (double)ape[(size_t)s * D + c];
+                    if (z > zmax) zmax = z;
+                }
+                double den = 0.0, num = 0.0;
+                for (int s = 0; s < kpool; ++s) {
+                    long long tok = first_key + p * kpool + s;
+                    double z = (double)gate[((size_t)tok * B + b) * D + c] +
+                               (double)ape[(size_t)s * D + c];
+                    double e = exp(z - zmax);
+                    den += e;
+                    num += e * bf16_to_double(k[((size_t)tok * B + b) * D + c]);
+                }
+                out_keys[((size_t)p * B + b) * D + c] = num / den;
+            }
+        }
+    }
+    return P;
+}
+
+/*
+ * Selection expansion (page "Module glm5next_dsa": expand_selection in
+ * "Shape of the pipeline", "-1 = invalid"; "dsa_expand_selection writes -1
+ * over the whole index row before it stores any index, so every slot is
+ * written").  Each row's select_k pool ids become select_k * kpool token
+ * ids: slot i*kpool + s holds first_key + pool_i*kpool + s, or -1 when
+ * pool_i is -1.
+ */
+void oracle_expand_selection(const int32_t *pools, long long rows,
+                             int select_k, int kpool, int first_key,
+                             int32_t *out_tokens)
+{
+    const long long width = (long long)select_k * kpool;
+    for (long long r = 0; r < rows; ++r) {
+        int32_t *out = out_tokens + (size_t)r * width;
+        for (long long i = 0; i < width; ++i) out[i] = -1;
+        for (int i = 0; i < select_k; ++i) {
+            int32_t pool = pools[(size_t)r * select_k + i];
+            if (pool < 0) continue;
+            for (int s = 0; s < kpool; ++s)
+                out[(size_t)i * kpool + s] =
+                    (int32_t)((long long)first_key + (long long)pool * kpool + s);
         }
     }
 }

@@ -437,3 +437,170 @@ def test_backward_closed_form_and_relu_convention():
     np.testing.assert_array_equal(bwd["grad_k"][1], 0.0)
     assert bwd["grad_w"][0, 0, 0] == 3.0 * 3.0
     assert bwd["grad_w"][1, 0, 0] == 0.0
+
+
+# ---- the pool variant: key validity, pool compression, expansion ----------
+
+@pytest.mark.parametrize("ratio,topk", [(1, 6), (2, 4), (1, 40)])
+def test_key_valid_mask_matches_exact_brute_force(ratio, topk):
+    """A key whose valid flag is 0 is not a candidate: exact rational brute
+    force over the valid visible keys only (integer inputs, frequent ties),
+    -inf logits and -inf given-index scores for the masked keys."""
+    rng = np.random.default_rng(77 + ratio)
+    S, B, H, D, S_kv = 24, 2, 3, 5, 12
+    qi = rng.integers(-3, 4, size=(S, B, H, D))
+    ki = rng.integers(-3, 4, size=(S_kv, B, D))
+    wi = rng.choice([1, -1, 0.5, -0.5, 0.25], size=(S, B, H))
+    kv = (rng.random((S_kv, B)) > 0.3).astype(np.uint8)
+    q = torch.from_numpy(qi.astype(np.float32)).to(torch.bfloat16)
+    k = torch.from_numpy(ki.astype(np.float32)).to(torch.bfloat16)
+    w = torch.from_numpy(wi.astype(np.float32))
+    out = oracle.indexer_fwd(q, k, w, ratio, topk, key_valid=kv,
+                             want_logits=True)
+    for b in range(B):
+        for s in range(S):
+            sc = {j: v for j, v in _exact_scores(qi, ki, wi, ratio, b, s,
+                                                 s).items() if kv[j, b]}
+            r = b * S + s
+            assert out["nvis"][r] == len(sc)
+            for j in range(S_kv):
+                if j not in sc:
+                    assert out["logits"][r, j] == -math.inf
+            left = dict(sc)
+            want = []
+            for _ in range(topk):
+                if not left:
+                    want.append(-1)
+                    continue
+                best = max(left.values())
+                j = min(jj for jj, v in left.items() if v == best)
+                want.append(j)
+                del left[j]
+            assert out["idx"][r].tolist() == want, (b, s)
+    # given indices: a masked key scores -inf, its index is copied through
+    gi = torch.from_numpy(rng.integers(0, S_kv, size=(B, S, 4)).astype(
+        np.int32))
+    g = oracle.indexer_fwd(q, k, w, ratio, 4, in_idx=gi, key_valid=kv)
+    for b in range(B):
+        for s in range(S):
+            for i in range(4):
+                j = int(gi[b, s, i])
+                val = g["scores64"][b * S + s, i]
+                if not kv[j, b] or (j + 1) * ratio - 1 > s:
+                    assert val == -math.inf
+                else:
+                    assert val == float(_exact_scores(qi, ki, wi, ratio, b, s,
+                                                      s)[j])
+
+
+def _pool_inputs(T, B, D, kpool, seed):
+    g = torch.Generator().manual_seed(seed)
+    k = torch.randn((T, B, D), generator=g).to(torch.bfloat16)
+    gate = torch.randn((T, B, D), generator=g)
+    ape = torch.randn((kpool, D), generator=g) * 0.5
+    return k, gate, ape
+
+
+def test_kpool_single_slot_is_the_key():
+    """kpool = 1: the softmax over one slot is 1, the pooled key is the
+    token's key exactly."""
+    k, gate, ape = _pool_inputs(11, 2, 16, 1, 1)
+    c = oracle.kpool_compress(k, gate, ape, None, 1, 0)
+    assert c["P"] == 11
+    np.testing.assert_array_equal(c["keys"], k.float().numpy())
+
+
+def test_kpool_hand_example():
+    """kpool = 2, gate 0 on both slots, position embedding (0, ln 3): the
+    weights are 1/4 and 3/4 in every channel, so the pooled key is
+    k0/4 + 3*k1/4 (integer keys, exact up to the exponential's rounding)."""
+    D = 6
+    k = torch.tensor([[[1, -2, 3, 0, 5, -7]], [[3, 2, -1, 4, 1, 1]]],
+                     dtype=torch.float32).to(torch.bfloat16)
+    gate = torch.zeros((2, 1, D))
+    ape = torch.tensor([[0.0] * D, [math.log(3.0)] * D])
+    c = oracle.kpool_compress(k, gate, ape, None, 2, 0)
+    want = np.array([1, -2, 3, 0, 5, -7]) / 4 + 3 * np.array(
+        [3, 2, -1, 4, 1, 1]) / 4
+    # ape is fp32: ln 3 rounded to fp32 shifts the weights by < 1e-7
+    np.testing.assert_allclose(c["keys"][0, 0], want, rtol=0, atol=1e-6)
+
+
+def test_kpool_equal_logits_give_the_mean_per_channel():
+    """Slot logits equal across the slots (varying across channels and
+    pools): every channel's pooled value is the plain mean of its slots.
+    A softmax taken over channels instead of slots fails this."""
+    T, B, D, kp = 24, 2, 16, 4
+    k, _, _ = _pool_inputs(T, B, D, kp, 2)
+    rng = np.random.default_rng(3)
+    per_pool = rng.normal(size=(T // kp, B, D)).astype(np.float32)
+    gate = torch.from_numpy(np.repeat(per_pool, kp, axis=0))
+    ape = torch.zeros((kp, D))
+    c = oracle.kpool_compress(k, gate, ape, None, kp, 0)
+    want = k.float().numpy().reshape(T // kp, kp, B, D).mean(axis=1)
+    np.testing.assert_allclose(c["keys"], want, rtol=0, atol=1e-12)
+
+
+def test_kpool_shift_invariance_and_dominant_slot():
+    """Adding one constant per (pool, channel) to every slot's logit leaves
+    the pooled key unchanged; a slot whose logit is 60 above the others
+    gives (nearly) that slot's key."""
+    T, B, D, kp = 16, 1, 8, 4
+    k, gate, ape = _pool_inputs(T, B, D, kp, 4)
+    c0 = oracle.kpool_compress(k, gate, ape, None, kp, 0)
+    shift = np.repeat(np.random.default_rng(5).normal(
+        size=(T // kp, B, D)).astype(np.float32) * 3, kp, axis=0)
+    c1 = oracle.kpool_compress(k, gate + torch.from_numpy(shift), ape, None,
+                               kp, 0)
+    np.testing.assert_allclose(c1["keys"], c0["keys"], rtol=0, atol=1e-6)
+    g2 = torch.zeros((T, B, D))
+    g2[2::kp] = 60.0  # slot 2 of every pool dominates
+    c2 = oracle.kpool_compress(k, g2, torch.zeros((kp, D)), None, kp, 0)
+    np.testing.assert_allclose(c2["keys"], k.float().numpy()[2::kp],
+                               rtol=0, atol=1e-20 + 1e-24)
+
+
+def test_kpool_first_key_count_and_validity():
+    """Pools start at first_key and only whole pools count; a pool is valid
+    iff each of its tokens is."""
+    T, B, D, kp, fk = 37, 2, 8, 4, 5
+    k, gate, ape = _pool_inputs(T, B, D, kp, 6)
+    valid = (np.random.default_rng(7).random((T, B)) > 0.1).astype(np.uint8)
+    c = oracle.kpool_compress(k, gate, ape, valid, kp, fk)
+    assert c["P"] == (T - fk) // kp == 8
+    # the same pools from the tokens after first_key with first_key = 0
+    c0 = oracle.kpool_compress(k[fk:], gate[fk:], ape, valid[fk:], kp, 0)
+    np.testing.assert_array_equal(c["keys"], c0["keys"])
+    want_valid = valid[fk:fk + 8 * kp].reshape(8, kp, B).all(axis=1)
+    np.testing.assert_array_equal(c["valid"], want_valid.astype(np.uint8))
+    assert oracle.kpool_compress(k[:4], gate[:4], ape, None, kp, 1)["P"] == 0
+
+
+def test_expand_selection_closed_form():
+    pools = np.array([[[3, -1, 0]], [[-1, -1, 7]]], np.int32)  # [2, 1, 3]
+    t = oracle.expand_selection(pools, 4, 10)
+    assert t.shape == (2, 1, 12)
+    assert t[0, 0].tolist() == [22, 23, 24, 25, -1, -1, -1, -1,
+                                10, 11, 12, 13]
+    assert t[1, 0].tolist() == [-1] * 8 + [38, 39, 40, 41]
+
+
+def test_bf16_rounding_ties_to_even():
+    x = np.array([1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, 1.0 + 2.0 ** -9,
+                  -(1.0 + 2.0 ** -8 + 2.0 ** -30), 0.0, -0.0, 2.0 ** -126])
+    bits = oracle.round_bf16(x).tolist()
+    assert bits == [0x3F80, 0x3F82, 0x3F80, 0xBF81, 0x0000, 0x8000, 0x0080]
+
+
+def test_pooled_forward_with_one_slot_pools_is_the_plain_forward():
+    """kpool = 1, first_key = 0, every token valid: pools are the tokens and
+    the pool variant is the plain top-k forward (tokens = indices)."""
+    S, B, H, D = 40, 2, 4, 16
+    q, k, w = _rand_problem(S, B, H, D, S, 8)
+    gate = torch.randn((S, B, D))
+    ape = torch.zeros((1, D))
+    pooled = oracle.indexer_pooled_fwd(q, k, gate, ape, None, w, 1, 0, 9)
+    plain = oracle.indexer_fwd(q, k, w, 1, 9)
+    np.testing.assert_array_equal(pooled["tokens"].reshape(B * S, 9),
+                                  plain["idx"])
+    np.testing.assert_array_equal(pooled["scores"], plain["scores"])
