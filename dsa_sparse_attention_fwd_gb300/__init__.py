@@ -29,7 +29,9 @@ __all__ = [
     "dsa_status_string", "dsa_selftest_wait_limit", "v4_lighting_indexer",
     "indexer_logits", "dsa_indexer_host_buffer_size", "dsa_indexer_fwd_host",
     "dsa_indexer_varlen_workspace_size", "dsa_indexer_fwd_varlen",
-    "dsa_indexer_bwd", "dsa_indexer_bwd_workspace_size", "STATUS",
+    "dsa_indexer_bwd", "dsa_indexer_bwd_workspace_size",
+    "dsa_kpool_compress", "dsa_expand_selection",
+    "dsa_indexer_pooled_workspace_size", "dsa_indexer_fwd_pooled", "STATUS",
 ]
 
 STATUS = {
@@ -99,6 +101,17 @@ def load_library(path: str | None = None):
         lib.dsa_indexer_bwd.restype = I
         lib.dsa_indexer_bwd.argtypes = [P, P, P, I, I, I, I, I, I, I, P, P, P,
                                         P, P, P, P, Z, P]
+        L = ctypes.c_longlong
+        lib.dsa_kpool_compress.restype = I
+        lib.dsa_kpool_compress.argtypes = [P, P, P, P, I, I, I, I, I, P, P, P]
+        lib.dsa_expand_selection.restype = I
+        lib.dsa_expand_selection.argtypes = [P, L, I, I, I, P, P]
+        lib.dsa_indexer_pooled_workspace_size.restype = Z
+        lib.dsa_indexer_pooled_workspace_size.argtypes = [I] * 8
+        lib.dsa_indexer_fwd_pooled.restype = I
+        lib.dsa_indexer_fwd_pooled.argtypes = [P, P, P, P, P, P, I, I, I, I,
+                                               I, I, I, I, P, P, P, P, P, Z,
+                                               P]
         _lib = lib
         return lib
 
@@ -225,6 +238,107 @@ def dsa_indexer_bwd(q, k, w, compress_ratio, idx, grad_scores, q_pos=None,
     if rc != 0:
         raise DsaError(rc, "dsa_indexer_bwd")
     return grad_q, grad_k, grad_w, workspace
+
+
+def _pool_inputs(k, gate, ape, valid, kpool):
+    if k.dtype != torch.bfloat16 or k.dim() != 3 or not k.is_contiguous():
+        raise ValueError("k must be contiguous bf16 [T, B, D]")
+    T, B, D = k.shape
+    if (gate.dtype != torch.float32 or tuple(gate.shape) != (T, B, D)
+            or not gate.is_contiguous()):
+        raise ValueError("gate must be contiguous fp32 [T, B, D]")
+    if (ape.dtype != torch.float32 or tuple(ape.shape) != (kpool, D)
+            or not ape.is_contiguous()):
+        raise ValueError("ape must be contiguous fp32 [kpool, D]")
+    if valid is not None and (valid.dtype != torch.uint8
+                              or tuple(valid.shape) != (T, B)
+                              or not valid.is_contiguous()):
+        raise ValueError("valid must be contiguous uint8 [T, B]")
+    return T, B, D
+
+
+def dsa_kpool_compress(k, gate, ape, kpool, first_key=0, valid=None,
+                       stream=None):
+    """Pool compression on device tensors: returns (keys [P, B, D] bf16,
+    pool_valid [P, B] uint8)."""
+    lib = load_library()
+    T, B, D = _pool_inputs(k, gate, ape, valid, kpool)
+    P = max(0, (T - first_key) // kpool)
+    keys = torch.empty((max(P, 1), B, D), dtype=torch.bfloat16,
+                       device=k.device)
+    pv = torch.empty((max(P, 1), B), dtype=torch.uint8, device=k.device)
+    rc = lib.dsa_kpool_compress(_ptr(k), _ptr(gate), _ptr(ape), _ptr(valid),
+                                T, B, D, int(kpool), int(first_key),
+                                _ptr(keys), _ptr(pv), _stream(stream))
+    if rc != 0:
+        raise DsaError(rc, "dsa_kpool_compress")
+    return keys[:P], pv[:P]
+
+
+def dsa_expand_selection(pools, kpool, first_key=0, out=None, stream=None):
+    """Pool ids [..., select_k] int32 -> token ids [..., select_k*kpool]."""
+    lib = load_library()
+    if pools.dtype != torch.int32 or not pools.is_contiguous():
+        raise ValueError("pools must be contiguous int32")
+    select_k = pools.shape[-1]
+    if out is None:
+        out = torch.empty(tuple(pools.shape[:-1]) + (select_k * kpool,),
+                          dtype=torch.int32, device=pools.device)
+    rows = pools.numel() // select_k
+    rc = lib.dsa_expand_selection(_ptr(pools), rows, select_k, int(kpool),
+                                  int(first_key), _ptr(out), _stream(stream))
+    if rc != 0:
+        raise DsaError(rc, "dsa_expand_selection")
+    return out
+
+
+def dsa_indexer_pooled_workspace_size(S, B, H, D, T, kpool, first_key,
+                                      index_topk) -> int:
+    return int(load_library().dsa_indexer_pooled_workspace_size(
+        S, B, H, D, T, kpool, first_key, index_topk))
+
+
+def dsa_indexer_fwd_pooled(q, k, gate, ape, w, kpool, first_key, index_topk,
+                           valid=None, q_pos=None, out_tokens=None,
+                           out_pools=None, out_scores=None, workspace=None,
+                           stream=None):
+    """The pool variant on device tensors: q [S,B,H,D] bf16, per-token k
+    [T,B,D] bf16, gate [T,B,D] fp32, ape [kpool,D] fp32, w [S,B,H] fp32,
+    valid [T,B] uint8 or None.  Returns (tokens [B,S,index_topk] int32,
+    pools [B,S,index_topk/kpool] int32, scores [B,S,index_topk/kpool] fp32,
+    workspace)."""
+    lib = load_library()
+    T, B, D = _pool_inputs(k, gate, ape, valid, kpool)
+    if q.dtype != torch.bfloat16 or not q.is_contiguous():
+        raise ValueError("q must be contiguous bf16")
+    S, Bq, H, Dq = q.shape
+    if (Bq, Dq) != (B, D) or tuple(w.shape) != (S, B, H):
+        raise ValueError("q / w shapes do not match k")
+    if index_topk % kpool:
+        raise ValueError("index_topk must be a multiple of kpool")
+    sk = index_topk // kpool
+    dev = q.device
+    if out_tokens is None:
+        out_tokens = torch.empty((B, S, index_topk), dtype=torch.int32,
+                                 device=dev)
+    if out_pools is None:
+        out_pools = torch.empty((B, S, sk), dtype=torch.int32, device=dev)
+    if out_scores is None:
+        out_scores = torch.empty((B, S, sk), dtype=torch.float32, device=dev)
+    if workspace is None:
+        n = dsa_indexer_pooled_workspace_size(S, B, H, D, T, kpool,
+                                              first_key, index_topk)
+        if n == 0:
+            raise DsaError(2, "dsa_indexer_pooled_workspace_size")
+        workspace = torch.empty(n, dtype=torch.uint8, device=dev)
+    rc = lib.dsa_indexer_fwd_pooled(
+        _ptr(q), _ptr(k), _ptr(gate), _ptr(ape), _ptr(valid), _ptr(w), S, B,
+        H, D, T, int(kpool), int(first_key), int(index_topk), _ptr(q_pos),
+        _ptr(out_tokens), _ptr(out_pools), _ptr(out_scores), _ptr(workspace),
+        workspace.numel(), _stream(stream))
+    if rc != 0:
+        raise DsaError(rc, "dsa_indexer_fwd_pooled")
+    return out_tokens, out_pools, out_scores, workspace
 
 
 def dsa_indexer_logits(q, k, w, compress_ratio, q_pos=None, logits=None,

@@ -259,8 +259,9 @@ int forward_core(const void *q, const void *k, const float *w, int S, int B,
                  const int32_t *q_pos, const int32_t *in_idx, int32_t *out_idx,
                  float *out_scores, void *workspace, size_t workspace_bytes,
                  void *cuda_stream, void *const *stage_events, int n_events,
-                 bool clear_status) {
+                 bool clear_status, const uint8_t *kv_valid) {
   if (!q || !k || !w || !out_idx || !out_scores) return DSA_ERR_INVALID_ARG;
+  if (kv_valid && in_idx) return DSA_ERR_UNSUPPORTED;
   int rc = check_shape(S, B, H, D, S_kv, compress_ratio);
   if (rc != DSA_OK) return rc;
   if (topk <= 0) return DSA_ERR_INVALID_ARG;
@@ -287,7 +288,8 @@ int forward_core(const void *q, const void *k, const float *w, int S, int B,
   int *status = static_cast<int *>(workspace);
   float *logits = reinterpret_cast<float *>(static_cast<char *>(workspace) +
                                             kHeaderBytes);
-  const Problem p{q, k, w, q_pos, S, B, H, D, S_kv, compress_ratio};
+  Problem p{q, k, w, q_pos, S, B, H, D, S_kv, compress_ratio};
+  p.kv_valid = kv_valid;
   auto mark = [&](int i) {
     return i < n_events
                ? cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), st)

@@ -19,6 +19,9 @@ struct Problem {
   const float *w;        // [S, B, H] fp32
   const int32_t *q_pos;  // [B] or nullptr: row s of sequence b at q_pos[b]+s
   int S, B, H, D, S_kv, ratio;
+  // [S_kv, B] or nullptr: a key whose flag is 0 is not a candidate (its
+  // logit is -inf; the selection turns a selected -inf into -1)
+  const uint8_t *kv_valid = nullptr;
 };
 
 // Position of query row s of sequence b.
@@ -135,12 +138,14 @@ int device_num_sms(int *num_sms);
 // The forward behind the C entry points (arguments and return codes of
 // dsa_indexer_fwd_profiled); clear_status = false keeps the workspace's
 // status word, so forwards sharing a workspace accumulate device errors.
+// kv_valid ([S_kv, B] or nullptr): keys whose flag is 0 are not candidates
+// (top-k path only).
 int forward_core(const void *q, const void *k, const float *w, int S, int B,
                  int H, int D, int S_kv, int compress_ratio, int topk,
                  const int32_t *q_pos, const int32_t *in_idx, int32_t *out_idx,
                  float *out_scores, void *workspace, size_t workspace_bytes,
                  void *cuda_stream, void *const *stage_events, int n_events,
-                 bool clear_status);
+                 bool clear_status, const uint8_t *kv_valid = nullptr);
 
 cudaError_t launch_wait_selftest(int limit_us, int *status, cudaStream_t st);
 

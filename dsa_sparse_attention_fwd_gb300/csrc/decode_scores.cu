@@ -78,6 +78,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                          const __grid_constant__ CUtensorMap tm_k,
                          const float *__restrict__ w,
                          const int32_t *__restrict__ q_pos,
+                         const uint8_t *__restrict__ kv_valid,
                          float *__restrict__ logits,
                          uint32_t *__restrict__ row_hist, int S, int B,
                          int S_kv, int ratio, int n_items, int *status) {
@@ -273,7 +274,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         }
         const int j = (it.tile0 + t) * kTileKeys + sp * 32 + lane;
         if ((long long)(j + 1) * ratio - 1 <= pos && j < S_kv) {
-          const float sc = s0 + s1;
+          // a key that is not a candidate scores -inf (pool variant)
+          const bool kv_ok = kv_valid == nullptr ||
+                             __ldg(kv_valid + (size_t)j * B + it.b) != 0;
+          const float sc = kv_ok ? s0 + s1 : -__int_as_float(0x7f800000);
           out[j] = sc;
           if (row_hist)
             atomicAdd(row_hist + (size_t)it.row * kRowHistBins +
@@ -313,9 +317,10 @@ cudaError_t launch_dec(const Problem &p, const CUtensorMap &tm_q,
   if (n_items <= 0) return cudaSuccess;
   if (n_items > 0x7fffffffLL) return cudaErrorInvalidValue;
   const int grid = (int)(n_items < num_sms ? n_items : num_sms);
-  kern<<<grid, kDecThreads, smem, st>>>(tm_q, tm_k, p.w, p.q_pos, logits,
-                                        row_hist, p.S, p.B, p.S_kv, p.ratio,
-                                        (int)n_items, status);
+  kern<<<grid, kDecThreads, smem, st>>>(tm_q, tm_k, p.w, p.q_pos,
+                                        p.kv_valid, logits, row_hist, p.S,
+                                        p.B, p.S_kv, p.ratio, (int)n_items,
+                                        status);
   return cudaGetLastError();
 }
 

@@ -90,6 +90,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                         const __grid_constant__ CUtensorMap tm_k,
                         const float *__restrict__ w,
                         const int32_t *__restrict__ q_pos,
+                        const uint8_t *__restrict__ kv_valid,
                         float *__restrict__ logits,
                         uint32_t *__restrict__ row_hist, int S, int B,
                         int S_kv, int ratio, int *status) {
@@ -304,6 +305,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         if (lane == 0) mbar_arrive(acc_empty(acc));
 
         const int j = tile * kTileKeys + sp * 32 + lane;
+        // a key that is not a candidate scores -inf (pool variant)
+        const bool kv_ok = kv_valid == nullptr || j >= S_kv ||
+                           __ldg(kv_valid + (size_t)j * B + it.b) != 0;
 #pragma unroll
         for (int qq = 0; qq < QH; ++qq) {
           const int tq = half * QH + qq;
@@ -349,10 +353,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           const int t = it.t0 + tq;
           const bool vis = (long long)(j + 1) * ratio - 1 <= qbase + t;
           if (t < S && vis && j < S_kv) {
-            logits[((size_t)it.b * S + t) * S_kv + j] = score;
+            const float sv = kv_ok ? score : -__int_as_float(0x7f800000);
+            logits[((size_t)it.b * S + t) * S_kv + j] = sv;
             if (do_hist)
               atomicAdd(&sHist[tq * kRowHistBins +
-                               (ordered_key(score) >> kRowHistShift)],
+                               (ordered_key(sv) >> kRowHistShift)],
                         1u);
           }
         }
@@ -398,9 +403,9 @@ cudaError_t launch_h(const Problem &p, const CUtensorMap &tm_q,
   const long long n_items = (long long)((p.S + TQ - 1) / TQ) * p.B;
   const int grid = (int)(n_items < num_sms ? n_items : num_sms);
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, kScoreThreads, smem, st>>>(tm_q, tm_k, p.w, p.q_pos, logits,
-                                          row_hist, p.S, p.B, p.S_kv, p.ratio,
-                                          status);
+  kern<<<grid, kScoreThreads, smem, st>>>(tm_q, tm_k, p.w, p.q_pos,
+                                          p.kv_valid, logits, row_hist, p.S,
+                                          p.B, p.S_kv, p.ratio, status);
   return cudaGetLastError();
 }
 

@@ -553,8 +553,10 @@ __global__ void __launch_bounds__(NT, NT == kSelThreads ? 4 : 1)
   for (int i = tid; i < topk; i += NT) {
     if (i < m) {  // m >= topk or m = n_visible < topk
       const uint64_t c = cur[i];
-      oi[i] = (int32_t)(uint32_t)c;
-      os[i] = key_to_float((uint32_t)(c >> 32));
+      const float v = key_to_float((uint32_t)(c >> 32));
+      // -inf marks a key that is not a candidate (it sorts last)
+      oi[i] = v == -__int_as_float(0x7f800000) ? -1 : (int32_t)(uint32_t)c;
+      os[i] = v;
     } else {
       oi[i] = -1;
       os[i] = -__int_as_float(0x7f800000);

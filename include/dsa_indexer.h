@@ -333,6 +333,71 @@ DSA_API int dsa_indexer_bwd(const void *q, const void *k, const float *w,
                             float *grad_k, float *grad_w, void *workspace,
                             size_t workspace_bytes, void *cuda_stream);
 
+/*
+ * The pool variant (metrale.ai page "Module glm5next_dsa", section "Shape
+ * of the pipeline": k, gate, valid, ape -> kpool_compress -> index_scores ->
+ * topk_pools -> expand_selection -> token ids, -1 = invalid; section
+ * "Checkpoint and kernel facts": the pool softmax runs over the slot axis
+ * per channel, pooling starts at first_key, a pool counts only if all of its
+ * slots are valid, expand_selection writes every slot of the row).
+ *
+ * Pool p of sequence b covers tokens first_key + p*kpool + s (s < kpool);
+ * P = (T - first_key) / kpool whole pools (a trailing partial pool is not a
+ * pool).  Pooled key, per channel c, with z_s = gate[token_s, b, c] +
+ * ape[s, c]:  key[p, b, c] = sum_s softmax_s(z)_s * k[token_s, b, c]
+ * (fp32, stored bf16).  A pool is a candidate iff every token's valid flag
+ * is nonzero (valid NULL: all valid).  Query row s of sequence b at position
+ * t = (q_pos ? q_pos[b] : 0) + s sees pool p iff its last token is at or
+ * before t.
+ *
+ *   k [T, B, D] bf16 (per-token indexer keys), gate [T, B, D] fp32,
+ *   ape [kpool, D] fp32, valid [T, B] uint8 or NULL; 1 <= kpool <= 8,
+ *   D a multiple of 8; k, gate and ape 16-byte aligned.
+ */
+
+/* The compression alone: out_keys [P, B, D] bf16 (16-byte aligned),
+ * out_valid [P, B] uint8 (nullable).  Asynchronous on cuda_stream. */
+DSA_API int dsa_kpool_compress(const void *k, const float *gate,
+                               const float *ape, const uint8_t *valid, int T,
+                               int B, int D, int kpool, int first_key,
+                               void *out_keys, uint8_t *out_valid,
+                               void *cuda_stream);
+
+/* The expansion alone: pools [rows, select_k] int32 (pool ids or -1) ->
+ * out_tokens [rows, select_k * kpool], slot i*kpool + s = first_key +
+ * pool_i*kpool + s, or -1 when pool_i is -1. */
+DSA_API int dsa_expand_selection(const int32_t *pools, long long rows,
+                                 int select_k, int kpool, int first_key,
+                                 int32_t *out_tokens, void *cuda_stream);
+
+/* Workspace bytes of dsa_indexer_fwd_pooled (0 = invalid or unsupported
+ * shape). */
+DSA_API size_t dsa_indexer_pooled_workspace_size(int S, int B, int H, int D,
+                                                 int T, int kpool,
+                                                 int first_key,
+                                                 int index_topk);
+
+/*
+ * The whole variant: compression, the indexer forward over the pools (q
+ * [S, B, H, D] bf16, w [S, B, H] fp32 as for dsa_indexer_fwd; the
+ * index_topk / kpool best candidate pools per row, descending score, ties
+ * to the lower pool), and expansion to index_topk token ids.
+ *   index_topk: a nonzero multiple of kpool ("index_topk is a nonzero
+ *   multiple of index_kpool").
+ *   out_tokens [B, S, index_topk] int32; out_pools [B, S, index_topk/kpool]
+ *   int32 (-1 for empty slots); out_scores [B, S, index_topk/kpool] fp32
+ *   (-inf for empty slots).
+ *   workspace: dsa_indexer_pooled_workspace_size() bytes, 256-byte aligned;
+ *   its status word is read by dsa_indexer_check().
+ * Asynchronous on cuda_stream; argument errors return before any work.
+ */
+DSA_API int dsa_indexer_fwd_pooled(
+    const void *q, const void *k, const float *gate, const float *ape,
+    const uint8_t *valid, const float *w, int S, int B, int H, int D, int T,
+    int kpool, int first_key, int index_topk, const int32_t *q_pos,
+    int32_t *out_tokens, int32_t *out_pools, float *out_scores,
+    void *workspace, size_t workspace_bytes, void *cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -50,6 +50,15 @@ def lib():
     L.dsa_indexer_fwd_host.restype = I
     L.dsa_indexer_fwd_host.argtypes = [P, P, P, I, I, I, I, I, I, I, P, P, P,
                                        P, P, Z, P]
+    L.dsa_kpool_compress.restype = I
+    L.dsa_kpool_compress.argtypes = [P, P, P, P, I, I, I, I, I, P, P, P]
+    L.dsa_expand_selection.restype = I
+    L.dsa_expand_selection.argtypes = [P, ctypes.c_longlong, I, I, I, P, P]
+    L.dsa_indexer_pooled_workspace_size.restype = Z
+    L.dsa_indexer_pooled_workspace_size.argtypes = [I] * 8
+    L.dsa_indexer_fwd_pooled.restype = I
+    L.dsa_indexer_fwd_pooled.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I,
+                                         I, I, P, P, P, P, P, Z, P]
     L.dsa_indexer_bwd_workspace_size.restype = Z
     L.dsa_indexer_bwd_workspace_size.argtypes = []
     L.dsa_indexer_bwd.restype = I
@@ -288,3 +297,37 @@ def test_bwd_rejects_bad_arguments(lib):
     assert call(ws=None) == WORKSPACE
     assert call(nb=255) == WORKSPACE
     assert call(ws=FAKE + 16) == INVALID
+
+
+def test_pool_entry_points_reject_bad_arguments(lib):
+    pw = lib.dsa_indexer_pooled_workspace_size
+    assert pw(16, 1, 64, 128, 64, 4, 0, 32) > 256
+    assert pw(16, 1, 64, 128, 64, 4, 0, 30) == 0   # topk not a multiple
+    assert pw(16, 1, 64, 128, 64, 0, 0, 32) == 0   # kpool 0
+    assert pw(16, 1, 64, 128, 3, 4, 0, 32) == 256  # no whole pool
+    need = pw(16, 1, 64, 128, 64, 4, 0, 32)
+    f = lib.dsa_indexer_fwd_pooled
+
+    def call(q=FAKE, k=FAKE, kpool=4, topk=32, D=128, ws=FAKE, nb=need,
+             fk=0):
+        return f(q, k, FAKE, FAKE, None, FAKE, 16, 1, 64, D, 64, kpool, fk,
+                 topk, None, FAKE, FAKE, FAKE, ws, nb, None)
+    assert call(q=None) == INVALID
+    assert call(k=None) == INVALID
+    assert call(kpool=9) == UNSUPPORTED   # more slots than the kernel holds
+    assert call(topk=30) == INVALID
+    assert call(D=60) == UNSUPPORTED
+    assert call(fk=-1) == INVALID
+    assert call(ws=None) == WORKSPACE
+    assert call(nb=need - 1) == WORKSPACE
+    assert call(ws=FAKE + 16) == INVALID
+    c = lib.dsa_kpool_compress
+    assert c(None, FAKE, FAKE, None, 64, 1, 128, 4, 0, FAKE, None,
+             None) == INVALID
+    assert c(FAKE, FAKE, FAKE, None, 64, 1, 128, 9, 0, FAKE, None,
+             None) == UNSUPPORTED
+    assert c(FAKE + 8, FAKE, FAKE, None, 64, 1, 128, 4, 0, FAKE, None,
+             None) == INVALID
+    e = lib.dsa_expand_selection
+    assert e(None, 1, 4, 4, 0, FAKE, None) == INVALID
+    assert e(FAKE, 1, 0, 4, 0, FAKE, None) == INVALID
