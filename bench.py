@@ -24,6 +24,7 @@ the same workload; only rank 0 runs it.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -785,6 +786,166 @@ def run_backward(args):
     return 0
 
 
+def run_pooled(args):
+    """The pool variant at the C4 prefill shape: 2 x 16384 tokens pooled 4
+    at a time (4096 pools per sequence), 16384 queries per sequence, the
+    best 512 pools = 2048 tokens per row."""
+    import numpy as np
+    import torch
+
+    import dsa_sparse_attention_fwd_gb300 as dsa
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dsa.build()
+    dsa.load_library()
+    B, S, T, H, D, kpool, fk, itopk = 2, 16384, 16384, 64, 128, 4, 0, 2048
+    g = torch.Generator().manual_seed(21)
+    q = torch.randn((S, B, H, D), generator=g).to(torch.bfloat16)
+    k = torch.randn((T, B, D), generator=g).to(torch.bfloat16)
+    gate = torch.randn((T, B, D), generator=g)
+    ape = torch.randn((kpool, D), generator=g) * 0.5
+    w = torch.randn((S, B, H), generator=g) * 0.125
+    P = (T - fk) // kpool
+    pos = np.arange(S, dtype=np.int64)
+    pairs = B * int(np.clip((pos + 1 - fk) // kpool, 0, P).sum())
+    flops = 2.0 * H * D * pairs
+    qd, kd, gd, ad, wd = (t.to(dev) for t in (q, k, gate, ape, w))
+    sk = itopk // kpool
+    tok = torch.empty((B, S, itopk), dtype=torch.int32, device=dev)
+    pl = torch.empty((B, S, sk), dtype=torch.int32, device=dev)
+    sc = torch.empty((B, S, sk), dtype=torch.float32, device=dev)
+    ws = torch.empty(dsa.dsa_indexer_pooled_workspace_size(
+        S, B, H, D, T, kpool, fk, itopk), dtype=torch.uint8, device=dev)
+    keys = torch.empty((P, B, D), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    lib = dsa.load_library()
+
+    def step():
+        dsa.dsa_indexer_fwd_pooled(qd, kd, gd, ad, wd, kpool, fk, itopk,
+                                   out_tokens=tok, out_pools=pl,
+                                   out_scores=sc, workspace=ws, stream=stream)
+
+    def compress():
+        rc = lib.dsa_kpool_compress(
+            ctypes.c_void_p(kd.data_ptr()), ctypes.c_void_p(gd.data_ptr()),
+            ctypes.c_void_p(ad.data_ptr()), None, T, B, D, kpool, fk,
+            ctypes.c_void_p(keys.data_ptr()), None,
+            ctypes.c_void_p(stream.cuda_stream))
+        if rc != 0:
+            raise RuntimeError(f"dsa_kpool_compress {rc}")
+    for _ in range(max(args.warmup, 3)):
+        flush.fill_(1.0)
+        step()
+        compress()
+    torch.cuda.synchronize()
+    if dsa.dsa_indexer_check(ws) != 0:
+        raise RuntimeError("device status")
+    K = args.steps
+    mk = lambda: torch.cuda.Event(enable_timing=True)
+    ev = [(mk(), mk(), mk(), mk()) for _ in range(K)]
+    sampler = ClockSampler(local)
+    torch.cuda.synchronize()
+    barrier_ranks(world)
+    sampler.start()
+    time.sleep(0.2)
+    t0 = time.perf_counter()
+    for i in range(K):
+        flush.fill_(1.0)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+        flush.fill_(1.0)
+        ev[i][2].record(stream)
+        compress()
+        ev[i][3].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    barrier_ranks(world)
+    clocks = sampler.stop()
+    t_step = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in ev) / K,
+                            world, dev)
+    t_comp = sum(e[2].elapsed_time(e[3]) for e in ev) / K
+    # end to end: inputs in from pinned host memory, token ids back
+    hin = [t.pin_memory() for t in (q, k, gate, ape, w)]
+    din = [qd, kd, gd, ad, wd]
+    hout = torch.empty(tok.shape, dtype=torch.int32, pin_memory=True)
+    e2e = []
+    for i in range(max(3, min(K, 10)) + 2):
+        a_, b_ = mk(), mk()
+        a_.record(stream)
+        for d_, h_ in zip(din, hin):
+            d_.copy_(h_, non_blocking=True)
+        step()
+        hout.copy_(tok, non_blocking=True)
+        b_.record(stream)
+        b_.synchronize()
+        if i >= 2:
+            e2e.append(a_.elapsed_time(b_))
+    t_e2e = max_over_ranks(sum(e2e) / len(e2e), world, dev)
+    if rank != 0:
+        return 0
+    peaks, peak_src = read_peaks()
+    hbm_peak = float(peaks["hbm_gbs"])
+    cbytes = T * B * D * (2 + 4) + kpool * D * 4 + P * B * D * 2
+    comp_gbs = cbytes / (t_comp * 1e-3) / 1e9
+    value = world * flops / (t_step * 1e-3) / 1e12
+    line = {
+        "metric": "indexer pooled fwd TFLOP/s (visible pool pairs)",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": t_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "c4_pool (pool variant)", "B": B, "S": S,
+                   "T_tokens": T, "kpool": kpool, "first_key": fk,
+                   "pools": P, "index_topk": itopk, "H": H, "D": D,
+                   "visible_pool_pairs": pairs, "flops_per_step": flops,
+                   "l2": "flushed before each step (256 MiB write, outside "
+                         "the timed events)",
+                   "parallelism": f"replicas x{world}"},
+        "queries_per_s": world * B * S / (t_step * 1e-3),
+        "kernels_ms": {"whole call (compress + score + select + expand)":
+                       t_step, "kpool_compress alone": t_comp},
+        "roofline": {"kernel": "kpool_compress", "bound": "hbm",
+                     "achieved": comp_gbs, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": comp_gbs / hbm_peak,
+                     "peak_source": f"{peak_src} copy bandwidth",
+                     "algorithmic": f"{cbytes:.4g} B per launch (k bf16 + "
+                                    "gate fp32 read, pooled keys written)",
+                     "traffic": read_traffic("pool")},
+        "e2e": {"value": world * flops / (t_e2e * 1e-3) / 1e12,
+                "unit": "TFLOP/s", "ms_per_step": t_e2e,
+                "h2d_bytes_per_step": sum(t.numel() * t.element_size()
+                                          for t in hin),
+                "d2h_bytes_per_step": hout.numel() * 4,
+                "api": "torch copies + dsa_indexer_fwd_pooled"},
+        "gpu_launches": K * 5,
+        "clocks": clocks,
+        "wall_s_timed_region": wall,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        rows = np.arange(B * S - 1, -1, -(B * S // 16), dtype=np.int64)
+        t0 = time.perf_counter()
+        ref = oracle.indexer_pooled_fwd(q, k, gate, ape, None, w, kpool, fk,
+                                        itopk, rows=rows)
+        dt = time.perf_counter() - t0
+        sp = int(np.asarray(ref["nvis"], np.int64).sum())
+        line["cpu_baseline"] = {
+            "value": 2.0 * H * D * sp / dt / 1e12, "unit": "TFLOP/s",
+            "cores": int(ref["threads"]), "kind": "oracle",
+            "sample": f"compression of all {P * B} pools + {rows.size} rows "
+                      f"({sp} visible pool pairs), {dt:.2f} s"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -804,6 +965,8 @@ def main():
         return run_varlen(args)
     if args.backward:
         return run_backward(args)
+    if args.workload == "c4_pool":
+        return run_pooled(args)
     return run_ours(args)
 
 

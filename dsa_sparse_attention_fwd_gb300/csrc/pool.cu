@@ -36,16 +36,19 @@ long long pool_count(int T, int kpool, int first_key) {
   return T > first_key ? (long long)(T - first_key) / kpool : 0;
 }
 
-// One thread per (pool, sequence, 4 channels): the kpool slots' gate, k
-// and position-embedding values are read once, the softmax over slots is
-// taken per channel in registers.  Consecutive threads cover consecutive
-// channels, so every load and store is coalesced.
+// One thread per (pool, sequence, 4 channels): the KP slots' gate, k and
+// position-embedding values are read once (every load issued before the
+// first use), the softmax over slots is taken per channel in registers.
+// Consecutive threads cover consecutive channels, so every load and store
+// is coalesced.
+template <int KP>
 __global__ void kpool_compress_kernel(
     const uint16_t *__restrict__ k, const float *__restrict__ gate,
     const float *__restrict__ ape, const uint8_t *__restrict__ valid, int B,
-    int D, int kpool, int first_key, long long P, uint16_t *__restrict__ keys,
+    int D, int first_key, long long P, uint16_t *__restrict__ keys,
     uint8_t *__restrict__ pool_valid, const int32_t *__restrict__ q_pos,
     int32_t *__restrict__ q_pos_shifted) {
+  constexpr int kpool = KP;  // slots per pool
   if (q_pos_shifted && blockIdx.x == 0)
     for (int b = threadIdx.x; b < B; b += blockDim.x)
       q_pos_shifted[b] = (q_pos ? __ldg(q_pos + b) : 0) - first_key;
@@ -58,43 +61,39 @@ __global__ void kpool_compress_kernel(
     const int b = (int)(pb % B);
     const long long p = pb / B;
     const long long tok0 = first_key + p * kpool;
-    float z[kMaxKpool][4], kv[kMaxKpool][4];
+    float z[KP][4], kv[KP][4];
     float zmax[4] = {-__int_as_float(0x7f800000), -__int_as_float(0x7f800000),
                      -__int_as_float(0x7f800000), -__int_as_float(0x7f800000)};
     bool all_valid = true;
 #pragma unroll
-    for (int s = 0; s < kMaxKpool; ++s) {
-      if (s < kpool) {
-        const size_t row = (size_t)(tok0 + s) * B + b;
-        const float4 g4 =
-            __ldg(reinterpret_cast<const float4 *>(gate + row * D) + c4);
-        const float4 a4 =
-            __ldg(reinterpret_cast<const float4 *>(ape + (size_t)s * D) + c4);
-        const uint2 k4 = __ldg(reinterpret_cast<const uint2 *>(k + row * D) +
-                               c4);
-        z[s][0] = g4.x + a4.x;
-        z[s][1] = g4.y + a4.y;
-        z[s][2] = g4.z + a4.z;
-        z[s][3] = g4.w + a4.w;
-        kv[s][0] = __uint_as_float(k4.x << 16);
-        kv[s][1] = __uint_as_float(k4.x & 0xFFFF0000u);
-        kv[s][2] = __uint_as_float(k4.y << 16);
-        kv[s][3] = __uint_as_float(k4.y & 0xFFFF0000u);
+    for (int s = 0; s < KP; ++s) {
+      const size_t row = (size_t)(tok0 + s) * B + b;
+      const float4 g4 =
+          __ldg(reinterpret_cast<const float4 *>(gate + row * D) + c4);
+      const float4 a4 =
+          __ldg(reinterpret_cast<const float4 *>(ape + (size_t)s * D) + c4);
+      const uint2 k4 =
+          __ldg(reinterpret_cast<const uint2 *>(k + row * D) + c4);
+      z[s][0] = g4.x + a4.x;
+      z[s][1] = g4.y + a4.y;
+      z[s][2] = g4.z + a4.z;
+      z[s][3] = g4.w + a4.w;
+      kv[s][0] = __uint_as_float(k4.x << 16);
+      kv[s][1] = __uint_as_float(k4.x & 0xFFFF0000u);
+      kv[s][2] = __uint_as_float(k4.y << 16);
+      kv[s][3] = __uint_as_float(k4.y & 0xFFFF0000u);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) zmax[q] = fmaxf(zmax[q], z[s][q]);
-        if (valid && c4 == 0) all_valid &= __ldg(valid + row) != 0;
-      }
+      for (int q = 0; q < 4; ++q) zmax[q] = fmaxf(zmax[q], z[s][q]);
+      if (valid && c4 == 0) all_valid &= __ldg(valid + row) != 0;
     }
     float num[4] = {0.f, 0.f, 0.f, 0.f}, den[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int s = 0; s < kMaxKpool; ++s) {
-      if (s < kpool) {
+    for (int s = 0; s < KP; ++s) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float ex = expf(z[s][q] - zmax[q]);
-          den[q] += ex;
-          num[q] = fmaf(ex, kv[s][q], num[q]);
-        }
+      for (int q = 0; q < 4; ++q) {
+        const float ex = expf(z[s][q] - zmax[q]);
+        den[q] += ex;
+        num[q] = fmaf(ex, kv[s][q], num[q]);
       }
     }
     uint2 out;
@@ -136,6 +135,35 @@ int grid_for(long long work) {
   return g < 1 ? 1 : (int)g;
 }
 
+cudaError_t launch_compress(const uint16_t *k, const float *gate,
+                            const float *ape, const uint8_t *valid, int B,
+                            int D, int kpool, int first_key, long long P,
+                            uint16_t *keys, uint8_t *pool_valid,
+                            const int32_t *q_pos, int32_t *q_pos_shifted,
+                            cudaStream_t st) {
+  const int grid = grid_for(P * B * (D / 4));
+#define DSA_KP_CASE(N)                                                       \
+  case N:                                                                    \
+    kpool_compress_kernel<N><<<grid, 256, 0, st>>>(                          \
+        k, gate, ape, valid, B, D, first_key, P, keys, pool_valid, q_pos,    \
+        q_pos_shifted);                                                      \
+    break;
+  switch (kpool) {
+    DSA_KP_CASE(1)
+    DSA_KP_CASE(2)
+    DSA_KP_CASE(3)
+    DSA_KP_CASE(4)
+    DSA_KP_CASE(5)
+    DSA_KP_CASE(6)
+    DSA_KP_CASE(7)
+    DSA_KP_CASE(8)
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef DSA_KP_CASE
+  return cudaGetLastError();
+}
+
 bool al(const void *p, unsigned a) {
   return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
 }
@@ -166,11 +194,12 @@ int dsa_kpool_compress(const void *k, const float *gate, const float *ape,
   if (P == 0) return DSA_OK;
   if (!out_keys || !dsa::al(out_keys, 16)) return DSA_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
-  dsa::kpool_compress_kernel<<<dsa::grid_for(P * B * (D / 4)), 256, 0, st>>>(
-      static_cast<const uint16_t *>(k), gate, ape, valid, B, D, kpool,
-      first_key, P, static_cast<uint16_t *>(out_keys), out_valid, nullptr,
-      nullptr);
-  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  return dsa::launch_compress(static_cast<const uint16_t *>(k), gate, ape,
+                              valid, B, D, kpool, first_key, P,
+                              static_cast<uint16_t *>(out_keys), out_valid,
+                              nullptr, nullptr, st) == cudaSuccess
+             ? DSA_OK
+             : DSA_ERR_CUDA;
 }
 
 int dsa_expand_selection(const int32_t *pools, long long rows, int select_k,
@@ -249,10 +278,10 @@ int dsa_indexer_fwd_pooled(const void *q, const void *k, const float *gate,
   int32_t *qp = reinterpret_cast<int32_t *>(
       ws + dsa::up256(fw) + dsa::up256((size_t)P * B * D * 2) +
       dsa::up256((size_t)P * B));
-  dsa::kpool_compress_kernel<<<dsa::grid_for(P * B * (D / 4)), 256, 0, st>>>(
-      static_cast<const uint16_t *>(k), gate, ape, valid, B, D, kpool,
-      first_key, P, keys, pool_valid, q_pos, qp);
-  if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
+  if (dsa::launch_compress(static_cast<const uint16_t *>(k), gate, ape, valid,
+                           B, D, kpool, first_key, P, keys, pool_valid, q_pos,
+                           qp, st) != cudaSuccess)
+    return DSA_ERR_CUDA;
   rc = dsa::forward_core(q, keys, w, S, B, H, D, (int)P, kpool, select_k, qp,
                          nullptr, out_pools, out_scores, workspace, fw, st,
                          nullptr, 0, true, pool_valid);

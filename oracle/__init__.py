@@ -244,7 +244,7 @@ def round_bf16(x) -> np.ndarray:
 
 def indexer_pooled_fwd(q, k_raw, gate, ape, valid, w, kpool: int,
                        first_key: int, index_topk: int, q_pos=None,
-                       want_logits: bool = False):
+                       want_logits: bool = False, rows=None):
     """The pool variant end to end (page "Module glm5next_dsa", "Shape of the
     pipeline"): kpool_compress -> index_scores over pools (a pool is a
     candidate when valid and whole-block visible) -> top index_topk / kpool
@@ -265,7 +265,8 @@ def indexer_pooled_fwd(q, k_raw, gate, ape, valid, w, kpool: int,
         _arr(q_pos, np.int32).astype(np.int64).reshape(B)
     shifted = (base - first_key).astype(np.int32)
     out = indexer_fwd(q, kt, w, kpool, index_topk // kpool, q_pos=shifted,
-                      want_logits=want_logits, key_valid=c["valid"])
+                      want_logits=want_logits, key_valid=c["valid"],
+                      rows=rows)
     out["tokens"] = expand_selection(out["idx"], kpool, first_key)
     out["keys_bf16"] = keys
     out["pool_valid"] = c["valid"]
