@@ -59,6 +59,11 @@ def _load():
             lib.oracle_kpool_compress.argtypes = [
                 P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_int, ctypes.c_int, P, P]
+            lib.oracle_sparse_mla_fwd.restype = ctypes.c_int
+            lib.oracle_sparse_mla_fwd.argtypes = [
+                P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                P, P, ctypes.c_int]
             lib.oracle_expand_selection.restype = None
             lib.oracle_expand_selection.argtypes = [
                 P, ctypes.c_longlong, ctypes.c_int, ctypes.c_int,
@@ -271,3 +276,26 @@ def indexer_pooled_fwd(q, k_raw, gate, ape, valid, w, kpool: int,
     out["keys_bf16"] = keys
     out["pool_valid"] = c["valid"]
     return out
+
+
+def sparse_mla_fwd(q, c, idx, scale: float, n_threads: int | None = None):
+    """Sparse MLA forward over selected tokens (see oracle_sparse_mla_fwd in
+    the C file): q [S,B,H,Dc] bf16, latent cache c [T,B,Dc] bf16, idx
+    [B,S,topk] int32 token ids.  Returns {"o": [S,B,H,Dc] float64,
+    "lse": [S,B,H] float64}."""
+    lib = _load()
+    qb, cb = _bits(q), _bits(c)
+    S, B, H, Dc = qb.shape
+    T = cb.shape[0]
+    assert cb.shape == (T, B, Dc), cb.shape
+    gi = _arr(idx, np.int32)
+    topk = gi.shape[-1]
+    gi = gi.reshape(B, S, topk)
+    o = np.empty((S, B, H, Dc), np.float64)
+    lse = np.empty((S, B, H), np.float64)
+    if n_threads is None:
+        n_threads = os.cpu_count() or 1
+    lib.oracle_sparse_mla_fwd(_ptr(qb), _ptr(cb), _ptr(gi), S, B, H, Dc, T,
+                              topk, float(scale), _ptr(o), _ptr(lse),
+                              int(n_threads))
+    return {"o": o, "lse": lse}

@@ -423,3 +423,112 @@ void oracle_expand_selection(const int32_t *pools, long long rows,
         }
     }
 }
+
+/*
+ * Sparse MLA forward over the selected tokens (page "Module glm5next_dsa",
+ * "Shape of the pipeline": "-> NoPE MLA restricted to those tokens"; the
+ * NeMo AutoModel pages list tilelang_sparse_mla_fwd after the indexer; the
+ * latent width is kv_lora_rank, section "Constants", KERNEL_KV_LORA_DIM).
+ * The pages print no formula; this is attention in the MLA latent space
+ * with no rotary part, the latent row of a selected token serving as both
+ * key and value:
+ *
+ *   for row (b, s), head h, and the slots i whose token j_i = idx[b,s,i]
+ *   lies in [0, T) (-1 and out-of-range slots are skipped; repeated tokens
+ *   count once per slot):
+ *     x_i = scale * sum_d q[s,b,h,d] * c[j_i,b,d]
+ *     o[s,b,h,:] = sum_i softmax(x)_i * c[j_i,b,:]
+ *     lse[s,b,h] = log sum_i exp(x_i)           (natural log)
+ *   a row with no such slot: o = 0, lse = -inf.
+ *
+ * q [S, B, H, Dc] bf16 bits, c [T, B, Dc] bf16 bits, idx [B, S, topk];
+ * out_o [S, B, H, Dc] double, out_lse [S, B, H] double.  Rows in parallel.
+ */
+typedef struct {
+    const uint16_t *q, *c;
+    const int32_t *idx;
+    int S, B, H, Dc, T, topk;
+    double scale;
+    double *o, *lse;
+    long long next;
+    pthread_mutex_t lock;
+} mla_job_t;
+
+static void mla_row(mla_job_t *jb, long long row)
+{
+    const int b = (int)(row / jb->S), s = (int)(row % jb->S);
+    const int32_t *sel = jb->idx + ((size_t)b * jb->S + s) * jb->topk;
+    double *x = (double *)malloc(sizeof(double) * (size_t)(jb->topk > 0 ? jb->topk : 1));
+    for (int h = 0; h < jb->H; ++h) {
+        const uint16_t *qh = jb->q + (((size_t)s * jb->B + b) * jb->H + h) * jb->Dc;
+        double *oh = jb->o + (((size_t)s * jb->B + b) * jb->H + h) * jb->Dc;
+        double xmax = -INFINITY;
+        int n = 0;
+        for (int i = 0; i < jb->topk; ++i) {
+            const int32_t j = sel[i];
+            x[i] = -INFINITY;
+            if (j < 0 || j >= jb->T) continue;
+            const uint16_t *cj = jb->c + ((size_t)j * jb->B + b) * jb->Dc;
+            double dot = 0.0;
+            for (int d = 0; d < jb->Dc; ++d)
+                dot += bf16_to_double(qh[d]) * bf16_to_double(cj[d]);
+            x[i] = jb->scale * dot;
+            if (x[i] > xmax) xmax = x[i];
+            ++n;
+        }
+        for (int d = 0; d < jb->Dc; ++d) oh[d] = 0.0;
+        if (n == 0) {
+            jb->lse[((size_t)s * jb->B + b) * jb->H + h] = -INFINITY;
+            continue;
+        }
+        double den = 0.0;
+        for (int i = 0; i < jb->topk; ++i) {
+            const int32_t j = sel[i];
+            if (j < 0 || j >= jb->T) continue;
+            const double e = exp(x[i] - xmax);
+            den += e;
+            const uint16_t *cj = jb->c + ((size_t)j * jb->B + b) * jb->Dc;
+            for (int d = 0; d < jb->Dc; ++d) oh[d] += e * bf16_to_double(cj[d]);
+        }
+        for (int d = 0; d < jb->Dc; ++d) oh[d] /= den;
+        jb->lse[((size_t)s * jb->B + b) * jb->H + h] = xmax + log(den);
+    }
+    free(x);
+}
+
+static void *mla_worker(void *arg)
+{
+    mla_job_t *jb = (mla_job_t *)arg;
+    const long long rows = (long long)jb->S * jb->B;
+    for (;;) {
+        pthread_mutex_lock(&jb->lock);
+        long long r = jb->next++;
+        pthread_mutex_unlock(&jb->lock);
+        if (r >= rows) break;
+        mla_row(jb, r);
+    }
+    return NULL;
+}
+
+int oracle_sparse_mla_fwd(const uint16_t *q, const uint16_t *c,
+                          const int32_t *idx, int S, int B, int H, int Dc,
+                          int T, int topk, double scale, double *out_o,
+                          double *out_lse, int n_threads)
+{
+    mla_job_t jb;
+    memset(&jb, 0, sizeof jb);
+    jb.q = q; jb.c = c; jb.idx = idx;
+    jb.S = S; jb.B = B; jb.H = H; jb.Dc = Dc; jb.T = T; jb.topk = topk;
+    jb.scale = scale; jb.o = out_o; jb.lse = out_lse; jb.next = 0;
+    pthread_mutex_init(&jb.lock, NULL);
+    if (n_threads < 1) n_threads = 1;
+    if (n_threads > 256) n_threads = 256;
+    pthread_t th[256];
+    int started = 0;
+    for (int i = 1; i < n_threads; ++i)
+        if (pthread_create(&th[started], NULL, mla_worker, &jb) == 0) ++started;
+    mla_worker(&jb);
+    for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
+    pthread_mutex_destroy(&jb.lock);
+    return started + 1;
+}

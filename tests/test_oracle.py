@@ -604,3 +604,94 @@ def test_pooled_forward_with_one_slot_pools_is_the_plain_forward():
     np.testing.assert_array_equal(pooled["tokens"].reshape(B * S, 9),
                                   plain["idx"])
     np.testing.assert_array_equal(pooled["scores"], plain["scores"])
+
+
+# ---- sparse MLA forward over selected tokens ------------------------------
+
+def _mla_inputs(S, B, H, Dc, T, seed):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn((S, B, H, Dc), generator=g).to(torch.bfloat16)
+    c = torch.randn((T, B, Dc), generator=g).to(torch.bfloat16)
+    return q, c
+
+
+def test_mla_single_slot_and_repeated_token():
+    """One valid slot: the output is that token's latent row and lse its
+    scaled score; the same token in n slots: the same output, lse + log n."""
+    S, B, H, Dc, T = 3, 2, 4, 16, 9
+    q, c = _mla_inputs(S, B, H, Dc, T, 1)
+    qf, cf = q.double().numpy(), c.double().numpy()
+    idx = np.full((B, S, 5), -1, np.int32)
+    idx[:, :, 2] = 4
+    r = oracle.sparse_mla_fwd(q, c, idx, 0.125)
+    for s in range(S):
+        for b in range(B):
+            for h in range(H):
+                np.testing.assert_array_equal(r["o"][s, b, h], cf[4, b])
+                x = 0.125 * float(qf[s, b, h] @ cf[4, b])
+                assert abs(r["lse"][s, b, h] - x) <= 1e-12 * (1 + abs(x))
+    idx[:, :, :] = 4
+    r3 = oracle.sparse_mla_fwd(q, c, idx, 0.125)
+    np.testing.assert_allclose(r3["o"], r["o"], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(r3["lse"], r["lse"] + math.log(5), rtol=0,
+                               atol=1e-12)
+
+
+def test_mla_two_slot_closed_form():
+    """Two tokens whose scaled scores differ by ln 3: weights 1/4 and 3/4."""
+    Dc = 8
+    q = torch.zeros((1, 1, 1, Dc))
+    q[0, 0, 0, 0] = 1.0
+    c = torch.zeros((2, 1, Dc))
+    c[0, 0] = torch.tensor([0.0, 1, 2, 3, 4, 5, 6, 7])
+    c[1, 0] = torch.tensor([2.0, -1, 0, 1, 8, 0, 2, 2])
+    # scores (scale 1): c[0,0,0] = 0 and c[1,0,0] = 2; choose scale so that
+    # scale * 2 = ln 3
+    scale = math.log(3.0) / 2.0
+    r = oracle.sparse_mla_fwd(q.to(torch.bfloat16), c.to(torch.bfloat16),
+                              np.array([[[0, 1]]], np.int32), scale)
+    want = 0.25 * c[0, 0].numpy() + 0.75 * c[1, 0].numpy()
+    np.testing.assert_allclose(r["o"][0, 0, 0], want, rtol=0, atol=1e-12)
+    assert abs(r["lse"][0, 0, 0] - math.log(4.0)) <= 1e-12
+
+
+def test_mla_invalid_slots_permutation_and_shift():
+    """-1 and out-of-range slots are skipped; permuting the slots changes
+    nothing; an empty row gives o = 0 and lse = -inf."""
+    S, B, H, Dc, T, k = 5, 2, 3, 32, 20, 12
+    q, c = _mla_inputs(S, B, H, Dc, T, 2)
+    rng = np.random.default_rng(3)
+    idx = rng.integers(0, T, size=(B, S, k)).astype(np.int32)
+    idx[:, :, ::4] = -1
+    r = oracle.sparse_mla_fwd(q, c, idx, 0.1)
+    bad = idx.copy()
+    bad[:, :, ::4] = T + 3  # out of range: skipped like -1
+    rb = oracle.sparse_mla_fwd(q, c, bad, 0.1)
+    np.testing.assert_array_equal(rb["o"], r["o"])
+    perm = rng.permutation(k)
+    rp = oracle.sparse_mla_fwd(q, c, idx[:, :, perm], 0.1)
+    np.testing.assert_allclose(rp["o"], r["o"], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(rp["lse"], r["lse"], rtol=0, atol=1e-12)
+    empty = np.full((B, S, k), -1, np.int32)
+    re_ = oracle.sparse_mla_fwd(q, c, empty, 0.1)
+    assert np.all(re_["o"] == 0) and np.all(np.isneginf(re_["lse"]))
+
+
+def test_mla_convex_combination_and_head_independence():
+    """Each output is a convex combination of the selected rows (inside
+    their per-channel range), and a head's output depends on its own query
+    only (heads permute with the queries)."""
+    S, B, H, Dc, T, k = 4, 1, 6, 16, 30, 9
+    q, c = _mla_inputs(S, B, H, Dc, T, 4)
+    idx = np.random.default_rng(5).integers(0, T, size=(B, S, k)).astype(
+        np.int32)
+    r = oracle.sparse_mla_fwd(q, c, idx, 0.2)
+    cf = c.double().numpy()
+    for s in range(S):
+        rows = cf[idx[0, s], 0]
+        lo, hi = rows.min(axis=0), rows.max(axis=0)
+        assert np.all(r["o"][s, 0] >= lo - 1e-12)
+        assert np.all(r["o"][s, 0] <= hi + 1e-12)
+    perm = np.random.default_rng(6).permutation(H)
+    rp = oracle.sparse_mla_fwd(q[:, :, perm].contiguous(), c, idx, 0.2)
+    np.testing.assert_array_equal(rp["o"], r["o"][:, :, perm])
