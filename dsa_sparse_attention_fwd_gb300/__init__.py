@@ -31,7 +31,8 @@ __all__ = [
     "dsa_indexer_varlen_workspace_size", "dsa_indexer_fwd_varlen",
     "dsa_indexer_bwd", "dsa_indexer_bwd_workspace_size",
     "dsa_kpool_compress", "dsa_expand_selection",
-    "dsa_indexer_pooled_workspace_size", "dsa_indexer_fwd_pooled", "STATUS",
+    "dsa_indexer_pooled_workspace_size", "dsa_indexer_fwd_pooled",
+    "dsa_sparse_mla_fwd", "dsa_sparse_mla_workspace_size", "STATUS",
 ]
 
 STATUS = {
@@ -112,6 +113,11 @@ def load_library(path: str | None = None):
         lib.dsa_indexer_fwd_pooled.argtypes = [P, P, P, P, P, P, I, I, I, I,
                                                I, I, I, I, P, P, P, P, P, Z,
                                                P]
+        lib.dsa_sparse_mla_workspace_size.restype = Z
+        lib.dsa_sparse_mla_workspace_size.argtypes = []
+        lib.dsa_sparse_mla_fwd.restype = I
+        lib.dsa_sparse_mla_fwd.argtypes = [P, P, P, I, I, I, I, I, I,
+                                           ctypes.c_float, P, P, P, Z, P]
         _lib = lib
         return lib
 
@@ -339,6 +345,42 @@ def dsa_indexer_fwd_pooled(q, k, gate, ape, w, kpool, first_key, index_topk,
     if rc != 0:
         raise DsaError(rc, "dsa_indexer_fwd_pooled")
     return out_tokens, out_pools, out_scores, workspace
+
+
+def dsa_sparse_mla_workspace_size() -> int:
+    return int(load_library().dsa_sparse_mla_workspace_size())
+
+
+def dsa_sparse_mla_fwd(q, c, idx, scale, out_o=None, out_lse=None,
+                       workspace=None, stream=None):
+    """Sparse MLA forward on device tensors: q [S,B,H,Dc] bf16, latent
+    cache c [T,B,Dc] bf16, idx [B,S,topk] int32 token ids.  Returns (o
+    [S,B,H,Dc] fp32, lse [S,B,H] fp32, workspace)."""
+    lib = load_library()
+    for name, t, dt in (("q", q, torch.bfloat16), ("c", c, torch.bfloat16),
+                        ("idx", idx, torch.int32)):
+        if t.dtype != dt or not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous {dt}")
+    S, B, H, Dc = q.shape
+    T = c.shape[0]
+    if tuple(c.shape) != (T, B, Dc) or idx.shape[:2] != (B, S):
+        raise ValueError("c must be [T, B, Dc] and idx [B, S, topk]")
+    topk = idx.shape[-1]
+    dev = q.device
+    if out_o is None:
+        out_o = torch.empty((S, B, H, Dc), dtype=torch.float32, device=dev)
+    if out_lse is None:
+        out_lse = torch.empty((S, B, H), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(dsa_sparse_mla_workspace_size(),
+                                dtype=torch.uint8, device=dev)
+    rc = lib.dsa_sparse_mla_fwd(_ptr(q), _ptr(c), _ptr(idx), S, B, H, Dc, T,
+                                topk, float(scale), _ptr(out_o),
+                                _ptr(out_lse), _ptr(workspace),
+                                workspace.numel(), _stream(stream))
+    if rc != 0:
+        raise DsaError(rc, "dsa_sparse_mla_fwd")
+    return out_o, out_lse, workspace
 
 
 def dsa_indexer_logits(q, k, w, compress_ratio, q_pos=None, logits=None,

@@ -96,6 +96,11 @@ namespace dsa {
 // 64 d x H heads x 1 sequence x `queries` queries (256/H for the prefill
 // tile = 256 rows of 128 bytes; 1 for decode, given indices and backward).
 int encode_q(CUtensorMap *m, const Problem &p, int queries) {
+  return encode_q_heads(m, p, queries, p.H);
+}
+
+// As encode_q with a box of `heads` heads (a divisor of H).
+int encode_q_heads(CUtensorMap *m, const Problem &p, int queries, int heads) {
   auto fn = encode_fn();
   if (!fn) return DSA_ERR_CUDA;
   const cuuint64_t dims[4] = {(cuuint64_t)p.D, (cuuint64_t)p.H,
@@ -103,7 +108,7 @@ int encode_q(CUtensorMap *m, const Problem &p, int queries) {
   const cuuint64_t strides[3] = {(cuuint64_t)p.D * 2,
                                  (cuuint64_t)p.H * p.D * 2,
                                  (cuuint64_t)p.B * p.H * p.D * 2};
-  const cuuint32_t box[4] = {(cuuint32_t)dsa::kChunk, (cuuint32_t)p.H, 1,
+  const cuuint32_t box[4] = {(cuuint32_t)dsa::kChunk, (cuuint32_t)heads, 1,
                              (cuuint32_t)queries};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,

@@ -131,6 +131,7 @@ cudaError_t launch_fill_masked(float *logits, size_t n, cudaStream_t st);
 // TMA map of q [S, B, H, D] bf16 as (d, h, b, s) with a box of 64 d x H
 // heads x 1 x `queries` (returns a dsa_status code).
 int encode_q(CUtensorMap *m, const Problem &p, int queries);
+int encode_q_heads(CUtensorMap *m, const Problem &p, int queries, int heads);
 
 // Multiprocessor count of the current device (a dsa_status code).
 int device_num_sms(int *num_sms);

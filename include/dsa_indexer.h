@@ -398,6 +398,34 @@ DSA_API int dsa_indexer_fwd_pooled(
     int32_t *out_tokens, int32_t *out_pools, float *out_scores,
     void *workspace, size_t workspace_bytes, void *cuda_stream);
 
+/*
+ * Sparse MLA forward over selected tokens (page "Module glm5next_dsa",
+ * "Shape of the pipeline": "-> NoPE MLA restricted to those tokens"; the
+ * latent width is kv_lora_rank).  Attention in the latent space, no rotary
+ * part, the latent row of a selected token being both key and value: for
+ * row (b, s), head h and the slots i whose token j_i = idx[b, s, i] is in
+ * [0, T),
+ *     x_i = scale * q[s, b, h, :] . c[j_i, b, :]
+ *     out_o[s, b, h, :] = sum_i softmax(x)_i * c[j_i, b, :]
+ *     out_lse[s, b, h]  = ln sum_i exp(x_i)
+ * (-1 slots skipped, repeated tokens counted once per slot; a row with no
+ * valid slot gets o = 0 and lse = -inf; an index outside [-1, T) also sets
+ * DSA_ERR_INDEX_RANGE in the status word).
+ *   q [S, B, H, Dc] bf16 (latent-space queries), c [T, B, Dc] bf16 (latent
+ *   cache), idx [B, S, topk] int32 (e.g. the pool variant's token ids);
+ *   out_o [S, B, H, Dc] fp32, out_lse [S, B, H] fp32.
+ *   Envelope: H a multiple of 64, Dc in {128, 256, 384, 512}, scale > 0;
+ *   q and c 16-byte aligned.  Precision: scores and outputs accumulate in
+ *   fp32; the softmax weights enter the output product as bf16.
+ *   workspace: dsa_sparse_mla_workspace_size() bytes, 256-byte aligned.
+ */
+DSA_API size_t dsa_sparse_mla_workspace_size(void);
+DSA_API int dsa_sparse_mla_fwd(const void *q, const void *c,
+                               const int32_t *idx, int S, int B, int H,
+                               int Dc, int T, int topk, float scale,
+                               float *out_o, float *out_lse, void *workspace,
+                               size_t workspace_bytes, void *cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif

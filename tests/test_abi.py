@@ -59,6 +59,11 @@ def lib():
     L.dsa_indexer_fwd_pooled.restype = I
     L.dsa_indexer_fwd_pooled.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I,
                                          I, I, P, P, P, P, P, Z, P]
+    L.dsa_sparse_mla_workspace_size.restype = Z
+    L.dsa_sparse_mla_workspace_size.argtypes = []
+    L.dsa_sparse_mla_fwd.restype = I
+    L.dsa_sparse_mla_fwd.argtypes = [P, P, P, I, I, I, I, I, I,
+                                     ctypes.c_float, P, P, P, Z, P]
     L.dsa_indexer_bwd_workspace_size.restype = Z
     L.dsa_indexer_bwd_workspace_size.argtypes = []
     L.dsa_indexer_bwd.restype = I
@@ -331,3 +336,22 @@ def test_pool_entry_points_reject_bad_arguments(lib):
     e = lib.dsa_expand_selection
     assert e(None, 1, 4, 4, 0, FAKE, None) == INVALID
     assert e(FAKE, 1, 0, 4, 0, FAKE, None) == INVALID
+
+
+def test_sparse_mla_rejects_bad_arguments(lib):
+    f = lib.dsa_sparse_mla_fwd
+    assert lib.dsa_sparse_mla_workspace_size() == 256
+
+    def call(q=FAKE, H=64, Dc=512, scale=0.05, ws=FAKE, nb=256, topk=32):
+        return f(q, FAKE, FAKE, 4, 1, H, Dc, 100, topk, scale, FAKE, FAKE, ws,
+                 nb, None)
+    assert call(q=None) == INVALID
+    assert call(topk=0) == INVALID
+    assert call(scale=0.0) == INVALID
+    assert call(scale=-1.0) == INVALID
+    assert call(H=32) == UNSUPPORTED
+    assert call(Dc=576) == UNSUPPORTED
+    assert call(Dc=64) == UNSUPPORTED
+    assert call(q=FAKE + 8) == INVALID
+    assert call(ws=None) == WORKSPACE
+    assert call(nb=100) == WORKSPACE
