@@ -7,15 +7,16 @@
 //     o[t, h, :] = sum_i softmax(x)_i * c[j_i, :],   lse[t, h] = ln sum e^x
 //
 // A work item is one query row and 64 of its heads; a tile is 128
-// consecutive slots.  Two passes over the row's tiles, each tile's latent
-// rows gathered into shared memory (cp.async, zero fill for -1 slots):
-//   pass A: S^T[slot, h] = C_g . Q^T on the tensor cores (M = 128 slots,
-//           N = 64 heads, K = Dc); the epilogue keeps each head's maximum.
-//   pass B: S^T again; the epilogue forms P^T = exp2(S * scale*log2(e) -
-//           m) in bf16 (0 for invalid slots) and each head's sum;
-//           O^T[d, h] += C_g^T . P^T (M = 128 latent dims per block, N =
-//           64, K = 128 slots; the gathered tile read d-major and P^T
-//           head-major), accumulated in tensor memory over the row.
+// consecutive slots, its latent rows gathered into shared memory (cp.async,
+// zero fill for -1 slots).  One pass over the row's tiles:
+//   S^T[slot, h] = C_g . Q^T on the tensor cores (M = 128 slots, N = 64
+//   heads, K = Dc); the epilogue takes each head's tile maximum, moves the
+//   running maximum m when a tile exceeds it by more than 2^8 (rescaling
+//   the accumulated O^T and l by the change), forms P^T = exp2(S *
+//   scale*log2(e) - m) in bf16 (0 for invalid slots; at most 2^8) and each
+//   head's sum l; O^T[d, h] += C_g^T . P^T (M = 128 latent dims per block,
+//   N = 64, K = 128 slots; the gathered tile read d-major and P^T
+//   head-major), accumulated in tensor memory over the row.
 // The row ends with o = O^T / l and lse = (m + log2 l) * ln 2; a row
 // without a valid slot gets o = 0 and lse = -inf.
 //
@@ -54,7 +55,8 @@ struct MlaSmem {
   static constexpr int kOffRed = kOffRing + kMlaRing * kRingBytes;  // [4][64]
   static constexpr int kOffM = kOffRed + 4 * kMlaH * 4;             // [64]
   static constexpr int kOffL = kOffM + kMlaH * 4;                   // [64]
-  static constexpr int kOffBar = kOffL + kMlaH * 4;
+  static constexpr int kOffF = kOffL + kMlaH * 4;  // [64] factors + flag
+  static constexpr int kOffBar = kOffF + (kMlaH + 4) * 4;
   // k_full k_empty q_full q_empty r_full[8] r_empty[8] s_full[2]
   // s_empty[2] p_full p_empty o_full o_empty
   static constexpr int kNumBars = 4 + 2 * kMlaRing + 4 + 4;
@@ -71,10 +73,10 @@ struct MlaGeom {
   int items, S, HG, ntiles;
 };
 
-// Walks this CTA's tile visits: items round by round (zig-zag over the
-// CTAs), each item's tiles in pass A then again in pass B.
+// Walks this CTA's tiles: items round by round (zig-zag over the CTAs),
+// each item's tiles in order.
 struct MlaCursor {
-  int round, row, b, s, hg, pass, tile;
+  int round, row, b, s, hg, tile;
   bool valid;
 };
 
@@ -88,7 +90,6 @@ __device__ __forceinline__ void mla_set_item(MlaCursor &c, const MlaGeom &g) {
   c.hg = (int)(it % g.HG);
   c.b = c.row / g.S;
   c.s = c.row % g.S;
-  c.pass = 0;
   c.tile = 0;
 }
 
@@ -99,15 +100,9 @@ __device__ __forceinline__ MlaCursor mla_begin(const MlaGeom &g) {
   return c;
 }
 
-// Advances one tile visit; returns 0 (same pass), 1 (pass B starts) or 2
-// (a new item starts).
+// Advances one tile; returns 0 (same item) or 2 (a new item starts).
 __device__ __forceinline__ int mla_next(MlaCursor &c, const MlaGeom &g) {
   if (++c.tile < g.ntiles) return 0;
-  if (c.pass == 0) {
-    c.pass = 1;
-    c.tile = 0;
-    return 1;
-  }
   ++c.round;
   mla_set_item(c, g);
   return 2;
@@ -313,9 +308,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         mma_bf16_by(d1, a1 + ao, b1 + bo, kIdescS, t != 0 ? 1u : 0u, lead);
       }
       mma_commit_by(s_full(sa), lead);
-      if (cur.pass == 0) {
-        mma_commit_by(k_empty, lead);
-      } else {
+      {
         const bool first = cur.tile == 0, last = cur.tile + 1 == g.ntiles;
         if (!wall(p_full, nb & 1u)) break;
         if (first && !wall(o_empty, (nitem & 1u) ^ 1u)) break;
@@ -350,92 +343,119 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     const int et = threadIdx.x - 32 * kMlaEpiWarp0;  // 0..127
     const int i = sp * 32 + lane;  // TMEM lane: the slot, or the latent dim
     const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
+    float *sF = reinterpret_cast<float *>(smem + L::kOffF);  // [64] factors
+    // the running maximum moves only when a tile exceeds it by more than
+    // 2^kSlack, so a weight is at most 2^kSlack and rescales stay rare
+    constexpr float kSlack = 8.f;
     MlaCursor cur = mla_begin(g);
-    uint32_t nv = 0, nb = 0, nitem = 0;
+    uint32_t nv = 0, nitem = 0;
     bool ok = true;
-    // one tile visit: S^T of this thread's slot into v (raw dots), and
-    // whether the slot holds a valid token
-    auto load_tile = [&](float (&v)[64], bool &valid, bool &bad) -> bool {
-      const int slot = nv % kMlaRing;
-      const uint32_t rph = (nv / kMlaRing) & 1u;
-      const int sa = nv & 1;
-      const uint32_t sph = (nv >> 1) & 1u;
-      const bool got = wait_bar(s_full(sa), sph, abort_flag, status) &&
-                       wait_bar(r_full(slot), rph, abort_flag, status);
-      if (!__all_sync(0xffffffffu, got)) return false;
-      tc_fence_after();
+    auto load_s = [&](uint32_t taddr, float (&v)[64]) {
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t u[32];
-        tmem_ld32(tmem + lane_off + kTmemSm + sa * Hg + c * 32, u);
+        __syncwarp();
+        tmem_ld32(taddr + c * 32, u);
         tmem_ld_wait();
         reg_fence32(u);
 #pragma unroll
         for (int q = 0; q < 32; ++q) v[c * 32 + q] = __uint_as_float(u[q]);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_empty(sa));
-      const int e = cur.tile * kTileKeys + i;
-      const bool in_row = e < topk;
-      const int j =
-          in_row ? reinterpret_cast<const int32_t *>(sRing +
-                                                     slot * L::kRingBytes)[i]
-                 : -1;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(r_empty(slot));
-      valid = j >= 0 && j < T;
-      bad |= in_row && (j < -1 || j >= T);
-      ++nv;
-      return true;
     };
 
     while (cur.valid) {
       if (named_bar_or(1, 128, !ok)) break;
       const int b = cur.b, s = cur.s, hg = cur.hg;
-      float acc0 = neg_inf, acc1 = neg_inf;
+      if (et < 64) sM[et] = neg_inf;  // running maximum (log2 domain)
+      named_bar_sync(3, 128);
+      float l0 = 0.f, l1 = 0.f;  // l of heads 2*lane, 2*lane + 1 (partial)
       bool bad = false;
       int step = 0;
-      // ---- pass A: each head's largest scaled score over valid slots ----
       while (ok && step == 0) {
-        float v[64];
-        bool valid;
-        if (!load_tile(v, valid, bad)) {
+        const int slot = nv % kMlaRing;
+        const uint32_t rph = (nv / kMlaRing) & 1u;
+        const int sa = nv & 1;
+        const uint32_t sph = (nv >> 1) & 1u;
+        const bool got = wait_bar(s_full(sa), sph, abort_flag, status) &&
+                         wait_bar(r_full(slot), rph, abort_flag, status);
+        if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }
+        tc_fence_after();
+        const uint32_t sS = tmem + lane_off + kTmemSm + sa * Hg;
+        const int e = cur.tile * kTileKeys + i;
+        const bool in_row = e < topk;
+        const int j =
+            in_row ? reinterpret_cast<const int32_t *>(sRing +
+                                                       slot * L::kRingBytes)[i]
+                   : -1;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(r_empty(slot));
+        const bool valid = j >= 0 && j < T;
+        bad |= in_row && (j < -1 || j >= T);
+        // each head's largest scaled score in the tile
+        float v[64];
+        load_s(sS, v);
 #pragma unroll
-        for (int h = 0; h < 64; ++h) v[h] = valid ? v[h] * scale_log2e : neg_inf;
+        for (int h = 0; h < 64; ++h)
+          v[h] = valid ? v[h] * scale_log2e : neg_inf;
         warp_fold64<true>(v, lane);
-        acc0 = fmaxf(acc0, v[0]);
-        acc1 = fmaxf(acc1, v[1]);
-        step = mla_next(cur, g);
-      }
-      if (named_bar_or(2, 128, !ok)) break;
-      sRed[sp * 64 + 2 * lane] = acc0;
-      sRed[sp * 64 + 2 * lane + 1] = acc1;
-      named_bar_sync(3, 128);
-      if (et < 64)
-        sM[et] = fmaxf(fmaxf(sRed[et], sRed[64 + et]),
-                       fmaxf(sRed[128 + et], sRed[192 + et]));
-      named_bar_sync(3, 128);
-      // ---- pass B: P^T in bf16 for the tensor core, each head's sum ----
-      acc0 = 0.f;
-      acc1 = 0.f;
-      step = 0;
-      const float4 *m4 = reinterpret_cast<const float4 *>(sM);
-      while (ok && step == 0) {
-        float v[64];
-        bool valid;
-        if (!load_tile(v, valid, bad)) {
-          ok = false;
-          break;
+        sRed[sp * 64 + 2 * lane] = v[0];
+        sRed[sp * 64 + 2 * lane + 1] = v[1];
+        named_bar_sync(3, 128);
+        bool moved = false;
+        if (et < 64) {
+          const float tmax = fmaxf(fmaxf(sRed[et], sRed[64 + et]),
+                                   fmaxf(sRed[128 + et], sRed[192 + et]));
+          const float mold = sM[et];
+          float f = 1.f;
+          if (tmax > mold + kSlack) {
+            f = exp2f(mold - tmax);  // 0 while nothing is accumulated
+            sM[et] = tmax;
+            moved = true;
+          }
+          sF[et] = f;
         }
-        if (!__all_sync(0xffffffffu, wait_bar(p_empty, (nb & 1u) ^ 1u,
+        // every thread sees the new maxima and factors, and whether any moved
+        const bool rescale = named_bar_or(3, 128, moved);
+        // the accumulator is idle once MMA2 of the previous tile is done
+        if (!__all_sync(0xffffffffu, wait_bar(p_empty, (nv & 1u) ^ 1u,
                                               abort_flag, status))) {
           ok = false;
           break;
         }
+        tc_fence_after();
+        if (rescale) {
+          l0 *= sF[2 * lane];
+          l1 *= sF[2 * lane + 1];
+          if (cur.tile > 0) {
+            // O^T[d, h] *= f[h]: this warp's 32 latent dims of every block
+#pragma unroll 1
+            for (int blk = 0; blk < NB; ++blk) {
+#pragma unroll 1
+              for (int c = 0; c < 2; ++c) {
+                const uint32_t ta = tmem + lane_off + kTmemO + blk * Hg + c * 32;
+                uint32_t u[32];
+                __syncwarp();
+                tmem_ld32(ta, u);
+                tmem_ld_wait();
+                reg_fence32(u);
+#pragma unroll
+                for (int q = 0; q < 32; ++q)
+                  u[q] = __float_as_uint(__uint_as_float(u[q]) * sF[c * 32 + q]);
+                tmem_st32(ta, u);
+              }
+            }
+            tmem_st_wait();
+          }
+        }
+        // P^T = exp2(x - m) for the tensor core (the fold consumed v)
+        load_s(sS, v);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_empty(sa));
+        const float4 *m4 = reinterpret_cast<const float4 *>(sM);
         const uint32_t prow = sP + i * 128;
 #pragma unroll
         for (int u8 = 0; u8 < 8; ++u8) {
@@ -460,19 +480,19 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
           }
           st_shared_v4(prow + ((u8 ^ (i & 7)) << 4), pk);
         }
-        // the tensor core (async proxy) reads P^T next
+        // the tensor core (async proxy) reads P^T and the rescaled O^T next
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(p_full);
-        ++nb;
         warp_fold64<false>(v, lane);
-        acc0 += v[0];
-        acc1 += v[1];
+        l0 += v[0];
+        l1 += v[1];
+        ++nv;
         step = mla_next(cur, g);
       }
       if (named_bar_or(2, 128, !ok)) break;
-      sRed[sp * 64 + 2 * lane] = acc0;
-      sRed[sp * 64 + 2 * lane + 1] = acc1;
+      sRed[sp * 64 + 2 * lane] = l0;
+      sRed[sp * 64 + 2 * lane + 1] = l1;
       named_bar_sync(3, 128);
       if (et < 64)
         sL[et] = ((sRed[et] + sRed[64 + et]) + sRed[128 + et]) + sRed[192 + et];
