@@ -119,3 +119,25 @@ def test_sparse_mla_over_pooled_selection(dsa):
     q = torch.randn((S, B, 64, Dc), generator=g).to(torch.bfloat16)
     c = torch.randn((T, B, Dc), generator=g).to(torch.bfloat16)
     check(dsa, q, c, tok.cpu(), 1.0 / math.sqrt(Dc))
+
+
+def test_sparse_mla_running_maximum_moves(dsa):
+    """Latent rows whose norm grows along the sequence, selected in
+    increasing token order: every later tile of 64 slots raises each head's
+    running maximum, many times by more than the kernel's 2^8 slack, so the
+    accumulated output and sums are rescaled tile after tile. The input is
+    checked to do that before the kernel runs."""
+    S, B, H, Dc, T, topk = 6, 1, 64, 256, 640, 640
+    scale = 0.5
+    g = torch.Generator().manual_seed(12)
+    q = torch.randn((S, B, H, Dc), generator=g).to(torch.bfloat16)
+    grow = (1.0 + torch.arange(T, dtype=torch.float32) / 40.0)[:, None, None]
+    c = (torch.randn((T, B, Dc), generator=g) * grow).to(torch.bfloat16)
+    idx = torch.arange(T, dtype=torch.int32).repeat(B, S, 1).contiguous()
+    x = scale * math.log2(math.e) * torch.einsum(
+        "shd,td->sht", q[:, 0].double(), c[:, 0].double())
+    tile_max = x.reshape(S, H, T // 64, 64).amax(dim=3)
+    running = torch.cummax(tile_max, dim=2).values
+    jumps = (running[:, :, 1:] - running[:, :, :-1]) > 8
+    assert jumps.sum(dim=2).min() >= 2
+    check(dsa, q, c, idx, scale)
