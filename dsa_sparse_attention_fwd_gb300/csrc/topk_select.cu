@@ -6,6 +6,17 @@
 // are fewer rows than SMs.  Scores are compared as order-preserving unsigned
 // keys (larger float <-> larger key; -0.0 folded onto +0.0 so the index
 // tie-break decides between them).
+//
+// Bucket route (every row except long rows whose histogram the scoring
+// kernel built): the row, staged in shared memory when it fits, is counted
+// into 4096 fine buckets spread linearly over its finite value range.  A
+// scan of the counts gives the bucket holding the topk-th key and each
+// kept bucket's start; the kept keys are scattered to their buckets and
+// each key's final position is its bucket start plus the number of keys of
+// the same bucket that precede it (larger key, or equal key and lower
+// index).  Three passes over the row, no sort.  A row where a bucket
+// holding kept keys has more than 32 keys (heavy ties, a tight cluster, a
+// far outlier) continues on the radix route:
 //   1. n <= topk: every visible key is a candidate.
 //      n > topk: a 4096-bin histogram of the top 12 key bits (the sign, the
 //      exponent and three mantissa bits) -- the scoring kernel's, or one
@@ -231,13 +242,201 @@ __device__ __forceinline__ bool run_fixup(const uint64_t *src, uint64_t *dst,
   return any;
 }
 
+// ---- bucket route ----
+// One histogram of kBucketBins fine buckets over the row's finite value
+// range [lo, hi] both finds the threshold and groups the kept keys; keys
+// inside a bucket are then ordered by counting.  The bucket of a key is a
+// non-decreasing function of the key (keys at or below the smallest finite
+// key go to the lowest bucket, keys at or above the largest to the highest,
+// the rest linearly in their float value), so every key of a higher bucket
+// comes before every key of a lower one and the count inside the bucket
+// gives the exact position.  Rows where a bucket holding kept keys has more
+// than kBucketLimit keys (ties, clusters, outliers) take the radix route.
+constexpr int kBucketBins = 4096;
+constexpr int kBucketLimit = 32;
+// (start << 16 | count) packing of the kept bins needs topk + 31 < 2^16
+constexpr int kBucketMaxTopk = 32768;
+
+struct BucketMap {
+  uint32_t kmin, kmax;  // order keys of the smallest / largest finite value
+  float lo, sc;         // lo = value of kmin, sc = bins per unit value
+  // descending bin: 0 holds the largest keys
+  __device__ __forceinline__ uint32_t desc(uint32_t k) const {
+    if (k <= kmin) return kBucketBins - 1;
+    if (k >= kmax) return 0u;
+    // cvt.rzi saturates; (v - lo) * sc is finite and >= 0 here
+    const uint32_t b = __float2uint_rz((key_to_float(k) - lo) * sc);
+    return b < kBucketBins - 1 ? (kBucketBins - 1) - b : 0u;
+  }
+};
+
+// Bank spread for the scan, where thread t reads bins [16t, 16t + 16):
+// a permutation inside each aligned group of 16 bins.
+__device__ __forceinline__ uint32_t bin_slot(uint32_t b) {
+  return b ^ ((b >> 4) & 15u);
+}
+
+// Selects and orders the row's top min(nv, topk) keys and writes the output
+// row.  Returns false (block-uniform, before writing anything) when a
+// bucket holding kept keys is too full; nothing the radix route reads has
+// been changed then except the staged keys, which it reloads.
+// stage: [stage_cap] u32 (the row's keys when nv fits); bins:
+// [kBucketBins] u32; grouped: [>= min(nv, topk) + kBucketLimit] u64.
+template <int NT>
+__device__ __forceinline__ bool bucket_topk(const float *__restrict__ L, int nv,
+                                         int topk, uint32_t *stage,
+                                         int stage_cap, uint32_t *bins,
+                                         uint64_t *grouped, SelShared &sh,
+                                         int32_t *__restrict__ oi,
+                                         float *__restrict__ os) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int per = kBucketBins / NT;
+  const bool staged = nv <= stage_cap;
+  const float neg_inf = -__int_as_float(0x7f800000);
+
+  for (int i = tid; i < kBucketBins; i += NT) bins[i] = 0u;
+  // row keys (staged when they fit) and the finite value range
+  uint32_t kmn = 0xffffffffu, kmx = 0u;
+  for (int j0 = tid; j0 < nv; j0 += 4 * NT) {
+    float v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j = j0 + u * NT;
+      v[u] = j < nv ? __ldg(L + j) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j = j0 + u * NT;
+      if (j < nv) {
+        const uint32_t k = ordered_key(v[u]);
+        if (staged) stage[j] = k;
+        if (fabsf(v[u]) <= 3.402823466e38f) {
+          kmn = min(kmn, k);
+          kmx = max(kmx, k);
+        }
+      }
+    }
+  }
+  kmn = __reduce_min_sync(0xffffffffu, kmn);
+  kmx = __reduce_max_sync(0xffffffffu, kmx);
+  if (lane == 0) {
+    sh.wand[warp] = kmn;
+    sh.wor[warp] = kmx;
+  }
+  if (tid == 0) sh.overflow = 0;
+  __syncthreads();
+  BucketMap map;
+  map.kmin = 0xffffffffu;
+  map.kmax = 0u;
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) {
+    map.kmin = min(map.kmin, sh.wand[w]);
+    map.kmax = max(map.kmax, sh.wor[w]);
+  }
+  map.lo = key_to_float(map.kmin);
+  map.sc = 0.f;
+  if (map.kmin < map.kmax) {
+    const float span = key_to_float(map.kmax) - map.lo;
+    if (span > 0.f && span <= 3.402823466e38f)
+      map.sc = fminf((float)kBucketBins / span, 1e30f);
+  }
+  auto key_of = [&](int j) -> uint32_t {
+    return staged ? stage[j] : ordered_key(__ldg(L + j));
+  };
+
+  for (int j = tid; j < nv; j += NT)
+    atomicAdd(&bins[bin_slot(map.desc(key_of(j)))], 1u);
+  __syncthreads();
+
+  // thread t owns descending bins [t*per, t*per + per)
+  uint32_t c[per];
+  uint32_t lsum = 0;
+#pragma unroll
+  for (int i = 0; i < per; ++i) {
+    c[i] = bins[bin_slot(tid * per + i)];
+    lsum += c[i];
+  }
+  const uint32_t above = block_excl_scan<NT>(lsum, sh);
+  const uint32_t want = (uint32_t)min(nv, topk);
+  if (tid == 0 && want == 0) {
+    sh.sel_digit = 0xffffffffu;  // no bin holds a kept key
+    sh.sel_count = 0;
+  }
+  if (want > 0 && above < want && want <= above + lsum) {
+    uint32_t run = above;
+#pragma unroll
+    for (int i = 0; i < per; ++i) {
+      if (run + c[i] >= want) {
+        sh.sel_digit = (uint32_t)(tid * per + i);
+        sh.sel_count = run + c[i];
+        break;
+      }
+      run += c[i];
+    }
+  }
+  __syncthreads();
+  const uint32_t thr = sh.sel_digit;  // last bin holding kept keys
+  const int m = (int)sh.sel_count;    // keys in bins 0..thr
+  // kept bins become (start << 16 | count); the scatter advances start
+  uint32_t occ = 0, run = above;
+#pragma unroll
+  for (int i = 0; i < per; ++i) {
+    const uint32_t b = (uint32_t)(tid * per + i);
+    if (thr != 0xffffffffu && b <= thr) {
+      bins[bin_slot(b)] = (run << 16) | c[i];
+      occ = max(occ, c[i]);
+    }
+    run += c[i];
+  }
+  occ = __reduce_max_sync(0xffffffffu, occ);
+  if (lane == 0 && occ > (uint32_t)kBucketLimit) sh.overflow = 1;
+  __syncthreads();
+  if (sh.overflow) {
+    __syncthreads();  // every thread has read the flag
+    return false;
+  }
+
+  for (int j = tid; j < nv; j += NT) {
+    const uint32_t k = key_of(j);
+    const uint32_t b = map.desc(k);
+    if (b <= thr) {
+      const uint32_t pos = atomicAdd(&bins[bin_slot(b)], 1u << 16) >> 16;
+      grouped[pos] = ((uint64_t)k << 32) | (uint32_t)j;
+    }
+  }
+  __syncthreads();
+
+  for (int p = tid; p < m; p += NT) {
+    const uint64_t cv = grouped[p];
+    const uint32_t k = (uint32_t)(cv >> 32), j = (uint32_t)cv;
+    const uint32_t e = bins[bin_slot(map.desc(k))];
+    const int end = (int)(e >> 16), start = end - (int)(e & 0xffffu);
+    int r = start;
+    for (int q = start; q < end; ++q) {
+      const uint64_t u = grouped[q];
+      const uint32_t uk = (uint32_t)(u >> 32);
+      r += (uk > k) || (uk == k && (uint32_t)u < j);
+    }
+    if (r < topk) {
+      const float v = key_to_float(k);
+      oi[r] = v == neg_inf ? -1 : (int32_t)j;
+      os[r] = v;
+    }
+  }
+  for (int i = m + tid; i < topk; i += NT) {
+    oi[i] = -1;
+    os[i] = neg_inf;
+  }
+  return true;
+}
+
 template <int EPT, int NT>
 __global__ void __launch_bounds__(NT, NT == kSelThreads ? 4 : 1)
     topk_select_kernel(const float *__restrict__ logits,
                        const uint32_t *__restrict__ row_hist,
                        const int32_t *__restrict__ q_pos, int S, int S_kv,
                        int ratio, int topk, int mcap, int bcap, int keys_cap,
-                       int32_t *__restrict__ out_idx,
+                       int region_u32, int32_t *__restrict__ out_idx,
                        float *__restrict__ out_scores) {
   // the logits and histograms come from the scoring kernel, which this
   // launch may overlap (programmatic dependent launch)
@@ -257,6 +456,16 @@ __global__ void __launch_bounds__(NT, NT == kSelThreads ? 4 : 1)
   const int nv = n_visible(row_pos(q_pos, b, s), ratio, S_kv);
   const float *L = logits + (size_t)row * S_kv;
   const uint32_t lt = lanemask_lt();
+  int32_t *oi = out_idx + (size_t)row * topk;
+  float *os = out_scores + (size_t)row * topk;
+
+  // the bucket route first, except for long rows whose top-12-bit histogram
+  // the scoring kernel already built (the radix route then reads each key
+  // once from global memory)
+  if (!(row_hist && nv > topk) && topk <= kBucketMaxTopk &&
+      bucket_topk<NT>(L, nv, topk, keys, region_u32,
+                      reinterpret_cast<uint32_t *>(bufB), bufA, sh, oi, os))
+    return;
 
   // the candidates, (key << 32 | j) in index order (within each of the
   // "above T" and "equal to T" groups), into bufA
@@ -548,8 +757,6 @@ __global__ void __launch_bounds__(NT, NT == kSelThreads ? 4 : 1)
     }
   }
 
-  int32_t *oi = out_idx + (size_t)row * topk;
-  float *os = out_scores + (size_t)row * topk;
   for (int i = tid; i < topk; i += NT) {
     if (i < m) {  // m >= topk or m = n_visible < topk
       const uint64_t c = cur[i];
@@ -601,6 +808,8 @@ __global__ void fill_neg_inf_kernel(float *p, size_t n) {
 // 8 KB: the sort's per-warp histograms reuse it once the keys are dead).
 struct SelLayout {
   int mcap, bcap, keys_cap;
+  int region_u32;  // u32 slots of the key region (the bucket route stages
+                   // rows that fit)
   size_t dyn;
 };
 
@@ -616,8 +825,9 @@ SelLayout sel_layout(int S_kv, int topk, bool hist, int threads) {
   const size_t key_bytes = hist ? 0 : (size_t)S_kv * 4;
   const size_t whist_bytes = (size_t)(threads / 32) * 256 * 4;
   l.keys_cap = hist ? 0 : S_kv;
-  l.dyn = (size_t)(l.mcap + l.bcap) * 8 +
-          (key_bytes > whist_bytes ? key_bytes : whist_bytes);
+  const size_t region = key_bytes > whist_bytes ? key_bytes : whist_bytes;
+  l.region_u32 = (int)(region / 4);
+  l.dyn = (size_t)(l.mcap + l.bcap) * 8 + region;
   return l;
 }
 
@@ -652,7 +862,7 @@ cudaError_t launch_sel(const Problem &p, const float *logits, int topk,
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, logits, row_hist, p.q_pos, p.S,
                             p.S_kv, p.ratio, topk, l.mcap, l.bcap, l.keys_cap,
-                            out_idx, out_scores);
+                            l.region_u32, out_idx, out_scores);
 }
 
 }  // namespace
