@@ -430,6 +430,198 @@ __device__ __forceinline__ bool bucket_topk(const float *__restrict__ L, int nv,
   return true;
 }
 
+// The same route for rows of at most R * NT keys, held in registers: thread
+// t owns keys 4(t + NT i) + c (c < 4, i < R/4), read as float4 when the row
+// is 16-byte aligned.  The bucket map here is a clamped fused multiply-add
+// whose result lands in [2^23, 2^23 + 4095], where the float's low mantissa
+// bits are the bucket; rows holding a NaN take the radix route.  A kept key
+// is stored as (key << 32 | bucket << 20 | (2^20 - 1 - j)), so inside a
+// bucket "comes before" is one unsigned 64-bit comparison.
+struct RegMap {
+  float sc, off;  // bucket + 2^23 = clamp(v * sc + off)
+  __device__ __forceinline__ uint32_t desc(uint32_t k) const {
+    // key_to_float without a branch: flip the sign bit of keys >= 2^31,
+    // every bit of the others
+    const uint32_t flip = ~(uint32_t)((int32_t)k >> 31) | 0x80000000u;
+    const float v = __uint_as_float(k ^ flip);
+    const float t = fminf(fmaxf(fmaf(v, sc, off), 8388608.0f),
+                          8388608.0f + (float)(kBucketBins - 1));
+    return ~__float_as_uint(t) & (uint32_t)(kBucketBins - 1);
+  }
+};
+
+// vec: the row is 16-byte aligned and its length a multiple of four.
+template <int NT, int R>
+__device__ __forceinline__ bool bucket_topk_reg(
+    const float *__restrict__ L, int nv, int topk, bool vec, uint32_t *bins,
+    uint64_t *grouped, SelShared &sh, int32_t *__restrict__ oi,
+    float *__restrict__ os) {
+  static_assert(R % 4 == 0, "keys are read four at a time");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int per = kBucketBins / NT;
+  const float neg_inf = -__int_as_float(0x7f800000);
+
+  {
+    // bins follow a u64 buffer of any length: 8-byte aligned only
+    uint2 *b2 = reinterpret_cast<uint2 *>(bins);
+#pragma unroll
+    for (int i = tid; i < kBucketBins / 2; i += NT) b2[i] = make_uint2(0u, 0u);
+  }
+  uint32_t kr[R];
+  uint32_t kmn = 0xffffffffu, kmx = 0u;
+  bool nan = false;
+#pragma unroll
+  for (int i = 0; i < R / 4; ++i) {
+    const int j0 = 4 * (tid + NT * i);
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    if (vec) {
+      // j0 < nv <= row length, both multiples of four: the group of four
+      // lies inside the row
+      if (j0 < nv) {
+        const float4 f = __ldg(reinterpret_cast<const float4 *>(L + j0));
+        v[0] = f.x;
+        v[1] = f.y;
+        v[2] = f.z;
+        v[3] = f.w;
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        if (j0 + c < nv) v[c] = __ldg(L + j0 + c);
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t k = ordered_key(v[c]);
+      kr[4 * i + c] = k;
+      if (j0 + c < nv) {
+        nan |= v[c] != v[c];
+        if (fabsf(v[c]) <= 3.402823466e38f) {
+          kmn = min(kmn, k);
+          kmx = max(kmx, k);
+        }
+      }
+    }
+  }
+  kmn = __reduce_min_sync(0xffffffffu, kmn);
+  kmx = __reduce_max_sync(0xffffffffu, kmx);
+  nan = __any_sync(0xffffffffu, nan);
+  if (lane == 0) {
+    sh.wand[warp] = kmn;
+    sh.wor[warp] = kmx;
+    sh.wgt[warp] = nan ? 1u : 0u;
+  }
+  if (tid == 0) sh.overflow = 0;
+  __syncthreads();
+  uint32_t kmin = 0xffffffffu, kmax = 0u, anynan = 0u;
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) {
+    kmin = min(kmin, sh.wand[w]);
+    kmax = max(kmax, sh.wor[w]);
+    anynan |= sh.wgt[w];
+  }
+  if (anynan) return false;  // block-uniform; nothing written yet
+  RegMap map;
+  map.sc = 0.f;
+  map.off = 8388608.0f;
+  if (kmin < kmax) {
+    const float lo = key_to_float(kmin);
+    const float span = key_to_float(kmax) - lo;
+    if (span > 0.f && span <= 3.402823466e38f) {
+      map.sc = fminf((float)kBucketBins / span, 1e30f);
+      // lo * sc lands within a rounding of the bins' range; the clamp
+      // absorbs the error and keeps the map monotone
+      map.off = 8388608.0f - lo * map.sc;
+    }
+  }
+
+#pragma unroll
+  for (int i = 0; i < R / 4; ++i)
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      if (4 * (tid + NT * i) + c < nv)
+        atomicAdd(&bins[bin_slot(map.desc(kr[4 * i + c]))], 1u);
+  __syncthreads();
+
+  // counts are re-read from shared memory rather than held across the
+  // scan (the row's keys already take R registers)
+  uint32_t lsum = 0;
+#pragma unroll
+  for (int i = 0; i < per; ++i) lsum += bins[bin_slot(tid * per + i)];
+  const uint32_t above = block_excl_scan<NT>(lsum, sh);
+  const uint32_t want = (uint32_t)min(nv, topk);
+  if (tid == 0 && want == 0) {
+    sh.sel_digit = 0xffffffffu;
+    sh.sel_count = 0;
+  }
+  if (want > 0 && above < want && want <= above + lsum) {
+    uint32_t run = above;
+    for (int i = 0; i < per; ++i) {
+      const uint32_t c = bins[bin_slot(tid * per + i)];
+      if (run + c >= want) {
+        sh.sel_digit = (uint32_t)(tid * per + i);
+        sh.sel_count = run + c;
+        break;
+      }
+      run += c;
+    }
+  }
+  __syncthreads();
+  const uint32_t thr = sh.sel_digit;
+  const int m = (int)sh.sel_count;
+  uint32_t occ = 0, run = above;
+#pragma unroll
+  for (int i = 0; i < per; ++i) {
+    const uint32_t b = (uint32_t)(tid * per + i);
+    const uint32_t c = bins[bin_slot(b)];
+    if (thr != 0xffffffffu && b <= thr) {
+      bins[bin_slot(b)] = (run << 16) | c;
+      occ = max(occ, c);
+    }
+    run += c;
+  }
+  occ = __reduce_max_sync(0xffffffffu, occ);
+  if (lane == 0 && occ > (uint32_t)kBucketLimit) sh.overflow = 1;
+  __syncthreads();
+  if (sh.overflow) {
+    __syncthreads();
+    return false;
+  }
+
+#pragma unroll
+  for (int i = 0; i < R / 4; ++i)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int j = 4 * (tid + NT * i) + c;
+      const uint32_t k = kr[4 * i + c];
+      const uint32_t b = map.desc(k);
+      if (j < nv && b <= thr) {
+        const uint32_t pos = atomicAdd(&bins[bin_slot(b)], 1u << 16) >> 16;
+        grouped[pos] = ((uint64_t)k << 32) |
+                       (b << 20) | (0xfffffu - (uint32_t)j);
+      }
+    }
+  __syncthreads();
+
+  for (int p = tid; p < m; p += NT) {
+    const uint64_t cv = grouped[p];
+    const uint32_t lo32 = (uint32_t)cv;
+    const uint32_t e = bins[bin_slot(lo32 >> 20)];
+    const int end = (int)(e >> 16), start = end - (int)(e & 0xffffu);
+    int r = start;
+    for (int q = start; q < end; ++q) r += grouped[q] > cv;
+    if (r < topk) {
+      const float v = key_to_float((uint32_t)(cv >> 32));
+      oi[r] = v == neg_inf ? -1 : (int32_t)(0xfffffu - (lo32 & 0xfffffu));
+      os[r] = v;
+    }
+  }
+  for (int i = m + tid; i < topk; i += NT) {
+    oi[i] = -1;
+    os[i] = neg_inf;
+  }
+  return true;
+}
+
 template <int EPT, int NT>
 __global__ void __launch_bounds__(NT, NT == kSelThreads ? 4 : 1)
     topk_select_kernel(const float *__restrict__ logits,
@@ -462,10 +654,21 @@ __global__ void __launch_bounds__(NT, NT == kSelThreads ? 4 : 1)
   // the bucket route first, except for long rows whose top-12-bit histogram
   // the scoring kernel already built (the radix route then reads each key
   // once from global memory)
-  if (!(row_hist && nv > topk) && topk <= kBucketMaxTopk &&
-      bucket_topk<NT>(L, nv, topk, keys, region_u32,
-                      reinterpret_cast<uint32_t *>(bufB), bufA, sh, oi, os))
-    return;
+  if (!(row_hist && nv > topk) && topk <= kBucketMaxTopk) {
+    constexpr int R = kBucketBins / NT;  // keys per thread in registers
+    if (nv <= R * NT) {
+      const bool vec = (S_kv & 3) == 0 &&
+                       (reinterpret_cast<uintptr_t>(L) & 15u) == 0;
+      if (bucket_topk_reg<NT, R>(L, nv, topk, vec,
+                                 reinterpret_cast<uint32_t *>(bufB), bufA, sh,
+                                 oi, os))
+        return;
+    } else if (bucket_topk<NT>(L, nv, topk, keys, region_u32,
+                               reinterpret_cast<uint32_t *>(bufB), bufA, sh,
+                               oi, os)) {
+      return;
+    }
+  }
 
   // the candidates, (key << 32 | j) in index order (within each of the
   // "above T" and "equal to T" groups), into bufA

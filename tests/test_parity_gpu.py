@@ -366,3 +366,29 @@ def test_integer_inputs_bit_exact_few_rows(dsa, topk, distinct_keys):
     ref = oracle.indexer_fwd(q, k, w, 1, topk, q_pos=pos)
     np.testing.assert_array_equal(idx.reshape(-1, topk), ref["idx"])
     np.testing.assert_array_equal(sc.reshape(-1, topk), ref["scores"])
+
+
+@pytest.mark.parametrize("S,B,outlier", [(300, 2, 2048.0), (300, 2, -2048.0),
+                                         (40, 2, 2048.0)])
+def test_far_outlier_rows_bit_exact(dsa, S, B, outlier):
+    """One key vector scaled far beyond the rest: its scores stretch each
+    row's value range so that the other keys crowd into a few of the fine
+    buckets, and those rows must leave the bucket route for the radix
+    route.  Integer q, k and dyadic w keep every score exact, so the order
+    must match the oracle exactly (many rows: 256-thread selection; 80 rows:
+    1024-thread selection)."""
+    rng = np.random.default_rng(77 + S)
+    H, D, S_kv, topk = 16, 32, 290, 60
+    qi = rng.integers(-2, 3, size=(S, B, H, D)).astype(np.float32)
+    ki = rng.integers(-2, 3, size=(S_kv, B, D)).astype(np.float32)
+    ki[3] *= outlier
+    wi = rng.choice([1, -1, 0.5, -0.5], size=(S, B, H)).astype(np.float32)
+    q = torch.from_numpy(qi).to(torch.bfloat16)
+    k = torch.from_numpy(ki).to(torch.bfloat16)
+    w = torch.from_numpy(wi)
+    pos = None if S == 300 else torch.tensor([200, 255], dtype=torch.int32)
+    sc, idx, st = gpu_run(dsa, q, k, w, 1, topk, q_pos=pos)
+    assert st == 0
+    ref = oracle.indexer_fwd(q, k, w, 1, topk, q_pos=pos)
+    np.testing.assert_array_equal(idx.reshape(-1, topk), ref["idx"])
+    np.testing.assert_array_equal(sc.reshape(-1, topk), ref["scores"])
