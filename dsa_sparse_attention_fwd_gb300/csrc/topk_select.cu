@@ -550,38 +550,31 @@ __device__ __forceinline__ bool bucket_topk_reg(
   const uint32_t above = block_excl_scan<NT>(lsum, sh);
   const uint32_t want = (uint32_t)min(nv, topk);
   if (tid == 0 && want == 0) {
-    sh.sel_digit = 0xffffffffu;
+    sh.sel_digit = 0xffffffffu;  // no bin holds a kept key
     sh.sel_count = 0;
   }
-  if (want > 0 && above < want && want <= above + lsum) {
-    uint32_t run = above;
-    for (int i = 0; i < per; ++i) {
-      const uint32_t c = bins[bin_slot(tid * per + i)];
-      if (run + c >= want) {
-        sh.sel_digit = (uint32_t)(tid * per + i);
-        sh.sel_count = run + c;
-        break;
-      }
-      run += c;
-    }
-  }
-  __syncthreads();
-  const uint32_t thr = sh.sel_digit;
-  const int m = (int)sh.sel_count;
+  // a bin holds kept keys iff fewer than `want` keys lie in the bins
+  // before it; the one where the running count reaches `want` is the last
   uint32_t occ = 0, run = above;
 #pragma unroll
   for (int i = 0; i < per; ++i) {
     const uint32_t b = (uint32_t)(tid * per + i);
     const uint32_t c = bins[bin_slot(b)];
-    if (thr != 0xffffffffu && b <= thr) {
+    if (run < want) {
       bins[bin_slot(b)] = (run << 16) | c;
       occ = max(occ, c);
+      if (run + c >= want) {
+        sh.sel_digit = b;
+        sh.sel_count = run + c;
+      }
     }
     run += c;
   }
   occ = __reduce_max_sync(0xffffffffu, occ);
   if (lane == 0 && occ > (uint32_t)kBucketLimit) sh.overflow = 1;
   __syncthreads();
+  const uint32_t thr = sh.sel_digit;  // last bin holding kept keys
+  const int m = (int)sh.sel_count;    // keys in bins 0..thr
   if (sh.overflow) {
     __syncthreads();
     return false;
