@@ -72,7 +72,7 @@ __device__ __forceinline__ int dec_item_for(int round, int n_items) {
   return idx < n_items ? idx : -1;
 }
 
-template <int H, int KC>
+template <int H, int KC, bool KV>
 __global__ void __launch_bounds__(kDecThreads, 1)
     decode_scores_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         const int j = (it.tile0 + t) * kTileKeys + sp * 32 + lane;
         if ((long long)(j + 1) * ratio - 1 <= pos && j < S_kv) {
           // a key that is not a candidate scores -inf (pool variant)
-          const bool kv_ok = kv_valid == nullptr ||
+          const bool kv_ok = !KV ||
                              __ldg(kv_valid + (size_t)j * B + it.b) != 0;
           const float sc = kv_ok ? s0 + s1 : -__int_as_float(0x7f800000);
           out[j] = sc;
@@ -305,7 +305,9 @@ cudaError_t launch_dec(const Problem &p, const CUtensorMap &tm_q,
                        const CUtensorMap &tm_k, float *logits,
                        uint32_t *row_hist, int *status, int num_sms,
                        cudaStream_t st) {
-  auto kern = decode_scores_kernel<H, KC>;
+  // only the masked instantiation reads the key-validity mask
+  auto kern = p.kv_valid ? decode_scores_kernel<H, KC, true>
+                         : decode_scores_kernel<H, KC, false>;
   const int smem = DecSmem<H, KC>::kAlloc;
   cudaError_t e = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

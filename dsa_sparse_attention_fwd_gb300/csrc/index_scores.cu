@@ -84,7 +84,7 @@ __device__ __forceinline__ int item_for(int round, int n_items) {
   return idx < n_items ? idx : -1;
 }
 
-template <int H, int KC, bool HIST>
+template <int H, int KC, bool HIST, bool KV>
 __global__ void __launch_bounds__(kScoreThreads, 1)
     index_scores_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
@@ -306,7 +306,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 
         const int j = tile * kTileKeys + sp * 32 + lane;
         // a key that is not a candidate scores -inf (pool variant)
-        const bool kv_ok = kv_valid == nullptr || j >= S_kv ||
+        // (only the masked instantiation reads the mask: the load costs the
+        // unmasked epilogue ~8% even when the pointer is null)
+        const bool kv_ok = !KV || j >= S_kv ||
                            __ldg(kv_valid + (size_t)j * B + it.b) != 0;
 #pragma unroll
         for (int qq = 0; qq < QH; ++qq) {
@@ -389,13 +391,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   }
 }
 
-template <int H, int KC, bool HIST>
+template <int H, int KC, bool HIST, bool KV>
 cudaError_t launch_h(const Problem &p, const CUtensorMap &tm_q,
                      const CUtensorMap &tm_k, float *logits,
                      uint32_t *row_hist, int *status, int num_sms,
                      cudaStream_t st) {
   constexpr int TQ = kTileCols / H;
-  auto kern = index_scores_kernel<H, KC, HIST>;
+  auto kern = index_scores_kernel<H, KC, HIST, KV>;
   const int smem = ScoreSmem<H, KC, HIST>::kAlloc;
   cudaError_t e = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -416,11 +418,17 @@ cudaError_t launch_t(const Problem &p, const CUtensorMap &tm_q,
                      cudaStream_t st) {
   if constexpr (H >= 64) {
     if (row_hist)
-      return launch_h<H, KC, true>(p, tm_q, tm_k, logits, row_hist, status,
-                                   num_sms, st);
+      return p.kv_valid
+                 ? launch_h<H, KC, true, true>(p, tm_q, tm_k, logits, row_hist,
+                                               status, num_sms, st)
+                 : launch_h<H, KC, true, false>(p, tm_q, tm_k, logits,
+                                                row_hist, status, num_sms, st);
   }
-  return launch_h<H, KC, false>(p, tm_q, tm_k, logits, nullptr, status,
-                                num_sms, st);
+  return p.kv_valid
+             ? launch_h<H, KC, false, true>(p, tm_q, tm_k, logits, nullptr,
+                                            status, num_sms, st)
+             : launch_h<H, KC, false, false>(p, tm_q, tm_k, logits, nullptr,
+                                             status, num_sms, st);
 }
 
 template <int KC>
