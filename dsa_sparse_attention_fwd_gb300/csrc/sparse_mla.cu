@@ -8,7 +8,10 @@
 //
 // A work item is one query row and 64 of its heads; a tile is 128
 // consecutive slots, its latent rows gathered into shared memory (cp.async,
-// zero fill for -1 slots).  One pass over the row's tiles:
+// zero fill for -1 slots) one block of 128 latent dims at a time, each
+// block with its own full/empty barriers: the next tile's block b is
+// gathered as soon as the output product has read block b, and the score
+// product consumes blocks as they land.  One pass over the row's tiles:
 //   S^T[slot, h] = C_g . Q^T on the tensor cores (M = 128 slots, N = 64
 //   heads, K = Dc); the epilogue takes each head's tile maximum, moves the
 //   running maximum m when a tile exceeds it by more than 2^8 (rescaling
@@ -57,9 +60,9 @@ struct MlaSmem {
   static constexpr int kOffL = kOffM + kMlaH * 4;                   // [64]
   static constexpr int kOffF = kOffL + kMlaH * 4;  // [64] factors + flag
   static constexpr int kOffBar = kOffF + (kMlaH + 4) * 4;
-  // k_full k_empty q_full q_empty r_full[8] r_empty[8] s_full[2]
+  // k_full[NB] k_empty[NB] q_full q_empty r_full[8] r_empty[8] s_full[2]
   // s_empty[2] p_full p_empty o_full o_empty
-  static constexpr int kNumBars = 4 + 2 * kMlaRing + 4 + 4;
+  static constexpr int kNumBars = 2 * NB + 2 + 2 * kMlaRing + 4 + 4;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;
@@ -154,11 +157,13 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
   float *sL = reinterpret_cast<float *>(smem + L::kOffL);
   const uint32_t bars = base + L::kOffBar;
   auto bar = [&](int i) { return bars + 8u * i; };
-  const uint32_t k_full = bar(0), k_empty = bar(1), q_full = bar(2),
-                 q_empty = bar(3);
-  auto r_full = [&](int i) { return bar(4 + i); };
-  auto r_empty = [&](int i) { return bar(4 + kMlaRing + i); };
-  constexpr int kB2 = 4 + 2 * kMlaRing;
+  // block b of the gathered tile: latent dims [128 b, 128 b + 128)
+  auto k_full = [&](int b_) { return bar(b_); };
+  auto k_empty = [&](int b_) { return bar(NB + b_); };
+  const uint32_t q_full = bar(2 * NB), q_empty = bar(2 * NB + 1);
+  auto r_full = [&](int i) { return bar(2 * NB + 2 + i); };
+  auto r_empty = [&](int i) { return bar(2 * NB + 2 + kMlaRing + i); };
+  constexpr int kB2 = 2 * NB + 2 + 2 * kMlaRing;
   auto s_full = [&](int i) { return bar(kB2 + i); };
   auto s_empty = [&](int i) { return bar(kB2 + 2 + i); };
   const uint32_t p_full = bar(kB2 + 4), p_empty = bar(kB2 + 5);
@@ -170,8 +175,10 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    mbar_init(k_full, 32 * kMlaGatWarps);  // one per gather lane
-    mbar_init(k_empty, 1);
+    for (int b_ = 0; b_ < NB; ++b_) {
+      mbar_init(k_full(b_), 32 * kMlaGatWarps);  // one per gather lane
+      mbar_init(k_empty(b_), 1);
+    }
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     for (int i = 0; i < kMlaRing; ++i) {
@@ -239,7 +246,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp <= kMlaGatWarps) {
     // ---------------- latent-row gathers ----------------
-    constexpr int kSegs = CH * 8;  // 16-byte pieces of one latent row
+    constexpr int kSegs = 16;  // 16-byte pieces of a row's 128-dim block
     constexpr int kRows = kTileKeys / kMlaGatWarps;  // rows per warp
     constexpr int kPer = kRows * kSegs / 32;         // copies per lane
     const int gw = warp - 1;
@@ -252,28 +259,44 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       if (!__all_sync(0xffffffffu,
                       wait_bar(r_full(slot), rph, abort_flag, status)))
         break;
-      if (!__all_sync(0xffffffffu, wait_bar(k_empty, (nv & 1u) ^ 1u,
-                                            abort_flag, status)))
-        break;
       const int32_t *sIdx =
           reinterpret_cast<const int32_t *>(sRing + slot * L::kRingBytes);
       const int live = topk - cur.tile * kTileKeys;
       const uint8_t *cb = cache + (size_t)cur.b * row_bytes;
       const size_t tok_stride = (size_t)B * row_bytes;
-#pragma unroll 4
+      // this lane's rows (2u + lane/16 of the warp's 16) and their tokens,
+      // the same for every block; -1 for a slot with no valid token
+      int jr[kPer];
+#pragma unroll
       for (int u = 0; u < kPer; ++u) {
-        const int flat = u * 32 + lane;
-        const int rr = gw * kRows + flat / kSegs;
-        const int seg = flat % kSegs;
-        const int c = seg >> 3, s8 = seg & 7;
+        const int rr = gw * kRows + (u * 32 + lane) / kSegs;
         const int j = rr < live ? sIdx[rr] : -1;
-        const bool valid = j >= 0 && j < T;
-        cp_async16_zfill(sC + c * (kTileKeys * 128) + rr * 128 +
-                             ((s8 ^ (rr & 7)) << 4),
-                         cb + (valid ? (size_t)j * tok_stride : 0) + seg * 16,
-                         valid ? 16u : 0u);
+        jr[u] = j >= 0 && j < T ? j : -1;
       }
-      cp_async_arrive_noinc(k_full);
+      bool stop = false;
+#pragma unroll 1
+      for (int blk = 0; blk < NB; ++blk) {
+        if (!__all_sync(0xffffffffu, wait_bar(k_empty(blk), (nv & 1u) ^ 1u,
+                                              abort_flag, status))) {
+          stop = true;
+          break;
+        }
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+          const int flat = u * 32 + lane;
+          const int rr = gw * kRows + flat / kSegs;
+          const int seg = flat % kSegs;  // 0..15 within the block
+          const int c = 2 * blk + (seg >> 3), s8 = seg & 7;
+          const int j = jr[u];
+          cp_async16_zfill(sC + c * (kTileKeys * 128) + rr * 128 +
+                               ((s8 ^ (rr & 7)) << 4),
+                           cb + (j >= 0 ? (size_t)j * tok_stride : 0) +
+                               (blk * kSegs + seg) * 16,
+                           j >= 0 ? 16u : 0u);
+        }
+        cp_async_arrive_noinc(k_full(blk));
+      }
+      if (stop) break;
       ++nv;
       mla_next(cur, g);
     }
@@ -294,19 +317,30 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       }
       const int sa = nv & 1;
       const uint32_t sph = (nv >> 1) & 1u;
-      if (!wall(s_empty(sa), sph ^ 1u) || !wall(k_full, nv & 1u)) break;
-      // the tile was written by cp.async (generic proxy)
-      fence_proxy_async_smem();
-      tc_fence_after();
-      // S^T = C_g . Q^T: CH chunks of four K = 16 steps
+      if (!wall(s_empty(sa), sph ^ 1u)) break;
+      // S^T = C_g . Q^T: CH chunks of four K = 16 steps, two chunks per
+      // gathered block, each block as soon as it lands
       const uint64_t a1 = sdesc_k_sw128(sC), b1 = sdesc_k_sw128(sQ);
       const uint32_t d1 = tmem + kTmemSm + sa * Hg;
+      bool stop = false;
 #pragma unroll 1
-      for (int t = 0; t < CH * 4; ++t) {
-        const uint32_t ao = ((t >> 2) * (kTileKeys * 128) + (t & 3) * 32) >> 4;
-        const uint32_t bo = ((t >> 2) * (Hg * 128) + (t & 3) * 32) >> 4;
-        mma_bf16_by(d1, a1 + ao, b1 + bo, kIdescS, t != 0 ? 1u : 0u, lead);
+      for (int blk = 0; blk < NB; ++blk) {
+        if (!wall(k_full(blk), nv & 1u)) {
+          stop = true;
+          break;
+        }
+        // the block was written by cp.async (generic proxy)
+        fence_proxy_async_smem();
+        tc_fence_after();
+#pragma unroll 1
+        for (int t = blk * 8; t < blk * 8 + 8; ++t) {
+          const uint32_t ao =
+              ((t >> 2) * (kTileKeys * 128) + (t & 3) * 32) >> 4;
+          const uint32_t bo = ((t >> 2) * (Hg * 128) + (t & 3) * 32) >> 4;
+          mma_bf16_by(d1, a1 + ao, b1 + bo, kIdescS, t != 0 ? 1u : 0u, lead);
+        }
       }
+      if (stop) break;
       mma_commit_by(s_full(sa), lead);
       {
         const bool first = cur.tile == 0, last = cur.tile + 1 == g.ntiles;
@@ -318,14 +352,16 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         const uint64_t a2 = sdesc_mn_sw128(sC, kTileKeys * 128, 1024);
         const uint64_t b2 = sdesc_mn_sw128(sP, 1024, 1024);
 #pragma unroll 1
-        for (int t = 0; t < NB * 8; ++t) {
-          const int blk = t >> 3, ks = t & 7;
-          mma_bf16_by(tmem + kTmemO + blk * Hg,
-                      a2 + ((blk * 2 * kTileKeys * 128 + ks * 2048) >> 4),
-                      b2 + ((ks * 2048) >> 4), kIdescO,
-                      (first && ks == 0) ? 0u : 1u, lead);
+        for (int blk = 0; blk < NB; ++blk) {
+#pragma unroll 1
+          for (int ks = 0; ks < 8; ++ks)
+            mma_bf16_by(tmem + kTmemO + blk * Hg,
+                        a2 + ((blk * 2 * kTileKeys * 128 + ks * 2048) >> 4),
+                        b2 + ((ks * 2048) >> 4), kIdescO,
+                        (first && ks == 0) ? 0u : 1u, lead);
+          // the next tile's block blk may be gathered once these are done
+          mma_commit_by(k_empty(blk), lead);
         }
-        mma_commit_by(k_empty, lead);
         mma_commit_by(p_empty, lead);
         if (last) {
           mma_commit_by(o_full, lead);
