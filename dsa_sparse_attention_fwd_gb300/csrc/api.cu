@@ -172,22 +172,9 @@ bool use_decode_path(const Problem &p, const DeviceInfo &dev) {
          (size_t)dev.max_smem_optin >= dsa::decode_smem_bytes(p.H, p.D);
 }
 
-// Scoring kernels that also count each row's top 12 key bits for the
-// selection: the decode kernel, and the prefill kernel when H >= 64.
-bool hist_shape(int S, int H, int D, int S_kv) {
-  return decode_shape(S, H, D) || dsa::index_scores_histograms(H, S_kv);
-}
-
-// Bytes of the per-row key histograms in the workspace.
-size_t row_hist_bytes(int S, int B, int H, int D, int S_kv) {
-  return hist_shape(S, H, D, S_kv)
-             ? (size_t)B * S * dsa::kRowHistBins * sizeof(uint32_t)
-             : 0;
-}
-
 // Device checks + tensor maps + the scoring launch.
-int run_scores(const Problem &p, float *logits, uint32_t *row_hist,
-               int *status, const DeviceInfo &dev, cudaStream_t st) {
+int run_scores(const Problem &p, float *logits, int *status,
+               const DeviceInfo &dev, cudaStream_t st) {
   const bool decode = use_decode_path(p, dev);
   if (!decode &&
       (size_t)dev.max_smem_optin < dsa::index_scores_smem_bytes(p.H, p.D))
@@ -198,10 +185,10 @@ int run_scores(const Problem &p, float *logits, uint32_t *row_hist,
   rc = encode_k(&tm_k, p);
   if (rc != DSA_OK) return rc;
   const cudaError_t e =
-      decode ? dsa::launch_decode_scores(p, tm_q, tm_k, logits, row_hist,
-                                         status, dev.num_sms, st)
-             : dsa::launch_index_scores(p, tm_q, tm_k, logits, row_hist,
-                                        status, dev.num_sms, st);
+      decode ? dsa::launch_decode_scores(p, tm_q, tm_k, logits, status,
+                                         dev.num_sms, st)
+             : dsa::launch_index_scores(p, tm_q, tm_k, logits, status,
+                                        dev.num_sms, st);
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
@@ -231,8 +218,7 @@ size_t dsa_indexer_workspace_size(int S, int B, int H, int D, int S_kv,
     return gather_direct_shape(B, H, D, S_kv)
                ? kHeaderBytes
                : kHeaderBytes + logits_bytes(S, B, S_kv);
-  return kHeaderBytes + logits_bytes(S, B, S_kv) +
-         row_hist_bytes(S, B, H, D, S_kv);
+  return kHeaderBytes + logits_bytes(S, B, S_kv);
 }
 
 size_t dsa_indexer_logits_workspace_size(void) { return kHeaderBytes; }
@@ -257,8 +243,7 @@ namespace dsa {
 
 // The forward behind every entry point.  clear_status = false keeps the
 // workspace's status word (several forwards sharing one workspace then
-// accumulate their device errors); the decode histograms are cleared either
-// way.
+// accumulate their device errors).
 int forward_core(const void *q, const void *k, const float *w, int S, int B,
                  int H, int D, int S_kv, int compress_ratio, int topk,
                  const int32_t *q_pos, const int32_t *in_idx, int32_t *out_idx,
@@ -301,29 +286,10 @@ int forward_core(const void *q, const void *k, const float *w, int S, int B,
                : cudaSuccess;
   };
 
-  // Workspace: status header, then the per-row key histograms when the
-  // scoring kernel counts them (filled by it, read by the selection), then
-  // the logits.  The decode kernel counts with global atomics, so its
-  // histograms start at zero: one memset clears them with the header.
-  uint32_t *row_hist = nullptr;
-  size_t clear_bytes = kHeaderBytes;
-  const bool decode = use_decode_path(p, dev);
-  if (!in_idx && ((decode && hist_shape(S, H, D, S_kv)) ||
-                  (!decode && dsa::index_scores_histograms(H, S_kv)))) {
-    row_hist = reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) +
-                                            kHeaderBytes);
-    logits = reinterpret_cast<float *>(reinterpret_cast<char *>(row_hist) +
-                                       row_hist_bytes(S, B, H, D, S_kv));
-    if (decode) clear_bytes += row_hist_bytes(S, B, H, D, S_kv);
-  }
-  if (clear_status) {
-    if (cudaMemsetAsync(status, 0, clear_bytes, st) != cudaSuccess)
-      return DSA_ERR_CUDA;
-  } else if (clear_bytes > kHeaderBytes &&
-             cudaMemsetAsync(row_hist, 0, clear_bytes - kHeaderBytes, st) !=
-                 cudaSuccess) {
+  // Workspace: status header, then the logits.
+  if (clear_status &&
+      cudaMemsetAsync(status, 0, kHeaderBytes, st) != cudaSuccess)
     return DSA_ERR_CUDA;
-  }
   if (in_idx && gather_direct_shape(B, H, D, S_kv)) {
     // one kernel: gathered keys -> scores at the given slots
     if ((size_t)dev.max_smem_optin < dsa::gather_smem_bytes(H, D))
@@ -340,7 +306,7 @@ int forward_core(const void *q, const void *k, const float *w, int S, int B,
     return DSA_OK;
   }
   if (mark(0) != cudaSuccess) return DSA_ERR_CUDA;
-  rc = run_scores(p, logits, row_hist, status, dev, st);
+  rc = run_scores(p, logits, status, dev, st);
   if (rc != DSA_OK) return rc;
   if (mark(1) != cudaSuccess) return DSA_ERR_CUDA;
   cudaError_t e;
@@ -348,8 +314,8 @@ int forward_core(const void *q, const void *k, const float *w, int S, int B,
     e = dsa::launch_gather_logits(p, logits, in_idx, topk, out_idx, out_scores,
                                   status, dev.num_sms, st);
   else
-    e = dsa::launch_topk_select(p, logits, topk, row_hist, out_idx,
-                                out_scores, dev.num_sms, st);
+    e = dsa::launch_topk_select(p, logits, topk, out_idx, out_scores,
+                                dev.num_sms, st);
   if (e != cudaSuccess) return DSA_ERR_CUDA;
   if (mark(2) != cudaSuccess) return DSA_ERR_CUDA;
   return DSA_OK;
@@ -390,7 +356,7 @@ int dsa_indexer_logits(const void *q, const void *k, const float *w, int S,
   if (dsa::launch_fill_masked(logits, logits_bytes(S, B, S_kv) / 4, st) !=
       cudaSuccess)
     return DSA_ERR_CUDA;
-  return run_scores(p, logits, nullptr, status, dev, st);
+  return run_scores(p, logits, status, dev, st);
 }
 
 int dsa_indexer_check(void *workspace, void *cuda_stream) {

@@ -65,11 +65,6 @@ __device__ __forceinline__ float key_to_float(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// Per-row histogram of the top 12 key bits, built by the decode scoring
-// kernel and read by the selection (bins per row).
-constexpr int kRowHistBins = 4096;
-constexpr int kRowHistShift = 20;
-
 // Scoring kernel tile geometry.
 constexpr int kTileKeys = 128;      // MMA M: compressed keys per tile
 constexpr int kTileCols = 256;      // MMA N: (query, head) columns per tile
@@ -84,21 +79,14 @@ constexpr int kDecChunkTiles = 4;   // decode: key tiles per work item
 
 // Launchers (return cudaSuccess or the launch error).  `logits` is
 // [B, S, S_kv] fp32; only visible entries are written.
-// row_hist (nullable): per-row top-12-bit key histograms, written for every
-// scored row (pass it only when index_scores_histograms(H, S_kv)).
 cudaError_t launch_index_scores(const Problem &p, const CUtensorMap &tm_q,
                                 const CUtensorMap &tm_k, float *logits,
-                                uint32_t *row_hist, int *status, int num_sms,
-                                cudaStream_t st);
+                                int *status, int num_sms, cudaStream_t st);
 size_t index_scores_smem_bytes(int H, int D);
-bool index_scores_histograms(int H, int S_kv);
 
-// row_hist: per-row top-12-bit key histograms from the decode scoring
-// kernel, or nullptr (the selection then builds its own).
 cudaError_t launch_topk_select(const Problem &p, const float *logits, int topk,
-                               const uint32_t *row_hist, int32_t *out_idx,
-                               float *out_scores, int num_sms,
-                               cudaStream_t st);
+                               int32_t *out_idx, float *out_scores,
+                               int num_sms, cudaStream_t st);
 size_t topk_select_smem_bytes(int S_kv, int topk);
 
 // Given indices, scores read from written logits (any H).
@@ -121,8 +109,7 @@ size_t gather_smem_bytes(int H, int D);
 // cudaErrorNotSupported when (H, D) has no decode instantiation.
 cudaError_t launch_decode_scores(const Problem &p, const CUtensorMap &tm_q,
                                  const CUtensorMap &tm_k, float *logits,
-                                 uint32_t *row_hist, int *status, int num_sms,
-                                 cudaStream_t st);
+                                 int *status, int num_sms, cudaStream_t st);
 bool decode_supported(int H, int D);
 size_t decode_smem_bytes(int H, int D);
 

@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                          const int32_t *__restrict__ q_pos,
                          const uint8_t *__restrict__ kv_valid,
                          float *__restrict__ logits,
-                         uint32_t *__restrict__ row_hist, int S, int B,
+                         int S, int B,
                          int S_kv, int ratio, int n_items, int *status) {
   using L = DecSmem<H, KC>;
   constexpr uint32_t kIdesc = idesc_bf16_f32(kTileKeys, H);
@@ -279,10 +279,6 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                              __ldg(kv_valid + (size_t)j * B + it.b) != 0;
           const float sc = kv_ok ? s0 + s1 : -__int_as_float(0x7f800000);
           out[j] = sc;
-          if (row_hist)
-            atomicAdd(row_hist + (size_t)it.row * kRowHistBins +
-                          (ordered_key(sc) >> kRowHistShift),
-                      1u);
         }
         acc ^= 1u;
         if (acc == 0) aph ^= 1u;
@@ -303,8 +299,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 template <int H, int KC>
 cudaError_t launch_dec(const Problem &p, const CUtensorMap &tm_q,
                        const CUtensorMap &tm_k, float *logits,
-                       uint32_t *row_hist, int *status, int num_sms,
-                       cudaStream_t st) {
+                       int *status, int num_sms, cudaStream_t st) {
   // only the masked instantiation reads the key-validity mask
   auto kern = p.kv_valid ? decode_scores_kernel<H, KC, true>
                          : decode_scores_kernel<H, KC, false>;
@@ -320,7 +315,7 @@ cudaError_t launch_dec(const Problem &p, const CUtensorMap &tm_q,
   if (n_items > 0x7fffffffLL) return cudaErrorInvalidValue;
   const int grid = (int)(n_items < num_sms ? n_items : num_sms);
   kern<<<grid, kDecThreads, smem, st>>>(tm_q, tm_k, p.w, p.q_pos,
-                                        p.kv_valid, logits, row_hist, p.S,
+                                        p.kv_valid, logits, p.S,
                                         p.B, p.S_kv, p.ratio, (int)n_items,
                                         status);
   return cudaGetLastError();
@@ -341,19 +336,18 @@ size_t decode_smem_bytes(int H, int D) {
 
 cudaError_t launch_decode_scores(const Problem &p, const CUtensorMap &tm_q,
                                  const CUtensorMap &tm_k, float *logits,
-                                 uint32_t *row_hist, int *status, int num_sms,
-                                 cudaStream_t st) {
+                                 int *status, int num_sms, cudaStream_t st) {
   const bool k1 = p.D <= kChunk;
   switch (p.H) {
     case 32:
-      return k1 ? launch_dec<32, 1>(p, tm_q, tm_k, logits, row_hist, status, num_sms, st)
-                : launch_dec<32, 2>(p, tm_q, tm_k, logits, row_hist, status, num_sms, st);
+      return k1 ? launch_dec<32, 1>(p, tm_q, tm_k, logits, status, num_sms, st)
+                : launch_dec<32, 2>(p, tm_q, tm_k, logits, status, num_sms, st);
     case 64:
-      return k1 ? launch_dec<64, 1>(p, tm_q, tm_k, logits, row_hist, status, num_sms, st)
-                : launch_dec<64, 2>(p, tm_q, tm_k, logits, row_hist, status, num_sms, st);
+      return k1 ? launch_dec<64, 1>(p, tm_q, tm_k, logits, status, num_sms, st)
+                : launch_dec<64, 2>(p, tm_q, tm_k, logits, status, num_sms, st);
     case 128:
-      return k1 ? launch_dec<128, 1>(p, tm_q, tm_k, logits, row_hist, status, num_sms, st)
-                : launch_dec<128, 2>(p, tm_q, tm_k, logits, row_hist, status, num_sms, st);
+      return k1 ? launch_dec<128, 1>(p, tm_q, tm_k, logits, status, num_sms, st)
+                : launch_dec<128, 2>(p, tm_q, tm_k, logits, status, num_sms, st);
     default:
       return cudaErrorNotSupported;
   }

@@ -28,23 +28,17 @@
 namespace dsa {
 namespace {
 
-template <int H, int KC, bool HIST>
+template <int H, int KC>
 struct ScoreSmem {
   static constexpr int kTQ = kTileCols / H;              // queries per item
-  // Per-query top-12-bit key histograms (u32 bins) for the selection, kept
-  // in shared memory while an item is scored; only instantiated when an item
-  // has few queries (H >= 64), making room with a single Q buffer.
-  static constexpr bool kHist = HIST && H >= 64;
-  static constexpr int kHistBytes = kHist ? kTQ * kRowHistBins * 4 : 0;
-  static constexpr int kQSlots = kHist ? 1 : 2;
+  static constexpr int kQSlots = 2;
   static constexpr int kStages = KC == 1 ? 4 : 3;        // K ring depth
   static constexpr int kQBytes = KC * kTileCols * 128;  // one Q tile
   static constexpr int kKBytes = KC * kTileKeys * 128;  // one K stage
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kQSlots * kQBytes;
   static constexpr int kOffW = kOffK + kStages * kKBytes;
-  static constexpr int kOffHist = kOffW + kTileCols * 4;
-  static constexpr int kOffBar = kOffHist + kHistBytes;
+  static constexpr int kOffBar = kOffW + kTileCols * 4;
   // barriers: k_full[S], k_empty[S], q_full[2], q_empty[2], acc_full[2],
   // acc_empty[2]
   static constexpr int kNumBars = 2 * kStages + 4 + 4;
@@ -84,19 +78,17 @@ __device__ __forceinline__ int item_for(int round, int n_items) {
   return idx < n_items ? idx : -1;
 }
 
-template <int H, int KC, bool HIST, bool KV>
+template <int H, int KC, bool KV>
 __global__ void __launch_bounds__(kScoreThreads, 1)
     index_scores_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
                         const float *__restrict__ w,
                         const int32_t *__restrict__ q_pos,
                         const uint8_t *__restrict__ kv_valid,
-                        float *__restrict__ logits,
-                        uint32_t *__restrict__ row_hist, int S, int B,
+                        float *__restrict__ logits, int S, int B,
                         int S_kv, int ratio, int *status) {
-  using L = ScoreSmem<H, KC, HIST>;
+  using L = ScoreSmem<H, KC>;
   constexpr int NQ = L::kQSlots;
-  const bool do_hist = L::kHist && row_hist != nullptr;
   constexpr int kStages = L::kStages;
   constexpr int TQ = kTileCols / H;  // queries per work item
   constexpr int QH = TQ / 2;         // queries per epilogue column half
@@ -110,7 +102,6 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   const uint32_t sQ = base + L::kOffQ;
   const uint32_t sK = base + L::kOffK;
   float *sW = reinterpret_cast<float *>(smem + L::kOffW);
-  uint32_t *sHist = reinterpret_cast<uint32_t *>(smem + L::kOffHist);
   const uint32_t bars = base + L::kOffBar;
   auto k_full = [&](int s) { return bars + 8u * s; };
   auto k_empty = [&](int s) { return bars + 8u * (kStages + s); };
@@ -141,9 +132,6 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
   }
-  if (do_hist)
-    for (int i = threadIdx.x; i < L::kHistBytes / 4; i += kScoreThreads)
-      sHist[i] = 0u;
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_holder), 512);
     tmem_relinquish();
@@ -357,26 +345,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           if (t < S && vis && j < S_kv) {
             const float sv = kv_ok ? score : -__int_as_float(0x7f800000);
             logits[((size_t)it.b * S + t) * S_kv + j] = sv;
-            if (do_hist)
-              atomicAdd(&sHist[tq * kRowHistBins +
-                               (ordered_key(sv) >> kRowHistShift)],
-                        1u);
           }
         }
         acc ^= 1u;
         if (acc == 0) aph ^= 1u;
-      }
-      if (do_hist) {
-        // the item's rows are complete: write their histograms out and clear
-        // them (the next item starts after the barrier at its top)
-        named_bar_sync(2, 256);
-        for (int i = et; i < L::kTQ * kRowHistBins; i += 256) {
-          const int t = it.t0 + (i / kRowHistBins);
-          if (t < S)
-            row_hist[((size_t)it.b * S + t) * kRowHistBins +
-                     (i % kRowHistBins)] = sHist[i];
-          sHist[i] = 0u;
-        }
       }
       it = nx;
       r = r_next;
@@ -391,14 +363,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   }
 }
 
-template <int H, int KC, bool HIST, bool KV>
+template <int H, int KC, bool KV>
 cudaError_t launch_h(const Problem &p, const CUtensorMap &tm_q,
-                     const CUtensorMap &tm_k, float *logits,
-                     uint32_t *row_hist, int *status, int num_sms,
-                     cudaStream_t st) {
+                     const CUtensorMap &tm_k, float *logits, int *status,
+                     int num_sms, cudaStream_t st) {
   constexpr int TQ = kTileCols / H;
-  auto kern = index_scores_kernel<H, KC, HIST, KV>;
-  const int smem = ScoreSmem<H, KC, HIST>::kAlloc;
+  auto kern = index_scores_kernel<H, KC, KV>;
+  const int smem = ScoreSmem<H, KC>::kAlloc;
   cudaError_t e = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -406,49 +377,38 @@ cudaError_t launch_h(const Problem &p, const CUtensorMap &tm_q,
   const int grid = (int)(n_items < num_sms ? n_items : num_sms);
   if (grid <= 0) return cudaSuccess;
   kern<<<grid, kScoreThreads, smem, st>>>(tm_q, tm_k, p.w, p.q_pos,
-                                          p.kv_valid, logits, row_hist, p.S,
-                                          p.B, p.S_kv, p.ratio, status);
+                                          p.kv_valid, logits, p.S, p.B,
+                                          p.S_kv, p.ratio, status);
   return cudaGetLastError();
 }
 
 template <int H, int KC>
 cudaError_t launch_t(const Problem &p, const CUtensorMap &tm_q,
-                     const CUtensorMap &tm_k, float *logits,
-                     uint32_t *row_hist, int *status, int num_sms,
-                     cudaStream_t st) {
-  if constexpr (H >= 64) {
-    if (row_hist)
-      return p.kv_valid
-                 ? launch_h<H, KC, true, true>(p, tm_q, tm_k, logits, row_hist,
-                                               status, num_sms, st)
-                 : launch_h<H, KC, true, false>(p, tm_q, tm_k, logits,
-                                                row_hist, status, num_sms, st);
-  }
-  return p.kv_valid
-             ? launch_h<H, KC, false, true>(p, tm_q, tm_k, logits, nullptr,
-                                            status, num_sms, st)
-             : launch_h<H, KC, false, false>(p, tm_q, tm_k, logits, nullptr,
-                                             status, num_sms, st);
+                     const CUtensorMap &tm_k, float *logits, int *status,
+                     int num_sms, cudaStream_t st) {
+  return p.kv_valid ? launch_h<H, KC, true>(p, tm_q, tm_k, logits, status,
+                                            num_sms, st)
+                    : launch_h<H, KC, false>(p, tm_q, tm_k, logits, status,
+                                             num_sms, st);
 }
 
 template <int KC>
 cudaError_t launch_kc(const Problem &p, const CUtensorMap &tm_q,
-                      const CUtensorMap &tm_k, float *logits,
-                      uint32_t *row_hist, int *status, int num_sms,
-                      cudaStream_t st) {
+                      const CUtensorMap &tm_k, float *logits, int *status,
+                      int num_sms, cudaStream_t st) {
   switch (p.H) {
-    case 1: return launch_t<1, KC>(p, tm_q, tm_k, logits, row_hist, status, num_sms, st);
-    case 2: return launch_t<2, KC>(p, tm_q, tm_k, logits, row_hist, status, num_sms, st);
-    case 4: return launch_t<4, KC>(p, tm_q, tm_k, logits, row_hist, status, num_sms, st);
-    case 8: return launch_t<8, KC>(p, tm_q, tm_k, logits, row_hist, status, num_sms, st);
+    case 1: return launch_t<1, KC>(p, tm_q, tm_k, logits, status, num_sms, st);
+    case 2: return launch_t<2, KC>(p, tm_q, tm_k, logits, status, num_sms, st);
+    case 4: return launch_t<4, KC>(p, tm_q, tm_k, logits, status, num_sms, st);
+    case 8: return launch_t<8, KC>(p, tm_q, tm_k, logits, status, num_sms, st);
     case 16:
-      return launch_t<16, KC>(p, tm_q, tm_k, logits, row_hist, status, num_sms, st);
+      return launch_t<16, KC>(p, tm_q, tm_k, logits, status, num_sms, st);
     case 32:
-      return launch_t<32, KC>(p, tm_q, tm_k, logits, row_hist, status, num_sms, st);
+      return launch_t<32, KC>(p, tm_q, tm_k, logits, status, num_sms, st);
     case 64:
-      return launch_t<64, KC>(p, tm_q, tm_k, logits, row_hist, status, num_sms, st);
+      return launch_t<64, KC>(p, tm_q, tm_k, logits, status, num_sms, st);
     case 128:
-      return launch_t<128, KC>(p, tm_q, tm_k, logits, row_hist, status, num_sms, st);
+      return launch_t<128, KC>(p, tm_q, tm_k, logits, status, num_sms, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -459,28 +419,19 @@ size_t index_scores_smem_bytes(int H, int D) {
   size_t m = 0;
 #define DSA_SMEM_CASE(HH)                                           \
   if (H == HH)                                                      \
-    m = D <= kChunk ? ScoreSmem<HH, 1, HH >= 64>::kAlloc            \
-                    : ScoreSmem<HH, 2, HH >= 64>::kAlloc;
+    m = D <= kChunk ? ScoreSmem<HH, 1>::kAlloc : ScoreSmem<HH, 2>::kAlloc;
   DSA_SMEM_CASE(1) DSA_SMEM_CASE(2) DSA_SMEM_CASE(4) DSA_SMEM_CASE(8)
   DSA_SMEM_CASE(16) DSA_SMEM_CASE(32) DSA_SMEM_CASE(64) DSA_SMEM_CASE(128)
 #undef DSA_SMEM_CASE
   return m;
 }
 
-// Histograms pay off when the selection would otherwise stage long rows
-// (S_kv >= 8192 keys) in shared memory; for shorter rows the extra work in
-// the scoring epilogue costs more than the selection saves.
-bool index_scores_histograms(int H, int S_kv) {
-  return H >= 64 && S_kv >= 8192;
-}
-
 cudaError_t launch_index_scores(const Problem &p, const CUtensorMap &tm_q,
                                 const CUtensorMap &tm_k, float *logits,
-                                uint32_t *row_hist, int *status, int num_sms,
-                                cudaStream_t st) {
+                                int *status, int num_sms, cudaStream_t st) {
   if (p.D <= kChunk)
-    return launch_kc<1>(p, tm_q, tm_k, logits, row_hist, status, num_sms, st);
-  return launch_kc<2>(p, tm_q, tm_k, logits, row_hist, status, num_sms, st);
+    return launch_kc<1>(p, tm_q, tm_k, logits, status, num_sms, st);
+  return launch_kc<2>(p, tm_q, tm_k, logits, status, num_sms, st);
 }
 
 }  // namespace dsa

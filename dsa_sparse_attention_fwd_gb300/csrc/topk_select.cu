@@ -7,8 +7,8 @@
 // keys (larger float <-> larger key; -0.0 folded onto +0.0 so the index
 // tie-break decides between them).
 //
-// Bucket route (every row except long rows whose histogram the scoring
-// kernel built): the row, staged in shared memory when it fits, is counted
+// Bucket route (every row first): the row -- in registers up to 4096 keys,
+// else staged in shared memory when it fits, else read from L2 -- is counted
 // into 4096 fine buckets spread linearly over its finite value range.  A
 // scan of the counts gives the bucket holding the topk-th key and each
 // kept bucket's start; the kept keys are scattered to their buckets and
@@ -19,9 +19,8 @@
 // far outlier) continues on the radix route:
 //   1. n <= topk: every visible key is a candidate.
 //      n > topk: a 4096-bin histogram of the top 12 key bits (the sign, the
-//      exponent and three mantissa bits) -- the scoring kernel's, or one
-//      built here from the row staged in shared memory -- gives the bucket
-//      holding the topk-th largest key.  If the keys in and above that
+//      exponent and three mantissa bits) gives the bucket holding the
+//      topk-th largest key.  If the keys in and above that
 //      bucket fit topk plus a slack, one pass keeps them all (in any
 //      order); otherwise two more passes (12 and 8 bits) find the exact
 //      threshold T and an ordered compaction keeps every key > T and the
@@ -618,13 +617,12 @@ __device__ __forceinline__ bool bucket_topk_reg(
 template <int EPT, int NT>
 __global__ void __launch_bounds__(NT, NT == kSelThreads ? 4 : 1)
     topk_select_kernel(const float *__restrict__ logits,
-                       const uint32_t *__restrict__ row_hist,
                        const int32_t *__restrict__ q_pos, int S, int S_kv,
                        int ratio, int topk, int mcap, int bcap, int keys_cap,
                        int region_u32, int32_t *__restrict__ out_idx,
                        float *__restrict__ out_scores) {
-  // the logits and histograms come from the scoring kernel, which this
-  // launch may overlap (programmatic dependent launch)
+  // the logits come from the scoring kernel, which this launch may overlap
+  // (programmatic dependent launch)
   pdl_wait();
   extern __shared__ __align__(16) uint8_t smem[];
   uint64_t *bufA = reinterpret_cast<uint64_t *>(smem);  // [mcap]
@@ -644,10 +642,8 @@ __global__ void __launch_bounds__(NT, NT == kSelThreads ? 4 : 1)
   int32_t *oi = out_idx + (size_t)row * topk;
   float *os = out_scores + (size_t)row * topk;
 
-  // the bucket route first, except for long rows whose top-12-bit histogram
-  // the scoring kernel already built (the radix route then reads each key
-  // once from global memory)
-  if (!(row_hist && nv > topk) && topk <= kBucketMaxTopk) {
+  // the bucket route first; the radix route takes the rows it declines
+  if (topk <= kBucketMaxTopk) {
     constexpr int R = kBucketBins / NT;  // keys per thread in registers
     if (nv <= R * NT) {
       const bool vec = (S_kv & 3) == 0 &&
@@ -667,9 +663,8 @@ __global__ void __launch_bounds__(NT, NT == kSelThreads ? 4 : 1)
   // "above T" and "equal to T" groups), into bufA
   uint32_t T = 0;
   int need = 0, n_gt = 0;
-  bool unordered = false;  // candidates not in index order (fix-up needed)
-  // without a row-key buffer (the histogram route) keys come straight from
-  // the logits; only the rare fallbacks read them that way
+  // without a row-key buffer (long rows, many of them) keys come straight
+  // from the logits in L2
   const bool staged = keys_cap >= nv;
   auto key_at = [&](int j) -> uint32_t {
     return staged ? keys[j] : ordered_key(__ldg(L + j));
@@ -754,73 +749,6 @@ __global__ void __launch_bounds__(NT, NT == kSelThreads ? 4 : 1)
   if (nv <= topk) {
     load_all();
     done = true;
-  } else if (row_hist) {
-    // the scoring kernel already counted this row's top 12 key bits: find
-    // the threshold bucket there and compact straight from the logits
-    const uint32_t *gh = row_hist + (size_t)row * kRowHistBins;
-    constexpr int per = kRowHistBins / NT;
-    const int o = NT - 1 - tid;
-    uint32_t c[per];
-    uint32_t lsum = 0;
-#pragma unroll
-    for (int i = 0; i < per; ++i) {
-      c[i] = __ldg(gh + o * per + i);
-      lsum += c[i];
-    }
-    const uint32_t above = block_excl_scan<NT>(lsum, sh);
-    if (above < (uint32_t)topk && (uint32_t)topk <= above + lsum) {
-      uint32_t run = above;
-      for (int i = per - 1; i >= 0; --i) {
-        if (run + c[i] >= (uint32_t)topk) {
-          sh.sel_digit = (uint32_t)(o * per + i);
-          sh.sel_above = run;
-          sh.sel_count = c[i];
-          break;
-        }
-        run += c[i];
-      }
-    }
-    __syncthreads();
-    const uint32_t dsel = sh.sel_digit, dabove = sh.sel_above;
-    const uint32_t dcount = sh.sel_count;
-    __syncthreads();
-    if (dabove + dcount <= (uint32_t)mcap) {
-      // one pass over the row: keep keys whose top 12 bits reach the
-      // threshold bucket, appended in any order (the fix-up below orders
-      // equal keys by index explicitly)
-      T = dsel << kRowHistShift;
-      need = 0;
-      n_gt = (int)(dabove + dcount);
-      m = n_gt;
-      if (tid == 0) sh.cursor = 0;
-      __syncthreads();
-      for (int c0 = 0; c0 < nv; c0 += 4 * NT) {
-        float v[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int j = c0 + u * NT + tid;
-          v[u] = j < nv ? __ldg(L + j) : 0.f;
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int j = c0 + u * NT + tid;
-          const uint32_t key = ordered_key(v[u]);
-          const bool keep = j < nv && key >= T;
-          const uint32_t bal = __ballot_sync(0xffffffffu, keep);
-          uint32_t base = 0;
-          if (lane == 0 && bal) base = atomicAdd(&sh.cursor, __popc(bal));
-          base = __shfl_sync(0xffffffffu, base, 0);
-          const uint32_t pos = base + __popc(bal & lt);
-          if (keep && pos < (uint32_t)mcap)
-            bufA[pos] = ((uint64_t)key << 32) | (uint32_t)j;
-        }
-      }
-      __syncthreads();
-      // equals the histogram's count; the bound only guards the buffer
-      m = min((int)sh.cursor, mcap);
-      unordered = true;
-      done = true;
-    }
   }
   if (!done) {
     load_keys();
@@ -928,7 +856,7 @@ __global__ void __launch_bounds__(NT, NT == kSelThreads ? 4 : 1)
     cur = alt;
     alt = t;
   }
-  if ((diff & 0xFFu) != 0u || unordered) {
+  if ((diff & 0xFFu) != 0u) {
     if (!run_fixup<NT>(cur, alt, m, sh)) {
       uint64_t *t = cur;
       cur = alt;
@@ -1009,36 +937,36 @@ struct SelLayout {
   size_t dyn;
 };
 
-SelLayout sel_layout(int S_kv, int topk, bool hist, int threads) {
+SelLayout sel_layout(int S_kv, int topk, bool unstaged, int threads) {
   SelLayout l;
   // room for the candidates of a one-pass select: topk plus the rest of
   // the threshold bucket (up to kSelSlack keys, twice that for small topk)
   const int slack = topk < 1024 ? 2 * kSelSlack : kSelSlack;
   l.mcap = topk + slack < S_kv ? topk + slack : S_kv;
   l.bcap = l.mcap > kHistBins / 2 ? l.mcap : kHistBins / 2;
-  // with precomputed row histograms the row is never staged in shared
-  // memory; the region then only holds the sort's per-warp counters
-  const size_t key_bytes = hist ? 0 : (size_t)S_kv * 4;
+  // unstaged rows are never copied to shared memory whole (their keys are
+  // read from L2); the region then holds the sort's per-warp counters, or
+  // a row short enough to fit
+  const size_t key_bytes = unstaged ? 0 : (size_t)S_kv * 4;
   const size_t whist_bytes = (size_t)(threads / 32) * 256 * 4;
-  l.keys_cap = hist ? 0 : S_kv;
+  l.keys_cap = unstaged ? 0 : S_kv;
   const size_t region = key_bytes > whist_bytes ? key_bytes : whist_bytes;
   l.region_u32 = (int)(region / 4);
   l.dyn = (size_t)(l.mcap + l.bcap) * 8 + region;
   return l;
 }
 
-// Rows skip the shared-memory copy of their keys when histograms are
-// precomputed and there are enough rows that more CTAs per SM pay off; a
-// few rows (decode) keep it, so their rare fallbacks stay fast.
-bool unstaged_rows(const Problem &p, const uint32_t *row_hist) {
-  return row_hist != nullptr && (long long)p.B * p.S >= 2048;
+// Rows longer than 4096 keys (past the register route) skip the
+// shared-memory copy when there are enough rows that more CTAs per SM pay
+// off; a few rows (decode) keep it, so their passes stay in shared memory.
+bool unstaged_rows(const Problem &p) {
+  return p.S_kv > 4096 && (long long)p.B * p.S >= 2048;
 }
 
 template <int EPT, int NT>
 cudaError_t launch_sel(const Problem &p, const float *logits, int topk,
-                       const uint32_t *row_hist, int32_t *out_idx,
-                       float *out_scores, cudaStream_t st) {
-  const SelLayout l = sel_layout(p.S_kv, topk, unstaged_rows(p, row_hist), NT);
+                       int32_t *out_idx, float *out_scores, cudaStream_t st) {
+  const SelLayout l = sel_layout(p.S_kv, topk, unstaged_rows(p), NT);
   auto kern = topk_select_kernel<EPT, NT>;
   cudaError_t e = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)l.dyn);
@@ -1056,7 +984,7 @@ cudaError_t launch_sel(const Problem &p, const float *logits, int topk,
   attr.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, logits, row_hist, p.q_pos, p.S,
+  return cudaLaunchKernelEx(&cfg, kern, logits, p.q_pos, p.S,
                             p.S_kv, p.ratio, topk, l.mcap, l.bcap, l.keys_cap,
                             l.region_u32, out_idx, out_scores);
 }
@@ -1072,26 +1000,25 @@ size_t topk_select_smem_bytes(int S_kv, int topk) {
 constexpr size_t kWideSmemCap = 160 * 1024;
 
 cudaError_t launch_topk_select(const Problem &p, const float *logits, int topk,
-                               const uint32_t *row_hist, int32_t *out_idx,
-                               float *out_scores, int num_sms,
-                               cudaStream_t st) {
-  const bool unstaged = unstaged_rows(p, row_hist);
+                               int32_t *out_idx, float *out_scores,
+                               int num_sms, cudaStream_t st) {
+  const bool unstaged = unstaged_rows(p);
   const int mcap = sel_layout(p.S_kv, topk, unstaged, kSelThreads).mcap;
   // Fewer rows than SMs: each row gets 1024 threads, so a row's passes
   // take a quarter of the iterations (the rows run side by side anyway).
   const long long rows = (long long)p.B * p.S;
   if (rows < num_sms && mcap <= kSelThreadsWide * 4 &&
       sel_layout(p.S_kv, topk, unstaged, kSelThreadsWide).dyn <= kWideSmemCap)
-    return launch_sel<4, kSelThreadsWide>(p, logits, topk, row_hist, out_idx,
+    return launch_sel<4, kSelThreadsWide>(p, logits, topk, out_idx,
                                           out_scores, st);
   if (mcap <= kSelThreads * 8)
-    return launch_sel<8, kSelThreads>(p, logits, topk, row_hist, out_idx,
+    return launch_sel<8, kSelThreads>(p, logits, topk, out_idx,
                                       out_scores, st);
   if (mcap <= kSelThreads * 16)
-    return launch_sel<16, kSelThreads>(p, logits, topk, row_hist, out_idx,
+    return launch_sel<16, kSelThreads>(p, logits, topk, out_idx,
                                        out_scores, st);
   return launch_sel<DSA_SEL_MAX_EPT + 2, kSelThreads>(
-      p, logits, topk, row_hist, out_idx, out_scores, st);
+      p, logits, topk, out_idx, out_scores, st);
 }
 
 cudaError_t launch_gather_logits(const Problem &p, const float *logits,

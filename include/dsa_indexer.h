@@ -79,10 +79,8 @@ typedef enum dsa_status {
  * Bytes of device workspace dsa_indexer_fwd() needs for this shape
  * (has_in_idx != 0 selects the given-indices path).  Returns 0 when the
  * shape is invalid.  The workspace starts with a 256-byte status header.
- * Top-k path: the header is followed, when H >= 64 with S_kv >= 8192 or
- * when a sequence has fewer than 256/H queries (the decode kernel), by one
- * 4096-bin u32 key histogram per query row (16 KiB per row), then by the
- * fp32 logits [B, S, S_kv] of the visible keys.
+ * Top-k path: the header is followed by the fp32 logits [B, S, S_kv] of the
+ * visible keys.
  * Given-indices path: H in {16, 32, 64, 128} scores the gathered keys
  * directly and needs the header only; other H take the header plus the
  * logits.
@@ -268,8 +266,7 @@ DSA_API int dsa_selftest_wait_limit(int limit_us, void *workspace,
  *
  *   - Limit: problems whose dsa_indexer_workspace_size() exceeds
  *     DSA_STATIC_SCRATCH_BYTES (64 MiB plus a 256-byte header: e.g. the
- *     4096 x 4096 prefill's 64 MiB of logits, B*S*S_kv <= 16,777,216 when no
- *     row histograms apply) are refused with DSA_ERR_UNSUPPORTED before any device work.  Other
+ *     4096 x 4096 prefill's 64 MiB of logits, B*S*S_kv <= 16,777,216) are refused with DSA_ERR_UNSUPPORTED before any device work.  Other
  *     argument errors are those of dsa_indexer_fwd().
  *   - Memory: every GPU that loads this part of the library holds one copy
  *     of the array until the process exits.  No call allocates or frees

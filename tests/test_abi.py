@@ -114,15 +114,13 @@ def test_status_strings(lib):
 
 def test_workspace_size(lib):
     ws = lib.dsa_indexer_workspace_size
-    hist = 4096 * 4  # per-row key histogram (decode shapes, long H >= 64)
+    # top-k path: the status header, then the fp32 logits of every row
     assert ws(4096, 1, 64, 128, 4096, 1, 2048, 0) == 256 + 4096 * 4096 * 4
     assert ws(16384, 2, 64, 128, 4096, 4, 512, 0) == 256 + 2 * 16384 * 4096 * 4
-    assert ws(8192, 1, 64, 128, 8192, 1, 2048, 0) == (256 + 8192 * 8192 * 4
-                                                      + 8192 * hist)
+    assert ws(8192, 1, 64, 128, 8192, 1, 2048, 0) == 256 + 8192 * 8192 * 4
     assert ws(8192, 1, 32, 128, 8192, 1, 2048, 0) == 256 + 8192 * 8192 * 4
-    assert ws(64, 1, 16, 64, 64, 1, 8, 0) == 256 + 64 * 64 * 4  # no histograms
-    assert ws(1, 64, 32, 64, 8192, 4, 512, 0) == (256 + 64 * 8192 * 4
-                                                  + 64 * hist)  # decode
+    assert ws(64, 1, 16, 64, 64, 1, 8, 0) == 256 + 64 * 64 * 4
+    assert ws(1, 64, 32, 64, 8192, 4, 512, 0) == 256 + 64 * 8192 * 4  # decode
     # given indices: H in {16, 32, 64, 128} gathers keys (status header
     # only); other H read the scores back from logits
     assert ws(65536, 1, 64, 128, 16384, 4, 2048, 1) == 256

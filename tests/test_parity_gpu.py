@@ -319,11 +319,12 @@ def test_decode_path_match_oracle(dsa, S, B, H, D, S_kv, ratio, topk):
     (42, 2, 9000, 4, 512),    # ragged query tail and key tail
     (9, 1, 8192, 1, 2048),    # exactly 64 key tiles, large topk
 ])
-def test_long_rows_histogram_path(dsa, S, B, S_kv, ratio, topk):
-    """Prefill shapes with H >= 64 and S_kv >= 8192 score with the kernel that
-    also counts each row's key histogram for the selection.  Query positions
-    deep into the sequence give every row thousands of visible keys while
-    keeping the rows few enough for the oracle."""
+def test_long_rows(dsa, S, B, S_kv, ratio, topk):
+    """Rows of more than 4096 visible keys: the selection's bucket route
+    with the row staged in shared memory (few rows) rather than held in
+    registers.  Query positions deep into the sequence give every row
+    thousands of visible keys while keeping the rows few enough for the
+    oracle."""
     H, D = 64, 128
     wl = Workload("t", B=B, S=S, S_kv=S_kv, H=H, D=D, compress_ratio=ratio,
                   topk=topk, w_scale=H ** -0.5, seed=S_kv + S)

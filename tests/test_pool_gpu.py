@@ -167,8 +167,9 @@ def test_pooled_forward_decode_rows(dsa):
                  invalid=0.01, q_pos=pos)
 
 
-def test_pooled_forward_long_rows_with_histograms(dsa):
-    """8192 pools per row (the scoring kernel's row-histogram route)."""
+def test_pooled_forward_long_rows(dsa):
+    """8192 pools per row: rows past the register-held selection (keys
+    read from L2), with some pools masked invalid."""
     S, B, T, kpool = 64, 1, 32800, 4
     pos = torch.tensor([T - S], dtype=torch.int32)
     check_pooled(dsa, S, B, 64, 128, T, kpool, 0, 2048, seed=41,
