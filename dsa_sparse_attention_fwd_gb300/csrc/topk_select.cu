@@ -534,11 +534,18 @@ __device__ __forceinline__ bool bucket_topk_reg(
   }
 
 #pragma unroll
+  // each key's bucket, two to a register, for the scatter below
+  uint32_t bk[R / 2];
+#pragma unroll
+  for (int i = 0; i < R / 2; ++i) bk[i] = 0u;
+#pragma unroll
   for (int i = 0; i < R / 4; ++i)
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
-      if (4 * (tid + NT * i) + c < nv)
-        atomicAdd(&bins[bin_slot(map.desc(kr[4 * i + c]))], 1u);
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t b = map.desc(kr[4 * i + c]);
+      bk[2 * i + (c >> 1)] |= b << (16 * (c & 1));
+      if (4 * (tid + NT * i) + c < nv) atomicAdd(&bins[bin_slot(b)], 1u);
+    }
   __syncthreads();
 
   // counts are re-read from shared memory rather than held across the
@@ -585,7 +592,7 @@ __device__ __forceinline__ bool bucket_topk_reg(
     for (int c = 0; c < 4; ++c) {
       const int j = 4 * (tid + NT * i) + c;
       const uint32_t k = kr[4 * i + c];
-      const uint32_t b = map.desc(k);
+      const uint32_t b = (bk[2 * i + (c >> 1)] >> (16 * (c & 1))) & 0xffffu;
       if (j < nv && b <= thr) {
         const uint32_t pos = atomicAdd(&bins[bin_slot(b)], 1u << 16) >> 16;
         grouped[pos] = ((uint64_t)k << 32) |
