@@ -466,11 +466,18 @@ __device__ __forceinline__ bool bucket_topk_reg(
 #pragma unroll
     for (int i = tid; i < kBucketBins / 2; i += NT) b2[i] = make_uint2(0u, 0u);
   }
+  // the loops over a thread's key groups skip, block-uniformly, the groups
+  // past the row's end (a short row runs a fraction of the unrolled code)
   uint32_t kr[R];
   uint32_t kmn = 0xffffffffu, kmx = 0u;
   bool nan = false;
 #pragma unroll
   for (int i = 0; i < R / 4; ++i) {
+    if (4 * NT * i >= nv) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) kr[4 * i + c] = 0u;
+      continue;
+    }
     const int j0 = 4 * (tid + NT * i);
     float v[4] = {0.f, 0.f, 0.f, 0.f};
     if (vec) {
@@ -539,13 +546,15 @@ __device__ __forceinline__ bool bucket_topk_reg(
 #pragma unroll
   for (int i = 0; i < R / 2; ++i) bk[i] = 0u;
 #pragma unroll
-  for (int i = 0; i < R / 4; ++i)
+  for (int i = 0; i < R / 4; ++i) {
+    if (4 * NT * i >= nv) continue;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const uint32_t b = map.desc(kr[4 * i + c]);
       bk[2 * i + (c >> 1)] |= b << (16 * (c & 1));
       if (4 * (tid + NT * i) + c < nv) atomicAdd(&bins[bin_slot(b)], 1u);
     }
+  }
   __syncthreads();
 
   // counts are re-read from shared memory rather than held across the
@@ -587,7 +596,8 @@ __device__ __forceinline__ bool bucket_topk_reg(
   }
 
 #pragma unroll
-  for (int i = 0; i < R / 4; ++i)
+  for (int i = 0; i < R / 4; ++i) {
+    if (4 * NT * i >= nv) continue;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const int j = 4 * (tid + NT * i) + c;
@@ -599,6 +609,7 @@ __device__ __forceinline__ bool bucket_topk_reg(
                        (b << 20) | (0xfffffu - (uint32_t)j);
       }
     }
+  }
   __syncthreads();
 
   for (int p = tid; p < m; p += NT) {
