@@ -25,7 +25,8 @@
 //
 // Warp roles (one CTA per SM, persistent): warp 0 fetch (index ring, query
 // tile), warps 1..8 gathers, warp 9 TMEM allocator and MMA issuer, warps
-// 10..13 epilogue.
+// 10..17 epilogue (warp w reads TMEM lanes 32 (w % 4) .. + 31 and heads
+// 32 ((w - 10) / 4) .. + 31).
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -37,7 +38,8 @@ namespace {
 
 constexpr int kMlaH = 64;  // heads per item
 constexpr int kMlaGatWarps = 8;
-constexpr int kMlaThreads = 32 * (kMlaGatWarps + 6);
+constexpr int kMlaEpiWarps = 8;  // two per TMEM lane quarter, 32 heads each
+constexpr int kMlaThreads = 32 * (kMlaGatWarps + 2 + kMlaEpiWarps);
 constexpr int kMlaMmaWarp = kMlaGatWarps + 1;
 constexpr int kMlaEpiWarp0 = kMlaGatWarps + 2;
 constexpr int kMlaRing = 8;  // index ring (tile visits)
@@ -111,13 +113,14 @@ __device__ __forceinline__ int mla_next(MlaCursor &c, const MlaGeom &g) {
   return 2;
 }
 
-// Sum (MAX = false) or maximum (MAX = true) of 64 per-lane values over the
+// Sum (MAX = false) or maximum (MAX = true) of N per-lane values over the
 // warp's 32 lanes: halve the set five times, each lane keeping the half its
-// lane bit selects; lane l ends with heads 2l and 2l + 1 in v[0], v[1].
-template <bool MAX>
-__device__ __forceinline__ void warp_fold64(float (&v)[64], int lane) {
+// lane bit selects; lane l ends with values N/32 l .. N/32 l + N/32 - 1 in
+// v[0 .. N/32).
+template <int N, bool MAX>
+__device__ __forceinline__ void warp_fold(float (&v)[N], int lane) {
 #pragma unroll
-  for (int o = 16, m = 64; o >= 1; o >>= 1, m >>= 1) {
+  for (int o = 16, m = N; o >= 1; o >>= 1, m >>= 1) {
     const bool up = (lane & o) != 0;
 #pragma unroll
     for (int h = 0; h < m / 2; ++h) {
@@ -183,16 +186,16 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     mbar_init(q_empty, 1);
     for (int i = 0; i < kMlaRing; ++i) {
       mbar_init(r_full(i), 32);
-      mbar_init(r_empty(i), 4);
+      mbar_init(r_empty(i), kMlaEpiWarps);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(s_full(i), 1);
-      mbar_init(s_empty(i), 4);
+      mbar_init(s_empty(i), kMlaEpiWarps);
     }
-    mbar_init(p_full, 4);
+    mbar_init(p_full, kMlaEpiWarps);
     mbar_init(p_empty, 1);
     mbar_init(o_full, 1);
-    mbar_init(o_empty, 4);
+    mbar_init(o_empty, kMlaEpiWarps);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
@@ -374,10 +377,13 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       step = mla_next(cur, g);
     }
   } else {
-    // ---------------- epilogue (warps kMlaEpiWarp0 .. + 3) ----------------
-    const int sp = warp & 3;
-    const int et = threadIdx.x - 32 * kMlaEpiWarp0;  // 0..127
+    // ---------------- epilogue (warps kMlaEpiWarp0 .. + 7) ----------------
+    constexpr int kEpiThreads = 32 * kMlaEpiWarps;
+    const int sp = warp & 3;                         // TMEM lane quarter
+    const int hh = (warp - kMlaEpiWarp0) >> 2;       // head half
+    const int et = threadIdx.x - 32 * kMlaEpiWarp0;  // 0..255
     const int i = sp * 32 + lane;  // TMEM lane: the slot, or the latent dim
+    const int hl = hh * 32 + lane;  // the head this lane folds to
     const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
     float *sF = reinterpret_cast<float *>(smem + L::kOffF);  // [64] factors
     // the running maximum moves only when a tile exceeds it by more than
@@ -386,25 +392,23 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     MlaCursor cur = mla_begin(g);
     uint32_t nv = 0, nitem = 0;
     bool ok = true;
-    auto load_s = [&](uint32_t taddr, float (&v)[64]) {
+    // this thread's 32 heads of its TMEM lane
+    auto load32 = [&](uint32_t taddr, float (&v)[32]) {
+      uint32_t u[32];
+      __syncwarp();
+      tmem_ld32(taddr, u);
+      tmem_ld_wait();
+      reg_fence32(u);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t u[32];
-        __syncwarp();
-        tmem_ld32(taddr + c * 32, u);
-        tmem_ld_wait();
-        reg_fence32(u);
-#pragma unroll
-        for (int q = 0; q < 32; ++q) v[c * 32 + q] = __uint_as_float(u[q]);
-      }
+      for (int q = 0; q < 32; ++q) v[q] = __uint_as_float(u[q]);
     };
 
     while (cur.valid) {
-      if (named_bar_or(1, 128, !ok)) break;
+      if (named_bar_or(1, kEpiThreads, !ok)) break;
       const int b = cur.b, s = cur.s, hg = cur.hg;
       if (et < 64) sM[et] = neg_inf;  // running maximum (log2 domain)
-      named_bar_sync(3, 128);
-      float l0 = 0.f, l1 = 0.f;  // l of heads 2*lane, 2*lane + 1 (partial)
+      named_bar_sync(3, kEpiThreads);
+      float lp = 0.f;  // l of head hl (this warp's slots)
       bool bad = false;
       int step = 0;
       while (ok && step == 0) {
@@ -419,7 +423,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t sS = tmem + lane_off + kTmemSm + sa * Hg;
+        const uint32_t sS = tmem + lane_off + kTmemSm + sa * Hg + hh * 32;
         const int e = cur.tile * kTileKeys + i;
         const bool in_row = e < topk;
         const int j =
@@ -431,15 +435,14 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         const bool valid = j >= 0 && j < T;
         bad |= in_row && (j < -1 || j >= T);
         // each head's largest scaled score in the tile
-        float v[64];
-        load_s(sS, v);
+        float v[32];
+        load32(sS, v);
 #pragma unroll
-        for (int h = 0; h < 64; ++h)
+        for (int h = 0; h < 32; ++h)
           v[h] = valid ? v[h] * scale_log2e : neg_inf;
-        warp_fold64<true>(v, lane);
-        sRed[sp * 64 + 2 * lane] = v[0];
-        sRed[sp * 64 + 2 * lane + 1] = v[1];
-        named_bar_sync(3, 128);
+        warp_fold<32, true>(v, lane);
+        sRed[sp * 64 + hl] = v[0];
+        named_bar_sync(3, kEpiThreads);
         bool moved = false;
         if (et < 64) {
           const float tmax = fmaxf(fmaxf(sRed[et], sRed[64 + et]),
@@ -454,7 +457,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
           sF[et] = f;
         }
         // every thread sees the new maxima and factors, and whether any moved
-        const bool rescale = named_bar_or(3, 128, moved);
+        const bool rescale = named_bar_or(3, kEpiThreads, moved);
         // the accumulator is idle once MMA2 of the previous tile is done
         if (!__all_sync(0xffffffffu, wait_bar(p_empty, (nv & 1u) ^ 1u,
                                               abort_flag, status))) {
@@ -463,42 +466,39 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         }
         tc_fence_after();
         if (rescale) {
-          l0 *= sF[2 * lane];
-          l1 *= sF[2 * lane + 1];
+          lp *= sF[hl];
           if (cur.tile > 0) {
-            // O^T[d, h] *= f[h]: this warp's 32 latent dims of every block
+            // O^T[d, h] *= f[h]: this warp's 32 latent dims and 32 heads of
+            // every block
 #pragma unroll 1
             for (int blk = 0; blk < NB; ++blk) {
-#pragma unroll 1
-              for (int c = 0; c < 2; ++c) {
-                const uint32_t ta = tmem + lane_off + kTmemO + blk * Hg + c * 32;
-                uint32_t u[32];
-                __syncwarp();
-                tmem_ld32(ta, u);
-                tmem_ld_wait();
-                reg_fence32(u);
+              const uint32_t ta = tmem + lane_off + kTmemO + blk * Hg + hh * 32;
+              uint32_t u[32];
+              __syncwarp();
+              tmem_ld32(ta, u);
+              tmem_ld_wait();
+              reg_fence32(u);
 #pragma unroll
-                for (int q = 0; q < 32; ++q)
-                  u[q] = __float_as_uint(__uint_as_float(u[q]) * sF[c * 32 + q]);
-                tmem_st32(ta, u);
-              }
+              for (int q = 0; q < 32; ++q)
+                u[q] = __float_as_uint(__uint_as_float(u[q]) * sF[hh * 32 + q]);
+              tmem_st32(ta, u);
             }
             tmem_st_wait();
           }
         }
         // P^T = exp2(x - m) for the tensor core (the fold consumed v)
-        load_s(sS, v);
+        load32(sS, v);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(s_empty(sa));
-        const float4 *m4 = reinterpret_cast<const float4 *>(sM);
+        const float4 *m4 = reinterpret_cast<const float4 *>(sM + hh * 32);
         const uint32_t prow = sP + i * 128;
 #pragma unroll
-        for (int u8 = 0; u8 < 8; ++u8) {
+        for (int k8 = 0; k8 < 4; ++k8) {
           uint32_t pk[4];
 #pragma unroll
           for (int hq = 0; hq < 2; ++hq) {
-            const int h = u8 * 8 + hq * 4;
+            const int h = k8 * 8 + hq * 4;
             const float4 mv = m4[h >> 2];
             const float p0 = valid ? exp2f(fmaf(v[h], scale_log2e, -mv.x)) : 0.f;
             const float p1 =
@@ -514,25 +514,25 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
             pk[2 * hq] = pack_bf16x2(p0, p1);
             pk[2 * hq + 1] = pack_bf16x2(p2, p3);
           }
+          // 16-byte chunk u8 of the 128-byte P^T row holds heads 8 u8 .. + 7
+          const int u8 = hh * 4 + k8;
           st_shared_v4(prow + ((u8 ^ (i & 7)) << 4), pk);
         }
         // the tensor core (async proxy) reads P^T and the rescaled O^T next
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(p_full);
-        warp_fold64<false>(v, lane);
-        l0 += v[0];
-        l1 += v[1];
+        warp_fold<32, false>(v, lane);
+        lp += v[0];
         ++nv;
         step = mla_next(cur, g);
       }
-      if (named_bar_or(2, 128, !ok)) break;
-      sRed[sp * 64 + 2 * lane] = l0;
-      sRed[sp * 64 + 2 * lane + 1] = l1;
-      named_bar_sync(3, 128);
+      if (named_bar_or(2, kEpiThreads, !ok)) break;
+      sRed[sp * 64 + hl] = lp;
+      named_bar_sync(3, kEpiThreads);
       if (et < 64)
         sL[et] = ((sRed[et] + sRed[64 + et]) + sRed[128 + et]) + sRed[192 + et];
-      named_bar_sync(3, 128);
+      named_bar_sync(3, kEpiThreads);
       // ---- o = O^T / l, lse = (m + log2 l) ln 2 ----
       ok = __all_sync(0xffffffffu,
                       wait_bar(o_full, nitem & 1u, abort_flag, status));
@@ -541,21 +541,18 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         float *orow = out_o + (((size_t)s * B + b) * H + hg * Hg) * Dc;
 #pragma unroll 1
         for (int blk = 0; blk < NB; ++blk) {
-#pragma unroll 1
-          for (int c = 0; c < 2; ++c) {
-            uint32_t u[32];
-            __syncwarp();
-            tmem_ld32(tmem + lane_off + kTmemO + blk * Hg + c * 32, u);
-            tmem_ld_wait();
-            reg_fence32(u);
-            // lane = latent dim: each store covers 32 consecutive dims
+          uint32_t u[32];
+          __syncwarp();
+          tmem_ld32(tmem + lane_off + kTmemO + blk * Hg + hh * 32, u);
+          tmem_ld_wait();
+          reg_fence32(u);
+          // lane = latent dim: each store covers 32 consecutive dims
 #pragma unroll
-            for (int hh = 0; hh < 32; ++hh) {
-              const int h = c * 32 + hh;
-              const float l = sL[h];
-              orow[(size_t)h * Dc + blk * 128 + i] =
-                  l > 0.f ? __uint_as_float(u[hh]) / l : 0.f;
-            }
+          for (int q = 0; q < 32; ++q) {
+            const int h = hh * 32 + q;
+            const float l = sL[h];
+            orow[(size_t)h * Dc + blk * 128 + i] =
+                l > 0.f ? __uint_as_float(u[q]) / l : 0.f;
           }
         }
         tc_fence_before();
