@@ -1050,8 +1050,8 @@ def run_mla(args):
                      "unit": "TFLOP/s", "frac": achieved / tc_peak,
                      "peak_source": f"{peak_src} bf16 burst",
                      "algorithmic": f"{flops:.4g} FLOP per launch (4*H*Dc "
-                                    "per valid slot; the max pass's "
-                                    "recomputed scores not counted)",
+                                    "per valid slot: the score and the "
+                                    "output products)",
                      "traffic": read_traffic("sparse_mla")},
         "e2e": {"value": world * flops / (t_e2e * 1e-3) / 1e12,
                 "unit": "TFLOP/s", "ms_per_step": t_e2e,
