@@ -102,7 +102,12 @@ DSA_API size_t dsa_indexer_workspace_size(int S, int B, int H, int D,
  *
  * in_idx == NULL: per row, the min(topk, n_visible) visible keys with the
  * largest score, sorted by descending score, equal scores by ascending key
- * index; remaining slots hold -1 and -inf.
+ * index; remaining slots hold -1 and -inf.  Scores compare as IEEE values
+ * with -0.0 equal to +0.0 (the score written is +0.0).  With non-finite
+ * inputs a score may be +-inf or NaN: a NaN orders by its bits (positive
+ * NaN above +inf, negative NaN below -inf), and any kept slot whose score
+ * is -inf holds index -1.  Only finite inputs are covered by the parity
+ * tests.
  * in_idx != NULL: out_idx is a copy of in_idx; out_scores holds the score at
  * each given index, or -inf where the index is -1, not visible, or outside
  * [0, S_kv) (the latter also sets DSA_ERR_INDEX_RANGE in the status word).
