@@ -2,11 +2,13 @@
 """Benchmark of the DSA lightning-indexer forward on GB300.
 
 One step = the whole forward (scoring + top-k selection) over one batch of
-synthetic input of the V3.2-style prefill workload (B=1, S=4096, S_kv=4096,
-H=64, D=128, topk=2048, causal, ratio 1), inputs resident in HBM.  Metric:
+synthetic input of the long-context C4 prefill workload (B=1, S=65536,
+compress_ratio=4 so S_kv=16384, H=64, D=128, topk=2048, causal), the
+largest configuration that fits one GPU, inputs resident in HBM.  Metric:
 TFLOP/s over visible (query, key) pairs, 2*H*D FLOPs per pair, plus
 queries/s.  L2 is flushed (a 256 MiB write, outside the timed events)
-before every timed step.
+before every timed step.  `--workload v32_prefill | c4_prefill | decode |
+tiny` times the other configurations.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload NAME] [--given-indices]
@@ -40,7 +42,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = ("indexer fwd TFLOP/s (visible pairs) + queries/s; "
           "% of bf16 TC peak / HBM BW")
-WORKLOAD = "v32_prefill"
+WORKLOAD = "long_c4"
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -184,6 +186,19 @@ def max_over_ranks(value: float, world: int, device) -> float:
     t = torch.tensor([value], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+# the oracle's pace on the host (fp64 multiply-adds per second over all
+# cores), used only to size the timed row sample to about 15 s of work
+ORACLE_MAC_PER_S = 1.5e10
+CPU_SAMPLE_S = 15.0
+
+
+def cpu_sample_stride(wl, pairs: int) -> int:
+    """Row stride that gives the oracle about CPU_SAMPLE_S seconds of work
+    (1 = every row)."""
+    macs = float(pairs) * wl.H * wl.D
+    return max(1, int(math.ceil(macs / (ORACLE_MAC_PER_S * CPU_SAMPLE_S))))
 
 
 def cpu_oracle_sample(wl, rows_every: int, in_idx=None):
@@ -491,7 +506,8 @@ def run_ours(args):
     }
     if world == 1 and not args.no_cpu_baseline:
         if gi is None:
-            line["cpu_baseline"] = cpu_oracle_sample(wl, 1)
+            line["cpu_baseline"] = cpu_oracle_sample(
+                wl, cpu_sample_stride(wl, pairs))
         else:
             every = max(1, wl.B * wl.S // 1024)
             line["cpu_baseline"] = cpu_oracle_sample(wl, every, in_idx=gi)

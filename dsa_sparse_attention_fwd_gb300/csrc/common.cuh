@@ -30,7 +30,7 @@ __device__ __forceinline__ long long row_pos(const int32_t *q_pos, int b,
   return q_pos ? (long long)__ldg(q_pos + b) + s : (long long)s;
 }
 
-// Causal rule over compressed keys (DeepSeek-V4 indexer, "causal masking";
+// Causal rule over compressed keys (DeepSeek-V4 indexer, causal masking;
 // a compressed key stands for source tokens [j*r, (j+1)*r) and is visible
 // only when the whole block is at or before the query): (j+1)*r - 1 <= pos.
 // Returns how many keys (a prefix 0..n-1) are visible.

@@ -3,19 +3,19 @@
 // topk_pools -> expand_selection -> token ids, -1 = invalid).
 //
 //   kpool_compress: pool p of sequence b covers tokens first_key + p*kpool
-//     + s (s < kpool); only whole pools count ("a trailing partial pool is
-//     not a pool"), and a pool is a candidate only if all its tokens are
+//     + s (s < kpool); only whole pools count (an incomplete pool at the
+//     end is dropped), and a pool is a candidate only if all its tokens are
 //     valid.  Per channel c, with slot logits z_s = gate[token_s, b, c] +
 //     ape[s, c], the pooled key is sum_s softmax_s(z)_s * k[token_s, b, c]
-//     ("the pool softmax runs over the pool-slot axis, per channel"),
+//     (the softmax runs across a pool's slots, separately per channel),
 //     computed in fp32 and stored as bf16 (the indexer's key format).
 //   index_scores + topk_pools: the lightning-indexer forward over the pools
 //     with compress_ratio = kpool at positions shifted by first_key (pool p
 //     is visible once its last token is), invalid pools masked out.
 //   expand_selection: each row's index_topk / kpool pool ids become
-//     index_topk token ids, -1 for the slots of an empty pool slot ("writes
-//     -1 over the whole index row before it stores any index, so every slot
-//     is written").
+//     index_topk token ids, -1 for the slots of an empty pool slot (the
+//     whole output row is filled with -1 first, so no slot is left
+//     unwritten).
 //
 // kpool <= 8: the page's compression kernel holds at most 8 slots
 // (KERNEL_MAX_KPOOL) and its configuration refuses more.

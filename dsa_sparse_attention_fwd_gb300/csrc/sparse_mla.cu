@@ -1,6 +1,7 @@
 // sparse_mla: attention over the tokens the indexer selected, in the MLA
 // latent space with no rotary part (page "Module glm5next_dsa", "Shape of
-// the pipeline": "-> NoPE MLA restricted to those tokens"; the latent width
+// the pipeline": the selected tokens feed an MLA attention without the
+// rotary part, over those tokens only; the latent width
 // is kv_lora_rank, section "Constants").  The latent row of a selected
 // token is both key and value:
 //     x_i = scale * q[t, h, :] . c[j_i, :]       (j_i = idx[t, i], valid)

@@ -10,10 +10,11 @@
 // The array is a file-scope __device__ variable: each GPU on which this
 // library's module is loaded holds its own copy until the process exits.
 // Host code cannot use the array's name as a device address (on the host
-// the name is only a stand-in), so the device address is looked up once per
-// device with cudaGetSymbolAddress while that device is current.
-#include <mutex>
-
+// the name is only a stand-in), so the device address is looked up with
+// cudaGetSymbolAddress on every call, with the caller's device current.  The
+// lookup allocates nothing and is cheap; not caching it keeps the address
+// right after a device reset or a reload of the module, where the array may
+// move.
 #include "dsa_indexer.h"
 
 namespace {
@@ -21,23 +22,12 @@ namespace {
 static __device__ __align__(256) unsigned char
     g_static_scratch[DSA_STATIC_SCRATCH_BYTES];
 
-std::mutex g_scratch_mu;
-void *g_scratch_ptr[64] = {};
-
-// Device address of this device's copy of the scratch array (looked up on
-// the first call per device, with that device current).
+// Device address of the current device's copy of the scratch array.
 int static_scratch_address(void **out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return DSA_ERR_CUDA;
-  if (dev < 0 || dev >= 64) return DSA_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p)
-      return DSA_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p)
+    return DSA_ERR_CUDA;
+  *out = p;
   return DSA_OK;
 }
 

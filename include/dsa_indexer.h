@@ -7,12 +7,12 @@
  *   - `V4IndexerFunction` / `v4_lighting_indexer(index_q, index_k, weights,
  *     compress_ratio, topk, topk_indices=None)`: inputs in SBHD layout,
  *     q [seqlen, batch, heads, dim] bf16, k [seqlen_kv, batch, dim] bf16,
- *     weights [seqlen, batch, heads] fp32, `compress_ratio` ("4 for C4
- *     layers"), `topk`, optional pre-computed `topk_indices [batch, seqlen,
+ *     weights [seqlen, batch, heads] fp32, `compress_ratio` (4 on C4
+ *     layers), `topk`, optional pre-computed `topk_indices [batch, seqlen,
  *     topk] int32`; result `[batch, seqlen, topk] fp32` ("Returns").
  *   - `pytorch_extract_topk_scores(logits, topk_indices, dim=-1)`: the
  *     given-indices path gathers the scores at caller-supplied indices.
- *   - "causal masking" (module summary).
+ *   - causal masking (module summary).
  * and the index conventions of the metrale.ai page "Module glm5next_dsa"
  * ("-1 = invalid", section "Shape of the pipeline"; the whole index row is
  * written, -1 first, section "Checkpoint and kernel facts"; kernels refuse
@@ -271,14 +271,17 @@ DSA_API int dsa_selftest_wait_limit(int limit_us, void *workspace,
  *
  *   - Limit: problems whose dsa_indexer_workspace_size() exceeds
  *     DSA_STATIC_SCRATCH_BYTES (64 MiB plus a 256-byte header: e.g. the
- *     4096 x 4096 prefill's 64 MiB of logits, B*S*S_kv <= 16,777,216) are refused with DSA_ERR_UNSUPPORTED before any device work.  Other
+ *     4096 x 4096 prefill's 64 MiB of logits, B*S*S_kv <= 16,777,216) are
+ *     refused with DSA_ERR_UNSUPPORTED before any device work.  Other
  *     argument errors are those of dsa_indexer_fwd().
  *   - Memory: every GPU that loads this part of the library holds one copy
  *     of the array until the process exits.  No call allocates or frees
  *     device memory.
- *   - Set-up: the first call on each device looks up that device's copy of
- *     the array (cudaGetSymbolAddress, with the device current); make that
- *     first call before any stream capture.
+ *   - Set-up: every call looks up the current device's copy of the array
+ *     (cudaGetSymbolAddress, which allocates nothing), so a device reset or
+ *     module reload between calls is harmless.  The first call on a device
+ *     may also load the library's kernels onto it; make that first call
+ *     before any stream capture.
  *   - Sharing: all calls on a device share the one array, which keeps the
  *     last call's contents.  Calls that overlap on the GPU (different
  *     streams, or threads without ordering) race on it; order them on one
@@ -344,8 +347,8 @@ DSA_API int dsa_indexer_bwd(const void *q, const void *k, const float *w,
  * slots are valid, expand_selection writes every slot of the row).
  *
  * Pool p of sequence b covers tokens first_key + p*kpool + s (s < kpool);
- * P = (T - first_key) / kpool whole pools (a trailing partial pool is not a
- * pool).  Pooled key, per channel c, with z_s = gate[token_s, b, c] +
+ * P = (T - first_key) / kpool whole pools (an incomplete pool at the end is
+ * dropped).  Pooled key, per channel c, with z_s = gate[token_s, b, c] +
  * ape[s, c]:  key[p, b, c] = sum_s softmax_s(z)_s * k[token_s, b, c]
  * (fp32, stored bf16).  A pool is a candidate iff every token's valid flag
  * is nonzero (valid NULL: all valid).  Query row s of sequence b at position
@@ -402,7 +405,8 @@ DSA_API int dsa_indexer_fwd_pooled(
 
 /*
  * Sparse MLA forward over selected tokens (page "Module glm5next_dsa",
- * "Shape of the pipeline": "-> NoPE MLA restricted to those tokens"; the
+ * "Shape of the pipeline": the selected tokens feed an MLA attention
+ * without the rotary part, over those tokens only; the
  * latent width is kv_lora_rank).  Attention in the latent space, no rotary
  * part, the latent row of a selected token being both key and value: for
  * row (b, s), head h and the slots i whose token j_i = idx[b, s, i] is in

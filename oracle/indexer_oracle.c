@@ -22,19 +22,20 @@
  *        I[t, j] = sum_h w[t, h] * ReLU( sum_d q[t, h, d] * k[j, d] )
  *    (the pages name the "lighting_indexer" but do not print the formula;
  *    this is the DeepSeek Sparse Attention lightning-indexer definition).
- *  - Causal masking over compressed keys ("Adapts GLM-5's lighting_indexer
- *    to V4's SBHD data layout and causal masking"; `compress_ratio`,
- *    "compression ratio (4 for C4 layers)"): compressed key j summarises
- *    source tokens [j*r, (j+1)*r), and a key counts only when its whole block
- *    is at or before the query position, (j+1)*r - 1 <= t.  This is the same
- *    rule as "a trailing partial pool is not a pool" on the metrale.ai page
- *    "Module glm5next_dsa", section "Checkpoint and kernel facts".
+ *  - Causal masking over compressed keys (the module summary says the
+ *    indexer was moved onto V4's SBHD layout with causal masking; the
+ *    `compress_ratio` parameter is 4 on C4 layers): compressed key j
+ *    summarises source tokens [j*r, (j+1)*r), and a key counts only when its
+ *    whole block is at or before the query position, (j+1)*r - 1 <= t.  The
+ *    metrale.ai page "Module glm5next_dsa", section "Checkpoint and kernel
+ *    facts", applies the same rule to pools: an incomplete pool at the end
+ *    does not count.
  *  - Top-k: the `topk` visible keys with the largest score, returned in
  *    descending score order, equal scores ordered by the lower key index
- *    first; slots past the number of visible keys hold index -1 ("-1 =
- *    invalid", page "Module glm5next_dsa", section "Shape of the pipeline";
- *    "writes -1 over the whole index row before it stores any index",
- *    section "Checkpoint and kernel facts") and score -inf.
+ *    first; slots past the number of visible keys hold index -1 (the page
+ *    "Module glm5next_dsa" marks an invalid index with -1, section "Shape of
+ *    the pipeline", and fills the whole index row with -1 before storing the
+ *    real indices, section "Checkpoint and kernel facts") and score -inf.
  *  - Given indices (`topk_indices` parameter, and `pytorch_extract_topk_scores
  *    (logits, topk_indices, dim=-1)`): the score of each given slot is the
  *    logit at that index, -inf where the index is -1, out of range or not
@@ -341,13 +342,14 @@ void oracle_indexer_bwd(const uint16_t *q, const uint16_t *k, const float *w,
 
 /*
  * Pool compression (page "Module glm5next_dsa": kpool_compress in "Shape of
- * the pipeline"; "The pool softmax runs over the pool-slot axis, per
- * channel", "Pooling starts at first_key. A pool counts only if every one of
- * its index_kpool slots is valid" in "Checkpoint and kernel facts").
+ * the pipeline"; section "Checkpoint and kernel facts": the softmax of a
+ * pool is taken across its slots separately for each channel, pools begin
+ * at first_key, and a pool is a candidate only when all of its slots are
+ * valid).
  *
  * Pool p of sequence b covers the tokens first_key + p*kpool + s,
- * s = 0..kpool-1; there are P = (T - first_key) / kpool whole pools (a
- * trailing partial pool is not a pool).  For channel c, with the slot logits
+ * s = 0..kpool-1; there are P = (T - first_key) / kpool whole pools (an
+ * incomplete pool at the end is dropped).  For channel c, with the slot logits
  * z_s = gate[token_s, b, c] + ape[s, c]:
  *     key[p, b, c] = sum_s softmax_s(z)_s * k[token_s, b, c]
  * (the page names the inputs k, gate, valid and ape and the softmax axis; the
@@ -400,9 +402,9 @@ long long oracle_kpool_compress(const uint16_t *k, const float *gate,
 
 /*
  * Selection expansion (page "Module glm5next_dsa": expand_selection in
- * "Shape of the pipeline", "-1 = invalid"; "dsa_expand_selection writes -1
- * over the whole index row before it stores any index, so every slot is
- * written").  Each row's select_k pool ids become select_k * kpool token
+ * "Shape of the pipeline", where -1 marks an invalid id; section
+ * "Checkpoint and kernel facts": the expansion fills its whole output row
+ * with -1 first, so no slot is left unwritten).  Each row's select_k pool ids become select_k * kpool token
  * ids: slot i*kpool + s holds first_key + pool_i*kpool + s, or -1 when
  * pool_i is -1.
  */
@@ -426,7 +428,8 @@ void oracle_expand_selection(const int32_t *pools, long long rows,
 
 /*
  * Sparse MLA forward over the selected tokens (page "Module glm5next_dsa",
- * "Shape of the pipeline": "-> NoPE MLA restricted to those tokens"; the
+ * "Shape of the pipeline": the selected tokens feed an MLA attention
+ * without the rotary part, over those tokens only; the
  * NeMo AutoModel pages list tilelang_sparse_mla_fwd after the indexer; the
  * latent width is kv_lora_rank, section "Constants", KERNEL_KV_LORA_DIM).
  * The pages print no formula; this is attention in the MLA latent space

@@ -25,21 +25,23 @@ def score_tol(o):
     return 1e-3 + 2e-3 * np.abs(o)
 
 
-def compare_topk_row(g_idx, g_sc, o_idx, o_sc64, o_next, logits64=None):
+def compare_topk_row(g_idx, g_sc, o_idx, o_sc64, o_next, logits64):
     """Compare one row of GPU top-k output with the oracle's.
 
     g_idx/g_sc: GPU indices (int32) and scores (fp32) for the row.
     o_idx/o_sc64: oracle indices and fp64 scores; o_next: the oracle's
     (topk+1)-th visible score (-inf if there is none).  logits64: the
     oracle's full fp64 row (-inf where invisible), used to look up the
-    oracle score of any GPU index; required for the near-tie branch.
+    oracle score of every GPU index.
 
     Returns None when the row matches, else a message.
     Rule: the -1 slots match exactly; scores agree slot by slot within the
-    tolerance; index sets are equal when the oracle's k-th and (k+1)-th
-    scores are at least a tolerance apart, otherwise every oracle index
-    scored clearly above the k-th is kept and every GPU index scores at
-    least the k-th minus the tolerance.
+    tolerance; every returned score is the oracle score of the index
+    returned in the same slot, within the tolerance (so an output whose
+    indices are permuted against its scores fails); index sets are equal
+    when the oracle's k-th and (k+1)-th scores are at least a tolerance
+    apart, otherwise every oracle index scored clearly above the k-th is
+    kept and every GPU index scores at least the k-th minus the tolerance.
     """
     g_idx = np.asarray(g_idx)
     g_sc = np.asarray(g_sc, dtype=np.float64)
@@ -60,6 +62,15 @@ def compare_topk_row(g_idx, g_sc, o_idx, o_sc64, o_next, logits64=None):
     gv = g_idx[valid]
     if len(set(gv.tolist())) != gv.size:
         return "duplicate indices"
+    L = np.asarray(logits64, dtype=np.float64)
+    if gv.size and (gv.min() < 0 or gv.max() >= L.size):
+        return "index outside the row"
+    own = L[gv]
+    pair_bad = ~(np.abs(g_sc[valid] - own) <= score_tol(own))
+    if np.any(pair_bad):
+        i = int(np.flatnonzero(pair_bad)[0])
+        return (f"slot {i}: score {g_sc[valid][i]!r} is not the score of its "
+                f"index {int(gv[i])} (oracle {own[i]!r})")
     ov = o_idx[valid]
     if ov.size == 0:
         return None
@@ -68,8 +79,6 @@ def compare_topk_row(g_idx, g_sc, o_idx, o_sc64, o_next, logits64=None):
         if set(gv.tolist()) != set(ov.tolist()):
             return "index sets differ away from a near-tie"
         return None
-    assert logits64 is not None, "near-tie row needs the oracle logits"
-    L = np.asarray(logits64)
     tol = score_tol(kth)
     must = set(ov[o_sc[valid] > kth + tol].tolist())
     if not must.issubset(set(gv.tolist())):

@@ -69,12 +69,12 @@ def check_invariants(sc, idx, nvis, topk):
 
 def compare_rows(sc, idx, ref, rows, S):
     bad = []
-    logits = ref.get("logits")
+    logits = ref["logits"]  # the oracle must be run with want_logits=True
     for n, r in enumerate(rows):
         b, s = divmod(int(r), S)
         msg = compare_topk_row(idx[b, s], sc[b, s], ref["idx"][n],
                                ref["scores64"][n], ref["next"][n],
-                               None if logits is None else logits[n])
+                               logits[n])
         if msg:
             bad.append((b, s, msg))
     assert not bad, bad[:5]

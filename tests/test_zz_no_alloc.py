@@ -48,20 +48,35 @@ def _p(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def run_static(lib, q, k, w, ratio, topk, q_pos=None, in_idx=None):
-    """One call of the allocation-free entry point; returns numpy outputs,
-    the device status word and the synchronous return code."""
-    S, B, H, D = q.shape
-    S_kv = k.shape[0]
+def alloc_outputs(B, S, topk):
     out_idx = torch.full((B, S, topk), 7, dtype=torch.int32, device="cuda")
     out_sc = torch.full((B, S, topk), 7.0, dtype=torch.float32,
                         device="cuda")
     status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    return out_idx, out_sc, status
+
+
+def call_static(lib, q, k, w, ratio, topk, outs, q_pos=None, in_idx=None):
+    """One call of the allocation-free entry point into caller-owned
+    outputs; returns the synchronous return code."""
+    S, B, H, D = q.shape
+    S_kv = k.shape[0]
+    out_idx, out_sc, status = outs
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    rc = lib.dsa_indexer_fwd_static_scratch(
+    return lib.dsa_indexer_fwd_static_scratch(
         _p(q), _p(k), _p(w), S, B, H, D, S_kv, ratio, topk, _p(q_pos),
         _p(in_idx), _p(out_idx), _p(out_sc), _p(status), stream)
+
+
+def run_static(lib, q, k, w, ratio, topk, q_pos=None, in_idx=None):
+    """One call of the allocation-free entry point; returns numpy outputs,
+    the device status word and the synchronous return code."""
+    S, B = q.shape[0], q.shape[1]
+    outs = alloc_outputs(B, S, topk)
+    rc = call_static(lib, q, k, w, ratio, topk, outs, q_pos=q_pos,
+                     in_idx=in_idx)
     torch.cuda.synchronize()
+    out_idx, out_sc, status = outs
     return out_sc.cpu().numpy(), out_idx.cpu().numpy(), int(status.item()), rc
 
 
@@ -101,6 +116,45 @@ def test_matches_workspace_forward_on_consecutive_calls(dsa, lib):
                                                q_pos=pos)
         assert ref_st == 0
         assert_same(sc, idx, ref_sc, ref_idx)
+
+
+def test_matches_oracle_on_sampled_rows(dsa, lib):
+    """The 4096 x 4096 prefill through the allocation-free entry point,
+    compared with the CPU oracle on sampled rows (the oracle computes them
+    one by one), by the same rule as the other GPU parity tests."""
+    import oracle
+    from tests.helpers import compare_topk_row
+    wl, q, k, w, pos = device_inputs("v32_prefill")
+    sc, idx, st, rc = run_static(lib, q, k, w, wl.compress_ratio, wl.topk)
+    assert rc == OK and st == 0
+    rows = np.array([0, 1, 700, 2047, 2048, 2049, 3000, 4095],
+                    dtype=np.int64)
+    ref = oracle.indexer_fwd(q.cpu(), k.cpu(), w.cpu(), wl.compress_ratio,
+                             wl.topk, rows=rows, want_logits=True)
+    sc, idx = sc.reshape(-1, wl.topk), idx.reshape(-1, wl.topk)
+    for n, r in enumerate(rows):
+        msg = compare_topk_row(idx[r], sc[r], ref["idx"][n],
+                               ref["scores64"][n], ref["next"][n],
+                               ref["logits"][n])
+        assert msg is None, (int(r), msg)
+
+
+def test_allocates_no_device_memory(dsa, lib):
+    """After a first call (which may load the library's kernels onto the
+    device), a call changes the device's free memory by nothing: the entry
+    point allocates and frees no device memory.  Inputs and outputs are
+    allocated before the measurement."""
+    wl, q, k, w, pos = device_inputs("v32_prefill")
+    outs = alloc_outputs(wl.B, wl.S, wl.topk)
+    assert call_static(lib, q, k, w, 1, wl.topk, outs) == OK
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(2):
+        assert call_static(lib, q, k, w, 1, wl.topk, outs) == OK
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
+    assert int(outs[2].item()) == 0
 
 
 def test_repeat_call_gives_same_result(dsa, lib):
