@@ -218,6 +218,10 @@ size_t dsa_indexer_workspace_size(int S, int B, int H, int D, int S_kv,
     return gather_direct_shape(B, H, D, S_kv)
                ? kHeaderBytes
                : kHeaderBytes + logits_bytes(S, B, S_kv);
+  // prefill rows: scores and selection in one kernel, which needs only its
+  // per-CTA scratch; decode rows and other shapes write the logits
+  if (dsa::index_topk_supported(S, H, D, S_kv, topk))
+    return kHeaderBytes + dsa::index_topk_scratch_bytes(H, S_kv);
   return kHeaderBytes + logits_bytes(S, B, S_kv);
 }
 
@@ -269,7 +273,9 @@ int forward_core(const void *q, const void *k, const float *w, int S, int B,
   DeviceInfo dev;
   rc = current_device_info(&dev);
   if (rc != DSA_OK) return rc;
-  if (!in_idx) {
+  const bool fused =
+      !in_idx && dsa::index_topk_supported(S, H, D, S_kv, topk);
+  if (!in_idx && !fused) {
     const size_t sel = dsa::topk_select_smem_bytes(S_kv, topk) + 4096;
     if (sel > (size_t)dev.max_smem_optin) return DSA_ERR_UNSUPPORTED;
   }
@@ -301,6 +307,23 @@ int forward_core(const void *q, const void *k, const float *w, int S, int B,
     if (dsa::launch_gather_scores(p, tm_q, in_idx, topk, out_idx,
                                   out_scores, status, dev.num_sms,
                                   st) != cudaSuccess)
+      return DSA_ERR_CUDA;
+    if (mark(1) != cudaSuccess || mark(2) != cudaSuccess) return DSA_ERR_CUDA;
+    return DSA_OK;
+  }
+  if (fused) {
+    // one kernel: scores into the per-CTA scratch, selection beside them
+    if ((size_t)dev.max_smem_optin < dsa::index_topk_smem_bytes(H, D, topk))
+      return DSA_ERR_UNSUPPORTED;
+    CUtensorMap tm_q, tm_k;
+    rc = encode_q(&tm_q, p, dsa::kTileCols / H);
+    if (rc != DSA_OK) return rc;
+    rc = encode_k(&tm_k, p);
+    if (rc != DSA_OK) return rc;
+    if (mark(0) != cudaSuccess) return DSA_ERR_CUDA;
+    if (dsa::launch_index_topk(p, tm_q, tm_k, topk, logits, out_idx,
+                               out_scores, status, dev.num_sms,
+                               st) != cudaSuccess)
       return DSA_ERR_CUDA;
     if (mark(1) != cudaSuccess || mark(2) != cudaSuccess) return DSA_ERR_CUDA;
     return DSA_OK;

@@ -115,6 +115,23 @@ size_t decode_smem_bytes(int H, int D);
 
 cudaError_t launch_fill_masked(float *logits, size_t n, cudaStream_t st);
 
+// Prefill forward in one kernel: scores and per-row top-k, the scores kept
+// in a per-CTA scratch (two work-item slots of 256/H rows of S_kv fp32,
+// for at most kIndexTopkMaxCtas CTAs) instead of [B, S, S_kv] logits.
+constexpr int kIndexTopkMaxCtas = 160;
+constexpr int kIndexTopkMaxTopk = 2048;
+constexpr size_t kIndexTopkMaxSmem = 232448;  // 227 KB opt-in per block
+bool index_topk_supported(int S, int H, int D, int S_kv, int topk);
+size_t index_topk_smem_bytes(int H, int D, int topk);
+size_t index_topk_scratch_bytes(int H, int S_kv);
+int index_topk_row_stride(int S_kv);
+// tm_q: q with a box of 256/H queries (as for launch_index_scores).
+cudaError_t launch_index_topk(const Problem &p, const CUtensorMap &tm_q,
+                              const CUtensorMap &tm_k, int topk,
+                              float *scratch, int32_t *out_idx,
+                              float *out_scores, int *status, int num_sms,
+                              cudaStream_t st);
+
 // TMA map of q [S, B, H, D] bf16 as (d, h, b, s) with a box of 64 d x H
 // heads x 1 x `queries` (returns a dsa_status code).
 int encode_q(CUtensorMap *m, const Problem &p, int queries);

@@ -4,7 +4,8 @@
 // allocator owns all free memory, plugin hosts that hand out only the
 // tensors they manage, and hot paths where an allocation would synchronise
 // the device.  For them this entry point runs the same forward as
-// dsa_indexer_fwd() with its scratch (the status header and the fp32 logits)
+// dsa_indexer_fwd() with its scratch (the status header, then per-CTA score
+// rows of the one-kernel prefill or the fp32 logits of the other shapes)
 // taken from a fixed array in this file instead of a caller workspace.
 //
 // The array is a file-scope __device__ variable: each GPU on which this
@@ -49,7 +50,7 @@ extern "C" int dsa_indexer_fwd_static_scratch(
   int rc = static_scratch_address(&scratch);
   if (rc != DSA_OK) return rc;
   // The forward clears the status header itself before its kernels run;
-  // the logits region needs no clearing (every entry that is read was
+  // the rest of the array needs no clearing (every entry that is read was
   // written earlier in the same call).
   rc = dsa_indexer_fwd(q, k, w, S, B, H, D, S_kv, compress_ratio, topk, q_pos,
                        in_idx, out_idx, out_scores, scratch,

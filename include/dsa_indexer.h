@@ -265,15 +265,17 @@ DSA_API int dsa_selftest_wait_limit(int limit_us, void *workspace,
  * For callers that cannot call cudaMalloc -- code running while a caching
  * allocator holds all free device memory, plugin hosts that only hand out
  * the tensors they own, or paths where an allocation would synchronise the
- * device.  The forward's scratch (status header + fp32 logits) comes from a
- * fixed array of DSA_STATIC_SCRATCH_BYTES inside the library instead of a
- * caller workspace; the caller still passes every input and output.
+ * device.  The forward's scratch (status header, then the one-kernel
+ * prefill's per-CTA score rows or the written logits) comes from a fixed
+ * array of DSA_STATIC_SCRATCH_BYTES inside the library instead of a caller
+ * workspace; the caller still passes every input and output.
  *
  *   - Limit: problems whose dsa_indexer_workspace_size() exceeds
- *     DSA_STATIC_SCRATCH_BYTES (64 MiB plus a 256-byte header: e.g. the
- *     4096 x 4096 prefill's 64 MiB of logits, B*S*S_kv <= 16,777,216) are
- *     refused with DSA_ERR_UNSUPPORTED before any device work.  Other
- *     argument errors are those of dsa_indexer_fwd().
+ *     DSA_STATIC_SCRATCH_BYTES (64 MiB plus a 256-byte header: e.g. a
+ *     one-kernel prefill with H = 64 and S_kv <= 6528 whatever S, or a
+ *     written-logits shape with B*S*S_kv <= 16,777,216) are refused with
+ *     DSA_ERR_UNSUPPORTED before any device work.  Other argument errors
+ *     are those of dsa_indexer_fwd().
  *   - Memory: every GPU that loads this part of the library holds one copy
  *     of the array until the process exits.  No call allocates or frees
  *     device memory.
@@ -285,8 +287,9 @@ DSA_API int dsa_selftest_wait_limit(int limit_us, void *workspace,
  *   - Sharing: all calls on a device share the one array, which keeps the
  *     last call's contents.  Calls that overlap on the GPU (different
  *     streams, or threads without ordering) race on it; order them on one
- *     stream.  Each call clears the status word it uses; the logits need no
- *     clearing.
+ *     stream.  Each call clears the status word it uses; the rest of the
+ *     array needs no clearing (every entry read was written earlier in the
+ *     same call).
  *   - out_status: NULL, or one device int32 that receives this call's device
  *     status bits (0 = ok; bit 0 = a given index outside [-1, S_kv); bit 1 =
  *     a bounded wait expired), written asynchronously on `cuda_stream`.

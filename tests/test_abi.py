@@ -114,13 +114,23 @@ def test_status_strings(lib):
 
 def test_workspace_size(lib):
     ws = lib.dsa_indexer_workspace_size
-    # top-k path: the status header, then the fp32 logits of every row
-    assert ws(4096, 1, 64, 128, 4096, 1, 2048, 0) == 256 + 4096 * 4096 * 4
-    assert ws(16384, 2, 64, 128, 4096, 4, 512, 0) == 256 + 2 * 16384 * 4096 * 4
-    assert ws(8192, 1, 64, 128, 8192, 1, 2048, 0) == 256 + 8192 * 8192 * 4
-    assert ws(8192, 1, 32, 128, 8192, 1, 2048, 0) == 256 + 8192 * 8192 * 4
+    # prefill top-k path with H in {32, 64, 128} and topk <= 2048: scores
+    # and selection in one kernel; the status header, then the kernel's
+    # per-CTA scratch (160 CTAs x 2 item slots x 256/H rows x S_kv rounded up
+    # to 32, fp32), whatever the number of query rows
+    fused = lambda H, S_kv: 256 + 160 * 2 * (256 // H) * (
+        (S_kv + 31) // 32 * 32) * 4
+    assert ws(4096, 1, 64, 128, 4096, 1, 2048, 0) == fused(64, 4096)
+    assert ws(16384, 2, 64, 128, 4096, 4, 512, 0) == fused(64, 4096)
+    assert ws(65536, 1, 64, 128, 16384, 4, 2048, 0) == fused(64, 16384)
+    assert ws(8192, 1, 32, 128, 8192, 1, 2048, 0) == fused(32, 8192)
+    assert ws(40, 1, 128, 128, 40, 1, 7, 0) == fused(128, 40)
+    assert ws(8, 1, 64, 64, 1000, 1, 100, 0) == fused(64, 1000)
+    # other shapes: the status header, then the fp32 logits of every row
+    assert ws(8192, 1, 64, 128, 8192, 1, 4096, 0) == 256 + 8192 * 8192 * 4
     assert ws(64, 1, 16, 64, 64, 1, 8, 0) == 256 + 64 * 64 * 4
     assert ws(1, 64, 32, 64, 8192, 4, 512, 0) == 256 + 64 * 8192 * 4  # decode
+    assert ws(3, 2, 64, 128, 500, 1, 16, 0) == 256 + 2 * 3 * 500 * 4
     # given indices: H in {16, 32, 64, 128} gathers keys (status header
     # only); other H read the scores back from logits
     assert ws(65536, 1, 64, 128, 16384, 4, 2048, 1) == 256
@@ -206,11 +216,16 @@ def test_host_buffer_size(lib):
     inputs = S_kv * B * D * 2 + S * B * H * D * 2 + S * B * H * 4
     assert need >= inputs + 2 * B * S * k * 4 + ws(S, B, H, D, S_kv, 1, k, 0)
     # eight chunks of 512 rows: the workspace is one chunk's, not the call's
-    big = hb(4096, 1, 64, 128, 4096, 1, 2048, 0)
-    assert big < (4096 * 64 * 128 * 2 + 2 * 4096 * 2048 * 4
-                  + ws(4096, 1, 64, 128, 4096, 1, 2048, 0))
-    assert big >= 4096 * 64 * 128 * 2 + 2 * 4096 * 2048 * 4 + ws(
-        512, 1, 64, 128, 4096, 1, 2048, 0)
+    # (H = 16 writes logits, whose size grows with the rows)
+    big = hb(4096, 1, 16, 128, 4096, 1, 2048, 0)
+    assert big < (4096 * 16 * 128 * 2 + 2 * 4096 * 2048 * 4
+                  + ws(4096, 1, 16, 128, 4096, 1, 2048, 0))
+    assert big >= 4096 * 16 * 128 * 2 + 2 * 4096 * 2048 * 4 + ws(
+        512, 1, 16, 128, 4096, 1, 2048, 0)
+    # the one-kernel prefill's scratch does not grow with the rows at all
+    f = hb(4096, 1, 64, 128, 4096, 1, 2048, 0)
+    assert f >= 4096 * 64 * 128 * 2 + 2 * 4096 * 2048 * 4 + ws(
+        4096, 1, 64, 128, 4096, 1, 2048, 0)
 
 
 def test_host_fwd_rejects_bad_arguments(lib):

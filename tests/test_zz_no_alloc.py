@@ -104,7 +104,8 @@ def device_inputs(name):
 
 def test_matches_workspace_forward_on_consecutive_calls(dsa, lib):
     # three calls in a row share the library's one scratch array: a small
-    # problem, the largest one that fits exactly, then a decode batch
+    # problem, the 4096 x 4096 prefill (one kernel, its per-CTA scratch in
+    # the array), then a decode batch (logits in the array)
     for name in ("tiny", "v32_prefill", "decode"):
         wl, q, k, w, pos = device_inputs(name)
         sc, idx, st, rc = run_static(lib, q, k, w, wl.compress_ratio,
@@ -189,8 +190,9 @@ def test_refuses_problems_beyond_the_fixed_scratch(lib):
         fake, fake, fake, wl.S, wl.B, wl.H, wl.D, wl.S_kv, wl.compress_ratio,
         wl.topk, None, None, fake, fake, None, None)
     assert rc == UNSUPPORTED
-    # one query row more than the largest problem that fits is refused too
+    # with 16 heads the forward writes [S, S_kv] fp32 logits: 4096 query
+    # rows over 4096 keys fill the 64 MiB exactly, one row more is refused
     rc = lib.dsa_indexer_fwd_static_scratch(
-        fake, fake, fake, 4097, 1, 64, 128, 4096, 1, 2048, None, None, fake,
+        fake, fake, fake, 4097, 1, 16, 128, 4096, 1, 2048, None, None, fake,
         fake, None, None)
     assert rc == UNSUPPORTED
