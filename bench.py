@@ -46,12 +46,12 @@ WORKLOAD = "long_c4"
 L2_FLUSH_BYTES = 256 << 20
 
 
-def fused_shape(S: int, H: int, S_kv: int, topk: int) -> bool:
-    """Prefill top-k shapes the one-kernel forward (scores and selection in
-    the same kernel) covers; the others write logits and select in a second
-    kernel."""
-    return (H in (32, 64, 128) and S >= 256 // H and topk <= 2048
-            and S_kv < (1 << 20))
+def prefill_policy(dsa, name: str) -> None:
+    """Apply --prefill (auto: one kernel for rows of at least 8192 keys,
+    else scores then selection; one / two: force a path)."""
+    dsa.dsa_set_prefill_policy({"auto": dsa.PREFILL_AUTO,
+                                "one": dsa.PREFILL_ONE_KERNEL,
+                                "two": dsa.PREFILL_TWO_KERNELS}[name])
 
 
 def visible_pairs(wl, q_pos=None) -> int:
@@ -302,6 +302,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     dsa.build()
     dsa.load_library()
+    prefill_policy(dsa, args.prefill)
 
     wl = WORKLOADS[args.workload]
     q, k, w, q_pos = make_inputs(wl)
@@ -369,20 +370,28 @@ def run_ours(args):
     step_ms = [a.elapsed_time(b) for a, b in ev]
     t_step = max_over_ranks(sum(step_ms) / K, world, dev)
 
-    # per-kernel split: another K steps with events recorded between the
-    # stages (these can keep the next kernel from starting early, so they
-    # time the kernels, not the step)
-    sev = [(mk(), mk(), mk()) for _ in range(K)]
-    for tri in sev:
-        for e in tri:
+    # per-kernel split: another K steps with an event after every kernel
+    # (these can keep the next kernel from starting early, so they time the
+    # kernels, not the step).  The two-kernel forward alternates scores and
+    # selection, chunk by chunk.
+    n_launch = dsa.dsa_indexer_fwd_launches(
+        wl.S, wl.B, wl.H, wl.D, wl.S_kv, wl.compress_ratio, wl.topk,
+        gi is not None)
+    sev = [[mk() for _ in range(1 + max(2, n_launch))] for _ in range(K)]
+    for evs in sev:
+        for e in evs:
             e.record(stream)
     torch.cuda.synchronize()
     for i in range(K):
         flush.fill_(1.0)
         step(sev[i])
     torch.cuda.synchronize()
-    score_ms = [a.elapsed_time(b) for a, b, _ in sev]
-    select_ms = [b.elapsed_time(c) for _, b, c in sev]
+    score_ms = [sum(e[j].elapsed_time(e[j + 1])
+                    for j in range(0, max(1, n_launch - 1), 2))
+                for e in sev]
+    select_ms = [sum(e[j].elapsed_time(e[j + 1])
+                     for j in range(1, max(2, n_launch), 2))
+                 for e in sev]
 
     # ---- end to end through the C entry point on host buffers ----
     # (page-locked inputs and outputs and the device buffer are allocated
@@ -437,9 +446,8 @@ def run_ours(args):
     # the given-indices path is one kernel when H has a gather instantiation
     direct = gi is not None and wl.H in (16, 32, 64, 128)
     decode_shape = wl.S < 256 // wl.H
-    # prefill top-k shapes the one-kernel forward (scores and selection
-    # together) covers
-    fused = gi is None and fused_shape(wl.S, wl.H, wl.S_kv, wl.topk)
+    # the one-kernel forward (scores and selection together) ran
+    fused = gi is None and n_launch == 1
 
     def tensor_line(kernel, ms):
         a = flops / (ms * 1e-3) / 1e12
@@ -482,7 +490,7 @@ def run_ours(args):
                      second: hbm_line(second, t_second, sbytes,
                                       "visible logits read + idx/scores "
                                       "written")}
-        launches = 2
+        launches = n_launch
     top = max((k for k in kernels if k != "step"), key=lambda k: kernels[k])
     name = wl.name + (" given-indices" if gi is not None else "")
     line = {
@@ -504,6 +512,8 @@ def run_ours(args):
                    "visible_pairs": pairs, "flops_per_step": flops,
                    "l2": "flushed before each step (256 MiB write, outside "
                          "the timed events)",
+                   "prefill_path": ("one kernel" if fused else
+                                    f"{n_launch} kernels"),
                    "parallelism": f"replicas x{world}"},
         "queries_per_s": world * wl.B * wl.S / (t_step * 1e-3),
         "pct_of_bf16_peak": 100.0 * value / world / tc_peak,
@@ -548,6 +558,7 @@ def run_varlen(args):
     dev = torch.device("cuda", local)
     dsa.build()
     dsa.load_library()
+    prefill_policy(dsa, args.prefill)
     vw = VARLEN_WORKLOADS[args.workload]
     q, k, w, cq, ck = make_varlen_inputs(vw)
     pairs = 0
@@ -646,12 +657,12 @@ def run_varlen(args):
                 w.numel() * 4,
                 "d2h_bytes_per_step": oi.numel() * 8,
                 "api": "torch copies + dsa_indexer_fwd_varlen"},
-        # per sequence with keys one kernel (scores and selection together)
-        # or two (logits, then selection), plus the status merge when more
-        # than one stream slice ran
+        # per sequence with keys the kernels of one B = 1 forward, plus the
+        # status merge when more than one stream slice ran
         "gpu_launches": K * (sum(
-            1 if fused_shape(cq[i + 1] - cq[i], vw.H, ck[i + 1] - ck[i],
-                             vw.topk) else 2
+            dsa.dsa_indexer_fwd_launches(cq[i + 1] - cq[i], 1, vw.H, vw.D,
+                                         ck[i + 1] - ck[i], vw.compress_ratio,
+                                         vw.topk)
             for i in range(len(vw.lens_q))
             if ck[i + 1] > ck[i] and cq[i + 1] > cq[i])
             + (1 if ws.numel() > ws.numel() // 2 and
@@ -839,6 +850,7 @@ def run_pooled(args):
     dev = torch.device("cuda", local)
     dsa.build()
     dsa.load_library()
+    prefill_policy(dsa, args.prefill)
     B, S, T, H, D, kpool, fk, itopk = 2, 16384, 16384, 64, 128, 4, 0, 2048
     g = torch.Generator().manual_seed(21)
     q = torch.randn((S, B, H, D), generator=g).to(torch.bfloat16)
@@ -960,9 +972,10 @@ def run_pooled(args):
                                           for t in hin),
                 "d2h_bytes_per_step": hout.numel() * 4,
                 "api": "torch copies + dsa_indexer_fwd_pooled"},
-        # per step: compression, the one-kernel forward over the pools and
-        # the expansion, plus the compression timed alone
-        "gpu_launches": K * 4,
+        # per step: compression, the forward over the pools and the
+        # expansion, plus the compression timed alone
+        "gpu_launches": K * (3 + dsa.dsa_indexer_fwd_launches(
+            S, B, H, D, P, kpool, itopk // kpool)),
         "clocks": clocks,
         "wall_s_timed_region": wall,
     }
@@ -1128,6 +1141,10 @@ def main():
     ap.add_argument("--given-indices", action="store_true")
     ap.add_argument("--backward", action="store_true",
                     help="time the indexer backward instead of the forward")
+    ap.add_argument("--prefill", choices=["auto", "one", "two"],
+                    default="auto",
+                    help="prefill top-k path: auto (one kernel for rows of "
+                         "at least 8192 keys), or force one / two kernels")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

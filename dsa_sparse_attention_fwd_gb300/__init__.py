@@ -25,6 +25,8 @@ from ._build import LIB_PATH, build
 
 __all__ = [
     "DsaError", "load_library", "build", "dsa_indexer_workspace_size",
+    "dsa_set_prefill_policy", "dsa_indexer_fwd_launches", "PREFILL_AUTO",
+    "PREFILL_ONE_KERNEL", "PREFILL_TWO_KERNELS",
     "dsa_indexer_fwd", "dsa_indexer_logits", "dsa_indexer_check",
     "dsa_status_string", "dsa_selftest_wait_limit", "v4_lighting_indexer",
     "indexer_logits", "dsa_indexer_host_buffer_size", "dsa_indexer_fwd_host",
@@ -69,6 +71,10 @@ def load_library(path: str | None = None):
         P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
         lib.dsa_indexer_workspace_size.restype = Z
         lib.dsa_indexer_workspace_size.argtypes = [I] * 8
+        lib.dsa_set_prefill_policy.restype = I
+        lib.dsa_set_prefill_policy.argtypes = [I]
+        lib.dsa_indexer_fwd_launches.restype = I
+        lib.dsa_indexer_fwd_launches.argtypes = [I] * 8
         lib.dsa_indexer_fwd.restype = I
         lib.dsa_indexer_fwd.argtypes = [P, P, P, I, I, I, I, I, I, I, P, P, P,
                                         P, P, Z, P]
@@ -134,6 +140,25 @@ def _stream(stream):
 
 def dsa_status_string(code: int) -> str:
     return load_library().dsa_status_string(int(code)).decode()
+
+
+# prefill top-k path policies (dsa_set_prefill_policy)
+PREFILL_AUTO, PREFILL_ONE_KERNEL, PREFILL_TWO_KERNELS = 0, 1, 2
+
+
+def dsa_set_prefill_policy(policy: int) -> None:
+    """Process-wide choice between the one-kernel and the two-kernel prefill
+    forward (PREFILL_AUTO picks by row length)."""
+    rc = load_library().dsa_set_prefill_policy(int(policy))
+    if rc != 0:
+        raise DsaError(rc, "dsa_set_prefill_policy")
+
+
+def dsa_indexer_fwd_launches(S, B, H, D, S_kv, compress_ratio, topk,
+                             has_in_idx=False) -> int:
+    """Kernels one forward of this shape launches under the current policy."""
+    return int(load_library().dsa_indexer_fwd_launches(
+        S, B, H, D, S_kv, compress_ratio, topk, 1 if has_in_idx else 0))
 
 
 def dsa_indexer_workspace_size(S, B, H, D, S_kv, compress_ratio, topk,

@@ -5,6 +5,7 @@
 // pytorch_extract_topk_scores).
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -16,6 +17,7 @@ namespace {
 using dsa::Problem;
 
 constexpr size_t kHeaderBytes = 256;  // status word + padding
+constexpr int kMaxStageEvents = 1024;  // dsa_indexer_fwd_profiled
 
 struct DeviceInfo {
   bool valid = false;
@@ -83,6 +85,37 @@ int check_shape(int S, int B, int H, int D, int S_kv, int ratio) {
 
 size_t logits_bytes(int S, int B, int S_kv) {
   return (size_t)B * (size_t)S * (size_t)S_kv * sizeof(float);
+}
+
+// The two-kernel prefill writes the logits of at most this many bytes of
+// query rows at a time (scores, then their selection, chunk after chunk),
+// so the buffer stays in L2 and does not grow with S.
+constexpr size_t kLogitsChunkBytes = (size_t)64 << 20;
+
+// Query rows per chunk of the two-kernel top-k path (a multiple of the
+// scoring tile's 256/H rows, or all S rows).
+int logits_chunk_rows(int S, int B, int H, int S_kv) {
+  const size_t per_row = (size_t)B * (size_t)S_kv * sizeof(float);
+  if ((size_t)S * per_row <= kLogitsChunkBytes) return S;
+  const long long tq = dsa::kTileCols / H;
+  long long rows = (long long)(kLogitsChunkBytes / per_row) / tq * tq;
+  if (rows < tq) rows = tq;
+  return rows < S ? (int)rows : S;
+}
+
+// Prefill top-k path policy (dsa_set_prefill_policy).
+std::atomic<int> g_prefill_policy{DSA_PREFILL_AUTO};
+
+// Whether a top-k call of this shape runs the one-kernel forward: the
+// shape must fit it, and under the automatic policy the rows must be long
+// (at least 8192 compressed keys), where the selection keeps pace with the
+// scoring; shorter rows run scores then selection in two kernels.
+bool use_one_kernel(int S, int H, int D, int S_kv, int topk) {
+  if (!dsa::index_topk_supported(S, H, D, S_kv, topk)) return false;
+  const int pol = g_prefill_policy.load(std::memory_order_relaxed);
+  if (pol == DSA_PREFILL_TWO_KERNELS) return false;
+  if (pol == DSA_PREFILL_ONE_KERNEL) return true;
+  return S_kv >= 8192;
 }
 
 bool aligned16(const void *p) {
@@ -174,7 +207,7 @@ bool use_decode_path(const Problem &p, const DeviceInfo &dev) {
 
 // Device checks + tensor maps + the scoring launch.
 int run_scores(const Problem &p, float *logits, int *status,
-               const DeviceInfo &dev, cudaStream_t st) {
+               const DeviceInfo &dev, cudaStream_t st, int s0, int Sc) {
   const bool decode = use_decode_path(p, dev);
   if (!decode &&
       (size_t)dev.max_smem_optin < dsa::index_scores_smem_bytes(p.H, p.D))
@@ -188,7 +221,7 @@ int run_scores(const Problem &p, float *logits, int *status,
       decode ? dsa::launch_decode_scores(p, tm_q, tm_k, logits, status,
                                          dev.num_sms, st)
              : dsa::launch_index_scores(p, tm_q, tm_k, logits, status,
-                                        dev.num_sms, st);
+                                        dev.num_sms, st, s0, Sc);
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
@@ -218,11 +251,29 @@ size_t dsa_indexer_workspace_size(int S, int B, int H, int D, int S_kv,
     return gather_direct_shape(B, H, D, S_kv)
                ? kHeaderBytes
                : kHeaderBytes + logits_bytes(S, B, S_kv);
-  // prefill rows: scores and selection in one kernel, which needs only its
-  // per-CTA scratch; decode rows and other shapes write the logits
-  if (dsa::index_topk_supported(S, H, D, S_kv, topk))
+  // scores and selection in one kernel need only its per-CTA scratch; the
+  // two-kernel path needs the logits of one chunk of query rows
+  if (use_one_kernel(S, H, D, S_kv, topk))
     return kHeaderBytes + dsa::index_topk_scratch_bytes(H, S_kv);
-  return kHeaderBytes + logits_bytes(S, B, S_kv);
+  return kHeaderBytes + logits_bytes(logits_chunk_rows(S, B, H, S_kv), B, S_kv);
+}
+
+int dsa_set_prefill_policy(int policy) {
+  if (policy != DSA_PREFILL_AUTO && policy != DSA_PREFILL_ONE_KERNEL &&
+      policy != DSA_PREFILL_TWO_KERNELS)
+    return DSA_ERR_INVALID_ARG;
+  g_prefill_policy.store(policy, std::memory_order_relaxed);
+  return DSA_OK;
+}
+
+int dsa_indexer_fwd_launches(int S, int B, int H, int D, int S_kv,
+                             int compress_ratio, int topk, int has_in_idx) {
+  if (check_shape(S, B, H, D, S_kv, compress_ratio) != DSA_OK) return 0;
+  if (topk <= 0 || topk > DSA_MAX_TOPK) return 0;
+  if (has_in_idx) return gather_direct_shape(B, H, D, S_kv) ? 1 : 2;
+  if (use_one_kernel(S, H, D, S_kv, topk)) return 1;
+  const int rows = logits_chunk_rows(S, B, H, S_kv);
+  return 2 * ((S + rows - 1) / rows);
 }
 
 size_t dsa_indexer_logits_workspace_size(void) { return kHeaderBytes; }
@@ -261,7 +312,8 @@ int forward_core(const void *q, const void *k, const float *w, int S, int B,
   if (topk <= 0) return DSA_ERR_INVALID_ARG;
   if (topk > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k)) return DSA_ERR_INVALID_ARG;
-  if (n_events < 0 || n_events > 3 || (n_events > 0 && !stage_events))
+  if (n_events < 0 || n_events > kMaxStageEvents ||
+      (n_events > 0 && !stage_events))
     return DSA_ERR_INVALID_ARG;
   for (int i = 0; i < n_events; ++i)
     if (!stage_events[i]) return DSA_ERR_INVALID_ARG;
@@ -273,8 +325,7 @@ int forward_core(const void *q, const void *k, const float *w, int S, int B,
   DeviceInfo dev;
   rc = current_device_info(&dev);
   if (rc != DSA_OK) return rc;
-  const bool fused =
-      !in_idx && dsa::index_topk_supported(S, H, D, S_kv, topk);
+  const bool fused = !in_idx && use_one_kernel(S, H, D, S_kv, topk);
   if (!in_idx && !fused) {
     const size_t sel = dsa::topk_select_smem_bytes(S_kv, topk) + 4096;
     if (sel > (size_t)dev.max_smem_optin) return DSA_ERR_UNSUPPORTED;
@@ -290,6 +341,12 @@ int forward_core(const void *q, const void *k, const float *w, int S, int B,
     return i < n_events
                ? cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), st)
                : cudaSuccess;
+  };
+  // after the last launch: every remaining event
+  auto mark_rest = [&](int from) {
+    for (int i = from; i < n_events; ++i)
+      if (mark(i) != cudaSuccess) return cudaErrorUnknown;
+    return cudaSuccess;
   };
 
   // Workspace: status header, then the logits.
@@ -308,7 +365,7 @@ int forward_core(const void *q, const void *k, const float *w, int S, int B,
                                   out_scores, status, dev.num_sms,
                                   st) != cudaSuccess)
       return DSA_ERR_CUDA;
-    if (mark(1) != cudaSuccess || mark(2) != cudaSuccess) return DSA_ERR_CUDA;
+    if (mark_rest(1) != cudaSuccess) return DSA_ERR_CUDA;
     return DSA_OK;
   }
   if (fused) {
@@ -325,22 +382,37 @@ int forward_core(const void *q, const void *k, const float *w, int S, int B,
                                out_scores, status, dev.num_sms,
                                st) != cudaSuccess)
       return DSA_ERR_CUDA;
-    if (mark(1) != cudaSuccess || mark(2) != cudaSuccess) return DSA_ERR_CUDA;
+    if (mark_rest(1) != cudaSuccess) return DSA_ERR_CUDA;
     return DSA_OK;
   }
   if (mark(0) != cudaSuccess) return DSA_ERR_CUDA;
-  rc = run_scores(p, logits, status, dev, st);
-  if (rc != DSA_OK) return rc;
-  if (mark(1) != cudaSuccess) return DSA_ERR_CUDA;
-  cudaError_t e;
-  if (in_idx)
-    e = dsa::launch_gather_logits(p, logits, in_idx, topk, out_idx, out_scores,
-                                  status, dev.num_sms, st);
-  else
-    e = dsa::launch_topk_select(p, logits, topk, out_idx, out_scores,
-                                dev.num_sms, st);
-  if (e != cudaSuccess) return DSA_ERR_CUDA;
-  if (mark(2) != cudaSuccess) return DSA_ERR_CUDA;
+  if (in_idx) {
+    // other H: the given indices read the scores back from full logits
+    rc = run_scores(p, logits, status, dev, st, 0, S);
+    if (rc != DSA_OK) return rc;
+    if (mark(1) != cudaSuccess) return DSA_ERR_CUDA;
+    if (dsa::launch_gather_logits(p, logits, in_idx, topk, out_idx,
+                                  out_scores, status, dev.num_sms,
+                                  st) != cudaSuccess)
+      return DSA_ERR_CUDA;
+    if (mark_rest(2) != cudaSuccess) return DSA_ERR_CUDA;
+    return DSA_OK;
+  }
+  // scores then selection, one chunk of query rows at a time: the chunk's
+  // logits are read back while they are still in L2
+  const int rows = logits_chunk_rows(S, B, H, S_kv);
+  int ev = 1;
+  for (int s0 = 0; s0 < S; s0 += rows) {
+    const int sc = S - s0 < rows ? S - s0 : rows;
+    rc = run_scores(p, logits, status, dev, st, s0, sc);
+    if (rc != DSA_OK) return rc;
+    if (mark(ev++) != cudaSuccess) return DSA_ERR_CUDA;
+    if (dsa::launch_topk_select(p, logits, topk, out_idx, out_scores,
+                                dev.num_sms, st, s0, sc) != cudaSuccess)
+      return DSA_ERR_CUDA;
+    if (mark(ev++) != cudaSuccess) return DSA_ERR_CUDA;
+  }
+  if (mark_rest(ev) != cudaSuccess) return DSA_ERR_CUDA;
   return DSA_OK;
 }
 
@@ -379,7 +451,7 @@ int dsa_indexer_logits(const void *q, const void *k, const float *w, int S,
   if (dsa::launch_fill_masked(logits, logits_bytes(S, B, S_kv) / 4, st) !=
       cudaSuccess)
     return DSA_ERR_CUDA;
-  return run_scores(p, logits, status, dev, st);
+  return run_scores(p, logits, status, dev, st, 0, S);
 }
 
 int dsa_indexer_check(void *workspace, void *cuda_stream) {

@@ -77,16 +77,19 @@ constexpr int kDecChunkTiles = 4;   // decode: key tiles per work item
 // (= DSA_MAX_TOPK).
 #define DSA_SEL_MAX_EPT 32
 
-// Launchers (return cudaSuccess or the launch error).  `logits` is
-// [B, S, S_kv] fp32; only visible entries are written.
+// Launchers (return cudaSuccess or the launch error).  The scoring and
+// selection launches cover query rows [s0, s0 + Sc) of every sequence;
+// `logits` is [B, Sc, S_kv] fp32 for those rows (only visible entries are
+// written), the outputs are the full [B, S, topk].
 cudaError_t launch_index_scores(const Problem &p, const CUtensorMap &tm_q,
                                 const CUtensorMap &tm_k, float *logits,
-                                int *status, int num_sms, cudaStream_t st);
+                                int *status, int num_sms, cudaStream_t st,
+                                int s0, int Sc);
 size_t index_scores_smem_bytes(int H, int D);
 
 cudaError_t launch_topk_select(const Problem &p, const float *logits, int topk,
                                int32_t *out_idx, float *out_scores,
-                               int num_sms, cudaStream_t st);
+                               int num_sms, cudaStream_t st, int s0, int Sc);
 size_t topk_select_smem_bytes(int S_kv, int topk);
 
 // Given indices, scores read from written logits (any H).

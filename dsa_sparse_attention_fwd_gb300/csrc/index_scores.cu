@@ -54,8 +54,9 @@ struct ItemInfo {
   int b, t0, ntiles;
 };
 
+// Rows [s0, s0 + S) of every sequence (one chunk of the query rows).
 template <int H>
-__device__ __forceinline__ ItemInfo item_info(int item, int S, int B,
+__device__ __forceinline__ ItemInfo item_info(int item, int s0, int S, int B,
                                               int S_kv, int ratio,
                                               const int32_t *q_pos) {
   constexpr int TQ = kTileCols / H;
@@ -63,8 +64,8 @@ __device__ __forceinline__ ItemInfo item_info(int item, int S, int B,
   ItemInfo it;
   const int qb = n_qb - 1 - item / B;  // longest (latest) query blocks first
   it.b = item % B;
-  it.t0 = qb * TQ;
-  const int t_last = min(it.t0 + TQ - 1, S - 1);
+  it.t0 = s0 + qb * TQ;
+  const int t_last = min(it.t0 + TQ - 1, s0 + S - 1);
   const int nv = n_visible(row_pos(q_pos, it.b, t_last), ratio, S_kv);
   it.ntiles = (nv + kTileKeys - 1) / kTileKeys;
   return it;
@@ -85,7 +86,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                         const float *__restrict__ w,
                         const int32_t *__restrict__ q_pos,
                         const uint8_t *__restrict__ kv_valid,
-                        float *__restrict__ logits, int S, int B,
+                        float *__restrict__ logits, int s0, int S, int B,
                         int S_kv, int ratio, int *status) {
   using L = ScoreSmem<H, KC>;
   constexpr int NQ = L::kQSlots;
@@ -152,7 +153,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       for (int r = 0; ok; ++r) {
         const int item = item_for(r, n_items);
         if (item < 0) break;
-        const ItemInfo it = item_info<H>(item, S, B, S_kv, ratio, q_pos);
+        const ItemInfo it = item_info<H>(item, s0, S, B, S_kv, ratio, q_pos);
         if (it.ntiles == 0) continue;
         const int qs = nq % NQ;
         const uint32_t qph = (nq / NQ) & 1u;
@@ -184,7 +185,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       for (int r = 0; ok; ++r) {
         const int item = item_for(r, n_items);
         if (item < 0) break;
-        const ItemInfo it = item_info<H>(item, S, B, S_kv, ratio, q_pos);
+        const ItemInfo it = item_info<H>(item, s0, S, B, S_kv, ratio, q_pos);
         if (it.ntiles == 0) continue;
         const int qs = nq % NQ;
         const uint32_t qph = (nq / NQ) & 1u;
@@ -231,14 +232,15 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     const int tq_mine = et / H, h_mine = et % H;  // the weight this thread loads
     auto weight_of = [&](const ItemInfo &it) -> float {
       const int t = it.t0 + tq_mine;
-      return t < S ? __ldg(w + ((size_t)t * B + it.b) * H + h_mine) : 0.f;
+      return t < s0 + S ? __ldg(w + ((size_t)t * B + it.b) * H + h_mine)
+                        : 0.f;
     };
     // first item with work at or after round r (ntiles = -1: none)
     auto next_item = [&](int r, int &round) -> ItemInfo {
       for (;; ++r) {
         const int item = item_for(r, n_items);
         if (item < 0) break;
-        const ItemInfo it = item_info<H>(item, S, B, S_kv, ratio, q_pos);
+        const ItemInfo it = item_info<H>(item, s0, S, B, S_kv, ratio, q_pos);
         if (it.ntiles > 0) {
           round = r;
           return it;
@@ -342,9 +344,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           }
           const int t = it.t0 + tq;
           const bool vis = (long long)(j + 1) * ratio - 1 <= qbase + t;
-          if (t < S && vis && j < S_kv) {
+          if (t < s0 + S && vis && j < S_kv) {
             const float sv = kv_ok ? score : -__int_as_float(0x7f800000);
-            logits[((size_t)it.b * S + t) * S_kv + j] = sv;
+            logits[((size_t)it.b * S + (t - s0)) * S_kv + j] = sv;
           }
         }
         acc ^= 1u;
@@ -366,18 +368,18 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 template <int H, int KC, bool KV>
 cudaError_t launch_h(const Problem &p, const CUtensorMap &tm_q,
                      const CUtensorMap &tm_k, float *logits, int *status,
-                     int num_sms, cudaStream_t st) {
+                     int num_sms, cudaStream_t st, int s0, int Sc) {
   constexpr int TQ = kTileCols / H;
   auto kern = index_scores_kernel<H, KC, KV>;
   const int smem = ScoreSmem<H, KC>::kAlloc;
   cudaError_t e = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const long long n_items = (long long)((p.S + TQ - 1) / TQ) * p.B;
+  const long long n_items = (long long)((Sc + TQ - 1) / TQ) * p.B;
   const int grid = (int)(n_items < num_sms ? n_items : num_sms);
   if (grid <= 0) return cudaSuccess;
   kern<<<grid, kScoreThreads, smem, st>>>(tm_q, tm_k, p.w, p.q_pos,
-                                          p.kv_valid, logits, p.S, p.B,
+                                          p.kv_valid, logits, s0, Sc, p.B,
                                           p.S_kv, p.ratio, status);
   return cudaGetLastError();
 }
@@ -385,30 +387,30 @@ cudaError_t launch_h(const Problem &p, const CUtensorMap &tm_q,
 template <int H, int KC>
 cudaError_t launch_t(const Problem &p, const CUtensorMap &tm_q,
                      const CUtensorMap &tm_k, float *logits, int *status,
-                     int num_sms, cudaStream_t st) {
+                     int num_sms, cudaStream_t st, int s0, int Sc) {
   return p.kv_valid ? launch_h<H, KC, true>(p, tm_q, tm_k, logits, status,
-                                            num_sms, st)
+                                            num_sms, st, s0, Sc)
                     : launch_h<H, KC, false>(p, tm_q, tm_k, logits, status,
-                                             num_sms, st);
+                                             num_sms, st, s0, Sc);
 }
 
 template <int KC>
 cudaError_t launch_kc(const Problem &p, const CUtensorMap &tm_q,
                       const CUtensorMap &tm_k, float *logits, int *status,
-                      int num_sms, cudaStream_t st) {
+                      int num_sms, cudaStream_t st, int s0, int Sc) {
   switch (p.H) {
-    case 1: return launch_t<1, KC>(p, tm_q, tm_k, logits, status, num_sms, st);
-    case 2: return launch_t<2, KC>(p, tm_q, tm_k, logits, status, num_sms, st);
-    case 4: return launch_t<4, KC>(p, tm_q, tm_k, logits, status, num_sms, st);
-    case 8: return launch_t<8, KC>(p, tm_q, tm_k, logits, status, num_sms, st);
+    case 1: return launch_t<1, KC>(p, tm_q, tm_k, logits, status, num_sms, st, s0, Sc);
+    case 2: return launch_t<2, KC>(p, tm_q, tm_k, logits, status, num_sms, st, s0, Sc);
+    case 4: return launch_t<4, KC>(p, tm_q, tm_k, logits, status, num_sms, st, s0, Sc);
+    case 8: return launch_t<8, KC>(p, tm_q, tm_k, logits, status, num_sms, st, s0, Sc);
     case 16:
-      return launch_t<16, KC>(p, tm_q, tm_k, logits, status, num_sms, st);
+      return launch_t<16, KC>(p, tm_q, tm_k, logits, status, num_sms, st, s0, Sc);
     case 32:
-      return launch_t<32, KC>(p, tm_q, tm_k, logits, status, num_sms, st);
+      return launch_t<32, KC>(p, tm_q, tm_k, logits, status, num_sms, st, s0, Sc);
     case 64:
-      return launch_t<64, KC>(p, tm_q, tm_k, logits, status, num_sms, st);
+      return launch_t<64, KC>(p, tm_q, tm_k, logits, status, num_sms, st, s0, Sc);
     case 128:
-      return launch_t<128, KC>(p, tm_q, tm_k, logits, status, num_sms, st);
+      return launch_t<128, KC>(p, tm_q, tm_k, logits, status, num_sms, st, s0, Sc);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -428,10 +430,11 @@ size_t index_scores_smem_bytes(int H, int D) {
 
 cudaError_t launch_index_scores(const Problem &p, const CUtensorMap &tm_q,
                                 const CUtensorMap &tm_k, float *logits,
-                                int *status, int num_sms, cudaStream_t st) {
+                                int *status, int num_sms, cudaStream_t st,
+                                int s0, int Sc) {
   if (p.D <= kChunk)
-    return launch_kc<1>(p, tm_q, tm_k, logits, status, num_sms, st);
-  return launch_kc<2>(p, tm_q, tm_k, logits, status, num_sms, st);
+    return launch_kc<1>(p, tm_q, tm_k, logits, status, num_sms, st, s0, Sc);
+  return launch_kc<2>(p, tm_q, tm_k, logits, status, num_sms, st, s0, Sc);
 }
 
 }  // namespace dsa

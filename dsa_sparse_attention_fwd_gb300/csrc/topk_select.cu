@@ -635,9 +635,10 @@ __device__ __forceinline__ bool bucket_topk_reg(
 template <int EPT, int NT>
 __global__ void __launch_bounds__(NT, NT == kSelThreads ? 4 : 1)
     topk_select_kernel(const float *__restrict__ logits,
-                       const int32_t *__restrict__ q_pos, int S, int S_kv,
-                       int ratio, int topk, int mcap, int bcap, int keys_cap,
-                       int region_u32, int32_t *__restrict__ out_idx,
+                       const int32_t *__restrict__ q_pos, int s0, int S,
+                       int S_out, int S_kv, int ratio, int topk, int mcap,
+                       int bcap, int keys_cap, int region_u32,
+                       int32_t *__restrict__ out_idx,
                        float *__restrict__ out_scores) {
   // the logits come from the scoring kernel, which this launch may overlap
   // (programmatic dependent launch)
@@ -651,14 +652,16 @@ __global__ void __launch_bounds__(NT, NT == kSelThreads ? 4 : 1)
   if (threadIdx.x == 0)
     sh.whist = reinterpret_cast<uint32_t(*)[256]>(keys);
 
-  const int row = blockIdx.x;  // row id = b * S + s, the output order
-  const int b = row / S, s = row % S;
+  // this launch covers rows [s0, s0 + S) of every sequence; the logits hold
+  // just those rows, the outputs every row ([B, S_out, topk])
+  const int row = blockIdx.x;  // b * S + (s - s0)
+  const int b = row / S, s = s0 + row % S;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nv = n_visible(row_pos(q_pos, b, s), ratio, S_kv);
   const float *L = logits + (size_t)row * S_kv;
   const uint32_t lt = lanemask_lt();
-  int32_t *oi = out_idx + (size_t)row * topk;
-  float *os = out_scores + (size_t)row * topk;
+  int32_t *oi = out_idx + ((size_t)b * S_out + s) * topk;
+  float *os = out_scores + ((size_t)b * S_out + s) * topk;
 
   // the bucket route first; the radix route takes the rows it declines
   if (topk <= kBucketMaxTopk) {
@@ -977,19 +980,20 @@ SelLayout sel_layout(int S_kv, int topk, bool unstaged, int threads) {
 // Rows longer than 4096 keys (past the register route) skip the
 // shared-memory copy when there are enough rows that more CTAs per SM pay
 // off; a few rows (decode) keep it, so their passes stay in shared memory.
-bool unstaged_rows(const Problem &p) {
-  return p.S_kv > 4096 && (long long)p.B * p.S >= 2048;
+bool unstaged_rows(const Problem &p, int rows_per_seq) {
+  return p.S_kv > 4096 && (long long)p.B * rows_per_seq >= 2048;
 }
 
 template <int EPT, int NT>
 cudaError_t launch_sel(const Problem &p, const float *logits, int topk,
-                       int32_t *out_idx, float *out_scores, cudaStream_t st) {
-  const SelLayout l = sel_layout(p.S_kv, topk, unstaged_rows(p), NT);
+                       int32_t *out_idx, float *out_scores, cudaStream_t st,
+                       int s0, int Sc) {
+  const SelLayout l = sel_layout(p.S_kv, topk, unstaged_rows(p, Sc), NT);
   auto kern = topk_select_kernel<EPT, NT>;
   cudaError_t e = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)l.dyn);
   if (e != cudaSuccess) return e;
-  const long long rows = (long long)p.B * p.S;
+  const long long rows = (long long)p.B * Sc;
   // launched with programmatic stream serialization: the CTAs are queued
   // while the scoring kernel runs and wait for it inside the kernel
   cudaLaunchConfig_t cfg = {};
@@ -1002,7 +1006,7 @@ cudaError_t launch_sel(const Problem &p, const float *logits, int topk,
   attr.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, logits, p.q_pos, p.S,
+  return cudaLaunchKernelEx(&cfg, kern, logits, p.q_pos, s0, Sc, p.S,
                             p.S_kv, p.ratio, topk, l.mcap, l.bcap, l.keys_cap,
                             l.region_u32, out_idx, out_scores);
 }
@@ -1019,24 +1023,24 @@ constexpr size_t kWideSmemCap = 160 * 1024;
 
 cudaError_t launch_topk_select(const Problem &p, const float *logits, int topk,
                                int32_t *out_idx, float *out_scores,
-                               int num_sms, cudaStream_t st) {
-  const bool unstaged = unstaged_rows(p);
+                               int num_sms, cudaStream_t st, int s0, int Sc) {
+  const bool unstaged = unstaged_rows(p, Sc);
   const int mcap = sel_layout(p.S_kv, topk, unstaged, kSelThreads).mcap;
   // Fewer rows than SMs: each row gets 1024 threads, so a row's passes
   // take a quarter of the iterations (the rows run side by side anyway).
-  const long long rows = (long long)p.B * p.S;
+  const long long rows = (long long)p.B * Sc;
   if (rows < num_sms && mcap <= kSelThreadsWide * 4 &&
       sel_layout(p.S_kv, topk, unstaged, kSelThreadsWide).dyn <= kWideSmemCap)
     return launch_sel<4, kSelThreadsWide>(p, logits, topk, out_idx,
-                                          out_scores, st);
+                                          out_scores, st, s0, Sc);
   if (mcap <= kSelThreads * 8)
     return launch_sel<8, kSelThreads>(p, logits, topk, out_idx,
-                                      out_scores, st);
+                                      out_scores, st, s0, Sc);
   if (mcap <= kSelThreads * 16)
     return launch_sel<16, kSelThreads>(p, logits, topk, out_idx,
-                                       out_scores, st);
+                                       out_scores, st, s0, Sc);
   return launch_sel<DSA_SEL_MAX_EPT + 2, kSelThreads>(
-      p, logits, topk, out_idx, out_scores, st);
+      p, logits, topk, out_idx, out_scores, st, s0, Sc);
 }
 
 cudaError_t launch_gather_logits(const Problem &p, const float *logits,

@@ -79,15 +79,53 @@ typedef enum dsa_status {
  * Bytes of device workspace dsa_indexer_fwd() needs for this shape
  * (has_in_idx != 0 selects the given-indices path).  Returns 0 when the
  * shape is invalid.  The workspace starts with a 256-byte status header.
- * Top-k path: the header is followed by the fp32 logits [B, S, S_kv] of the
- * visible keys.
+ * Top-k path, one kernel (scores and selection in the same kernel, chosen by
+ * the prefill policy below): the header is followed by the kernel's per-CTA
+ * scratch, 160 x 2 x (256 / H) x S_kv (rounded up to 32) fp32, whatever S.
+ * Top-k path, two kernels: the header is followed by the fp32 logits of one
+ * chunk of query rows, [B, rows, S_kv] with B * rows * S_kv * 4 <= 64 MiB
+ * (all S rows when they fit, else a multiple of 256 / H rows, at least one
+ * scoring tile), whatever S.
  * Given-indices path: H in {16, 32, 64, 128} scores the gathered keys
  * directly and needs the header only; other H take the header plus the
- * logits.
+ * full logits [B, S, S_kv].
+ * The result depends on the prefill policy in force when it is called.
  */
 DSA_API size_t dsa_indexer_workspace_size(int S, int B, int H, int D,
                                           int S_kv, int compress_ratio,
                                           int topk, int has_in_idx);
+
+/*
+ * Prefill top-k path policy (process-wide; the default is
+ * DSA_PREFILL_AUTO).  Both paths give the same indices and scores.
+ *   DSA_PREFILL_AUTO        the one-kernel forward for rows of at least 8192
+ *                           compressed keys (S_kv >= 8192), where its
+ *                           selection keeps pace with the scoring; the
+ *                           two-kernel forward (scores, then selection, one
+ *                           L2-sized chunk of query rows at a time) below.
+ *   DSA_PREFILL_ONE_KERNEL  the one-kernel forward whenever the shape fits it
+ *                           (H in {32, 64, 128}, S >= 256 / H, topk <= 2048,
+ *                           S_kv < 2^20).
+ *   DSA_PREFILL_TWO_KERNELS always the two-kernel forward.
+ * Decode-shaped rows (S < 256 / H) always take the split-over-keys decode
+ * kernel and the selection kernel.  Set the policy before sizing a
+ * workspace: the size depends on it.  Returns DSA_OK or
+ * DSA_ERR_INVALID_ARG.
+ */
+#define DSA_PREFILL_AUTO 0
+#define DSA_PREFILL_ONE_KERNEL 1
+#define DSA_PREFILL_TWO_KERNELS 2
+DSA_API int dsa_set_prefill_policy(int policy);
+
+/*
+ * Number of kernels dsa_indexer_fwd() launches for this shape under the
+ * current policy (1 for the one-kernel forward and the direct given-indices
+ * path; 2 per chunk of query rows for the two-kernel forward); 0 for an
+ * invalid shape.  dsa_indexer_fwd_profiled() records one event after each.
+ */
+DSA_API int dsa_indexer_fwd_launches(int S, int B, int H, int D, int S_kv,
+                                     int compress_ratio, int topk,
+                                     int has_in_idx);
 
 /*
  * The indexer forward (v4_lighting_indexer / V4IndexerFunction.forward).
@@ -207,11 +245,14 @@ DSA_API int dsa_indexer_fwd_host(const void *q, const void *k, const float *w,
                                  void *cuda_stream);
 
 /*
- * dsa_indexer_fwd() with stage timing: `stage_events` holds `n_events` (0..3)
- * caller-created cudaEvent_t handles, recorded on `cuda_stream` before the
- * scoring kernel (0), after it (1) and after the selection or gather kernel
- * (2).  Events past n_events are not recorded.  Same work, outputs and
- * errors as dsa_indexer_fwd() (plus DSA_ERR_INVALID_ARG for a NULL event).
+ * dsa_indexer_fwd() with stage timing: `stage_events` holds `n_events`
+ * (0..1024) caller-created cudaEvent_t handles, recorded on `cuda_stream`:
+ * event 0 before the first kernel, then one event after each kernel launch
+ * in launch order (dsa_indexer_fwd_launches() of them: scores and selection
+ * alternate for the two-kernel forward, chunk by chunk); events past the
+ * last launch are recorded after it, events past n_events not at all.  Same
+ * work, outputs and errors as dsa_indexer_fwd() (plus DSA_ERR_INVALID_ARG
+ * for a NULL event or n_events outside 0..1024).
  */
 DSA_API int dsa_indexer_fwd_profiled(const void *q, const void *k,
                                      const float *w, int S, int B, int H,

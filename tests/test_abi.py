@@ -33,6 +33,10 @@ def lib():
     L.dsa_indexer_logits.argtypes = [P, P, P, I, I, I, I, I, I, P, P, P, Z, P]
     L.dsa_indexer_workspace_size.restype = Z
     L.dsa_indexer_workspace_size.argtypes = [I] * 8
+    L.dsa_set_prefill_policy.restype = I
+    L.dsa_set_prefill_policy.argtypes = [I]
+    L.dsa_indexer_fwd_launches.restype = I
+    L.dsa_indexer_fwd_launches.argtypes = [I] * 8
     L.dsa_indexer_logits_workspace_size.restype = Z
     L.dsa_status_string.restype = ctypes.c_char_p
     L.dsa_status_string.argtypes = [I]
@@ -87,7 +91,8 @@ def test_header_declares_entry_points():
     names = declared_functions()
     for n in ("dsa_indexer_fwd", "dsa_indexer_workspace_size",
               "dsa_status_string", "dsa_indexer_check", "dsa_indexer_logits",
-              "dsa_indexer_fwd_profiled"):
+              "dsa_indexer_fwd_profiled", "dsa_set_prefill_policy",
+              "dsa_indexer_fwd_launches"):
         assert n in names
 
 
@@ -114,23 +119,46 @@ def test_status_strings(lib):
 
 def test_workspace_size(lib):
     ws = lib.dsa_indexer_workspace_size
-    # prefill top-k path with H in {32, 64, 128} and topk <= 2048: scores
-    # and selection in one kernel; the status header, then the kernel's
-    # per-CTA scratch (160 CTAs x 2 item slots x 256/H rows x S_kv rounded up
-    # to 32, fp32), whatever the number of query rows
+    # one-kernel prefill (scores and selection in the same kernel): the
+    # status header, then the kernel's per-CTA scratch (160 CTAs x 2 item
+    # slots x 256/H rows x S_kv rounded up to 32, fp32), whatever S
     fused = lambda H, S_kv: 256 + 160 * 2 * (256 // H) * (
         (S_kv + 31) // 32 * 32) * 4
-    assert ws(4096, 1, 64, 128, 4096, 1, 2048, 0) == fused(64, 4096)
-    assert ws(16384, 2, 64, 128, 4096, 4, 512, 0) == fused(64, 4096)
+    # two-kernel top-k path: the status header, then the logits of one chunk
+    # of query rows (all rows when B*S*S_kv*4 <= 64 MiB, else the most whole
+    # scoring tiles of 256/H rows that fit), whatever S
+    def chunked(S, B, H, S_kv):
+        per_row = B * S_kv * 4
+        if S * per_row <= 64 << 20:
+            return 256 + S * per_row
+        tq = 256 // H
+        rows = max(tq, (64 << 20) // per_row // tq * tq)
+        return 256 + min(rows, S) * per_row
+    # default policy: one kernel for rows of at least 8192 keys
     assert ws(65536, 1, 64, 128, 16384, 4, 2048, 0) == fused(64, 16384)
     assert ws(8192, 1, 32, 128, 8192, 1, 2048, 0) == fused(32, 8192)
-    assert ws(40, 1, 128, 128, 40, 1, 7, 0) == fused(128, 40)
-    assert ws(8, 1, 64, 64, 1000, 1, 100, 0) == fused(64, 1000)
-    # other shapes: the status header, then the fp32 logits of every row
-    assert ws(8192, 1, 64, 128, 8192, 1, 4096, 0) == 256 + 8192 * 8192 * 4
+    assert ws(4096, 1, 64, 128, 4096, 1, 2048, 0) == chunked(4096, 1, 64, 4096)
+    assert ws(4096, 1, 64, 128, 4096, 1, 2048, 0) == 256 + (64 << 20)
+    assert ws(16384, 2, 64, 128, 4096, 4, 512, 0) == 256 + 2 * 2048 * 4096 * 4
+    assert ws(40, 1, 128, 128, 40, 1, 7, 0) == chunked(40, 1, 128, 40)
+    # shapes the one-kernel forward does not take: chunked logits
+    assert ws(8192, 1, 64, 128, 8192, 1, 4096, 0) == chunked(8192, 1, 64, 8192)
     assert ws(64, 1, 16, 64, 64, 1, 8, 0) == 256 + 64 * 64 * 4
     assert ws(1, 64, 32, 64, 8192, 4, 512, 0) == 256 + 64 * 8192 * 4  # decode
     assert ws(3, 2, 64, 128, 500, 1, 16, 0) == 256 + 2 * 3 * 500 * 4
+    # forced policies
+    try:
+        assert lib.dsa_set_prefill_policy(1) == 0
+        assert ws(4096, 1, 64, 128, 4096, 1, 2048, 0) == fused(64, 4096)
+        assert ws(16384, 2, 64, 128, 4096, 4, 512, 0) == fused(64, 4096)
+        assert ws(8, 1, 64, 64, 1000, 1, 100, 0) == fused(64, 1000)
+        assert ws(64, 1, 16, 64, 64, 1, 8, 0) == 256 + 64 * 64 * 4  # H = 16
+        assert lib.dsa_set_prefill_policy(2) == 0
+        assert ws(65536, 1, 64, 128, 16384, 4, 2048, 0) == chunked(
+            65536, 1, 64, 16384)
+        assert lib.dsa_set_prefill_policy(3) == 1  # DSA_ERR_INVALID_ARG
+    finally:
+        assert lib.dsa_set_prefill_policy(0) == 0
     # given indices: H in {16, 32, 64, 128} gathers keys (status header
     # only); other H read the scores back from logits
     assert ws(65536, 1, 64, 128, 16384, 4, 2048, 1) == 256
@@ -205,6 +233,17 @@ def test_python_binding_fails_loudly_without_library(tmp_path):
         m._lib = saved
 
 
+def test_launch_counts(lib):
+    n = lib.dsa_indexer_fwd_launches
+    assert n(65536, 1, 64, 128, 16384, 4, 2048, 0) == 1   # one kernel
+    assert n(4096, 1, 64, 128, 4096, 1, 2048, 0) == 2     # one chunk
+    assert n(16384, 2, 64, 128, 4096, 4, 512, 0) == 16    # 8 chunks x 2
+    assert n(65536, 1, 64, 128, 16384, 4, 2048, 1) == 1   # gathered keys
+    assert n(64, 1, 4, 32, 64, 1, 8, 1) == 2              # logits + gather
+    assert n(1, 64, 64, 128, 8192, 4, 512, 0) == 2        # decode
+    assert n(0, 1, 64, 128, 4096, 1, 2048, 0) == 0
+
+
 def test_host_buffer_size(lib):
     hb = lib.dsa_indexer_host_buffer_size
     ws = lib.dsa_indexer_workspace_size
@@ -216,16 +255,11 @@ def test_host_buffer_size(lib):
     inputs = S_kv * B * D * 2 + S * B * H * D * 2 + S * B * H * 4
     assert need >= inputs + 2 * B * S * k * 4 + ws(S, B, H, D, S_kv, 1, k, 0)
     # eight chunks of 512 rows: the workspace is one chunk's, not the call's
-    # (H = 16 writes logits, whose size grows with the rows)
     big = hb(4096, 1, 16, 128, 4096, 1, 2048, 0)
     assert big < (4096 * 16 * 128 * 2 + 2 * 4096 * 2048 * 4
                   + ws(4096, 1, 16, 128, 4096, 1, 2048, 0))
     assert big >= 4096 * 16 * 128 * 2 + 2 * 4096 * 2048 * 4 + ws(
         512, 1, 16, 128, 4096, 1, 2048, 0)
-    # the one-kernel prefill's scratch does not grow with the rows at all
-    f = hb(4096, 1, 64, 128, 4096, 1, 2048, 0)
-    assert f >= 4096 * 64 * 128 * 2 + 2 * 4096 * 2048 * 4 + ws(
-        4096, 1, 64, 128, 4096, 1, 2048, 0)
 
 
 def test_host_fwd_rejects_bad_arguments(lib):

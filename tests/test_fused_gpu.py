@@ -1,6 +1,7 @@
 """GPU parity of the one-kernel prefill forward (scores and top-k in the
 same kernel, the scores never written to device memory) and of the routes
-its selection takes, against the CPU oracle.
+its selection takes, against the CPU oracle; the one-kernel forward is
+forced here wherever the shape fits it.
 
 Every row is compared with tests.helpers.compare_topk_row: scores slot by
 slot within |g - o| <= 1e-3 + 2e-3 |o|, each returned score the oracle score
@@ -32,10 +33,15 @@ pytestmark = pytest.mark.gpu
 
 @pytest.fixture(scope="module")
 def dsa():
+    """The library with the one-kernel prefill forced wherever the shape fits
+    it (the default policy keeps it for rows of at least 8192 keys); the
+    default is restored afterwards."""
     import dsa_sparse_attention_fwd_gb300 as m
     m.build()
     m.load_library()
-    return m
+    m.dsa_set_prefill_policy(m.PREFILL_ONE_KERNEL)
+    yield m
+    m.dsa_set_prefill_policy(m.PREFILL_AUTO)
 
 
 def run_and_compare(dsa, q, k, w, ratio, topk, q_pos=None, exact=False):
@@ -194,3 +200,89 @@ def test_fused_matches_written_logits_path(dsa):
         assert idx[r, :kk].tolist() == order, r
         assert torch.equal(sc[r, :kk], row[order]), r
         assert bool((idx[r, kk:] == -1).all())
+
+
+@pytest.mark.parametrize("name,per_batch", [("v32_prefill", 24),
+                                            ("c4_prefill", 12)])
+def test_fused_full_size_sampled(dsa, name, per_batch):
+    """The 4096 x 4096 and C4 prefills through the one-kernel forward (the
+    default policy gives them the two-kernel forward), sampled rows against
+    the oracle."""
+    from dsa_inputs import WORKLOADS
+    wl = WORKLOADS[name]
+    q, k, w, _ = make_inputs(wl)
+    dev = torch.device("cuda")
+    sc, idx, ws = dsa.dsa_indexer_fwd(q.to(dev), k.to(dev), w.to(dev),
+                                      wl.compress_ratio, wl.topk)
+    assert dsa.dsa_indexer_check(ws) == 0
+    sc = sc.cpu().numpy().reshape(wl.B * wl.S, wl.topk)
+    idx = idx.cpu().numpy().reshape(wl.B * wl.S, wl.topk)
+    rng = np.random.default_rng(1)
+    rows = np.unique(np.concatenate([
+        [0, 1, wl.S - 1, wl.B * wl.S - 1],
+        rng.integers(0, wl.B * wl.S, size=per_batch * wl.B)])).astype(np.int64)
+    ref = oracle.indexer_fwd(q, k, w, wl.compress_ratio, wl.topk, rows=rows,
+                             want_logits=True)
+    for n, r in enumerate(rows):
+        msg = compare_topk_row(idx[r], sc[r], ref["idx"][n],
+                               ref["scores64"][n], ref["next"][n],
+                               ref["logits"][n])
+        assert msg is None, (int(r), msg)
+
+
+def test_one_and_two_kernel_paths_agree(dsa):
+    """The same problem through both prefill paths: identical indices, and
+    scores equal (both take the same tensor-core products and the same
+    epilogue arithmetic)."""
+    wl = Workload("t", B=2, S=700, S_kv=2500, H=64, D=128, compress_ratio=4,
+                  topk=256, w_scale=0.125, seed=21)
+    q, k, w, _ = make_inputs(wl)
+    dev = torch.device("cuda")
+    outs = []
+    for pol in (dsa.PREFILL_ONE_KERNEL, dsa.PREFILL_TWO_KERNELS):
+        dsa.dsa_set_prefill_policy(pol)
+        sc, idx, ws = dsa.dsa_indexer_fwd(q.to(dev), k.to(dev), w.to(dev),
+                                          4, 256)
+        assert dsa.dsa_indexer_check(ws) == 0
+        outs.append((sc.cpu(), idx.cpu()))
+    dsa.dsa_set_prefill_policy(dsa.PREFILL_ONE_KERNEL)
+    assert torch.equal(outs[0][1], outs[1][1])
+    assert torch.equal(outs[0][0], outs[1][0])
+
+
+def test_two_kernel_path_in_several_chunks(dsa):
+    """More query rows than one 64 MiB logits chunk holds: the two-kernel
+    forward scores and selects chunk after chunk; rows on both sides of each
+    chunk boundary are compared with the oracle, every row's invariants
+    checked."""
+    wl = Workload("t", B=2, S=2600, S_kv=4096, H=64, D=128, compress_ratio=1,
+                  topk=64, w_scale=0.125, seed=33)
+    q, k, w, _ = make_inputs(wl)
+    assert dsa.dsa_indexer_fwd_launches(wl.S, wl.B, wl.H, wl.D, wl.S_kv, 1,
+                                        wl.topk) == 1  # one kernel (forced)
+    dsa.dsa_set_prefill_policy(dsa.PREFILL_TWO_KERNELS)
+    try:
+        # 2 x 4096 x 4 bytes per row: 2048 rows per chunk, two chunks
+        assert dsa.dsa_indexer_fwd_launches(wl.S, wl.B, wl.H, wl.D, wl.S_kv,
+                                            1, wl.topk) == 4
+        dev = torch.device("cuda")
+        sc, idx, ws = dsa.dsa_indexer_fwd(q.to(dev), k.to(dev), w.to(dev), 1,
+                                          wl.topk)
+        assert dsa.dsa_indexer_check(ws) == 0
+    finally:
+        dsa.dsa_set_prefill_policy(dsa.PREFILL_ONE_KERNEL)
+    sc = sc.cpu().numpy().reshape(wl.B * wl.S, wl.topk)
+    idx = idx.cpu().numpy().reshape(wl.B * wl.S, wl.topk)
+    nv = np.minimum(np.arange(wl.S) + 1, wl.S_kv)
+    for b in range(wl.B):
+        rb = slice(b * wl.S, (b + 1) * wl.S)
+        kept = np.minimum(nv, wl.topk)
+        assert np.array_equal((idx[rb] >= 0).sum(-1), kept)
+    rows = np.array([0, 1, 2047, 2048, 2049, 2599, 2600, 2600 + 2047,
+                     2600 + 2048, 5199], dtype=np.int64)
+    ref = oracle.indexer_fwd(q, k, w, 1, wl.topk, rows=rows, want_logits=True)
+    for n, r in enumerate(rows):
+        msg = compare_topk_row(idx[r], sc[r], ref["idx"][n],
+                               ref["scores64"][n], ref["next"][n],
+                               ref["logits"][n])
+        assert msg is None, (int(r), msg)

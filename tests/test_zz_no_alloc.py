@@ -190,9 +190,10 @@ def test_refuses_problems_beyond_the_fixed_scratch(lib):
         fake, fake, fake, wl.S, wl.B, wl.H, wl.D, wl.S_kv, wl.compress_ratio,
         wl.topk, None, None, fake, fake, None, None)
     assert rc == UNSUPPORTED
-    # with 16 heads the forward writes [S, S_kv] fp32 logits: 4096 query
-    # rows over 4096 keys fill the 64 MiB exactly, one row more is refused
+    # given indices with 4 heads read the scores back from the full [S, S_kv]
+    # fp32 logits: 4096 query rows over 4096 keys fill the 64 MiB exactly,
+    # one row more is refused
     rc = lib.dsa_indexer_fwd_static_scratch(
-        fake, fake, fake, 4097, 1, 16, 128, 4096, 1, 2048, None, None, fake,
+        fake, fake, fake, 4097, 1, 4, 32, 4096, 1, 16, None, fake, fake,
         fake, None, None)
     assert rc == UNSUPPORTED
