@@ -62,6 +62,13 @@ WORKLOADS = {
     "long_c4": Workload("long_c4", B=1, S=65536, S_kv=16384, H=64, D=128,
                         compress_ratio=4, topk=2048, w_scale=0.125, seed=4,
                         idx_seed=5),
+    # the last 12288 query rows of the long-context prefill (positions
+    # 53248..65535, 13312..16384 visible keys each): a profiling slice of
+    # the same kernels at a fifth of the size (q is 192 MiB, past L2)
+    "long_c4_tail": Workload("long_c4_tail", B=1, S=12288, S_kv=16384, H=64,
+                             D=128, compress_ratio=4, topk=2048,
+                             w_scale=0.125, seed=7,
+                             pos_range=(53248, 53248), idx_seed=8),
 }
 
 

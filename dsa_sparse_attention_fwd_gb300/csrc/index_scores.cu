@@ -141,6 +141,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  // launched behind the previous chunk's selection, which still reads the
+  // logits buffer: wait for it before anything is written (the setup above
+  // overlapped its tail)
+  pdl_wait();
   // the selection kernel may be scheduled now; it waits for this grid to
   // finish before it reads anything
   pdl_allow_dependents();
@@ -148,6 +152,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
+      // q is read once: keep it from pushing the logits out of L2
+      const uint64_t pol_q = l2_policy_evict_first();
       uint32_t kst = 0, kph = 0, nq = 0;
       bool ok = true;
       for (int r = 0; ok; ++r) {
@@ -161,8 +167,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         if (!(ok = wait_bar(q_empty(qs), qph ^ 1u, abort_flag, status))) break;
         mbar_arrive_expect_tx(q_full(qs), L::kQBytes);
         for (int c = 0; c < KC; ++c)
-          tma_load_4d(sQ + qs * L::kQBytes + c * (kTileCols * 128), &tm_q,
-                      q_full(qs), c * kChunk, 0, it.b, it.t0);
+          tma_load_4d_hint(sQ + qs * L::kQBytes + c * (kTileCols * 128),
+                           &tm_q, q_full(qs), c * kChunk, 0, it.b, it.t0,
+                           pol_q);
         for (int tile = 0; tile < it.ntiles; ++tile) {
           if (!(ok = wait_bar(k_empty(kst), kph ^ 1u, abort_flag, status)))
             break;
@@ -378,10 +385,20 @@ cudaError_t launch_h(const Problem &p, const CUtensorMap &tm_q,
   const long long n_items = (long long)((Sc + TQ - 1) / TQ) * p.B;
   const int grid = (int)(n_items < num_sms ? n_items : num_sms);
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, kScoreThreads, smem, st>>>(tm_q, tm_k, p.w, p.q_pos,
-                                          p.kv_valid, logits, s0, Sc, p.B,
-                                          p.S_kv, p.ratio, status);
-  return cudaGetLastError();
+  // programmatic stream serialization: the CTAs may start while the
+  // previous kernel (a selection) drains, and wait for it in the kernel
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kScoreThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tm_q, tm_k, p.w, p.q_pos, p.kv_valid,
+                            logits, s0, Sc, p.B, p.S_kv, p.ratio, status);
 }
 
 template <int H, int KC>

@@ -223,8 +223,8 @@ __device__ __forceinline__ void write_padding(int from, int topk, int st,
                                               int32_t *oi, float *os) {
   const float neg_inf = -__int_as_float(0x7f800000);
   for (int i = from + st; i < topk; i += kSelT) {
-    oi[i] = -1;
-    os[i] = neg_inf;
+    __stcs(oi + i, -1);
+    __stcs(os + i, neg_inf);
   }
 }
 
@@ -351,11 +351,11 @@ __device__ __noinline__ void select_exact(const float *R, int n, int topk,
     if (i < want) {
       const uint64_t e = grouped[i];
       const float v = key_to_float((uint32_t)(e >> 32));
-      oi[i] = v == neg_inf ? -1 : (int32_t)(0xffffffffu - (uint32_t)e);
-      os[i] = v;
+      __stcs(oi + i, v == neg_inf ? -1 : (int32_t)(0xffffffffu - (uint32_t)e));
+      __stcs(os + i, v);
     } else {
-      oi[i] = -1;
-      os[i] = neg_inf;
+      __stcs(oi + i, -1);
+      __stcs(os + i, neg_inf);
     }
   }
   sel_sync();
@@ -419,8 +419,8 @@ __device__ __forceinline__ void bucket_rank_write(int m, int topk, int st,
     int r = start;
     for (int q = start; q < end; ++q) r += grouped[q] > cv;
     if (r < topk) {
-      oi[r] = (int32_t)(0xfffffu - (lo32 & 0xfffffu));
-      os[r] = key_to_float((uint32_t)(cv >> 32));
+      __stcs(oi + r, (int32_t)(0xfffffu - (lo32 & 0xfffffu)));
+      __stcs(os + r, key_to_float((uint32_t)(cv >> 32)));
     }
   }
   write_padding(m, topk, st, oi, os);
@@ -619,6 +619,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
+      // q is read once: keep it from pushing the score scratch out of L2
+      const uint64_t pol_q = l2_policy_evict_first();
       uint32_t kst = 0, kph = 0, nq = 0;
       bool ok = true;
       for (int r = 0; ok; ++r) {
@@ -632,8 +634,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         if (!(ok = wait_bar(q_empty(qs), qph ^ 1u, abort_flag, status))) break;
         mbar_arrive_expect_tx(q_full(qs), L::kQBytes);
         for (int c = 0; c < KC; ++c)
-          tma_load_4d(sQ + qs * L::kQBytes + c * (kTileCols * 128), &tm_q,
-                      q_full(qs), c * kChunk, 0, it.b, it.t0);
+          tma_load_4d_hint(sQ + qs * L::kQBytes + c * (kTileCols * 128),
+                           &tm_q, q_full(qs), c * kChunk, 0, it.b, it.t0,
+                           pol_q);
         for (int tile = 0; tile < it.ntiles && ok; ++tile) {
           for (int c = 0; c < KC; ++c) {
             if (!(ok = wait_bar(k_empty(kst), kph ^ 1u, abort_flag, status)))
@@ -878,6 +881,17 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         select_row(srow + (size_t)tq * row_stride, nv, topk, lo, hi, bad, st,
                    bins, grouped, sm, out_idx + orow, out_scores + orow);
       }
+      // the slot's score rows are dead: drop their L2 lines instead of
+      // letting them be written back (rows start on 128-byte lines)
+      for (int tq = 0; tq < TQ; ++tq) {
+        const int t = it.t0 + tq;
+        if (t >= S) break;
+        const int nv = n_visible(row_pos(q_pos, it.b, t), ratio, S_kv);
+        const float *row = srow + (size_t)tq * row_stride;
+        for (int l = st; l < (nv + 31) / 32; l += kSelT)
+          discard_l2_line(row + 32 * l);
+      }
+      sel_sync();  // every read and discard of the slot precedes its reuse
       if (st == 0) mbar_arrive(slot_empty(slot));
       ++n_it;
     }
@@ -946,7 +960,9 @@ cudaError_t launch_kc(const Problem &p, const CUtensorMap &tm_q,
 
 }  // namespace
 
-int index_topk_row_stride(int S_kv) { return (S_kv + 31) / 32 * 32; }
+// Score rows start on 128-byte lines, and one line more than S_kv needs
+// keeps rows of power-of-two length from falling into the same L2 sets.
+int index_topk_row_stride(int S_kv) { return (S_kv + 31) / 32 * 32 + 32; }
 
 size_t index_topk_smem_bytes(int H, int D, int topk) {
   const bool k1 = D <= kChunk;

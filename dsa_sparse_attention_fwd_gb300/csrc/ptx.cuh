@@ -116,6 +116,50 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap,
       : "memory");
 }
 
+// tma_load_4d with an L2 cache policy (from l2_policy_*), e.g. evict-first
+// for data read once.
+__device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const void *tmap,
+                                                 uint32_t bar, int c0, int c1,
+                                                 int c2, int c3,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::"
+      "complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, %4, %5, %6}], [%2], "
+      "%7;" ::"r"(dst),
+      "l"(tmap), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(policy)
+      : "memory");
+}
+
+// L2 cache policies: evict-first (streamed, read once) and evict-last (kept
+// for a later read in the same kernel).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;"
+               : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;"
+               : "=l"(p));
+  return p;
+}
+
+// fp32 store with an L2 cache policy.
+__device__ __forceinline__ void st_global_hint(float *p, float v,
+                                               uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v),
+               "l"(policy)
+               : "memory");
+}
+
+// Drops the 128-byte L2 line at `p` (128-byte aligned) without writing it
+// back: for data that has been read for the last time.  Later reads of the
+// line are undefined until it is written again.
+__device__ __forceinline__ void discard_l2_line(const void *p) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
 // 4-byte asynchronous copy global -> shared (both 4-byte aligned).
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src)

@@ -38,6 +38,7 @@
 //      (heavily tied inputs), the candidates are rebuilt and sorted on all
 //      four digits instead.
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace dsa {
 namespace {
@@ -643,6 +644,9 @@ __global__ void __launch_bounds__(NT, NT == kSelThreads ? 4 : 1)
   // the logits come from the scoring kernel, which this launch may overlap
   // (programmatic dependent launch)
   pdl_wait();
+  // the next chunk's scoring kernel may be scheduled once every CTA of this
+  // grid has started; it waits for this grid to finish before it writes
+  pdl_allow_dependents();
   extern __shared__ __align__(16) uint8_t smem[];
   uint64_t *bufA = reinterpret_cast<uint64_t *>(smem);  // [mcap]
   uint64_t *bufB = bufA + mcap;                          // [bcap] (>= 4096 u32)
@@ -663,6 +667,8 @@ __global__ void __launch_bounds__(NT, NT == kSelThreads ? 4 : 1)
   int32_t *oi = out_idx + ((size_t)b * S_out + s) * topk;
   float *os = out_scores + ((size_t)b * S_out + s) * topk;
 
+  // (one pass of a do-while: the routes leave it when the row is done)
+  do {
   // the bucket route first; the radix route takes the rows it declines
   if (topk <= kBucketMaxTopk) {
     constexpr int R = kBucketBins / NT;  // keys per thread in registers
@@ -672,11 +678,11 @@ __global__ void __launch_bounds__(NT, NT == kSelThreads ? 4 : 1)
       if (bucket_topk_reg<NT, R>(L, nv, topk, vec,
                                  reinterpret_cast<uint32_t *>(bufB), bufA, sh,
                                  oi, os))
-        return;
+        break;
     } else if (bucket_topk<NT>(L, nv, topk, keys, region_u32,
                                reinterpret_cast<uint32_t *>(bufB), bufA, sh,
                                oi, os)) {
-      return;
+      break;
     }
   }
 
@@ -913,6 +919,19 @@ __global__ void __launch_bounds__(NT, NT == kSelThreads ? 4 : 1)
       oi[i] = -1;
       os[i] = -__int_as_float(0x7f800000);
     }
+  }
+  } while (0);
+
+  // the row's logits are dead: drop the L2 lines that lie wholly inside
+  // the row instead of letting them be written back
+  __syncthreads();
+  {
+    const uintptr_t r0 = reinterpret_cast<uintptr_t>(L);
+    const uintptr_t r1 = r0 + (uintptr_t)S_kv * sizeof(float);
+    const uintptr_t first = (r0 + 127) & ~(uintptr_t)127;
+    for (uintptr_t a = first + (uintptr_t)tid * 128; a + 128 <= r1;
+         a += (uintptr_t)NT * 128)
+      discard_l2_line(reinterpret_cast<const void *>(a));
   }
 }
 

@@ -81,7 +81,8 @@ typedef enum dsa_status {
  * shape is invalid.  The workspace starts with a 256-byte status header.
  * Top-k path, one kernel (scores and selection in the same kernel, chosen by
  * the prefill policy below): the header is followed by the kernel's per-CTA
- * scratch, 160 x 2 x (256 / H) x S_kv (rounded up to 32) fp32, whatever S.
+ * scratch, 160 x 2 x (256 / H) x (S_kv rounded up to 32, plus 32) fp32,
+ * whatever S.
  * Top-k path, two kernels: the header is followed by the fp32 logits of one
  * chunk of query rows, [B, rows, S_kv] with B * rows * S_kv * 4 <= 64 MiB
  * (all S rows when they fit, else a multiple of 256 / H rows, at least one

@@ -121,9 +121,9 @@ def test_workspace_size(lib):
     ws = lib.dsa_indexer_workspace_size
     # one-kernel prefill (scores and selection in the same kernel): the
     # status header, then the kernel's per-CTA scratch (160 CTAs x 2 item
-    # slots x 256/H rows x S_kv rounded up to 32, fp32), whatever S
+    # slots x 256/H rows of S_kv rounded up to 32, plus 32, fp32), whatever S
     fused = lambda H, S_kv: 256 + 160 * 2 * (256 // H) * (
-        (S_kv + 31) // 32 * 32) * 4
+        (S_kv + 31) // 32 * 32 + 32) * 4
     # two-kernel top-k path: the status header, then the logits of one chunk
     # of query rows (all rows when B*S*S_kv*4 <= 64 MiB, else the most whole
     # scoring tiles of 256/H rows that fit), whatever S
