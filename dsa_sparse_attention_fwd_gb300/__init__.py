@@ -196,8 +196,10 @@ def dsa_indexer_fwd(q, k, w, compress_ratio, topk, q_pos=None, in_idx=None,
                     stream=None, stage_events=None):
     """Enqueue the forward on device tensors; returns (out_scores, out_idx,
     workspace).  Raises DsaError on a synchronous error.  `stage_events`
-    (up to 3 torch.cuda.Event, created with enable_timing) are recorded
-    before the scoring kernel, after it, and after the selection kernel."""
+    (torch.cuda.Event created with enable_timing, at most 1024) are recorded
+    before the first kernel and after each kernel launch, in launch order
+    (dsa_indexer_fwd_launches gives the count); events left over after the
+    last launch are recorded at the end."""
     lib = load_library()
     S, B, H, D, S_kv = _check_inputs(q, k, w, q_pos, in_idx)
     dev = q.device

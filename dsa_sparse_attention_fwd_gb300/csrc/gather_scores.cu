@@ -208,8 +208,9 @@ __global__ void __launch_bounds__(GatRoles<H>::kThreads, 1)
         const int qs = nq % NQ;
         const uint32_t qph = (nq / NQ) & 1u;
         ++nq;
-        ok = __all_sync(0xffffffffu,
-                        wait_bar(q_empty(qs), qph ^ 1u, abort_flag, status));
+        ok = __all_sync(
+            0xffffffffu,
+            wait_bar_inl(q_empty(qs), qph ^ 1u, abort_flag, status));
         if (!ok) break;
         if (lane == 0) {
           mbar_arrive_expect_tx(q_full(qs), L::kQBytes);
@@ -221,7 +222,7 @@ __global__ void __launch_bounds__(GatRoles<H>::kThreads, 1)
       const int slot = nf % kIdxSlots;
       const uint32_t ph = (nf / kIdxSlots) & 1u;
       ok = __all_sync(0xffffffffu,
-                      wait_bar(i_empty(slot), ph ^ 1u, abort_flag, status));
+                      wait_bar_inl(i_empty(slot), ph ^ 1u, abort_flag, status));
       if (!ok) break;
       const int32_t *src =
           in_idx + (size_t)f.row * topk + (size_t)f.tile * kTileKeys;
@@ -257,10 +258,10 @@ __global__ void __launch_bounds__(GatRoles<H>::kThreads, 1)
       const int slot = ng % kIdxSlots;
       const uint32_t iph = (ng / kIdxSlots) & 1u;
       if (!__all_sync(0xffffffffu,
-                      wait_bar(i_full(slot), iph, abort_flag, status)))
+                      wait_bar_inl(i_full(slot), iph, abort_flag, status)))
         break;
       if (!__all_sync(0xffffffffu,
-                      wait_bar(k_empty(kst), kph ^ 1u, abort_flag, status)))
+                      wait_bar_inl(k_empty(kst), kph ^ 1u, abort_flag, status)))
         break;
       const uint32_t stage = sK + kst * L::kKBytes + c * (kTileKeys * 128);
       const uint8_t *kb = k + (size_t)cur.b * D * 2 + seg_off;
@@ -306,10 +307,10 @@ __global__ void __launch_bounds__(GatRoles<H>::kThreads, 1)
           qs = nq % NQ;
           const uint32_t qph = (nq / NQ) & 1u;
           ++nq;
-          if (!wait_bar(q_full(qs), qph, abort_flag, status)) break;
+          if (!wait_bar_inl(q_full(qs), qph, abort_flag, status)) break;
         }
-        if (!wait_bar(acc_empty(acc), aph ^ 1u, abort_flag, status)) break;
-        if (!wait_bar(k_full(kst), kph, abort_flag, status)) break;
+        if (!wait_bar_inl(acc_empty(acc), aph ^ 1u, abort_flag, status)) break;
+        if (!wait_bar_inl(k_full(kst), kph, abort_flag, status)) break;
         // the stage was written by cp.async (generic proxy); order those
         // writes, observed through the barrier, before the tensor core's
         // operand reads (async proxy)
@@ -369,8 +370,8 @@ __global__ void __launch_bounds__(GatRoles<H>::kThreads, 1)
         const int slot = nt % kIdxSlots;
         const uint32_t iph = (nt / kIdxSlots) & 1u;
         ++nt;
-        const bool got = wait_bar(acc_full(acc), aph, abort_flag, status) &&
-                         wait_bar(i_full(slot), iph, abort_flag, status);
+        const bool got = wait_bar_inl(acc_full(acc), aph, abort_flag, status) &&
+                         wait_bar_inl(i_full(slot), iph, abort_flag, status);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;

@@ -254,8 +254,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int qs = nq & 1;
         const uint32_t qph = (nq >> 1) & 1u;
         ++nq;
-        if (!__all_sync(0xffffffffu,
-                        wait_bar(q_empty(qs), qph ^ 1u, abort_flag, status)))
+        if (!__all_sync(
+                0xffffffffu,
+                wait_bar_inl(q_empty(qs), qph ^ 1u, abort_flag, status)))
           break;
         if (lane == 0) {
           mbar_arrive_expect_tx(q_full(qs), q_chunks * H * 128);
@@ -267,7 +268,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int slot = nr % kBwdRing;
       const uint32_t ph = (nr / kBwdRing) & 1u;
       if (!__all_sync(0xffffffffu,
-                      wait_bar(r_empty(slot), ph ^ 1u, abort_flag, status)))
+                      wait_bar_inl(r_empty(slot), ph ^ 1u, abort_flag, status)))
         break;
       const size_t off = (size_t)f.row * topk + (size_t)f.tile * kTileKeys;
       const int cnt = topk - f.tile * kTileKeys;
@@ -305,10 +306,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int slot = ng % kBwdRing;
       const uint32_t rph = (ng / kBwdRing) & 1u;
       if (!__all_sync(0xffffffffu,
-                      wait_bar(r_full(slot), rph, abort_flag, status)))
+                      wait_bar_inl(r_full(slot), rph, abort_flag, status)))
         break;
       if (!__all_sync(0xffffffffu,
-                      wait_bar(k_empty(kst), kph ^ 1u, abort_flag, status)))
+                      wait_bar_inl(k_empty(kst), kph ^ 1u, abort_flag, status)))
         break;
       const int32_t *sIdx =
           reinterpret_cast<const int32_t *>(sRing + slot * L::kRingBytes);
@@ -347,7 +348,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // predicate rather than a branch.
     const uint32_t lead = lane == 0;
     auto wait_all = [&](uint32_t b, uint32_t ph) -> bool {
-      return __all_sync(0xffffffffu, wait_bar(b, ph, abort_flag, status));
+      return __all_sync(0xffffffffu, wait_bar_inl(b, ph, abort_flag, status));
     };
     // MMA2 and MMA3 of a finished tile: A^T += K_g^T G', dK = G' Q'
     auto issue_back = [&](const BwdPending &p) -> bool {
@@ -472,7 +473,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int db = dk_n & 1;
       const uint32_t dph = (dk_n >> 1) & 1u;
       if (!__all_sync(0xffffffffu,
-                      wait_bar(dk_full(db), dph, abort_flag, status)))
+                      wait_bar_inl(dk_full(db), dph, abort_flag, status)))
         return false;
       tc_fence_after();
       const uint32_t live = __ballot_sync(0xffffffffu, dk_live);
@@ -530,8 +531,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t sQs = sQ + qs * L::kQBytes;
       // Q' = w * Q for this row's MMA3s, once the previous row's are done
       ok = __all_sync(0xffffffffu,
-                      wait_bar(q_full(qs), qph, abort_flag, status) &&
-                          wait_bar(qw_empty, (nrow & 1u) ^ 1u, abort_flag,
+                      wait_bar_inl(q_full(qs), qph, abort_flag, status) &&
+                          wait_bar_inl(qw_empty, (nrow & 1u) ^ 1u, abort_flag,
                                    status));
       if (ok) {
 #pragma unroll 2
@@ -558,8 +559,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t rph = (n / kBwdRing) & 1u;
         const int sa = n & 1;
         const uint32_t sph = (n >> 1) & 1u;
-        const bool got = wait_bar(s_full(sa), sph, abort_flag, status) &&
-                         wait_bar(r_full(slot), rph, abort_flag, status);
+        const bool got = wait_bar_inl(s_full(sa), sph, abort_flag, status) &&
+                         wait_bar_inl(r_full(slot), rph, abort_flag, status);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
@@ -630,7 +631,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t dqph = (nrow >> 1) & 1u;
       if (ok)
         ok = __all_sync(0xffffffffu,
-                        wait_bar(dq_full(dq), dqph, abort_flag, status));
+                        wait_bar_inl(dq_full(dq), dqph, abort_flag, status));
       // this warp's share of grad_w: zero unless the row completes
       sGW[sp * H + lane] = 0.f;
       sGW[sp * H + 32 + lane] = 0.f;

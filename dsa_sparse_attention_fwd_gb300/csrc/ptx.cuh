@@ -61,12 +61,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// The polling loop of wait_bar(), kept out of line: waits are many and
-// mostly satisfied at the first test, so only that test is inlined at each
-// call site and the hot loops stay small in the instruction cache.
-static __device__ __noinline__ bool wait_bar_poll(uint32_t bar, uint32_t parity,
-                                                  volatile int *abort_flag,
-                                                  int *status) {
+// The bounded polling loop behind both waits below.
+__device__ __forceinline__ bool wait_bar_loop(uint32_t bar, uint32_t parity,
+                                              volatile int *abort_flag,
+                                              int *status) {
   const uint64_t t0 = globaltimer_ns();
   for (uint64_t it = 1; it < kWaitMaxPolls; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -80,14 +78,35 @@ static __device__ __noinline__ bool wait_bar_poll(uint32_t bar, uint32_t parity,
   return false;
 }
 
+// The polling loop kept out of line: only the first test is inlined at
+// each call site, so hot loops with many waits stay small in the
+// instruction cache.
+static __device__ __noinline__ bool wait_bar_poll(uint32_t bar, uint32_t parity,
+                                                  volatile int *abort_flag,
+                                                  int *status) {
+  return wait_bar_loop(bar, parity, abort_flag, status);
+}
+
 // Bounded wait for the phase with parity `parity` of barrier `bar`.
 // Returns false (after raising the CTA's abort flag and the status bit) when
 // the limit expires or another role of the CTA has already aborted.
+// The slow path is a call; the scoring kernels use this form.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity,
                                          volatile int *abort_flag,
                                          int *status) {
   if (mbar_try_wait(bar, parity)) return true;
   return wait_bar_poll(bar, parity, abort_flag, status);
+}
+
+// wait_bar() with the polling loop inlined at the call site.  The kernels
+// whose roles wait often while they still hold live state (the gathers of
+// the given-indices, backward and sparse MLA kernels) run faster this way:
+// the call's register saves and restores cost more than the larger code.
+__device__ __forceinline__ bool wait_bar_inl(uint32_t bar, uint32_t parity,
+                                             volatile int *abort_flag,
+                                             int *status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_bar_loop(bar, parity, abort_flag, status);
 }
 
 // ---- TMA (tiled tensor loads into shared memory) ----------------------------

@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         const uint32_t qph = nq & 1u;
         ++nq;
         if (!__all_sync(0xffffffffu,
-                        wait_bar(q_empty, qph ^ 1u, abort_flag, status)))
+                        wait_bar_inl(q_empty, qph ^ 1u, abort_flag, status)))
           break;
         if (lane == 0) {
           mbar_arrive_expect_tx(q_full, L::kQBytes);
@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       const int slot = nr % kMlaRing;
       const uint32_t ph = (nr / kMlaRing) & 1u;
       if (!__all_sync(0xffffffffu,
-                      wait_bar(r_empty(slot), ph ^ 1u, abort_flag, status)))
+                      wait_bar_inl(r_empty(slot), ph ^ 1u, abort_flag, status)))
         break;
       const size_t off = ((size_t)f.b * g.S + f.s) * topk +
                          (size_t)f.tile * kTileKeys;
@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       const int slot = nv % kMlaRing;
       const uint32_t rph = (nv / kMlaRing) & 1u;
       if (!__all_sync(0xffffffffu,
-                      wait_bar(r_full(slot), rph, abort_flag, status)))
+                      wait_bar_inl(r_full(slot), rph, abort_flag, status)))
         break;
       const int32_t *sIdx =
           reinterpret_cast<const int32_t *>(sRing + slot * L::kRingBytes);
@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       bool stop = false;
 #pragma unroll 1
       for (int blk = 0; blk < NB; ++blk) {
-        if (!__all_sync(0xffffffffu, wait_bar(k_empty(blk), (nv & 1u) ^ 1u,
+        if (!__all_sync(0xffffffffu, wait_bar_inl(k_empty(blk), (nv & 1u) ^ 1u,
                                               abort_flag, status))) {
           stop = true;
           break;
@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     // ---------------- MMA issuer (whole warp; lane 0 issues) ----------------
     const uint32_t lead = lane == 0;
     auto wall = [&](uint32_t b_, uint32_t ph) -> bool {
-      return __all_sync(0xffffffffu, wait_bar(b_, ph, abort_flag, status));
+      return __all_sync(0xffffffffu, wait_bar_inl(b_, ph, abort_flag, status));
     };
     MlaCursor cur = mla_begin(g);
     uint32_t nv = 0, nq = 0, nb = 0, nitem = 0;
@@ -417,8 +417,8 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         const uint32_t rph = (nv / kMlaRing) & 1u;
         const int sa = nv & 1;
         const uint32_t sph = (nv >> 1) & 1u;
-        const bool got = wait_bar(s_full(sa), sph, abort_flag, status) &&
-                         wait_bar(r_full(slot), rph, abort_flag, status);
+        const bool got = wait_bar_inl(s_full(sa), sph, abort_flag, status) &&
+                         wait_bar_inl(r_full(slot), rph, abort_flag, status);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
@@ -460,7 +460,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         // every thread sees the new maxima and factors, and whether any moved
         const bool rescale = named_bar_or(3, kEpiThreads, moved);
         // the accumulator is idle once MMA2 of the previous tile is done
-        if (!__all_sync(0xffffffffu, wait_bar(p_empty, (nv & 1u) ^ 1u,
+        if (!__all_sync(0xffffffffu, wait_bar_inl(p_empty, (nv & 1u) ^ 1u,
                                               abort_flag, status))) {
           ok = false;
           break;
@@ -536,7 +536,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       named_bar_sync(3, kEpiThreads);
       // ---- o = O^T / l, lse = (m + log2 l) ln 2 ----
       ok = __all_sync(0xffffffffu,
-                      wait_bar(o_full, nitem & 1u, abort_flag, status));
+                      wait_bar_inl(o_full, nitem & 1u, abort_flag, status));
       if (ok) {
         tc_fence_after();
         float *orow = out_o + (((size_t)s * B + b) * H + hg * Hg) * Dc;
