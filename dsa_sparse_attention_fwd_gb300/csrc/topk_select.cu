@@ -439,11 +439,9 @@ __device__ __forceinline__ bool bucket_topk(const float *__restrict__ L, int nv,
 // bucket "comes before" is one unsigned 64-bit comparison.
 struct RegMap {
   float sc, off;  // bucket + 2^23 = clamp(v * sc + off)
-  __device__ __forceinline__ uint32_t desc(uint32_t k) const {
-    // key_to_float without a branch: flip the sign bit of keys >= 2^31,
-    // every bit of the others
-    const uint32_t flip = ~(uint32_t)((int32_t)k >> 31) | 0x80000000u;
-    const float v = __uint_as_float(k ^ flip);
+  // descending bucket of a value: monotone non-increasing in v; -inf (and,
+  // with sc = 0, everything) lands in the last bucket
+  __device__ __forceinline__ uint32_t desc(float v) const {
     const float t = fminf(fmaxf(fmaf(v, sc, off), 8388608.0f),
                           8388608.0f + (float)(kBucketBins - 1));
     return ~__float_as_uint(t) & (uint32_t)(kBucketBins - 1);
@@ -451,6 +449,8 @@ struct RegMap {
 };
 
 // vec: the row is 16-byte aligned and its length a multiple of four.
+// The keys stay floats until they are kept: the range and the buckets are
+// computed on the values, and only the kept keys get their order key.
 template <int NT, int R>
 __device__ __forceinline__ bool bucket_topk_reg(
     const float *__restrict__ L, int nv, int topk, bool vec, uint32_t *bins,
@@ -460,6 +460,7 @@ __device__ __forceinline__ bool bucket_topk_reg(
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int per = kBucketBins / NT;
   const float neg_inf = -__int_as_float(0x7f800000);
+  const float pos_inf = __int_as_float(0x7f800000);
 
   {
     // bins follow a u64 buffer of any length: 8-byte aligned only
@@ -469,18 +470,18 @@ __device__ __forceinline__ bool bucket_topk_reg(
   }
   // the loops over a thread's key groups skip, block-uniformly, the groups
   // past the row's end (a short row runs a fraction of the unrolled code)
-  uint32_t kr[R];
-  uint32_t kmn = 0xffffffffu, kmx = 0u;
+  float kv[R];
+  float lo = pos_inf, hi = neg_inf;  // range of the finite values
   bool nan = false;
 #pragma unroll
   for (int i = 0; i < R / 4; ++i) {
     if (4 * NT * i >= nv) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) kr[4 * i + c] = 0u;
+      for (int c = 0; c < 4; ++c) kv[4 * i + c] = neg_inf;
       continue;
     }
     const int j0 = 4 * (tid + NT * i);
-    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    float v[4] = {neg_inf, neg_inf, neg_inf, neg_inf};
     if (vec) {
       // j0 < nv <= row length, both multiples of four: the group of four
       // lies inside the row
@@ -498,19 +499,19 @@ __device__ __forceinline__ bool bucket_topk_reg(
     }
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      const uint32_t k = ordered_key(v[c]);
-      kr[4 * i + c] = k;
-      if (j0 + c < nv) {
-        nan |= v[c] != v[c];
-        if (fabsf(v[c]) <= 3.402823466e38f) {
-          kmn = min(kmn, k);
-          kmx = max(kmx, k);
-        }
+      kv[4 * i + c] = v[c];
+      // keys past the row's end are -inf here and never counted
+      nan |= v[c] != v[c];
+      if (fabsf(v[c]) <= 3.402823466e38f) {
+        lo = fminf(lo, v[c]);
+        hi = fmaxf(hi, v[c]);
       }
     }
   }
-  kmn = __reduce_min_sync(0xffffffffu, kmn);
-  kmx = __reduce_max_sync(0xffffffffu, kmx);
+  // block range through order-preserving integers (+-inf when no value is
+  // finite)
+  uint32_t kmn = __reduce_min_sync(0xffffffffu, ordered_key(lo));
+  uint32_t kmx = __reduce_max_sync(0xffffffffu, ordered_key(hi));
   nan = __any_sync(0xffffffffu, nan);
   if (lane == 0) {
     sh.wand[warp] = kmn;
@@ -531,17 +532,16 @@ __device__ __forceinline__ bool bucket_topk_reg(
   map.sc = 0.f;
   map.off = 8388608.0f;
   if (kmin < kmax) {
-    const float lo = key_to_float(kmin);
-    const float span = key_to_float(kmax) - lo;
+    const float flo = key_to_float(kmin);
+    const float span = key_to_float(kmax) - flo;
     if (span > 0.f && span <= 3.402823466e38f) {
       map.sc = fminf((float)kBucketBins / span, 1e30f);
       // lo * sc lands within a rounding of the bins' range; the clamp
       // absorbs the error and keeps the map monotone
-      map.off = 8388608.0f - lo * map.sc;
+      map.off = 8388608.0f - flo * map.sc;
     }
   }
 
-#pragma unroll
   // each key's bucket, two to a register, for the scatter below
   uint32_t bk[R / 2];
 #pragma unroll
@@ -551,7 +551,7 @@ __device__ __forceinline__ bool bucket_topk_reg(
     if (4 * NT * i >= nv) continue;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      const uint32_t b = map.desc(kr[4 * i + c]);
+      const uint32_t b = map.desc(kv[4 * i + c]);
       bk[2 * i + (c >> 1)] |= b << (16 * (c & 1));
       if (4 * (tid + NT * i) + c < nv) atomicAdd(&bins[bin_slot(b)], 1u);
     }
@@ -602,11 +602,10 @@ __device__ __forceinline__ bool bucket_topk_reg(
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const int j = 4 * (tid + NT * i) + c;
-      const uint32_t k = kr[4 * i + c];
       const uint32_t b = (bk[2 * i + (c >> 1)] >> (16 * (c & 1))) & 0xffffu;
       if (j < nv && b <= thr) {
         const uint32_t pos = atomicAdd(&bins[bin_slot(b)], 1u << 16) >> 16;
-        grouped[pos] = ((uint64_t)k << 32) |
+        grouped[pos] = ((uint64_t)ordered_key(kv[4 * i + c]) << 32) |
                        (b << 20) | (0xfffffu - (uint32_t)j);
       }
     }
