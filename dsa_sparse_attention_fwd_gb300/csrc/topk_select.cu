@@ -432,33 +432,35 @@ __device__ __forceinline__ bool bucket_topk(const float *__restrict__ L, int nv,
 
 // The same route for rows of at most R * NT keys, held in registers: thread
 // t owns keys 4(t + NT i) + c (c < 4, i < R/4), read as float4 when the row
-// is 16-byte aligned.  The bucket map here is a clamped fused multiply-add
-// whose result lands in [2^23, 2^23 + 4095], where the float's low mantissa
-// bits are the bucket; rows holding a NaN take the radix route.  A kept key
+// is 16-byte aligned, over NB buckets (NB = R * NT: 1024, 2048 or 4096).
+// The bucket map here is a clamped fused multiply-add whose result lands in
+// [2^23, 2^23 + NB - 1], where the float's low mantissa bits are the
+// bucket; rows holding a NaN take the radix route.  A kept key
 // is stored as (key << 32 | bucket << 20 | (2^20 - 1 - j)), so inside a
 // bucket "comes before" is one unsigned 64-bit comparison.
+template <int NB>
 struct RegMap {
   float sc, off;  // bucket + 2^23 = clamp(v * sc + off)
-  // descending bucket of a value: monotone non-increasing in v; -inf (and,
-  // with sc = 0, everything) lands in the last bucket
+  // descending bucket of a value among NB: monotone non-increasing in v;
+  // -inf (and, with sc = 0, everything) lands in the last bucket
   __device__ __forceinline__ uint32_t desc(float v) const {
     const float t = fminf(fmaxf(fmaf(v, sc, off), 8388608.0f),
-                          8388608.0f + (float)(kBucketBins - 1));
-    return ~__float_as_uint(t) & (uint32_t)(kBucketBins - 1);
+                          8388608.0f + (float)(NB - 1));
+    return ~__float_as_uint(t) & (uint32_t)(NB - 1);
   }
 };
 
 // vec: the row is 16-byte aligned and its length a multiple of four.
 // The keys stay floats until they are kept: the range and the buckets are
 // computed on the values, and only the kept keys get their order key.
-template <int NT, int R>
+template <int NT, int R, int NB>
 __device__ __forceinline__ bool bucket_topk_reg(
     const float *__restrict__ L, int nv, int topk, bool vec, uint32_t *bins,
     uint64_t *grouped, SelShared &sh, int32_t *__restrict__ oi,
     float *__restrict__ os) {
   static_assert(R % 4 == 0, "keys are read four at a time");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  constexpr int per = kBucketBins / NT;
+  constexpr int per = NB / NT;
   const float neg_inf = -__int_as_float(0x7f800000);
   const float pos_inf = __int_as_float(0x7f800000);
 
@@ -466,7 +468,7 @@ __device__ __forceinline__ bool bucket_topk_reg(
     // bins follow a u64 buffer of any length: 8-byte aligned only
     uint2 *b2 = reinterpret_cast<uint2 *>(bins);
 #pragma unroll
-    for (int i = tid; i < kBucketBins / 2; i += NT) b2[i] = make_uint2(0u, 0u);
+    for (int i = tid; i < NB / 2; i += NT) b2[i] = make_uint2(0u, 0u);
   }
   // the loops over a thread's key groups skip, block-uniformly, the groups
   // past the row's end (a short row runs a fraction of the unrolled code)
@@ -528,14 +530,14 @@ __device__ __forceinline__ bool bucket_topk_reg(
     anynan |= sh.wgt[w];
   }
   if (anynan) return false;  // block-uniform; nothing written yet
-  RegMap map;
+  RegMap<NB> map;
   map.sc = 0.f;
   map.off = 8388608.0f;
   if (kmin < kmax) {
     const float flo = key_to_float(kmin);
     const float span = key_to_float(kmax) - flo;
     if (span > 0.f && span <= 3.402823466e38f) {
-      map.sc = fminf((float)kBucketBins / span, 1e30f);
+      map.sc = fminf((float)NB / span, 1e30f);
       // lo * sc lands within a rounding of the bins' range; the clamp
       // absorbs the error and keeps the map monotone
       map.off = 8388608.0f - flo * map.sc;
@@ -674,10 +676,25 @@ __global__ void __launch_bounds__(NT, NT == kSelThreads ? 4 : 1)
     if (nv <= R * NT) {
       const bool vec = (S_kv & 3) == 0 &&
                        (reinterpret_cast<uintptr_t>(L) & 15u) == 0;
-      if (bucket_topk_reg<NT, R>(L, nv, topk, vec,
-                                 reinterpret_cast<uint32_t *>(bufB), bufA, sh,
-                                 oi, os))
-        break;
+      // as many buckets as the row has keys, rounded up to 1024, 2048 or
+      // 4096: the clear and the scan cost per bucket
+      uint32_t *bins = reinterpret_cast<uint32_t *>(bufB);
+      bool done;
+      if constexpr (R % 16 == 0) {
+        if (nv <= kBucketBins / 4)
+          done = bucket_topk_reg<NT, R / 4, kBucketBins / 4>(
+              L, nv, topk, vec, bins, bufA, sh, oi, os);
+        else if (nv <= kBucketBins / 2)
+          done = bucket_topk_reg<NT, R / 2, kBucketBins / 2>(
+              L, nv, topk, vec, bins, bufA, sh, oi, os);
+        else
+          done = bucket_topk_reg<NT, R, kBucketBins>(L, nv, topk, vec, bins,
+                                                     bufA, sh, oi, os);
+      } else {
+        done = bucket_topk_reg<NT, R, kBucketBins>(L, nv, topk, vec, bins,
+                                                   bufA, sh, oi, os);
+      }
+      if (done) break;
     } else if (bucket_topk<NT>(L, nv, topk, keys, region_u32,
                                reinterpret_cast<uint32_t *>(bufB), bufA, sh,
                                oi, os)) {
