@@ -343,6 +343,33 @@ def test_long_rows(dsa, S, B, S_kv, ratio, topk):
     compare_rows(sc, idx, ref, np.arange(B * S), S)
 
 
+@pytest.mark.parametrize("topk", [512, 2048])
+def test_selection_bucket_count_boundaries(dsa, topk):
+    """The register route sizes its buckets to the row: 1024, 2048 or 4096
+    for rows of at most that many keys, and rows past 4096 keys leave the
+    registers.  Three sequences whose query positions start just below
+    1024, 2048 and 4096 visible keys give 600 rows (the 256-thread
+    selection) of every length across each boundary."""
+    H, D, S, S_kv = 64, 128, 200, 4200
+    B = 3
+    wl = Workload("t", B=B, S=S, S_kv=S_kv, H=H, D=D, compress_ratio=1,
+                  topk=topk, w_scale=H ** -0.5, seed=topk + 7)
+    q, k, w, _ = make_inputs(wl)
+    # row s of sequence b sees pos_b + s + 1 keys
+    pos = torch.tensor([1024 - 101, 2048 - 101, 4096 - 101],
+                       dtype=torch.int32)
+    nvis = row_nvis(S, B, 1, S_kv, pos)
+    for edge in (1024, 2048, 4096):
+        assert np.any(nvis == edge) and np.any(nvis == edge + 1)
+    sc, idx, st = gpu_run(dsa, q, k, w, 1, topk, q_pos=pos)
+    assert st == 0
+    sc = sc.reshape(B, S, topk)
+    idx = idx.reshape(B, S, topk)
+    check_invariants(sc, idx, nvis, topk)
+    ref = oracle.indexer_fwd(q, k, w, 1, topk, q_pos=pos, want_logits=True)
+    compare_rows(sc, idx, ref, np.arange(B * S), S)
+
+
 @pytest.mark.parametrize("topk,distinct_keys", [(7, None), (100, None),
                                                 (300, None), (100, 8),
                                                 (300, 8)])
