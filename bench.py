@@ -94,18 +94,22 @@ def kernel_source_sha(kernel: str = "index_scores") -> str:
     return h.hexdigest()[:16]
 
 
-def read_traffic(kernel: str = "index_scores"):
-    """DRAM bytes per launch of a kernel from the committed ncu summary,
-    only if it was taken on the current kernel source."""
+def read_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of a kernel on a bench workload, from the
+    committed ncu summary, only if it was taken on the current kernel source
+    and for this workload (a call that launches the kernel once per row
+    chunk records the sum over the call's launches)."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_traffic.json")
     try:
         with open(path) as fh:
             d = json.load(fh)
     except (OSError, ValueError):
         return None
-    if d.get("source_sha") != kernel_source_sha(kernel):
-        return None
-    return d.get("dram_bytes_per_launch")
+    sha = kernel_source_sha(kernel)
+    for e in d.get("entries", []):
+        if e.get("bench_workload") == workload and e.get("source_sha") == sha:
+            return e.get("dram_bytes_per_launch")
+    return None
 
 
 class ClockSampler:
@@ -448,6 +452,7 @@ def run_ours(args):
     decode_shape = wl.S < 256 // wl.H
     # the one-kernel forward (scores and selection together) ran
     fused = gi is None and n_launch == 1
+    wkey = wl.name + (" given-indices" if gi is not None else "")
 
     def tensor_line(kernel, ms):
         a = flops / (ms * 1e-3) / 1e12
@@ -455,7 +460,7 @@ def run_ours(args):
                 "peak": tc_peak, "unit": "TFLOP/s", "frac": a / tc_peak,
                 "peak_source": f"{peak_src} bf16 burst",
                 "algorithmic": f"{flops:.4g} FLOP per launch (2*H*D per pair)",
-                "traffic": read_traffic(kernel)}
+                "traffic": read_traffic(kernel, wkey)}
 
     def hbm_line(kernel, ms, nbytes, what):
         a = nbytes / (ms * 1e-3) / 1e9
@@ -463,7 +468,7 @@ def run_ours(args):
                 "peak": hbm_peak, "unit": "GB/s", "frac": a / hbm_peak,
                 "peak_source": f"{peak_src} copy bandwidth",
                 "algorithmic": f"{nbytes:.4g} B per launch ({what})",
-                "traffic": read_traffic(kernel)}
+                "traffic": read_traffic(kernel, wkey)}
 
     if direct:
         kernels = {"gather_scores": t_score, "step": t_step}
@@ -818,7 +823,8 @@ def run_backward(args):
                                     "per valid slot)",
                      "timed": "the C call: grad_k clear + status clear + "
                               "the kernel",
-                     "traffic": read_traffic("indexer_bwd")},
+                     "traffic": read_traffic("indexer_bwd",
+                                             wl.name + " backward")},
         "e2e": {"value": world * flops / (t_e2e * 1e-3) / 1e12,
                 "unit": "TFLOP/s", "ms_per_step": t_e2e,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -965,7 +971,7 @@ def run_pooled(args):
                      "peak_source": f"{peak_src} copy bandwidth",
                      "algorithmic": f"{cbytes:.4g} B per launch (k bf16 + "
                                     "gate fp32 read, pooled keys written)",
-                     "traffic": read_traffic("pool")},
+                     "traffic": read_traffic("pool", "c4_pool")},
         "e2e": {"value": world * flops / (t_e2e * 1e-3) / 1e12,
                 "unit": "TFLOP/s", "ms_per_step": t_e2e,
                 "h2d_bytes_per_step": sum(t.numel() * t.element_size()
@@ -1102,7 +1108,7 @@ def run_mla(args):
                      "algorithmic": f"{flops:.4g} FLOP per launch (4*H*Dc "
                                     "per valid slot: the score and the "
                                     "output products)",
-                     "traffic": read_traffic("sparse_mla")},
+                     "traffic": read_traffic("sparse_mla", "sparse_mla")},
         "e2e": {"value": world * flops / (t_e2e * 1e-3) / 1e12,
                 "unit": "TFLOP/s", "ms_per_step": t_e2e,
                 "h2d_bytes_per_step": sum(t.numel() * t.element_size()
