@@ -754,65 +754,64 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         const int j = tile * kTileKeys + sp * 32 + lane;
         const bool kv_ok = !KV || j >= S_kv ||
                            __ldg(kv_valid + (size_t)j * B + it.b) != 0;
-        float2 part = make_float2(0.f, 0.f);  // H = 128: first half's sum
+        // This warp's 128 columns in four quarters of 32, double-buffered:
+        // quarter qt + 1 is loaded while quarter qt is reduced.  Quarter qt
+        // holds heads [32 qt mod H, +32) of the half's row 32 qt / H; a row's
+        // sum runs over its heads in increasing order whatever the split
+        // (the same order as the two-kernel scorer).
+        static_assert(H >= 32, "a quarter holds one row's heads");
+        const uint32_t taddr = tmem + ((uint32_t)(sp * 32) << 16) +
+                               acc * kTileCols + half * 128;
+        uint32_t v[2][32];
+        tmem_ld32(taddr, v[0]);
+        tmem_ld_wait();
+        reg_fence32(v[0]);
+        float2 acc2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int rd = 0; rd < 2; ++rd) {
-          const uint32_t taddr = tmem + ((uint32_t)(sp * 32) << 16) +
-                                 acc * kTileCols + half * 128 + rd * 64;
-          uint32_t v[2][32];
-          tmem_ld32(taddr + 0, v[0]);
-          tmem_ld32(taddr + 32, v[1]);
-          tmem_ld_wait();
-          reg_fence32(v[0]);
-          reg_fence32(v[1]);
-          if (rd == 1) {
+        for (int qt = 0; qt < 4; ++qt) {
+          const int cur = qt & 1;
+          if (qt < 3) tmem_ld32(taddr + 32 * (qt + 1), v[cur ^ 1]);
+          const int qq = (32 * qt) / H;  // row within the half
+          const int h0 = (32 * qt) % H;  // first head of the quarter
+          const int tq = half * QH + qq;
+          if (h0 == 0) acc2 = make_float2(0.f, 0.f);
+          const float4 *wq4 =
+              reinterpret_cast<const float4 *>(sW + tq * H + h0);
+#pragma unroll
+          for (int h = 0; h < 32; h += 4) {
+            const float4 wv = wq4[h >> 2];
+            const float r0 = fmaxf(__uint_as_float(v[cur][h]), 0.f);
+            const float r1 = fmaxf(__uint_as_float(v[cur][h + 1]), 0.f);
+            const float r2 = fmaxf(__uint_as_float(v[cur][h + 2]), 0.f);
+            const float r3 = fmaxf(__uint_as_float(v[cur][h + 3]), 0.f);
+            acc2 = __ffma2_rn(make_float2(wv.x, wv.y), make_float2(r0, r1),
+                              acc2);
+            acc2 = __ffma2_rn(make_float2(wv.z, wv.w), make_float2(r2, r3),
+                              acc2);
+          }
+          if (qt < 3) {
+            tmem_ld_wait();
+            reg_fence32(v[cur ^ 1]);
+          }
+          if (qt == 2) {
+            // the last quarter has landed: the accumulator is free
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_empty(acc));
           }
-          // queries finished in this round and the heads each one spans here
-          constexpr int QPR = H <= 64 ? 64 / H : 1;
-          constexpr int HPR = H <= 64 ? H : 64;
-#pragma unroll
-          for (int qi = 0; qi < QPR; ++qi) {
-            float2 acc2 = H <= 64 ? make_float2(0.f, 0.f) : part;
-            const int tq = H <= 64 ? half * QH + rd * QPR + qi : half;
-            const float4 *wq4 = reinterpret_cast<const float4 *>(
-                sW + tq * H + (H <= 64 ? 0 : rd * 64));
-#pragma unroll
-            for (int h = 0; h < HPR; h += 4) {
-              const float4 wv = wq4[h >> 2];
-              const int c = qi * HPR + h;
-              const float r0 = fmaxf(__uint_as_float(v[c >> 5][c & 31]), 0.f);
-              const float r1 =
-                  fmaxf(__uint_as_float(v[(c + 1) >> 5][(c + 1) & 31]), 0.f);
-              const float r2 =
-                  fmaxf(__uint_as_float(v[(c + 2) >> 5][(c + 2) & 31]), 0.f);
-              const float r3 =
-                  fmaxf(__uint_as_float(v[(c + 3) >> 5][(c + 3) & 31]), 0.f);
-              acc2 = __ffma2_rn(make_float2(wv.x, wv.y), make_float2(r0, r1),
-                                acc2);
-              acc2 = __ffma2_rn(make_float2(wv.z, wv.w), make_float2(r2, r3),
-                                acc2);
-            }
-            if (H > 64 && rd == 0) {
-              part = acc2;
-              continue;
-            }
-            const float score = acc2.x + acc2.y;
-            const int qq = H <= 64 ? rd * QPR + qi : 0;  // row within half
-            const int t = it.t0 + tq;
-            const bool vis = (long long)(j + 1) * ratio - 1 <= qbase + t;
-            if (t < S && vis && j < S_kv) {
-              float *dst = srow + (size_t)tq * row_stride + j;
-              if (kv_ok) {
-                *dst = score;
-                lo[qq] = fminf(lo[qq], score);
-                hi[qq] = fmaxf(hi[qq], score);
-                chk = fmaf(score, 0.f, chk);
-              } else {
-                *dst = neg_inf;  // not a candidate: sorts last
-              }
+          if (h0 + 32 < H) continue;  // the row goes on in the next quarter
+          const float score = acc2.x + acc2.y;
+          const int t = it.t0 + tq;
+          const bool vis = (long long)(j + 1) * ratio - 1 <= qbase + t;
+          if (t < S && vis && j < S_kv) {
+            float *dst = srow + (size_t)tq * row_stride + j;
+            if (kv_ok) {
+              *dst = score;
+              lo[qq] = fminf(lo[qq], score);
+              hi[qq] = fmaxf(hi[qq], score);
+              chk = fmaf(score, 0.f, chk);
+            } else {
+              *dst = neg_inf;  // not a candidate: sorts last
             }
           }
         }
