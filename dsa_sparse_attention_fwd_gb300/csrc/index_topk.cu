@@ -55,7 +55,6 @@ constexpr int kSelBar = 2;     // named barrier of the 8 selection warps
 constexpr int kSelT = 256;     // selection threads
 constexpr int kSelFirstThread = 320;
 constexpr int kBins = 4096;    // fast-route buckets
-constexpr int kBinsPer = kBins / kSelT;
 constexpr int kCrowd = 32;     // most keys a kept bucket may hold
 constexpr int kRegGroups = 4;  // float4 groups per thread held in registers
 constexpr int kRegKeys = 4 * kRegGroups * kSelT;  // 4096
@@ -76,13 +75,14 @@ __device__ __forceinline__ uint32_t bslot(uint32_t b) {
   return b ^ ((b >> 4) & 15u);
 }
 
-// Descending bucket of a finite score: clamp(v * sc + off) lands in
-// [2^23, 2^23 + 4095], where the float's low 12 mantissa bits count up with
-// v; their complement counts down.  Monotone (non-increasing) in v.
+// Descending bucket among NB of a finite score: clamp(v * sc + off) lands
+// in [2^23, 2^23 + NB - 1], where the float's low mantissa bits count up
+// with v; their complement counts down.  Monotone (non-increasing) in v.
+template <int NB = kBins>
 __device__ __forceinline__ uint32_t bucket_desc(float v, float sc, float off) {
   const float t = fminf(fmaxf(fmaf(v, sc, off), 8388608.0f),
-                        8388608.0f + (float)(kBins - 1));
-  return ~__float_as_uint(t) & (uint32_t)(kBins - 1);
+                        8388608.0f + (float)(NB - 1));
+  return ~__float_as_uint(t) & (uint32_t)(NB - 1);
 }
 
 __host__ __device__ __forceinline__ int pow2_ceil(int x) {
@@ -364,14 +364,16 @@ __device__ __noinline__ void select_exact(const float *R, int n, int topk,
 // Fast route after the histogram: scan, threshold bucket and kept buckets'
 // starts.  Returns false (block-uniform) when a kept bucket is crowded.
 // On return m = keys in the kept buckets, thr = last kept bucket (or -1).
+template <int NB = kBins>
 __device__ __forceinline__ bool bucket_scan(int topk, int st, uint32_t *bins,
                                             SelMisc &sm, int &m, int &thr) {
+  constexpr int per = NB / kSelT;  // buckets per thread
   const int lane = st & 31;
-  uint32_t c[kBinsPer];
+  uint32_t c[per];
   uint32_t lsum = 0;
 #pragma unroll
-  for (int i = 0; i < kBinsPer; ++i) {
-    c[i] = bins[bslot(st * kBinsPer + i)];
+  for (int i = 0; i < per; ++i) {
+    c[i] = bins[bslot(st * per + i)];
     lsum += c[i];
   }
   uint32_t total;
@@ -379,8 +381,8 @@ __device__ __forceinline__ bool bucket_scan(int topk, int st, uint32_t *bins,
   const uint32_t want = total < (uint32_t)topk ? total : (uint32_t)topk;
   uint32_t occ = 0, run = above;
 #pragma unroll
-  for (int i = 0; i < kBinsPer; ++i) {
-    const uint32_t b = (uint32_t)(st * kBinsPer + i);
+  for (int i = 0; i < per; ++i) {
+    const uint32_t b = (uint32_t)(st * per + i);
     if (run < want) {
       bins[bslot(b)] = (run << 16) | c[i];
       occ = max(occ, c[i]);
@@ -426,6 +428,81 @@ __device__ __forceinline__ void bucket_rank_write(int m, int topk, int st,
   write_padding(m, topk, st, oi, os);
 }
 
+// The register route of select_row() for a row of n <= NB scores, over NB
+// buckets (NB = 1024, 2048 or 4096, the smallest that holds the row: the
+// clear and the scan cost per bucket).  Ends with a selection barrier.
+template <int NB>
+__device__ __forceinline__ void select_reg(const float *R, int n, int topk,
+                                           float lo, float hi, int st,
+                                           uint32_t *bins, uint64_t *grouped,
+                                           SelMisc &sm, int32_t *oi,
+                                           float *os) {
+  constexpr int G = NB / (4 * kSelT);  // float4 groups per thread
+  const float neg_inf = -__int_as_float(0x7f800000);
+  float sc = 0.f, off = 8388608.0f;
+  if (hi > lo) {
+    const float span = hi - lo;
+    if (span <= 3.402823466e38f) {
+      sc = fminf((float)NB / span, 1e30f);
+      off = 8388608.0f - lo * sc;
+    }
+  }
+  {
+    uint2 *b2 = reinterpret_cast<uint2 *>(bins);
+    for (int i = st; i < NB / 2; i += kSelT) b2[i] = make_uint2(0u, 0u);
+  }
+  if (st == 0) sm.flag = 0u;
+  int m, thr;
+  // thread st owns keys 4 (st + 256 i) + c, i < G
+  float kv[4 * G];
+#pragma unroll
+  for (int i = 0; i < G; ++i) {
+    const int j0 = 4 * (st + kSelT * i);
+    float4 f = make_float4(neg_inf, neg_inf, neg_inf, neg_inf);
+    if (4 * kSelT * i < n && j0 < n)
+      f = __ldcg(reinterpret_cast<const float4 *>(R + j0));
+    kv[4 * i + 0] = j0 + 0 < n ? f.x : neg_inf;
+    kv[4 * i + 1] = j0 + 1 < n ? f.y : neg_inf;
+    kv[4 * i + 2] = j0 + 2 < n ? f.z : neg_inf;
+    kv[4 * i + 3] = j0 + 3 < n ? f.w : neg_inf;
+  }
+  sel_sync();  // bins cleared
+#pragma unroll
+  for (int i = 0; i < G; ++i) {
+    if (4 * kSelT * i >= n) continue;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const float v = kv[4 * i + c];
+      if (v != neg_inf)
+        atomicAdd(&bins[bslot(bucket_desc<NB>(v, sc, off))], 1u);
+    }
+  }
+  sel_sync();
+  if (!bucket_scan<NB>(topk, st, bins, sm, m, thr)) {
+    select_exact(R, n, topk, st, bins, grouped, sm, oi, os);
+    return;
+  }
+#pragma unroll
+  for (int i = 0; i < G; ++i) {
+    if (4 * kSelT * i >= n) continue;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const float v = kv[4 * i + c];
+      if (v == neg_inf) continue;
+      const uint32_t b = bucket_desc<NB>(v, sc, off);
+      if ((int)b <= thr) {
+        const int j = 4 * (st + kSelT * i) + c;
+        const uint32_t pos = atomicAdd(&bins[bslot(b)], 1u << 16) >> 16;
+        grouped[pos] = ((uint64_t)ordered_key(v) << 32) | (b << 20) |
+                       (0xfffffu - (uint32_t)j);
+      }
+    }
+  }
+  sel_sync();
+  bucket_rank_write(m, topk, st, bins, grouped, oi, os);
+  sel_sync();
+}
+
 // One row's selection.  R: the row's n scores (scratch, 16-byte aligned,
 // readable up to n rounded up to 4); [lo, hi]: the range of its finite
 // unmasked scores; bad: some score is non-finite.  Ends with a selection
@@ -445,6 +522,18 @@ __device__ __forceinline__ void select_row(const float *R, int n, int topk,
     select_exact(R, n, topk, st, bins, grouped, sm, oi, os);
     return;
   }
+  if (n <= kRegKeys / 4) {
+    select_reg<kBins / 4>(R, n, topk, lo, hi, st, bins, grouped, sm, oi, os);
+    return;
+  }
+  if (n <= kRegKeys / 2) {
+    select_reg<kBins / 2>(R, n, topk, lo, hi, st, bins, grouped, sm, oi, os);
+    return;
+  }
+  if (n <= kRegKeys) {
+    select_reg<kBins>(R, n, topk, lo, hi, st, bins, grouped, sm, oi, os);
+    return;
+  }
   float sc = 0.f, off = 8388608.0f;
   if (hi > lo) {
     const float span = hi - lo;
@@ -459,69 +548,45 @@ __device__ __forceinline__ void select_row(const float *R, int n, int topk,
   }
   if (st == 0) sm.flag = 0u;
   int m, thr;
-  if (n <= kRegKeys) {
-    // thread st owns keys 4 (st + 256 i) + c
-    float kv[4 * kRegGroups];
+  sel_sync();  // bins cleared
+  // both passes over the row keep four 16-byte L2 reads in flight per
+  // thread before using them
+  const float4 ninf4 = make_float4(neg_inf, neg_inf, neg_inf, neg_inf);
+  for (int g0 = st; 4 * g0 < n; g0 += 4 * kSelT) {
+    float4 f[4];
 #pragma unroll
-    for (int i = 0; i < kRegGroups; ++i) {
-      const int j0 = 4 * (st + kSelT * i);
-      float4 f = make_float4(neg_inf, neg_inf, neg_inf, neg_inf);
-      if (4 * kSelT * i < n && j0 < n)
-        f = __ldcg(reinterpret_cast<const float4 *>(R + j0));
-      kv[4 * i + 0] = j0 + 0 < n ? f.x : neg_inf;
-      kv[4 * i + 1] = j0 + 1 < n ? f.y : neg_inf;
-      kv[4 * i + 2] = j0 + 2 < n ? f.z : neg_inf;
-      kv[4 * i + 3] = j0 + 3 < n ? f.w : neg_inf;
-    }
-    sel_sync();  // bins cleared
-#pragma unroll
-    for (int i = 0; i < kRegGroups; ++i) {
-      if (4 * kSelT * i >= n) continue;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const float v = kv[4 * i + c];
-        if (v != neg_inf) atomicAdd(&bins[bslot(bucket_desc(v, sc, off))], 1u);
-      }
-    }
-    sel_sync();
-    if (!bucket_scan(topk, st, bins, sm, m, thr)) {
-      select_exact(R, n, topk, st, bins, grouped, sm, oi, os);
-      return;
+    for (int u = 0; u < 4; ++u) {
+      const int g = g0 + u * kSelT;
+      f[u] = 4 * g < n ? __ldcg(reinterpret_cast<const float4 *>(R) + g)
+                       : ninf4;
     }
 #pragma unroll
-    for (int i = 0; i < kRegGroups; ++i) {
-      if (4 * kSelT * i >= n) continue;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const float v = kv[4 * i + c];
-        if (v == neg_inf) continue;
-        const uint32_t b = bucket_desc(v, sc, off);
-        if ((int)b <= thr) {
-          const int j = 4 * (st + kSelT * i) + c;
-          const uint32_t pos = atomicAdd(&bins[bslot(b)], 1u << 16) >> 16;
-          grouped[pos] = ((uint64_t)ordered_key(v) << 32) | (b << 20) |
-                         (0xfffffu - (uint32_t)j);
-        }
-      }
-    }
-  } else {
-    sel_sync();  // bins cleared
-    for (int g = st; 4 * g < n; g += kSelT) {
-      const float4 f = __ldcg(reinterpret_cast<const float4 *>(R) + g);
-      const float vv[4] = {f.x, f.y, f.z, f.w};
+    for (int u = 0; u < 4; ++u) {
+      const int g = g0 + u * kSelT;
+      const float vv[4] = {f[u].x, f[u].y, f[u].z, f[u].w};
 #pragma unroll
       for (int c = 0; c < 4; ++c)
         if (4 * g + c < n && vv[c] != neg_inf)
           atomicAdd(&bins[bslot(bucket_desc(vv[c], sc, off))], 1u);
     }
-    sel_sync();
-    if (!bucket_scan(topk, st, bins, sm, m, thr)) {
-      select_exact(R, n, topk, st, bins, grouped, sm, oi, os);
-      return;
+  }
+  sel_sync();
+  if (!bucket_scan(topk, st, bins, sm, m, thr)) {
+    select_exact(R, n, topk, st, bins, grouped, sm, oi, os);
+    return;
+  }
+  for (int g0 = st; 4 * g0 < n; g0 += 4 * kSelT) {
+    float4 f[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int g = g0 + u * kSelT;
+      f[u] = 4 * g < n ? __ldcg(reinterpret_cast<const float4 *>(R) + g)
+                       : ninf4;
     }
-    for (int g = st; 4 * g < n; g += kSelT) {
-      const float4 f = __ldcg(reinterpret_cast<const float4 *>(R) + g);
-      const float vv[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int g = g0 + u * kSelT;
+      const float vv[4] = {f[u].x, f[u].y, f[u].z, f[u].w};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int j = 4 * g + c;
