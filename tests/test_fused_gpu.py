@@ -95,6 +95,21 @@ def test_fused_routes_real_valued(dsa, S, B, H, D, S_kv, ratio, topk,
     run_and_compare(dsa, q, k, w, ratio, topk, q_pos=pos)
 
 
+@pytest.mark.parametrize("topk", [512, 2048])
+def test_fused_bucket_count_boundaries(dsa, topk):
+    """The register route sizes its buckets to the row (1024, 2048 or 4096
+    for rows of at most that many keys; longer rows are read from L2).
+    Three sequences starting 100 rows below each boundary give rows of every
+    length across 1024, 2048 and 4096 visible keys."""
+    H, D, S, S_kv = 64, 128, 200, 4200
+    wl = Workload("t", B=3, S=S, S_kv=S_kv, H=H, D=D, compress_ratio=1,
+                  topk=topk, w_scale=H ** -0.5, seed=topk + 11)
+    q, k, w, _ = make_inputs(wl)
+    pos = torch.tensor([1024 - 101, 2048 - 101, 4096 - 101],
+                       dtype=torch.int32)
+    run_and_compare(dsa, q, k, w, 1, topk, q_pos=pos)
+
+
 @pytest.mark.parametrize("S,B,H,D,S_kv,ratio,topk", [
     (300, 2, 32, 128, 300, 1, 50),     # H = 32: 8 rows per work item
     (260, 1, 128, 128, 500, 2, 64),    # H = 128: 2 rows per work item
