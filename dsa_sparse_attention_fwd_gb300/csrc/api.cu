@@ -255,7 +255,7 @@ size_t dsa_indexer_workspace_size(int S, int B, int H, int D, int S_kv,
   // two-kernel path needs the logits of one chunk of query rows
   if (use_one_kernel(S, H, D, S_kv, topk))
     return kHeaderBytes + dsa::index_topk_scratch_bytes(H, S_kv);
-  return kHeaderBytes + logits_bytes(logits_chunk_rows(S, B, H, S_kv), B, S_kv);
+  return dsa::two_kernel_workspace_bytes(S, B, H, S_kv);
 }
 
 int dsa_set_prefill_policy(int policy) {
@@ -296,15 +296,22 @@ int dsa_indexer_fwd_profiled(const void *q, const void *k, const float *w,
 
 namespace dsa {
 
+size_t two_kernel_workspace_bytes(int S, int B, int H, int S_kv) {
+  return kHeaderBytes + logits_bytes(logits_chunk_rows(S, B, H, S_kv), B, S_kv);
+}
+
 // The forward behind every entry point.  clear_status = false keeps the
 // workspace's status word (several forwards sharing one workspace then
-// accumulate their device errors).
+// accumulate their device errors).  one_kernel_ok = false makes a top-k
+// prefill run scores then selection whatever the policy (for a scratch too
+// small for the one-kernel forward).
 int forward_core(const void *q, const void *k, const float *w, int S, int B,
                  int H, int D, int S_kv, int compress_ratio, int topk,
                  const int32_t *q_pos, const int32_t *in_idx, int32_t *out_idx,
                  float *out_scores, void *workspace, size_t workspace_bytes,
                  void *cuda_stream, void *const *stage_events, int n_events,
-                 bool clear_status, const uint8_t *kv_valid) {
+                 bool clear_status, const uint8_t *kv_valid,
+                 bool one_kernel_ok) {
   if (!q || !k || !w || !out_idx || !out_scores) return DSA_ERR_INVALID_ARG;
   if (kv_valid && in_idx) return DSA_ERR_UNSUPPORTED;
   int rc = check_shape(S, B, H, D, S_kv, compress_ratio);
@@ -317,15 +324,19 @@ int forward_core(const void *q, const void *k, const float *w, int S, int B,
     return DSA_ERR_INVALID_ARG;
   for (int i = 0; i < n_events; ++i)
     if (!stage_events[i]) return DSA_ERR_INVALID_ARG;
-  const size_t need = dsa_indexer_workspace_size(
-      S, B, H, D, S_kv, compress_ratio, topk, in_idx != nullptr);
+  const bool fused =
+      !in_idx && one_kernel_ok && use_one_kernel(S, H, D, S_kv, topk);
+  const size_t need =
+      !in_idx && !fused
+          ? two_kernel_workspace_bytes(S, B, H, S_kv)
+          : dsa_indexer_workspace_size(S, B, H, D, S_kv, compress_ratio, topk,
+                                       in_idx != nullptr);
   if (!workspace || workspace_bytes < need) return DSA_ERR_WORKSPACE;
   if (!aligned16(workspace)) return DSA_ERR_INVALID_ARG;
 
   DeviceInfo dev;
   rc = current_device_info(&dev);
   if (rc != DSA_OK) return rc;
-  const bool fused = !in_idx && use_one_kernel(S, H, D, S_kv, topk);
   if (!in_idx && !fused) {
     const size_t sel = dsa::topk_select_smem_bytes(S_kv, topk) + 4096;
     if (sel > (size_t)dev.max_smem_optin) return DSA_ERR_UNSUPPORTED;

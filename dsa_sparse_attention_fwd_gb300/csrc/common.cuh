@@ -153,7 +153,12 @@ int forward_core(const void *q, const void *k, const float *w, int S, int B,
                  const int32_t *q_pos, const int32_t *in_idx, int32_t *out_idx,
                  float *out_scores, void *workspace, size_t workspace_bytes,
                  void *cuda_stream, void *const *stage_events, int n_events,
-                 bool clear_status, const uint8_t *kv_valid = nullptr);
+                 bool clear_status, const uint8_t *kv_valid = nullptr,
+                 bool one_kernel_ok = true);
+
+// Workspace bytes of a top-k prefill that runs scores then selection over
+// row chunks (at most the header plus a 64 MiB logits chunk).
+size_t two_kernel_workspace_bytes(int S, int B, int H, int S_kv);
 
 cudaError_t launch_wait_selftest(int limit_us, int *status, cudaStream_t st);
 

@@ -8,6 +8,10 @@
 // rows of the one-kernel prefill or the fp32 logits of the other shapes)
 // taken from a fixed array in this file instead of a caller workspace.
 //
+// A top-k prefill whose one-kernel scratch (per-CTA score rows, which grow
+// with S_kv) does not fit the array runs scores then selection instead:
+// that path's logits chunk is at most 64 MiB, so every top-k prefill fits.
+//
 // The array is a file-scope __device__ variable: each GPU on which this
 // library's module is loaded holds its own copy until the process exits.
 // Host code cannot use the array's name as a device address (on the host
@@ -16,6 +20,7 @@
 // lookup allocates nothing and is cheap; not caching it keeps the address
 // right after a device reset or a reload of the module, where the array may
 // move.
+#include "common.cuh"
 #include "dsa_indexer.h"
 
 namespace {
@@ -39,12 +44,19 @@ extern "C" int dsa_indexer_fwd_static_scratch(
     int S_kv, int compress_ratio, int topk, const int32_t *q_pos,
     const int32_t *in_idx, int32_t *out_idx, float *out_scores,
     int32_t *out_status, void *cuda_stream) {
-  const size_t need = dsa_indexer_workspace_size(
+  size_t need = dsa_indexer_workspace_size(
       S, B, H, D, S_kv, compress_ratio, topk, in_idx != nullptr);
   if (need == 0)  // invalid shape: report the forward's own argument error
     return dsa_indexer_fwd(q, k, w, S, B, H, D, S_kv, compress_ratio, topk,
                            q_pos, in_idx, out_idx, out_scores, nullptr, 0,
                            cuda_stream);
+  bool one_kernel_ok = true;
+  if (need > (size_t)DSA_STATIC_SCRATCH_BYTES && !in_idx) {
+    // too long for the one-kernel forward's score rows: scores then
+    // selection, a bounded chunk of rows at a time
+    need = dsa::two_kernel_workspace_bytes(S, B, H, S_kv);
+    one_kernel_ok = false;
+  }
   if (need > (size_t)DSA_STATIC_SCRATCH_BYTES) return DSA_ERR_UNSUPPORTED;
   void *scratch = nullptr;
   int rc = static_scratch_address(&scratch);
@@ -52,9 +64,10 @@ extern "C" int dsa_indexer_fwd_static_scratch(
   // The forward clears the status header itself before its kernels run;
   // the rest of the array needs no clearing (every entry that is read was
   // written earlier in the same call).
-  rc = dsa_indexer_fwd(q, k, w, S, B, H, D, S_kv, compress_ratio, topk, q_pos,
-                       in_idx, out_idx, out_scores, scratch,
-                       (size_t)DSA_STATIC_SCRATCH_BYTES, cuda_stream);
+  rc = dsa::forward_core(q, k, w, S, B, H, D, S_kv, compress_ratio, topk,
+                         q_pos, in_idx, out_idx, out_scores, scratch,
+                         (size_t)DSA_STATIC_SCRATCH_BYTES, cuda_stream,
+                         nullptr, 0, true, nullptr, one_kernel_ok);
   if (rc != DSA_OK) return rc;
   if (out_status &&
       cudaMemcpyAsync(out_status, scratch, sizeof(int32_t),

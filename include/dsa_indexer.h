@@ -312,12 +312,16 @@ DSA_API int dsa_selftest_wait_limit(int limit_us, void *workspace,
  * array of DSA_STATIC_SCRATCH_BYTES inside the library instead of a caller
  * workspace; the caller still passes every input and output.
  *
- *   - Limit: problems whose dsa_indexer_workspace_size() exceeds
- *     DSA_STATIC_SCRATCH_BYTES (64 MiB plus a 256-byte header: e.g. a
- *     one-kernel prefill with H = 64 and S_kv <= 6528 whatever S, or a
- *     written-logits shape with B*S*S_kv <= 16,777,216) are refused with
- *     DSA_ERR_UNSUPPORTED before any device work.  Other argument errors
- *     are those of dsa_indexer_fwd().
+ *   - Limit: every top-k shape runs.  A prefill whose one-kernel scratch
+ *     (dsa_indexer_workspace_size(); it grows with S_kv: it fits up to
+ *     S_kv = 6496, 13056 and 26176 for H = 32, 64 and 128) exceeds
+ *     DSA_STATIC_SCRATCH_BYTES (64 MiB plus a 256-byte header) runs scores
+ *     then selection instead, whose logits chunk is at
+ *     most 64 MiB whatever S (the same results; slower on long rows).  A
+ *     given-indices shape that reads scores back from written logits (H not
+ *     in {16, 32, 64, 128}) and needs more than the array (B*S*S_kv >
+ *     16,777,216) is refused with DSA_ERR_UNSUPPORTED before any device
+ *     work.  Other argument errors are those of dsa_indexer_fwd().
  *   - Memory: every GPU that loads this part of the library holds one copy
  *     of the array until the process exits.  No call allocates or frees
  *     device memory.

@@ -183,13 +183,42 @@ def test_given_indices_and_status_word(dsa, lib):
     assert run_static(lib, q, k, w, 1, wl.topk, in_idx=gi)[2] == 0
 
 
+def test_long_rows_run_scores_then_selection(dsa, lib):
+    """Rows of 16384 keys need 84 MB of one-kernel score rows, more than the
+    fixed array: the entry point runs scores then selection over row chunks
+    instead, with the same results as the workspace forward (which takes
+    the one-kernel path here) and the oracle on sampled rows."""
+    import oracle
+    from dsa_inputs import Workload
+    from tests.helpers import compare_topk_row
+    S, S_kv, ratio, topk = 256, 16384, 4, 2048
+    wl = Workload("t", B=1, S=S, S_kv=S_kv, H=64, D=128, compress_ratio=ratio,
+                  topk=topk, w_scale=0.125, seed=41)
+    q, k, w, _ = make_inputs(wl, device="cuda")
+    # row s sits at position 47999 + s and sees 12000 + s // 4 keys
+    pos = torch.tensor([12000 * ratio - 1], dtype=torch.int32, device="cuda")
+    need = dsa.dsa_indexer_workspace_size(S, 1, 64, 128, S_kv, ratio, topk,
+                                          False)
+    assert need > STATIC_SCRATCH_BYTES
+    sc, idx, st, rc = run_static(lib, q, k, w, ratio, topk, q_pos=pos)
+    assert rc == OK and st == 0
+    ref_sc, ref_idx, ref_st = run_existing(dsa, q, k, w, ratio, topk,
+                                           q_pos=pos)
+    assert ref_st == 0
+    assert_same(sc, idx, ref_sc, ref_idx)
+    rows = np.array([0, 1, 100, 255], dtype=np.int64)
+    ref = oracle.indexer_fwd(q.cpu(), k.cpu(), w.cpu(), ratio, topk,
+                             q_pos=pos.cpu(), rows=rows, want_logits=True)
+    sc, idx = sc.reshape(-1, topk), idx.reshape(-1, topk)
+    for n, r in enumerate(rows):
+        msg = compare_topk_row(idx[r], sc[r], ref["idx"][n],
+                               ref["scores64"][n], ref["next"][n],
+                               ref["logits"][n])
+        assert msg is None, (int(r), msg)
+
+
 def test_refuses_problems_beyond_the_fixed_scratch(lib):
-    wl = WORKLOADS["long_c4"]
     fake = ctypes.c_void_p(1 << 20)  # never touched: refused before any use
-    rc = lib.dsa_indexer_fwd_static_scratch(
-        fake, fake, fake, wl.S, wl.B, wl.H, wl.D, wl.S_kv, wl.compress_ratio,
-        wl.topk, None, None, fake, fake, None, None)
-    assert rc == UNSUPPORTED
     # given indices with 4 heads read the scores back from the full [S, S_kv]
     # fp32 logits: 4096 query rows over 4096 keys fill the 64 MiB exactly,
     # one row more is refused
