@@ -17,7 +17,9 @@
 // Warp roles (576 threads, one CTA per SM):
 //   warp 0       TMA producer (Q tile per work item, K chunks through a ring)
 //   warp 1       tensor-memory allocator and MMA issuer (one thread)
-//   warps 2..9   epilogue: tensor memory -> registers, ReLU, weighted head
+//   warps 2..9   epilogue: tensor memory -> registers (a tile's 128 columns
+//                per warp in four 32-column quarters, the next quarter's
+//                load in flight while one is reduced), ReLU, weighted head
 //                sum, causal mask; each visible score goes to the item's
 //                scratch row, and each row's finite value range [lo, hi] and
 //                a non-finite flag are kept on the side
@@ -26,14 +28,17 @@
 //                other slot with the next item
 //
 // Selection of one row (n visible scores, k = topk):
-//   fast route  the scores are counted into 4096 buckets spread linearly over
-//               [lo, hi] (higher score -> lower bucket).  A scan gives the
+//   fast route  the scores are counted into NB buckets spread linearly over
+//               [lo, hi] (higher score -> lower bucket; NB = 1024, 2048 or
+//               4096, the smallest that holds a row of up to 4096 keys, else
+//               4096).  A scan gives the
 //               last bucket holding kept keys and each kept bucket's start;
 //               the kept keys are scattered to their buckets, and a key's
 //               final rank is its bucket's start plus the keys of the same
 //               bucket that precede it (larger score, or equal score and
 //               lower index).  Rows of up to 4096 keys are read once into
-//               registers, longer ones twice from L2.
+//               registers, longer ones twice from L2 (four 16-byte reads
+//               in flight per thread).
 //   exact route rows with a non-finite score, or where a kept bucket holds
 //               more than 32 keys (ties, clusters, outliers): a radix select
 //               over the order-preserving 32-bit keys (12 + 12 + 8 bits) finds
