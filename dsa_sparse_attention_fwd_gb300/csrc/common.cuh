@@ -65,6 +65,10 @@ __device__ __forceinline__ float key_to_float(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
+// Twice ReLU(x), exactly: x + |x| is 2x for x >= 0 and +0 otherwise (the
+// scoring epilogues pair it with halved weights, on the FMA pipe).
+__device__ __forceinline__ float relu2(float x) { return x + fabsf(x); }
+
 // Scoring kernel tile geometry.
 constexpr int kTileKeys = 128;      // MMA M: compressed keys per tile
 constexpr int kTileCols = 256;      // MMA N: (query, head) columns per tile

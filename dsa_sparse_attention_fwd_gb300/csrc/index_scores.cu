@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       // everyone is done with the previous weights; stop together if any
       // epilogue warp gave up on a wait
       if (named_bar_or(1, 256, !ok)) break;
-      sW[et] = w_next;
+      sW[et] = 0.5f * w_next;  // halved: see the ReLU below
       named_bar_sync(1, 256);
       int r_next;
       const ItemInfo nx = next_item(r + 1, r_next);
@@ -320,13 +320,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             for (int h = 0; h < H; h += 4) {
               const float4 wv = wq4[h >> 2];
               const int c = qq * H + h;
-              const float r0 = fmaxf(__uint_as_float(v[c >> 5][c & 31]), 0.f);
+              const float r0 = relu2(__uint_as_float(v[c >> 5][c & 31]));
               const float r1 =
-                  fmaxf(__uint_as_float(v[(c + 1) >> 5][(c + 1) & 31]), 0.f);
+                  relu2(__uint_as_float(v[(c + 1) >> 5][(c + 1) & 31]));
               const float r2 =
-                  fmaxf(__uint_as_float(v[(c + 2) >> 5][(c + 2) & 31]), 0.f);
+                  relu2(__uint_as_float(v[(c + 2) >> 5][(c + 2) & 31]));
               const float r3 =
-                  fmaxf(__uint_as_float(v[(c + 3) >> 5][(c + 3) & 31]), 0.f);
+                  relu2(__uint_as_float(v[(c + 3) >> 5][(c + 3) & 31]));
               acc2 = __ffma2_rn(make_float2(wv.x, wv.y), make_float2(r0, r1),
                                 acc2);
               acc2 = __ffma2_rn(make_float2(wv.z, wv.w), make_float2(r2, r3),
@@ -339,11 +339,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             for (int h = 0; h < H; h += 2) {
               const int c0 = qq * H + h;
               s0 = fmaf(wq[h],
-                        fmaxf(__uint_as_float(v[c0 >> 5][c0 & 31]), 0.f), s0);
+                        relu2(__uint_as_float(v[c0 >> 5][c0 & 31])), s0);
               if (h + 1 < H) {
                 const int c1 = c0 + 1;
                 s1 = fmaf(wq[h + 1],
-                          fmaxf(__uint_as_float(v[c1 >> 5][c1 & 31]), 0.f),
+                          relu2(__uint_as_float(v[c1 >> 5][c1 & 31])),
                           s1);
               }
             }

@@ -790,7 +790,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       bool got = wait_bar(slot_empty(slot), ((n_it >> 1) & 1u) ^ 1u,
                           abort_flag, status);
       if (named_bar_or(kEpiBar, 256, !(ok && got))) break;
-      sW[et] = w_next;
+      sW[et] = 0.5f * w_next;  // halved: see the ReLU below
       if (et < TQ) {
         int *s3 = stat(slot, et);
         s3[0] = kOrdPosInf;
@@ -850,10 +850,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 #pragma unroll
           for (int h = 0; h < 32; h += 4) {
             const float4 wv = wq4[h >> 2];
-            const float r0 = fmaxf(__uint_as_float(v[cur][h]), 0.f);
-            const float r1 = fmaxf(__uint_as_float(v[cur][h + 1]), 0.f);
-            const float r2 = fmaxf(__uint_as_float(v[cur][h + 2]), 0.f);
-            const float r3 = fmaxf(__uint_as_float(v[cur][h + 3]), 0.f);
+            const float r0 = relu2(__uint_as_float(v[cur][h]));
+            const float r1 = relu2(__uint_as_float(v[cur][h + 1]));
+            const float r2 = relu2(__uint_as_float(v[cur][h + 2]));
+            const float r3 = relu2(__uint_as_float(v[cur][h + 3]));
             acc2 = __ffma2_rn(make_float2(wv.x, wv.y), make_float2(r0, r1),
                               acc2);
             acc2 = __ffma2_rn(make_float2(wv.z, wv.w), make_float2(r2, r3),
