@@ -65,8 +65,10 @@ __device__ __forceinline__ float key_to_float(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// Twice ReLU(x), exactly: x + |x| is 2x for x >= 0 and +0 otherwise (the
-// scoring epilogues pair it with halved weights, on the FMA pipe).
+// Twice ReLU(x): x + |x| is 2x for x >= 0 and +0 otherwise, exactly unless
+// 2x overflows.  The scoring epilogues pair it with halved weights (exact
+// unless a weight is subnormal), so w/2 * (x + |x|) is the same product as
+// w * ReLU(x), computed on the FMA pipe instead of the integer/ALU one.
 __device__ __forceinline__ float relu2(float x) { return x + fabsf(x); }
 
 // Scoring kernel tile geometry.

@@ -267,9 +267,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         float s0 = 0.f, s1 = 0.f;
 #pragma unroll
         for (int h = 0; h < H; h += 2) {
-          s0 = fmaf(wq[h], fmaxf(__uint_as_float(v[h >> 5][h & 31]), 0.f), s0);
+          s0 = fmaf(wq[h], relu2(__uint_as_float(v[h >> 5][h & 31])), s0);
           s1 = fmaf(wq[h + 1],
-                    fmaxf(__uint_as_float(v[(h + 1) >> 5][(h + 1) & 31]), 0.f),
+                    relu2(__uint_as_float(v[(h + 1) >> 5][(h + 1) & 31])),
                     s1);
         }
         const int j = (it.tile0 + t) * kTileKeys + sp * 32 + lane;
@@ -277,7 +277,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           // a key that is not a candidate scores -inf (pool variant)
           const bool kv_ok = !KV ||
                              __ldg(kv_valid + (size_t)j * B + it.b) != 0;
-          const float sc = kv_ok ? s0 + s1 : -__int_as_float(0x7f800000);
+          // the sums are of w * 2 ReLU (x + |x|): halving them is exact
+          const float sc =
+              kv_ok ? 0.5f * (s0 + s1) : -__int_as_float(0x7f800000);
           out[j] = sc;
         }
         acc ^= 1u;

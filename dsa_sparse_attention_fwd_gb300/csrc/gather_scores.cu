@@ -399,13 +399,13 @@ __global__ void __launch_bounds__(GatRoles<H>::kThreads, 1)
 #pragma unroll
           for (int h = 0; h < H; h += 4) {
             const float4 wv = w4[h >> 2];
-            const float r0 = fmaxf(__uint_as_float(v[h >> 5][h & 31]), 0.f);
+            const float r0 = relu2(__uint_as_float(v[h >> 5][h & 31]));
             const float r1 =
-                fmaxf(__uint_as_float(v[(h + 1) >> 5][(h + 1) & 31]), 0.f);
+                relu2(__uint_as_float(v[(h + 1) >> 5][(h + 1) & 31]));
             const float r2 =
-                fmaxf(__uint_as_float(v[(h + 2) >> 5][(h + 2) & 31]), 0.f);
+                relu2(__uint_as_float(v[(h + 2) >> 5][(h + 2) & 31]));
             const float r3 =
-                fmaxf(__uint_as_float(v[(h + 3) >> 5][(h + 3) & 31]), 0.f);
+                relu2(__uint_as_float(v[(h + 3) >> 5][(h + 3) & 31]));
             a0 = __ffma2_rn(make_float2(wv.x, wv.y), make_float2(r0, r1), a0);
             a1 = __ffma2_rn(make_float2(wv.z, wv.w), make_float2(r2, r3), a1);
           }
@@ -420,10 +420,10 @@ __global__ void __launch_bounds__(GatRoles<H>::kThreads, 1)
 #pragma unroll
           for (int h = 0; h < 16; h += 4) {
             const float4 wv = w4[h >> 2];
-            const float r0 = fmaxf(__uint_as_float(v[h]), 0.f);
-            const float r1 = fmaxf(__uint_as_float(v[h + 1]), 0.f);
-            const float r2 = fmaxf(__uint_as_float(v[h + 2]), 0.f);
-            const float r3 = fmaxf(__uint_as_float(v[h + 3]), 0.f);
+            const float r0 = relu2(__uint_as_float(v[h]));
+            const float r1 = relu2(__uint_as_float(v[h + 1]));
+            const float r2 = relu2(__uint_as_float(v[h + 2]));
+            const float r3 = relu2(__uint_as_float(v[h + 3]));
             a0 = __ffma2_rn(make_float2(wv.x, wv.y), make_float2(r0, r1), a0);
             a1 = __ffma2_rn(make_float2(wv.z, wv.w), make_float2(r2, r3), a1);
           }
@@ -442,7 +442,8 @@ __global__ void __launch_bounds__(GatRoles<H>::kThreads, 1)
         if (in_row) {
           const size_t o = (size_t)row * topk + e;
           out_idx[o] = j;
-          out_scores[o] = (j >= 0 && j < nv) ? s0 + s1 : neg_inf;
+          // the sums are of w * 2 ReLU (x + |x|): halving them is exact
+          out_scores[o] = (j >= 0 && j < nv) ? 0.5f * (s0 + s1) : neg_inf;
           bad |= j < -1 || j >= S_kv;
         }
         item_end = gat_next(cur, g);

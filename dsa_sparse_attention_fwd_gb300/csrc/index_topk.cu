@@ -80,14 +80,19 @@ __device__ __forceinline__ uint32_t bslot(uint32_t b) {
   return b ^ ((b >> 4) & 15u);
 }
 
-// Descending bucket among NB of a finite score: clamp(v * sc + off) lands
-// in [2^23, 2^23 + NB - 1], where the float's low mantissa bits count up
-// with v; their complement counts down.  Monotone (non-increasing) in v.
+// Descending bucket among NB of a score: t = sat(v * sc + off) in [0, 1]
+// (sc = 1 / span, off = -lo / span), then t * (NB - 1) + 2^23 rounds to an
+// integer in [2^23, 2^23 + NB - 1] whose low mantissa bits count up with v;
+// their complement counts down.  Monotone (non-increasing) in v; both steps
+// run on the FMA pipe.
 template <int NB = kBins>
 __device__ __forceinline__ uint32_t bucket_desc(float v, float sc, float off) {
-  const float t = fminf(fmaxf(fmaf(v, sc, off), 8388608.0f),
-                        8388608.0f + (float)(NB - 1));
-  return ~__float_as_uint(t) & (uint32_t)(NB - 1);
+  float t;
+  asm("fma.rn.sat.f32 %0, %1, %2, %3;"
+      : "=f"(t)
+      : "f"(v), "f"(sc), "f"(off));
+  const float u = fmaf(t, (float)(NB - 1), 8388608.0f);
+  return ~__float_as_uint(u) & (uint32_t)(NB - 1);
 }
 
 __host__ __device__ __forceinline__ int pow2_ceil(int x) {
@@ -444,12 +449,12 @@ __device__ __forceinline__ void select_reg(const float *R, int n, int topk,
                                            float *os) {
   constexpr int G = NB / (4 * kSelT);  // float4 groups per thread
   const float neg_inf = -__int_as_float(0x7f800000);
-  float sc = 0.f, off = 8388608.0f;
+  float sc = 0.f, off = 0.f;  // bucket map, see bucket_desc
   if (hi > lo) {
     const float span = hi - lo;
     if (span <= 3.402823466e38f) {
-      sc = fminf((float)NB / span, 1e30f);
-      off = 8388608.0f - lo * sc;
+      sc = fminf(1.f / span, 1e30f);
+      off = -lo * sc;
     }
   }
   {
@@ -539,12 +544,12 @@ __device__ __forceinline__ void select_row(const float *R, int n, int topk,
     select_reg<kBins>(R, n, topk, lo, hi, st, bins, grouped, sm, oi, os);
     return;
   }
-  float sc = 0.f, off = 8388608.0f;
+  float sc = 0.f, off = 0.f;  // bucket map, see bucket_desc
   if (hi > lo) {
     const float span = hi - lo;
     if (span <= 3.402823466e38f) {
-      sc = fminf((float)kBins / span, 1e30f);
-      off = 8388608.0f - lo * sc;
+      sc = fminf(1.f / span, 1e30f);
+      off = -lo * sc;
     }
   }
   {

@@ -440,13 +440,18 @@ __device__ __forceinline__ bool bucket_topk(const float *__restrict__ L, int nv,
 // bucket "comes before" is one unsigned 64-bit comparison.
 template <int NB>
 struct RegMap {
-  float sc, off;  // bucket + 2^23 = clamp(v * sc + off)
-  // descending bucket of a value among NB: monotone non-increasing in v;
-  // -inf (and, with sc = 0, everything) lands in the last bucket
+  float sc, off;  // t = sat(v * sc + off) in [0, 1]
+  // descending bucket of a value among NB: t * (NB - 1) + 2^23 rounds to an
+  // integer whose low mantissa bits are the ascending bucket; monotone
+  // non-increasing in v, both steps on the FMA pipe; -inf (and, with sc = 0,
+  // everything) lands in the last bucket
   __device__ __forceinline__ uint32_t desc(float v) const {
-    const float t = fminf(fmaxf(fmaf(v, sc, off), 8388608.0f),
-                          8388608.0f + (float)(NB - 1));
-    return ~__float_as_uint(t) & (uint32_t)(NB - 1);
+    float t;
+    asm("fma.rn.sat.f32 %0, %1, %2, %3;"
+      : "=f"(t)
+      : "f"(v), "f"(sc), "f"(off));
+    const float u = fmaf(t, (float)(NB - 1), 8388608.0f);
+    return ~__float_as_uint(u) & (uint32_t)(NB - 1);
   }
 };
 
@@ -532,15 +537,15 @@ __device__ __forceinline__ bool bucket_topk_reg(
   if (anynan) return false;  // block-uniform; nothing written yet
   RegMap<NB> map;
   map.sc = 0.f;
-  map.off = 8388608.0f;
+  map.off = 0.f;
   if (kmin < kmax) {
     const float flo = key_to_float(kmin);
     const float span = key_to_float(kmax) - flo;
     if (span > 0.f && span <= 3.402823466e38f) {
-      map.sc = fminf((float)NB / span, 1e30f);
-      // lo * sc lands within a rounding of the bins' range; the clamp
+      map.sc = fminf(1.f / span, 1e30f);
+      // v * sc - lo * sc lands within a rounding of [0, 1]; the saturation
       // absorbs the error and keeps the map monotone
-      map.off = 8388608.0f - flo * map.sc;
+      map.off = -flo * map.sc;
     }
   }
 
