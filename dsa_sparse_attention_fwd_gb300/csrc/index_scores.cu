@@ -276,6 +276,16 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       if (nx.ntiles > 0) w_next = weight_of(nx);
       // position of query row t is qbase + t
       const long long qbase = row_pos(q_pos, it.b, 0);
+      // keys visible to the half's rows (none past the chunk's last row),
+      // kept in registers when the half has at most four rows: key j of a
+      // row counts iff j < nvq
+      constexpr int NQ = QH <= 4 ? QH : 1;
+      int nvq[NQ];
+#pragma unroll
+      for (int qq = 0; qq < NQ; ++qq) {
+        const int t = it.t0 + half * QH + qq;
+        nvq[qq] = t < s0 + S ? n_visible(qbase + t, ratio, S_kv) : 0;
+      }
 
       for (int tile = 0; tile < it.ntiles; ++tile) {
         bool got = wait_bar(acc_full(acc), aph, abort_flag, status);
@@ -350,8 +360,14 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             score = s0 + s1;
           }
           const int t = it.t0 + tq;
-          const bool vis = (long long)(j + 1) * ratio - 1 <= qbase + t;
-          if (t < s0 + S && vis && j < S_kv) {
+          bool vis;
+          if constexpr (QH <= 4) {
+            vis = j < nvq[qq];
+          } else {
+            vis = t < s0 + S && j < S_kv &&
+                  (long long)(j + 1) * ratio - 1 <= qbase + t;
+          }
+          if (vis) {
             const float sv = kv_ok ? score : -__int_as_float(0x7f800000);
             logits[((size_t)it.b * S + (t - s0)) * S_kv + j] = sv;
           }

@@ -809,6 +809,14 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       if (nx.ntiles > 0) w_next = weight_of(nx);
       const long long qbase = row_pos(q_pos, it.b, 0);
       float *srow = scratch + (size_t)(blockIdx.x * 2 + slot) * TQ * row_stride;
+      // keys visible to the half's rows (none past the last row): key j of
+      // a row counts iff j < nvq
+      int nvq[QH];
+#pragma unroll
+      for (int qq = 0; qq < QH; ++qq) {
+        const int t = it.t0 + half * QH + qq;
+        nvq[qq] = t < S ? n_visible(qbase + t, ratio, S_kv) : 0;
+      }
 
       float lo[QH], hi[QH];
 #pragma unroll
@@ -876,9 +884,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           }
           if (h0 + 32 < H) continue;  // the row goes on in the next quarter
           const float score = acc2.x + acc2.y;
-          const int t = it.t0 + tq;
-          const bool vis = (long long)(j + 1) * ratio - 1 <= qbase + t;
-          if (t < S && vis && j < S_kv) {
+          if (j < nvq[qq]) {
             float *dst = srow + (size_t)tq * row_stride + j;
             if (kv_ok) {
               *dst = score;
