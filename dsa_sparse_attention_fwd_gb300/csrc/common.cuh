@@ -70,6 +70,10 @@ __device__ __forceinline__ float key_to_float(uint32_t k) {
 // unless a weight is subnormal), so w/2 * (x + |x|) is the same product as
 // w * ReLU(x), computed on the FMA pipe instead of the integer/ALU one.
 __device__ __forceinline__ float relu2(float x) { return x + fabsf(x); }
+// relu2 of two values with one packed add (the same result lane by lane).
+__device__ __forceinline__ float2 relu2x2(float a, float b) {
+  return __fadd2_rn(make_float2(a, b), make_float2(fabsf(a), fabsf(b)));
+}
 
 // Scoring kernel tile geometry.
 constexpr int kTileKeys = 128;      // MMA M: compressed keys per tile

@@ -399,15 +399,14 @@ __global__ void __launch_bounds__(GatRoles<H>::kThreads, 1)
 #pragma unroll
           for (int h = 0; h < H; h += 4) {
             const float4 wv = w4[h >> 2];
-            const float r0 = relu2(__uint_as_float(v[h >> 5][h & 31]));
-            const float r1 =
-                relu2(__uint_as_float(v[(h + 1) >> 5][(h + 1) & 31]));
-            const float r2 =
-                relu2(__uint_as_float(v[(h + 2) >> 5][(h + 2) & 31]));
-            const float r3 =
-                relu2(__uint_as_float(v[(h + 3) >> 5][(h + 3) & 31]));
-            a0 = __ffma2_rn(make_float2(wv.x, wv.y), make_float2(r0, r1), a0);
-            a1 = __ffma2_rn(make_float2(wv.z, wv.w), make_float2(r2, r3), a1);
+            const float2 r01 =
+                relu2x2(__uint_as_float(v[h >> 5][h & 31]),
+                        __uint_as_float(v[(h + 1) >> 5][(h + 1) & 31]));
+            const float2 r23 =
+                relu2x2(__uint_as_float(v[(h + 2) >> 5][(h + 2) & 31]),
+                        __uint_as_float(v[(h + 3) >> 5][(h + 3) & 31]));
+            a0 = __ffma2_rn(make_float2(wv.x, wv.y), r01, a0);
+            a1 = __ffma2_rn(make_float2(wv.z, wv.w), r23, a1);
           }
         } else {
           uint32_t v[16];
@@ -420,12 +419,12 @@ __global__ void __launch_bounds__(GatRoles<H>::kThreads, 1)
 #pragma unroll
           for (int h = 0; h < 16; h += 4) {
             const float4 wv = w4[h >> 2];
-            const float r0 = relu2(__uint_as_float(v[h]));
-            const float r1 = relu2(__uint_as_float(v[h + 1]));
-            const float r2 = relu2(__uint_as_float(v[h + 2]));
-            const float r3 = relu2(__uint_as_float(v[h + 3]));
-            a0 = __ffma2_rn(make_float2(wv.x, wv.y), make_float2(r0, r1), a0);
-            a1 = __ffma2_rn(make_float2(wv.z, wv.w), make_float2(r2, r3), a1);
+            const float2 r01 = relu2x2(__uint_as_float(v[h]),
+                                       __uint_as_float(v[h + 1]));
+            const float2 r23 = relu2x2(__uint_as_float(v[h + 2]),
+                                       __uint_as_float(v[h + 3]));
+            a0 = __ffma2_rn(make_float2(wv.x, wv.y), r01, a0);
+            a1 = __ffma2_rn(make_float2(wv.z, wv.w), r23, a1);
           }
         }
         const float s0 = a0.x + a0.y, s1 = a1.x + a1.y;

@@ -330,17 +330,14 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             for (int h = 0; h < H; h += 4) {
               const float4 wv = wq4[h >> 2];
               const int c = qq * H + h;
-              const float r0 = relu2(__uint_as_float(v[c >> 5][c & 31]));
-              const float r1 =
-                  relu2(__uint_as_float(v[(c + 1) >> 5][(c + 1) & 31]));
-              const float r2 =
-                  relu2(__uint_as_float(v[(c + 2) >> 5][(c + 2) & 31]));
-              const float r3 =
-                  relu2(__uint_as_float(v[(c + 3) >> 5][(c + 3) & 31]));
-              acc2 = __ffma2_rn(make_float2(wv.x, wv.y), make_float2(r0, r1),
-                                acc2);
-              acc2 = __ffma2_rn(make_float2(wv.z, wv.w), make_float2(r2, r3),
-                                acc2);
+              const float2 r01 =
+                  relu2x2(__uint_as_float(v[c >> 5][c & 31]),
+                          __uint_as_float(v[(c + 1) >> 5][(c + 1) & 31]));
+              const float2 r23 =
+                  relu2x2(__uint_as_float(v[(c + 2) >> 5][(c + 2) & 31]),
+                          __uint_as_float(v[(c + 3) >> 5][(c + 3) & 31]));
+              acc2 = __ffma2_rn(make_float2(wv.x, wv.y), r01, acc2);
+              acc2 = __ffma2_rn(make_float2(wv.z, wv.w), r23, acc2);
             }
             score = acc2.x + acc2.y;
           } else {

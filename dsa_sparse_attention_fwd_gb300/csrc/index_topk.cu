@@ -863,14 +863,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 #pragma unroll
           for (int h = 0; h < 32; h += 4) {
             const float4 wv = wq4[h >> 2];
-            const float r0 = relu2(__uint_as_float(v[cur][h]));
-            const float r1 = relu2(__uint_as_float(v[cur][h + 1]));
-            const float r2 = relu2(__uint_as_float(v[cur][h + 2]));
-            const float r3 = relu2(__uint_as_float(v[cur][h + 3]));
-            acc2 = __ffma2_rn(make_float2(wv.x, wv.y), make_float2(r0, r1),
-                              acc2);
-            acc2 = __ffma2_rn(make_float2(wv.z, wv.w), make_float2(r2, r3),
-                              acc2);
+            const float2 r01 = relu2x2(__uint_as_float(v[cur][h]),
+                                       __uint_as_float(v[cur][h + 1]));
+            const float2 r23 = relu2x2(__uint_as_float(v[cur][h + 2]),
+                                       __uint_as_float(v[cur][h + 3]));
+            acc2 = __ffma2_rn(make_float2(wv.x, wv.y), r01, acc2);
+            acc2 = __ffma2_rn(make_float2(wv.z, wv.w), r23, acc2);
           }
           if (qt < 3) {
             tmem_ld_wait();
