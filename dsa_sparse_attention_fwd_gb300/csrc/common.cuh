@@ -67,8 +67,10 @@ __device__ __forceinline__ float key_to_float(uint32_t k) {
 
 // Twice ReLU(x): x + |x| is 2x for x >= 0 and +0 otherwise, exactly unless
 // 2x overflows.  The scoring epilogues pair it with halved weights (exact
-// unless a weight is subnormal), so w/2 * (x + |x|) is the same product as
-// w * ReLU(x), computed on the FMA pipe instead of the integer/ALU one.
+// unless a weight is subnormal: w/2 * (x + |x|) is the same product as
+// w * ReLU(x)) or halve the finished sum (every term and partial sum was
+// exactly doubled), and it runs on the FMA pipe instead of the integer/ALU
+// one.
 __device__ __forceinline__ float relu2(float x) { return x + fabsf(x); }
 // relu2 of two values with one packed add (the same result lane by lane).
 __device__ __forceinline__ float2 relu2x2(float a, float b) {
