@@ -2,7 +2,7 @@
 // sorted by descending score with equal scores ordered by ascending key
 // index; the rest of the row is -1 / -inf.
 //
-// One CTA per row: 256 threads when there are many rows, 1024 when there
+// One CTA per row: 256 threads when there are many rows, 512 when there
 // are fewer rows than SMs.  Scores are compared as order-preserving unsigned
 // keys (larger float <-> larger key; -0.0 folded onto +0.0 so the index
 // tie-break decides between them).
@@ -44,7 +44,7 @@ namespace dsa {
 namespace {
 
 constexpr int kSelThreads = 256;       // threads per row, many rows
-constexpr int kSelThreadsWide = 1024;  // threads per row, few rows
+constexpr int kSelThreadsWide = 512;   // threads per row, few rows
 constexpr int kSelMaxWarps = kSelThreadsWide / 32;
 constexpr int kHistBins = 4096;  // 12-bit select digit
 constexpr int kSelSlack = 256;   // extra candidates a one-pass select keeps
@@ -432,7 +432,8 @@ __device__ __forceinline__ bool bucket_topk(const float *__restrict__ L, int nv,
 
 // The same route for rows of at most R * NT keys, held in registers: thread
 // t owns keys 4(t + NT i) + c (c < 4, i < R/4), read as float4 when the row
-// is 16-byte aligned, over NB buckets (NB = R * NT: 1024, 2048 or 4096).
+// is 16-byte aligned, over NB buckets (1024, 2048 or 4096: R * NT, or half
+// of it for rows of up to 8192 keys in a 512-thread CTA).
 // The bucket map here is a clamped fused multiply-add whose result lands in
 // [2^23, 2^23 + NB - 1], where the float's low mantissa bits are the
 // bucket; rows holding a NaN take the radix route.  A kept key
@@ -678,7 +679,9 @@ __global__ void __launch_bounds__(NT, NT == kSelThreads ? 4 : 1)
   // the bucket route first; the radix route takes the rows it declines
   if (topk <= kBucketMaxTopk) {
     constexpr int R = kBucketBins / NT;  // keys per thread in registers
-    if (nv <= R * NT) {
+    // a 512-thread CTA holds rows of up to 8192 keys, 16 per thread
+    constexpr int RW = NT == kSelThreadsWide ? 2 * R : R;
+    if (nv <= RW * NT) {
       const bool vec = (S_kv & 3) == 0 &&
                        (reinterpret_cast<uintptr_t>(L) & 15u) == 0;
       // as many buckets as the row has keys, rounded up to 1024, 2048 or
@@ -695,6 +698,13 @@ __global__ void __launch_bounds__(NT, NT == kSelThreads ? 4 : 1)
         else
           done = bucket_topk_reg<NT, R, kBucketBins>(L, nv, topk, vec, bins,
                                                      bufA, sh, oi, os);
+      } else if constexpr (RW != R) {
+        if (nv <= R * NT)
+          done = bucket_topk_reg<NT, R, kBucketBins>(L, nv, topk, vec, bins,
+                                                     bufA, sh, oi, os);
+        else
+          done = bucket_topk_reg<NT, RW, kBucketBins>(L, nv, topk, vec, bins,
+                                                      bufA, sh, oi, os);
       } else {
         done = bucket_topk_reg<NT, R, kBucketBins>(L, nv, topk, vec, bins,
                                                    bufA, sh, oi, os);
@@ -1057,8 +1067,8 @@ size_t topk_select_smem_bytes(int S_kv, int topk) {
   return sel_layout(S_kv, topk, false, kSelThreads).dyn + sizeof(SelShared);
 }
 
-// Shared memory the wide (1024-thread) variant may take: its per-warp sort
-// counters need 32 KB, which the key region usually covers already.
+// Shared memory the wide (512-thread) variant may take: its per-warp sort
+// counters need 16 KB, which the key region usually covers already.
 constexpr size_t kWideSmemCap = 160 * 1024;
 
 cudaError_t launch_topk_select(const Problem &p, const float *logits, int topk,
@@ -1066,12 +1076,12 @@ cudaError_t launch_topk_select(const Problem &p, const float *logits, int topk,
                                int num_sms, cudaStream_t st, int s0, int Sc) {
   const bool unstaged = unstaged_rows(p, Sc);
   const int mcap = sel_layout(p.S_kv, topk, unstaged, kSelThreads).mcap;
-  // Fewer rows than SMs: each row gets 1024 threads, so a row's passes
-  // take a quarter of the iterations (the rows run side by side anyway).
+  // Fewer rows than SMs: each row gets 512 threads, so a row's passes
+  // take half the iterations (the rows run side by side anyway).
   const long long rows = (long long)p.B * Sc;
-  if (rows < num_sms && mcap <= kSelThreadsWide * 4 &&
+  if (rows < num_sms && mcap <= kSelThreadsWide * 8 &&
       sel_layout(p.S_kv, topk, unstaged, kSelThreadsWide).dyn <= kWideSmemCap)
-    return launch_sel<4, kSelThreadsWide>(p, logits, topk, out_idx,
+    return launch_sel<8, kSelThreadsWide>(p, logits, topk, out_idx,
                                           out_scores, st, s0, Sc);
   if (mcap <= kSelThreads * 8)
     return launch_sel<8, kSelThreads>(p, logits, topk, out_idx,

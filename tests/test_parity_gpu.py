@@ -11,6 +11,8 @@ them one by one) plus invariants checked on every row.
 """
 from __future__ import annotations
 
+import contextlib
+
 import numpy as np
 import pytest
 import torch
@@ -39,6 +41,16 @@ def gpu_run(dsa, q, k, w, ratio, topk, q_pos=None, in_idx=None):
                                       in_idx=gd)
     status = dsa.dsa_indexer_check(ws)
     return sc.cpu().numpy(), idx.cpu().numpy(), status
+
+
+@contextlib.contextmanager
+def prefill_policy(dsa, policy):
+    """Run a block under a prefill top-k policy, then restore automatic."""
+    dsa.dsa_set_prefill_policy(policy)
+    try:
+        yield
+    finally:
+        dsa.dsa_set_prefill_policy(dsa.PREFILL_AUTO)
 
 
 def row_nvis(S, B, ratio, S_kv, q_pos=None):
@@ -315,16 +327,19 @@ def test_decode_path_match_oracle(dsa, S, B, H, D, S_kv, ratio, topk):
     assert np.all(np.abs(L[fin] - R[fin]) <= score_tol(R[fin]))
 
 
+@pytest.mark.parametrize("policy", ["auto", "two"])
 @pytest.mark.parametrize("S,B,S_kv,ratio,topk", [
     (42, 2, 9000, 4, 512),    # ragged query tail and key tail
     (9, 1, 8192, 1, 2048),    # exactly 64 key tiles, large topk
 ])
-def test_long_rows(dsa, S, B, S_kv, ratio, topk):
-    """Rows of more than 4096 visible keys: the selection's bucket route
-    with the row staged in shared memory (few rows) rather than held in
-    registers.  Query positions deep into the sequence give every row
-    thousands of visible keys while keeping the rows few enough for the
-    oracle."""
+def test_long_rows(dsa, S, B, S_kv, ratio, topk, policy):
+    """Rows of more than 4096 visible keys.  Under the automatic policy
+    these shapes (at least 8192 keys) run the one-kernel forward; forced to
+    two kernels, fewer rows than SMs take the 512-thread selection, which
+    holds rows of up to 8192 keys in registers, 16 per thread, and stages
+    longer ones in shared memory.  Query positions deep into the sequence
+    give every row thousands of visible keys while keeping the rows few
+    enough for the oracle."""
     H, D = 64, 128
     wl = Workload("t", B=B, S=S, S_kv=S_kv, H=H, D=D, compress_ratio=ratio,
                   topk=topk, w_scale=H ** -0.5, seed=S_kv + S)
@@ -333,7 +348,9 @@ def test_long_rows(dsa, S, B, S_kv, ratio, topk):
     pos = rng.integers(S_kv * ratio // 2, S_kv * ratio, size=B)
     pos[-1] = S_kv * ratio - S // 2   # the last rows see every key
     pos = torch.from_numpy(pos.astype(np.int32))
-    sc, idx, st = gpu_run(dsa, q, k, w, ratio, topk, q_pos=pos)
+    pol = {"auto": dsa.PREFILL_AUTO, "two": dsa.PREFILL_TWO_KERNELS}[policy]
+    with prefill_policy(dsa, pol):
+        sc, idx, st = gpu_run(dsa, q, k, w, ratio, topk, q_pos=pos)
     assert st == 0
     sc = sc.reshape(B, S, topk)
     idx = idx.reshape(B, S, topk)
@@ -341,6 +358,56 @@ def test_long_rows(dsa, S, B, S_kv, ratio, topk):
     ref = oracle.indexer_fwd(q, k, w, ratio, topk, q_pos=pos,
                              want_logits=True)
     compare_rows(sc, idx, ref, np.arange(B * S), S)
+
+
+@pytest.mark.parametrize("topk", [512, 2048])
+def test_wide_selection_row_length_boundaries(dsa, topk):
+    """Fewer rows than SMs take the 512-thread selection, which holds rows
+    of up to 4096 keys eight per thread, rows of up to 8192 keys 16 per
+    thread, and stages longer rows in shared memory.  Two sequences whose
+    positions start just below 4096 and 8192 visible keys give 40 rows
+    across both boundaries."""
+    H, D, S, S_kv, B = 64, 128, 20, 8300, 2
+    wl = Workload("t", B=B, S=S, S_kv=S_kv, H=H, D=D, compress_ratio=1,
+                  topk=topk, w_scale=H ** -0.5, seed=topk + 8300)
+    q, k, w, _ = make_inputs(wl)
+    pos = torch.tensor([4096 - 11, 8192 - 11], dtype=torch.int32)
+    nvis = row_nvis(S, B, 1, S_kv, pos)
+    for edge in (4096, 8192):
+        assert np.any(nvis == edge) and np.any(nvis == edge + 1)
+    # S_kv >= 8192 would run the one-kernel forward under the automatic
+    # policy
+    with prefill_policy(dsa, dsa.PREFILL_TWO_KERNELS):
+        sc, idx, st = gpu_run(dsa, q, k, w, 1, topk, q_pos=pos)
+    assert st == 0
+    sc = sc.reshape(B, S, topk)
+    idx = idx.reshape(B, S, topk)
+    check_invariants(sc, idx, nvis, topk)
+    ref = oracle.indexer_fwd(q, k, w, 1, topk, q_pos=pos, want_logits=True)
+    compare_rows(sc, idx, ref, np.arange(B * S), S)
+
+
+def test_wide_selection_long_rows_ties_bit_exact(dsa):
+    """Integer q, k and dyadic w on few rows of 5000 to 8192 keys: every
+    score is exact and heavy ties crowd the fine buckets, so the 512-thread
+    selection leaves its register route for the radix route.  Order must
+    match the oracle exactly."""
+    rng = np.random.default_rng(8192)
+    S, B, S_kv, H, D, topk = 6, 2, 8192, 16, 32, 512
+    qi = rng.integers(-2, 3, size=(S, B, H, D)).astype(np.float32)
+    ki = rng.integers(-2, 3, size=(S_kv, B, D)).astype(np.float32)
+    wi = rng.choice([1, -1, 0.5, -0.5], size=(S, B, H)).astype(np.float32)
+    q = torch.from_numpy(qi).to(torch.bfloat16)
+    k = torch.from_numpy(ki).to(torch.bfloat16)
+    w = torch.from_numpy(wi)
+    pos = torch.tensor([5000, 8186], dtype=torch.int32)
+    # (H = 16 has no one-kernel forward; forced all the same)
+    with prefill_policy(dsa, dsa.PREFILL_TWO_KERNELS):
+        sc, idx, st = gpu_run(dsa, q, k, w, 1, topk, q_pos=pos)
+    assert st == 0
+    ref = oracle.indexer_fwd(q, k, w, 1, topk, q_pos=pos)
+    np.testing.assert_array_equal(idx.reshape(-1, topk), ref["idx"])
+    np.testing.assert_array_equal(sc.reshape(-1, topk), ref["scores"])
 
 
 @pytest.mark.parametrize("topk", [512, 2048])
@@ -374,7 +441,7 @@ def test_selection_bucket_count_boundaries(dsa, topk):
                                                 (300, None), (100, 8),
                                                 (300, 8)])
 def test_integer_inputs_bit_exact_few_rows(dsa, topk, distinct_keys):
-    """Fewer rows than SMs take the 1024-thread selection.  Integer q, k and
+    """Fewer rows than SMs take the 512-thread selection.  Integer q, k and
     dyadic w make every score exact and produce runs of tied scores; with
     only 8 distinct key vectors the runs exceed the fix-up's limit and the
     full-sort fallback runs.  Order must match the oracle exactly."""
@@ -404,7 +471,7 @@ def test_far_outlier_rows_bit_exact(dsa, S, B, outlier):
     buckets, and those rows must leave the bucket route for the radix
     route.  Integer q, k and dyadic w keep every score exact, so the order
     must match the oracle exactly (many rows: 256-thread selection; 80 rows:
-    1024-thread selection)."""
+    512-thread selection)."""
     rng = np.random.default_rng(77 + S)
     H, D, S_kv, topk = 16, 32, 290, 60
     qi = rng.integers(-2, 3, size=(S, B, H, D)).astype(np.float32)
