@@ -7,9 +7,11 @@
 // keys (larger float <-> larger key; -0.0 folded onto +0.0 so the index
 // tie-break decides between them).
 //
-// Bucket route (every row first): the row -- in registers up to 4096 keys,
-// else staged in shared memory when it fits, else read from L2 -- is counted
-// into 4096 fine buckets spread linearly over its finite value range.  A
+// Bucket route (every row first): the row -- in registers up to 4096 keys
+// (8192 in a 512-thread CTA), else staged in shared memory when it fits,
+// else read from L2 -- is counted into fine buckets spread linearly over
+// its finite value range (4096, or for a row held in registers as many as
+// it has keys rounded up to 1024, 2048 or 4096).  A
 // scan of the counts gives the bucket holding the topk-th key and each
 // kept bucket's start; the kept keys are scattered to their buckets and
 // each key's final position is its bucket start plus the number of keys of
