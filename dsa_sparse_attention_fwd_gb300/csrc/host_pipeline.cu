@@ -2,12 +2,18 @@
 // copies pipelined against the kernels.
 //
 // The query rows are split into chunks along S (rows [s0, s1) of every
-// sequence), taken last rows first (under the causal mask the later rows
-// cost the most, so the chunk left after the last copy is the cheapest).
-// One stream copies the inputs in (k and w first, then the q rows of each
-// chunk), the caller's stream runs each chunk's forward as soon as its rows
-// have landed, and a third stream copies each chunk's indices and scores
-// back while the next chunks are scored.  Every row's result is
+// sequence).  One stream copies the inputs in (k and w first, then the q
+// rows of each chunk), the caller's stream runs each chunk's forward as
+// soon as its rows have landed, and a third stream copies each chunk's
+// indices and scores back while the next chunks are scored.  Under the
+// causal mask a chunk's cost grows with its rows' positions while its
+// copies do not, so the chunk order matters:
+//  - link-bound shapes (few visible keys per copied byte) take the last
+//    rows first, so the chunk left after the last copy is the cheapest;
+//  - compute-bound shapes alternate the costliest and the cheapest chunk
+//    left (last, first, second last, second, ...): taken last rows first,
+//    their cheap chunks at the end finish scoring faster than their results
+//    can be copied out and the copies back up behind the kernels.  Every row's result is
 // bit-identical to one unchunked call: no row's arithmetic depends on the
 // other rows.  A chunk after the first sees its rows through per-chunk
 // query positions (q_pos[b] + s0, or s0 for prefill).
@@ -42,6 +48,41 @@ int chunk_start(int S, int chunks, int i) {
   if (i >= chunks) return S;
   const long long s = ((long long)S * i / chunks) & ~3ll;
   return (int)s;
+}
+
+// Tensor-core FLOPs the kernels run per byte crossing the host link, above
+// which the pipeline is compute-bound: about the one-kernel forward's rate
+// (1.3 PFLOP/s) over the link's rate with copies both ways (0.34 TB/s),
+// discounted.
+constexpr double kComputeBoundFlopPerByte = 3000.0;
+
+// Processing order of the chunks (see the file comment): ord[n] is the
+// n-th chunk to copy in, score and copy out.  The cost estimate takes each
+// chunk's middle row per sequence as its average row.
+void chunk_order(int S, int B, int H, int D, int S_kv, int ratio, int topk,
+                 const int32_t *q_pos, bool has_in_idx, int C, int *ord) {
+  double flops = 0.0, bytes = 0.0;
+  for (int i = 0; i < C; ++i) {
+    const int s0 = chunk_start(S, C, i), s1 = chunk_start(S, C, i + 1);
+    const int mid = s0 + (s1 - s0) / 2;
+    for (int b = 0; b < B; ++b) {
+      const long long pos = (q_pos ? (long long)q_pos[b] : 0) + mid;
+      int n = dsa::n_visible(pos, ratio, S_kv);
+      if (has_in_idx && n > topk) n = topk;
+      flops += 2.0 * H * D * (double)n * (s1 - s0);
+    }
+  }
+  // q and w in, indices and scores out (and given indices in)
+  bytes = (double)S * B * ((double)H * D * 2 + (double)H * 4 +
+                           (double)topk * (has_in_idx ? 12 : 8));
+  const bool alternate = flops > kComputeBoundFlopPerByte * bytes;
+  int lo = 0, hi = C - 1;
+  for (int n = 0; n < C; ++n) {
+    if (!alternate || (n & 1) == 0)
+      ord[n] = hi--;
+    else
+      ord[n] = lo++;
+  }
 }
 
 struct HostLayout {
@@ -192,6 +233,9 @@ int dsa_indexer_fwd_host(const void *q, const void *k, const float *w, int S,
             (q_pos ? q_pos[b] : 0) + chunk_start(S, C, i);
   bool ok = true;
   auto chk = [&](cudaError_t e) { ok = ok && e == cudaSuccess; };
+  int ord[kMaxChunks];
+  chunk_order(S, B, H, D, S_kv, compress_ratio, topk, q_pos,
+              in_idx != nullptr, C, ord);
 
   // inputs: k, w, positions, then each chunk's q rows (and given indices)
   chk(cudaEventRecord(P.start, st));
@@ -203,10 +247,8 @@ int dsa_indexer_fwd_host(const void *q, const void *k, const float *w, int S,
   if (chunk_pos)
     chk(cudaMemcpyAsync(base + L.pos, pos_h, (size_t)C * B * 4,
                         cudaMemcpyHostToDevice, P.in));
-  // chunks go last-rows-first: under the causal mask the later rows are the
-  // costly ones, so the cheapest chunk is the one left after the last copy
   for (int n = 0; n < C && ok; ++n) {
-    const int i = C - 1 - n;
+    const int i = ord[n];
     const int s0 = chunk_start(S, C, i), rows = chunk_start(S, C, i + 1) - s0;
     chk(cudaMemcpyAsync(base + L.q + (size_t)s0 * q_row,
                         static_cast<const char *>(q) + (size_t)s0 * q_row,
@@ -221,7 +263,7 @@ int dsa_indexer_fwd_host(const void *q, const void *k, const float *w, int S,
 
   // each chunk's forward on the caller's stream, then its results out
   for (int n = 0; n < C && ok; ++n) {
-    const int i = C - 1 - n;
+    const int i = ord[n];
     const int s0 = chunk_start(S, C, i), rows = chunk_start(S, C, i + 1) - s0;
     chk(cudaStreamWaitEvent(st, P.in_done[i], 0));
     if (!ok) break;

@@ -99,3 +99,23 @@ def test_host_given_indices_and_status(dsa):
     h_sc, h_idx, h_rc = host_run(dsa, q, k, w, ratio, topk, in_idx=gi)
     assert h_rc == 6  # DSA_ERR_INDEX_RANGE
     assert np.isneginf(h_sc[1, 2000, 5]) and h_idx[1, 2000, 5] == S_kv
+
+
+def test_host_compute_bound_chunk_order(dsa):
+    """Rows deep into a long sequence give many visible keys per copied
+    byte (above 3000 FLOP per byte), so the chunks are processed
+    alternately from the costly and the cheap end (4 chunks); every row's
+    result must still equal the device-buffer forward bit for bit."""
+    S, B, H, D, S_kv, ratio, topk = 2048, 1, 64, 128, 8192, 1, 64
+    wl = Workload("h", B=B, S=S, S_kv=S_kv, H=H, D=D, compress_ratio=ratio,
+                  topk=topk, w_scale=H ** -0.5, seed=4099)
+    q, k, w, _ = make_inputs(wl)
+    q_pos = torch.tensor([4096], dtype=torch.int32)
+    # 2 H D n_vis per row against q, w, indices and scores per row
+    nv = np.minimum(S_kv, (4096 + np.arange(S) + 1) // ratio)
+    assert (2 * H * D * nv.sum()) / (S * (2 * H * D + 4 * H + 8 * topk)) > 3000
+    d_sc, d_idx, d_st = device_run(dsa, q, k, w, ratio, topk, q_pos=q_pos)
+    h_sc, h_idx, h_rc = host_run(dsa, q, k, w, ratio, topk, q_pos=q_pos)
+    assert d_st == 0 and h_rc == 0
+    np.testing.assert_array_equal(h_idx, d_idx)
+    assert same_bits(h_sc, d_sc)
