@@ -44,9 +44,31 @@ int plan_chunks(int S) {
   return c < 1 ? 1 : c;
 }
 
-int chunk_start(int S, int chunks, int i) {
+// Query rows per wave of prefill work items on this device (one item is
+// 256/H rows of one sequence, one CTA per SM): chunk starts on whole waves
+// leave no part-filled last wave in each chunk's launch.  4 when unknown.
+int wave_rows(int B, int H) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+          cudaSuccess ||
+      sms <= 0 || H <= 0 || B <= 0)
+    return 4;
+  const long long tq = H < 256 ? 256 / H : 1;
+  const long long u = ((long long)sms * tq / B) & ~3ll;
+  return u < 4 ? 4 : (u > (1 << 20) ? (1 << 20) : (int)u);
+}
+
+// Start of chunk i: an even split, on a multiple of 4 rows, moved to the
+// nearest whole wave of `unit` rows when the chunks hold at least one
+// (starts then still increase and stay below S).
+int chunk_start(int S, int chunks, int i, int unit) {
   if (i >= chunks) return S;
-  const long long s = ((long long)S * i / chunks) & ~3ll;
+  long long s = (long long)S * i / chunks;
+  if (unit > 4 && S / chunks >= unit)
+    s = (s + unit / 2) / unit * unit;
+  else
+    s &= ~3ll;
   return (int)s;
 }
 
@@ -60,10 +82,12 @@ constexpr double kComputeBoundFlopPerByte = 3000.0;
 // n-th chunk to copy in, score and copy out.  The cost estimate takes each
 // chunk's middle row per sequence as its average row.
 void chunk_order(int S, int B, int H, int D, int S_kv, int ratio, int topk,
-                 const int32_t *q_pos, bool has_in_idx, int C, int *ord) {
+                 const int32_t *q_pos, bool has_in_idx, int C, int unit,
+                 int *ord) {
   double flops = 0.0, bytes = 0.0;
   for (int i = 0; i < C; ++i) {
-    const int s0 = chunk_start(S, C, i), s1 = chunk_start(S, C, i + 1);
+    const int s0 = chunk_start(S, C, i, unit);
+    const int s1 = chunk_start(S, C, i + 1, unit);
     const int mid = s0 + (s1 - s0) / 2;
     for (int b = 0; b < B; ++b) {
       const long long pos = (q_pos ? (long long)q_pos[b] : 0) + mid;
@@ -86,7 +110,7 @@ void chunk_order(int S, int B, int H, int D, int S_kv, int ratio, int topk,
 }
 
 struct HostLayout {
-  int chunks = 1, max_rows = 0;
+  int chunks = 1, max_rows = 0, unit = 4;
   size_t k = 0, q = 0, w = 0, pos = 0, in_idx = 0, out_idx = 0, out_sc = 0,
          status = 0, ws = 0, ws_bytes = 0, total = 0;
 };
@@ -95,8 +119,10 @@ HostLayout host_layout(int S, int B, int H, int D, int S_kv, int ratio,
                        int topk, bool has_in_idx) {
   HostLayout L;
   L.chunks = plan_chunks(S);
+  L.unit = wave_rows(B, H);
   for (int i = 0; i < L.chunks; ++i) {
-    const int r = chunk_start(S, L.chunks, i + 1) - chunk_start(S, L.chunks, i);
+    const int r = chunk_start(S, L.chunks, i + 1, L.unit) -
+                  chunk_start(S, L.chunks, i, L.unit);
     if (r > L.max_rows) L.max_rows = r;
   }
   L.ws_bytes = dsa_indexer_workspace_size(L.max_rows, B, H, D, S_kv, ratio,
@@ -230,12 +256,12 @@ int dsa_indexer_fwd_host(const void *q, const void *k, const float *w, int S,
     for (int i = 0; i < C; ++i)
       for (int b = 0; b < B; ++b)
         pos_h[(size_t)i * B + b] =
-            (q_pos ? q_pos[b] : 0) + chunk_start(S, C, i);
+            (q_pos ? q_pos[b] : 0) + chunk_start(S, C, i, L.unit);
   bool ok = true;
   auto chk = [&](cudaError_t e) { ok = ok && e == cudaSuccess; };
   int ord[kMaxChunks];
   chunk_order(S, B, H, D, S_kv, compress_ratio, topk, q_pos,
-              in_idx != nullptr, C, ord);
+              in_idx != nullptr, C, L.unit, ord);
 
   // inputs: k, w, positions, then each chunk's q rows (and given indices)
   chk(cudaEventRecord(P.start, st));
@@ -249,7 +275,8 @@ int dsa_indexer_fwd_host(const void *q, const void *k, const float *w, int S,
                         cudaMemcpyHostToDevice, P.in));
   for (int n = 0; n < C && ok; ++n) {
     const int i = ord[n];
-    const int s0 = chunk_start(S, C, i), rows = chunk_start(S, C, i + 1) - s0;
+    const int s0 = chunk_start(S, C, i, L.unit);
+    const int rows = chunk_start(S, C, i + 1, L.unit) - s0;
     chk(cudaMemcpyAsync(base + L.q + (size_t)s0 * q_row,
                         static_cast<const char *>(q) + (size_t)s0 * q_row,
                         (size_t)rows * q_row, cudaMemcpyHostToDevice, P.in));
@@ -264,7 +291,8 @@ int dsa_indexer_fwd_host(const void *q, const void *k, const float *w, int S,
   // each chunk's forward on the caller's stream, then its results out
   for (int n = 0; n < C && ok; ++n) {
     const int i = ord[n];
-    const int s0 = chunk_start(S, C, i), rows = chunk_start(S, C, i + 1) - s0;
+    const int s0 = chunk_start(S, C, i, L.unit);
+    const int rows = chunk_start(S, C, i + 1, L.unit) - s0;
     chk(cudaStreamWaitEvent(st, P.in_done[i], 0));
     if (!ok) break;
     const size_t oo = (size_t)B * s0 * topk4;  // chunk block offset

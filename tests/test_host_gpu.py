@@ -60,8 +60,8 @@ def test_host_path_equals_device_path(dsa, name):
 
 
 @pytest.mark.parametrize("S,B,H,D,S_kv,ratio,topk,pos", [
-    (2100, 2, 64, 128, 600, 4, 300, None),      # 2 chunks, strided copies
-    (3000, 3, 32, 64, 3000, 1, 100, [0, 7, 900]),  # 2 chunks with positions
+    (2100, 2, 64, 128, 600, 4, 300, None),      # 4 chunks, strided copies
+    (3000, 3, 32, 64, 3000, 1, 100, [0, 7, 900]),  # 5 chunks with positions
 ])
 def test_host_chunks_with_batches(dsa, S, B, H, D, S_kv, ratio, topk, pos):
     wl = Workload("h", B=B, S=S, S_kv=S_kv, H=H, D=D, compress_ratio=ratio,
