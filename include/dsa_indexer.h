@@ -222,11 +222,17 @@ DSA_API size_t dsa_indexer_host_buffer_size(int S, int B, int H, int D,
  * `device_buf` (caller-owned device memory of dsa_indexer_host_buffer_size()
  * bytes, 256-byte aligned), runs the forward there and copies the results
  * back, pipelining the copies against the kernels: the query rows are split
- * along S into up to 16 chunks of at least 512 rows (none for S < 1024);
- * the next chunk's rows are copied in while one chunk is scored, and its
- * results are copied out while the following ones are scored.  Results are identical to one dsa_indexer_fwd()
- * call.  The copies overlap only when the host buffers are page-locked
- * (pinned); pageable buffers work but serialise.
+ * along S into up to 16 chunks of at least 512 rows (none for S < 1024),
+ * whose starts fall on whole waves of work items of the current device when
+ * the chunks hold at least one; the next chunk's rows are copied in while
+ * one chunk is scored, and its results are copied out while the following
+ * ones are scored.  Chunks run last rows first, or, when the kernels
+ * outweigh the copies (many visible keys per copied byte), alternately
+ * from the costliest and the cheapest end.  Results are identical to one
+ * dsa_indexer_fwd() call whatever the chunking.  The copies overlap only
+ * when the host buffers are page-locked (pinned); pageable buffers work but
+ * serialise.  dsa_indexer_host_buffer_size() and this call must see the
+ * same current device (the chunking reads its SM count).
  *
  * The work is ordered after everything already queued on `cuda_stream` and
  * the call returns once the results are in the host outputs (it
