@@ -94,6 +94,9 @@ def load_library(path: str | None = None):
         lib.dsa_selftest_wait_limit.argtypes = [I, P, Z, P]
         lib.dsa_indexer_host_buffer_size.restype = Z
         lib.dsa_indexer_host_buffer_size.argtypes = [I] * 8
+        lib.dsa_indexer_host_plan.restype = I
+        lib.dsa_indexer_host_plan.argtypes = [I, I, I, I, I, I, I, P, I, I,
+                                              P, P]
         lib.dsa_indexer_varlen_workspace_size.restype = Z
         lib.dsa_indexer_varlen_workspace_size.argtypes = [I, P, P, I, I, I, I,
                                                           I]
@@ -516,6 +519,27 @@ def dsa_indexer_host_buffer_size(S, B, H, D, S_kv, compress_ratio, topk,
                                  has_in_idx=False) -> int:
     return int(load_library().dsa_indexer_host_buffer_size(
         S, B, H, D, S_kv, compress_ratio, topk, int(bool(has_in_idx))))
+
+
+def dsa_indexer_host_plan(S, B, H, D, S_kv, compress_ratio, topk,
+                          q_pos=None, has_in_idx=False, sms=0):
+    """How dsa_indexer_fwd_host splits and orders the query rows: returns
+    (chunk starts, the last one S; processing order).  q_pos: host int32
+    [B] or None.  sms: the SM count the chunk starts assume (0: the current
+    device's).  Raises DsaError for an invalid shape."""
+    lib = load_library()
+    starts = (ctypes.c_int * 17)()
+    order = (ctypes.c_int * 16)()
+    pos = None
+    if q_pos is not None:
+        pos = _host_i32(q_pos)
+    n = lib.dsa_indexer_host_plan(
+        S, B, H, D, S_kv, int(compress_ratio), int(topk),
+        None if pos is None else pos.data_ptr(), int(bool(has_in_idx)),
+        int(sms), starts, order)
+    if n <= 0:
+        raise DsaError(1, "dsa_indexer_host_plan")
+    return list(starts[:n + 1]), list(order[:n])
 
 
 def dsa_indexer_fwd_host(q, k, w, compress_ratio, topk, q_pos=None,

@@ -44,16 +44,18 @@ int plan_chunks(int S) {
   return c < 1 ? 1 : c;
 }
 
-// Query rows per wave of prefill work items on this device (one item is
-// 256/H rows of one sequence, one CTA per SM): chunk starts on whole waves
-// leave no part-filled last wave in each chunk's launch.  4 when unknown.
-int wave_rows(int B, int H) {
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
-          cudaSuccess ||
-      sms <= 0 || H <= 0 || B <= 0)
-    return 4;
+// Query rows per wave of prefill work items on a GPU of `sms` SMs (the
+// current device's when sms <= 0; one item is 256/H rows of one sequence,
+// one CTA per SM): chunk starts on whole waves leave no part-filled last
+// wave in each chunk's launch.  4 when unknown.
+int wave_rows(int B, int H, int sms) {
+  int dev = 0;
+  if (sms <= 0 &&
+      (cudaGetDevice(&dev) != cudaSuccess ||
+       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+           cudaSuccess))
+    sms = 0;
+  if (sms <= 0 || H <= 0 || B <= 0) return 4;
   const long long tq = H < 256 ? 256 / H : 1;
   const long long u = ((long long)sms * tq / B) & ~3ll;
   return u < 4 ? 4 : (u > (1 << 20) ? (1 << 20) : (int)u);
@@ -116,10 +118,10 @@ struct HostLayout {
 };
 
 HostLayout host_layout(int S, int B, int H, int D, int S_kv, int ratio,
-                       int topk, bool has_in_idx) {
+                       int topk, bool has_in_idx, int sms = 0) {
   HostLayout L;
   L.chunks = plan_chunks(S);
-  L.unit = wave_rows(B, H);
+  L.unit = wave_rows(B, H, sms);
   for (int i = 0; i < L.chunks; ++i) {
     const int r = chunk_start(S, L.chunks, i + 1, L.unit) -
                   chunk_start(S, L.chunks, i, L.unit);
@@ -204,6 +206,22 @@ int get_pipe(Pipe **out) {
 }  // namespace
 
 extern "C" {
+
+int dsa_indexer_host_plan(int S, int B, int H, int D, int S_kv,
+                          int compress_ratio, int topk, const int32_t *q_pos,
+                          int has_in_idx, int sms, int *starts, int *order) {
+  if (!starts || !order) return 0;
+  if (dsa_indexer_workspace_size(S, B, H, D, S_kv, compress_ratio, topk,
+                                 has_in_idx) == 0)
+    return 0;
+  const HostLayout L = host_layout(S, B, H, D, S_kv, compress_ratio, topk,
+                                   has_in_idx != 0, sms);
+  for (int i = 0; i <= L.chunks; ++i)
+    starts[i] = chunk_start(S, L.chunks, i, L.unit);
+  chunk_order(S, B, H, D, S_kv, compress_ratio, topk, q_pos, has_in_idx != 0,
+              L.chunks, L.unit, order);
+  return L.chunks;
+}
 
 size_t dsa_indexer_host_buffer_size(int S, int B, int H, int D, int S_kv,
                                     int compress_ratio, int topk,

@@ -207,6 +207,22 @@ DSA_API int dsa_indexer_fwd_varlen(const void *q, const void *k,
                                    void *cuda_stream);
 
 /*
+ * How dsa_indexer_fwd_host() splits and orders the query rows of a call of
+ * this shape (for inspection; no device work).  Writes the chunk starts
+ * (chunks + 1 values, increasing, the last one S) to `starts` and the
+ * processing order (a permutation of 0..chunks-1) to `order`, both
+ * caller-owned host arrays of at least 17 ints.  q_pos: host [B] or NULL,
+ * as in dsa_indexer_fwd_host().  `sms`: the SM count the wave alignment
+ * assumes (0 or less: the current device's; none without a device).
+ * Returns the chunk count (1..16), or 0 for an invalid shape or a NULL
+ * array.
+ */
+DSA_API int dsa_indexer_host_plan(int S, int B, int H, int D, int S_kv,
+                                  int compress_ratio, int topk,
+                                  const int32_t *q_pos, int has_in_idx,
+                                  int sms, int *starts, int *order);
+
+/*
  * Bytes of DEVICE memory dsa_indexer_fwd_host() needs for this shape: room
  * for the inputs, the outputs and the workspace of its chunked pipeline.
  * Returns 0 when the shape is invalid.

@@ -402,3 +402,63 @@ def test_sparse_mla_rejects_bad_arguments(lib):
     assert call(q=FAKE + 8) == INVALID
     assert call(ws=None) == WORKSPACE
     assert call(nb=100) == WORKSPACE
+
+
+# ---- how the host-buffer entry point splits and orders the rows ----------
+
+def _plan(S, B, H, D, S_kv, ratio, topk, q_pos=None, given=False, sms=152):
+    import dsa_sparse_attention_fwd_gb300 as m
+    return m.dsa_indexer_host_plan(S, B, H, D, S_kv, ratio, topk, q_pos=q_pos,
+                                   has_in_idx=given, sms=sms)
+
+
+def _check_starts(starts, S, unit):
+    assert starts[0] == 0 and starts[-1] == S
+    assert all(b > a for a, b in zip(starts, starts[1:]))
+    assert all(s % 4 == 0 for s in starts[:-1])
+    assert all(s % unit == 0 for s in starts[:-1])
+
+
+def test_host_plan_compute_bound_alternates():
+    """Long-context C4 (about 4070 tensor FLOPs per copied byte) alternates
+    the costliest and the cheapest chunk left; with 152 SMs and H = 64 the
+    chunk starts fall on whole waves of 152 items of 4 rows."""
+    starts, order = _plan(65536, 1, 64, 128, 16384, 4, 2048)
+    assert len(order) == 16
+    _check_starts(starts, 65536, 608)
+    assert order == [15, 0, 14, 1, 13, 2, 12, 3, 11, 4, 10, 5, 9, 6, 8, 7]
+    # rows deep into a long sequence: compute-bound at 2048 rows as well
+    starts, order = _plan(2048, 1, 64, 128, 8192, 1, 64, q_pos=[4096])
+    assert order == [3, 0, 2, 1] and starts == [0, 512, 1024, 1536, 2048]
+
+
+def test_host_plan_link_bound_takes_last_rows_first():
+    # C4 prefill: 2 sequences, so a wave of 152 items is 304 rows
+    starts, order = _plan(16384, 2, 64, 128, 4096, 4, 512)
+    _check_starts(starts, 16384, 304)
+    assert order == list(range(15, -1, -1))
+    # V3.2: 512-row chunks hold less than a wave, plain 4-row starts
+    starts, order = _plan(4096, 1, 64, 128, 4096, 1, 2048)
+    assert starts == [512 * i for i in range(9)]
+    assert order == list(range(7, -1, -1))
+    # given indices at long C4: q, the indices and the outputs per row
+    # against at most topk products per row
+    starts, order = _plan(65536, 1, 64, 128, 16384, 4, 2048, given=True)
+    assert order == list(range(15, -1, -1))
+
+
+def test_host_plan_edges():
+    # fewer than 1024 rows: one chunk
+    assert _plan(1000, 1, 64, 128, 4096, 4, 512) == ([0, 1000], [0])
+    # decode rows: one chunk
+    assert _plan(1, 64, 64, 128, 8192, 4, 512,
+                 q_pos=list(range(2048, 2048 + 64))) == ([0, 1], [0])
+    # no SM count given and no device: 4-row starts of an even split
+    import torch
+    if not torch.cuda.is_available():
+        starts, _ = _plan(65536, 1, 64, 128, 16384, 4, 2048, sms=0)
+        assert starts == [4096 * i for i in range(17)]
+    # an invalid shape is refused
+    import dsa_sparse_attention_fwd_gb300 as m
+    with pytest.raises(m.DsaError):
+        _plan(0, 1, 64, 128, 16384, 4, 2048)
