@@ -13,10 +13,12 @@
 //  - compute-bound shapes alternate the costliest and the cheapest chunk
 //    left (last, first, second last, second, ...): taken last rows first,
 //    their cheap chunks at the end finish scoring faster than their results
-//    can be copied out and the copies back up behind the kernels.  Every row's result is
-// bit-identical to one unchunked call: no row's arithmetic depends on the
-// other rows.  A chunk after the first sees its rows through per-chunk
-// query positions (q_pos[b] + s0, or s0 for prefill).
+//    can be copied out and the copies back up behind the kernels.
+// Chunk starts fall on whole waves of work items where the chunks hold at
+// least one.  Every row's result is bit-identical to one unchunked call: no
+// row's arithmetic depends on the other rows.  A chunk after the first
+// sees its rows through per-chunk query positions (q_pos[b] + s0, or s0 for
+// prefill).
 //
 // Device memory is the caller's buffer (dsa_indexer_host_buffer_size()
 // bytes): [k][q][w][positions][given indices][indices][scores][status]
@@ -37,7 +39,7 @@ constexpr int kMinChunkRows = 512;  // keeps each chunk's launch busy
 size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // Chunks along S: as many as there are kMinChunkRows-row blocks, at most
-// kMaxChunks; chunk starts are multiples of 4 rows.
+// kMaxChunks (chunk_start places them).
 int plan_chunks(int S) {
   int c = S / kMinChunkRows;
   if (c > kMaxChunks) c = kMaxChunks;
@@ -86,7 +88,7 @@ constexpr double kComputeBoundFlopPerByte = 3000.0;
 void chunk_order(int S, int B, int H, int D, int S_kv, int ratio, int topk,
                  const int32_t *q_pos, bool has_in_idx, int C, int unit,
                  int *ord) {
-  double flops = 0.0, bytes = 0.0;
+  double flops = 0.0;
   for (int i = 0; i < C; ++i) {
     const int s0 = chunk_start(S, C, i, unit);
     const int s1 = chunk_start(S, C, i + 1, unit);
@@ -99,8 +101,8 @@ void chunk_order(int S, int B, int H, int D, int S_kv, int ratio, int topk,
     }
   }
   // q and w in, indices and scores out (and given indices in)
-  bytes = (double)S * B * ((double)H * D * 2 + (double)H * 4 +
-                           (double)topk * (has_in_idx ? 12 : 8));
+  const double bytes = (double)S * B * ((double)H * D * 2 + (double)H * 4 +
+                                        (double)topk * (has_in_idx ? 12 : 8));
   const bool alternate = flops > kComputeBoundFlopPerByte * bytes;
   int lo = 0, hi = C - 1;
   for (int n = 0; n < C; ++n) {
