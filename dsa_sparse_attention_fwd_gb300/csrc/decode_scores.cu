@@ -4,7 +4,7 @@
 //
 // A work item is (query row r = b*S + s, chunk of kDecChunkTiles x 128 keys).
 // One MMA tile is 128 keys (M) x H heads of the row's single query (N = H),
-// K = D, so no MMA column is padding.  The K ring (kDecStages x 128 keys) is
+// K = D, so no MMA column is padding.  The K ring (5 or 6 x 128 keys) is
 // filled by TMA; the row's Q tile (H x D) is loaded once per item into one of
 // two buffers.  The fp32 accumulator sits in TMEM (lane = key, column =
 // head); each of the four epilogue warps owns 32 keys and reduces the
@@ -20,25 +20,27 @@
 namespace dsa {
 namespace {
 
-constexpr int kDecStages = 5;
-static_assert(kDecChunkTiles <= kDecStages,
-              "an item's K tiles are issued before its Q and must fit the ring");
 constexpr int kDecThreads = 192;
 
 template <int H, int KC>
 struct DecSmem {
-  // Q/weight slots: enough lookahead that the next items' Q tiles are in
-  // flight while the current (short) item is multiplied
-  static constexpr int kQSlots = H <= 64 ? 4 : 2;
+  // K ring stages: six where two Q/weight slots leave room (H <= 64; 3.5%
+  // faster on the decode batch than five stages and four Q slots), else
+  // five.  Two Q slots keep the next item's Q tile in flight.
+  static constexpr int kStages = H <= 64 ? 6 : 5;
+  static constexpr int kQSlots = 2;
+  static_assert(kDecChunkTiles <= kStages,
+                "an item's K tiles are issued before its Q and must fit the "
+                "ring");
   static constexpr int kQBytes = KC * H * 128;           // one Q tile
   static constexpr int kKBytes = KC * kTileKeys * 128;   // one K stage
   static constexpr int kWBytes = H * 4;                  // one weight row
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kQSlots * kQBytes;
-  static constexpr int kOffW = kOffK + kDecStages * kKBytes;
+  static constexpr int kOffW = kOffK + kStages * kKBytes;
   static constexpr int kOffBar = kOffW + kQSlots * kWBytes;
   // k_full[S], k_empty[S], q_full[Q], q_empty[Q], acc_full[2], acc_empty[2]
-  static constexpr int kNumBars = 2 * kDecStages + 2 * kQSlots + 4;
+  static constexpr int kNumBars = 2 * kStages + 2 * kQSlots + 4;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;
@@ -83,6 +85,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                          int S, int B,
                          int S_kv, int ratio, int n_items, int *status) {
   using L = DecSmem<H, KC>;
+  constexpr int kDecStages = L::kStages;
   constexpr uint32_t kIdesc = idesc_bf16_f32(kTileKeys, H);
   constexpr int kAccCols = H;  // TMEM columns per accumulator
 
