@@ -26,8 +26,10 @@
  * sits at q_pos[b] + s.
  *
  * Memory: every pointer argument is DEVICE memory owned by the caller,
- * dense and contiguous in the stated layout; q and k must be 16-byte
- * aligned.  The library allocates no device memory: it works in the
+ * dense and contiguous in the stated layout (the varlen entry points'
+ * cu_seqlens and the host-buffer entry points dsa_indexer_fwd_host() and
+ * dsa_indexer_host_plan() take HOST arrays, as stated there); q and k must
+ * be 16-byte aligned.  The library allocates no device memory: it works in the
  * caller's workspace (dsa_indexer_fwd_static_scratch() instead uses a fixed
  * array inside the library).  Every call is asynchronous on `cuda_stream` (a
  * cudaStream_t; NULL = the legacy default stream): outputs are valid once
@@ -108,8 +110,9 @@ DSA_API size_t dsa_indexer_workspace_size(int S, int B, int H, int D,
  *                           (H in {32, 64, 128}, S >= 256 / H, topk <= 2048,
  *                           S_kv < 2^20).
  *   DSA_PREFILL_TWO_KERNELS always the two-kernel forward.
- * Decode-shaped rows (S < 256 / H) always take the split-over-keys decode
- * kernel and the selection kernel.  Set the policy before sizing a
+ * Decode-shaped rows (S < 256 / H, with H in {32, 64, 128}, D <= 128 and
+ * w 16-byte aligned) always take the split-over-keys decode kernel and the
+ * selection kernel; other small shapes take the two-kernel forward.  Set the policy before sizing a
  * workspace: the size depends on it.  Returns DSA_OK or
  * DSA_ERR_INVALID_ARG.
  */
