@@ -170,6 +170,24 @@ def dsa_indexer_workspace_size(S, B, H, D, S_kv, compress_ratio, topk,
         S, B, H, D, S_kv, compress_ratio, topk, int(bool(has_in_idx))))
 
 
+def _require_cuda(where: str, **tensors):
+    """Device entry points read every tensor's pointer as device memory:
+    each given tensor must be a CUDA tensor, all on one device (host
+    tensors go through dsa_indexer_fwd_host / v4_lighting_indexer)."""
+    dev = None
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if t.device.type != "cuda":
+            raise ValueError(f"{where}: {name} must be a CUDA tensor, got "
+                             f"{t.device}")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"{where}: {name} is on {t.device}, the other "
+                             f"tensors on {dev}")
+
+
 def _check_inputs(q, k, w, q_pos, in_idx):
     for name, t, dt in (("index_q", q, torch.bfloat16),
                         ("index_k", k, torch.bfloat16),
@@ -204,6 +222,9 @@ def dsa_indexer_fwd(q, k, w, compress_ratio, topk, q_pos=None, in_idx=None,
     (dsa_indexer_fwd_launches gives the count); events left over after the
     last launch are recorded at the end."""
     lib = load_library()
+    _require_cuda("dsa_indexer_fwd", q=q, k=k, w=w, q_pos=q_pos,
+                  in_idx=in_idx, out_idx=out_idx, out_scores=out_scores,
+                  workspace=workspace)
     S, B, H, D, S_kv = _check_inputs(q, k, w, q_pos, in_idx)
     dev = q.device
     if in_idx is not None and tuple(in_idx.shape) != (B, S, topk):
@@ -248,6 +269,9 @@ def dsa_indexer_bwd(q, k, w, compress_ratio, idx, grad_scores, q_pos=None,
     [S, B, H, D], grad_k [S_kv, B, D] and grad_w [S, B, H] (fp32).  Returns
     (grad_q, grad_k, grad_w, workspace)."""
     lib = load_library()
+    _require_cuda("dsa_indexer_bwd", q=q, k=k, w=w, idx=idx,
+                  grad_scores=grad_scores, q_pos=q_pos, grad_q=grad_q,
+                  grad_k=grad_k, grad_w=grad_w, workspace=workspace)
     S, B, H, D, S_kv = _check_inputs(q, k, w, q_pos, idx)
     topk = idx.shape[-1]
     if tuple(idx.shape) != (B, S, topk):
@@ -298,6 +322,8 @@ def dsa_kpool_compress(k, gate, ape, kpool, first_key=0, valid=None,
     """Pool compression on device tensors: returns (keys [P, B, D] bf16,
     pool_valid [P, B] uint8)."""
     lib = load_library()
+    _require_cuda("dsa_kpool_compress", k=k, gate=gate, ape=ape,
+                  valid=valid)
     T, B, D = _pool_inputs(k, gate, ape, valid, kpool)
     P = max(0, (T - first_key) // kpool)
     keys = torch.empty((max(P, 1), B, D), dtype=torch.bfloat16,
@@ -314,6 +340,7 @@ def dsa_kpool_compress(k, gate, ape, kpool, first_key=0, valid=None,
 def dsa_expand_selection(pools, kpool, first_key=0, out=None, stream=None):
     """Pool ids [..., select_k] int32 -> token ids [..., select_k*kpool]."""
     lib = load_library()
+    _require_cuda("dsa_expand_selection", pools=pools, out=out)
     if pools.dtype != torch.int32 or not pools.is_contiguous():
         raise ValueError("pools must be contiguous int32")
     select_k = pools.shape[-1]
@@ -344,6 +371,10 @@ def dsa_indexer_fwd_pooled(q, k, gate, ape, w, kpool, first_key, index_topk,
     pools [B,S,index_topk/kpool] int32, scores [B,S,index_topk/kpool] fp32,
     workspace)."""
     lib = load_library()
+    _require_cuda("dsa_indexer_fwd_pooled", q=q, k=k, gate=gate, ape=ape,
+                  w=w, valid=valid, q_pos=q_pos, out_tokens=out_tokens,
+                  out_pools=out_pools, out_scores=out_scores,
+                  workspace=workspace)
     T, B, D = _pool_inputs(k, gate, ape, valid, kpool)
     if q.dtype != torch.bfloat16 or not q.is_contiguous():
         raise ValueError("q must be contiguous bf16")
@@ -387,6 +418,8 @@ def dsa_sparse_mla_fwd(q, c, idx, scale, out_o=None, out_lse=None,
     cache c [T,B,Dc] bf16, idx [B,S,topk] int32 token ids.  Returns (o
     [S,B,H,Dc] fp32, lse [S,B,H] fp32, workspace)."""
     lib = load_library()
+    _require_cuda("dsa_sparse_mla_fwd", q=q, c=c, idx=idx, out_o=out_o,
+                  out_lse=out_lse, workspace=workspace)
     for name, t, dt in (("q", q, torch.bfloat16), ("c", c, torch.bfloat16),
                         ("idx", idx, torch.int32)):
         if t.dtype != dt or not t.is_contiguous():
@@ -418,6 +451,8 @@ def dsa_indexer_logits(q, k, w, compress_ratio, q_pos=None, logits=None,
     """Enqueue the scoring step alone: logits [B, S, S_kv] fp32 (-inf where
     a key is not visible).  Returns (logits, workspace)."""
     lib = load_library()
+    _require_cuda("dsa_indexer_logits", q=q, k=k, w=w, q_pos=q_pos,
+                  logits=logits, workspace=workspace)
     S, B, H, D, S_kv = _check_inputs(q, k, w, q_pos, None)
     dev = q.device
     if logits is None:
@@ -436,11 +471,13 @@ def dsa_indexer_logits(q, k, w, compress_ratio, q_pos=None, logits=None,
 
 def dsa_indexer_check(workspace, stream=None) -> int:
     """Synchronise the stream and return the device status code (0 = ok)."""
+    _require_cuda("dsa_indexer_check", workspace=workspace)
     return int(load_library().dsa_indexer_check(_ptr(workspace),
                                                  _stream(stream)))
 
 
 def dsa_selftest_wait_limit(limit_us: int, workspace, stream=None) -> int:
+    _require_cuda("dsa_selftest_wait_limit", workspace=workspace)
     return int(load_library().dsa_selftest_wait_limit(
         int(limit_us), _ptr(workspace), workspace.numel(), _stream(stream)))
 
@@ -472,6 +509,9 @@ def dsa_indexer_fwd_varlen(q, k, w, cu_seqlens_q, cu_seqlens_k,
     offsets [N + 1].  Returns (out_scores [T, topk], out_idx [T, topk],
     workspace); indices are local to each row's sequence."""
     lib = load_library()
+    _require_cuda("dsa_indexer_fwd_varlen", q=q, k=k, w=w, q_pos=q_pos,
+                  in_idx=in_idx, out_idx=out_idx, out_scores=out_scores,
+                  workspace=workspace)
     cq, ck = _host_i32(cu_seqlens_q), _host_i32(cu_seqlens_k)
     N = cq.numel() - 1
     if ck.numel() != N + 1 or N < 1:
@@ -554,9 +594,11 @@ def dsa_indexer_fwd_host(q, k, w, compress_ratio, topk, q_pos=None,
     lib = load_library()
     S, B, H, D, S_kv = _check_inputs(q, k, w, q_pos, in_idx)
     for name, t in (("index_q", q), ("index_k", k), ("weights", w),
-                    ("q_pos", q_pos), ("topk_indices", in_idx)):
+                    ("q_pos", q_pos), ("topk_indices", in_idx),
+                    ("out_idx", out_idx), ("out_scores", out_scores)):
         if t is not None and t.device.type != "cpu":
             raise ValueError(f"{name} must be a host tensor")
+    _require_cuda("dsa_indexer_fwd_host", device_buf=device_buf)
     if in_idx is not None and tuple(in_idx.shape) != (B, S, topk):
         raise ValueError("topk_indices must be [B, S, topk]")
     pinned = q.is_pinned()
